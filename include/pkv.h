@@ -1,0 +1,212 @@
+/*
+ * pkv.h -- C ABI of the paged KV-cache attention library for GB300 (sm_103a).
+ *
+ * The operations follow the problem statement of the pages this library is
+ * built from:
+ *  - "mini-infer系统实战-06 True PagedAttention" (smarter.xin), sections 1
+ *    and 3: one call writes the new token's K/V in place into the page slot
+ *    that block_table and cache_seqlens select, then attends directly over
+ *    the physical pages (no dense gather) and returns the output.  Cache
+ *    tensors are [num_blocks, block_size, num_kv_heads, head_dim];
+ *    block_table is int32 [batch, max_blocks]; cache_seqlens is int32
+ *    [batch], the current length of every request.
+ *  - "flex_attention + paged KV + CUDA graphs vs vLLM", "Why this works" and
+ *    "What broke correctness": physical page 0 is a reserved null page and
+ *    padded rows must yield finite output; decode runs under CUDA-graph
+ *    capture, so no call syncs the host or allocates.
+ *  - "[flashinfer] H100 D256 paged attention cuDNN auto-dispatch", code
+ *    analysis part 1: ragged causal prefill over HND pages
+ *    [num_pages, num_kv_heads, page_size, head_dim], end aligned (query i of
+ *    q queries over kv keys sees kv - q + i + 1 keys), with host-resident
+ *    lengths never read back from the device.
+ *
+ * Conventions shared by every entry point:
+ *  - All tensors are dense, row major, in the shapes stated; "bf16" is the
+ *    bfloat16 bit layout.  Device pointers must be 16-byte aligned.
+ *  - The caller owns every buffer.  The library never allocates or frees
+ *    device memory and never synchronises the host inside a device call, so
+ *    every device call can be captured in a CUDA graph.  `stream` is a
+ *    cudaStream_t (NULL = the legacy default stream).
+ *  - GQA: query head h reads kv head h / (num_q_heads / num_kv_heads).
+ *  - cache_seqlens[b] is the length BEFORE the append.  A negative value
+ *    marks an inactive (padding) row: nothing is appended, its output is 0
+ *    and its lse is -inf, and no error is raised.
+ *  - Argument errors (shapes, alignment, unsupported sizes, too small a
+ *    workspace) are returned synchronously as a pkv_status and nothing is
+ *    launched.
+ *  - Data errors are found on the device: a block_table entry a row needs
+ *    that is outside [1, num_pages), or a row whose tokens do not fit in
+ *    max_blocks * page_size.  The row's appends are dropped, its output is
+ *    0 with lse -inf, and the matching PKV_ERR_* bit is OR-ed into
+ *    *err_flag (when err_flag is not NULL).  No address outside the buffers
+ *    is ever formed.  The host reads err_flag whenever it chooses.
+ */
+#ifndef PKV_H
+#define PKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    PKV_NHD = 0, /* [num_pages, page_size, num_kv_heads, head_dim] */
+    PKV_HND = 1  /* [num_pages, num_kv_heads, page_size, head_dim] */
+} pkv_layout;
+
+typedef enum {
+    PKV_OK = 0,
+    PKV_EINVAL = 1,       /* bad argument (NULL, shape, alignment, range) */
+    PKV_EUNSUPPORTED = 2, /* valid but not built (head_dim, page size, group) */
+    PKV_ECUDA = 3,        /* a CUDA runtime / driver call failed */
+    PKV_ENOPAGES = 4,     /* page pool exhausted; nothing was taken */
+    PKV_EWORKSPACE = 5    /* workspace NULL or smaller than required */
+} pkv_status;
+
+/* Device-side error bits OR-ed into *err_flag. */
+#define PKV_ERR_PAGE 1     /* a needed block_table entry is outside [1, num_pages) */
+#define PKV_ERR_OVERFLOW 2 /* a row's tokens exceed max_blocks * page_size */
+#define PKV_ERR_TIMEOUT 4  /* an on-chip pipeline wait ran out of time (row zeroed) */
+
+/* Geometry of one K or V page pool (both share it).  page_size is a power of
+ * two in [1, 256]; head_dim is 64, 128 or 256; num_pages >= 2 (page 0 is the
+ * null page and is never read or written for a live token). */
+typedef struct {
+    int32_t num_pages;
+    int32_t page_size;
+    int32_t num_kv_heads;
+    int32_t head_dim;
+    int32_t layout; /* pkv_layout */
+} pkv_cache_desc;
+
+/* Opaque host-side page pool (see pkv_pool_create). */
+typedef struct pkv_pool pkv_pool;
+
+/*
+ * pkv_append -- write new tokens' K/V into their page slots (bit copy).
+ * Source: "mini-infer系统实战-06 True PagedAttention", section 1 (step 1 of
+ * the fused call: k_new/v_new written in place into the right block slot).
+ *
+ *  k_cache, v_cache  device bf16 pools described by `desc` (modified).
+ *  k_new, v_new      device bf16 [T, num_kv_heads, head_dim].
+ *  append_indptr     device int32 [batch + 1] (row b appends tokens
+ *                    append_indptr[b] .. append_indptr[b+1]-1 of k_new at
+ *                    positions cache_seqlens[b], cache_seqlens[b]+1, ...),
+ *                    or NULL for exactly one token per row (T = batch).
+ *  block_table       device int32 [batch, max_blocks].
+ *  cache_seqlens     device int32 [batch]; not modified (the caller advances
+ *                    it).
+ *  err_flag          device int32, or NULL.  Only the pages that receive a
+ *                    token are checked; a failing row appends nothing.
+ * Returns PKV_OK once the kernel is enqueued on `stream`.
+ */
+pkv_status pkv_append(const pkv_cache_desc *desc, void *k_cache, void *v_cache, const void *k_new,
+                      const void *v_new, const int32_t *append_indptr, const int32_t *block_table,
+                      int32_t max_blocks, const int32_t *cache_seqlens, int32_t batch,
+                      int32_t *err_flag, void *stream);
+
+/*
+ * pkv_decode_workspace_size -- bytes of device workspace pkv_decode_attn
+ * needs for these sizes (0 on invalid arguments).  The workspace holds the
+ * split-KV partial results and one combine ticket per (row, kv head).  It
+ * must be zero-filled once before its first use (e.g. cudaMemsetAsync);
+ * every completed call leaves the tickets at zero again, so it can be reused
+ * by later calls with the same or smaller sizes.  After a call that raised
+ * PKV_ERR_TIMEOUT, zero it again.  Calls that share a workspace must not run
+ * concurrently.
+ */
+size_t pkv_decode_workspace_size(int32_t batch, int32_t max_blocks, int32_t num_q_heads,
+                                 const pkv_cache_desc *desc);
+
+/*
+ * pkv_decode_attn -- fused append + single-token GQA decode attention
+ * straight over the paged cache, with split-KV partitioning planned on the
+ * device and a log-sum-exp combine of the partial results.
+ * Source: "mini-infer系统实战-06 True PagedAttention", sections 1, 3 and 6
+ * (flash_attn_with_kvcache with block_table / cache_seqlens; the split-KV
+ * decode kernel behind it); "flex_attention + paged KV + CUDA graphs vs
+ * vLLM", "Best config" (q pre-scaled by the softmax scale).
+ *
+ *  q                 device bf16 [batch, num_q_heads, head_dim].
+ *  k_new, v_new      device bf16 [batch, num_kv_heads, head_dim], or both
+ *                    NULL (attend only).  When given, row b's token is
+ *                    written at position cache_seqlens[b] and the row attends
+ *                    cache_seqlens[b] + 1 keys; otherwise cache_seqlens[b].
+ *  softmax_scale     scale applied to q.k (finite).
+ *  out               device bf16 [batch, num_q_heads, head_dim]
+ *                    (round to nearest even from fp32).
+ *  lse               device fp32 [batch, num_q_heads] natural-log
+ *                    log-sum-exp of the scaled scores, or NULL.
+ *  workspace         device buffer of at least pkv_decode_workspace_size
+ *                    bytes (see there).
+ *  batch             0 .. 1024.
+ * Rows that see no key (inactive, or attend-only with length 0) give out = 0
+ * and lse = -inf.
+ */
+pkv_status pkv_decode_attn(const pkv_cache_desc *desc, void *k_cache, void *v_cache, const void *q,
+                           const void *k_new, const void *v_new, const int32_t *block_table,
+                           int32_t max_blocks, const int32_t *cache_seqlens, int32_t batch,
+                           int32_t num_q_heads, float softmax_scale, void *out, float *lse,
+                           void *workspace, size_t workspace_bytes, int32_t *err_flag,
+                           void *stream);
+
+/* ---------------------------------------------------------------------
+ * Host page-pool and block-table helpers (no device memory involved).
+ * Source: "flex_attention + paged KV + CUDA graphs vs vLLM", "What each
+ * option did" (PageTable.reserve hands out pages sequentially on a fresh
+ * batch) and "Why this works" (page 0 reserved as a no-op slot).
+ * --------------------------------------------------------------------- */
+
+/* A pool of pages 1 .. num_pages-1 (page 0 is never handed out), handed out
+ * lowest-numbered first.  Returns NULL if num_pages < 2 or on allocation
+ * failure.  Not thread safe. */
+pkv_pool *pkv_pool_create(int32_t num_pages);
+void pkv_pool_destroy(pkv_pool *pool);
+
+/* Takes n free pages into pages_out[0..n-1].  PKV_ENOPAGES if fewer than n
+ * are free (then nothing is taken). */
+pkv_status pkv_pool_alloc(pkv_pool *pool, int32_t n, int32_t *pages_out);
+
+/* Returns n pages.  PKV_EINVAL if a page is 0, out of range or already free
+ * (then nothing is returned). */
+pkv_status pkv_pool_free(pkv_pool *pool, const int32_t *pages, int32_t n);
+
+int32_t pkv_pool_num_free(const pkv_pool *pool);
+
+/* Mixes the free list with a seeded permutation (splitmix64-driven
+ * Fisher-Yates), so later allocations are scattered over the pool. */
+pkv_status pkv_pool_shuffle(pkv_pool *pool, uint64_t seed);
+
+/* Makes a host block_table row cover new_len tokens when it covers cur_len:
+ * fills entries [ceil(cur_len/P), ceil(new_len/P)) from the pool.
+ * PKV_EINVAL if new_len < cur_len or the row would exceed max_blocks;
+ * PKV_ENOPAGES if the pool is short (then the row is unchanged). */
+pkv_status pkv_table_reserve(pkv_pool *pool, int32_t *block_table_row, int32_t max_blocks,
+                             int32_t page_size, int32_t cur_len, int32_t new_len);
+
+/* Returns the pages of a row covering len tokens to the pool and zeroes the
+ * row's entries. */
+pkv_status pkv_table_release(pkv_pool *pool, int32_t *block_table_row, int32_t max_blocks,
+                             int32_t page_size, int32_t len);
+
+/* Host-side check of block_table / cache_seqlens (host copies) for a decode
+ * or append of extra_tokens per row: returns PKV_EINVAL with *bad_row set to
+ * the first failing row, else PKV_OK.  For tests and debugging. */
+pkv_status pkv_validate_host(const pkv_cache_desc *desc, const int32_t *block_table_host,
+                             int32_t max_blocks, const int32_t *seqlens_host, int32_t batch,
+                             int32_t extra_tokens, int32_t *bad_row);
+
+/* Bytes of one K or V pool for `desc` (num_pages * page_size * num_kv_heads
+ * * head_dim * 2), 0 on invalid arguments. */
+uint64_t pkv_pool_bytes(const pkv_cache_desc *desc);
+
+/* Static description of a status code. */
+const char *pkv_status_str(pkv_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_H */

@@ -35,6 +35,8 @@
  *  - a needed block_table entry outside [1, num_pages), or a row whose
  *    tokens do not fit max_blocks * page_size, is a data error: the row's
  *    appends are dropped, out = 0, lse = -inf and an error bit is raised.
+ *    "Needed" means touched: attention needs every page of the row, a
+ *    standalone append only the pages it writes.
  *  - lse is the natural-log log-sum-exp of the scaled scores.
  *
  * All values are bf16 bit patterns (uint16).  bf16 -> double is exact.
@@ -92,16 +94,24 @@ static int64_t page_of(const oracle_cache *c, const int32_t *block_table, int ma
     return page;
 }
 
-/* Error bits for a row that must hold `len` tokens. */
-static int row_check(const oracle_cache *c, const int32_t *block_table, int max_blocks, int b,
-                     int64_t len)
+/* Error bits for a row whose tokens first .. len-1 are touched (pages of
+ * all of them must be usable) and which must hold `len` tokens. */
+static int range_check(const oracle_cache *c, const int32_t *block_table, int max_blocks, int b,
+                       int64_t first, int64_t len)
 {
     if (len > (int64_t)max_blocks * c->page_size)
         return ORACLE_ERR_OVERFLOW;
-    for (int64_t t = 0; t < len; t += c->page_size)
+    for (int64_t t = first; t < len; t++)
         if (page_of(c, block_table, max_blocks, b, t) < 0)
             return ORACLE_ERR_PAGE;
     return 0;
+}
+
+/* Error bits for a row that reads all of its `len` tokens. */
+static int row_check(const oracle_cache *c, const int32_t *block_table, int max_blocks, int b,
+                     int64_t len)
+{
+    return range_check(c, block_table, max_blocks, b, 0, len);
 }
 
 /* Writes n_new tokens of row b at logical positions L, L+1, ... (bit copy). */
@@ -128,6 +138,8 @@ static void write_tokens(const oracle_cache *c, uint16_t *k_cache, uint16_t *v_c
  * cache_seqlens[b] ... cache_seqlens[b] + n_b - 1, where n_b =
  * append_indptr[b+1] - append_indptr[b] (or 1 when append_indptr is NULL);
  * its K/V rows are k_new[append_indptr[b] + i] ([T, Hkv, D] bf16).
+ * Only the pages receiving a token are checked (the append reads no other
+ * page); a failing row appends nothing.
  * Returns the OR of the error bits; err_rows[b] (optional) gets each row's.
  */
 int oracle_append(const oracle_cache *c, uint16_t *k_cache, uint16_t *v_cache,
@@ -143,7 +155,7 @@ int oracle_append(const oracle_cache *c, uint16_t *k_cache, uint16_t *v_cache,
         int64_t L = cache_seqlens[b];
         int err = 0;
         if (L >= 0 && n_new > 0) {
-            err = row_check(c, block_table, max_blocks, b, L + n_new);
+            err = range_check(c, block_table, max_blocks, b, L, L + n_new);
             if (!err)
                 write_tokens(c, k_cache, v_cache, k_new + first * H * D, v_new + first * H * D,
                              n_new, block_table, max_blocks, b, L);

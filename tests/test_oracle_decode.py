@@ -287,3 +287,23 @@ def test_threads_do_not_change_bits(oracle_mod):
     o1, l1, _, _ = oracle_mod.decode(d, k.copy(), v.copy(), *args, nthreads=1)
     o4, l4, _, _ = oracle_mod.decode(d, k.copy(), v.copy(), *args, nthreads=4)
     assert o1.tobytes() == o4.tobytes() and l1.tobytes() == l4.tobytes()
+
+
+def test_standalone_append_checks_only_destination_pages(oracle_mod):
+    case = wl.tiny()
+    case.block_table = case.block_table.copy()
+    case.block_table[3, 0] = 0  # a page row 3 reads, but an append at 64 does not touch
+    k = wl.bits(case.k_cache).copy()
+    v = wl.bits(case.v_cache).copy()
+    d = _desc(oracle_mod, case)
+    err, err_rows = oracle_mod.append(d, k, v, wl.bits(case.k_new), wl.bits(case.v_new), None,
+                                      case.block_table, case.cache_seqlens)
+    assert err == 0
+    page = case.block_table[3, 64 // case.page_size]
+    assert np.array_equal(k[page, 0], wl.bits(case.k_new)[3])
+    case.block_table[3, 64 // case.page_size] = case.num_pages + 3  # now the destination is bad
+    k2 = wl.bits(case.k_cache).copy()
+    err, err_rows = oracle_mod.append(d, k2, v.copy(), wl.bits(case.k_new), wl.bits(case.v_new), None,
+                                      case.block_table, case.cache_seqlens)
+    assert err == oracle_mod.ERR_PAGE and list(err_rows) == [0, 0, 0, oracle_mod.ERR_PAGE]
+    assert np.array_equal(k2[page], wl.bits(case.k_cache)[page])  # row 3 wrote nothing
