@@ -1,0 +1,399 @@
+"""Paged decode benchmark: fused append + GQA decode over a paged KV cache.
+
+Workload (one step = one decode step of a 36-layer Qwen3-4B-shaped model's
+attention): the batch sweep at B=64, Hq=32, Hkv=8, D=128, page 128, prompt
+uniform in [64, 512], 36 per-layer K/V pools sharing one block table,
+shuffled page layout.  Every step appends one token per row in every layer
+and attends over all cached tokens; lengths grow by one per step and wrap
+after 512 decode steps (the reserved capacity).  Each step reads ~5 GB of
+K/V, far above the 129 MB L2, so no flush is needed between steps.
+
+Prints one JSON line.  `value` = algorithmic KV-path bytes / device time
+(GB/s) over the timed steps; `roofline` = the decode kernel's average
+launch (CUDA events around every launch); `e2e` = the same metric through
+the C ABI with the step's q / k_new / v_new copied from pinned host memory
+and the outputs copied back inside the timed region.
+
+`--impl reference` times the fp64 CPU oracle on the host cores instead
+(bounded samples of the same workload).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "paged decode KV-read GB/s (% of HBM peak) and decode tok/s per attn layer"
+HQ, HKV, D, P = 32, 8, 128, 128
+DECODE_CAPACITY = 512
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_kernel_traffic.txt")
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            m = json.load(f)
+        return float(m["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def call_bytes(lens: np.ndarray, batch: int) -> int:
+    """Algorithmic bytes of one fused append + decode call (one layer):
+    cached K/V read + q read + out write + new K/V read + append write +
+    block-table entries read + seqlens read."""
+    kv_read = int(lens.sum()) * 2 * HKV * D * 2
+    q_out = 2 * batch * HQ * D * 2
+    new_tok = 2 * batch * 2 * HKV * D * 2
+    table = 4 * int(((lens + 1 + P - 1) // P).sum())
+    return kv_read + q_out + new_tok + table + 4 * batch
+
+
+def source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "paged_kv_decode_append_gb300", "csrc")
+    for name in ("pkv_decode.cu", "pkv_device.cuh", "pkv_internal.h"):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def recorded_traffic():
+    """DRAM bytes per decode launch from the committed ncu summary, scaled to
+    this workload's launch, if it was taken on the current kernel source."""
+    try:
+        rec = {}
+        with open(TRAFFIC_FILE) as f:
+            for line in f:
+                if ":" in line and not line.startswith("#"):
+                    k, v = line.split(":", 1)
+                    rec[k.strip()] = v.strip()
+        if rec.get("source_sha256") != source_hash():
+            return None
+        return float(rec["dram_bytes_per_algorithmic_byte"])
+    except Exception:
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._t = threading.Thread(target=self._read, daemon=True)
+            self._t.start()
+            time.sleep(0.3)
+        except FileNotFoundError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_setup(n_gpus: int):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend, device_id=torch.device(f"cuda:{local}") if backend == "nccl" else None)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(x: float, world: int, device) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def cpu_baseline(sw, lens_step0: np.ndarray, budget_s: float = 12.0):
+    """Times the fp64 oracle (all host cores) on whole layers of decode step 0
+    until `budget_s` is spent; returns GB/s of the same algorithmic bytes."""
+    import oracle
+    from paged_kv_decode_append_gb300 import workloads as wl
+
+    inputs = wl.sweep_step_inputs(sw, 0, sw.k_caches[0].device, layers=1)
+    q, kn, vn = (wl.bits(t) for t in inputs[0])
+    rows = list(range(sw.batch))
+    need = lens_step0 + 1
+    done_bytes, elapsed, layers = 0, 0.0, 0
+    threads = oracle.max_threads(0)
+    while elapsed < budget_s and layers < sw.layers:
+        k, v, bt = wl.compact_rows(sw.k_caches[layers], sw.v_caches[layers], sw.block_table, rows, need, P)
+        d = oracle.CacheDesc(k.shape[0], P, HKV, D, oracle.NHD)
+        t0 = time.perf_counter()
+        oracle.decode(d, k, v, q, kn, vn, bt, lens_step0, sw.softmax_scale, nthreads=0)
+        elapsed += time.perf_counter() - t0
+        done_bytes += call_bytes(lens_step0, sw.batch)
+        layers += 1
+    return {"value": done_bytes / elapsed / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "sample": f"{layers} of 36 layers of decode step 0 (B={sw.batch}, all rows and heads), fp64 oracle "
+                      f"with OpenMP over (row, head), {elapsed:.1f} s"}
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+    from paged_kv_decode_append_gb300 import workloads as wl
+
+    oracle.build()
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    sw = wl.batch_sweep(args.batch, device=dev, contiguous=args.layout == "contiguous", layers=1,
+                        data_device=dev)
+    rows = list(range(sw.batch))
+    threads = oracle.max_threads(0)
+    times, nbytes = [], []
+    host = []
+    for s in range(args.warmup + args.steps):
+        lens = (sw.prompt_lens + (s % DECODE_CAPACITY)).astype(np.int32)
+        k, v, bt = wl.compact_rows(sw.k_caches[0], sw.v_caches[0], sw.block_table, rows, lens + 1, P)
+        q, kn, vn = (wl.bits(t) for t in wl.sweep_step_inputs(sw, s, dev, layers=1)[0])
+        host.append((k, v, bt, q, kn, vn, lens))
+        if len(host) > 2:
+            host.pop(0)
+        d = oracle.CacheDesc(k.shape[0], P, HKV, D, oracle.NHD)
+        t0 = time.perf_counter()
+        oracle.decode(d, k, v, q, kn, vn, bt, lens, sw.softmax_scale, nthreads=0)
+        dt = time.perf_counter() - t0
+        if s >= args.warmup:
+            times.append(dt)
+            nbytes.append(call_bytes(lens, sw.batch))
+    total_t = float(sum(times))
+    value = sum(nbytes) / total_t / 1e9
+    out = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * total_t / len(times), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(args),
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle",
+                         "sample": f"one layer per step (layer 0 of the 36), B={args.batch}, fp64 oracle"},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(out))
+
+
+def workload_config(args):
+    return {"workload": f"paged decode batch sweep B={args.batch} (Qwen3-4B-shaped: Hq=32, Hkv=8, D=128), "
+                        f"page 128, {args.layout} pages, prompt U[64,512] + decode steps, 36 layer caches per step",
+            "batch": args.batch, "num_q_heads": HQ, "num_kv_heads": HKV, "head_dim": D, "page_size": P,
+            "layers": args.layers, "layout": args.layout,
+            "l2": "inputs larger than L2: every step streams 36 distinct layer caches (~5 GB)"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=600)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--batch", type=int, default=64)
+    ap.add_argument("--layers", type=int, default=36)
+    ap.add_argument("--layout", default="shuffled", choices=["shuffled", "contiguous"])
+    ap.add_argument("--e2e-steps", type=int, default=100)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+        return
+
+    import paged_kv_decode_append_gb300 as pkv
+    from paged_kv_decode_append_gb300 import workloads as wl
+
+    pkv.api._lib.load()
+    rank, world, local = dist_setup(args.gpus)
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    B, L = args.batch, args.layers
+    sw = wl.batch_sweep(B, device=dev, contiguous=args.layout == "contiguous", layers=L, seed=2 + rank)
+    bt = torch.as_tensor(sw.block_table, device=dev)
+    lens_all = (sw.prompt_lens[None, :] + np.arange(DECODE_CAPACITY)[:, None]).astype(np.int32)
+    lens_dev = torch.as_tensor(lens_all, device=dev)
+    desc = pkv.cache_desc(sw.k_caches[0])
+    ws = pkv.decode_workspace(B, sw.max_blocks, HQ, desc, dev)
+    ring = 8  # distinct per-step input sets, reused round-robin
+    inputs = [wl.sweep_step_inputs(sw, s, dev, layers=L) for s in range(ring)]
+    outs = [torch.empty(B, HQ, D, dtype=torch.bfloat16, device=dev) for _ in range(L)]
+    step_bytes = [L * call_bytes(lens_all[s], B) for s in range(DECODE_CAPACITY)]
+    stream = torch.cuda.current_stream(dev)
+
+    def layer_call(step, layer, q, kn, vn):
+        pkv.pkv_decode_attn(sw.k_caches[layer], sw.v_caches[layer], q, kn, vn, bt, lens_dev[step % DECODE_CAPACITY],
+                            sw.softmax_scale, out=outs[layer], workspace=ws)
+
+    for s in range(args.warmup):
+        for layer, (q, kn, vn) in enumerate(inputs[s % ring]):
+            layer_call(s, layer, q, kn, vn)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+
+    n_ev = args.steps * L
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_ev)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    total_bytes = 0
+    with ClockSampler(local) as clocks:
+        torch.cuda.synchronize(dev)
+        barrier(world)
+        torch.cuda.nvtx.range_push("timed")
+        start.record(stream)
+        i = 0
+        for s in range(args.warmup, args.warmup + args.steps):
+            for layer, (q, kn, vn) in enumerate(inputs[s % ring]):
+                ev[i][0].record(stream)
+                layer_call(s, layer, q, kn, vn)
+                ev[i][1].record(stream)
+                i += 1
+            total_bytes += step_bytes[s % DECODE_CAPACITY]
+        end.record(stream)
+        torch.cuda.nvtx.range_pop()
+        torch.cuda.synchronize(dev)
+        barrier(world)
+    ms = start.elapsed_time(end)
+    launch_ms = np.array([a.elapsed_time(b) for a, b in ev])
+    ms_max = max_over_ranks(ms, world, dev)
+    all_bytes = sum_over_ranks(float(total_bytes), world, dev)
+    value = all_bytes / (ms_max * 1e-3) / 1e9
+    launch_bytes = total_bytes / n_ev
+    kernel_ms = float(launch_ms.mean())
+    achieved = launch_bytes / (kernel_ms * 1e-3) / 1e9
+    peak, peak_kind = peaks()
+    traffic_ratio = recorded_traffic()
+
+    # end to end: host inputs each step (pinned), outputs back to host
+    e2e_steps = min(args.e2e_steps, args.steps)
+    h_in = [[tuple(t.cpu().pin_memory() for t in trip) for trip in inputs[r]] for r in range(2)]
+    h_out = [torch.empty(B, HQ, D, dtype=torch.bfloat16).pin_memory() for _ in range(L)]
+    d_in = [tuple(torch.empty_like(t) for t in trip) for trip in inputs[0]]
+    h2d = sum(t.numel() * 2 for trip in inputs[0] for t in trip)
+    d2h = L * B * HQ * D * 2
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e_bytes = 0
+    e_start.record(stream)
+    for s in range(e2e_steps):
+        src = h_in[s % 2]
+        for layer in range(L):
+            for dst, hs in zip(d_in[layer], src[layer]):
+                dst.copy_(hs, non_blocking=True)
+        for layer in range(L):
+            layer_call(s, layer, *d_in[layer])
+        for layer in range(L):
+            h_out[layer].copy_(outs[layer], non_blocking=True)
+        e_bytes += step_bytes[s % DECODE_CAPACITY]
+    e_end.record(stream)
+    torch.cuda.synchronize(dev)
+    e_ms = max_over_ranks(e_start.elapsed_time(e_end), world, dev)
+    e_all = sum_over_ranks(float(e_bytes), world, dev)
+    e2e_value = e_all / (e_ms * 1e-3) / 1e9
+
+    if rank != 0:
+        return
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        cpu = cpu_baseline(sw, lens_all[0])
+    steps_tok = B / (ms / args.steps / L * 1e-3)  # decode tokens/s per attention layer
+    out = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": workload_config(args),
+        "pct_of_hbm_peak": 100.0 * value / peak,
+        "decode_tok_s_per_attn_layer": steps_tok * world,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": None if traffic_ratio is None else traffic_ratio * launch_bytes,
+                     "peak_kind": peak_kind, "kernel": "pkv::decode_kernel<128,4>",
+                     "algorithmic_bytes_per_launch": launch_bytes, "launch_ms_mean": kernel_ms,
+                     "launch_ms_median": float(np.median(launch_ms)), "launch_ms_best": float(launch_ms.min())},
+        "clocks": clocks.summary(),
+        "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "steps": e2e_steps},
+        "gpu_launches": n_ev,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(out))
+
+
+if __name__ == "__main__":
+    main()

@@ -47,6 +47,12 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#if defined(__GNUC__)
+#define PKV_API __attribute__((visibility("default")))
+#else
+#define PKV_API
+#endif
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -68,7 +74,8 @@ typedef enum {
 /* Device-side error bits OR-ed into *err_flag. */
 #define PKV_ERR_PAGE 1     /* a needed block_table entry is outside [1, num_pages) */
 #define PKV_ERR_OVERFLOW 2 /* a row's tokens exceed max_blocks * page_size */
-#define PKV_ERR_TIMEOUT 4  /* an on-chip pipeline wait ran out of time (row zeroed) */
+#define PKV_ERR_TIMEOUT 4  /* an on-chip pipeline wait ran out of time: the call's outputs are
+                              unspecified and its workspace must be zero-filled again */
 
 /* Geometry of one K or V page pool (both share it).  page_size is a power of
  * two in [1, 256]; head_dim is 64, 128 or 256; num_pages >= 2 (page 0 is the
@@ -91,6 +98,7 @@ typedef struct pkv_pool pkv_pool;
  *
  *  k_cache, v_cache  device bf16 pools described by `desc` (modified).
  *  k_new, v_new      device bf16 [T, num_kv_heads, head_dim].
+ *  num_tokens        T (must equal batch when append_indptr is NULL).
  *  append_indptr     device int32 [batch + 1] (row b appends tokens
  *                    append_indptr[b] .. append_indptr[b+1]-1 of k_new at
  *                    positions cache_seqlens[b], cache_seqlens[b]+1, ...),
@@ -102,10 +110,10 @@ typedef struct pkv_pool pkv_pool;
  *                    token are checked; a failing row appends nothing.
  * Returns PKV_OK once the kernel is enqueued on `stream`.
  */
-pkv_status pkv_append(const pkv_cache_desc *desc, void *k_cache, void *v_cache, const void *k_new,
-                      const void *v_new, const int32_t *append_indptr, const int32_t *block_table,
-                      int32_t max_blocks, const int32_t *cache_seqlens, int32_t batch,
-                      int32_t *err_flag, void *stream);
+PKV_API pkv_status pkv_append(const pkv_cache_desc *desc, void *k_cache, void *v_cache, const void *k_new,
+                      const void *v_new, int32_t num_tokens, const int32_t *append_indptr,
+                      const int32_t *block_table, int32_t max_blocks, const int32_t *cache_seqlens,
+                      int32_t batch, int32_t *err_flag, void *stream);
 
 /*
  * pkv_decode_workspace_size -- bytes of device workspace pkv_decode_attn
@@ -117,7 +125,7 @@ pkv_status pkv_append(const pkv_cache_desc *desc, void *k_cache, void *v_cache, 
  * PKV_ERR_TIMEOUT, zero it again.  Calls that share a workspace must not run
  * concurrently.
  */
-size_t pkv_decode_workspace_size(int32_t batch, int32_t max_blocks, int32_t num_q_heads,
+PKV_API size_t pkv_decode_workspace_size(int32_t batch, int32_t max_blocks, int32_t num_q_heads,
                                  const pkv_cache_desc *desc);
 
 /*
@@ -145,7 +153,7 @@ size_t pkv_decode_workspace_size(int32_t batch, int32_t max_blocks, int32_t num_
  * Rows that see no key (inactive, or attend-only with length 0) give out = 0
  * and lse = -inf.
  */
-pkv_status pkv_decode_attn(const pkv_cache_desc *desc, void *k_cache, void *v_cache, const void *q,
+PKV_API pkv_status pkv_decode_attn(const pkv_cache_desc *desc, void *k_cache, void *v_cache, const void *q,
                            const void *k_new, const void *v_new, const int32_t *block_table,
                            int32_t max_blocks, const int32_t *cache_seqlens, int32_t batch,
                            int32_t num_q_heads, float softmax_scale, void *out, float *lse,
@@ -162,48 +170,48 @@ pkv_status pkv_decode_attn(const pkv_cache_desc *desc, void *k_cache, void *v_ca
 /* A pool of pages 1 .. num_pages-1 (page 0 is never handed out), handed out
  * lowest-numbered first.  Returns NULL if num_pages < 2 or on allocation
  * failure.  Not thread safe. */
-pkv_pool *pkv_pool_create(int32_t num_pages);
-void pkv_pool_destroy(pkv_pool *pool);
+PKV_API pkv_pool *pkv_pool_create(int32_t num_pages);
+PKV_API void pkv_pool_destroy(pkv_pool *pool);
 
 /* Takes n free pages into pages_out[0..n-1].  PKV_ENOPAGES if fewer than n
  * are free (then nothing is taken). */
-pkv_status pkv_pool_alloc(pkv_pool *pool, int32_t n, int32_t *pages_out);
+PKV_API pkv_status pkv_pool_alloc(pkv_pool *pool, int32_t n, int32_t *pages_out);
 
 /* Returns n pages.  PKV_EINVAL if a page is 0, out of range or already free
  * (then nothing is returned). */
-pkv_status pkv_pool_free(pkv_pool *pool, const int32_t *pages, int32_t n);
+PKV_API pkv_status pkv_pool_free(pkv_pool *pool, const int32_t *pages, int32_t n);
 
-int32_t pkv_pool_num_free(const pkv_pool *pool);
+PKV_API int32_t pkv_pool_num_free(const pkv_pool *pool);
 
 /* Mixes the free list with a seeded permutation (splitmix64-driven
  * Fisher-Yates), so later allocations are scattered over the pool. */
-pkv_status pkv_pool_shuffle(pkv_pool *pool, uint64_t seed);
+PKV_API pkv_status pkv_pool_shuffle(pkv_pool *pool, uint64_t seed);
 
 /* Makes a host block_table row cover new_len tokens when it covers cur_len:
  * fills entries [ceil(cur_len/P), ceil(new_len/P)) from the pool.
  * PKV_EINVAL if new_len < cur_len or the row would exceed max_blocks;
  * PKV_ENOPAGES if the pool is short (then the row is unchanged). */
-pkv_status pkv_table_reserve(pkv_pool *pool, int32_t *block_table_row, int32_t max_blocks,
+PKV_API pkv_status pkv_table_reserve(pkv_pool *pool, int32_t *block_table_row, int32_t max_blocks,
                              int32_t page_size, int32_t cur_len, int32_t new_len);
 
 /* Returns the pages of a row covering len tokens to the pool and zeroes the
  * row's entries. */
-pkv_status pkv_table_release(pkv_pool *pool, int32_t *block_table_row, int32_t max_blocks,
+PKV_API pkv_status pkv_table_release(pkv_pool *pool, int32_t *block_table_row, int32_t max_blocks,
                              int32_t page_size, int32_t len);
 
 /* Host-side check of block_table / cache_seqlens (host copies) for a decode
  * or append of extra_tokens per row: returns PKV_EINVAL with *bad_row set to
  * the first failing row, else PKV_OK.  For tests and debugging. */
-pkv_status pkv_validate_host(const pkv_cache_desc *desc, const int32_t *block_table_host,
+PKV_API pkv_status pkv_validate_host(const pkv_cache_desc *desc, const int32_t *block_table_host,
                              int32_t max_blocks, const int32_t *seqlens_host, int32_t batch,
                              int32_t extra_tokens, int32_t *bad_row);
 
 /* Bytes of one K or V pool for `desc` (num_pages * page_size * num_kv_heads
  * * head_dim * 2), 0 on invalid arguments. */
-uint64_t pkv_pool_bytes(const pkv_cache_desc *desc);
+PKV_API uint64_t pkv_pool_bytes(const pkv_cache_desc *desc);
 
 /* Static description of a status code. */
-const char *pkv_status_str(pkv_status status);
+PKV_API const char *pkv_status_str(pkv_status status);
 
 #ifdef __cplusplus
 }

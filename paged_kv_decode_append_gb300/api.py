@@ -1,0 +1,175 @@
+"""Python binding of the C ABI (``include/pkv.h``): same names, torch tensors
+in, argument marshalling only.  Every step of the computation runs in the
+library's CUDA kernels; there is no Python or CPU fallback, and a missing or
+unloadable library raises.
+"""
+from __future__ import annotations
+
+import ctypes
+
+import numpy as np
+import torch
+
+from . import _lib
+from ._lib import CacheDesc
+
+NHD = 0
+HND = 1
+
+OK, EINVAL, EUNSUPPORTED, ECUDA, ENOPAGES, EWORKSPACE = range(6)
+ERR_PAGE, ERR_OVERFLOW, ERR_TIMEOUT = 1, 2, 4
+
+
+class PkvError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        msg = _lib.load().pkv_status_str(status).decode()
+        super().__init__(f"{what}: {msg} (status {status})")
+
+
+def _check(status: int, what: str) -> None:
+    if status != OK:
+        raise PkvError(status, what)
+
+
+def cache_desc(k_cache: torch.Tensor, layout: int = NHD) -> CacheDesc:
+    """Descriptor of a pool tensor: NHD ``[pages, P, Hkv, D]`` or HND
+    ``[pages, Hkv, P, D]``."""
+    if k_cache.dim() != 4:
+        raise ValueError("cache must be 4-D")
+    if layout == NHD:
+        n, p, h, d = k_cache.shape
+    else:
+        n, h, p, d = k_cache.shape
+    return CacheDesc(n, p, h, d, layout)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(device) -> ctypes.c_void_p:
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _bf16(t, name):
+    if t is None:
+        return
+    if t.dtype != torch.bfloat16 or not t.is_contiguous() or not t.is_cuda:
+        raise ValueError(f"{name}: expected a contiguous CUDA bfloat16 tensor")
+
+
+def _i32(t, name):
+    if t is None:
+        return
+    if t.dtype != torch.int32 or not t.is_contiguous() or not t.is_cuda:
+        raise ValueError(f"{name}: expected a contiguous CUDA int32 tensor")
+
+
+def pkv_decode_workspace_size(batch: int, max_blocks: int, num_q_heads: int, desc: CacheDesc) -> int:
+    return int(_lib.load().pkv_decode_workspace_size(batch, max_blocks, num_q_heads, ctypes.byref(desc)))
+
+
+def decode_workspace(batch: int, max_blocks: int, num_q_heads: int, desc: CacheDesc, device) -> torch.Tensor:
+    """A zero-filled workspace for pkv_decode_attn (reusable across calls)."""
+    n = pkv_decode_workspace_size(batch, max_blocks, num_q_heads, desc)
+    if n == 0:
+        raise PkvError(EUNSUPPORTED, "pkv_decode_workspace_size")
+    return torch.zeros(n, dtype=torch.uint8, device=device)
+
+
+def pkv_append(k_cache, v_cache, k_new, v_new, block_table, cache_seqlens, append_indptr=None, err_flag=None,
+               layout: int = NHD) -> None:
+    """Bit-copy ``k_new``/``v_new`` ``[T, Hkv, D]`` into their page slots."""
+    for t, n in ((k_cache, "k_cache"), (v_cache, "v_cache"), (k_new, "k_new"), (v_new, "v_new")):
+        _bf16(t, n)
+    for t, n in ((block_table, "block_table"), (cache_seqlens, "cache_seqlens"), (append_indptr, "append_indptr"),
+                 (err_flag, "err_flag")):
+        _i32(t, n)
+    desc = cache_desc(k_cache, layout)
+    st = _lib.load().pkv_append(ctypes.byref(desc), _ptr(k_cache), _ptr(v_cache), _ptr(k_new), _ptr(v_new),
+                                k_new.shape[0], _ptr(append_indptr), _ptr(block_table), block_table.shape[1],
+                                _ptr(cache_seqlens), cache_seqlens.shape[0], _ptr(err_flag),
+                                _stream(k_cache.device))
+    _check(st, "pkv_append")
+
+
+def pkv_decode_attn(k_cache, v_cache, q, k_new, v_new, block_table, cache_seqlens, softmax_scale: float,
+                    out=None, lse=None, workspace=None, err_flag=None, layout: int = NHD) -> torch.Tensor:
+    """Fused append + decode attention; returns ``out`` ``[B, Hq, D]`` bf16."""
+    for t, n in ((k_cache, "k_cache"), (v_cache, "v_cache"), (q, "q"), (k_new, "k_new"), (v_new, "v_new"),
+                 (out, "out")):
+        _bf16(t, n)
+    for t, n in ((block_table, "block_table"), (cache_seqlens, "cache_seqlens"), (err_flag, "err_flag")):
+        _i32(t, n)
+    if lse is not None and (lse.dtype != torch.float32 or not lse.is_contiguous()):
+        raise ValueError("lse: expected contiguous float32")
+    desc = cache_desc(k_cache, layout)
+    B, Hq, D = q.shape
+    if out is None:
+        out = torch.empty_like(q)
+    if workspace is None:
+        workspace = decode_workspace(B, block_table.shape[1], Hq, desc, q.device)
+    st = _lib.load().pkv_decode_attn(
+        ctypes.byref(desc), _ptr(k_cache), _ptr(v_cache), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(block_table),
+        block_table.shape[1], _ptr(cache_seqlens), B, Hq, float(softmax_scale), _ptr(out), _ptr(lse),
+        _ptr(workspace), workspace.numel(), _ptr(err_flag), _stream(q.device))
+    _check(st, "pkv_decode_attn")
+    return out
+
+
+def pkv_pool_bytes(desc: CacheDesc) -> int:
+    return int(_lib.load().pkv_pool_bytes(ctypes.byref(desc)))
+
+
+def pkv_validate_host(desc: CacheDesc, block_table: np.ndarray, seqlens: np.ndarray, extra_tokens: int):
+    """Host check of a block table; returns (status, first bad row or -1)."""
+    bt = np.ascontiguousarray(block_table, dtype=np.int32)
+    sl = np.ascontiguousarray(seqlens, dtype=np.int32)
+    bad = ctypes.c_int32(-1)
+    st = _lib.load().pkv_validate_host(ctypes.byref(desc), bt.ctypes.data_as(_lib.I32P), bt.shape[1],
+                                       sl.ctypes.data_as(_lib.I32P), sl.shape[0], extra_tokens, ctypes.byref(bad))
+    return st, bad.value
+
+
+class PagePool:
+    """Host page pool (``pkv_pool_*``): pages 1..num_pages-1, page 0 never
+    handed out; a fresh pool hands pages out in ascending order."""
+
+    def __init__(self, num_pages: int):
+        self._lib = _lib.load()
+        self._p = self._lib.pkv_pool_create(num_pages)
+        if not self._p:
+            raise PkvError(EINVAL, "pkv_pool_create")
+
+    def __del__(self):
+        if getattr(self, "_p", None):
+            self._lib.pkv_pool_destroy(self._p)
+            self._p = None
+
+    @property
+    def num_free(self) -> int:
+        return int(self._lib.pkv_pool_num_free(self._p))
+
+    def alloc(self, n: int) -> np.ndarray:
+        out = np.zeros(max(n, 0), np.int32)
+        _check(self._lib.pkv_pool_alloc(self._p, n, out.ctypes.data_as(_lib.I32P)), "pkv_pool_alloc")
+        return out
+
+    def free(self, pages) -> None:
+        pages = np.ascontiguousarray(pages, dtype=np.int32)
+        _check(self._lib.pkv_pool_free(self._p, pages.ctypes.data_as(_lib.I32P), pages.size), "pkv_pool_free")
+
+    def shuffle(self, seed: int) -> None:
+        _check(self._lib.pkv_pool_shuffle(self._p, seed), "pkv_pool_shuffle")
+
+    def reserve(self, row: np.ndarray, page_size: int, cur_len: int, new_len: int) -> None:
+        """Extend one block-table row (an int32 numpy view) from cur_len to new_len tokens."""
+        assert row.dtype == np.int32 and row.flags.c_contiguous
+        _check(self._lib.pkv_table_reserve(self._p, row.ctypes.data_as(_lib.I32P), row.size, page_size, cur_len,
+                                           new_len), "pkv_table_reserve")
+
+    def release(self, row: np.ndarray, page_size: int, length: int) -> None:
+        assert row.dtype == np.int32 and row.flags.c_contiguous
+        _check(self._lib.pkv_table_release(self._p, row.ctypes.data_as(_lib.I32P), row.size, page_size, length),
+               "pkv_table_release")

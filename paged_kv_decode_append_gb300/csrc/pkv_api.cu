@@ -1,0 +1,272 @@
+// pkv_api.cu -- C ABI front end: argument validation (no device reads, no
+// host sync), workspace sizing, TMA tensor-map encoding and kernel launches.
+#include <cudaTypedefs.h>
+#include <math.h>
+#include <mutex>
+
+#include "pkv_internal.h"
+
+namespace pkv {
+
+namespace {
+
+bool aligned16(const void *p)
+{
+    return (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
+}
+
+int log2_exact(int x)
+{
+    if (x <= 0 || (x & (x - 1)) != 0)
+        return -1;
+    int s = 0;
+    while ((1 << s) < x)
+        ++s;
+    return s;
+}
+
+// Geometry checks shared by every entry point.
+pkv_status check_desc(const pkv_cache_desc *d)
+{
+    if (d == nullptr)
+        return PKV_EINVAL;
+    if (d->num_pages < 2 || d->num_kv_heads < 1 || d->page_size < 1 || d->head_dim < 1)
+        return PKV_EINVAL;
+    if (d->layout != PKV_NHD && d->layout != PKV_HND)
+        return PKV_EINVAL;
+    if (log2_exact(d->page_size) < 0 || d->page_size > 256)
+        return PKV_EUNSUPPORTED;
+    if (d->head_dim != 64 && d->head_dim != 128 && d->head_dim != 256)
+        return PKV_EUNSUPPORTED;
+    // TMA coordinates are int32: the token (NHD) or page-head (HND) axis must fit.
+    const int64_t rows = d->layout == PKV_NHD ? (int64_t)d->num_pages * d->page_size
+                                              : (int64_t)d->num_pages * d->num_kv_heads;
+    if (rows > INT32_MAX)
+        return PKV_EUNSUPPORTED;
+    return PKV_OK;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+int current_device()
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return -1;
+    return dev;
+}
+
+constexpr int kMaxDevices = 64;
+
+} // namespace
+
+int sm_count(int device)
+{
+    static int cache[kMaxDevices] = {0};
+    if (device < 0 || device >= kMaxDevices)
+        return 1;
+    if (cache[device] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, device) != cudaSuccess || n < 1)
+            n = 1;
+        cache[device] = n;
+    }
+    return cache[device];
+}
+
+CUresult encode_pool_map(CUtensorMap *map, const pkv_cache_desc &d, void *base, int box_tokens)
+{
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (enc == nullptr)
+        return CUDA_ERROR_NOT_FOUND;
+    const cuuint64_t D = (cuuint64_t)d.head_dim;
+    cuuint64_t dims[3];
+    cuuint64_t strides[2]; // bytes, for dims 1 and 2
+    cuuint32_t box[3];
+    if (d.layout == PKV_NHD) { // [pages*P, Hkv, D]
+        dims[0] = D;
+        dims[1] = (cuuint64_t)d.num_kv_heads;
+        dims[2] = (cuuint64_t)d.num_pages * d.page_size;
+        strides[0] = D * 2;
+        strides[1] = D * 2 * d.num_kv_heads;
+        box[0] = (cuuint32_t)D;
+        box[1] = 1;
+        box[2] = (cuuint32_t)box_tokens;
+    } else { // [pages*Hkv, P, D]
+        dims[0] = D;
+        dims[1] = (cuuint64_t)d.page_size;
+        dims[2] = (cuuint64_t)d.num_pages * d.num_kv_heads;
+        strides[0] = D * 2;
+        strides[1] = D * 2 * d.page_size;
+        box[0] = (cuuint32_t)D;
+        box[1] = (cuuint32_t)box_tokens;
+        box[2] = 1;
+    }
+    const cuuint32_t elem_strides[3] = {1, 1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, elem_strides,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
+} // namespace pkv
+
+using namespace pkv;
+
+extern "C" {
+
+const char *pkv_status_str(pkv_status status)
+{
+    switch (status) {
+    case PKV_OK:
+        return "ok";
+    case PKV_EINVAL:
+        return "invalid argument";
+    case PKV_EUNSUPPORTED:
+        return "unsupported size or layout";
+    case PKV_ECUDA:
+        return "CUDA call failed";
+    case PKV_ENOPAGES:
+        return "page pool exhausted";
+    case PKV_EWORKSPACE:
+        return "workspace missing or too small";
+    }
+    return "unknown status";
+}
+
+uint64_t pkv_pool_bytes(const pkv_cache_desc *desc)
+{
+    if (desc == nullptr || desc->num_pages < 0 || desc->page_size < 0 || desc->num_kv_heads < 0 ||
+        desc->head_dim < 0)
+        return 0;
+    return (uint64_t)desc->num_pages * (uint64_t)desc->page_size * (uint64_t)desc->num_kv_heads *
+           (uint64_t)desc->head_dim * 2u;
+}
+
+pkv_status pkv_append(const pkv_cache_desc *desc, void *k_cache, void *v_cache, const void *k_new,
+                      const void *v_new, int32_t num_tokens, const int32_t *append_indptr,
+                      const int32_t *block_table, int32_t max_blocks, const int32_t *cache_seqlens, int32_t batch,
+                      int32_t *err_flag, void *stream)
+{
+    const pkv_status st = check_desc(desc);
+    if (st != PKV_OK)
+        return st;
+    if (batch < 0 || num_tokens < 0 || max_blocks < 1)
+        return PKV_EINVAL;
+    if (append_indptr == nullptr && num_tokens != batch)
+        return PKV_EINVAL;
+    if (batch == 0 || num_tokens == 0)
+        return PKV_OK;
+    if (k_cache == nullptr || v_cache == nullptr || k_new == nullptr || v_new == nullptr ||
+        block_table == nullptr || cache_seqlens == nullptr)
+        return PKV_EINVAL;
+    if (!aligned16(k_cache) || !aligned16(v_cache) || !aligned16(k_new) || !aligned16(v_new))
+        return PKV_EINVAL;
+    AppendArgs a;
+    a.desc = *desc;
+    a.page_shift = log2_exact(desc->page_size);
+    a.k_cache = k_cache;
+    a.v_cache = v_cache;
+    a.k_new = k_new;
+    a.v_new = v_new;
+    a.num_tokens = num_tokens;
+    a.append_indptr = append_indptr;
+    a.block_table = block_table;
+    a.max_blocks = max_blocks;
+    a.cache_seqlens = cache_seqlens;
+    a.batch = batch;
+    a.err_flag = err_flag;
+    return launch_append(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PKV_OK : PKV_ECUDA;
+}
+
+size_t pkv_decode_workspace_size(int32_t batch, int32_t max_blocks, int32_t num_q_heads, const pkv_cache_desc *desc)
+{
+    if (check_desc(desc) != PKV_OK || batch < 0 || batch > kMaxDecodeBatch || max_blocks < 1 || num_q_heads < 1)
+        return 0;
+    DecodeShape s;
+    if (!decode_shape(batch, max_blocks, num_q_heads, *desc, &s))
+        return 0;
+    return s.bytes;
+}
+
+pkv_status pkv_decode_attn(const pkv_cache_desc *desc, void *k_cache, void *v_cache, const void *q,
+                           const void *k_new, const void *v_new, const int32_t *block_table, int32_t max_blocks,
+                           const int32_t *cache_seqlens, int32_t batch, int32_t num_q_heads, float softmax_scale,
+                           void *out, float *lse, void *workspace, size_t workspace_bytes, int32_t *err_flag,
+                           void *stream)
+{
+    const pkv_status st = check_desc(desc);
+    if (st != PKV_OK)
+        return st;
+    if (batch < 0 || max_blocks < 1 || num_q_heads < 1 || !isfinite(softmax_scale))
+        return PKV_EINVAL;
+    if (batch > kMaxDecodeBatch)
+        return PKV_EUNSUPPORTED;
+    if ((k_new == nullptr) != (v_new == nullptr))
+        return PKV_EINVAL;
+    if (num_q_heads % desc->num_kv_heads != 0)
+        return PKV_EINVAL;
+    DecodeShape shape;
+    if (!decode_shape(batch, max_blocks, num_q_heads, *desc, &shape))
+        return PKV_EUNSUPPORTED;
+    if (batch == 0)
+        return PKV_OK;
+    if (k_cache == nullptr || v_cache == nullptr || q == nullptr || out == nullptr || block_table == nullptr ||
+        cache_seqlens == nullptr)
+        return PKV_EINVAL;
+    if (!aligned16(k_cache) || !aligned16(v_cache) || !aligned16(q) || !aligned16(out) ||
+        (k_new != nullptr && (!aligned16(k_new) || !aligned16(v_new))))
+        return PKV_EINVAL;
+    if (workspace == nullptr || workspace_bytes < shape.bytes || !aligned16(workspace))
+        return PKV_EWORKSPACE;
+
+    const int dev = current_device();
+    if (dev < 0)
+        return PKV_ECUDA;
+    DecodeArgs a;
+    a.desc = *desc;
+    a.page_shift = log2_exact(desc->page_size);
+    a.batch = batch;
+    a.num_q_heads = num_q_heads;
+    a.max_blocks = max_blocks;
+    a.q_scale = softmax_scale * 1.4426950408889634f;
+    a.block_table = block_table;
+    a.cache_seqlens = cache_seqlens;
+    a.q = q;
+    a.k_new = k_new;
+    a.v_new = v_new;
+    a.k_cache = k_cache;
+    a.v_cache = v_cache;
+    a.out = out;
+    a.lse = lse;
+    a.workspace = workspace;
+    a.err_flag = err_flag;
+    a.shape = shape;
+    a.target_items = decode_target_items(dev, desc->head_dim, shape.heads_per_cta);
+    const int64_t units = (int64_t)batch * shape.units_per_row;
+    int64_t grid = a.target_items + units;
+    if (grid > shape.cap_items)
+        grid = shape.cap_items;
+    a.grid = (int)grid;
+
+    const int box = desc->page_size < kDecodeTile ? desc->page_size : kDecodeTile;
+    CUtensorMap tm_k, tm_v;
+    if (encode_pool_map(&tm_k, *desc, k_cache, box) != CUDA_SUCCESS ||
+        encode_pool_map(&tm_v, *desc, v_cache, box) != CUDA_SUCCESS)
+        return PKV_ECUDA;
+    return launch_decode(a, tm_k, tm_v, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PKV_OK : PKV_ECUDA;
+}
+
+} // extern "C"

@@ -1,0 +1,93 @@
+// pkv_internal.h -- host-side plumbing shared by the C-ABI front end and the
+// kernel launchers.  Not part of the public interface.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "pkv.h"
+
+namespace pkv {
+
+// Largest batch one decode call plans for (the per-CTA plan lives in shared
+// memory: two int32 per row).
+constexpr int kMaxDecodeBatch = 1024;
+// Tokens per pipeline tile of the decode kernel.
+constexpr int kDecodeTile = 32;
+// Smallest split-KV chunk, in tokens.
+constexpr int kDecodeChunkMin = 64;
+// A chunk never spans more than this many pages (its page ids are staged in
+// shared memory).
+constexpr int kDecodeChunkMaxPages = 256;
+
+// Static split of the decode problem: which heads one CTA owns and how the
+// workspace is carved.  Computed identically by the workspace-size query and
+// by the launch.
+struct DecodeShape {
+    int group;          // num_q_heads / num_kv_heads
+    int heads_per_cta;  // q heads of one kv head handled by one CTA
+    int n_sub;          // group / heads_per_cta
+    int units_per_row;  // num_kv_heads * n_sub
+    int chunk_max;      // largest chunk in tokens (multiple of kDecodeTile)
+    int64_t cap_items;  // partial-result slots in the workspace
+    size_t off_ml, off_o, bytes;
+};
+
+// Fills `s`; returns false for unsupported combinations.
+bool decode_shape(int batch, int max_blocks, int num_q_heads, const pkv_cache_desc &d, DecodeShape *s);
+
+// Number of split-KV work items a call aims for on this device (a few per
+// resident CTA slot).
+int decode_target_items(int device, int head_dim, int heads_per_cta);
+
+struct DecodeArgs {
+    pkv_cache_desc desc;
+    int page_shift;
+    int batch, num_q_heads, max_blocks;
+    float q_scale; // softmax_scale * log2(e)
+    const int32_t *block_table;
+    const int32_t *cache_seqlens;
+    const void *q;
+    const void *k_new;
+    const void *v_new;
+    void *k_cache;
+    void *v_cache;
+    void *out;
+    float *lse;
+    void *workspace;
+    int32_t *err_flag;
+    DecodeShape shape;
+    int target_items;
+    int grid;
+};
+
+cudaError_t launch_decode(const DecodeArgs &a, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
+                          cudaStream_t stream);
+
+struct AppendArgs {
+    pkv_cache_desc desc;
+    int page_shift;
+    void *k_cache;
+    void *v_cache;
+    const void *k_new;
+    const void *v_new;
+    int num_tokens;
+    const int32_t *append_indptr;
+    const int32_t *block_table;
+    int max_blocks;
+    const int32_t *cache_seqlens;
+    int batch;
+    int32_t *err_flag;
+};
+
+cudaError_t launch_append(const AppendArgs &a, cudaStream_t stream);
+
+// Tensor map over one K or V pool whose boxes are `box_tokens` consecutive
+// tokens of one kv head ([box_tokens, head_dim] in shared memory).
+CUresult encode_pool_map(CUtensorMap *map, const pkv_cache_desc &d, void *base, int box_tokens);
+
+int sm_count(int device);
+
+} // namespace pkv

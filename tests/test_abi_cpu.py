@@ -1,0 +1,168 @@
+"""The C-ABI library on the CPU: it loads, exports every symbol include/pkv.h
+declares, and its host-only parts (page pool, block-table helpers, host
+validation, sizing, argument checks that return before any CUDA call) behave
+as documented.  No compute call is made here."""
+import ctypes
+import json
+import os
+import re
+
+import numpy as np
+import pytest
+
+import paged_kv_decode_append_gb300 as pkv
+from paged_kv_decode_append_gb300 import _lib
+from paged_kv_decode_append_gb300.api import CacheDesc
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = open(os.path.join(ROOT, "include", "pkv.h")).read()
+GOLDEN = json.load(open(os.path.join(ROOT, "tests", "golden", "printed_values.json")))
+
+
+def declared_functions():
+    return re.findall(r"PKV_API\s+[\w\s\*]*?\b(pkv_\w+)\s*\(", HEADER)
+
+
+def test_every_declared_symbol_is_exported_and_bound():
+    lib = _lib.load()
+    names = declared_functions()
+    assert len(names) >= 14
+    for n in names:
+        assert hasattr(lib, n), n
+        assert n in _lib.SIGNATURES, f"{n} has no ctypes signature"
+    assert set(_lib.SIGNATURES) == set(names)
+
+
+def test_status_strings():
+    lib = _lib.load()
+    for code in range(6):
+        assert lib.pkv_status_str(code) not in (None, b"", b"unknown status")
+    assert lib.pkv_status_str(99) == b"unknown status"
+
+
+def test_pool_hands_out_ascending_and_never_page_zero():
+    pool = pkv.PagePool(8)
+    assert pool.num_free == 7
+    assert list(pool.alloc(3)) == [1, 2, 3]
+    with pytest.raises(pkv.PkvError) as e:
+        pool.alloc(5)  # only 4 left: nothing taken
+    assert e.value.status == pkv.api.ENOPAGES
+    assert pool.num_free == 4
+    assert list(pool.alloc(4)) == [4, 5, 6, 7]
+    assert pool.num_free == 0
+
+
+def test_pool_free_validates_everything_first():
+    pool = pkv.PagePool(6)
+    got = pool.alloc(3)
+    for bad in ([0], [6], [4], [1, 1], [2, -1]):
+        with pytest.raises(pkv.PkvError):
+            pool.free(bad)
+        assert pool.num_free == 2  # nothing returned
+    pool.free([3, 1])
+    assert pool.num_free == 4
+    assert list(pool.alloc(2)) == [3, 1]  # returned pages are reused first
+    assert set(got) == {1, 2, 3}
+
+
+def test_shuffle_is_a_seeded_permutation():
+    a, b, c = pkv.PagePool(1000), pkv.PagePool(1000), pkv.PagePool(1000)
+    a.shuffle(7)
+    b.shuffle(7)
+    c.shuffle(8)
+    pa, pb, pc = a.alloc(999), b.alloc(999), c.alloc(999)
+    assert np.array_equal(pa, pb) and not np.array_equal(pa, pc)
+    assert sorted(pa.tolist()) == list(range(1, 1000))
+    assert not np.array_equal(pa, np.arange(1, 1000))
+
+
+def test_table_reserve_and_release():
+    pool = pkv.PagePool(20)
+    row = np.zeros(6, np.int32)
+    pool.reserve(row, 16, 0, 17)          # 2 blocks
+    assert list(row[:2]) == [1, 2] and row[2] == 0
+    pool.reserve(row, 16, 17, 32)         # still 2 blocks
+    assert pool.num_free == 17
+    pool.reserve(row, 16, 32, 33)         # third block
+    assert list(row[:3]) == [1, 2, 3]
+    with pytest.raises(pkv.PkvError):
+        pool.reserve(row, 16, 33, 7 * 16)  # beyond max_blocks
+    with pytest.raises(pkv.PkvError):
+        pool.reserve(row, 16, 33, 20)      # shrinking
+    pool.release(row, 16, 33)
+    assert pool.num_free == 19 and not row.any()
+    small = pkv.PagePool(3)
+    row2 = np.zeros(4, np.int32)
+    with pytest.raises(pkv.PkvError) as e:
+        small.reserve(row2, 4, 0, 13)     # needs 4 pages, 2 free
+    assert e.value.status == pkv.api.ENOPAGES and not row2.any() and small.num_free == 2
+
+
+def test_validate_host():
+    d = CacheDesc(10, 4, 2, 64, 0)
+    bt = np.array([[1, 2, 0], [3, 0, 0], [9, 0, 0]], np.int32)
+    assert pkv.pkv_validate_host(d, bt, np.array([5, 3, -1], np.int32), 1) == (0, -1)
+    assert pkv.pkv_validate_host(d, bt, np.array([5, 4, -1], np.int32), 1) == (pkv.api.EINVAL, 1)
+    assert pkv.pkv_validate_host(d, bt, np.array([5, 3, 12], np.int32), 0) == (pkv.api.EINVAL, 2)
+    bt[2, 0] = 10  # == num_pages: out of range
+    assert pkv.pkv_validate_host(d, bt, np.array([5, 3, 1], np.int32), 0) == (pkv.api.EINVAL, 2)
+
+
+def test_pool_bytes_matches_printed_example():
+    g = GOLDEN["pool_bytes"]
+    per_layer_kv = 2 * pkv.pkv_pool_bytes(CacheDesc(g["num_pages"], g["page_size"], g["num_kv_heads"],
+                                                    g["head_dim"], 0))
+    assert per_layer_kv * g["layers"] == g["total_bytes"]
+
+
+def test_workspace_size():
+    d = CacheDesc(65536, 16, 8, 128, 0)
+    n = pkv.pkv_decode_workspace_size(32, 65, 32, d)
+    assert n > 0 and n % 256 == 0
+    assert pkv.pkv_decode_workspace_size(64, 2049, 32, d) > n
+    assert pkv.pkv_decode_workspace_size(1025, 65, 32, d) == 0
+    assert pkv.pkv_decode_workspace_size(32, 65, 30, d) == 0          # Hq % Hkv
+    assert pkv.pkv_decode_workspace_size(32, 65, 32, CacheDesc(100, 16, 8, 96, 0)) == 0   # D
+    assert pkv.pkv_decode_workspace_size(32, 65, 32, CacheDesc(100, 12, 8, 128, 0)) == 0  # P
+
+
+FAKE = ctypes.c_void_p(0x10000)  # aligned, never dereferenced on the host paths below
+
+
+def _decode(lib, desc, batch=4, hq=8, ws=FAKE, ws_bytes=1 << 30, q=FAKE, k_new=None, v_new=None, scale=0.1):
+    return lib.pkv_decode_attn(ctypes.byref(desc), FAKE, FAKE, q, k_new, v_new, FAKE, 4, FAKE, batch, hq, scale,
+                               FAKE, None, ws, ws_bytes, None, None)
+
+
+def test_decode_argument_errors_return_before_any_launch():
+    lib = _lib.load()
+    d = CacheDesc(64, 16, 2, 128, 0)
+    assert _decode(lib, CacheDesc(1, 16, 2, 128, 0)) == pkv.api.EINVAL        # no page beside the null page
+    assert _decode(lib, CacheDesc(64, 16, 2, 128, 3)) == pkv.api.EINVAL       # layout
+    assert _decode(lib, CacheDesc(64, 24, 2, 128, 0)) == pkv.api.EUNSUPPORTED  # page size
+    assert _decode(lib, CacheDesc(64, 16, 2, 80, 0)) == pkv.api.EUNSUPPORTED   # head dim
+    assert _decode(lib, d, hq=7) == pkv.api.EINVAL                             # Hq % Hkv
+    assert _decode(lib, d, hq=6) == pkv.api.EUNSUPPORTED                       # group 3
+    assert _decode(lib, d, q=None) == pkv.api.EINVAL
+    assert _decode(lib, d, q=ctypes.c_void_p(0x10008)) == pkv.api.EINVAL       # misaligned
+    assert _decode(lib, d, k_new=FAKE) == pkv.api.EINVAL                       # k_new without v_new
+    assert _decode(lib, d, scale=float("nan")) == pkv.api.EINVAL
+    assert _decode(lib, d, ws=None) == pkv.api.EWORKSPACE
+    assert _decode(lib, d, ws_bytes=16) == pkv.api.EWORKSPACE
+    assert _decode(lib, d, batch=0) == pkv.api.OK                              # nothing to do
+    assert _decode(lib, d, batch=2000) == pkv.api.EUNSUPPORTED
+
+
+def test_append_argument_errors():
+    lib = _lib.load()
+    d = CacheDesc(64, 16, 2, 128, 0)
+
+    def app(desc=d, k_new=FAKE, ntok=4, indptr=None, batch=4):
+        return lib.pkv_append(ctypes.byref(desc), FAKE, FAKE, k_new, FAKE, ntok, indptr, FAKE, 4, FAKE, batch,
+                              None, None)
+
+    assert app(ntok=3) == pkv.api.EINVAL            # one token per row without indptr
+    assert app(k_new=None) == pkv.api.EINVAL
+    assert app(k_new=ctypes.c_void_p(0x10004)) == pkv.api.EINVAL
+    assert app(desc=CacheDesc(64, 16, 2, 100, 0)) == pkv.api.EUNSUPPORTED
+    assert app(batch=0, ntok=0) == pkv.api.OK

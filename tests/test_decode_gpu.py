@@ -1,0 +1,222 @@
+"""GPU parity of the fused append + decode kernel against the fp64 oracle.
+
+Outputs within max-abs 1e-2 / max-rel 1e-2 (see gpu_util); appended cache
+bytes and page routing bit-exact (sha256 of whole pools).
+"""
+import hashlib
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_decode_append_gb300 as pkv
+from paged_kv_decode_append_gb300 import workloads as wl
+
+from gpu_util import assert_close, assert_lse_close, desc_of, f32, oracle_decode_compact
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+def _sha(t: torch.Tensor) -> str:
+    return hashlib.sha256(wl.bits(t).tobytes()).hexdigest()
+
+
+def _run(case, with_new=True, layout=None, err=None, workspace=None):
+    layout = case.layout if layout is None else layout
+    bt = torch.as_tensor(case.block_table, device=DEV)
+    sl = torch.as_tensor(case.cache_seqlens, device=DEV)
+    lse = torch.empty(case.batch, case.num_q_heads, dtype=torch.float32, device=DEV)
+    out = pkv.pkv_decode_attn(case.k_cache, case.v_cache, case.q,
+                              case.k_new if with_new else None, case.v_new if with_new else None,
+                              bt, sl, case.softmax_scale, lse=lse, err_flag=err, workspace=workspace,
+                              layout=layout)
+    torch.cuda.synchronize()
+    return out, lse
+
+
+def _oracle_full(case, with_new=True):
+    """Oracle on full host copies of the pools; returns out, lse, err, k, v."""
+    k, v = wl.bits(case.k_cache).copy(), wl.bits(case.v_cache).copy()
+    out, lse, err, err_rows = oracle.decode(desc_of(case), k, v, wl.bits(case.q),
+                                            wl.bits(case.k_new) if with_new else None,
+                                            wl.bits(case.v_new) if with_new else None,
+                                            case.block_table, case.cache_seqlens, case.softmax_scale)
+    return out, lse, err, k, v
+
+
+@pytest.mark.parametrize("with_new", [True, False])
+def test_tiny_parity_and_bit_exact_append(with_new):
+    case = wl.tiny(device=DEV)
+    ref_out, ref_lse, ref_err, ref_k, ref_v = _oracle_full(case, with_new)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out, lse = _run(case, with_new, err=err)
+    assert ref_err == 0 and int(err.item()) == 0
+    assert_close(f32(out), ref_out)
+    assert_lse_close(lse.cpu().numpy(), ref_lse)
+    assert hashlib.sha256(ref_k.tobytes()).hexdigest() == _sha(case.k_cache)
+    assert hashlib.sha256(ref_v.tobytes()).hexdigest() == _sha(case.v_cache)
+
+
+def test_qwen3_layer_full_parity():
+    case = wl.qwen3_decode(device=DEV)
+    ref_out, ref_lse, ref_err, _ = oracle_decode_compact(case)
+    out, lse = _run(case)
+    assert ref_err == 0
+    assert_close(f32(out), ref_out)
+    assert_lse_close(lse.cpu().numpy(), ref_lse)
+    # appended slots: each row's token L_b holds k_new / v_new bit for bit
+    kb, vb = wl.bits(case.k_cache), wl.bits(case.v_cache)
+    for b in range(case.batch):
+        L = int(case.cache_seqlens[b])
+        page, slot = case.block_table[b, L // 16], L % 16
+        assert np.array_equal(kb[page, slot], wl.bits(case.k_new)[b])
+        assert np.array_equal(vb[page, slot], wl.bits(case.v_new)[b])
+
+
+def test_skewed_full_parity():
+    case = wl.skewed_decode(device=DEV)
+    ref_out, ref_lse, ref_err, _ = oracle_decode_compact(case)
+    out, lse = _run(case)
+    assert ref_err == 0
+    assert_close(f32(out), ref_out)
+    assert_lse_close(lse.cpu().numpy(), ref_lse)
+
+
+@pytest.mark.parametrize("batch,contiguous", [(8, True), (64, False), (256, True)])
+def test_batch_sweep_steps(batch, contiguous):
+    """Three consecutive decode steps over two layer caches sharing one block
+    table; the oracle replays the same appends on its own copies."""
+    sw = wl.batch_sweep(batch, device=DEV, contiguous=contiguous, layers=2)
+    bt = torch.as_tensor(sw.block_table, device=DEV)
+    desc = pkv.cache_desc(sw.k_caches[0])
+    ws = pkv.decode_workspace(batch, sw.max_blocks, 32, desc, DEV)
+    host_k = [wl.bits(k).copy() for k in sw.k_caches]
+    host_v = [wl.bits(v).copy() for v in sw.v_caches]
+    od = oracle.CacheDesc(sw.num_pages, sw.page_size, 8, 128, wl.NHD)
+    for step in range(3):
+        lens = (sw.prompt_lens + step).astype(np.int32)
+        sl = torch.as_tensor(lens, device=DEV)
+        for layer, (q, kn, vn) in enumerate(wl.sweep_step_inputs(sw, step, DEV)):
+            lse = torch.empty(batch, 32, dtype=torch.float32, device=DEV)
+            out = pkv.pkv_decode_attn(sw.k_caches[layer], sw.v_caches[layer], q, kn, vn, bt, sl,
+                                      sw.softmax_scale, lse=lse, workspace=ws)
+            ref_out, ref_lse, err, _ = oracle.decode(od, host_k[layer], host_v[layer], wl.bits(q), wl.bits(kn),
+                                                     wl.bits(vn), sw.block_table, lens, sw.softmax_scale)
+            assert err == 0
+            assert_close(f32(out), ref_out)
+            assert_lse_close(lse.cpu().numpy(), ref_lse)
+    for layer in range(2):
+        assert hashlib.sha256(host_k[layer].tobytes()).hexdigest() == _sha(sw.k_caches[layer])
+        assert hashlib.sha256(host_v[layer].tobytes()).hexdigest() == _sha(sw.v_caches[layer])
+
+
+def _random_case(seed, B, Hq, Hkv, D, P, lens, layout=wl.NHD, spare=7):
+    g = torch.Generator().manual_seed(seed)
+    lens = np.asarray(lens, np.int32)
+    needed = (np.maximum(lens, 0) + 1 + P - 1) // P
+    NP = int(needed.sum()) + 1 + spare
+    max_blocks = int(needed.max()) + 1
+    order = (torch.randperm(NP - 1, generator=g).numpy() + 1).astype(np.int32)
+    bt = wl.assign_pages(needed, NP, max_blocks, order)
+    case = wl.PagedCase("rand", B, Hq, Hkv, D, P, NP, layout, max_blocks, bt, lens, 1.0 / math.sqrt(D),
+                        q=wl._randn_bf16((B, Hq, D), g, "cpu").to(DEV))
+    case.k_new = wl._randn_bf16((B, Hkv, D), g, "cpu").to(DEV)
+    case.v_new = wl._randn_bf16((B, Hkv, D), g, "cpu").to(DEV)
+    wl._fill_cache(case, g, DEV, "cpu")
+    return case
+
+
+SHAPES = [  # (Hq, Hkv, D, P)
+    (32, 8, 128, 16), (32, 8, 128, 128), (4, 2, 64, 16), (8, 8, 64, 1), (16, 2, 64, 8),
+    (64, 4, 64, 32), (8, 4, 256, 64), (8, 1, 256, 256), (16, 16, 128, 4), (32, 2, 128, 32),
+]
+
+
+@pytest.mark.parametrize("layout", [wl.NHD, wl.HND])
+@pytest.mark.parametrize("Hq,Hkv,D,P", SHAPES)
+def test_shapes_and_ragged_tails(layout, Hq, Hkv, D, P):
+    lens = [0, 1, 31, 32, 33, 95, 257, 700]
+    case = _random_case(100 + D + P + Hq, len(lens), Hq, Hkv, D, P, lens, layout)
+    ref_out, ref_lse, ref_err, ref_k, ref_v = _oracle_full(case)
+    out, lse = _run(case)
+    assert ref_err == 0
+    assert_close(f32(out), ref_out)
+    assert_lse_close(lse.cpu().numpy(), ref_lse)
+    assert hashlib.sha256(ref_k.tobytes()).hexdigest() == _sha(case.k_cache)
+    assert hashlib.sha256(ref_v.tobytes()).hexdigest() == _sha(case.v_cache)
+
+
+def test_single_key_is_exact():
+    case = wl.tiny(device=DEV)
+    case.cache_seqlens = np.zeros(case.batch, np.int32)
+    out, lse = _run(case)
+    want = wl.bits(case.v_new).repeat(case.group, axis=1)
+    assert np.array_equal(wl.bits(out), want)  # 1 key: softmax weight exactly 1
+
+
+def test_inactive_and_empty_rows():
+    case = wl.tiny(device=DEV)
+    case.cache_seqlens = np.array([-1, 0, 17, -5], np.int32)
+    before = _sha(case.k_cache)
+    out, lse = _run(case, with_new=False)
+    o = f32(out)
+    assert np.all(o[[0, 1, 3]] == 0) and np.all(np.isneginf(lse.cpu().numpy()[[0, 1, 3]]))
+    assert np.all(np.isfinite(o[2]))
+    assert _sha(case.k_cache) == before  # attend-only writes nothing
+
+
+def test_bad_pages_and_overflow_flag_and_zero_rows():
+    case = wl.tiny(device=DEV)
+    case.block_table = case.block_table.copy()
+    case.block_table[1, 1] = 0                     # null page used by a live token
+    case.block_table[2, 0] = case.num_pages + 5    # out of range
+    case.cache_seqlens = case.cache_seqlens.copy()
+    case.cache_seqlens[3] = case.max_blocks * case.page_size  # L + 1 does not fit
+    ref_out, ref_lse, ref_err, ref_k, ref_v = _oracle_full(case)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out, lse = _run(case, err=err)
+    assert int(err.item()) == ref_err == (oracle.ERR_PAGE | oracle.ERR_OVERFLOW)
+    o = f32(out)
+    assert np.all(o[1:] == 0) and np.all(np.isneginf(lse.cpu().numpy()[1:]))
+    assert_close(o[0], ref_out[0])
+    assert hashlib.sha256(ref_k.tobytes()).hexdigest() == _sha(case.k_cache)
+    assert hashlib.sha256(ref_v.tobytes()).hexdigest() == _sha(case.v_cache)
+
+
+def test_page_permutation_bit_identical():
+    case = wl.qwen3_decode(device=DEV, batch=8, num_pages=4096)
+    out0, lse0 = _run(case, with_new=False)
+    g = torch.Generator().manual_seed(5)
+    perm = np.concatenate([[0], torch.randperm(case.num_pages - 1, generator=g).numpy() + 1])
+    inv = torch.as_tensor(np.argsort(perm), device=DEV)
+    case.k_cache = case.k_cache[inv].contiguous()  # physical page p -> perm[p]
+    case.v_cache = case.v_cache[inv].contiguous()
+    case.block_table = np.where(case.block_table > 0, perm[case.block_table], 0).astype(np.int32)
+    out1, lse1 = _run(case, with_new=False)
+    assert torch.equal(out0, out1) and torch.equal(lse0, lse1)
+
+
+def test_workspace_reuse_is_stable():
+    case = wl.skewed_decode(device=DEV, batch=16, long_len=8192)
+    desc = pkv.cache_desc(case.k_cache)
+    ws = pkv.decode_workspace(case.batch, case.max_blocks, case.num_q_heads, desc, DEV)
+    a, la = _run(case, with_new=False, workspace=ws)
+    b, lb = _run(case, with_new=False, workspace=ws)
+    assert torch.equal(a, b) and torch.equal(la, lb)
+    assert int(ws[:4 * case.batch * 8].view(torch.int32).abs().sum().item()) == 0  # tickets back at zero
+
+
+def test_large_batch_limit():
+    lens = np.random.default_rng(0).integers(0, 40, 1024).astype(np.int32)
+    case = _random_case(9, 1024, 8, 2, 64, 16, lens)
+    ref_out, ref_lse, ref_err, _, _ = _oracle_full(case)
+    out, lse = _run(case)
+    assert_close(f32(out), ref_out)
+    assert_lse_close(lse.cpu().numpy(), ref_lse)
+    with pytest.raises(pkv.PkvError):
+        big = _random_case(9, 1025, 8, 2, 64, 16, np.zeros(1025, np.int32))
+        _run(big)
