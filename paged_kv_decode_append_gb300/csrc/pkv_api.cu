@@ -87,7 +87,8 @@ int sm_count(int device)
     return cache[device];
 }
 
-CUresult encode_pool_map(CUtensorMap *map, const pkv_cache_desc &d, void *base, int box_tokens)
+CUresult encode_pool_map(CUtensorMap *map, const pkv_cache_desc &d, void *base, int box_tokens, int box_dim,
+                         int swizzle)
 {
     PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
     if (enc == nullptr)
@@ -102,7 +103,7 @@ CUresult encode_pool_map(CUtensorMap *map, const pkv_cache_desc &d, void *base, 
         dims[2] = (cuuint64_t)d.num_pages * d.page_size;
         strides[0] = D * 2;
         strides[1] = D * 2 * d.num_kv_heads;
-        box[0] = (cuuint32_t)D;
+        box[0] = (cuuint32_t)box_dim;
         box[1] = 1;
         box[2] = (cuuint32_t)box_tokens;
     } else { // [pages*Hkv, P, D]
@@ -111,13 +112,14 @@ CUresult encode_pool_map(CUtensorMap *map, const pkv_cache_desc &d, void *base, 
         dims[2] = (cuuint64_t)d.num_pages * d.num_kv_heads;
         strides[0] = D * 2;
         strides[1] = D * 2 * d.page_size;
-        box[0] = (cuuint32_t)D;
+        box[0] = (cuuint32_t)box_dim;
         box[1] = (cuuint32_t)box_tokens;
         box[2] = 1;
     }
     const cuuint32_t elem_strides[3] = {1, 1, 1};
     return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, elem_strides,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 
@@ -254,17 +256,15 @@ pkv_status pkv_decode_attn(const pkv_cache_desc *desc, void *k_cache, void *v_ca
     a.workspace = workspace;
     a.err_flag = err_flag;
     a.shape = shape;
-    a.target_items = decode_target_items(dev, desc->head_dim, shape.heads_per_cta);
-    const int64_t units = (int64_t)batch * shape.units_per_row;
-    int64_t grid = a.target_items + units;
-    if (grid > shape.cap_items)
-        grid = shape.cap_items;
-    a.grid = (int)grid;
+    // persistent grid: every CTA that fits on the device at once
+    a.target_items = 0;
+    a.grid = decode_target_items(dev, desc->head_dim, shape.heads_per_cta);
 
-    const int box = desc->page_size < kDecodeTile ? desc->page_size : kDecodeTile;
+    const int box = decode_box_tokens(desc->page_size);
+    const int swz = decode_swizzle(desc->page_size);
     CUtensorMap tm_k, tm_v;
-    if (encode_pool_map(&tm_k, *desc, k_cache, box) != CUDA_SUCCESS ||
-        encode_pool_map(&tm_v, *desc, v_cache, box) != CUDA_SUCCESS)
+    if (encode_pool_map(&tm_k, *desc, k_cache, box, 64, swz) != CUDA_SUCCESS ||
+        encode_pool_map(&tm_v, *desc, v_cache, box, 64, swz) != CUDA_SUCCESS)
         return PKV_ECUDA;
     return launch_decode(a, tm_k, tm_v, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PKV_OK : PKV_ECUDA;
 }

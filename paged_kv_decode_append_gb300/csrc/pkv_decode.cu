@@ -10,24 +10,28 @@
 // structure (work split along the key axis, partial results merged by their
 // log-sum-exp) is the one the page's profile names (flash_fwd_splitkv_kernel).
 //
-// GB300 design:
-//  * One CTA = 1 producer warp + 4 consumer warps.  The producer streams
-//    32-token tiles of K and V for one kv head through a 3-6 stage
-//    shared-memory ring with TMA (cp.async.bulk.tensor, one box per page
-//    piece, L2 evict-first), completion tracked by mbarriers.
-//  * Consumers hold the pre-scaled queries of up to 4 heads (q * scale *
-//    log2 e, the pages' PRESCALE_QK lesson) in fp32 registers; 8 lanes
-//    share one key row (16 B vector reads from shared memory), QK and PV run
-//    as packed fp32x2 FMAs, online softmax in base 2 with a warp-uniform
-//    running max, reductions by warp shuffles.
-//  * Work items are (row, kv head, head group, key chunk).  Every CTA
-//    rebuilds the same plan from cache_seqlens (no host readback): the
-//    chunk size is the smallest multiple of the tile that yields about
-//    `target_items` items, so one long row is split over many SMs.
-//  * A chunk's CTA writes an fp32 partial (o, m, l); the last CTA of a unit
-//    to finish (atomic ticket, never a spin) merges them, folds in the new
-//    token (scores it from registers rather than re-reading the cache),
-//    performs the append and writes bf16 output and lse.
+// GB300 design (one persistent CTA per resident slot, four warps):
+//  * producer warp: streams 32-token tiles of K and V of one kv head through
+//    a shared-memory ring with TMA (one box per page piece and 64-column
+//    half row, 128-byte swizzle, L2 evict-first); page ids are prefetched 32
+//    at a time into registers, one window (and one slice) ahead.
+//  * two consumer warps: 16 token rows of every tile each, on tensor-core
+//    tiles (mma.sync m16n8k16, bf16 in, fp32 accumulate) with an online
+//    softmax in base 2; see consume_tile.  At the end of a slice they hand
+//    their softmax state to the epilogue warp through a double-buffered
+//    shared-memory slot and go straight on to the next slice.
+//  * epilogue warp: merges the two warps' states and finishes the slice off
+//    the streaming path: a unit cut into n slices writes n fp32 partials;
+//    the last slice to arrive (atomic ticket, never a spin) merges them by
+//    log-sum-exp, folds in the new token (scored from k_new, not re-read from
+//    the cache), performs the append and writes bf16 output and lse.
+//  * Stream-K split: the (row, kv head, head group) units are laid end to end
+//    as one list of key tokens and every CTA takes an equal contiguous slice
+//    (boundaries rounded down to 32 tokens inside a unit), so one long
+//    request is spread over many SMs and all CTAs finish together.  The plan
+//    is rebuilt by every CTA from cache_seqlens; nothing is read back by the
+//    host.  A unit slice is always the first or the last slice of its CTA,
+//    so two workspace slots per CTA hold every partial.
 //  * Every block_table entry is range-checked before an address is formed.
 #include <math.h>
 
@@ -37,15 +41,17 @@
 namespace pkv {
 namespace {
 
-constexpr int kWarps = 4;                      // consumer warps
-constexpr int kThreads = (kWarps + 1) * 32;    // + one producer warp
-constexpr int kConsumerThreads = kWarps * 32;
-constexpr int kTile = kDecodeTile;             // tokens per pipeline tile
-constexpr int kTokPerWarp = kTile / kWarps;    // 8 tokens per warp per tile
-constexpr int kSteps = kTokPerWarp / 4;        // 4 tokens (one per 8-lane group) per step
-constexpr int kTargetItemsMax = 2048;
-constexpr int kBarConsumers = 1;               // named barrier id for consumer warps
+constexpr int kWarps = 2;                    // consumer warps, 16 token rows each
+constexpr int kProducerWarp = kWarps;        // warp 2
+constexpr int kEpilogueWarp = kWarps + 1;    // warp 3
+constexpr int kThreads = (kWarps + 2) * 32;
+constexpr int kTile = kDecodeTile; // tokens per pipeline tile
+constexpr int kMaxGrid = 2048;     // persistent CTAs at most (workspace sizing)
+constexpr int kMinSlice = 64;      // tokens per CTA slice at least
+constexpr int kSlots = 2;          // consumer -> epilogue hand-off buffers
 constexpr float kNegInf = -INFINITY;
+
+static_assert(kTile == 16 * kWarps, "each consumer warp owns 16 rows of a tile");
 
 enum RowStatus { ROW_OK = 0, ROW_INACTIVE = 1, ROW_OVERFLOW = 2 };
 
@@ -65,7 +71,7 @@ struct KParams {
     int32_t *err_flag;
     int batch, num_q_heads, num_kv_heads, group, n_sub, units, max_blocks;
     int page_size, page_shift, num_pages, layout, box_tokens;
-    int target_items, chunk_max, with_new;
+    int with_new, swizzle;
     float q_scale;
 };
 
@@ -78,21 +84,22 @@ constexpr int stages_for()
 template <int D, int GC>
 struct Smem {
     static constexpr int kStages = stages_for<D>();
-    __nv_bfloat16 kv[kStages][2][kTile * D]; // [stage][K|V][token][dim]
-    float red_o[kWarps][GC][D];
-    float fin_o[GC][D];
-    float red_m[kWarps][GC], red_l[kWarps][GC];
-    float fin_m[GC], fin_l[GC], s_new[GC];
+    // [stage][K|V] tiles laid out [D/64][kTile][64] (128-byte rows, TMA
+    // SWIZZLE_128B when the page size allows 8-row boxes)
+    __nv_bfloat16 kv[kStages][2][kTile * D];
+    // per-warp softmax states of a finished slice: o (unnormalised), m, l
+    float red_o[kSlots][kWarps][GC][D];
+    float red_m[kSlots][kWarps][GC], red_l[kSlots][kWarps][GC];
+    int32_t red_bad[kSlots][kWarps];
     uint64_t full[kStages], empty[kStages];
+    uint64_t epi_full[kSlots], epi_empty[kSlots];
     int32_t stage_bad[kStages];
     int32_t len[kMaxDecodeBatch];
-    int32_t prefix[kMaxDecodeBatch + 1];
-    int32_t pages[kDecodeChunkMaxPages];
-    int32_t chunk;
-    int32_t flag;
-    int32_t bad;
+    int32_t rowtok[kMaxDecodeBatch + 1]; // prefix of cache tokens per row
+    long long work;                      // units * rowtok[batch]
+    long long slice;                     // work positions per CTA
+    int32_t geff;                        // CTAs that own a token slice
     int32_t abort;
-    int32_t stop;
 };
 
 __device__ __forceinline__ float ex2(float x)
@@ -109,11 +116,6 @@ __device__ __forceinline__ int row_status(const KParams &p, int L)
     if ((int64_t)L + p.with_new > (int64_t)p.max_blocks * p.page_size)
         return ROW_OVERFLOW;
     return ROW_OK;
-}
-
-__device__ __forceinline__ int row_chunks(const KParams &p, int L, int C)
-{
-    return (row_status(p, L) == ROW_OK && L > 0) ? (L + C - 1) / C : 1;
 }
 
 // Mbarrier wait that also gives up when another warp of the CTA aborted.
@@ -135,8 +137,10 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, vo
     }
 }
 
-// Every CTA derives the same split plan from cache_seqlens: chunk size C and
-// the first work item of every row (prefix[b]; prefix[batch] = item count).
+// ------------------------------------------------------------------ plan
+// Every CTA derives the same plan from cache_seqlens: the cache tokens of
+// every row (0 for inactive / overflowing rows), their prefix sum, the total
+// work (units per row * total tokens) and the slice length per CTA.
 template <int D, int GC>
 __device__ void build_plan(const KParams &p, Smem<D, GC> &sm)
 {
@@ -145,147 +149,219 @@ __device__ void build_plan(const KParams &p, Smem<D, GC> &sm)
     __syncthreads();
     if (threadIdx.x < 32) {
         const int lane = threadIdx.x;
-        long long work = 0;
-        for (int i = lane; i < p.batch; i += 32) {
-            const int L = sm.len[i];
-            if (row_status(p, L) == ROW_OK)
-                work += L;
-        }
-        for (int o = 16; o > 0; o >>= 1)
-            work += __shfl_xor_sync(0xffffffffu, work, o);
-        work *= p.units;
-        long long c = (work + p.target_items - 1) / p.target_items;
-        c = (c + kTile - 1) / kTile * kTile;
-        if (c < kDecodeChunkMin)
-            c = kDecodeChunkMin;
-        if (c > p.chunk_max)
-            c = p.chunk_max;
-        const int C = (int)c;
         int run = 0;
         for (int base = 0; base < p.batch; base += 32) {
             const int i = base + lane;
-            const int items = i < p.batch ? row_chunks(p, sm.len[i], C) * p.units : 0;
-            int incl = items;
+            int n = 0;
+            if (i < p.batch) {
+                const int L = sm.len[i];
+                n = row_status(p, L) == ROW_OK ? L : 0;
+            }
+            int incl = n;
             for (int o = 1; o < 32; o <<= 1) {
                 const int v = __shfl_up_sync(0xffffffffu, incl, o);
                 if (lane >= o)
                     incl += v;
             }
             if (i < p.batch)
-                sm.prefix[i] = run + incl - items;
+                sm.rowtok[i] = run + incl - n;
             run += __shfl_sync(0xffffffffu, incl, 31);
         }
         if (lane == 0) {
-            sm.prefix[p.batch] = run;
-            sm.chunk = C;
+            sm.rowtok[p.batch] = run;
+            const long long work = (long long)run * p.units;
+            long long g = work / kMinSlice;
+            if (g > gridDim.x)
+                g = gridDim.x;
+            if (g < 1)
+                g = 1;
+            const long long slice = work > 0 ? (work + g - 1) / g : 1;
+            sm.work = work;
+            sm.slice = slice;
+            sm.geff = work > 0 ? (int)((work + slice - 1) / slice) : 1;
         }
     }
     __syncthreads();
 }
 
-struct Item {
-    int b, unit, kvh, sub, chunk, nchunks, base, L, status, tok0, tok1;
-};
-
+// Unit containing global work position x (x < work): row b, unit r in the
+// row, offset rel inside the unit; returns the unit's first position.
+// units * row tokens < 2^31 (checked on the host), so in-row math is 32-bit.
 template <int D, int GC>
-__device__ __forceinline__ Item decode_item(const KParams &p, const Smem<D, GC> &sm, int it)
+__device__ __forceinline__ long long locate(const KParams &p, const Smem<D, GC> &sm, long long x, int &b, int &r,
+                                            int &rel)
 {
-    int lo = 0, hi = p.batch - 1;
+    int lo = 0, hi = p.batch - 1; // largest row starting at or before x (never an empty row)
     while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
-        if (sm.prefix[mid] <= it)
+        if ((long long)sm.rowtok[mid] * p.units <= x)
             lo = mid;
         else
             hi = mid - 1;
     }
-    Item I;
-    I.b = lo;
-    I.L = sm.len[lo];
-    I.status = row_status(p, I.L);
-    const int C = sm.chunk;
-    I.nchunks = row_chunks(p, I.L, C);
-    const int r = it - sm.prefix[lo];
-    const int unit_in_row = r / I.nchunks;
-    I.chunk = r - unit_in_row * I.nchunks;
-    I.base = it - I.chunk;
-    I.kvh = unit_in_row / p.n_sub;
-    I.sub = unit_in_row - I.kvh * p.n_sub;
-    I.unit = lo * p.units + unit_in_row;
-    const int ncache = I.status == ROW_OK ? I.L : 0;
-    I.tok0 = min(I.chunk * C, ncache);
-    I.tok1 = min(I.tok0 + C, ncache);
-    return I;
+    b = lo;
+    const long long base = (long long)sm.rowtok[lo] * p.units;
+    const int n = sm.rowtok[lo + 1] - sm.rowtok[lo];
+    const int d = (int)(x - base);
+    r = d / n;
+    rel = d - r * n;
+    return base + (long long)r * n;
 }
 
+// First work position of CTA k's slice (k in [0, geff]): k * slice, rounded
+// down to a multiple of the tile inside its unit.
+template <int D, int GC>
+__device__ __forceinline__ long long boundary(const KParams &p, const Smem<D, GC> &sm, int k)
+{
+    const long long x = (long long)k * sm.slice;
+    if (x >= sm.work)
+        return sm.work;
+    int b, r, rel;
+    const long long u0 = locate(p, sm, x, b, r, rel);
+    return u0 + (rel & ~(kTile - 1));
+}
+
+// CTA whose slice holds work position x (x < work).  boundary(k) lies in
+// (k * slice - kTile, k * slice], so it is floor(x / slice) or the next one.
+template <int D, int GC>
+__device__ __forceinline__ int owner_of(const KParams &p, const Smem<D, GC> &sm, long long x)
+{
+    int k = (int)(x / sm.slice);
+    if (k > sm.geff - 1)
+        k = sm.geff - 1;
+    while (k + 1 < sm.geff && boundary(p, sm, k + 1) <= x)
+        ++k;
+    while (k > 0 && boundary(p, sm, k) > x)
+        --k;
+    return k;
+}
+
+struct Seg {
+    int b, r, kvh, sub, unit, L, status, tok0, tok1;
+    long long u0; // unit's first work position
+    int n;        // unit's cache tokens
+};
+
+// Walks the slices of one CTA's range, one unit at a time.
+struct SegIter {
+    long long pos, end;
+    template <int D, int GC>
+    __device__ __forceinline__ void init(const KParams &p, const Smem<D, GC> &sm, int k)
+    {
+        if (k < sm.geff) {
+            pos = boundary(p, sm, k);
+            end = boundary(p, sm, k + 1);
+        } else {
+            pos = end = 0;
+        }
+    }
+    template <int D, int GC>
+    __device__ __forceinline__ bool next(const KParams &p, const Smem<D, GC> &sm, Seg &s)
+    {
+        if (pos >= end)
+            return false;
+        int rel;
+        s.u0 = locate(p, sm, pos, s.b, s.r, rel);
+        s.n = sm.rowtok[s.b + 1] - sm.rowtok[s.b];
+        const long long seg_end = min(end, s.u0 + s.n);
+        s.tok0 = rel;
+        s.tok1 = rel + (int)(seg_end - pos);
+        s.kvh = s.r / p.n_sub;
+        s.sub = s.r - s.kvh * p.n_sub;
+        s.unit = s.b * p.units + s.r;
+        s.L = sm.len[s.b];
+        s.status = row_status(p, s.L);
+        pos = seg_end;
+        return true;
+    }
+};
+
 // ---------------------------------------------------------------- producer
+// Page ids of 32 consecutive blocks of a row, one per lane (0 past `last`).
+__device__ __forceinline__ int load_window(const int32_t *bt_row, int first, int last, int lane)
+{
+    return first + lane <= last ? bt_row[first + lane] : 0;
+}
+
 template <int D, int GC>
 __device__ void producer(const KParams &p, Smem<D, GC> &sm, const CUtensorMap *tm_k, const CUtensorMap *tm_v)
 {
     constexpr int S = Smem<D, GC>::kStages;
     const int lane = threadIdx.x & 31;
-    const int n_items = sm.prefix[p.batch];
     const uint64_t policy = l2_evict_first_policy();
     const int box = p.box_tokens;
     const uint32_t box_bytes = (uint32_t)box * D * 2u;
     uint32_t g_tile = 0;
     volatile int32_t *abort = &sm.abort;
-
-    for (int it = blockIdx.x; it < n_items && !*abort; it += gridDim.x) {
-        const Item I = decode_item(p, sm, it);
-        if (I.tok1 <= I.tok0)
-            continue;
-        const int first_blk = I.tok0 >> p.page_shift;
-        const int nblk = ((I.tok1 - 1) >> p.page_shift) - first_blk + 1;
-        __syncwarp();
-        const int32_t *bt_row = p.block_table + (int64_t)I.b * p.max_blocks;
-        for (int i = lane; i < nblk; i += 32)
-            sm.pages[i] = bt_row[first_blk + i];
-        __syncwarp();
-        const int n_tiles = (I.tok1 - I.tok0 + kTile - 1) / kTile;
+    SegIter si;
+    si.init(p, sm, blockIdx.x);
+    Seg sg, nx;
+    bool have = si.next(p, sm, sg);
+    // first window of the current slice, prefetched one slice ahead
+    int win = have ? load_window(p.block_table + (int64_t)sg.b * p.max_blocks, sg.tok0 >> p.page_shift,
+                                 (sg.tok1 - 1) >> p.page_shift, lane)
+                   : 0;
+    while (have && !*abort) {
+        const int32_t *bt_row = p.block_table + (int64_t)sg.b * p.max_blocks;
+        const int last_pg = (sg.tok1 - 1) >> p.page_shift;
+        int wbase = sg.tok0 >> p.page_shift;
+        int nxt = load_window(bt_row, wbase + 32, last_pg, lane);
+        const bool more = si.next(p, sm, nx);
+        const int nwin = more ? load_window(p.block_table + (int64_t)nx.b * p.max_blocks, nx.tok0 >> p.page_shift,
+                                            (nx.tok1 - 1) >> p.page_shift, lane)
+                              : 0;
+        const int n_tiles = (sg.tok1 - sg.tok0 + kTile - 1) / kTile;
         for (int t = 0; t < n_tiles; ++t, ++g_tile) {
             const int s = g_tile % S;
             const uint32_t use = g_tile / S;
             if (use > 0 && !wait_or_abort(&sm.empty[s], (use - 1) & 1u, abort))
                 break;
+            const int tile0 = sg.tok0 + t * kTile;
+            const int nv = min(kTile, sg.tok1 - tile0);
+            const int nbox = (nv + box - 1) / box;
+            if ((tile0 >> p.page_shift) >= wbase + 32) { // tiles never straddle a window
+                wbase += 32;
+                win = nxt;
+                nxt = load_window(bt_row, wbase + 32, last_pg, lane);
+            }
+            // page of box `lane` (lanes >= nbox carry junk and are not used)
+            const int mine = __shfl_sync(0xffffffffu, win, (((tile0 + lane * box) >> p.page_shift) - wbase) & 31);
+            const bool ok = lane < nbox && mine >= 1 && mine < p.num_pages;
+            const unsigned okmask = __ballot_sync(0xffffffffu, ok);
+            const int bad = __popc(okmask) != nbox;
             if (lane == 0) {
-                const int tile0 = I.tok0 + t * kTile;
-                const int nv = min(kTile, I.tok1 - tile0);
-                const int nbox = (nv + box - 1) / box;
-                int bad = 0;
-                uint32_t bytes = 0;
-                for (int bx = 0; bx < nbox; ++bx) {
-                    const int page = sm.pages[((tile0 + bx * box) >> p.page_shift) - first_blk];
-                    if (page < 1 || page >= p.num_pages)
-                        bad = 1;
-                    else
-                        bytes += 2u * box_bytes;
-                }
                 sm.stage_bad[s] = bad;
-                mbar_arrive_expect_tx(&sm.full[s], bytes);
-                for (int bx = 0; bx < nbox; ++bx) {
-                    const int tok = tile0 + bx * box;
-                    const int page = sm.pages[(tok >> p.page_shift) - first_blk];
-                    if (page < 1 || page >= p.num_pages)
-                        continue;
-                    const int slot = tok & (p.page_size - 1);
+                mbar_arrive_expect_tx(&sm.full[s], 2u * box_bytes * (uint32_t)__popc(okmask));
+            }
+            __syncwarp();
+            for (int bx = 0; bx < nbox; ++bx) {
+                const int page = __shfl_sync(0xffffffffu, mine, bx);
+                if (lane == 0 && ((okmask >> bx) & 1u)) {
+                    const int slot = (tile0 + bx * box) & (p.page_size - 1);
                     int y, z;
                     if (p.layout == PKV_NHD) {
-                        y = I.kvh;
+                        y = sg.kvh;
                         z = page * p.page_size + slot;
                     } else {
                         y = slot;
-                        z = page * p.num_kv_heads + I.kvh;
+                        z = page * p.num_kv_heads + sg.kvh;
                     }
-                    __nv_bfloat16 *dst_k = sm.kv[s][0] + bx * box * D;
-                    __nv_bfloat16 *dst_v = sm.kv[s][1] + bx * box * D;
-                    tma_load_3d(dst_k, tm_k, 0, y, z, &sm.full[s], policy);
-                    tma_load_3d(dst_v, tm_v, 0, y, z, &sm.full[s], policy);
+                    // one 64-column box per 128-byte half row: [D/64][kTile][64]
+#pragma unroll
+                    for (int h = 0; h < D / 64; ++h) {
+                        const int off = (h * kTile + bx * box) * 64;
+                        tma_load_3d(sm.kv[s][0] + off, tm_k, 64 * h, y, z, &sm.full[s], policy);
+                        tma_load_3d(sm.kv[s][1] + off, tm_v, 64 * h, y, z, &sm.full[s], policy);
+                    }
                 }
-                if (bad)
-                    set_error(p.err_flag, PKV_ERR_PAGE);
             }
+            if (lane == 0 && bad)
+                set_error(p.err_flag, PKV_ERR_PAGE);
             __syncwarp();
         }
+        have = more;
+        sg = nx;
+        win = nwin;
     }
     // After an abort, let copies already issued land before the CTA exits.
     if (*abort && lane == 0) {
@@ -296,398 +372,565 @@ __device__ void producer(const KParams &p, Smem<D, GC> &sm, const CUtensorMap *t
 }
 
 // ---------------------------------------------------------------- consumers
-template <int D, int GC, bool MASKED>
-__device__ __forceinline__ void consume_tile(const __nv_bfloat16 *Ks, const __nv_bfloat16 *Vs, int nv, int warp,
-                                             int lane, const float2 (&qf)[GC][D / 64][4],
-                                             float2 (&acc)[GC][D / 64][4], float (&m_run)[GC],
-                                             float (&l_run)[GC])
+// Each consumer warp owns 16 of a tile's 32 token rows.  Tensor-core tiles
+// (mma.sync m16n8k16, bf16 in, fp32 accumulate) put the tokens on the M side
+// so only the 8-wide head side is padded (GC <= 8 heads share one kv head):
+//   S^T[16 tok][8 heads] = K[16 tok][D] . Q^T[D][8 heads]
+//   O^T[D][8 heads]     += V^T[D][16 tok] . P^T[16 tok][8 heads]
+// P^T moves from the accumulator layout to the B-operand layout with
+// movmatrix (an in-register 8x8 transpose).  P is split into bf16 high and
+// low parts (two MMAs) so the weights carry ~16 significant bits.
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4])
 {
-    constexpr int VPL = D / 64;
-    const int grp = lane >> 3, j = lane & 7;
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t (&r)[4])
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+
+__device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1)
+{
+    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+                 "{%0,%1,%2,%3};"
+                 : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+                 : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t a)
+{
+    uint32_t d;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
+    return d;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi)
+{
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+
+__device__ __forceinline__ float2 unpack_bf16(uint32_t w)
+{
+    return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+}
+
+// Shared-memory byte address of the 16-byte chunk `chunk` (0..D/8-1) of token
+// row `row` in a [D/64][kTile][64] tile; with swz = 7 the 128-byte rows are
+// stored TMA SWIZZLE_128B style (chunk index XOR row % 8).
+__device__ __forceinline__ uint32_t tile_addr(uint32_t base, int row, int chunk, int swz)
+{
+    const int half = chunk >> 3, c = chunk & 7;
+    return base + (uint32_t)((half * kTile + row) * 128 + ((c ^ (row & swz)) << 4));
+}
+
+template <int D, bool MASKED>
+__device__ __forceinline__ void consume_tile(const __nv_bfloat16 *Kt, __nv_bfloat16 *Vt, int nv, int warp, int lane,
+                                             int swz, float scale, const uint32_t (&qf)[D / 16][2],
+                                             float (&acc)[D / 16][4], float (&m_run)[2], float (&l_run)[2])
+{
+    constexpr int KS = D / 16;
+    const int row0 = warp * 16;
+    const int g = lane >> 2;
+    const uint32_t kbase = smem_addr(Kt), vbase = smem_addr(Vt);
+    if (MASKED && nv < row0 + 16) {
+        // zero V rows of masked tokens: P is 0 there, but 0 * NaN would not be
+        const int first = nv > row0 ? nv : row0;
+        for (int i = lane; i < (row0 + 16 - first) * (D / 8); i += 32) {
+            const int r = first + i / (D / 8), chunk = i % (D / 8);
+            *reinterpret_cast<uint4 *>(Vt + ((chunk >> 3) * kTile + r) * 64 + (chunk & 7) * 8) =
+                make_uint4(0u, 0u, 0u, 0u);
+        }
+        __syncwarp();
+    }
+    // ---- S^T = K Q^T, two accumulators for two independent MMA chains
+    float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+    const int krow = row0 + (lane & 15);
 #pragma unroll
-    for (int step = 0; step < kSteps; ++step) {
-        const int row = warp * kTokPerWarp + step * 4 + grp;
-        const bool valid = !MASKED || row < nv;
-        const uint4 *krow = reinterpret_cast<const uint4 *>(Ks + row * D);
-        float s[GC];
-        {
-            float2 sacc[GC];
+    for (int ks = 0; ks < KS; ++ks) {
+        uint32_t a[4];
+        ldsm_x4(tile_addr(kbase, krow, 2 * ks + (lane >> 4), swz), a);
+        if (ks & 1)
+            mma_16816(sb, a, qf[ks][0], qf[ks][1]);
+        else
+            mma_16816(sa, a, qf[ks][0], qf[ks][1]);
+    }
+    float v[4]; // rows g (v[0], v[1]) and g+8 (v[2], v[3]); heads 2c, 2c+1
 #pragma unroll
-            for (int g = 0; g < GC; ++g)
-                sacc[g] = make_float2(0.f, 0.f);
+    for (int i = 0; i < 4; ++i)
+        v[i] = (sa[i] + sb[i]) * scale;
+    if (MASKED) {
+        if (row0 + g >= nv)
+            v[0] = v[1] = kNegInf;
+        if (row0 + g + 8 >= nv)
+            v[2] = v[3] = kNegInf;
+    }
+    // ---- online softmax per head column (reduce over the 8 row groups)
+    float m_new[2];
+    bool grow = false;
 #pragma unroll
-            for (int i = 0; i < VPL; ++i) {
-                const uint4 kw = krow[j + 8 * i];
-                const uint32_t w4[4] = {kw.x, kw.y, kw.z, kw.w};
+    for (int j = 0; j < 2; ++j) {
+        float mt = fmaxf(v[j], v[2 + j]);
+        mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 4));
+        mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 8));
+        mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 16));
+        m_new[j] = fmaxf(m_run[j], mt);
+        grow |= m_new[j] > m_run[j];
+    }
+    if (__any_sync(0xffffffffu, grow)) {
 #pragma unroll
-                for (int w = 0; w < 4; ++w) {
-                    const float2 kf = bf16x2_to_float2(w4[w]);
+        for (int j = 0; j < 2; ++j) {
+            const float a = m_new[j] == kNegInf ? 1.f : ex2(m_run[j] - m_new[j]);
+            l_run[j] *= a;
 #pragma unroll
-                    for (int g = 0; g < GC; ++g)
-                        sacc[g] = ffma2(qf[g][i][w], kf, sacc[g]);
-                }
+            for (int mt = 0; mt < KS; ++mt) {
+                acc[mt][j] *= a;
+                acc[mt][2 + j] *= a;
             }
-#pragma unroll
-            for (int g = 0; g < GC; ++g)
-                s[g] = sacc[g].x + sacc[g].y;
+            m_run[j] = m_new[j];
         }
+    }
+    float pr[4];
 #pragma unroll
-        for (int g = 0; g < GC; ++g) {
-            s[g] += __shfl_xor_sync(0xffffffffu, s[g], 1);
-            s[g] += __shfl_xor_sync(0xffffffffu, s[g], 2);
-            s[g] += __shfl_xor_sync(0xffffffffu, s[g], 4);
-            if (MASKED && !valid)
-                s[g] = kNegInf;
-        }
-        bool grow = false;
-        float m_new[GC];
+    for (int i = 0; i < 4; ++i) {
+        const float m = m_run[i & 1];
+        pr[i] = ex2(v[i] - (m == kNegInf ? 0.f : m)); // masked: ex2(-inf) = 0
+    }
+    l_run[0] += pr[0] + pr[2];
+    l_run[1] += pr[1] + pr[3];
+    // ---- P^T as B fragments: high and low bf16 parts, transposed in registers
+    const uint32_t h01 = pack_bf16(pr[0], pr[1]), h23 = pack_bf16(pr[2], pr[3]);
+    const float2 f01 = unpack_bf16(h01), f23 = unpack_bf16(h23);
+    const uint32_t l01 = pack_bf16(pr[0] - f01.x, pr[1] - f01.y), l23 = pack_bf16(pr[2] - f23.x, pr[3] - f23.y);
+    const uint32_t bh0 = movmatrix_trans(h01), bh1 = movmatrix_trans(h23);
+    const uint32_t bl0 = movmatrix_trans(l01), bl1 = movmatrix_trans(l23);
+    // ---- O^T += V^T P^T
+    const int vrow = row0 + (lane & 7) + ((lane >> 4) << 3);
+    const int vchunk = (lane >> 3) & 1;
 #pragma unroll
-        for (int g = 0; g < GC; ++g) {
-            float mt = fmaxf(s[g], __shfl_xor_sync(0xffffffffu, s[g], 8));
-            mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 16));
-            m_new[g] = fmaxf(m_run[g], mt);
-            grow |= m_new[g] > m_run[g];
-        }
-        if (grow) { // warp-uniform: m_run and m_new are identical in all lanes
-#pragma unroll
-            for (int g = 0; g < GC; ++g) {
-                const float a = ex2(m_run[g] - m_new[g]); // m_run = -inf -> 0
-                l_run[g] *= a;
-                const float2 a2 = make_float2(a, a);
-#pragma unroll
-                for (int i = 0; i < VPL; ++i)
-#pragma unroll
-                    for (int w = 0; w < 4; ++w)
-                        acc[g][i][w] = fmul2(acc[g][i][w], a2);
-                m_run[g] = m_new[g];
-            }
-        }
-        float pr[GC];
-#pragma unroll
-        for (int g = 0; g < GC; ++g) {
-            pr[g] = valid ? ex2(s[g] - m_run[g]) : 0.f;
-            l_run[g] += pr[g];
-        }
-        if (valid) {
-            const uint4 *vrow = reinterpret_cast<const uint4 *>(Vs + row * D);
-#pragma unroll
-            for (int i = 0; i < VPL; ++i) {
-                const uint4 vw = vrow[j + 8 * i];
-                const uint32_t w4[4] = {vw.x, vw.y, vw.z, vw.w};
-#pragma unroll
-                for (int w = 0; w < 4; ++w) {
-                    const float2 vf = bf16x2_to_float2(w4[w]);
-#pragma unroll
-                    for (int g = 0; g < GC; ++g)
-                        acc[g][i][w] = ffma2(make_float2(pr[g], pr[g]), vf, acc[g][i][w]);
-                }
-            }
-        }
+    for (int mt = 0; mt < KS; ++mt) {
+        uint32_t a[4];
+        ldsm_x4_trans(tile_addr(vbase, vrow, 2 * mt + vchunk, swz), a);
+        mma_16816(acc[mt], a, bh0, bh1);
+        mma_16816(acc[mt], a, bl0, bl1);
     }
 }
 
-// Merges the split-KV partials of one unit (written by its nchunks CTAs)
-// into fin_*; returns nonzero if any chunk met a bad page.
+// Workspace slot of slice j of a unit whose first slice belongs to CTA kf:
+// slice 0 is CTA kf's last slice (slot 2kf+1), slice j >= 1 is CTA kf+j's
+// first slice (slot 2(kf+j)).
+__device__ __forceinline__ int slot_of(int kf, int j)
+{
+    return j == 0 ? 2 * kf + 1 : 2 * (kf + j);
+}
+
+// B fragments of Q^T for one slice: head g of the slice's head group (zero
+// beyond GC), dims 16ks + 2c (+8).
 template <int D, int GC>
-__device__ int combine_partials(const KParams &p, Smem<D, GC> &sm, const Item &I)
+__device__ __forceinline__ void load_q(const KParams &p, const Seg &sg, int lane, uint32_t (&qf)[D / 16][2])
 {
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const float2 *ml = p.part_ml + (int64_t)I.base * GC;
-    if (tid == 0)
-        sm.bad = 0;
-    named_sync(kBarConsumers, kConsumerThreads);
-    for (int g = warp; g < GC; g += kWarps) {
-        float M = kNegInf;
-        int bad = 0;
-        for (int i = lane; i < I.nchunks; i += 32) {
-            const float2 v = __ldcg(ml + (int64_t)i * GC + g);
-            M = fmaxf(M, v.x);
-            bad |= v.y < 0.f;
-        }
-        for (int o = 16; o > 0; o >>= 1)
-            M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-        bad = __any_sync(0xffffffffu, bad);
-        float l = 0.f;
-        for (int i = lane; i < I.nchunks; i += 32) {
-            const float2 v = __ldcg(ml + (int64_t)i * GC + g);
-            l += v.x == kNegInf ? 0.f : ex2(v.x - M) * v.y;
-        }
-        for (int o = 16; o > 0; o >>= 1)
-            l += __shfl_xor_sync(0xffffffffu, l, o);
-        if (lane == 0) {
-            sm.fin_m[g] = M;
-            sm.fin_l[g] = l;
-            if (bad)
-                sm.bad = 1;
-        }
-    }
-    named_sync(kBarConsumers, kConsumerThreads);
-    const float *po = p.part_o + (int64_t)I.base * GC * D;
-    for (int e = tid; e < GC * D; e += kConsumerThreads) {
-        const int g = e / D;
-        const float M = sm.fin_m[g];
-        float o = 0.f;
-        for (int i = 0; i < I.nchunks; ++i) {
-            const float m = __ldcg(&ml[(int64_t)i * GC + g].x);
-            if (m != kNegInf)
-                o += ex2(m - M) * __ldcg(po + (int64_t)i * GC * D + e);
-        }
-        (&sm.fin_o[0][0])[e] = o;
-    }
-    named_sync(kBarConsumers, kConsumerThreads);
-    return sm.bad;
-}
-
-// Writes the unit's output: zeros for inactive / failed rows, otherwise
-// merges the new token (when given), performs the append and normalises.
-template <int D, int GC>
-__device__ void finalize(const KParams &p, Smem<D, GC> &sm, const Item &I, int bad)
-{
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int h0 = I.kvh * p.group + I.sub * GC;
-    int err = 0;
-    if (I.status == ROW_OVERFLOW)
-        err = PKV_ERR_OVERFLOW;
-    else if (I.status == ROW_OK && bad)
-        err = PKV_ERR_PAGE;
-    int64_t dst = -1; // element offset of the appended token for this kv head
-    if (I.status == ROW_OK && !err && p.with_new) {
-        const int page = p.block_table[(int64_t)I.b * p.max_blocks + (I.L >> p.page_shift)];
-        if (page < 1 || page >= p.num_pages) {
-            err = PKV_ERR_PAGE;
-        } else {
-            const int slot = I.L & (p.page_size - 1);
-            dst = p.layout == PKV_NHD
-                      ? (((int64_t)page * p.page_size + slot) * p.num_kv_heads + I.kvh) * D
-                      : (((int64_t)page * p.num_kv_heads + I.kvh) * p.page_size + slot) * D;
-        }
-    }
-    const bool live = I.status == ROW_OK && !err;
-    if (tid == 0 && err)
-        set_error(p.err_flag, err);
-
-    const __nv_bfloat16 *kn = p.k_new + ((int64_t)I.b * p.num_kv_heads + I.kvh) * D;
-    const __nv_bfloat16 *vn = p.v_new + ((int64_t)I.b * p.num_kv_heads + I.kvh) * D;
-    if (live && p.with_new) {
-        // score of the new token for each head: (q * scale * log2 e) . k_new
-        for (int g = warp; g < GC; g += kWarps) {
-            const __nv_bfloat16 *qh = p.q + ((int64_t)I.b * p.num_q_heads + h0 + g) * D;
-            float s = 0.f;
-            for (int d = lane; d < D; d += 32)
-                s = fmaf(__bfloat162float(qh[d]) * p.q_scale, __bfloat162float(kn[d]), s);
-            for (int o = 16; o > 0; o >>= 1)
-                s += __shfl_xor_sync(0xffffffffu, s, o);
-            if (lane == 0)
-                sm.s_new[g] = s;
-        }
-        named_sync(kBarConsumers, kConsumerThreads);
-        if (I.sub == 0) { // the append: one bit copy per kv head
-            constexpr int kVec = D / 8;
-            for (int c = tid; c < 2 * kVec; c += kConsumerThreads) {
-                const bool is_v = c >= kVec;
-                const int v = is_v ? c - kVec : c;
-                const uint4 val = reinterpret_cast<const uint4 *>(is_v ? vn : kn)[v];
-                reinterpret_cast<uint4 *>((is_v ? p.v_cache : p.k_cache) + dst)[v] = val;
-            }
-        }
-    }
-    for (int e = tid; e < GC * D; e += kConsumerThreads) {
-        const int g = e / D, d = e - g * D;
-        const int64_t oidx = ((int64_t)I.b * p.num_q_heads + h0 + g) * D + d;
-        float o = 0.f, M = kNegInf, l = 0.f;
-        if (live) {
-            o = sm.fin_o[g][d];
-            M = sm.fin_m[g];
-            l = sm.fin_l[g];
-            if (p.with_new) {
-                const float sn = sm.s_new[g];
-                const float Mn = fmaxf(M, sn);
-                const float a = ex2(M - Mn); // M = -inf (no cached key) -> 0
-                const float c = ex2(sn - Mn);
-                o = fmaf(o, a, c * __bfloat162float(vn[d]));
-                l = fmaf(l, a, c);
-                M = Mn;
-            }
-        }
-        const bool any = l > 0.f;
-        p.out[oidx] = __float2bfloat16_rn(any ? o / l : 0.f);
-        if (p.lse != nullptr && d == 0)
-            p.lse[(int64_t)I.b * p.num_q_heads + h0 + g] = any ? (M + log2f(l)) * 0.69314718055994531f : kNegInf;
+    const int g = lane >> 2, c = lane & 3;
+    const int h0 = sg.kvh * p.group + sg.sub * GC;
+    const uint32_t *qrow = reinterpret_cast<const uint32_t *>(p.q + ((int64_t)sg.b * p.num_q_heads + h0 + g) * D);
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks) {
+        qf[ks][0] = g < GC ? __ldg(qrow + 8 * ks + c) : 0u;
+        qf[ks][1] = g < GC ? __ldg(qrow + 8 * ks + 4 + c) : 0u;
     }
 }
 
+// Consumer warp: runs the tile loop of every slice of this CTA and hands each
+// slice's softmax state (o, m, l per head) to the epilogue warp.
 template <int D, int GC>
 __device__ void consumers(const KParams &p, Smem<D, GC> &sm)
 {
     constexpr int S = Smem<D, GC>::kStages;
-    constexpr int VPL = D / 64;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int j = lane & 7;
-    const int n_items = sm.prefix[p.batch];
+    constexpr int KS = D / 16;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane >> 2, c = lane & 3;
+    const int swz = p.swizzle ? 7 : 0;
     volatile int32_t *abort = &sm.abort;
+    SegIter si;
+    si.init(p, sm, blockIdx.x);
+    Seg sg, nx;
+    bool have = si.next(p, sm, sg);
+    uint32_t qf[KS][2];
+    if (have)
+        load_q<D, GC>(p, sg, lane, qf);
     uint32_t g_tile = 0;
-
-    for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
-        const Item I = decode_item(p, sm, it);
-        const int h0 = I.kvh * p.group + I.sub * GC;
-        float2 qf[GC][VPL][4];
-        float2 acc[GC][VPL][4];
-        float m_run[GC], l_run[GC];
+    int seg_i = 0;
+    while (have) {
+        const bool more = si.next(p, sm, nx);
+        uint32_t qn[KS][2]; // next slice's queries, loading while this slice streams
+        if (more)
+            load_q<D, GC>(p, nx, lane, qn);
+        float acc[KS][4];
 #pragma unroll
-        for (int g = 0; g < GC; ++g) {
-            const uint4 *qrow = reinterpret_cast<const uint4 *>(p.q + ((int64_t)I.b * p.num_q_heads + h0 + g) * D);
-#pragma unroll
-            for (int i = 0; i < VPL; ++i) {
-                const uint4 qw = __ldg(qrow + j + 8 * i);
-                const uint32_t w4[4] = {qw.x, qw.y, qw.z, qw.w};
-#pragma unroll
-                for (int w = 0; w < 4; ++w) {
-                    const float2 f = bf16x2_to_float2(w4[w]);
-                    qf[g][i][w] = make_float2(f.x * p.q_scale, f.y * p.q_scale);
-                    acc[g][i][w] = make_float2(0.f, 0.f);
-                }
-            }
-            m_run[g] = kNegInf;
-            l_run[g] = 0.f;
-        }
+        for (int mt = 0; mt < KS; ++mt)
+            acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.f;
+        float m_run[2] = {kNegInf, kNegInf}, l_run[2] = {0.f, 0.f};
         int bad = 0;
-        const int n_tiles = (I.tok1 - I.tok0 + kTile - 1) / kTile;
+        bool ok = true;
+        const int n_tiles = (sg.tok1 - sg.tok0 + kTile - 1) / kTile;
         for (int t = 0; t < n_tiles; ++t, ++g_tile) {
             const int s = g_tile % S;
-            if (!wait_or_abort(&sm.full[s], (g_tile / S) & 1u, abort))
+            if (!wait_or_abort(&sm.full[s], (g_tile / S) & 1u, abort)) {
+                ok = false;
                 break;
+            }
             bad |= ((volatile int32_t *)sm.stage_bad)[s];
-            const int nv = min(kTile, I.tok1 - (I.tok0 + t * kTile));
-            if (nv == kTile)
-                consume_tile<D, GC, false>(sm.kv[s][0], sm.kv[s][1], nv, warp, lane, qf, acc, m_run, l_run);
-            else
-                consume_tile<D, GC, true>(sm.kv[s][0], sm.kv[s][1], nv, warp, lane, qf, acc, m_run, l_run);
+            const int nv = min(kTile, sg.tok1 - (sg.tok0 + t * kTile));
+            if (nv == kTile) {
+                consume_tile<D, false>(sm.kv[s][0], sm.kv[s][1], nv, warp, lane, swz, p.q_scale, qf, acc, m_run,
+                                       l_run);
+            } else {
+                consume_tile<D, true>(sm.kv[s][0], sm.kv[s][1], nv, warp, lane, swz, p.q_scale, qf, acc, m_run,
+                                      l_run);
+                // the zeroed V rows were written by the generic proxy; order
+                // them before the TMA that refills this stage
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            }
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(&sm.empty[s]);
         }
-        // warp: sum the four 8-lane groups (they share m_run)
+        if (!ok)
+            break;
+        // l over the 8 row groups
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            l_run[j] += __shfl_xor_sync(0xffffffffu, l_run[j], 4);
+            l_run[j] += __shfl_xor_sync(0xffffffffu, l_run[j], 8);
+            l_run[j] += __shfl_xor_sync(0xffffffffu, l_run[j], 16);
+        }
+        const int slot = seg_i & 1;
+        if (seg_i >= kSlots && !wait_or_abort(&sm.epi_empty[slot], ((seg_i >> 1) - 1) & 1u, abort))
+            break;
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const int h = 2 * c + j;
+            if (h < GC) {
+#pragma unroll
+                for (int mt = 0; mt < KS; ++mt) {
+                    sm.red_o[slot][warp][h][16 * mt + g] = acc[mt][j];
+                    sm.red_o[slot][warp][h][16 * mt + g + 8] = acc[mt][2 + j];
+                }
+                if (g == 0) {
+                    sm.red_m[slot][warp][h] = m_run[j];
+                    sm.red_l[slot][warp][h] = l_run[j];
+                }
+            }
+        }
+        if (lane == 0)
+            sm.red_bad[slot][warp] = bad;
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive(&sm.epi_full[slot]);
+        ++seg_i;
+        have = more;
+        sg = nx;
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+            qf[ks][0] = qn[ks][0];
+            qf[ks][1] = qn[ks][1];
+        }
+    }
+}
+
+// ---------------------------------------------------------------- epilogue
+// One warp; lane l holds elements e = l + 32 i (i < EPT) of the unit's
+// [GC][D] output, i.e. head e / D, dim e % D.
+template <int D, int GC>
+struct EpiState {
+    static constexpr int EPT = GC * D / 32;
+    float o[EPT];
+    float M[GC], L[GC];
+};
+
+// Writes one unit's output: zeros for inactive / failed rows, otherwise
+// merges the new token (when given), performs the append and normalises.
+template <int D, int GC>
+__device__ void finalize_warp(const KParams &p, const Seg &sg, EpiState<D, GC> &st, int bad, int lane)
+{
+    constexpr int EPT = EpiState<D, GC>::EPT;
+    const int h0 = sg.kvh * p.group + sg.sub * GC;
+    int err = 0;
+    if (sg.status == ROW_OVERFLOW)
+        err = PKV_ERR_OVERFLOW;
+    else if (sg.status == ROW_OK && bad)
+        err = PKV_ERR_PAGE;
+    int64_t dst = -1; // element offset of the appended token for this kv head
+    if (sg.status == ROW_OK && !err && p.with_new) {
+        const int page = p.block_table[(int64_t)sg.b * p.max_blocks + (sg.L >> p.page_shift)];
+        if (page < 1 || page >= p.num_pages) {
+            err = PKV_ERR_PAGE;
+        } else {
+            const int slot = sg.L & (p.page_size - 1);
+            dst = p.layout == PKV_NHD
+                      ? (((int64_t)page * p.page_size + slot) * p.num_kv_heads + sg.kvh) * D
+                      : (((int64_t)page * p.num_kv_heads + sg.kvh) * p.page_size + slot) * D;
+        }
+    }
+    const bool live = sg.status == ROW_OK && !err;
+    if (lane == 0 && err)
+        set_error(p.err_flag, err);
+    if (live && p.with_new) {
+        const __nv_bfloat16 *kn = p.k_new + ((int64_t)sg.b * p.num_kv_heads + sg.kvh) * D;
+        const __nv_bfloat16 *vn = p.v_new + ((int64_t)sg.b * p.num_kv_heads + sg.kvh) * D;
+        float sn[GC];
+#pragma unroll
+        for (int g = 0; g < GC; ++g) { // (q . k_new) * scale * log2 e
+            const __nv_bfloat16 *qh = p.q + ((int64_t)sg.b * p.num_q_heads + h0 + g) * D;
+            float s = 0.f;
+#pragma unroll
+            for (int d = lane; d < D; d += 32)
+                s = fmaf(__bfloat162float(qh[d]), __bfloat162float(kn[d]), s);
+            for (int o = 16; o > 0; o >>= 1)
+                s += __shfl_xor_sync(0xffffffffu, s, o);
+            sn[g] = s * p.q_scale;
+        }
+        if (sg.sub == 0) { // the append: one bit copy per kv head
+            constexpr int kVec = D / 8;
+            for (int cix = lane; cix < 2 * kVec; cix += 32) {
+                const bool is_v = cix >= kVec;
+                const int v = is_v ? cix - kVec : cix;
+                const uint4 val = reinterpret_cast<const uint4 *>(is_v ? vn : kn)[v];
+                reinterpret_cast<uint4 *>((is_v ? p.v_cache : p.k_cache) + dst)[v] = val;
+            }
+        }
+        float a[GC], cn[GC];
 #pragma unroll
         for (int g = 0; g < GC; ++g) {
-#pragma unroll
-            for (int i = 0; i < VPL; ++i)
-#pragma unroll
-                for (int w = 0; w < 4; ++w) {
-                    float2 v = acc[g][i][w];
-                    v.x += __shfl_xor_sync(0xffffffffu, v.x, 8);
-                    v.y += __shfl_xor_sync(0xffffffffu, v.y, 8);
-                    v.x += __shfl_xor_sync(0xffffffffu, v.x, 16);
-                    v.y += __shfl_xor_sync(0xffffffffu, v.y, 16);
-                    acc[g][i][w] = v;
-                }
-            l_run[g] += __shfl_xor_sync(0xffffffffu, l_run[g], 8);
-            l_run[g] += __shfl_xor_sync(0xffffffffu, l_run[g], 16);
+            const float Mn = fmaxf(st.M[g], sn[g]);
+            a[g] = ex2(st.M[g] - Mn); // M = -inf (no cached key) -> 0
+            cn[g] = ex2(sn[g] - Mn);
+            st.L[g] = fmaf(st.L[g], a[g], cn[g]);
+            st.M[g] = Mn;
         }
-        if (lane < 8) {
 #pragma unroll
-            for (int g = 0; g < GC; ++g) {
-#pragma unroll
-                for (int i = 0; i < VPL; ++i)
-#pragma unroll
-                    for (int w = 0; w < 4; ++w)
-                        *reinterpret_cast<float2 *>(&sm.red_o[warp][g][8 * (j + 8 * i) + 2 * w]) = acc[g][i][w];
-                if (lane == 0) {
-                    sm.red_m[warp][g] = m_run[g];
-                    sm.red_l[warp][g] = l_run[g];
-                }
-            }
+        for (int i = 0; i < EPT; ++i) {
+            const int e = lane + 32 * i, g = e / D, d = e % D;
+            st.o[i] = fmaf(st.o[i], a[g], cn[g] * __bfloat162float(vn[d]));
         }
-        named_sync(kBarConsumers, kConsumerThreads);
-        // CTA: merge the warps' partial softmax states
-        for (int e = tid; e < GC * D; e += kConsumerThreads) {
-            const int g = e / D, d = e - g * D;
-            float M = kNegInf;
-#pragma unroll
-            for (int w = 0; w < kWarps; ++w)
-                M = fmaxf(M, sm.red_m[w][g]);
-            float o = 0.f, l = 0.f;
-#pragma unroll
-            for (int w = 0; w < kWarps; ++w) {
-                const float m = sm.red_m[w][g];
-                const float a = m == kNegInf ? 0.f : ex2(m - M);
-                o = fmaf(a, sm.red_o[w][g][d], o);
-                l = fmaf(a, sm.red_l[w][g], l);
-            }
-            sm.fin_o[g][d] = o;
-            if (d == 0) {
-                sm.fin_m[g] = M;
-                sm.fin_l[g] = l;
-            }
-        }
-        // One thread decides whether the CTA stopped, so that every consumer
-        // thread takes the same path through the barriers below.
-        if (tid == 0)
-            sm.stop = *abort;
-        named_sync(kBarConsumers, kConsumerThreads);
-        const bool aborted = sm.stop != 0;
-        if (!aborted) {
-            if (I.nchunks == 1) {
-                finalize(p, sm, I, bad);
-            } else {
-                float *po = p.part_o + (int64_t)it * GC * D;
-                for (int e = tid; e < GC * D; e += kConsumerThreads)
-                    po[e] = (&sm.fin_o[0][0])[e];
-                if (tid < GC)
-                    p.part_ml[(int64_t)it * GC + tid] = make_float2(sm.fin_m[tid], bad ? -1.f : sm.fin_l[tid]);
-                __threadfence();
-                named_sync(kBarConsumers, kConsumerThreads);
-                if (tid == 0)
-                    sm.flag = atomicAdd(&p.tickets[I.unit], 1) == I.nchunks - 1;
-                named_sync(kBarConsumers, kConsumerThreads);
-                if (sm.flag) {
-                    __threadfence();
-                    const int any_bad = combine_partials(p, sm, I);
-                    finalize(p, sm, I, any_bad);
-                    if (tid == 0)
-                        p.tickets[I.unit] = 0; // ready for the next call
-                }
-            }
-        }
-        named_sync(kBarConsumers, kConsumerThreads);
-        if (aborted)
-            break;
     }
-    if (*abort && tid == 0)
+#pragma unroll
+    for (int i = 0; i < EPT; ++i) {
+        const int e = lane + 32 * i, g = e / D, d = e % D;
+        const bool any = live && st.L[g] > 0.f;
+        p.out[((int64_t)sg.b * p.num_q_heads + h0 + g) * D + d] = __float2bfloat16_rn(any ? st.o[i] / st.L[g] : 0.f);
+    }
+    if (p.lse != nullptr && lane < GC) {
+        float M = kNegInf, L = 0.f;
+#pragma unroll
+        for (int g = 0; g < GC; ++g)
+            if (g == lane) {
+                M = st.M[g];
+                L = st.L[g];
+            }
+        const bool any = live && L > 0.f;
+        p.lse[(int64_t)sg.b * p.num_q_heads + h0 + lane] = any ? (M + log2f(L)) * 0.69314718055994531f : kNegInf;
+    }
+}
+
+// Merges the n slice partials of one unit into st; returns nonzero if any
+// slice met a bad page.
+template <int D, int GC>
+__device__ int combine_warp(const KParams &p, EpiState<D, GC> &st, int kf, int n, int lane)
+{
+    constexpr int EPT = EpiState<D, GC>::EPT;
+    int bad = 0;
+#pragma unroll
+    for (int g = 0; g < GC; ++g) {
+        st.M[g] = kNegInf;
+        st.L[g] = 0.f;
+    }
+#pragma unroll
+    for (int i = 0; i < EPT; ++i)
+        st.o[i] = 0.f;
+    for (int j = 0; j < n; ++j) {
+        const int slot = slot_of(kf, j);
+        float2 ml[GC];
+        float ov[EPT];
+#pragma unroll
+        for (int g = 0; g < GC; ++g)
+            ml[g] = __ldcg(p.part_ml + (int64_t)slot * GC + g);
+#pragma unroll
+        for (int i = 0; i < EPT; ++i)
+            ov[i] = __ldcg(p.part_o + (int64_t)slot * GC * D + lane + 32 * i);
+        float a[GC], b[GC];
+#pragma unroll
+        for (int g = 0; g < GC; ++g) {
+            bad |= ml[g].y < 0.f;
+            const float l = fmaxf(ml[g].y, 0.f);
+            const float Mn = fmaxf(st.M[g], ml[g].x);
+            a[g] = st.M[g] == kNegInf ? 0.f : ex2(st.M[g] - Mn);
+            b[g] = ml[g].x == kNegInf ? 0.f : ex2(ml[g].x - Mn);
+            st.L[g] = st.L[g] * a[g] + l * b[g];
+            st.M[g] = Mn;
+        }
+#pragma unroll
+        for (int i = 0; i < EPT; ++i) {
+            const int g = (lane + 32 * i) / D;
+            st.o[i] = st.o[i] * a[g] + ov[i] * b[g];
+        }
+    }
+    return bad;
+}
+
+template <int D, int GC>
+__device__ void epilogue(const KParams &p, Smem<D, GC> &sm)
+{
+    constexpr int EPT = EpiState<D, GC>::EPT;
+    const int lane = threadIdx.x & 31;
+    volatile int32_t *abort = &sm.abort;
+    SegIter si;
+    si.init(p, sm, blockIdx.x);
+    Seg sg;
+    int seg_i = 0;
+    while (si.next(p, sm, sg)) {
+        const int slot = seg_i & 1;
+        if (!wait_or_abort(&sm.epi_full[slot], (seg_i >> 1) & 1u, abort))
+            break;
+        // merge the two consumer warps' states
+        EpiState<D, GC> st;
+        float w0[GC], w1[GC];
+#pragma unroll
+        for (int g = 0; g < GC; ++g) {
+            const float m0 = sm.red_m[slot][0][g], m1 = sm.red_m[slot][1][g];
+            const float M = fmaxf(m0, m1);
+            w0[g] = m0 == kNegInf ? 0.f : ex2(m0 - M);
+            w1[g] = m1 == kNegInf ? 0.f : ex2(m1 - M);
+            st.M[g] = M;
+            st.L[g] = w0[g] * sm.red_l[slot][0][g] + w1[g] * sm.red_l[slot][1][g];
+        }
+#pragma unroll
+        for (int i = 0; i < EPT; ++i) {
+            const int e = lane + 32 * i, g = e / D, d = e % D;
+            st.o[i] = w0[g] * sm.red_o[slot][0][g][d] + w1[g] * sm.red_o[slot][1][g][d];
+        }
+        int bad = sm.red_bad[slot][0] | sm.red_bad[slot][1];
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive(&sm.epi_empty[slot]); // consumers may refill this slot
+        ++seg_i;
+        const int kf = owner_of(p, sm, sg.u0);
+        const int n = owner_of(p, sm, sg.u0 + sg.n - 1) - kf + 1;
+        if (n == 1) {
+            finalize_warp<D, GC>(p, sg, st, bad, lane);
+            continue;
+        }
+        const int wslot = slot_of(kf, (int)blockIdx.x - kf);
+#pragma unroll
+        for (int i = 0; i < EPT; ++i)
+            p.part_o[(int64_t)wslot * GC * D + lane + 32 * i] = st.o[i];
+        if (lane < GC) {
+            float M = 0.f, L = 0.f;
+#pragma unroll
+            for (int g = 0; g < GC; ++g)
+                if (g == lane) {
+                    M = st.M[g];
+                    L = st.L[g];
+                }
+            p.part_ml[(int64_t)wslot * GC + lane] = make_float2(M, bad ? -1.f : L);
+        }
+        __threadfence();
+        __syncwarp();
+        int last = 0;
+        if (lane == 0)
+            last = atomicAdd(&p.tickets[sg.unit], 1) == n - 1;
+        last = __shfl_sync(0xffffffffu, last, 0);
+        if (last) {
+            __threadfence();
+            bad = combine_warp<D, GC>(p, st, kf, n, lane);
+            finalize_warp<D, GC>(p, sg, st, bad, lane);
+            if (lane == 0)
+                p.tickets[sg.unit] = 0; // ready for the next call
+        }
+    }
+    // Units with no cached token (inactive, overflowing or empty rows) get
+    // their output (zeros, or the new token alone) here: empty unit e goes
+    // to CTA e % gridDim.x.
+    if (!*abort) {
+        const int G = (int)gridDim.x, k = (int)blockIdx.x;
+        int e0 = 0; // empty units before row b, modulo G
+        for (int b = 0; b < p.batch; ++b) {
+            if (sm.rowtok[b + 1] != sm.rowtok[b])
+                continue;
+            for (int r = (k - e0 + G) % G; r < p.units; r += G) {
+                Seg es;
+                es.b = b;
+                es.r = r;
+                es.kvh = r / p.n_sub;
+                es.sub = r - es.kvh * p.n_sub;
+                es.unit = b * p.units + r;
+                es.L = sm.len[b];
+                es.status = row_status(p, es.L);
+                es.tok0 = es.tok1 = 0;
+                es.u0 = 0;
+                es.n = 0;
+                EpiState<D, GC> st;
+#pragma unroll
+                for (int g = 0; g < GC; ++g) {
+                    st.M[g] = kNegInf;
+                    st.L[g] = 0.f;
+                }
+#pragma unroll
+                for (int i = 0; i < EPT; ++i)
+                    st.o[i] = 0.f;
+                finalize_warp<D, GC>(p, es, st, 0, lane);
+            }
+            e0 = (e0 + p.units) % G;
+        }
+    }
+    if (*abort && lane == 0)
         set_error(p.err_flag, PKV_ERR_TIMEOUT);
 }
 
 template <int D, int GC>
-__global__ void __maxnreg__(200) decode_kernel(const __grid_constant__ KParams p,
+__global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant__ KParams p,
                                                           const __grid_constant__ CUtensorMap tm_k,
                                                           const __grid_constant__ CUtensorMap tm_v)
 {
     extern __shared__ unsigned char smem_raw[];
     Smem<D, GC> &sm = *reinterpret_cast<Smem<D, GC> *>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     constexpr int S = Smem<D, GC>::kStages;
+    const int warp = threadIdx.x >> 5;
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(&sm.full[s], 1);
             mbar_init(&sm.empty[s], kWarps);
         }
+        for (int s = 0; s < kSlots; ++s) {
+            mbar_init(&sm.epi_full[s], kWarps);
+            mbar_init(&sm.epi_empty[s], 1);
+        }
         sm.abort = 0;
         mbar_init_fence();
     }
-    if (threadIdx.x == kWarps * 32) {
+    if (threadIdx.x == kProducerWarp * 32) {
         prefetch_tensormap(&tm_k);
         prefetch_tensormap(&tm_v);
     }
     build_plan(p, sm); // ends with __syncthreads()
-    if (threadIdx.x >= kWarps * 32)
+    if (warp < kWarps)
+        consumers(p, sm);
+    else if (warp == kProducerWarp)
         producer(p, sm, &tm_k, &tm_v);
     else
-        consumers(p, sm);
+        epilogue(p, sm);
 }
 
 template <int D, int GC>
 size_t smem_bytes()
 {
-    return sizeof(Smem<D, GC>) + 128;
+    return sizeof(Smem<D, GC>) + 1024;
 }
 
 struct KernelEntry {
@@ -703,8 +946,8 @@ KernelEntry entry()
 }
 
 const KernelEntry kTable[] = {
-    entry<64, 1>(),  entry<64, 2>(),  entry<64, 4>(),  entry<64, 8>(),  entry<128, 1>(),
-        entry<128, 2>(), entry<128, 4>(), entry<256, 1>(), entry<256, 2>(),
+    entry<64, 1>(),  entry<64, 2>(),  entry<64, 4>(),  entry<64, 8>(),  entry<128, 1>(),  entry<128, 2>(),
+    entry<128, 4>(), entry<128, 8>(), entry<256, 1>(), entry<256, 2>(), entry<256, 4>(), entry<256, 8>(),
 };
 
 const KernelEntry *find_kernel(int D, int GC)
@@ -720,15 +963,24 @@ int kernel_index(const KernelEntry *e)
     return static_cast<int>(e - kTable);
 }
 
-int heads_per_cta(int group, int D)
+// Heads of one kv head that share a CTA: the MMA's N side holds 8.
+int heads_per_cta(int group)
 {
-    int gc = 1;
-    while (gc * 2 <= group && group % (gc * 2) == 0 && gc * 2 * D <= 512)
-        gc *= 2;
-    return gc;
+    return group < 8 ? group : 8;
 }
 
 } // namespace
+
+int decode_box_tokens(int page_size)
+{
+    return page_size < kDecodeTile ? page_size : kDecodeTile;
+}
+
+int decode_swizzle(int page_size)
+{
+    // 128-byte swizzle needs every box to start on a 1024-byte (8-row) boundary
+    return page_size >= 8 ? 1 : 0;
+}
 
 bool decode_shape(int batch, int max_blocks, int num_q_heads, const pkv_cache_desc &d, DecodeShape *s)
 {
@@ -737,54 +989,44 @@ bool decode_shape(int batch, int max_blocks, int num_q_heads, const pkv_cache_de
     s->group = num_q_heads / d.num_kv_heads;
     if (s->group & (s->group - 1))
         return false; // power-of-two groups only
-    s->heads_per_cta = heads_per_cta(s->group, d.head_dim);
+    s->heads_per_cta = heads_per_cta(s->group);
     if (find_kernel(d.head_dim, s->heads_per_cta) == nullptr)
+        return false;
+    // the plan counts tokens in int32
+    if ((int64_t)batch * max_blocks * d.page_size >= ((int64_t)1 << 31))
         return false;
     s->n_sub = s->group / s->heads_per_cta;
     s->units_per_row = d.num_kv_heads * s->n_sub;
-    int cmax = kDecodeChunkMaxPages * d.page_size;
-    if (cmax > 8192)
-        cmax = 8192;
-    if (cmax < kDecodeChunkMin)
-        cmax = kDecodeChunkMin;
-    s->chunk_max = cmax / kDecodeTile * kDecodeTile;
+    s->chunk_max = 0;
+    s->cap_items = 2 * (int64_t)kMaxGrid; // two partial slots per persistent CTA
     const int64_t units = (int64_t)batch * s->units_per_row;
-    const int64_t max_tokens = (int64_t)max_blocks * d.page_size;
-    int64_t per_unit = (max_tokens + s->chunk_max - 1) / s->chunk_max;
-    if (per_unit < 1)
-        per_unit = 1;
-    // The launch aims for at most kTargetItemsMax items when the chunk size is
-    // not capped (then items <= target + units); a capped chunk bounds the
-    // items of a unit by per_unit.  The layout does not depend on the device.
-    int64_t cap = kTargetItemsMax + units;
-    if (units * per_unit > cap)
-        cap = units * per_unit;
-    s->cap_items = cap;
     auto align = [](size_t x) { return (x + 255) & ~size_t(255); };
     const size_t tickets = align(sizeof(int32_t) * (size_t)units);
     s->off_ml = tickets;
-    s->off_o = s->off_ml + align(sizeof(float2) * (size_t)cap * s->heads_per_cta);
-    s->bytes = s->off_o + align(sizeof(float) * (size_t)cap * s->heads_per_cta * d.head_dim);
+    s->off_o = s->off_ml + align(sizeof(float2) * (size_t)s->cap_items * s->heads_per_cta);
+    s->bytes = s->off_o + align(sizeof(float) * (size_t)s->cap_items * s->heads_per_cta * d.head_dim);
     return true;
 }
 
 int decode_target_items(int device, int head_dim, int heads_per_cta)
 {
     // Per device and kernel: opt in to the kernel's shared memory once and
-    // size the plan for two items per resident CTA slot.
+    // size the persistent grid to the CTAs that fit on all SMs.
     constexpr int kDevices = 64, kKernels = 16;
     static int cache[kDevices][kKernels] = {};
     const KernelEntry *e = find_kernel(head_dim, heads_per_cta);
     if (e == nullptr || device < 0 || device >= kDevices)
-        return kTargetItemsMax;
+        return 1;
     int &slot = cache[device][kernel_index(e)];
     if (slot == 0) {
         int occ = 1;
         if (cudaFuncSetAttribute(e->fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)e->smem) != cudaSuccess ||
+            cudaFuncSetAttribute(e->fn, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 cudaSharedmemCarveoutMaxShared) != cudaSuccess ||
             cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, e->fn, kThreads, e->smem) != cudaSuccess || occ < 1)
             occ = 1;
-        const int t = 2 * sm_count(device) * occ;
-        slot = t > kTargetItemsMax ? kTargetItemsMax : t;
+        const int t = sm_count(device) * occ;
+        slot = t > kMaxGrid ? kMaxGrid : t;
     }
     return slot;
 }
@@ -821,10 +1063,9 @@ cudaError_t launch_decode(const DecodeArgs &a, const CUtensorMap &tm_k, const CU
     p.page_shift = a.page_shift;
     p.num_pages = a.desc.num_pages;
     p.layout = a.desc.layout;
-    p.box_tokens = a.desc.page_size < kDecodeTile ? a.desc.page_size : kDecodeTile;
-    p.target_items = a.target_items;
-    p.chunk_max = a.shape.chunk_max;
+    p.box_tokens = decode_box_tokens(a.desc.page_size);
     p.with_new = (a.k_new != nullptr) ? 1 : 0;
+    p.swizzle = decode_swizzle(a.desc.page_size);
     p.q_scale = a.q_scale;
     void *args[] = {&p, const_cast<CUtensorMap *>(&tm_k), const_cast<CUtensorMap *>(&tm_v)};
     return cudaLaunchKernel(e->fn, dim3(a.grid), dim3(kThreads), args, e->smem, stream);

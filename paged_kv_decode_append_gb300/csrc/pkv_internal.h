@@ -84,9 +84,15 @@ struct AppendArgs {
 
 cudaError_t launch_append(const AppendArgs &a, cudaStream_t stream);
 
+// Decode TMA geometry: tokens per box and whether boxes are 128B-swizzled.
+int decode_box_tokens(int page_size);
+int decode_swizzle(int page_size);
+
 // Tensor map over one K or V pool whose boxes are `box_tokens` consecutive
-// tokens of one kv head ([box_tokens, head_dim] in shared memory).
-CUresult encode_pool_map(CUtensorMap *map, const pkv_cache_desc &d, void *base, int box_tokens);
+// tokens of one kv head and `box_dim` of its head_dim values
+// ([box_tokens][box_dim] in shared memory), optionally 128-byte swizzled.
+CUresult encode_pool_map(CUtensorMap *map, const pkv_cache_desc &d, void *base, int box_tokens, int box_dim,
+                         int swizzle);
 
 int sm_count(int device);
 
