@@ -10,7 +10,7 @@
 // structure (work split along the key axis, partial results merged by their
 // log-sum-exp) is the one the page's profile names (flash_fwd_splitkv_kernel).
 //
-// GB300 design (one persistent CTA per resident slot, four warps):
+// GB300 design (one persistent CTA per resident slot, five warps):
 //  * producer warp: streams 32-token tiles of K and V of one kv head through
 //    a shared-memory ring with TMA (one box per page piece and 64-column
 //    half row, 128-byte swizzle, L2 evict-first); page ids are prefetched 32
@@ -18,10 +18,12 @@
 //  * two consumer warps: 16 token rows of every tile each, on tensor-core
 //    tiles (mma.sync m16n8k16, bf16 in, fp32 accumulate) with an online
 //    softmax in base 2; see consume_tile.  At the end of a slice they hand
-//    their softmax state to the epilogue warp through a double-buffered
+//    their softmax state to an epilogue warp through a double-buffered
 //    shared-memory slot and go straight on to the next slice.
-//  * epilogue warp: merges the two warps' states and finishes the slice off
-//    the streaming path: a unit cut into n slices writes n fp32 partials;
+//  * two epilogue warps (alternate slices): merge the two consumer warps'
+//    states and finish the slice off the streaming path, with every global
+//    input of the finish loaded before the state arrives: a unit cut into
+//    n slices writes n fp32 partials;
 //    the last slice to arrive (atomic ticket, never a spin) merges them by
 //    log-sum-exp, folds in the new token (scored from k_new, not re-read from
 //    the cache), performs the append and writes bf16 output and lse.
@@ -43,8 +45,8 @@ namespace {
 
 constexpr int kWarps = 2;                    // consumer warps, 16 token rows each
 constexpr int kProducerWarp = kWarps;        // warp 2
-constexpr int kEpilogueWarp = kWarps + 1;    // warp 3
-constexpr int kThreads = (kWarps + 2) * 32;
+constexpr int kEpilogueWarp = kWarps + 1;    // warps 3 and 4
+constexpr int kThreads = (kWarps + 3) * 32;
 constexpr int kTile = kDecodeTile; // tokens per pipeline tile
 constexpr int kMaxGrid = 2048;     // persistent CTAs at most (workspace sizing)
 constexpr int kMinSlice = 64;      // tokens per CTA slice at least
@@ -546,7 +548,7 @@ __device__ __forceinline__ void load_q(const KParams &p, const Seg &sg, int lane
 }
 
 // Consumer warp: runs the tile loop of every slice of this CTA and hands each
-// slice's softmax state (o, m, l per head) to the epilogue warp.
+// slice's softmax state (o, m, l per head) to an epilogue warp.
 template <int D, int GC>
 __device__ void consumers(const KParams &p, Smem<D, GC> &sm)
 {
@@ -644,8 +646,9 @@ __device__ void consumers(const KParams &p, Smem<D, GC> &sm)
 }
 
 // ---------------------------------------------------------------- epilogue
-// One warp; lane l holds elements e = l + 32 i (i < EPT) of the unit's
-// [GC][D] output, i.e. head e / D, dim e % D.
+// Two epilogue warps; warp w finishes the slices with index parity w.  Lane l
+// holds elements e = l + 32 i (i < EPT) of the unit's [GC][D] output, i.e.
+// head e / D, dim e % D.
 template <int D, int GC>
 struct EpiState {
     static constexpr int EPT = GC * D / 32;
@@ -653,10 +656,55 @@ struct EpiState {
     float M[GC], L[GC];
 };
 
+// Everything a unit's finish reads from global memory besides the partials,
+// loaded into registers before the slice's softmax state arrives.
+template <int D, int GC>
+struct EpiInputs {
+    static constexpr int KP = D / 64;  // bf16 pairs of one row per lane
+    static constexpr int VV = D / 32;  // v_new values per lane
+    static constexpr int CH = (2 * D / 8 + 31) / 32; // 16-byte append chunks per lane
+    uint32_t q2[GC][KP], k2[KP];
+    float vv[VV];
+    uint4 chunk[CH];
+    int page;
+};
+
+template <int D, int GC>
+__device__ __forceinline__ void load_epi_inputs(const KParams &p, const Seg &sg, int lane, EpiInputs<D, GC> &in)
+{
+    in.page = 0;
+    if (sg.status != ROW_OK || !p.with_new)
+        return;
+    const int h0 = sg.kvh * p.group + sg.sub * GC;
+    const __nv_bfloat16 *kn = p.k_new + ((int64_t)sg.b * p.num_kv_heads + sg.kvh) * D;
+    const __nv_bfloat16 *vn = p.v_new + ((int64_t)sg.b * p.num_kv_heads + sg.kvh) * D;
+#pragma unroll
+    for (int j = 0; j < EpiInputs<D, GC>::KP; ++j) {
+        in.k2[j] = reinterpret_cast<const uint32_t *>(kn)[lane + 32 * j];
+#pragma unroll
+        for (int g = 0; g < GC; ++g)
+            in.q2[g][j] = reinterpret_cast<const uint32_t *>(p.q + ((int64_t)sg.b * p.num_q_heads + h0 + g) * D)[lane + 32 * j];
+    }
+#pragma unroll
+    for (int m = 0; m < EpiInputs<D, GC>::VV; ++m)
+        in.vv[m] = __bfloat162float(vn[lane + 32 * m]);
+    constexpr int kVec = D / 8;
+#pragma unroll
+    for (int ci = 0; ci < EpiInputs<D, GC>::CH; ++ci) {
+        const int cix = lane + 32 * ci;
+        in.chunk[ci] = make_uint4(0u, 0u, 0u, 0u);
+        if (cix < 2 * kVec)
+            in.chunk[ci] = cix < kVec ? reinterpret_cast<const uint4 *>(kn)[cix]
+                                      : reinterpret_cast<const uint4 *>(vn)[cix - kVec];
+    }
+    in.page = p.block_table[(int64_t)sg.b * p.max_blocks + (sg.L >> p.page_shift)];
+}
+
 // Writes one unit's output: zeros for inactive / failed rows, otherwise
 // merges the new token (when given), performs the append and normalises.
 template <int D, int GC>
-__device__ void finalize_warp(const KParams &p, const Seg &sg, EpiState<D, GC> &st, int bad, int lane)
+__device__ void finalize_warp(const KParams &p, const Seg &sg, EpiState<D, GC> &st, const EpiInputs<D, GC> &in,
+                              int bad, int lane)
 {
     constexpr int EPT = EpiState<D, GC>::EPT;
     const int h0 = sg.kvh * p.group + sg.sub * GC;
@@ -665,43 +713,39 @@ __device__ void finalize_warp(const KParams &p, const Seg &sg, EpiState<D, GC> &
         err = PKV_ERR_OVERFLOW;
     else if (sg.status == ROW_OK && bad)
         err = PKV_ERR_PAGE;
-    int64_t dst = -1; // element offset of the appended token for this kv head
-    if (sg.status == ROW_OK && !err && p.with_new) {
-        const int page = p.block_table[(int64_t)sg.b * p.max_blocks + (sg.L >> p.page_shift)];
-        if (page < 1 || page >= p.num_pages) {
-            err = PKV_ERR_PAGE;
-        } else {
-            const int slot = sg.L & (p.page_size - 1);
-            dst = p.layout == PKV_NHD
-                      ? (((int64_t)page * p.page_size + slot) * p.num_kv_heads + sg.kvh) * D
-                      : (((int64_t)page * p.num_kv_heads + sg.kvh) * p.page_size + slot) * D;
-        }
-    }
+    if (sg.status == ROW_OK && !err && p.with_new && (in.page < 1 || in.page >= p.num_pages))
+        err = PKV_ERR_PAGE;
     const bool live = sg.status == ROW_OK && !err;
     if (lane == 0 && err)
         set_error(p.err_flag, err);
     if (live && p.with_new) {
-        const __nv_bfloat16 *kn = p.k_new + ((int64_t)sg.b * p.num_kv_heads + sg.kvh) * D;
-        const __nv_bfloat16 *vn = p.v_new + ((int64_t)sg.b * p.num_kv_heads + sg.kvh) * D;
-        float sn[GC];
+        float sn[GC]; // (q . k_new) * scale * log2 e
 #pragma unroll
-        for (int g = 0; g < GC; ++g) { // (q . k_new) * scale * log2 e
-            const __nv_bfloat16 *qh = p.q + ((int64_t)sg.b * p.num_q_heads + h0 + g) * D;
+        for (int g = 0; g < GC; ++g) {
             float s = 0.f;
 #pragma unroll
-            for (int d = lane; d < D; d += 32)
-                s = fmaf(__bfloat162float(qh[d]), __bfloat162float(kn[d]), s);
+            for (int j = 0; j < EpiInputs<D, GC>::KP; ++j) {
+                const float2 qv = unpack_bf16(in.q2[g][j]), kv = unpack_bf16(in.k2[j]);
+                s = fmaf(qv.x, kv.x, fmaf(qv.y, kv.y, s));
+            }
             for (int o = 16; o > 0; o >>= 1)
                 s += __shfl_xor_sync(0xffffffffu, s, o);
             sn[g] = s * p.q_scale;
         }
         if (sg.sub == 0) { // the append: one bit copy per kv head
             constexpr int kVec = D / 8;
-            for (int cix = lane; cix < 2 * kVec; cix += 32) {
-                const bool is_v = cix >= kVec;
-                const int v = is_v ? cix - kVec : cix;
-                const uint4 val = reinterpret_cast<const uint4 *>(is_v ? vn : kn)[v];
-                reinterpret_cast<uint4 *>((is_v ? p.v_cache : p.k_cache) + dst)[v] = val;
+            const int slot = sg.L & (p.page_size - 1);
+            const int64_t dst = p.layout == PKV_NHD
+                                    ? (((int64_t)in.page * p.page_size + slot) * p.num_kv_heads + sg.kvh) * D
+                                    : (((int64_t)in.page * p.num_kv_heads + sg.kvh) * p.page_size + slot) * D;
+#pragma unroll
+            for (int ci = 0; ci < EpiInputs<D, GC>::CH; ++ci) {
+                const int cix = lane + 32 * ci;
+                if (cix < 2 * kVec) {
+                    const bool is_v = cix >= kVec;
+                    reinterpret_cast<uint4 *>((is_v ? p.v_cache : p.k_cache) + dst)[is_v ? cix - kVec : cix] =
+                        in.chunk[ci];
+                }
             }
         }
         float a[GC], cn[GC];
@@ -715,8 +759,8 @@ __device__ void finalize_warp(const KParams &p, const Seg &sg, EpiState<D, GC> &
         }
 #pragma unroll
         for (int i = 0; i < EPT; ++i) {
-            const int e = lane + 32 * i, g = e / D, d = e % D;
-            st.o[i] = fmaf(st.o[i], a[g], cn[g] * __bfloat162float(vn[d]));
+            const int g = (lane + 32 * i) / D;
+            st.o[i] = fmaf(st.o[i], a[g], cn[g] * in.vv[i % EpiInputs<D, GC>::VV]);
         }
     }
 #pragma unroll
@@ -784,19 +828,37 @@ __device__ int combine_warp(const KParams &p, EpiState<D, GC> &st, int kf, int n
 }
 
 template <int D, int GC>
-__device__ void epilogue(const KParams &p, Smem<D, GC> &sm)
+__device__ void epilogue(const KParams &p, Smem<D, GC> &sm, int ew)
 {
     constexpr int EPT = EpiState<D, GC>::EPT;
     const int lane = threadIdx.x & 31;
+    const int k = (int)blockIdx.x;
     volatile int32_t *abort = &sm.abort;
     SegIter si;
-    si.init(p, sm, blockIdx.x);
+    si.init(p, sm, k);
     Seg sg;
     int seg_i = 0;
+    bool stopped = false;
     while (si.next(p, sm, sg)) {
-        const int slot = seg_i & 1;
-        if (!wait_or_abort(&sm.epi_full[slot], (seg_i >> 1) & 1u, abort))
+        const int mine = seg_i;
+        ++seg_i;
+        if ((mine & 1) != ew)
+            continue;
+        const int slot = mine & 1;
+        EpiInputs<D, GC> in;
+        load_epi_inputs<D, GC>(p, sg, lane, in);
+        // slices of this unit: kf .. kf + n - 1 (a slice from the unit's first
+        // to its last token is the whole unit)
+        int kf = k, n = 1;
+        if (sg.tok0 != 0 || sg.tok1 != sg.n) {
+            kf = sg.tok0 == 0 ? k : owner_of(p, sm, sg.u0);
+            const int kl = sg.tok1 == sg.n ? k : owner_of(p, sm, sg.u0 + sg.n - 1);
+            n = kl - kf + 1;
+        }
+        if (!wait_or_abort(&sm.epi_full[slot], (mine >> 1) & 1u, abort)) {
+            stopped = true;
             break;
+        }
         // merge the two consumer warps' states
         EpiState<D, GC> st;
         float w0[GC], w1[GC];
@@ -818,14 +880,11 @@ __device__ void epilogue(const KParams &p, Smem<D, GC> &sm)
         __syncwarp();
         if (lane == 0)
             mbar_arrive(&sm.epi_empty[slot]); // consumers may refill this slot
-        ++seg_i;
-        const int kf = owner_of(p, sm, sg.u0);
-        const int n = owner_of(p, sm, sg.u0 + sg.n - 1) - kf + 1;
         if (n == 1) {
-            finalize_warp<D, GC>(p, sg, st, bad, lane);
+            finalize_warp<D, GC>(p, sg, st, in, bad, lane);
             continue;
         }
-        const int wslot = slot_of(kf, (int)blockIdx.x - kf);
+        const int wslot = slot_of(kf, k - kf);
 #pragma unroll
         for (int i = 0; i < EPT; ++i)
             p.part_o[(int64_t)wslot * GC * D + lane + 32 * i] = st.o[i];
@@ -848,21 +907,23 @@ __device__ void epilogue(const KParams &p, Smem<D, GC> &sm)
         if (last) {
             __threadfence();
             bad = combine_warp<D, GC>(p, st, kf, n, lane);
-            finalize_warp<D, GC>(p, sg, st, bad, lane);
+            finalize_warp<D, GC>(p, sg, st, in, bad, lane);
             if (lane == 0)
                 p.tickets[sg.unit] = 0; // ready for the next call
         }
     }
     // Units with no cached token (inactive, overflowing or empty rows) get
-    // their output (zeros, or the new token alone) here: empty unit e goes
-    // to CTA e % gridDim.x.
-    if (!*abort) {
-        const int G = (int)gridDim.x, k = (int)blockIdx.x;
-        int e0 = 0; // empty units before row b, modulo G
+    // their output (zeros, or the new token alone) here: empty unit e goes to
+    // CTA e % gridDim.x, epilogue warp (e / gridDim.x) % 2.
+    if (!stopped && !*abort) {
+        const int G = (int)gridDim.x;
+        int e0 = 0; // empty units before row b
         for (int b = 0; b < p.batch; ++b) {
             if (sm.rowtok[b + 1] != sm.rowtok[b])
                 continue;
-            for (int r = (k - e0 + G) % G; r < p.units; r += G) {
+            for (int r = (int)(((long long)k - e0 % G + G) % G); r < p.units; r += G) {
+                if ((((long long)e0 + r) / G & 1) != ew)
+                    continue;
                 Seg es;
                 es.b = b;
                 es.r = r;
@@ -874,6 +935,8 @@ __device__ void epilogue(const KParams &p, Smem<D, GC> &sm)
                 es.tok0 = es.tok1 = 0;
                 es.u0 = 0;
                 es.n = 0;
+                EpiInputs<D, GC> in;
+                load_epi_inputs<D, GC>(p, es, lane, in);
                 EpiState<D, GC> st;
 #pragma unroll
                 for (int g = 0; g < GC; ++g) {
@@ -883,9 +946,9 @@ __device__ void epilogue(const KParams &p, Smem<D, GC> &sm)
 #pragma unroll
                 for (int i = 0; i < EPT; ++i)
                     st.o[i] = 0.f;
-                finalize_warp<D, GC>(p, es, st, 0, lane);
+                finalize_warp<D, GC>(p, es, st, in, 0, lane);
             }
-            e0 = (e0 + p.units) % G;
+            e0 += p.units;
         }
     }
     if (*abort && lane == 0)
@@ -924,7 +987,7 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
     else if (warp == kProducerWarp)
         producer(p, sm, &tm_k, &tm_v);
     else
-        epilogue(p, sm);
+        epilogue(p, sm, warp - kEpilogueWarp);
 }
 
 template <int D, int GC>
