@@ -184,29 +184,40 @@ def sum_over_ranks(x: float, world: int, device) -> float:
     return float(t.item())
 
 
-def cpu_baseline(sw, lens_step0: np.ndarray, budget_s: float = 12.0):
-    """Times the fp64 oracle (all host cores) on whole layers of decode step 0
-    until `budget_s` is spent; returns GB/s of the same algorithmic bytes."""
+def cpu_baseline(sw, prompt_lens: np.ndarray, budget_s: float = 12.0, max_steps: int = 64):
+    """Times the fp64 oracle (all host cores) on whole decode steps (all 36
+    layers, all rows and heads) from step 0 on, until `budget_s` of oracle
+    time is spent; returns GB/s of the same algorithmic bytes."""
     import oracle
     from paged_kv_decode_append_gb300 import workloads as wl
 
-    inputs = wl.sweep_step_inputs(sw, 0, sw.k_caches[0].device, layers=1)
-    q, kn, vn = (wl.bits(t) for t in inputs[0])
+    dev = sw.k_caches[0].device
     rows = list(range(sw.batch))
-    need = lens_step0 + 1
-    done_bytes, elapsed, layers = 0, 0.0, 0
+    need = prompt_lens + max_steps + 1
+    host = []
+    for layer in range(sw.layers):  # compact host copies, reused (and appended to) step after step
+        k, v, bt = wl.compact_rows(sw.k_caches[layer], sw.v_caches[layer], sw.block_table, rows, need, P)
+        host.append((k, v, bt))
+    d = oracle.CacheDesc(host[0][0].shape[0], P, HKV, D, oracle.NHD)
     threads = oracle.max_threads(0)
-    while elapsed < budget_s and layers < sw.layers:
-        k, v, bt = wl.compact_rows(sw.k_caches[layers], sw.v_caches[layers], sw.block_table, rows, need, P)
-        d = oracle.CacheDesc(k.shape[0], P, HKV, D, oracle.NHD)
-        t0 = time.perf_counter()
-        oracle.decode(d, k, v, q, kn, vn, bt, lens_step0, sw.softmax_scale, nthreads=0)
-        elapsed += time.perf_counter() - t0
-        done_bytes += call_bytes(lens_step0, sw.batch)
-        layers += 1
+    done_bytes, elapsed, calls, step = 0, 0.0, 0, 0
+    while elapsed < budget_s and step < max_steps:
+        lens = (prompt_lens + step).astype(np.int32)
+        inputs = wl.sweep_step_inputs(sw, step, dev, layers=sw.layers)
+        for layer in range(sw.layers):
+            q, kn, vn = (wl.bits(t) for t in inputs[layer])
+            k, v, bt = host[layer]
+            t0 = time.perf_counter()
+            oracle.decode(d, k, v, q, kn, vn, bt, lens, sw.softmax_scale, nthreads=0)
+            elapsed += time.perf_counter() - t0
+            done_bytes += call_bytes(lens, sw.batch)
+            calls += 1
+            if elapsed >= budget_s:
+                break
+        step += 1
     return {"value": done_bytes / elapsed / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
-            "sample": f"{layers} of 36 layers of decode step 0 (B={sw.batch}, all rows and heads), fp64 oracle "
-                      f"with OpenMP over (row, head), {elapsed:.1f} s"}
+            "sample": f"{calls} layer calls (decode steps 0..{step - 1} of the 36-layer B={sw.batch} workload, all "
+                      f"rows and heads), fp64 oracle with OpenMP over (row, head), {elapsed:.1f} s of oracle time"}
 
 
 def run_reference(args):
@@ -271,6 +282,8 @@ def main():
     ap.add_argument("--layout", default="shuffled", choices=["shuffled", "contiguous"])
     ap.add_argument("--e2e-steps", type=int, default=100)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-overlap", action="store_true",
+                    help="plain launches instead of programmatic dependent launch between layers")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -298,18 +311,31 @@ def main():
     step_bytes = [L * call_bytes(lens_all[s], B) for s in range(DECODE_CAPACITY)]
     stream = torch.cuda.current_stream(dev)
 
+    flags = 0 if args.no_overlap else pkv.api.DECODE_OVERLAP_PROLOGUE
+
     def layer_call(step, layer, q, kn, vn):
         pkv.pkv_decode_attn(sw.k_caches[layer], sw.v_caches[layer], q, kn, vn, bt, lens_dev[step % DECODE_CAPACITY],
-                            sw.softmax_scale, out=outs[layer], workspace=ws)
+                            sw.softmax_scale, out=outs[layer], workspace=ws, flags=flags)
 
+    # One CUDA graph per decode step (its 36 layer launches back to back),
+    # captured up front and replayed back to back in the timed region.  The
+    # region holds this one kernel only, so its average launch duration is the
+    # region time over the launches.
+    n_steps = args.warmup + args.steps
+    graphs = []
+    for s in range(n_steps):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for layer, (q, kn, vn) in enumerate(inputs[s % ring]):
+                layer_call(s, layer, q, kn, vn)
+        graphs.append(g)
+    torch.cuda.synchronize(dev)
     for s in range(args.warmup):
-        for layer, (q, kn, vn) in enumerate(inputs[s % ring]):
-            layer_call(s, layer, q, kn, vn)
+        graphs[s].replay()
     torch.cuda.synchronize(dev)
     barrier(world)
 
     n_ev = args.steps * L
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_ev)]
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     total_bytes = 0
     with ClockSampler(local) as clocks:
@@ -317,62 +343,88 @@ def main():
         barrier(world)
         torch.cuda.nvtx.range_push("timed")
         start.record(stream)
-        i = 0
-        for s in range(args.warmup, args.warmup + args.steps):
-            for layer, (q, kn, vn) in enumerate(inputs[s % ring]):
-                ev[i][0].record(stream)
-                layer_call(s, layer, q, kn, vn)
-                ev[i][1].record(stream)
-                i += 1
+        for s in range(args.warmup, n_steps):
+            graphs[s].replay()
             total_bytes += step_bytes[s % DECODE_CAPACITY]
         end.record(stream)
         torch.cuda.nvtx.range_pop()
         torch.cuda.synchronize(dev)
         barrier(world)
     ms = start.elapsed_time(end)
-    launch_ms = np.array([a.elapsed_time(b) for a, b in ev])
     ms_max = max_over_ranks(ms, world, dev)
     all_bytes = sum_over_ranks(float(total_bytes), world, dev)
     value = all_bytes / (ms_max * 1e-3) / 1e9
     launch_bytes = total_bytes / n_ev
-    kernel_ms = float(launch_ms.mean())
+    kernel_ms = ms / n_ev
     achieved = launch_bytes / (kernel_ms * 1e-3) / 1e9
     peak, peak_kind = peaks()
     traffic_ratio = recorded_traffic()
+    del graphs
 
-    # end to end: host inputs each step (pinned), outputs back to host
+    # Diagnostic: each launch alone (plain launch, CUDA events around it) for
+    # the first `iso_steps` steps, to show the duration of one kernel by itself.
+    iso_steps = min(20, args.steps)
+    iso_ev, iso_bytes = [], []
+    for s in range(iso_steps):
+        for layer, (q, kn, vn) in enumerate(inputs[s % ring]):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                pkv.pkv_decode_attn(sw.k_caches[layer], sw.v_caches[layer], q, kn, vn, bt,
+                                    lens_dev[s % DECODE_CAPACITY], sw.softmax_scale, out=outs[layer], workspace=ws)
+            torch.cuda.synchronize(dev)
+            a.record(stream)
+            g.replay()
+            b.record(stream)
+            iso_ev.append((a, b, g))
+            iso_bytes.append(call_bytes(lens_all[s % DECODE_CAPACITY], B))
+    torch.cuda.synchronize(dev)
+    iso_ms = np.array([a.elapsed_time(b) for a, b, _ in iso_ev])
+    iso_gbs = float(np.sum(iso_bytes) / (iso_ms.sum() * 1e-3) / 1e9)
+    del iso_ev
+
+    # End to end through the public API: each step copies its q / k_new / v_new
+    # for all layers from pinned host memory, runs the 36 calls and copies the
+    # outputs back (one graph per step, like the timed region).
     e2e_steps = min(args.e2e_steps, args.steps)
     h_in = [[tuple(t.cpu().pin_memory() for t in trip) for trip in inputs[r]] for r in range(2)]
     h_out = [torch.empty(B, HQ, D, dtype=torch.bfloat16).pin_memory() for _ in range(L)]
     d_in = [tuple(torch.empty_like(t) for t in trip) for trip in inputs[0]]
     h2d = sum(t.numel() * 2 for trip in inputs[0] for t in trip)
     d2h = L * B * HQ * D * 2
+    e_graphs = []
+    for s in range(e2e_steps):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            src = h_in[s % 2]
+            for layer in range(L):
+                for dst, hs in zip(d_in[layer], src[layer]):
+                    dst.copy_(hs, non_blocking=True)
+            for layer in range(L):
+                layer_call(s, layer, *d_in[layer])
+            for layer in range(L):
+                h_out[layer].copy_(outs[layer], non_blocking=True)
+        e_graphs.append(g)
     torch.cuda.synchronize(dev)
     barrier(world)
     e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e_bytes = 0
     e_start.record(stream)
     for s in range(e2e_steps):
-        src = h_in[s % 2]
-        for layer in range(L):
-            for dst, hs in zip(d_in[layer], src[layer]):
-                dst.copy_(hs, non_blocking=True)
-        for layer in range(L):
-            layer_call(s, layer, *d_in[layer])
-        for layer in range(L):
-            h_out[layer].copy_(outs[layer], non_blocking=True)
+        e_graphs[s].replay()
         e_bytes += step_bytes[s % DECODE_CAPACITY]
     e_end.record(stream)
     torch.cuda.synchronize(dev)
     e_ms = max_over_ranks(e_start.elapsed_time(e_end), world, dev)
     e_all = sum_over_ranks(float(e_bytes), world, dev)
     e2e_value = e_all / (e_ms * 1e-3) / 1e9
+    del e_graphs
 
     if rank != 0:
         return
     cpu = None
     if not args.no_cpu_baseline and world == 1:
-        cpu = cpu_baseline(sw, lens_all[0])
+        cpu = cpu_baseline(sw, sw.prompt_lens)
     steps_tok = B / (ms / args.steps / L * 1e-3)  # decode tokens/s per attention layer
     out = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
@@ -385,11 +437,14 @@ def main():
                      "traffic": None if traffic_ratio is None else traffic_ratio * launch_bytes,
                      "peak_kind": peak_kind, "kernel": "pkv::decode_kernel<128,4>",
                      "algorithmic_bytes_per_launch": launch_bytes, "launch_ms_mean": kernel_ms,
-                     "launch_ms_median": float(np.median(launch_ms)), "launch_ms_best": float(launch_ms.min())},
+                     "isolated_launch_ms_mean": float(iso_ms.mean()), "isolated_launch_ms_best": float(iso_ms.min()),
+                     "isolated_gbs": iso_gbs, "isolated_launches": int(iso_ms.size)},
         "clocks": clocks.summary(),
         "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "steps": e2e_steps},
         "gpu_launches": n_ev,
+        "launch": "one CUDA graph per decode step (36 kernel launches" + (
+            ")" if args.no_overlap else ", programmatic dependent launch between them)"),
         "cpu_baseline": cpu,
     }
     print(json.dumps(out))

@@ -160,6 +160,28 @@ PKV_API pkv_status pkv_decode_attn(const pkv_cache_desc *desc, void *k_cache, vo
                            void *workspace, size_t workspace_bytes, int32_t *err_flag,
                            void *stream);
 
+/* Flags of pkv_decode_attn_ex. */
+#define PKV_DECODE_OVERLAP_PROLOGUE 1u
+/* Launch with programmatic dependent launch: the kernel may start while the
+ * preceding kernel in the stream is still finishing, and reads cache_seqlens
+ * and block_table (only those) before that kernel has completed; every other
+ * input is read, and every output written, only after it has completed.
+ * Use it when the immediately preceding kernel does not write cache_seqlens
+ * or block_table (for instance the layers of one decode step, which share
+ * them).  Capturable in CUDA graphs. */
+
+/*
+ * pkv_decode_attn_ex -- pkv_decode_attn with launch flags (PKV_DECODE_*).
+ * flags = 0 behaves exactly like pkv_decode_attn.
+ */
+PKV_API pkv_status pkv_decode_attn_ex(const pkv_cache_desc *desc, void *k_cache, void *v_cache,
+                                      const void *q, const void *k_new, const void *v_new,
+                                      const int32_t *block_table, int32_t max_blocks,
+                                      const int32_t *cache_seqlens, int32_t batch,
+                                      int32_t num_q_heads, float softmax_scale, void *out,
+                                      float *lse, void *workspace, size_t workspace_bytes,
+                                      int32_t *err_flag, void *stream, uint32_t flags);
+
 /* ---------------------------------------------------------------------
  * Host page-pool and block-table helpers (no device memory involved).
  * Source: "flex_attention + paged KV + CUDA graphs vs vLLM", "What each

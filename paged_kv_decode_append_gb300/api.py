@@ -17,6 +17,7 @@ NHD = 0
 HND = 1
 
 OK, EINVAL, EUNSUPPORTED, ECUDA, ENOPAGES, EWORKSPACE = range(6)
+DECODE_OVERLAP_PROLOGUE = 1  # pkv_decode_attn_ex flag (see include/pkv.h)
 ERR_PAGE, ERR_OVERFLOW, ERR_TIMEOUT = 1, 2, 4
 
 
@@ -95,8 +96,10 @@ def pkv_append(k_cache, v_cache, k_new, v_new, block_table, cache_seqlens, appen
 
 
 def pkv_decode_attn(k_cache, v_cache, q, k_new, v_new, block_table, cache_seqlens, softmax_scale: float,
-                    out=None, lse=None, workspace=None, err_flag=None, layout: int = NHD) -> torch.Tensor:
-    """Fused append + decode attention; returns ``out`` ``[B, Hq, D]`` bf16."""
+                    out=None, lse=None, workspace=None, err_flag=None, layout: int = NHD,
+                    flags: int = 0) -> torch.Tensor:
+    """Fused append + decode attention; returns ``out`` ``[B, Hq, D]`` bf16.
+    ``flags`` (e.g. DECODE_OVERLAP_PROLOGUE) selects ``pkv_decode_attn_ex``."""
     for t, n in ((k_cache, "k_cache"), (v_cache, "v_cache"), (q, "q"), (k_new, "k_new"), (v_new, "v_new"),
                  (out, "out")):
         _bf16(t, n)
@@ -110,11 +113,13 @@ def pkv_decode_attn(k_cache, v_cache, q, k_new, v_new, block_table, cache_seqlen
         out = torch.empty_like(q)
     if workspace is None:
         workspace = decode_workspace(B, block_table.shape[1], Hq, desc, q.device)
-    st = _lib.load().pkv_decode_attn(
-        ctypes.byref(desc), _ptr(k_cache), _ptr(v_cache), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(block_table),
-        block_table.shape[1], _ptr(cache_seqlens), B, Hq, float(softmax_scale), _ptr(out), _ptr(lse),
-        _ptr(workspace), workspace.numel(), _ptr(err_flag), _stream(q.device))
-    _check(st, "pkv_decode_attn")
+    args = (ctypes.byref(desc), _ptr(k_cache), _ptr(v_cache), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(block_table),
+            block_table.shape[1], _ptr(cache_seqlens), B, Hq, float(softmax_scale), _ptr(out), _ptr(lse),
+            _ptr(workspace), workspace.numel(), _ptr(err_flag), _stream(q.device))
+    if flags:
+        _check(_lib.load().pkv_decode_attn_ex(*args, int(flags)), "pkv_decode_attn_ex")
+    else:
+        _check(_lib.load().pkv_decode_attn(*args), "pkv_decode_attn")
     return out
 
 

@@ -209,6 +209,18 @@ pkv_status pkv_decode_attn(const pkv_cache_desc *desc, void *k_cache, void *v_ca
                            void *out, float *lse, void *workspace, size_t workspace_bytes, int32_t *err_flag,
                            void *stream)
 {
+    return pkv_decode_attn_ex(desc, k_cache, v_cache, q, k_new, v_new, block_table, max_blocks, cache_seqlens, batch,
+                              num_q_heads, softmax_scale, out, lse, workspace, workspace_bytes, err_flag, stream, 0u);
+}
+
+pkv_status pkv_decode_attn_ex(const pkv_cache_desc *desc, void *k_cache, void *v_cache, const void *q,
+                              const void *k_new, const void *v_new, const int32_t *block_table, int32_t max_blocks,
+                              const int32_t *cache_seqlens, int32_t batch, int32_t num_q_heads, float softmax_scale,
+                              void *out, float *lse, void *workspace, size_t workspace_bytes, int32_t *err_flag,
+                              void *stream, uint32_t flags)
+{
+    if ((flags & ~PKV_DECODE_OVERLAP_PROLOGUE) != 0)
+        return PKV_EINVAL;
     const pkv_status st = check_desc(desc);
     if (st != PKV_OK)
         return st;
@@ -259,6 +271,7 @@ pkv_status pkv_decode_attn(const pkv_cache_desc *desc, void *k_cache, void *v_ca
     // persistent grid: every CTA that fits on the device at once
     a.target_items = 0;
     a.grid = decode_target_items(dev, desc->head_dim, shape.heads_per_cta);
+    a.flags = flags;
 
     const int box = decode_box_tokens(desc->page_size);
     const int swz = decode_swizzle(desc->page_size);

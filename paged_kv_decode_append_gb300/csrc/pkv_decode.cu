@@ -74,6 +74,7 @@ struct KParams {
     int batch, num_q_heads, num_kv_heads, group, n_sub, units, max_blocks;
     int page_size, page_shift, num_pages, layout, box_tokens;
     int with_new, swizzle;
+    int pdl; // launched with programmatic dependent launch
     float q_scale;
 };
 
@@ -101,8 +102,17 @@ struct Smem {
     long long work;                      // units * rowtok[batch]
     long long slice;                     // work positions per CTA
     int32_t geff;                        // CTAs that own a token slice
+    int32_t n_empty;                     // rows without a cached token
     int32_t abort;
 };
+
+// Programmatic dependent launch: wait for the preceding grid (and its memory)
+// before the first access that is not cache_seqlens / block_table.
+__device__ __forceinline__ void wait_prior_grid(const KParams &p)
+{
+    if (p.pdl)
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+}
 
 __device__ __forceinline__ float ex2(float x)
 {
@@ -151,7 +161,7 @@ __device__ void build_plan(const KParams &p, Smem<D, GC> &sm)
     __syncthreads();
     if (threadIdx.x < 32) {
         const int lane = threadIdx.x;
-        int run = 0;
+        int run = 0, empty = 0;
         for (int base = 0; base < p.batch; base += 32) {
             const int i = base + lane;
             int n = 0;
@@ -159,6 +169,7 @@ __device__ void build_plan(const KParams &p, Smem<D, GC> &sm)
                 const int L = sm.len[i];
                 n = row_status(p, L) == ROW_OK ? L : 0;
             }
+            empty += __popc(__ballot_sync(0xffffffffu, i < p.batch && n == 0));
             int incl = n;
             for (int o = 1; o < 32; o <<= 1) {
                 const int v = __shfl_up_sync(0xffffffffu, incl, o);
@@ -180,6 +191,7 @@ __device__ void build_plan(const KParams &p, Smem<D, GC> &sm)
             const long long slice = work > 0 ? (work + g - 1) / g : 1;
             sm.work = work;
             sm.slice = slice;
+            sm.n_empty = empty;
             sm.geff = work > 0 ? (int)((work + slice - 1) / slice) : 1;
         }
     }
@@ -244,37 +256,76 @@ struct Seg {
     int n;        // unit's cache tokens
 };
 
-// Walks the slices of one CTA's range, one unit at a time.
+// Walks the slices of one CTA's range [pos0, end), one unit each.  The two
+// boundary slices come first (the range's first and last unit, the only ones
+// that can be shared with a neighbouring CTA), then the whole units between
+// them, so the partial-merging work of shared units is not left for the end.
 struct SegIter {
-    long long pos, end;
+    long long pos0, end, f_end, mid_pos, mid_end;
+    long long u0_f, u0_l;
+    int b_f, r_f, rel_f, b_l, r_l;
+    int stage; // 0: first slice, 1: last slice, 2: middle units, 3: done
     template <int D, int GC>
     __device__ __forceinline__ void init(const KParams &p, const Smem<D, GC> &sm, int k)
     {
-        if (k < sm.geff) {
-            pos = boundary(p, sm, k);
-            end = boundary(p, sm, k + 1);
-        } else {
-            pos = end = 0;
-        }
+        stage = 3;
+        if (k >= sm.geff)
+            return;
+        const long long x = (long long)k * sm.slice;
+        if (x >= sm.work)
+            return;
+        u0_f = locate(p, sm, x, b_f, r_f, rel_f);
+        rel_f &= ~(kTile - 1);
+        pos0 = u0_f + rel_f;
+        end = boundary(p, sm, k + 1);
+        if (pos0 >= end)
+            return;
+        f_end = min(end, u0_f + (sm.rowtok[b_f + 1] - sm.rowtok[b_f]));
+        mid_pos = mid_end = f_end;
+        stage = 0;
+    }
+    template <int D, int GC>
+    __device__ __forceinline__ void fill(const KParams &p, const Smem<D, GC> &sm, Seg &s, int b, int r, long long u0,
+                                         long long from, long long to)
+    {
+        s.b = b;
+        s.r = r;
+        s.u0 = u0;
+        s.n = sm.rowtok[b + 1] - sm.rowtok[b];
+        s.tok0 = (int)(from - u0);
+        s.tok1 = (int)(to - u0);
+        s.kvh = r / p.n_sub;
+        s.sub = r - s.kvh * p.n_sub;
+        s.unit = b * p.units + r;
+        s.L = sm.len[b];
+        s.status = row_status(p, s.L);
     }
     template <int D, int GC>
     __device__ __forceinline__ bool next(const KParams &p, const Smem<D, GC> &sm, Seg &s)
     {
-        if (pos >= end)
-            return false;
-        int rel;
-        s.u0 = locate(p, sm, pos, s.b, s.r, rel);
-        s.n = sm.rowtok[s.b + 1] - sm.rowtok[s.b];
-        const long long seg_end = min(end, s.u0 + s.n);
-        s.tok0 = rel;
-        s.tok1 = rel + (int)(seg_end - pos);
-        s.kvh = s.r / p.n_sub;
-        s.sub = s.r - s.kvh * p.n_sub;
-        s.unit = s.b * p.units + s.r;
-        s.L = sm.len[s.b];
-        s.status = row_status(p, s.L);
-        pos = seg_end;
-        return true;
+        if (stage == 0) {
+            fill(p, sm, s, b_f, r_f, u0_f, pos0, f_end);
+            stage = f_end < end ? 1 : 3;
+            return true;
+        }
+        if (stage == 1) {
+            int rel_l;
+            u0_l = locate(p, sm, end - 1, b_l, r_l, rel_l);
+            mid_end = u0_l;
+            fill(p, sm, s, b_l, r_l, u0_l, u0_l, end);
+            stage = 2;
+            return true;
+        }
+        if (stage == 2 && mid_pos < mid_end) {
+            int b, r, rel;
+            const long long u0 = locate(p, sm, mid_pos, b, r, rel); // rel == 0: a whole unit
+            const long long e = u0 + (sm.rowtok[b + 1] - sm.rowtok[b]);
+            fill(p, sm, s, b, r, u0, u0, e);
+            mid_pos = e;
+            return true;
+        }
+        stage = 3;
+        return false;
     }
 };
 
@@ -303,15 +354,14 @@ __device__ void producer(const KParams &p, Smem<D, GC> &sm, const CUtensorMap *t
     int win = have ? load_window(p.block_table + (int64_t)sg.b * p.max_blocks, sg.tok0 >> p.page_shift,
                                  (sg.tok1 - 1) >> p.page_shift, lane)
                    : 0;
+    wait_prior_grid(p); // page ids are loading; K/V and the error flag come after
     while (have && !*abort) {
         const int32_t *bt_row = p.block_table + (int64_t)sg.b * p.max_blocks;
         const int last_pg = (sg.tok1 - 1) >> p.page_shift;
         int wbase = sg.tok0 >> p.page_shift;
         int nxt = load_window(bt_row, wbase + 32, last_pg, lane);
-        const bool more = si.next(p, sm, nx);
-        const int nwin = more ? load_window(p.block_table + (int64_t)nx.b * p.max_blocks, nx.tok0 >> p.page_shift,
-                                            (nx.tok1 - 1) >> p.page_shift, lane)
-                              : 0;
+        bool more = false;
+        int nwin = 0;
         const int n_tiles = (sg.tok1 - sg.tok0 + kTile - 1) / kTile;
         for (int t = 0; t < n_tiles; ++t, ++g_tile) {
             const int s = g_tile % S;
@@ -360,6 +410,12 @@ __device__ void producer(const KParams &p, Smem<D, GC> &sm, const CUtensorMap *t
             if (lane == 0 && bad)
                 set_error(p.err_flag, PKV_ERR_PAGE);
             __syncwarp();
+            if (t == 0) { // next slice and its first page window, off the first tile's critical path
+                more = si.next(p, sm, nx);
+                nwin = more ? load_window(p.block_table + (int64_t)nx.b * p.max_blocks, nx.tok0 >> p.page_shift,
+                                          (nx.tok1 - 1) >> p.page_shift, lane)
+                            : 0;
+            }
         }
         have = more;
         sg = nx;
@@ -563,15 +619,14 @@ __device__ void consumers(const KParams &p, Smem<D, GC> &sm)
     Seg sg, nx;
     bool have = si.next(p, sm, sg);
     uint32_t qf[KS][2];
+    wait_prior_grid(p);
     if (have)
         load_q<D, GC>(p, sg, lane, qf);
     uint32_t g_tile = 0;
     int seg_i = 0;
     while (have) {
-        const bool more = si.next(p, sm, nx);
+        bool more = false;
         uint32_t qn[KS][2]; // next slice's queries, loading while this slice streams
-        if (more)
-            load_q<D, GC>(p, nx, lane, qn);
         float acc[KS][4];
 #pragma unroll
         for (int mt = 0; mt < KS; ++mt)
@@ -601,6 +656,11 @@ __device__ void consumers(const KParams &p, Smem<D, GC> &sm)
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(&sm.empty[s]);
+            if (t == 0) {
+                more = si.next(p, sm, nx);
+                if (more)
+                    load_q<D, GC>(p, nx, lane, qn);
+            }
         }
         if (!ok)
             break;
@@ -647,24 +707,28 @@ __device__ void consumers(const KParams &p, Smem<D, GC> &sm)
 
 // ---------------------------------------------------------------- epilogue
 // Two epilogue warps; warp w finishes the slices with index parity w.  Lane l
-// holds elements e = l + 32 i (i < EPT) of the unit's [GC][D] output, i.e.
-// head e / D, dim e % D.
+// holds element pairs e = 2 l + 64 i (i < EPT2) of the unit's [GC][D]
+// output, i.e. head e / D, dims e % D and e % D + 1.
 template <int D, int GC>
 struct EpiState {
-    static constexpr int EPT = GC * D / 32;
-    float o[EPT];
+    static constexpr int EPT2 = GC * D / 64;
+    float2 o[EPT2];
     float M[GC], L[GC];
 };
+
+template <int D>
+__device__ __forceinline__ int pair_elem(int lane, int i)
+{
+    return 2 * lane + 64 * i;
+}
 
 // Everything a unit's finish reads from global memory besides the partials,
 // loaded into registers before the slice's softmax state arrives.
 template <int D, int GC>
 struct EpiInputs {
-    static constexpr int KP = D / 64;  // bf16 pairs of one row per lane
-    static constexpr int VV = D / 32;  // v_new values per lane
+    static constexpr int KP = D / 64;                // bf16 pairs of one row per lane
     static constexpr int CH = (2 * D / 8 + 31) / 32; // 16-byte append chunks per lane
-    uint32_t q2[GC][KP], k2[KP];
-    float vv[VV];
+    uint32_t q2[GC][KP], k2[KP], v2[KP];
     uint4 chunk[CH];
     int page;
 };
@@ -681,13 +745,11 @@ __device__ __forceinline__ void load_epi_inputs(const KParams &p, const Seg &sg,
 #pragma unroll
     for (int j = 0; j < EpiInputs<D, GC>::KP; ++j) {
         in.k2[j] = reinterpret_cast<const uint32_t *>(kn)[lane + 32 * j];
+        in.v2[j] = reinterpret_cast<const uint32_t *>(vn)[lane + 32 * j];
 #pragma unroll
         for (int g = 0; g < GC; ++g)
             in.q2[g][j] = reinterpret_cast<const uint32_t *>(p.q + ((int64_t)sg.b * p.num_q_heads + h0 + g) * D)[lane + 32 * j];
     }
-#pragma unroll
-    for (int m = 0; m < EpiInputs<D, GC>::VV; ++m)
-        in.vv[m] = __bfloat162float(vn[lane + 32 * m]);
     constexpr int kVec = D / 8;
 #pragma unroll
     for (int ci = 0; ci < EpiInputs<D, GC>::CH; ++ci) {
@@ -706,7 +768,8 @@ template <int D, int GC>
 __device__ void finalize_warp(const KParams &p, const Seg &sg, EpiState<D, GC> &st, const EpiInputs<D, GC> &in,
                               int bad, int lane)
 {
-    constexpr int EPT = EpiState<D, GC>::EPT;
+    constexpr int EPT2 = EpiState<D, GC>::EPT2;
+    constexpr int KP = EpiInputs<D, GC>::KP;
     const int h0 = sg.kvh * p.group + sg.sub * GC;
     int err = 0;
     if (sg.status == ROW_OVERFLOW)
@@ -724,7 +787,7 @@ __device__ void finalize_warp(const KParams &p, const Seg &sg, EpiState<D, GC> &
         for (int g = 0; g < GC; ++g) {
             float s = 0.f;
 #pragma unroll
-            for (int j = 0; j < EpiInputs<D, GC>::KP; ++j) {
+            for (int j = 0; j < KP; ++j) {
                 const float2 qv = unpack_bf16(in.q2[g][j]), kv = unpack_bf16(in.k2[j]);
                 s = fmaf(qv.x, kv.x, fmaf(qv.y, kv.y, s));
             }
@@ -758,16 +821,27 @@ __device__ void finalize_warp(const KParams &p, const Seg &sg, EpiState<D, GC> &
             st.M[g] = Mn;
         }
 #pragma unroll
-        for (int i = 0; i < EPT; ++i) {
-            const int g = (lane + 32 * i) / D;
-            st.o[i] = fmaf(st.o[i], a[g], cn[g] * in.vv[i % EpiInputs<D, GC>::VV]);
+        for (int i = 0; i < EPT2; ++i) {
+            const int g = pair_elem<D>(lane, i) / D;
+            const float2 v = unpack_bf16(in.v2[i % KP]);
+            st.o[i].x = fmaf(st.o[i].x, a[g], cn[g] * v.x);
+            st.o[i].y = fmaf(st.o[i].y, a[g], cn[g] * v.y);
         }
     }
+    // rows without a visible key (or failed rows) give exact zeros: select,
+    // never multiply, since their state may hold NaN from unread slots
+    float inv[GC];
+    bool any[GC];
 #pragma unroll
-    for (int i = 0; i < EPT; ++i) {
-        const int e = lane + 32 * i, g = e / D, d = e % D;
-        const bool any = live && st.L[g] > 0.f;
-        p.out[((int64_t)sg.b * p.num_q_heads + h0 + g) * D + d] = __float2bfloat16_rn(any ? st.o[i] / st.L[g] : 0.f);
+    for (int g = 0; g < GC; ++g) {
+        any[g] = live && st.L[g] > 0.f;
+        inv[g] = any[g] ? 1.f / st.L[g] : 0.f;
+    }
+    uint32_t *out = reinterpret_cast<uint32_t *>(p.out + ((int64_t)sg.b * p.num_q_heads + h0) * D);
+#pragma unroll
+    for (int i = 0; i < EPT2; ++i) {
+        const int e = pair_elem<D>(lane, i), g = e / D;
+        out[e >> 1] = any[g] ? pack_bf16(st.o[i].x * inv[g], st.o[i].y * inv[g]) : 0u;
     }
     if (p.lse != nullptr && lane < GC) {
         float M = kNegInf, L = 0.f;
@@ -783,11 +857,12 @@ __device__ void finalize_warp(const KParams &p, const Seg &sg, EpiState<D, GC> &
 }
 
 // Merges the n slice partials of one unit into st; returns nonzero if any
-// slice met a bad page.
+// slice met a bad page.  The loads of all slices are issued before the math.
 template <int D, int GC>
 __device__ int combine_warp(const KParams &p, EpiState<D, GC> &st, int kf, int n, int lane)
 {
-    constexpr int EPT = EpiState<D, GC>::EPT;
+    constexpr int EPT2 = EpiState<D, GC>::EPT2;
+    constexpr int kBatch = EPT2 >= 16 ? 1 : (EPT2 >= 8 ? 2 : 4); // slices whose loads are in flight together
     int bad = 0;
 #pragma unroll
     for (int g = 0; g < GC; ++g) {
@@ -795,33 +870,45 @@ __device__ int combine_warp(const KParams &p, EpiState<D, GC> &st, int kf, int n
         st.L[g] = 0.f;
     }
 #pragma unroll
-    for (int i = 0; i < EPT; ++i)
-        st.o[i] = 0.f;
-    for (int j = 0; j < n; ++j) {
-        const int slot = slot_of(kf, j);
-        float2 ml[GC];
-        float ov[EPT];
+    for (int i = 0; i < EPT2; ++i)
+        st.o[i] = make_float2(0.f, 0.f);
+    for (int j0 = 0; j0 < n; j0 += kBatch) {
+        float2 ml[kBatch][GC];
+        float2 ov[kBatch][EPT2];
 #pragma unroll
-        for (int g = 0; g < GC; ++g)
-            ml[g] = __ldcg(p.part_ml + (int64_t)slot * GC + g);
+        for (int jj = 0; jj < kBatch; ++jj) {
+            if (j0 + jj < n) {
+                const int slot = slot_of(kf, j0 + jj);
 #pragma unroll
-        for (int i = 0; i < EPT; ++i)
-            ov[i] = __ldcg(p.part_o + (int64_t)slot * GC * D + lane + 32 * i);
-        float a[GC], b[GC];
+                for (int g = 0; g < GC; ++g)
+                    ml[jj][g] = __ldcg(p.part_ml + (int64_t)slot * GC + g);
+                const float2 *po = reinterpret_cast<const float2 *>(p.part_o + (int64_t)slot * GC * D);
 #pragma unroll
-        for (int g = 0; g < GC; ++g) {
-            bad |= ml[g].y < 0.f;
-            const float l = fmaxf(ml[g].y, 0.f);
-            const float Mn = fmaxf(st.M[g], ml[g].x);
-            a[g] = st.M[g] == kNegInf ? 0.f : ex2(st.M[g] - Mn);
-            b[g] = ml[g].x == kNegInf ? 0.f : ex2(ml[g].x - Mn);
-            st.L[g] = st.L[g] * a[g] + l * b[g];
-            st.M[g] = Mn;
+                for (int i = 0; i < EPT2; ++i)
+                    ov[jj][i] = __ldcg(po + (pair_elem<D>(lane, i) >> 1));
+            }
         }
 #pragma unroll
-        for (int i = 0; i < EPT; ++i) {
-            const int g = (lane + 32 * i) / D;
-            st.o[i] = st.o[i] * a[g] + ov[i] * b[g];
+        for (int jj = 0; jj < kBatch; ++jj) {
+            if (j0 + jj >= n)
+                break;
+            float a[GC], b[GC];
+#pragma unroll
+            for (int g = 0; g < GC; ++g) {
+                bad |= ml[jj][g].y < 0.f;
+                const float l = fmaxf(ml[jj][g].y, 0.f);
+                const float Mn = fmaxf(st.M[g], ml[jj][g].x);
+                a[g] = st.M[g] == kNegInf ? 0.f : ex2(st.M[g] - Mn);
+                b[g] = ml[jj][g].x == kNegInf ? 0.f : ex2(ml[jj][g].x - Mn);
+                st.L[g] = st.L[g] * a[g] + l * b[g];
+                st.M[g] = Mn;
+            }
+#pragma unroll
+            for (int i = 0; i < EPT2; ++i) {
+                const int g = pair_elem<D>(lane, i) / D;
+                st.o[i].x = st.o[i].x * a[g] + ov[jj][i].x * b[g];
+                st.o[i].y = st.o[i].y * a[g] + ov[jj][i].y * b[g];
+            }
         }
     }
     return bad;
@@ -830,7 +917,7 @@ __device__ int combine_warp(const KParams &p, EpiState<D, GC> &st, int kf, int n
 template <int D, int GC>
 __device__ void epilogue(const KParams &p, Smem<D, GC> &sm, int ew)
 {
-    constexpr int EPT = EpiState<D, GC>::EPT;
+    constexpr int EPT2 = EpiState<D, GC>::EPT2;
     const int lane = threadIdx.x & 31;
     const int k = (int)blockIdx.x;
     volatile int32_t *abort = &sm.abort;
@@ -839,6 +926,7 @@ __device__ void epilogue(const KParams &p, Smem<D, GC> &sm, int ew)
     Seg sg;
     int seg_i = 0;
     bool stopped = false;
+    wait_prior_grid(p);
     while (si.next(p, sm, sg)) {
         const int mine = seg_i;
         ++seg_i;
@@ -872,9 +960,11 @@ __device__ void epilogue(const KParams &p, Smem<D, GC> &sm, int ew)
             st.L[g] = w0[g] * sm.red_l[slot][0][g] + w1[g] * sm.red_l[slot][1][g];
         }
 #pragma unroll
-        for (int i = 0; i < EPT; ++i) {
-            const int e = lane + 32 * i, g = e / D, d = e % D;
-            st.o[i] = w0[g] * sm.red_o[slot][0][g][d] + w1[g] * sm.red_o[slot][1][g][d];
+        for (int i = 0; i < EPT2; ++i) {
+            const int e = pair_elem<D>(lane, i), g = e / D;
+            const float2 r0 = *reinterpret_cast<const float2 *>(&(&sm.red_o[slot][0][0][0])[e]);
+            const float2 r1 = *reinterpret_cast<const float2 *>(&(&sm.red_o[slot][1][0][0])[e]);
+            st.o[i] = make_float2(w0[g] * r0.x + w1[g] * r1.x, w0[g] * r0.y + w1[g] * r1.y);
         }
         int bad = sm.red_bad[slot][0] | sm.red_bad[slot][1];
         __syncwarp();
@@ -885,9 +975,10 @@ __device__ void epilogue(const KParams &p, Smem<D, GC> &sm, int ew)
             continue;
         }
         const int wslot = slot_of(kf, k - kf);
+        float2 *po = reinterpret_cast<float2 *>(p.part_o + (int64_t)wslot * GC * D);
 #pragma unroll
-        for (int i = 0; i < EPT; ++i)
-            p.part_o[(int64_t)wslot * GC * D + lane + 32 * i] = st.o[i];
+        for (int i = 0; i < EPT2; ++i)
+            po[pair_elem<D>(lane, i) >> 1] = st.o[i];
         if (lane < GC) {
             float M = 0.f, L = 0.f;
 #pragma unroll
@@ -915,7 +1006,7 @@ __device__ void epilogue(const KParams &p, Smem<D, GC> &sm, int ew)
     // Units with no cached token (inactive, overflowing or empty rows) get
     // their output (zeros, or the new token alone) here: empty unit e goes to
     // CTA e % gridDim.x, epilogue warp (e / gridDim.x) % 2.
-    if (!stopped && !*abort) {
+    if (!stopped && !*abort && sm.n_empty > 0) {
         const int G = (int)gridDim.x;
         int e0 = 0; // empty units before row b
         for (int b = 0; b < p.batch; ++b) {
@@ -944,8 +1035,8 @@ __device__ void epilogue(const KParams &p, Smem<D, GC> &sm, int ew)
                     st.L[g] = 0.f;
                 }
 #pragma unroll
-                for (int i = 0; i < EPT; ++i)
-                    st.o[i] = 0.f;
+                for (int i = 0; i < EPT2; ++i)
+                    st.o[i] = make_float2(0.f, 0.f);
                 finalize_warp<D, GC>(p, es, st, in, 0, lane);
             }
             e0 += p.units;
@@ -965,6 +1056,8 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     constexpr int S = Smem<D, GC>::kStages;
     const int warp = threadIdx.x >> 5;
+    if (p.pdl && threadIdx.x == 0) // the next grid may start filling SMs this one frees
+        asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(&sm.full[s], 1);
@@ -1129,9 +1222,22 @@ cudaError_t launch_decode(const DecodeArgs &a, const CUtensorMap &tm_k, const CU
     p.box_tokens = decode_box_tokens(a.desc.page_size);
     p.with_new = (a.k_new != nullptr) ? 1 : 0;
     p.swizzle = decode_swizzle(a.desc.page_size);
+    p.pdl = (a.flags & PKV_DECODE_OVERLAP_PROLOGUE) ? 1 : 0;
     p.q_scale = a.q_scale;
     void *args[] = {&p, const_cast<CUtensorMap *>(&tm_k), const_cast<CUtensorMap *>(&tm_v)};
-    return cudaLaunchKernel(e->fn, dim3(a.grid), dim3(kThreads), args, e->smem, stream);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(a.grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = e->smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    if (p.pdl) {
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    return cudaLaunchKernelExC(&cfg, e->fn, args);
 }
 
 } // namespace pkv

@@ -61,6 +61,7 @@ struct DecodeArgs {
     DecodeShape shape;
     int target_items;
     int grid;
+    uint32_t flags; // PKV_DECODE_*
 };
 
 cudaError_t launch_decode(const DecodeArgs &a, const CUtensorMap &tm_k, const CUtensorMap &tm_v,

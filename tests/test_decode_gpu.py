@@ -160,7 +160,7 @@ def test_single_key_is_exact():
 
 def test_inactive_and_empty_rows():
     case = wl.tiny(device=DEV)
-    case.cache_seqlens = np.array([-1, 0, 17, -5], np.int32)
+    case.cache_seqlens = np.array([-1, 0, 1, -5], np.int32)  # row 2 keeps its one cached token
     before = _sha(case.k_cache)
     out, lse = _run(case, with_new=False)
     o = f32(out)
@@ -220,3 +220,45 @@ def test_large_batch_limit():
     with pytest.raises(pkv.PkvError):
         big = _random_case(9, 1025, 8, 2, 64, 16, np.zeros(1025, np.int32))
         _run(big)
+
+
+@pytest.mark.parametrize("graph", [False, True])
+def test_overlap_prologue_launch_is_bit_identical(graph):
+    """Back-to-back layers sharing one workspace, launched with programmatic
+    dependent launch (eagerly and inside a CUDA graph), give the same bits as
+    plain launches."""
+    layers = 3
+    sw = wl.batch_sweep(32, device=DEV, contiguous=False, layers=layers)
+    bt = torch.as_tensor(sw.block_table, device=DEV)
+    sl = torch.as_tensor(sw.prompt_lens.astype(np.int32), device=DEV)  # step 0: the prompt is cached
+    desc = pkv.cache_desc(sw.k_caches[0])
+    ins = wl.sweep_step_inputs(sw, 0, DEV)
+    results = []
+    for flags in (0, pkv.api.DECODE_OVERLAP_PROLOGUE):
+        kc = [k.clone() for k in sw.k_caches]
+        vc = [v.clone() for v in sw.v_caches]
+        ws = pkv.decode_workspace(32, sw.max_blocks, 32, desc, DEV)
+        outs = [torch.empty(32, 32, 128, dtype=torch.bfloat16, device=DEV) for _ in range(layers)]
+        lses = [torch.empty(32, 32, dtype=torch.float32, device=DEV) for _ in range(layers)]
+
+        def step():
+            for layer, (q, kn, vn) in enumerate(ins):
+                pkv.pkv_decode_attn(kc[layer], vc[layer], q, kn, vn, bt, sl, sw.softmax_scale, out=outs[layer],
+                                    lse=lses[layer], workspace=ws, flags=flags)
+
+        if graph and flags:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                step()
+            g.replay()
+        else:
+            step()
+        torch.cuda.synchronize()
+        results.append((outs, lses, kc, vc))
+    (o0, l0, k0, v0), (o1, l1, k1, v1) = results
+    for layer in range(layers):
+        assert torch.isfinite(o0[layer].float()).all()
+        assert torch.equal(o0[layer].view(torch.int16), o1[layer].view(torch.int16))
+        assert torch.equal(l0[layer].view(torch.int32), l1[layer].view(torch.int32))
+        assert torch.equal(k0[layer].view(torch.int16), k1[layer].view(torch.int16))
+        assert torch.equal(v0[layer].view(torch.int16), v1[layer].view(torch.int16))
