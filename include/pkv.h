@@ -68,7 +68,9 @@ typedef enum {
     PKV_EUNSUPPORTED = 2, /* valid but not built (head_dim, page size, group) */
     PKV_ECUDA = 3,        /* a CUDA runtime / driver call failed */
     PKV_ENOPAGES = 4,     /* page pool exhausted; nothing was taken */
-    PKV_EWORKSPACE = 5    /* workspace NULL or smaller than required */
+    PKV_EWORKSPACE = 5,   /* workspace NULL or smaller than required */
+    PKV_ETOOBIG = 6       /* problem needs more than the built-in scratch of
+                             pkv_decode_attn_noalloc */
 } pkv_status;
 
 /* Device-side error bits OR-ed into *err_flag. */
@@ -181,6 +183,35 @@ PKV_API pkv_status pkv_decode_attn_ex(const pkv_cache_desc *desc, void *k_cache,
                                       int32_t num_q_heads, float softmax_scale, void *out,
                                       float *lse, void *workspace, size_t workspace_bytes,
                                       int32_t *err_flag, void *stream, uint32_t flags);
+
+/*
+ * pkv_decode_attn_noalloc -- pkv_decode_attn without a caller workspace.
+ * The paper has no counterpart: this is a convenience of this library.
+ *
+ * For callers that cannot allocate device memory at all, such as code running
+ * inside a host framework that owns every byte of device memory and forbids
+ * its plug-ins to allocate, or a real-time serving loop that must not touch
+ * the allocator after start-up.  It computes exactly what pkv_decode_attn
+ * computes (same arguments minus the workspace, same outputs, same errors)
+ * and allocates nothing: the split-KV scratch is a 16 MiB array compiled into
+ * the library, which every GPU that loads the library holds until the process
+ * exits.
+ *  - Limit: problems whose pkv_decode_workspace_size is at most 16 MiB (for
+ *    instance head_dim 128 with up to 4 query heads per kv head and up to
+ *    1024 rows); larger ones return PKV_ETOOBIG and launch nothing.
+ *  - The first call on each device looks up the array's device address (a
+ *    one-time set-up); make that first call before any stream capture.
+ *  - Every call on a device shares the one array and its contents persist
+ *    between calls; each call clears what must start at zero (on its own
+ *    stream) first.  Calls that can overlap on the GPU (different streams,
+ *    or different host threads) race on it: serialise them.
+ */
+PKV_API pkv_status pkv_decode_attn_noalloc(const pkv_cache_desc *desc, void *k_cache, void *v_cache,
+                                           const void *q, const void *k_new, const void *v_new,
+                                           const int32_t *block_table, int32_t max_blocks,
+                                           const int32_t *cache_seqlens, int32_t batch,
+                                           int32_t num_q_heads, float softmax_scale, void *out,
+                                           float *lse, int32_t *err_flag, void *stream);
 
 /* ---------------------------------------------------------------------
  * Host page-pool and block-table helpers (no device memory involved).

@@ -16,7 +16,7 @@ from ._lib import CacheDesc
 NHD = 0
 HND = 1
 
-OK, EINVAL, EUNSUPPORTED, ECUDA, ENOPAGES, EWORKSPACE = range(6)
+OK, EINVAL, EUNSUPPORTED, ECUDA, ENOPAGES, EWORKSPACE, ETOOBIG = range(7)
 DECODE_OVERLAP_PROLOGUE = 1  # pkv_decode_attn_ex flag (see include/pkv.h)
 ERR_PAGE, ERR_OVERFLOW, ERR_TIMEOUT = 1, 2, 4
 
@@ -120,6 +120,31 @@ def pkv_decode_attn(k_cache, v_cache, q, k_new, v_new, block_table, cache_seqlen
         _check(_lib.load().pkv_decode_attn_ex(*args, int(flags)), "pkv_decode_attn_ex")
     else:
         _check(_lib.load().pkv_decode_attn(*args), "pkv_decode_attn")
+    return out
+
+
+def pkv_decode_attn_noalloc(k_cache, v_cache, q, k_new, v_new, block_table, cache_seqlens, softmax_scale: float,
+                            out=None, lse=None, err_flag=None, layout: int = NHD) -> torch.Tensor:
+    """pkv_decode_attn for callers that cannot allocate device memory: no
+    workspace argument, the library's built-in scratch is used instead (see
+    include/pkv.h for its size limit and sharing rules).  Pass ``out`` to
+    avoid the allocation of a fresh output tensor here."""
+    for t, n in ((k_cache, "k_cache"), (v_cache, "v_cache"), (q, "q"), (k_new, "k_new"), (v_new, "v_new"),
+                 (out, "out")):
+        _bf16(t, n)
+    for t, n in ((block_table, "block_table"), (cache_seqlens, "cache_seqlens"), (err_flag, "err_flag")):
+        _i32(t, n)
+    if lse is not None and (lse.dtype != torch.float32 or not lse.is_contiguous()):
+        raise ValueError("lse: expected contiguous float32")
+    desc = cache_desc(k_cache, layout)
+    B, Hq, D = q.shape
+    if out is None:
+        out = torch.empty_like(q)
+    st = _lib.load().pkv_decode_attn_noalloc(
+        ctypes.byref(desc), _ptr(k_cache), _ptr(v_cache), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(block_table),
+        block_table.shape[1], _ptr(cache_seqlens), B, Hq, float(softmax_scale), _ptr(out), _ptr(lse), _ptr(err_flag),
+        _stream(q.device))
+    _check(st, "pkv_decode_attn_noalloc")
     return out
 
 

@@ -144,6 +144,8 @@ const char *pkv_status_str(pkv_status status)
         return "page pool exhausted";
     case PKV_EWORKSPACE:
         return "workspace missing or too small";
+    case PKV_ETOOBIG:
+        return "problem larger than the built-in scratch (use pkv_decode_attn with a workspace)";
     }
     return "unknown status";
 }

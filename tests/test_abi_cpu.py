@@ -35,7 +35,7 @@ def test_every_declared_symbol_is_exported_and_bound():
 
 def test_status_strings():
     lib = _lib.load()
-    for code in range(6):
+    for code in range(7):
         assert lib.pkv_status_str(code) not in (None, b"", b"unknown status")
     assert lib.pkv_status_str(99) == b"unknown status"
 
@@ -166,3 +166,17 @@ def test_append_argument_errors():
     assert app(k_new=ctypes.c_void_p(0x10004)) == pkv.api.EINVAL
     assert app(desc=CacheDesc(64, 16, 2, 100, 0)) == pkv.api.EUNSUPPORTED
     assert app(batch=0, ntok=0) == pkv.api.OK
+
+
+def test_noalloc_rejects_problems_beyond_its_scratch():
+    lib = _lib.load()
+    big = CacheDesc(64, 16, 8, 256, 0)  # head_dim 256, 8 query heads per kv head: > 16 MiB of scratch
+    assert pkv.pkv_decode_workspace_size(4, 4, 64, big) > (16 << 20)
+    st = lib.pkv_decode_attn_noalloc(ctypes.byref(big), FAKE, FAKE, FAKE, None, None, FAKE, 4, FAKE, 4, 64, 0.1,
+                                     FAKE, None, None, None)
+    assert st == pkv.api.ETOOBIG
+    small = CacheDesc(64, 16, 8, 128, 0)
+    assert pkv.pkv_decode_workspace_size(1024, 65, 32, small) <= (16 << 20)
+    st = lib.pkv_decode_attn_noalloc(ctypes.byref(small), FAKE, FAKE, FAKE, None, None, FAKE, 4, FAKE, 4, 6 * 8, 0.1,
+                                     FAKE, None, None, None)
+    assert st == pkv.api.EUNSUPPORTED  # argument errors are those of pkv_decode_attn
