@@ -276,12 +276,15 @@ pkv_status pkv_decode_attn_ex(const pkv_cache_desc *desc, void *k_cache, void *v
     a.flags = flags;
 
     const int box = decode_box_tokens(desc->page_size);
+    const int small = box > kDecodeSmallBox ? kDecodeSmallBox : box;
     const int swz = decode_swizzle(desc->page_size);
-    CUtensorMap tm_k, tm_v;
-    if (encode_pool_map(&tm_k, *desc, k_cache, box, 64, swz) != CUDA_SUCCESS ||
-        encode_pool_map(&tm_v, *desc, v_cache, box, 64, swz) != CUDA_SUCCESS)
+    DecodeMaps maps;
+    if (encode_pool_map(&maps.k, *desc, k_cache, box, 64, swz) != CUDA_SUCCESS ||
+        encode_pool_map(&maps.v, *desc, v_cache, box, 64, swz) != CUDA_SUCCESS ||
+        encode_pool_map(&maps.k8, *desc, k_cache, small, 64, swz) != CUDA_SUCCESS ||
+        encode_pool_map(&maps.v8, *desc, v_cache, small, 64, swz) != CUDA_SUCCESS)
         return PKV_ECUDA;
-    return launch_decode(a, tm_k, tm_v, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PKV_OK : PKV_ECUDA;
+    return launch_decode(a, maps, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PKV_OK : PKV_ECUDA;
 }
 
 } // extern "C"

@@ -49,7 +49,8 @@ constexpr int kEpilogueWarp = kWarps + 1;    // warps 3 and 4
 constexpr int kThreads = (kWarps + 3) * 32;
 constexpr int kTile = kDecodeTile; // tokens per pipeline tile
 constexpr int kMaxGrid = 2048;     // persistent CTAs at most (workspace sizing)
-constexpr int kMinSlice = 64;      // tokens per CTA slice at least
+constexpr int kSliceStartCost = 64; // work positions charged per unit for starting a slice
+constexpr int kMinSlice = 192;      // work positions per CTA at least (> kSliceStartCost + kTile)
 constexpr int kSlots = 2;          // consumer -> epilogue hand-off buffers
 constexpr float kNegInf = -INFINITY;
 
@@ -99,6 +100,7 @@ struct Smem {
     int32_t stage_bad[kStages];
     int32_t len[kMaxDecodeBatch];
     int32_t rowtok[kMaxDecodeBatch + 1]; // prefix of cache tokens per row
+    long long rowbase[kMaxDecodeBatch + 1]; // first work position of every row
     long long work;                      // units * rowtok[batch]
     long long slice;                     // work positions per CTA
     int32_t geff;                        // CTAs that own a token slice
@@ -150,9 +152,13 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, vo
 }
 
 // ------------------------------------------------------------------ plan
-// Every CTA derives the same plan from cache_seqlens: the cache tokens of
-// every row (0 for inactive / overflowing rows), their prefix sum, the total
-// work (units per row * total tokens) and the slice length per CTA.
+// Every CTA derives the same plan from cache_seqlens.  Work is laid out as a
+// line: every (row, kv head, head group) unit with n > 0 cached tokens takes
+// kSliceStartCost virtual positions followed by its n token positions, units
+// in row-major order.  CTA k takes positions [k * slice, (k+1) * slice),
+// moved to token positions (see boundary), so the per-unit cost of starting
+// a slice (page ids, queries, a hand-off to the epilogue) is balanced along
+// with the tokens.
 template <int D, int GC>
 __device__ void build_plan(const KParams &p, Smem<D, GC> &sm)
 {
@@ -161,7 +167,7 @@ __device__ void build_plan(const KParams &p, Smem<D, GC> &sm)
     __syncthreads();
     if (threadIdx.x < 32) {
         const int lane = threadIdx.x;
-        int run = 0, empty = 0;
+        int run = 0, nonempty = 0;
         for (int base = 0; base < p.batch; base += 32) {
             const int i = base + lane;
             int n = 0;
@@ -169,20 +175,25 @@ __device__ void build_plan(const KParams &p, Smem<D, GC> &sm)
                 const int L = sm.len[i];
                 n = row_status(p, L) == ROW_OK ? L : 0;
             }
-            empty += __popc(__ballot_sync(0xffffffffu, i < p.batch && n == 0));
+            const unsigned ne = __ballot_sync(0xffffffffu, n > 0);
+            const int ne_before = nonempty + __popc(ne & ((1u << lane) - 1u));
+            nonempty += __popc(ne);
             int incl = n;
             for (int o = 1; o < 32; o <<= 1) {
                 const int v = __shfl_up_sync(0xffffffffu, incl, o);
                 if (lane >= o)
                     incl += v;
             }
-            if (i < p.batch)
+            if (i < p.batch) {
                 sm.rowtok[i] = run + incl - n;
+                sm.rowbase[i] = (long long)p.units * ((long long)(run + incl - n) + (long long)kSliceStartCost * ne_before);
+            }
             run += __shfl_sync(0xffffffffu, incl, 31);
         }
         if (lane == 0) {
             sm.rowtok[p.batch] = run;
-            const long long work = (long long)run * p.units;
+            sm.rowbase[p.batch] = (long long)p.units * ((long long)run + (long long)kSliceStartCost * nonempty);
+            const long long work = (long long)p.units * ((long long)run + (long long)kSliceStartCost * nonempty);
             long long g = work / kMinSlice;
             if (g > gridDim.x)
                 g = gridDim.x;
@@ -191,16 +202,17 @@ __device__ void build_plan(const KParams &p, Smem<D, GC> &sm)
             const long long slice = work > 0 ? (work + g - 1) / g : 1;
             sm.work = work;
             sm.slice = slice;
-            sm.n_empty = empty;
+            sm.n_empty = p.batch - nonempty;
             sm.geff = work > 0 ? (int)((work + slice - 1) / slice) : 1;
         }
     }
     __syncthreads();
 }
 
-// Unit containing global work position x (x < work): row b, unit r in the
-// row, offset rel inside the unit; returns the unit's first position.
-// units * row tokens < 2^31 (checked on the host), so in-row math is 32-bit.
+// Unit containing work position x (x < work): row b, unit r in the row and
+// the offset rel inside the unit's kSliceStartCost + n positions; returns the
+// unit's first token position.  units * (row tokens + cost) < 2^31 (checked
+// on the host), so in-row math is 32-bit.
 template <int D, int GC>
 __device__ __forceinline__ long long locate(const KParams &p, const Smem<D, GC> &sm, long long x, int &b, int &r,
                                             int &rel)
@@ -208,22 +220,23 @@ __device__ __forceinline__ long long locate(const KParams &p, const Smem<D, GC> 
     int lo = 0, hi = p.batch - 1; // largest row starting at or before x (never an empty row)
     while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
-        if ((long long)sm.rowtok[mid] * p.units <= x)
+        if (sm.rowbase[mid] <= x)
             lo = mid;
         else
             hi = mid - 1;
     }
     b = lo;
-    const long long base = (long long)sm.rowtok[lo] * p.units;
-    const int n = sm.rowtok[lo + 1] - sm.rowtok[lo];
+    const long long base = sm.rowbase[lo];
+    const int w = sm.rowtok[lo + 1] - sm.rowtok[lo] + kSliceStartCost;
     const int d = (int)(x - base);
-    r = d / n;
-    rel = d - r * n;
-    return base + (long long)r * n;
+    r = d / w;
+    rel = d - r * w;
+    return base + (long long)r * w + kSliceStartCost;
 }
 
-// First work position of CTA k's slice (k in [0, geff]): k * slice, rounded
-// down to a multiple of the tile inside its unit.
+// First position of CTA k's range (k in [0, geff]): k * slice moved to a
+// token position -- the unit's first token if it falls on the unit's virtual
+// positions, else rounded down to a multiple of the tile inside the unit.
 template <int D, int GC>
 __device__ __forceinline__ long long boundary(const KParams &p, const Smem<D, GC> &sm, int k)
 {
@@ -231,12 +244,13 @@ __device__ __forceinline__ long long boundary(const KParams &p, const Smem<D, GC
     if (x >= sm.work)
         return sm.work;
     int b, r, rel;
-    const long long u0 = locate(p, sm, x, b, r, rel);
-    return u0 + (rel & ~(kTile - 1));
+    const long long t0 = locate(p, sm, x, b, r, rel);
+    const int t = rel - kSliceStartCost;
+    return t0 + (t < 0 ? 0 : (t & ~(kTile - 1)));
 }
 
-// CTA whose slice holds work position x (x < work).  boundary(k) lies in
-// (k * slice - kTile, k * slice], so it is floor(x / slice) or the next one.
+// CTA whose range holds token position x (x < work): close to x / slice, the
+// boundaries being at most kTile below or kSliceStartCost above k * slice.
 template <int D, int GC>
 __device__ __forceinline__ int owner_of(const KParams &p, const Smem<D, GC> &sm, long long x)
 {
@@ -252,7 +266,7 @@ __device__ __forceinline__ int owner_of(const KParams &p, const Smem<D, GC> &sm,
 
 struct Seg {
     int b, r, kvh, sub, unit, L, status, tok0, tok1;
-    long long u0; // unit's first work position
+    long long u0; // unit's first token position
     int n;        // unit's cache tokens
 };
 
@@ -262,8 +276,8 @@ struct Seg {
 // them, so the partial-merging work of shared units is not left for the end.
 struct SegIter {
     long long pos0, end, f_end, mid_pos, mid_end;
-    long long u0_f, u0_l;
-    int b_f, r_f, rel_f, b_l, r_l;
+    long long t0_f, t0_l;
+    int b_f, r_f, b_l, r_l;
     int stage; // 0: first slice, 1: last slice, 2: middle units, 3: done
     template <int D, int GC>
     __device__ __forceinline__ void init(const KParams &p, const Smem<D, GC> &sm, int k)
@@ -274,26 +288,26 @@ struct SegIter {
         const long long x = (long long)k * sm.slice;
         if (x >= sm.work)
             return;
-        u0_f = locate(p, sm, x, b_f, r_f, rel_f);
-        rel_f &= ~(kTile - 1);
-        pos0 = u0_f + rel_f;
+        int rel;
+        t0_f = locate(p, sm, x, b_f, r_f, rel); // the unit of this range's first token
+        const int t = rel - kSliceStartCost;
+        pos0 = t0_f + (t < 0 ? 0 : (t & ~(kTile - 1)));
         end = boundary(p, sm, k + 1);
         if (pos0 >= end)
             return;
-        f_end = min(end, u0_f + (sm.rowtok[b_f + 1] - sm.rowtok[b_f]));
-        mid_pos = mid_end = f_end;
+        f_end = min(end, t0_f + (sm.rowtok[b_f + 1] - sm.rowtok[b_f]));
         stage = 0;
     }
     template <int D, int GC>
-    __device__ __forceinline__ void fill(const KParams &p, const Smem<D, GC> &sm, Seg &s, int b, int r, long long u0,
+    __device__ __forceinline__ void fill(const KParams &p, const Smem<D, GC> &sm, Seg &s, int b, int r, long long t0,
                                          long long from, long long to)
     {
         s.b = b;
         s.r = r;
-        s.u0 = u0;
+        s.u0 = t0;
         s.n = sm.rowtok[b + 1] - sm.rowtok[b];
-        s.tok0 = (int)(from - u0);
-        s.tok1 = (int)(to - u0);
+        s.tok0 = (int)(from - t0);
+        s.tok1 = (int)(to - t0);
         s.kvh = r / p.n_sub;
         s.sub = r - s.kvh * p.n_sub;
         s.unit = b * p.units + r;
@@ -304,25 +318,36 @@ struct SegIter {
     __device__ __forceinline__ bool next(const KParams &p, const Smem<D, GC> &sm, Seg &s)
     {
         if (stage == 0) {
-            fill(p, sm, s, b_f, r_f, u0_f, pos0, f_end);
-            stage = f_end < end ? 1 : 3;
+            fill(p, sm, s, b_f, r_f, t0_f, pos0, f_end);
+            stage = 3;
+            if (f_end < end) {
+                int rel;
+                t0_l = locate(p, sm, end - 1, b_l, r_l, rel);
+                mid_pos = f_end; // virtual start of the next unit
+                if (end > t0_l) { // the range ends inside a unit's tokens
+                    mid_end = t0_l - kSliceStartCost;
+                    stage = 1;
+                } else {
+                    mid_end = end;
+                    stage = 2;
+                }
+            }
             return true;
         }
         if (stage == 1) {
-            int rel_l;
-            u0_l = locate(p, sm, end - 1, b_l, r_l, rel_l);
-            mid_end = u0_l;
-            fill(p, sm, s, b_l, r_l, u0_l, u0_l, end);
+            fill(p, sm, s, b_l, r_l, t0_l, t0_l, end);
             stage = 2;
             return true;
         }
         if (stage == 2 && mid_pos < mid_end) {
             int b, r, rel;
-            const long long u0 = locate(p, sm, mid_pos, b, r, rel); // rel == 0: a whole unit
-            const long long e = u0 + (sm.rowtok[b + 1] - sm.rowtok[b]);
-            fill(p, sm, s, b, r, u0, u0, e);
-            mid_pos = e;
-            return true;
+            const long long t0 = locate(p, sm, mid_pos, b, r, rel); // rel == 0: a unit's virtual start
+            if (t0 < mid_end) {
+                const long long e = t0 + (sm.rowtok[b + 1] - sm.rowtok[b]);
+                fill(p, sm, s, b, r, t0, t0, e);
+                mid_pos = e;
+                return true;
+            }
         }
         stage = 3;
         return false;
@@ -337,13 +362,14 @@ __device__ __forceinline__ int load_window(const int32_t *bt_row, int first, int
 }
 
 template <int D, int GC>
-__device__ void producer(const KParams &p, Smem<D, GC> &sm, const CUtensorMap *tm_k, const CUtensorMap *tm_v)
+__device__ void producer(const KParams &p, Smem<D, GC> &sm, const DecodeMaps *maps)
 {
     constexpr int S = Smem<D, GC>::kStages;
     const int lane = threadIdx.x & 31;
     const uint64_t policy = l2_evict_first_policy();
     const int box = p.box_tokens;
-    const uint32_t box_bytes = (uint32_t)box * D * 2u;
+    // a partly used box is fetched in 8-row pieces (rows past the slice are not read)
+    const bool split_tail = box > kDecodeSmallBox;
     uint32_t g_tile = 0;
     volatile int32_t *abort = &sm.abort;
     SegIter si;
@@ -371,6 +397,8 @@ __device__ void producer(const KParams &p, Smem<D, GC> &sm, const CUtensorMap *t
             const int tile0 = sg.tok0 + t * kTile;
             const int nv = min(kTile, sg.tok1 - tile0);
             const int nbox = (nv + box - 1) / box;
+            const int nfull = split_tail ? nv / box : nbox;
+            const int tail_rows = split_tail ? ((nv - nfull * box + kDecodeSmallBox - 1) & ~(kDecodeSmallBox - 1)) : 0;
             if ((tile0 >> p.page_shift) >= wbase + 32) { // tiles never straddle a window
                 wbase += 32;
                 win = nxt;
@@ -382,8 +410,11 @@ __device__ void producer(const KParams &p, Smem<D, GC> &sm, const CUtensorMap *t
             const unsigned okmask = __ballot_sync(0xffffffffu, ok);
             const int bad = __popc(okmask) != nbox;
             if (lane == 0) {
+                const unsigned fullmask = nfull >= 32 ? 0xffffffffu : ((1u << nfull) - 1u);
+                const uint32_t rows = (uint32_t)box * __popc(okmask & fullmask) +
+                                      (nfull < nbox && ((okmask >> nfull) & 1u) ? (uint32_t)tail_rows : 0u);
                 sm.stage_bad[s] = bad;
-                mbar_arrive_expect_tx(&sm.full[s], 2u * box_bytes * (uint32_t)__popc(okmask));
+                mbar_arrive_expect_tx(&sm.full[s], 2u * rows * D * 2u);
             }
             __syncwarp();
             for (int bx = 0; bx < nbox; ++bx) {
@@ -399,11 +430,24 @@ __device__ void producer(const KParams &p, Smem<D, GC> &sm, const CUtensorMap *t
                         z = page * p.num_kv_heads + sg.kvh;
                     }
                     // one 64-column box per 128-byte half row: [D/64][kTile][64]
+                    if (bx < nfull) {
 #pragma unroll
-                    for (int h = 0; h < D / 64; ++h) {
-                        const int off = (h * kTile + bx * box) * 64;
-                        tma_load_3d(sm.kv[s][0] + off, tm_k, 64 * h, y, z, &sm.full[s], policy);
-                        tma_load_3d(sm.kv[s][1] + off, tm_v, 64 * h, y, z, &sm.full[s], policy);
+                        for (int h = 0; h < D / 64; ++h) {
+                            const int off = (h * kTile + bx * box) * 64;
+                            tma_load_3d(sm.kv[s][0] + off, &maps->k, 64 * h, y, z, &sm.full[s], policy);
+                            tma_load_3d(sm.kv[s][1] + off, &maps->v, 64 * h, y, z, &sm.full[s], policy);
+                        }
+                    } else { // the slice ends inside this box
+                        for (int r = 0; r < tail_rows; r += kDecodeSmallBox) {
+                            const int yr = p.layout == PKV_NHD ? y : y + r;
+                            const int zr = p.layout == PKV_NHD ? z + r : z;
+#pragma unroll
+                            for (int h = 0; h < D / 64; ++h) {
+                                const int off = (h * kTile + bx * box + r) * 64;
+                                tma_load_3d(sm.kv[s][0] + off, &maps->k8, 64 * h, yr, zr, &sm.full[s], policy);
+                                tma_load_3d(sm.kv[s][1] + off, &maps->v8, 64 * h, yr, zr, &sm.full[s], policy);
+                            }
+                        }
                     }
                 }
             }
@@ -1048,8 +1092,7 @@ __device__ void epilogue(const KParams &p, Smem<D, GC> &sm, int ew)
 
 template <int D, int GC>
 __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant__ KParams p,
-                                                          const __grid_constant__ CUtensorMap tm_k,
-                                                          const __grid_constant__ CUtensorMap tm_v)
+                                                          const __grid_constant__ DecodeMaps maps)
 {
     extern __shared__ unsigned char smem_raw[];
     Smem<D, GC> &sm = *reinterpret_cast<Smem<D, GC> *>(
@@ -1071,14 +1114,16 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
         mbar_init_fence();
     }
     if (threadIdx.x == kProducerWarp * 32) {
-        prefetch_tensormap(&tm_k);
-        prefetch_tensormap(&tm_v);
+        prefetch_tensormap(&maps.k);
+        prefetch_tensormap(&maps.v);
+        prefetch_tensormap(&maps.k8);
+        prefetch_tensormap(&maps.v8);
     }
     build_plan(p, sm); // ends with __syncthreads()
     if (warp < kWarps)
         consumers(p, sm);
     else if (warp == kProducerWarp)
-        producer(p, sm, &tm_k, &tm_v);
+        producer(p, sm, &maps);
     else
         epilogue(p, sm, warp - kEpilogueWarp);
 }
@@ -1148,11 +1193,13 @@ bool decode_shape(int batch, int max_blocks, int num_q_heads, const pkv_cache_de
     s->heads_per_cta = heads_per_cta(s->group);
     if (find_kernel(d.head_dim, s->heads_per_cta) == nullptr)
         return false;
-    // the plan counts tokens in int32
-    if ((int64_t)batch * max_blocks * d.page_size >= ((int64_t)1 << 31))
-        return false;
     s->n_sub = s->group / s->heads_per_cta;
     s->units_per_row = d.num_kv_heads * s->n_sub;
+    // the plan counts tokens of all rows, and work positions inside a row, in int32
+    const int64_t row_tokens = (int64_t)max_blocks * d.page_size;
+    if ((int64_t)batch * row_tokens >= ((int64_t)1 << 31) ||
+        (int64_t)s->units_per_row * (row_tokens + kSliceStartCost) >= ((int64_t)1 << 31))
+        return false;
     s->chunk_max = 0;
     s->cap_items = 2 * (int64_t)kMaxGrid; // two partial slots per persistent CTA
     const int64_t units = (int64_t)batch * s->units_per_row;
@@ -1187,8 +1234,7 @@ int decode_target_items(int device, int head_dim, int heads_per_cta)
     return slot;
 }
 
-cudaError_t launch_decode(const DecodeArgs &a, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
-                          cudaStream_t stream)
+cudaError_t launch_decode(const DecodeArgs &a, const DecodeMaps &maps, cudaStream_t stream)
 {
     const KernelEntry *e = find_kernel(a.desc.head_dim, a.shape.heads_per_cta);
     if (e == nullptr)
@@ -1224,7 +1270,7 @@ cudaError_t launch_decode(const DecodeArgs &a, const CUtensorMap &tm_k, const CU
     p.swizzle = decode_swizzle(a.desc.page_size);
     p.pdl = (a.flags & PKV_DECODE_OVERLAP_PROLOGUE) ? 1 : 0;
     p.q_scale = a.q_scale;
-    void *args[] = {&p, const_cast<CUtensorMap *>(&tm_k), const_cast<CUtensorMap *>(&tm_v)};
+    void *args[] = {&p, const_cast<DecodeMaps *>(&maps)};
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(a.grid);
     cfg.blockDim = dim3(kThreads);

@@ -64,8 +64,15 @@ struct DecodeArgs {
     uint32_t flags; // PKV_DECODE_*
 };
 
-cudaError_t launch_decode(const DecodeArgs &a, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
-                          cudaStream_t stream);
+// TMA descriptors of one decode call: K and V pools with full boxes
+// (decode_box_tokens rows) and with 8-row boxes for the ragged end of a slice.
+struct DecodeMaps {
+    CUtensorMap k, v, k8, v8;
+};
+
+constexpr int kDecodeSmallBox = 8;
+
+cudaError_t launch_decode(const DecodeArgs &a, const DecodeMaps &maps, cudaStream_t stream);
 
 struct AppendArgs {
     pkv_cache_desc desc;
