@@ -78,6 +78,8 @@ typedef enum {
 #define PKV_ERR_OVERFLOW 2 /* a row's tokens exceed max_blocks * page_size */
 #define PKV_ERR_TIMEOUT 4  /* an on-chip pipeline wait ran out of time: the call's outputs are
                               unspecified and its workspace must be zero-filled again */
+#define PKV_ERR_QLEN 8     /* prefill: a request with more queries than keys, a query range
+                              outside [0, total_q), or a decreasing qo_indptr */
 
 /* Geometry of one K or V page pool (both share it).  page_size is a power of
  * two in [1, 256]; head_dim is 64, 128 or 256; num_pages >= 2 (page 0 is the
@@ -212,6 +214,54 @@ PKV_API pkv_status pkv_decode_attn_noalloc(const pkv_cache_desc *desc, void *k_c
                                            const int32_t *cache_seqlens, int32_t batch,
                                            int32_t num_q_heads, float softmax_scale, void *out,
                                            float *lse, int32_t *err_flag, void *stream);
+
+/*
+ * pkv_prefill_workspace_size -- bytes of device workspace pkv_prefill_attn
+ * needs (0 on invalid or unsupported arguments).  The workspace holds the
+ * call's work plan; it needs no initialisation and is fully rewritten by every
+ * call.  Calls that share a workspace must not run concurrently.
+ */
+PKV_API size_t pkv_prefill_workspace_size(int32_t batch, int32_t total_q, int32_t num_q_heads,
+                                          const pkv_cache_desc *desc);
+
+/*
+ * pkv_prefill_attn -- ragged end-aligned causal prefill attention straight
+ * over the paged cache (no append: fill the cache first, e.g. with
+ * pkv_append and an append_indptr).
+ * Source: "[flashinfer] H100 D256 paged attention cuDNN auto-dispatch", code
+ * analysis part 1 (ragged batch over HND pages; request b with q_b queries
+ * over kv_b keys, q_b <= kv_b; its query i sees keys 0 .. kv_b - q_b + i).
+ *
+ *  k_cache, v_cache  device bf16 pools described by `desc` (read only);
+ *                    page_size must be at least 8.
+ *  q                 device bf16 [total_q, num_q_heads, head_dim]; request
+ *                    b owns rows qo_indptr[b] .. qo_indptr[b+1]-1.
+ *  qo_indptr         device int32 [batch + 1], non-decreasing, with
+ *                    qo_indptr[b+1] <= total_q.
+ *  kv_lens           device int32 [batch]: keys of request b (its cache
+ *                    length, the queries' own tokens included).
+ *  block_table       device int32 [batch, max_blocks].
+ *  num_q_heads       a power-of-two multiple (at most 128) of num_kv_heads.
+ *  softmax_scale     scale applied to q.k (finite).
+ *  out               device bf16 [total_q, num_q_heads, head_dim] (round to
+ *                    nearest even from fp32); rows no request owns are not
+ *                    written.
+ *  lse               device fp32 [total_q, num_q_heads], natural log, or NULL.
+ *  workspace         device buffer of pkv_prefill_workspace_size bytes.
+ *  batch             0 .. 1024.
+ * A request with q_b = 0 does nothing.  A request whose query range or
+ * length is malformed (PKV_ERR_QLEN), whose keys exceed max_blocks *
+ * page_size (PKV_ERR_OVERFLOW) or whose block_table holds a page outside
+ * [1, num_pages) among its first ceil(kv_b / page_size) entries
+ * (PKV_ERR_PAGE) gets out = 0 and lse = -inf on its query rows (those inside
+ * [0, total_q)) and sets the bit in *err_flag.
+ */
+PKV_API pkv_status pkv_prefill_attn(const pkv_cache_desc *desc, const void *k_cache, const void *v_cache,
+                                    const void *q, const int32_t *qo_indptr, const int32_t *kv_lens,
+                                    const int32_t *block_table, int32_t max_blocks, int32_t batch,
+                                    int32_t num_q_heads, int32_t total_q, float softmax_scale, void *out,
+                                    float *lse, void *workspace, size_t workspace_bytes, int32_t *err_flag,
+                                    void *stream);
 
 /* ---------------------------------------------------------------------
  * Host page-pool and block-table helpers (no device memory involved).

@@ -16,5 +16,8 @@ from .api import (  # noqa: F401
     pkv_decode_attn,
     pkv_decode_workspace_size,
     pkv_pool_bytes,
+    pkv_prefill_attn,
+    pkv_prefill_workspace_size,
+    prefill_workspace,
     pkv_validate_host,
 )

@@ -18,7 +18,7 @@ HND = 1
 
 OK, EINVAL, EUNSUPPORTED, ECUDA, ENOPAGES, EWORKSPACE, ETOOBIG = range(7)
 DECODE_OVERLAP_PROLOGUE = 1  # pkv_decode_attn_ex flag (see include/pkv.h)
-ERR_PAGE, ERR_OVERFLOW, ERR_TIMEOUT = 1, 2, 4
+ERR_PAGE, ERR_OVERFLOW, ERR_TIMEOUT, ERR_QLEN = 1, 2, 4, 8
 
 
 class PkvError(RuntimeError):
@@ -145,6 +145,45 @@ def pkv_decode_attn_noalloc(k_cache, v_cache, q, k_new, v_new, block_table, cach
         block_table.shape[1], _ptr(cache_seqlens), B, Hq, float(softmax_scale), _ptr(out), _ptr(lse), _ptr(err_flag),
         _stream(q.device))
     _check(st, "pkv_decode_attn_noalloc")
+    return out
+
+
+def pkv_prefill_workspace_size(batch: int, total_q: int, num_q_heads: int, desc: CacheDesc) -> int:
+    return int(_lib.load().pkv_prefill_workspace_size(batch, total_q, num_q_heads, ctypes.byref(desc)))
+
+
+def prefill_workspace(batch: int, total_q: int, num_q_heads: int, desc: CacheDesc, device) -> torch.Tensor:
+    """A workspace for pkv_prefill_attn (needs no initialisation)."""
+    n = pkv_prefill_workspace_size(batch, total_q, num_q_heads, desc)
+    if n == 0:
+        raise PkvError(EUNSUPPORTED, "pkv_prefill_workspace_size")
+    return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def pkv_prefill_attn(k_cache, v_cache, q, qo_indptr, kv_lens, block_table, softmax_scale: float, out=None,
+                     lse=None, workspace=None, err_flag=None, layout: int = NHD) -> torch.Tensor:
+    """Ragged end-aligned causal prefill over the paged cache; ``q`` is
+    ``[total_q, Hq, D]``, request b owns rows ``qo_indptr[b]:qo_indptr[b+1]``
+    and sees ``kv_lens[b]`` keys.  Returns ``out`` ``[total_q, Hq, D]`` bf16."""
+    for t, n in ((k_cache, "k_cache"), (v_cache, "v_cache"), (q, "q"), (out, "out")):
+        _bf16(t, n)
+    for t, n in ((qo_indptr, "qo_indptr"), (kv_lens, "kv_lens"), (block_table, "block_table"),
+                 (err_flag, "err_flag")):
+        _i32(t, n)
+    if lse is not None and (lse.dtype != torch.float32 or not lse.is_contiguous()):
+        raise ValueError("lse: expected contiguous float32")
+    desc = cache_desc(k_cache, layout)
+    total_q, Hq, D = q.shape
+    B = kv_lens.shape[0]
+    if out is None:
+        out = torch.empty_like(q)
+    if workspace is None:
+        workspace = prefill_workspace(B, total_q, Hq, desc, q.device)
+    st = _lib.load().pkv_prefill_attn(
+        ctypes.byref(desc), _ptr(k_cache), _ptr(v_cache), _ptr(q), _ptr(qo_indptr), _ptr(kv_lens),
+        _ptr(block_table), block_table.shape[1], B, Hq, total_q, float(softmax_scale), _ptr(out), _ptr(lse),
+        _ptr(workspace), workspace.numel(), _ptr(err_flag), _stream(q.device))
+    _check(st, "pkv_prefill_attn")
     return out
 
 

@@ -123,6 +123,24 @@ CUresult encode_pool_map(CUtensorMap *map, const pkv_cache_desc &d, void *base, 
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 
+
+// Tensor map over q [total_q, Hq, D] whose boxes are q_tile consecutive
+// queries x `group` consecutive heads x 64 columns, 128-byte swizzled
+// ([q_tile][group][64] in shared memory: row = query * group + head).
+CUresult encode_q_map(CUtensorMap *map, const void *q, int total_q, int num_q_heads, int head_dim, int group,
+                      int q_tile)
+{
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (enc == nullptr)
+        return CUDA_ERROR_NOT_FOUND;
+    const cuuint64_t dims[3] = {(cuuint64_t)head_dim, (cuuint64_t)num_q_heads, (cuuint64_t)total_q};
+    const cuuint64_t strides[2] = {(cuuint64_t)head_dim * 2, (cuuint64_t)head_dim * 2 * num_q_heads};
+    const cuuint32_t box[3] = {64, (cuuint32_t)group, (cuuint32_t)q_tile};
+    const cuuint32_t elem_strides[3] = {1, 1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(q), dims, strides, box, elem_strides,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
 } // namespace pkv
 
 using namespace pkv;
@@ -285,6 +303,68 @@ pkv_status pkv_decode_attn_ex(const pkv_cache_desc *desc, void *k_cache, void *v
         encode_pool_map(&maps.v8, *desc, v_cache, small, 64, swz) != CUDA_SUCCESS)
         return PKV_ECUDA;
     return launch_decode(a, maps, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PKV_OK : PKV_ECUDA;
+}
+
+size_t pkv_prefill_workspace_size(int32_t batch, int32_t total_q, int32_t num_q_heads, const pkv_cache_desc *desc)
+{
+    if (check_desc(desc) != PKV_OK || batch < 0 || batch > kMaxPrefillBatch || total_q < 0 || num_q_heads < 1)
+        return 0;
+    PrefillShape s;
+    if (!prefill_shape(batch, total_q, num_q_heads, *desc, &s))
+        return 0;
+    return s.bytes;
+}
+
+pkv_status pkv_prefill_attn(const pkv_cache_desc *desc, const void *k_cache, const void *v_cache, const void *q,
+                            const int32_t *qo_indptr, const int32_t *kv_lens, const int32_t *block_table,
+                            int32_t max_blocks, int32_t batch, int32_t num_q_heads, int32_t total_q,
+                            float softmax_scale, void *out, float *lse, void *workspace, size_t workspace_bytes,
+                            int32_t *err_flag, void *stream)
+{
+    const pkv_status st = check_desc(desc);
+    if (st != PKV_OK)
+        return st;
+    if (batch < 0 || total_q < 0 || max_blocks < 1 || num_q_heads < 1 || !isfinite(softmax_scale))
+        return PKV_EINVAL;
+    if (num_q_heads % desc->num_kv_heads != 0)
+        return PKV_EINVAL;
+    if (batch > kMaxPrefillBatch)
+        return PKV_EUNSUPPORTED;
+    PrefillShape shape;
+    if (!prefill_shape(batch, total_q, num_q_heads, *desc, &shape))
+        return PKV_EUNSUPPORTED;
+    if (batch == 0 || total_q == 0)
+        return PKV_OK;
+    if (k_cache == nullptr || v_cache == nullptr || q == nullptr || out == nullptr || qo_indptr == nullptr ||
+        kv_lens == nullptr || block_table == nullptr)
+        return PKV_EINVAL;
+    if (!aligned16(k_cache) || !aligned16(v_cache) || !aligned16(q) || !aligned16(out))
+        return PKV_EINVAL;
+    if (workspace == nullptr || workspace_bytes < shape.bytes || !aligned16(workspace))
+        return PKV_EWORKSPACE;
+
+    PrefillArgs a;
+    a.desc = *desc;
+    a.batch = batch;
+    a.num_q_heads = num_q_heads;
+    a.total_q = total_q;
+    a.max_blocks = max_blocks;
+    a.q_scale = softmax_scale * 1.4426950408889634f;
+    a.qo_indptr = qo_indptr;
+    a.kv_lens = kv_lens;
+    a.block_table = block_table;
+    a.out = out;
+    a.lse = lse;
+    a.workspace = workspace;
+    a.err_flag = err_flag;
+    a.shape = shape;
+    const int box = prefill_box_tokens(desc->page_size);
+    PrefillMaps maps;
+    if (encode_q_map(&maps.q, q, total_q, num_q_heads, desc->head_dim, shape.group, shape.q_tile) != CUDA_SUCCESS ||
+        encode_pool_map(&maps.k, *desc, const_cast<void *>(k_cache), box, 64, 1) != CUDA_SUCCESS ||
+        encode_pool_map(&maps.v, *desc, const_cast<void *>(v_cache), box, 64, 1) != CUDA_SUCCESS)
+        return PKV_ECUDA;
+    return launch_prefill(a, maps, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PKV_OK : PKV_ECUDA;
 }
 
 } // extern "C"

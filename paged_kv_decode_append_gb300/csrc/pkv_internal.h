@@ -104,4 +104,46 @@ CUresult encode_pool_map(CUtensorMap *map, const pkv_cache_desc &d, void *base, 
 
 int sm_count(int device);
 
+// ---------------------------------------------------------------- prefill
+
+// Largest batch one prefill call plans for (the plan lives in shared memory).
+constexpr int kMaxPrefillBatch = 1024;
+
+// Static shape of a prefill call: the query tile and the workspace size.
+struct PrefillShape {
+    int group;       // num_q_heads / num_kv_heads (a power of two <= 128)
+    int group_shift; // log2(group)
+    int q_tile;      // queries per work unit: 128 / group
+    int64_t cap_pairs; // upper bound on (request, query tile) pairs
+    size_t bytes;    // workspace bytes
+};
+
+// Fills `s`; returns false for unsupported combinations.
+bool prefill_shape(int batch, int total_q, int num_q_heads, const pkv_cache_desc &d, PrefillShape *s);
+
+struct PrefillArgs {
+    pkv_cache_desc desc;
+    int batch, num_q_heads, total_q, max_blocks;
+    float q_scale; // softmax_scale * log2(e)
+    const int32_t *qo_indptr;
+    const int32_t *kv_lens;
+    const int32_t *block_table;
+    void *out;
+    float *lse;
+    void *workspace;
+    int32_t *err_flag;
+    PrefillShape shape;
+};
+
+// TMA descriptors of one prefill call: q tiles ([128/G queries][G heads][64]
+// boxes) and 64-column boxes of min(page_size, 64) tokens of the K and V pools.
+struct PrefillMaps {
+    CUtensorMap q, k, v;
+};
+
+cudaError_t launch_prefill(const PrefillArgs &a, const PrefillMaps &maps, cudaStream_t stream);
+
+int prefill_box_tokens(int page_size);
+
+
 } // namespace pkv

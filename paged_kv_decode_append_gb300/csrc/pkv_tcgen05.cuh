@@ -1,0 +1,157 @@
+// pkv_tcgen05.cuh -- sm_103a 5th-generation tensor-core helpers: tensor
+// memory (TMEM) allocation, tcgen05.mma issue and completion, TMEM <-> register
+// moves, and the shared-memory matrix / instruction descriptors the MMA reads.
+//
+// Conventions used by every caller in this library:
+//  - one CTA (cta_group::1); the MMA is issued by one thread;
+//  - operands are bf16, staged in shared memory in the 128-byte-swizzled
+//    layout a TMA load with CU_TENSOR_MAP_SWIZZLE_128B writes: rows of 128
+//    bytes (64 bf16), 8-row atoms of 1024 bytes aligned to 1024;
+//  - accumulators are fp32 in TMEM: row i of an M = 128 tile lives in TMEM
+//    lane i, column n in TMEM column (base + n).
+#pragma once
+
+#include "pkv_device.cuh"
+
+namespace pkv {
+
+// --- tensor memory -------------------------------------------------------
+
+// Allocates `ncols` TMEM columns (a power of two >= 32) for this CTA and writes
+// their base address to shared memory.  Executed by one whole warp.
+__device__ __forceinline__ void tmem_alloc(uint32_t *dst_smem, uint32_t ncols)
+{
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(dst_smem)),
+                 "r"(ncols)
+                 : "memory");
+}
+
+// Declares that this CTA allocates no more TMEM (lets other CTAs' allocations
+// proceed).  One whole warp.
+__device__ __forceinline__ void tmem_relinquish()
+{
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+// Frees what tmem_alloc took.  One whole warp, the same one that allocated.
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols)
+{
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+// Orders this thread's earlier tcgen05 operations before a following
+// thread synchronisation (mbarrier arrive, bar.sync).
+__device__ __forceinline__ void tc_fence_before()
+{
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+
+// Orders later tcgen05 operations after a preceding thread synchronisation.
+__device__ __forceinline__ void tc_fence_after()
+{
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// --- MMA -----------------------------------------------------------------
+
+// Instruction descriptor of kind::f16 with bf16 A and B and an fp32
+// accumulator: bits 4-5 D format (1 = f32), 7-9 A format (1 = bf16), 10-12 B
+// format (1 = bf16), 15 / 16 A / B major-ness (0 = K-major, 1 = MN-major),
+// 17-22 N >> 3, 24-28 M >> 4.
+__host__ __device__ constexpr uint32_t tc_idesc_bf16(int M, int N, bool a_mn_major, bool b_mn_major)
+{
+    return (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(a_mn_major) << 15) | (uint32_t(b_mn_major) << 16) |
+           (uint32_t(N >> 3) << 17) | (uint32_t(M >> 4) << 24);
+}
+
+// Shared-memory matrix descriptor for a 128-byte-swizzled operand: bits 0-13
+// start address >> 4, 16-29 leading-dimension byte offset >> 4, 32-45
+// stride-dimension byte offset >> 4, 46-47 descriptor version (1), 61-63
+// layout (2 = 128-byte swizzle).  For a K-major operand the stride offset is
+// the distance between 8-row groups and the leading offset is unused; for an
+// MN-major operand the leading offset is the distance between 64-element
+// column blocks and the stride offset the distance between 8-row K groups.
+__device__ __forceinline__ uint64_t tc_sw128_desc(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes)
+{
+    return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)((lbo_bytes >> 4) & 0x3FFFu) << 16) |
+           ((uint64_t)((sbo_bytes >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
+}
+
+// D[tmem] (+)= A[smem] * B[smem]; `accumulate` = 0 overwrites D.
+__device__ __forceinline__ void tc_mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t accumulate)
+{
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "setp.ne.b32 p, %4, 0;\n\t"
+                 "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+                 "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+                 : "memory");
+}
+
+// Arrives once on `bar` when every tcgen05.mma this thread issued before has
+// completed (its shared-memory reads and TMEM writes included).
+__device__ __forceinline__ void tc_commit(uint64_t *bar)
+{
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                     smem_addr(bar))
+                 : "memory");
+}
+
+// --- TMEM <-> registers (warp-collective; warp w reaches lanes 32*(w%4)..+31)
+
+#define PKV_R8(i) "=r"(r[i]), "=r"(r[i + 1]), "=r"(r[i + 2]), "=r"(r[i + 3]), "=r"(r[i + 4]), "=r"(r[i + 5]), \
+                  "=r"(r[i + 6]), "=r"(r[i + 7])
+#define PKV_W8(i) "r"(r[i]), "r"(r[i + 1]), "r"(r[i + 2]), "r"(r[i + 3]), "r"(r[i + 4]), "r"(r[i + 5]), \
+                  "r"(r[i + 6]), "r"(r[i + 7])
+
+// 32 consecutive columns of this thread's lane, waited for before returning.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32])
+{
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+                 "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+                 "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];\n\t"
+                 "tcgen05.wait::ld.sync.aligned;"
+                 : PKV_R8(0), PKV_R8(8), PKV_R8(16), PKV_R8(24)
+                 : "r"(taddr)
+                 : "memory");
+}
+
+// Writes 32 consecutive columns of this thread's lane and waits for the write.
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32])
+{
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+                 "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
+                 "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};\n\t"
+                 "tcgen05.wait::st.sync.aligned;" ::"r"(taddr),
+                 PKV_W8(0), PKV_W8(8), PKV_W8(16), PKV_W8(24)
+                 : "memory");
+}
+
+#undef PKV_R8
+#undef PKV_W8
+
+// Makes this thread's generic-proxy shared-memory writes visible to the async
+// proxy (TMA, tcgen05.mma operand reads) after a following synchronisation.
+__device__ __forceinline__ void fence_proxy_async_smem()
+{
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// 3-D tiled TMA load with the default L2 policy.
+__device__ __forceinline__ void tma_load_3d_plain(void *dst, const CUtensorMap *map, int x, int y, int z,
+                                                  uint64_t *bar)
+{
+    asm volatile("cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+                 " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_addr(dst)),
+                 "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_addr(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ float ex2_approx(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+} // namespace pkv

@@ -231,6 +231,30 @@ def ragged_prefill(device="cpu", seed: int = 4, batch: int = 8, num_pages: int =
     return case
 
 
+def small_prefill(seed: int, q_lens, kv_lens, num_q_heads: int, num_kv_heads: int, head_dim: int,
+                  page_size: int, layout: int = HND, extra_pages: int = 3, device="cpu") -> PagedCase:
+    """A ragged prefill problem of chosen lengths: request b has q_lens[b]
+    queries over kv_lens[b] cached keys; pages from a seeded permutation,
+    every slot without a token NaN."""
+    g = _gen(seed)
+    q_lens = np.asarray(q_lens, np.int32)
+    kv_lens = np.asarray(kv_lens, np.int32)
+    B = len(q_lens)
+    P = page_size
+    indptr = np.concatenate([[0], np.cumsum(q_lens)]).astype(np.int32)
+    needed = (np.maximum(kv_lens, 0) + P - 1) // P
+    num_pages = int(needed.sum()) + 1 + extra_pages
+    max_blocks = max(int(needed.max()), 1)
+    order = (torch.randperm(num_pages - 1, generator=g).numpy() + 1).astype(np.int32)
+    bt = assign_pages(needed, num_pages, max_blocks, order)
+    case = PagedCase("prefill", B, num_q_heads, num_kv_heads, head_dim, P, num_pages, layout, max_blocks, bt,
+                     np.zeros(B, np.int32), 1.0 / math.sqrt(head_dim),
+                     q=_randn_bf16((int(indptr[-1]), num_q_heads, head_dim), g, "cpu").to(device),
+                     qo_indptr=indptr, kv_lens=kv_lens)
+    _fill_cache(case, g, device, "cpu")
+    return case
+
+
 @dataclass
 class SweepCase:
     """The batch sweep: ``layers`` per-layer K/V pools that share one block

@@ -180,3 +180,37 @@ def test_noalloc_rejects_problems_beyond_its_scratch():
     st = lib.pkv_decode_attn_noalloc(ctypes.byref(small), FAKE, FAKE, FAKE, None, None, FAKE, 4, FAKE, 4, 6 * 8, 0.1,
                                      FAKE, None, None, None)
     assert st == pkv.api.EUNSUPPORTED  # argument errors are those of pkv_decode_attn
+
+
+def _prefill(lib, desc, batch=2, hq=8, total_q=40, ws=FAKE, ws_bytes=1 << 30, q=FAKE, scale=0.1, max_blocks=4):
+    return lib.pkv_prefill_attn(ctypes.byref(desc), FAKE, FAKE, q, FAKE, FAKE, FAKE, max_blocks, batch, hq, total_q,
+                                scale, FAKE, None, ws, ws_bytes, None, None)
+
+
+def test_prefill_workspace_size():
+    d = CacheDesc(4096, 16, 6, 256, 1)
+    n = pkv.pkv_prefill_workspace_size(8, 4352, 48, d)
+    # plan header + one 32-byte record per (request, query tile): 4352/16 + 8 tiles at most
+    assert n == 256 + ((4352 // 16 + 8) * 32 + 255) // 256 * 256
+    assert pkv.pkv_prefill_workspace_size(8, 4352, 6 * 6, d) == 0         # group 6: not a power of two
+    assert pkv.pkv_prefill_workspace_size(8, 4352, 6 * 256, d) == 0       # group above 128
+    assert pkv.pkv_prefill_workspace_size(1025, 4352, 48, d) == 0
+    assert pkv.pkv_prefill_workspace_size(8, 4352, 48, CacheDesc(4096, 4, 6, 256, 1)) == 0  # page 4
+
+
+def test_prefill_argument_errors_return_before_any_launch():
+    lib = _lib.load()
+    d = CacheDesc(64, 16, 2, 128, 1)
+    assert _prefill(lib, CacheDesc(64, 16, 2, 96, 1)) == pkv.api.EUNSUPPORTED   # head dim
+    assert _prefill(lib, CacheDesc(64, 4, 2, 128, 1)) == pkv.api.EUNSUPPORTED   # page below 8
+    assert _prefill(lib, d, hq=7) == pkv.api.EINVAL                             # Hq % Hkv
+    assert _prefill(lib, d, hq=6) == pkv.api.EUNSUPPORTED                       # group 3
+    assert _prefill(lib, d, q=None) == pkv.api.EINVAL
+    assert _prefill(lib, d, q=ctypes.c_void_p(0x10008)) == pkv.api.EINVAL        # misaligned
+    assert _prefill(lib, d, scale=float("inf")) == pkv.api.EINVAL
+    assert _prefill(lib, d, ws=None) == pkv.api.EWORKSPACE
+    assert _prefill(lib, d, ws_bytes=16) == pkv.api.EWORKSPACE
+    assert _prefill(lib, d, batch=0) == pkv.api.OK
+    assert _prefill(lib, d, total_q=0) == pkv.api.OK
+    assert _prefill(lib, d, batch=1025) == pkv.api.EUNSUPPORTED
+    assert _prefill(lib, d, total_q=-1) == pkv.api.EINVAL
