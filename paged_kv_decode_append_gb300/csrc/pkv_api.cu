@@ -124,20 +124,32 @@ CUresult encode_pool_map(CUtensorMap *map, const pkv_cache_desc &d, void *base, 
 }
 
 
-// Tensor map over q [total_q, Hq, D] whose boxes are q_tile consecutive
-// queries x `group` consecutive heads x 64 columns, 128-byte swizzled
-// ([q_tile][group][64] in shared memory: row = query * group + head).
-CUresult encode_q_map(CUtensorMap *map, const void *q, int total_q, int num_q_heads, int head_dim, int group,
-                      int q_tile)
+
+CUresult encode_group_map(CUtensorMap *map, const pkv_cache_desc &d, void *base, int box_tokens)
 {
     PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
     if (enc == nullptr)
         return CUDA_ERROR_NOT_FOUND;
-    const cuuint64_t dims[3] = {(cuuint64_t)head_dim, (cuuint64_t)num_q_heads, (cuuint64_t)total_q};
-    const cuuint64_t strides[2] = {(cuuint64_t)head_dim * 2, (cuuint64_t)head_dim * 2 * num_q_heads};
-    const cuuint32_t box[3] = {64, (cuuint32_t)group, (cuuint32_t)q_tile};
-    const cuuint32_t elem_strides[3] = {1, 1, 1};
-    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(q), dims, strides, box, elem_strides,
+    const cuuint64_t D = (cuuint64_t)d.head_dim, P = (cuuint64_t)d.page_size, H = (cuuint64_t)d.num_kv_heads;
+    const cuuint32_t box[5] = {64, 8, (cuuint32_t)(D / 64), (cuuint32_t)(box_tokens / 8), 1};
+    const cuuint32_t elem_strides[5] = {1, 1, 1, 1, 1};
+    cuuint64_t dims[5], strides[4];
+    if (d.layout == PKV_HND) { // [pages * Hkv][P][D]
+        const cuuint64_t v_dims[5] = {64, 8, D / 64, P / 8, (cuuint64_t)d.num_pages * H};
+        const cuuint64_t v_strides[4] = {D * 2, 128, 8 * D * 2, P * D * 2};
+        for (int i = 0; i < 5; ++i)
+            dims[i] = v_dims[i];
+        for (int i = 0; i < 4; ++i)
+            strides[i] = v_strides[i];
+    } else { // [pages * P][Hkv][D]: token groups run across pages
+        const cuuint64_t v_dims[5] = {64, 8, D / 64, (cuuint64_t)d.num_pages * P / 8, H};
+        const cuuint64_t v_strides[4] = {H * D * 2, 128, 8 * H * D * 2, D * 2};
+        for (int i = 0; i < 5; ++i)
+            dims[i] = v_dims[i];
+        for (int i = 0; i < 4; ++i)
+            strides[i] = v_strides[i];
+    }
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, base, dims, strides, box, elem_strides,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
@@ -353,6 +365,7 @@ pkv_status pkv_prefill_attn(const pkv_cache_desc *desc, const void *k_cache, con
     a.qo_indptr = qo_indptr;
     a.kv_lens = kv_lens;
     a.block_table = block_table;
+    a.q = q;
     a.out = out;
     a.lse = lse;
     a.workspace = workspace;
@@ -360,9 +373,8 @@ pkv_status pkv_prefill_attn(const pkv_cache_desc *desc, const void *k_cache, con
     a.shape = shape;
     const int box = prefill_box_tokens(desc->page_size);
     PrefillMaps maps;
-    if (encode_q_map(&maps.q, q, total_q, num_q_heads, desc->head_dim, shape.group, shape.q_tile) != CUDA_SUCCESS ||
-        encode_pool_map(&maps.k, *desc, const_cast<void *>(k_cache), box, 64, 1) != CUDA_SUCCESS ||
-        encode_pool_map(&maps.v, *desc, const_cast<void *>(v_cache), box, 64, 1) != CUDA_SUCCESS)
+    if (encode_group_map(&maps.k, *desc, const_cast<void *>(k_cache), box) != CUDA_SUCCESS ||
+        encode_group_map(&maps.v, *desc, const_cast<void *>(v_cache), box) != CUDA_SUCCESS)
         return PKV_ECUDA;
     return launch_prefill(a, maps, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PKV_OK : PKV_ECUDA;
 }

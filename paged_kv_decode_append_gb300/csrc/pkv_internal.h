@@ -102,6 +102,16 @@ int decode_swizzle(int page_size);
 CUresult encode_pool_map(CUtensorMap *map, const pkv_cache_desc &d, void *base, int box_tokens, int box_dim,
                          int swizzle);
 
+// Tensor map over one K or V pool whose boxes are `box_tokens` (a multiple
+// of 8, within one page) consecutive tokens of one kv head with all head_dim
+// values, landing in shared memory as [box_tokens / 8][head_dim / 64][8][64]:
+// groups of 8 token rows (128 bytes each, 128-byte swizzle) for every 64-column
+// block.  Consecutive 8-row groups of one column block are then head_dim * 16
+// bytes apart whichever page they come from.  5-D: (64 columns, 8 tokens,
+// column blocks, token groups, page-heads) over HND, (64 columns, 8 tokens,
+// column blocks, token groups across pages, heads) over NHD.
+CUresult encode_group_map(CUtensorMap *map, const pkv_cache_desc &d, void *base, int box_tokens);
+
 int sm_count(int device);
 
 // ---------------------------------------------------------------- prefill
@@ -128,6 +138,7 @@ struct PrefillArgs {
     const int32_t *qo_indptr;
     const int32_t *kv_lens;
     const int32_t *block_table;
+    const void *q;
     void *out;
     float *lse;
     void *workspace;
@@ -135,10 +146,10 @@ struct PrefillArgs {
     PrefillShape shape;
 };
 
-// TMA descriptors of one prefill call: q tiles ([128/G queries][G heads][64]
-// boxes) and 64-column boxes of min(page_size, 64) tokens of the K and V pools.
+// TMA descriptors of one prefill call: token-group boxes (encode_group_map)
+// of min(page_size, 64) tokens of the K and V pools.
 struct PrefillMaps {
-    CUtensorMap q, k, v;
+    CUtensorMap k, v;
 };
 
 cudaError_t launch_prefill(const PrefillArgs &a, const PrefillMaps &maps, cudaStream_t stream);

@@ -17,20 +17,24 @@
 //  - A one-CTA plan kernel validates every request, lists the query tiles and
 //    orders them by their number of 64-token kv tiles, longest first; the
 //    persistent CTAs take units in that order, snaking over the grid.
-//  - Warp roles: warp 0 loads Q once per unit and the unit's K and V tiles,
-//    64 tokens x head_dim each, with TMA into a ring of shared-memory stages
-//    (in the order the MMAs consume them); warp 1 owns TMEM and one of its
-//    threads issues the MMAs; warps 2-5 (one per TMEM lane quarter) run the
+//  - Warp roles: warp 0 loads the unit's K and V tiles, 64 tokens x head_dim
+//    each, with TMA into a ring of shared-memory stages (in the order the
+//    MMAs consume them); warp 1 owns TMEM and one of its threads issues the
+//    MMAs; warps 2-5 (one per TMEM lane quarter) load Q into TMEM and run the
 //    online softmax and the epilogue, one row per thread.
-//  - TMEM: the O [128 x D] fp32 accumulator at columns 0..D-1 and two
-//    S [128 x 64] fp32 buffers after it, so S of tile j+1 is computed while
-//    the softmax of tile j runs.
-//  - S = Q K^T (K-major Q and K); the softmax writes P into shared memory in
-//    the K-major swizzled layout as two bf16 parts, p = hi + lo (about 16
+//  - TMEM: the O [128 x D] fp32 accumulator at columns 0..D-1, two
+//    S [128 x 64] fp32 buffers after it (S of tile j+1 is computed while the
+//    softmax of tile j runs), then the unit's Q [128 x D] as bf16 pairs.
+//    Keeping Q out of shared memory leaves room for a deep K/V ring: the
+//    tiles come mostly from L2, and it takes several of them in flight to
+//    cover its latency.  The next unit's Q is written while the last PV
+//    MMAs of the current one run.
+//  - S = Q K^T (Q from TMEM, K-major K); the softmax writes P back into the
+//    tile's S columns of TMEM as two bf16 parts, p = hi + lo (about 16
 //    significant bits: a single bf16 P alone, 8 bits, leaves errors near
 //    2^-9 of the row's scale, well above 1e-2 of the small outputs that
-//    cancellation produces); O += P_hi V + P_lo V with V as an MN-major
-//    operand (its rows are tokens, its columns head_dim).
+//    cancellation produces); O += P_hi V + P_lo V with P from TMEM and V as
+//    an MN-major operand (its rows are tokens, its columns head_dim).
 //  - Online softmax in base 2 on scores scaled by softmax_scale * log2(e).
 //    A row's O and running sum are rescaled only when its maximum grows by
 //    more than 8: until then the exponentials use the older maximum, which is
@@ -45,7 +49,9 @@
 namespace pkv {
 namespace {
 
-constexpr int kPfThreads = 192;
+constexpr int kPfSoftmaxWarps = 8; // two per TMEM lane quarter, each on half of a row's columns
+constexpr int kPfSoftmaxThreads = kPfSoftmaxWarps * 32;
+constexpr int kPfThreads = 64 + kPfSoftmaxThreads;
 constexpr int kPfProducerWarp = 0;
 constexpr int kPfMmaWarp = 1;
 constexpr int kPfRows = 128;    // M of every MMA
@@ -55,55 +61,66 @@ constexpr int kPlanThreads = 1024;
 constexpr float kRescaleLog2 = 8.0f;
 constexpr float kLn2 = 0.693147180559945309f;
 
+constexpr int kPfMaxStages = 12;
+
 template <int D> struct PfCfg {
-    static constexpr int kChunks = D / 64;                     // 128-byte column blocks of a row
-    static constexpr int kStages = D == 256 ? 3 : 6;           // K / V tiles in flight
-    static constexpr uint32_t kQBytes = kPfRows * D * 2;       // [chunk][128 rows][128 B]
-    static constexpr uint32_t kStageBytes = kPfTile * D * 2;   // [chunk][64 tokens][128 B]
-    static constexpr uint32_t kPHalf = kPfRows * kPfTile * 2;  // [128 rows][128 B]
-    static constexpr uint32_t kPBytes = 2 * kPHalf;            // P = hi + lo halves
-    static constexpr uint32_t kOffQ = 0;
-    static constexpr uint32_t kOffStage = kQBytes;
-    static constexpr uint32_t kOffP = kOffStage + kStages * kStageBytes;
-    static constexpr uint32_t kOffBar = kOffP + 2 * kPBytes;
-    static constexpr uint32_t kSmem = kOffBar + 256 + 1024; // + barriers + alignment slack
-    static constexpr uint32_t kTmemCols = D == 256 ? 512 : 256;
+    static constexpr int kChunks = D / 64;                                      // 128-byte column blocks of a row
+    static constexpr int kStages = D == 256 ? 6 : kPfMaxStages; // K / V tiles in flight
+    // A K or V stage is [8-token group][64-column block][8 rows][128 B]: for
+    // one column block, consecutive 8-row groups are kGroupStride apart.
+    static constexpr uint32_t kStageBytes = kPfTile * D * 2;
+    static constexpr uint32_t kGroupStride = 8 * D * 2;
+    static constexpr uint32_t kOffStage = 0;
+    static constexpr uint32_t kOffBar = kOffStage + kStages * kStageBytes;
+    static constexpr uint32_t kOffXchg = kOffBar + 512;     // softmax half-row exchange
+    static constexpr uint32_t kSmem = kOffXchg + 3 * 1024 + 1024; // + alignment slack
     static constexpr uint32_t kColO = 0;
+    // Two 64-column S buffers; the softmax overwrites S of a tile with its P
+    // (bf16 pairs: P_hi in the first 32 columns, P_lo in the last 32), which
+    // the PV MMA reads as its A operand.
     static constexpr uint32_t kColS = D;
+    static constexpr uint32_t kColQ = D + 2 * kPfTile;     // D / 2 columns of bf16 pairs
+    static constexpr uint32_t kTmemCols = (kColQ + D / 2) <= 256 ? 256 : 512;
 };
-static_assert(PfCfg<256>::kSmem <= 232448, "prefill shared memory over the per-CTA limit");
+static_assert(PfCfg<256>::kSmem <= 232448 && PfCfg<128>::kSmem <= 232448 && PfCfg<64>::kSmem <= 232448,
+              "prefill shared memory over the per-CTA limit");
+static_assert(PfCfg<256>::kColQ + 128 <= 512, "prefill TMEM columns");
 
 struct PfBars {
     uint64_t q_full, q_empty;
-    uint64_t full[6], empty[6];
+    uint64_t full[kPfMaxStages], empty[kPfMaxStages];
     uint64_t s_full[2], p_full[2], o_done[2];
     uint64_t o_free;
     uint64_t drain;
+    uint64_t pair[4]; // the two softmax warps of each TMEM lane quarter
     uint32_t tmem_base;
     int32_t abort;
 };
-static_assert(sizeof(PfBars) <= 256, "barrier block");
+static_assert(sizeof(PfBars) <= 512, "barrier block");
 
-// One query tile of one request (all kv heads share it).
+// `cluster` consecutive query tiles of one request (all kv heads share it):
+// CTA rank r of a cluster takes query tile t * cluster + r.
 struct PfUnit {
     int32_t b, t, q_start, q_len, kv_len, n_tiles, pad0, pad1;
 };
 static_assert(sizeof(PfUnit) == 32, "unit record");
 
 struct PfParams {
+    const __nv_bfloat16 *q;
     const int32_t *block_table;
     const PfUnit *units;
     const int32_t *n_pairs;
     __nv_bfloat16 *out;
     float *lse;
     int32_t *err_flag;
-    int max_blocks, num_q_heads, num_kv_heads;
+    int max_blocks, num_q_heads, num_kv_heads, total_q;
     int group_shift, q_tile, page_shift, box_shift, layout;
+    int cluster; // CTAs per cluster sharing every K / V tile (1, 2 or 4)
     float q_scale;
 };
 
 struct PfMapsDev {
-    CUtensorMap q, k, v;
+    CUtensorMap k, v; // token-group boxes (encode_group_map)
 };
 
 struct PfPlanParams {
@@ -115,7 +132,7 @@ struct PfPlanParams {
     __nv_bfloat16 *out;
     float *lse;
     int32_t *err_flag;
-    int batch, max_blocks, num_pages, page_shift, total_q, q_tile, num_q_heads, head_dim;
+    int batch, max_blocks, num_pages, page_shift, total_q, q_tile, num_q_heads, head_dim, cluster;
     int64_t cap_pairs;
 };
 
@@ -137,10 +154,11 @@ __device__ __forceinline__ int pf_item_v(int j, int nt)
     return j == nt - 1 ? 2 * nt - 1 : 2 * j + 2;
 }
 
-// k-th unit of this CTA: rounds of gridDim.x units, alternating direction.
-__device__ __forceinline__ int pf_unit_at(int k)
+// k-th unit of this CTA's cluster (every CTA of a cluster works on the same
+// unit): rounds of one unit per cluster, alternating direction.
+__device__ __forceinline__ int pf_unit_at(int k, int cluster)
 {
-    const int g = (int)gridDim.x, c = (int)blockIdx.x;
+    const int g = (int)gridDim.x / cluster, c = (int)blockIdx.x / cluster;
     return k * g + ((k & 1) ? g - 1 - c : c);
 }
 
@@ -175,37 +193,39 @@ __device__ __forceinline__ bool pf_wait_all(uint64_t *bar, uint32_t parity, PfBa
 
 // ---------------------------------------------------------------- producer
 
+// Issues one box of an item (token-group map coordinates: token group `c3`,
+// page-head or head `c4`): the TMA load lands in this CTA and, in a cluster,
+// is multicast to the same offset of every CTA of it.
+__device__ __forceinline__ void pf_tma5(const PfParams &p, void *dst, const CUtensorMap *map, int c3, int c4,
+                                        uint64_t *bar)
+{
+    if (p.cluster > 1)
+        tma_load_5d_mc(dst, map, 0, 0, 0, c3, c4, bar, (uint16_t)((1u << p.cluster) - 1u));
+    else
+        tma_load_5d_plain(dst, map, 0, 0, 0, c3, c4, bar);
+}
+
 template <int D>
 __device__ void pf_producer(const PfParams &p, const PfMapsDev &maps, uint8_t *smem, PfBars &bars, int n_units,
-                            int lane)
+                            int lane, int cl_rank)
 {
     using C = PfCfg<D>;
     const int Hkv = p.num_kv_heads;
-    const int G = 1 << p.group_shift;
     const int P = 1 << p.page_shift;
     const int BT = 1 << p.box_shift;             // tokens per box: min(page_size, 64)
     const int boxes = kPfTile >> p.box_shift;     // boxes per full tile
-    const uint32_t box_bytes = (uint32_t)BT * 128u;
+    const uint32_t box_bytes = (uint32_t)BT * D * 2; // BT tokens x all of head_dim
+    const bool nhd = p.layout == PKV_NHD;
     int ib = 0, issued = 0;
-    uint32_t uc = 0;
     bool ok = true;
     for (int k = 0; ok; ++k) {
-        const int u = pf_unit_at(k);
+        const int u = pf_unit_at(k, p.cluster);
         if (u >= n_units)
             break;
-        const int pair = u / Hkv, g = u - pair * Hkv;
-        const PfUnit un = p.units[pair];
+        const int grp = u / Hkv, g = u - grp * Hkv;
+        const PfUnit un = p.units[grp];
         const int32_t *bt_row = p.block_table + (int64_t)un.b * p.max_blocks;
         const int nt = un.n_tiles, kv = un.kv_len;
-
-        if (uc > 0 && !pf_wait_all(&bars.q_empty, (uc - 1) & 1, bars, p.err_flag))
-            break;
-        if (lane == 0) {
-            mbar_arrive_expect_tx(&bars.q_full, C::kQBytes);
-            const int z = un.q_start + un.t * p.q_tile;
-            for (int c = 0; c < C::kChunks; ++c)
-                tma_load_3d_plain(smem + C::kOffQ + c * (kPfRows * 128), &maps.q, 64 * c, g * G, z, &bars.q_full);
-        }
         // Lane i holds the page of box i of a tile (boxes <= 8 <= 32 lanes).
         auto page_ids = [&](int j) {
             const int tok = j * kPfTile + lane * BT;
@@ -223,6 +243,7 @@ __device__ void pf_producer(const PfParams &p, const PfMapsDev &maps, uint8_t *s
                 const int itg = ib + (kind == 0 ? pf_item_k(jj) : pf_item_v(jj, nt));
                 const int stage = itg % C::kStages;
                 const int n = itg / C::kStages;
+                // The stage is free once every CTA of the cluster has released it.
                 if (n > 0 && !pf_wait_all(&bars.empty[stage], (n - 1) & 1, bars, p.err_flag)) {
                     ok = false;
                     break;
@@ -231,26 +252,23 @@ __device__ void pf_producer(const PfParams &p, const PfMapsDev &maps, uint8_t *s
                 const int ntok = min(kPfTile, kv - tok0);
                 const int nbox = (ntok + BT - 1) >> p.box_shift;
                 uint8_t *dst = smem + C::kOffStage + stage * C::kStageBytes;
-                const CUtensorMap *map = kind == 0 ? &maps.k : &maps.v;
                 const int ids = kind == 0 ? ids_cur : ids_prev;
-                if (lane == 0)
-                    mbar_arrive_expect_tx(&bars.full[stage], (uint32_t)nbox * C::kChunks * box_bytes);
+                if (lane == 0) // the whole item, whichever CTA of the cluster loads each part
+                    mbar_arrive_expect_tx(&bars.full[stage], (uint32_t)nbox * box_bytes);
+                // Sub-boxes: K (and V when a box is a whole tile) in 64-column
+                // boxes, [block][64 tokens][128 B], so the S MMA sees evenly
+                // spaced rows; V otherwise in page boxes, [box][block][BT][128 B].
+                const CUtensorMap *map = kind == 0 ? &maps.k : &maps.v;
+                const int own = p.cluster - 1; // box i belongs to CTA rank (i & own)
                 for (int bx = 0; bx < nbox; ++bx) {
                     const int page = __shfl_sync(0xffffffffu, ids, bx);
-                    if (lane == 0) {
-                        const int slot = (tok0 + bx * BT) & (P - 1);
-                        int y, z;
-                        if (p.layout == PKV_NHD) {
-                            y = g;
-                            z = page * P + slot;
-                        } else {
-                            y = slot;
-                            z = page * Hkv + g;
-                        }
-                        for (int c = 0; c < C::kChunks; ++c)
-                            tma_load_3d_plain(dst + c * (kPfTile * 128) + bx * box_bytes, map, 64 * c, y, z,
-                                              &bars.full[stage]);
-                    }
+                    if (lane != 0 || (bx & own) != cl_rank)
+                        continue;
+                    const int slot = (tok0 + bx * BT) & (P - 1);
+                    if (nhd)
+                        pf_tma5(p, dst + bx * box_bytes, map, (page * P + slot) >> 3, g, &bars.full[stage]);
+                    else
+                        pf_tma5(p, dst + bx * box_bytes, map, slot >> 3, page * Hkv + g, &bars.full[stage]);
                 }
                 issued = itg + 1;
             }
@@ -259,11 +277,15 @@ __device__ void pf_producer(const PfParams &p, const PfMapsDev &maps, uint8_t *s
             ids_next = page_ids(j + 2);
         }
         ib += 2 * nt;
-        ++uc;
     }
-    // Own copies still in flight (none unless a wait above gave up).
-    for (int itg = issued > C::kStages ? issued - C::kStages : 0; itg < issued; ++itg)
-        mbar_wait(&bars.full[itg % C::kStages], (itg / C::kStages) & 1);
+    // Copies still in flight into this CTA, and (in a cluster) the peers'
+    // releases of the last stages: once they have arrived nothing of the
+    // cluster writes into this CTA any more.  Immediate unless a wait gave up.
+    for (int itg = issued > C::kStages ? issued - C::kStages : 0; itg < issued; ++itg) {
+        pf_wait(&bars.full[itg % C::kStages], (itg / C::kStages) & 1, bars, p.err_flag);
+        if (p.cluster > 1)
+            pf_wait(&bars.empty[itg % C::kStages], (itg / C::kStages) & 1, bars, p.err_flag);
+    }
 }
 
 // ---------------------------------------------------------------- MMA issuer
@@ -274,14 +296,13 @@ __device__ void pf_mma(const PfParams &p, uint8_t *smem, PfBars &bars, uint32_t 
     using C = PfCfg<D>;
     constexpr uint32_t kIdescS = tc_idesc_bf16(kPfRows, kPfTile, false, false);
     constexpr uint32_t kIdescO = tc_idesc_bf16(kPfRows, D, false, true);
-    const uint32_t q_base = smem_addr(smem + C::kOffQ);
     const uint32_t st_base = smem_addr(smem + C::kOffStage);
-    const uint32_t p_base = smem_addr(smem + C::kOffP);
     int ib = 0, gt0 = 0;
     uint32_t uc = 0;
     bool issued = false;
+    const uint16_t cl_mask = (uint16_t)((1u << p.cluster) - 1u);
     for (int k = 0;; ++k) {
-        const int u = pf_unit_at(k);
+        const int u = pf_unit_at(k, p.cluster);
         if (u >= n_units)
             break;
         const int nt = p.units[u / p.num_kv_heads].n_tiles;
@@ -300,12 +321,14 @@ __device__ void pf_mma(const PfParams &p, uint8_t *smem, PfBars &bars, uint32_t 
                 const uint32_t kb = st_base + stage * C::kStageBytes;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint64_t a = tc_sw128_desc(q_base + (kk >> 2) * (kPfRows * 128) + (kk & 3) * 32, 16, 1024);
-                    const uint64_t b = tc_sw128_desc(kb + (kk >> 2) * (kPfTile * 128) + (kk & 3) * 32, 16, 1024);
-                    tc_mma_bf16(d, a, b, kIdescS, kk > 0 ? 1u : 0u);
+                    const uint64_t b = tc_sw128_desc(kb + (kk >> 2) * 1024 + (kk & 3) * 32, 16, C::kGroupStride);
+                    tc_mma_bf16_ts(d, tmem + C::kColQ + kk * 8, b, kIdescS, kk > 0 ? 1u : 0u);
                 }
                 tc_commit(&bars.s_full[gt & 1]);
-                tc_commit(&bars.empty[stage]);
+                if (p.cluster > 1) // the stage is refilled for the whole cluster
+                    tc_commit_mc(&bars.empty[stage], cl_mask);
+                else
+                    tc_commit(&bars.empty[stage]);
                 if (j == nt - 1)
                     tc_commit(&bars.q_empty);
             }
@@ -321,16 +344,20 @@ __device__ void pf_mma(const PfParams &p, uint8_t *smem, PfBars &bars, uint32_t 
                     goto done;
                 tc_fence_after();
                 const uint32_t vb = st_base + stage * C::kStageBytes;
-                const uint32_t pb = p_base + (uint32_t)(gt & 1) * C::kPBytes;
+                const uint32_t pt = tmem + C::kColS + (uint32_t)(gt & 1) * kPfTile; // P of tile gt
 #pragma unroll
                 for (int kk = 0; kk < 2 * (kPfTile / 16); ++kk) { // hi part, then lo part
-                    const int k4 = kk & (kPfTile / 16 - 1);
-                    const uint64_t a = tc_sw128_desc(pb + (kk >> 2) * C::kPHalf + k4 * 32, 16, 1024);
-                    const uint64_t b = tc_sw128_desc(vb + k4 * (16 * 128), kPfTile * 128, 1024);
-                    tc_mma_bf16(tmem + C::kColO, a, b, kIdescO, (jv > 0 || kk > 0) ? 1u : 0u);
+                    const int k4 = kk & (kPfTile / 16 - 1);      // 16-token K step
+                    // V rows 16*k4 .. +15: two 8-row groups; N spans the column blocks (1024 B apart)
+                    const uint64_t b = tc_sw128_desc(vb + (uint32_t)(2 * k4) * C::kGroupStride, 1024, C::kGroupStride);
+                    tc_mma_bf16_ts(tmem + C::kColO, pt + (kk >> 2) * (kPfTile / 2) + k4 * 8, b, kIdescO,
+                                   (jv > 0 || kk > 0) ? 1u : 0u);
                 }
                 tc_commit(&bars.o_done[gt & 1]);
-                tc_commit(&bars.empty[stage]);
+                if (p.cluster > 1)
+                    tc_commit_mc(&bars.empty[stage], cl_mask);
+                else
+                    tc_commit(&bars.empty[stage]);
             }
         }
         gt0 += nt;
@@ -347,59 +374,138 @@ done:
 
 // ---------------------------------------------------------------- softmax + epilogue
 
+// Writes this thread's half of its row of a unit's Q tile (query r / G, head
+// r % G of the group; head_dim columns [half * D/2, (half+1) * D/2)) into TMEM
+// columns kColQ + half * D/4 .. as bf16 pairs; rows past total_q get 0.
 template <int D>
-__device__ void pf_softmax(const PfParams &p, uint8_t *smem, PfBars &bars, uint32_t tmem, int n_units, int warp,
-                           int lane)
+__device__ __forceinline__ void pf_load_q(const PfParams &p, const PfUnit &un, int g, int r, int half,
+                                          uint32_t t_row, int cl_rank)
 {
     using C = PfCfg<D>;
+    const int tok = un.q_start + (un.t * p.cluster + cl_rank) * p.q_tile + (r >> p.group_shift);
+    const int head = g * (1 << p.group_shift) + (r & ((1 << p.group_shift) - 1));
+    const bool in = tok < p.total_q;
+    const uint4 *src =
+        reinterpret_cast<const uint4 *>(p.q + ((int64_t)(in ? tok : 0) * p.num_q_heads + head) * D + half * (D / 2));
+    constexpr int kLoads = D / 16; // 16-byte loads of half a row (at most 16)
+    uint4 v[kLoads];
+#pragma unroll
+    for (int i = 0; i < kLoads; ++i)
+        v[i] = in ? __ldg(src + i) : make_uint4(0u, 0u, 0u, 0u);
+    if constexpr (kLoads >= 8) {
+#pragma unroll
+        for (int c = 0; c < kLoads / 8; ++c) {
+            uint32_t w[32];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                w[4 * i] = v[8 * c + i].x;
+                w[4 * i + 1] = v[8 * c + i].y;
+                w[4 * i + 2] = v[8 * c + i].z;
+                w[4 * i + 3] = v[8 * c + i].w;
+            }
+            tmem_st32(t_row + C::kColQ + half * (D / 4) + c * 32, w);
+        }
+    } else { // head_dim 64: half a row is 16 columns
+        uint32_t w[16];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            w[4 * i] = v[i].x;
+            w[4 * i + 1] = v[i].y;
+            w[4 * i + 2] = v[i].z;
+            w[4 * i + 3] = v[i].w;
+        }
+        tmem_st16(t_row + C::kColQ + half * (D / 4), w);
+    }
+}
+
+// Synchronises the two warps that share a TMEM lane quarter (their `phase`-th
+// meeting); bounded like every wait, false if it gave up.
+__device__ __forceinline__ bool pf_pair_sync(PfBars &bars, int quarter, uint32_t &phase, int32_t *err_flag)
+{
+    mbar_arrive(&bars.pair[quarter]);
+    return pf_wait_all(&bars.pair[quarter], (phase++) & 1, bars, err_flag);
+}
+
+template <int D>
+__device__ void pf_softmax(const PfParams &p, uint8_t *smem, PfBars &bars, uint32_t tmem, int n_units, int warp,
+                           int lane, int cl_rank)
+{
+    using C = PfCfg<D>;
+    constexpr int kCols = kPfTile / 2;    // S columns of this thread
     const int quarter = warp & 3;         // TMEM lanes this warp may access
+    const int half = (warp - 2) >> 2;     // which half of the row's columns
     const int r = quarter * 32 + lane;    // tile row = TMEM lane
+    const int st = half * kPfRows + r;    // index among the softmax threads
     const uint32_t t_row = tmem + ((uint32_t)(quarter * 32) << 16);
+    float *xchg = reinterpret_cast<float *>(smem + C::kOffXchg); // [2 parities][2 halves][128 rows] + [2][128] sums
     const int G = 1 << p.group_shift;
     const int q_in_tile = r >> p.group_shift;
     const int h_in_group = r & (G - 1);
     const float qs = p.q_scale;
     int ib = 0, gt0 = 0;
+    uint32_t pair_phase = 0;
+
+    int u = pf_unit_at(0, p.cluster);
+    if (u >= n_units)
+        return;
+    {
+        const int grp = u / p.num_kv_heads;
+        pf_load_q<D>(p, p.units[grp], u - grp * p.num_kv_heads, r, half, t_row, cl_rank);
+        tc_fence_before();
+        mbar_arrive(&bars.q_full);
+    }
     for (int k = 0;; ++k) {
-        const int u = pf_unit_at(k);
+        u = pf_unit_at(k, p.cluster);
         if (u >= n_units)
             break;
-        const int pair = u / p.num_kv_heads, g = u - pair * p.num_kv_heads;
-        const PfUnit un = p.units[pair];
+        const int grp = u / p.num_kv_heads, g = u - grp * p.num_kv_heads;
+        const PfUnit un = p.units[grp];
         const int nt = un.n_tiles, kv = un.kv_len;
-        const int qi = un.t * p.q_tile + q_in_tile; // query index within the request
-        const bool valid = qi < un.q_len;
-        const int limit = min(kv - un.q_len + qi, kv - 1);            // last key this row sees
-        const int limit_min = kv - un.q_len + un.t * p.q_tile;        // smallest limit of the tile
-        float m_used = -INFINITY, l = 0.f;
+        const int t = un.t * p.cluster + cl_rank;   // this CTA's query tile
+        const int qi = t * p.q_tile + q_in_tile;    // query index within the request
+        const bool valid = qi < un.q_len;           // a tile past the request's end computes nothing kept
+        const int limit = min(kv - un.q_len + qi, kv - 1);                      // last key this row sees
+        const int limit_min = min(kv - un.q_len + t * p.q_tile, kv - 1);       // smallest limit of the tile
+        const int u_next = pf_unit_at(k + 1, p.cluster);
+        float m_used = -INFINITY, l = 0.f; // l: this half's part of the row sum
         for (int j = 0; j < nt; ++j) {
             const int gt = gt0 + j;
             if (!pf_wait_all(&bars.s_full[gt & 1], (gt >> 1) & 1, bars, p.err_flag))
                 return;
             tc_fence_after();
-            float x[kPfTile];
+            // Raw scores of this half; a non-positive scale is applied here, a
+            // positive one is folded into the exponent.
+            float x[kCols];
             {
                 uint32_t rr[32];
-                const uint32_t sa = t_row + C::kColS + (uint32_t)(gt & 1) * kPfTile;
-                tmem_ld32(sa, rr);
+                tmem_ld32(t_row + C::kColS + (uint32_t)(gt & 1) * kPfTile + half * kCols, rr);
 #pragma unroll
-                for (int i = 0; i < 32; ++i)
-                    x[i] = __uint_as_float(rr[i]) * qs;
-                tmem_ld32(sa + 32, rr);
-#pragma unroll
-                for (int i = 0; i < 32; ++i)
-                    x[32 + i] = __uint_as_float(rr[i]) * qs;
+                for (int i = 0; i < kCols; ++i)
+                    x[i] = __uint_as_float(rr[i]);
             }
-            const int tok0 = j * kPfTile;
-            if (tok0 + kPfTile - 1 > limit_min) {
+            if (!(qs > 0.f)) {
 #pragma unroll
-                for (int i = 0; i < kPfTile; ++i)
+                for (int i = 0; i < kCols; ++i)
+                    x[i] *= qs;
+            }
+            const float qse = qs > 0.f ? qs : 1.f;
+            const int tok0 = j * kPfTile + half * kCols;
+            if (j * kPfTile + kPfTile - 1 > limit_min) {
+#pragma unroll
+                for (int i = 0; i < kCols; ++i)
                     x[i] = (tok0 + i <= limit) ? x[i] : -INFINITY;
             }
-            float mt = x[0];
+            float mx = x[0];
 #pragma unroll
-            for (int i = 1; i < kPfTile; ++i)
-                mt = fmaxf(mt, x[i]);
+            for (int i = 1; i < kCols; ++i)
+                mx = fmaxf(mx, x[i]);
+            // row maximum over both halves
+            float *xm = xchg + (gt & 1) * (2 * kPfRows);
+            xm[half * kPfRows + r] = mx;
+            if (!pf_pair_sync(bars, quarter, pair_phase, p.err_flag))
+                return;
+            mx = fmaxf(mx, xm[(1 - half) * kPfRows + r]);
+            const float mt = mx * qse; // tile maximum in log2 units
             const bool grow = mt > m_used + kRescaleLog2;
             float alpha = 1.f;
             if (grow) {
@@ -407,7 +513,26 @@ __device__ void pf_softmax(const PfParams &p, uint8_t *smem, PfBars &bars, uint3
                 l *= alpha;
                 m_used = mt;
             }
-            // O holds this unit's sum only after its first PV.
+            const float m_ref = m_used == -INFINITY ? 0.f : m_used; // a row that has seen no key yet
+            // p = 2^(x*qse - m_ref) = hi + lo, both bf16, packed in pairs
+            uint32_t whi[kCols / 2], wlo[kCols / 2];
+            float2 sum2 = make_float2(0.f, 0.f);
+            const float2 q2 = make_float2(qse, qse), nm2 = make_float2(-m_ref, -m_ref);
+#pragma unroll
+            for (int e = 0; e < kCols / 2; ++e) {
+                const float2 a = ffma2(make_float2(x[2 * e], x[2 * e + 1]), q2, nm2);
+                const float2 pp = make_float2(ex2_approx(a.x), ex2_approx(a.y));
+                sum2 = __fadd2_rn(sum2, pp);
+                const __nv_bfloat162 hi = __floats2bfloat162_rn(pp.x, pp.y);
+                const float2 hf = __bfloat1622float2(hi);
+                const float2 d = __fadd2_rn(pp, make_float2(-hf.x, -hf.y));
+                const __nv_bfloat162 lo = __floats2bfloat162_rn(d.x, d.y);
+                whi[e] = *reinterpret_cast<const uint32_t *>(&hi);
+                wlo[e] = *reinterpret_cast<const uint32_t *>(&lo);
+            }
+            l += sum2.x + sum2.y;
+            // O holds this unit's sum only after its first PV; rescale this
+            // half's columns once the PV of tile gt - 1 is done.
             const bool rescale_o = grow && j > 0;
             if (__any_sync(0xffffffffu, rescale_o)) {
                 const int gp = gt - 1;
@@ -415,7 +540,7 @@ __device__ void pf_softmax(const PfParams &p, uint8_t *smem, PfBars &bars, uint3
                     return;
                 tc_fence_after();
                 const float a = rescale_o ? alpha : 1.f;
-                for (int c = 0; c < D; c += 32) {
+                for (int c = half * (D / 2); c < (half + 1) * (D / 2); c += 32) {
                     uint32_t rr[32];
                     tmem_ld32(t_row + C::kColO + c, rr);
 #pragma unroll
@@ -424,64 +549,61 @@ __device__ void pf_softmax(const PfParams &p, uint8_t *smem, PfBars &bars, uint3
                     tmem_st32(t_row + C::kColO + c, rr);
                 }
             }
-            // This P buffer was last read by the PV MMA of global tile gt - 2.
-            if (gt >= 2) {
-                const int gp = gt - 2;
-                if (!pf_wait_all(&bars.o_done[gp & 1], (gp >> 1) & 1, bars, p.err_flag))
-                    return;
+            // P over S in TMEM (both halves of the row have read S: the pair
+            // sync above): hi pairs at columns [16 half, +16), lo at 32 + that.
+            {
+                const uint32_t pcol = t_row + C::kColS + (uint32_t)(gt & 1) * kPfTile + half * (kCols / 2);
+                tmem_st16(pcol, whi);
+                tmem_st16(pcol + kPfTile / 2, wlo);
             }
-            uint8_t *prow = smem + C::kOffP + (gt & 1) * C::kPBytes + r * 128;
-            const float m_ref = m_used == -INFINITY ? 0.f : m_used; // a row that has seen no key yet
-            float sum = 0.f;
-#pragma unroll
-            for (int c8 = 0; c8 < 8; ++c8) {
-                uint32_t whi[4], wlo[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float p0 = ex2_approx(x[c8 * 8 + 2 * e] - m_ref);
-                    const float p1 = ex2_approx(x[c8 * 8 + 2 * e + 1] - m_ref);
-                    sum += p0 + p1;
-                    const __nv_bfloat162 hi = __floats2bfloat162_rn(p0, p1);
-                    const float2 hf = __bfloat1622float2(hi);
-                    const __nv_bfloat162 lo = __floats2bfloat162_rn(p0 - hf.x, p1 - hf.y);
-                    whi[e] = *reinterpret_cast<const uint32_t *>(&hi);
-                    wlo[e] = *reinterpret_cast<const uint32_t *>(&lo);
-                }
-                // 128-byte swizzle: 16-byte piece c8 of row r sits at piece c8 ^ (r % 8)
-                const int off = (c8 ^ (r & 7)) << 4;
-                *reinterpret_cast<uint4 *>(prow + off) = make_uint4(whi[0], whi[1], whi[2], whi[3]);
-                *reinterpret_cast<uint4 *>(prow + C::kPHalf + off) = make_uint4(wlo[0], wlo[1], wlo[2], wlo[3]);
-            }
-            l += sum;
             // V rows at and past kv in the last tile hold another token's or no
             // data: zero them so that p = 0 there contributes exactly 0.
-            if (tok0 + kPfTile > kv) {
+            if (j * kPfTile + kPfTile > kv) {
                 const int itg = ib + pf_item_v(j, nt);
                 const int stage = itg % C::kStages;
                 if (!pf_wait_all(&bars.full[stage], (itg / C::kStages) & 1, bars, p.err_flag))
                     return;
-                const int r0 = kv - tok0;
-                uint8_t *vb = smem + C::kOffStage + stage * C::kStageBytes + r0 * 128;
-                const int per_chunk = (kPfTile - r0) * 8; // 16-byte pieces
-                for (int i = r; i < per_chunk * C::kChunks; i += kPfRows) {
-                    const int c = i / per_chunk;
-                    *reinterpret_cast<uint4 *>(vb + c * (kPfTile * 128) + (i - c * per_chunk) * 16) =
-                        make_uint4(0u, 0u, 0u, 0u);
+                const int r0 = kv - j * kPfTile;
+                uint8_t *vb = smem + C::kOffStage + stage * C::kStageBytes;
+                // 16-byte pieces of rows r0..63, every 64-column block
+                for (int i = st; i < (kPfTile - r0) * C::kChunks * 8; i += kPfSoftmaxThreads) {
+                    const int piece = i & 7, rest = i >> 3;
+                    const int c = rest % C::kChunks, tt = r0 + rest / C::kChunks;
+                    *reinterpret_cast<uint4 *>(vb + (tt >> 3) * C::kGroupStride + c * 1024 + (tt & 7) * 128 +
+                                               piece * 16) = make_uint4(0u, 0u, 0u, 0u);
                 }
             }
             fence_proxy_async_smem();
             tc_fence_before();
             mbar_arrive(&bars.p_full[gt & 1]);
         }
-        { // epilogue: O / l -> bf16, lse
+        // The next unit's Q, once this unit's S MMAs have read theirs; the MMA
+        // thread meanwhile runs this unit's last PV.
+        if (u_next < n_units) {
+            if (!pf_wait_all(&bars.q_empty, k & 1, bars, p.err_flag))
+                return;
+            tc_fence_after();
+            const int pn = u_next / p.num_kv_heads;
+            pf_load_q<D>(p, p.units[pn], u_next - pn * p.num_kv_heads, r, half, t_row, cl_rank);
+            tc_fence_before();
+            mbar_arrive(&bars.q_full);
+        }
+        { // epilogue: O / l -> bf16 (this half's columns), lse
+            float *xl = xchg + 4 * kPfRows;
+            xl[half * kPfRows + r] = l;
+            if (!pf_pair_sync(bars, quarter, pair_phase, p.err_flag))
+                return;
+            const float lt = l + xl[(1 - half) * kPfRows + r];
+            if (!pf_pair_sync(bars, quarter, pair_phase, p.err_flag)) // both read before the next unit's sums overwrite
+                return;
             const int gl = gt0 + nt - 1;
             if (!pf_wait_all(&bars.o_done[gl & 1], (gl >> 1) & 1, bars, p.err_flag))
                 return;
             tc_fence_after();
-            const float inv = l > 0.f ? 1.f / l : 0.f;
+            const float inv = lt > 0.f ? 1.f / lt : 0.f;
             const int64_t row = (int64_t)(un.q_start + qi) * p.num_q_heads + g * G + h_in_group;
             __nv_bfloat16 *orow = p.out + row * D;
-            for (int c = 0; c < D; c += 32) {
+            for (int c = half * (D / 2); c < (half + 1) * (D / 2); c += 32) {
                 uint32_t rr[32];
                 tmem_ld32(t_row + C::kColO + c, rr);
                 uint32_t w[16];
@@ -501,8 +623,8 @@ __device__ void pf_softmax(const PfParams &p, uint8_t *smem, PfBars &bars, uint3
             }
             tc_fence_before();
             mbar_arrive(&bars.o_free);
-            if (valid && p.lse != nullptr)
-                p.lse[row] = (m_used + log2f(l)) * kLn2;
+            if (half == 0 && valid && p.lse != nullptr)
+                p.lse[row] = (m_used + log2f(lt)) * kLn2;
         }
         gt0 += nt;
         ib += 2 * nt;
@@ -518,26 +640,28 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(pf_smem_raw) + 1023) & ~uintptr_t(1023));
     PfBars &bars = *reinterpret_cast<PfBars *>(smem + C::kOffBar);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int cl_rank = p.cluster > 1 ? (int)cluster_ctarank() : 0;
 
     if (threadIdx.x == 0) {
-        mbar_init(&bars.q_full, 1);
+        mbar_init(&bars.q_full, kPfSoftmaxThreads);
         mbar_init(&bars.q_empty, 1);
         for (int s = 0; s < C::kStages; ++s) {
             mbar_init(&bars.full[s], 1);
-            mbar_init(&bars.empty[s], 1);
+            mbar_init(&bars.empty[s], p.cluster); // released by the MMA of every CTA of the cluster
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&bars.s_full[i], 1);
-            mbar_init(&bars.p_full[i], kPfRows);
+            mbar_init(&bars.p_full[i], kPfSoftmaxThreads);
             mbar_init(&bars.o_done[i], 1);
         }
-        mbar_init(&bars.o_free, kPfRows);
+        mbar_init(&bars.o_free, kPfSoftmaxThreads);
+        for (int i = 0; i < 4; ++i)
+            mbar_init(&bars.pair[i], 64);
         mbar_init(&bars.drain, 1);
         bars.abort = 0;
         mbar_init_fence();
     }
     if (warp == kPfProducerWarp && lane == 0) {
-        prefetch_tensormap(&maps.q);
         prefetch_tensormap(&maps.k);
         prefetch_tensormap(&maps.v);
     }
@@ -546,22 +670,28 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         tmem_relinquish();
     }
     tc_fence_before();
-    __syncthreads();
+    if (p.cluster > 1)
+        cluster_sync(); // peers' barriers are initialised before any multicast reaches them
+    else
+        __syncthreads();
     tc_fence_after();
     const uint32_t tmem = bars.tmem_base;
     const int n_units = *p.n_pairs * p.num_kv_heads;
 
     if (warp == kPfProducerWarp)
-        pf_producer<D>(p, maps, smem, bars, n_units, lane);
+        pf_producer<D>(p, maps, smem, bars, n_units, lane, cl_rank);
     else if (warp == kPfMmaWarp) {
         if (lane == 0)
             pf_mma<D>(p, smem, bars, tmem, n_units);
         __syncwarp();
     } else
-        pf_softmax<D>(p, smem, bars, tmem, n_units, warp, lane);
+        pf_softmax<D>(p, smem, bars, tmem, n_units, warp, lane, cl_rank);
 
     tc_fence_before();
-    __syncthreads();
+    if (p.cluster > 1)
+        cluster_sync(); // no CTA leaves while a peer may still multicast into it
+    else
+        __syncthreads();
     tc_fence_after();
     if (warp == kPfMmaWarp)
         tmem_dealloc(tmem, C::kTmemCols);
@@ -655,10 +785,10 @@ __global__ void __launch_bounds__(kPlanThreads) prefill_plan_kernel(const PfPlan
         __syncthreads();
     }
 
-    // 2. Query tiles per request, prefix sum.
+    // 2. Groups of `cluster` query tiles per request, prefix sum.
     int v = 0;
     if (tid < pp.batch && s_bad[tid] == 0 && s_end[tid] > s_start[tid])
-        v = (s_end[tid] - s_start[tid] + pp.q_tile - 1) / pp.q_tile;
+        v = ((s_end[tid] - s_start[tid] + pp.q_tile - 1) / pp.q_tile + pp.cluster - 1) / pp.cluster;
     int n_pairs = 0;
     const int ex = block_exclusive_scan(v, s_warp, &n_pairs);
     if (tid < pp.batch)
@@ -679,12 +809,18 @@ __global__ void __launch_bounds__(kPlanThreads) prefill_plan_kernel(const PfPlan
         *b_out = lo;
         *t_out = pi - s_scan[lo];
     };
+    // kv tiles of a group: those its last query tile needs
+    auto tiles_of = [&](int b, int t) {
+        const int q = s_end[b] - s_start[b];
+        const int last = min(t * pp.cluster + pp.cluster - 1, (q + pp.q_tile - 1) / pp.q_tile - 1);
+        return pf_tiles(s_kv[b], q, last, pp.q_tile);
+    };
     auto bucket_of = [&](int b, int t) {
-        const int64_t c = pf_tiles(s_kv[b], s_end[b] - s_start[b], t, pp.q_tile);
+        const int64_t c = tiles_of(b, t);
         return (int)(c < kPfBuckets - 1 ? c : kPfBuckets - 1);
     };
 
-    // 3. Counting sort of the query tiles by kv tiles, longest first.
+    // 3. Counting sort of the groups by kv tiles, longest first.
     for (int pi = tid; pi < n_pairs; pi += kPlanThreads) {
         int b, t;
         locate(pi, &b, &t);
@@ -720,7 +856,7 @@ __global__ void __launch_bounds__(kPlanThreads) prefill_plan_kernel(const PfPlan
             un.q_start = s_start[b];
             un.q_len = s_end[b] - s_start[b];
             un.kv_len = s_kv[b];
-            un.n_tiles = (int)pf_tiles(un.kv_len, un.q_len, t, pp.q_tile);
+            un.n_tiles = (int)tiles_of(b, t);
             un.pad0 = un.pad1 = 0;
             pp.units[pos] = un;
         }
@@ -771,21 +907,37 @@ const PfKernelEntry *pf_find(int D)
     return nullptr;
 }
 
-// Persistent grid size: resident CTAs on all SMs (set up once per device).
-int pf_grid(int device, const PfKernelEntry *e)
+// CTAs per cluster that share each K / V tile load (TMA multicast).
+constexpr int kPfCluster = 2;
+
+// Persistent grid size for clusters of `cl` CTAs: every cluster that can be
+// resident at once, in CTAs (set up once per device).
+int pf_grid(int device, const PfKernelEntry *e, int cl)
 {
     constexpr int kDevices = 64;
-    static int cache[kDevices][3] = {};
-    if (device < 0 || device >= kDevices)
-        return 1;
-    int &slot = cache[device][e - kPfTable];
+    static int cache[kDevices][3][5] = {};
+    if (device < 0 || device >= kDevices || cl < 1 || cl > 4)
+        return cl;
+    int &slot = cache[device][e - kPfTable][cl];
     if (slot == 0) {
-        int occ = 1;
-        if (cudaFuncSetAttribute(e->fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)e->smem) != cudaSuccess ||
-            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, e->fn, kPfThreads, e->smem) != cudaSuccess ||
-            occ < 1)
-            occ = 1;
-        slot = sm_count(device) * occ;
+        int n = 0;
+        if (cudaFuncSetAttribute(e->fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)e->smem) == cudaSuccess) {
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3(sm_count(device));
+            cfg.blockDim = dim3(kPfThreads);
+            cfg.dynamicSmemBytes = e->smem;
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeClusterDimension;
+            attr[0].val.clusterDim.x = cl;
+            attr[0].val.clusterDim.y = 1;
+            attr[0].val.clusterDim.z = 1;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            int clusters = 0;
+            if (cudaOccupancyMaxActiveClusters(&clusters, e->fn, &cfg) == cudaSuccess && clusters > 0)
+                n = clusters * cl;
+        }
+        slot = n > 0 ? n : cl;
     }
     return slot;
 }
@@ -843,6 +995,7 @@ cudaError_t launch_prefill(const PrefillArgs &a, const PrefillMaps &maps, cudaSt
     pp.q_tile = a.shape.q_tile;
     pp.num_q_heads = a.num_q_heads;
     pp.head_dim = a.desc.head_dim;
+    pp.cluster = kPfCluster;
     pp.cap_pairs = a.shape.cap_pairs;
     prefill_plan_kernel<<<1, kPlanThreads, 0, stream>>>(pp);
     cudaError_t err = cudaGetLastError();
@@ -850,6 +1003,8 @@ cudaError_t launch_prefill(const PrefillArgs &a, const PrefillMaps &maps, cudaSt
         return err;
 
     PfParams p;
+    p.q = static_cast<const __nv_bfloat16 *>(a.q);
+    p.total_q = a.total_q;
     p.block_table = a.block_table;
     p.units = units;
     p.n_pairs = n_pairs;
@@ -864,27 +1019,36 @@ cudaError_t launch_prefill(const PrefillArgs &a, const PrefillMaps &maps, cudaSt
     p.page_shift = page_shift;
     p.box_shift = page_shift < 6 ? page_shift : 6;
     p.layout = a.desc.layout;
+    p.cluster = kPfCluster;
     p.q_scale = a.q_scale;
     PfMapsDev m;
-    m.q = maps.q;
     m.k = maps.k;
     m.v = maps.v;
 
     int dev = 0;
     if ((err = cudaGetDevice(&dev)) != cudaSuccess)
         return err;
-    int grid = pf_grid(dev, e);
-    const int64_t max_units = a.shape.cap_pairs * a.desc.num_kv_heads;
-    if (grid > max_units)
-        grid = (int)max_units;
-    if (grid < 1)
-        grid = 1;
+    const int cl = kPfCluster;
+    int grid = pf_grid(dev, e, cl);
+    const int64_t max_ctas = a.shape.cap_pairs * a.desc.num_kv_heads * cl; // one unit per cluster at least
+    if (grid > max_ctas)
+        grid = (int)max_ctas;
+    grid = grid / cl * cl;
+    if (grid < cl)
+        grid = cl;
     void *args[] = {&p, &m};
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(kPfThreads);
     cfg.dynamicSmemBytes = e->smem;
     cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = cl;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     return cudaLaunchKernelExC(&cfg, e->fn, args);
 }
 

@@ -88,6 +88,19 @@ __device__ __forceinline__ void tc_mma_bf16(uint32_t d_tmem, uint64_t a_desc, ui
                  : "memory");
 }
 
+// D[tmem] (+)= A[tmem] * B[smem].  A (M = 128) sits in TMEM lanes 0..127, one
+// row per lane, two bf16 per 32-bit column (lower K index in the low half):
+// K = 16 spans 8 columns from `a_tmem`.
+__device__ __forceinline__ void tc_mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                               uint32_t accumulate)
+{
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "setp.ne.b32 p, %4, 0;\n\t"
+                 "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+                 "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+                 : "memory");
+}
+
 // Arrives once on `bar` when every tcgen05.mma this thread issued before has
 // completed (its shared-memory reads and TMEM writes included).
 __device__ __forceinline__ void tc_commit(uint64_t *bar)
@@ -127,6 +140,16 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
                  : "memory");
 }
 
+// Writes 16 consecutive columns of this thread's lane and waits for the write.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16])
+{
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+                 "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};\n\t"
+                 "tcgen05.wait::st.sync.aligned;" ::"r"(taddr),
+                 PKV_W8(0), PKV_W8(8)
+                 : "memory");
+}
+
 #undef PKV_R8
 #undef PKV_W8
 
@@ -144,6 +167,84 @@ __device__ __forceinline__ void tma_load_3d_plain(void *dst, const CUtensorMap *
     asm volatile("cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
                  " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_addr(dst)),
                  "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_addr(bar))
+                 : "memory");
+}
+
+// 4-D and 5-D tiled TMA loads with the default L2 policy.
+__device__ __forceinline__ void tma_load_4d_plain(void *dst, const CUtensorMap *map, int c0, int c1, int c2, int c3,
+                                                  uint64_t *bar)
+{
+    asm volatile("cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes"
+                 " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(smem_addr(dst)),
+                 "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_addr(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void tma_load_5d_plain(void *dst, const CUtensorMap *map, int c0, int c1, int c2, int c3,
+                                                  int c4, uint64_t *bar)
+{
+    asm volatile("cp.async.bulk.tensor.5d.shared::cluster.global.mbarrier::complete_tx::bytes"
+                 " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(smem_addr(dst)),
+                 "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4),
+                 "r"(smem_addr(bar))
+                 : "memory");
+}
+
+// --- thread-block clusters ----------------------------------------------
+
+__device__ __forceinline__ uint32_t cluster_ctarank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// Barrier over every thread of every CTA of the cluster, with release /
+// acquire ordering of shared-memory accesses (mbarrier initialisation
+// included) across the cluster.
+__device__ __forceinline__ void cluster_sync()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Like tc_commit, but arrives on the barrier at the same shared-memory offset
+// in every CTA of the cluster named by `cta_mask`.
+__device__ __forceinline__ void tc_commit_mc(uint64_t *bar, uint16_t cta_mask)
+{
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::
+                     "r"(smem_addr(bar)),
+                 "h"(cta_mask)
+                 : "memory");
+}
+
+// Tiled TMA loads multicast to the same shared-memory offset (data and
+// complete_tx on the barrier at the same offset) in every CTA of `cta_mask`.
+__device__ __forceinline__ void tma_load_3d_mc(void *dst, const CUtensorMap *map, int x, int y, int z, uint64_t *bar,
+                                               uint16_t cta_mask)
+{
+    asm volatile("cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
+                 " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_addr(dst)),
+                 "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_addr(bar)), "h"(cta_mask)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tma_load_4d_mc(void *dst, const CUtensorMap *map, int c0, int c1, int c2, int c3,
+                                               uint64_t *bar, uint16_t cta_mask)
+{
+    asm volatile("cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
+                 " [%0], [%1, {%2, %3, %4, %5}], [%6], %7;" ::"r"(smem_addr(dst)),
+                 "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_addr(bar)),
+                 "h"(cta_mask)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tma_load_5d_mc(void *dst, const CUtensorMap *map, int c0, int c1, int c2, int c3,
+                                               int c4, uint64_t *bar, uint16_t cta_mask)
+{
+    asm volatile("cp.async.bulk.tensor.5d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
+                 " [%0], [%1, {%2, %3, %4, %5, %6}], [%7], %8;" ::"r"(smem_addr(dst)),
+                 "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4),
+                 "r"(smem_addr(bar)), "h"(cta_mask)
                  : "memory");
 }
 
