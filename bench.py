@@ -39,15 +39,29 @@ METRIC = "paged decode KV-read GB/s (% of HBM peak) and decode tok/s per attn la
 HQ, HKV, D, P = 32, 8, 128, 128
 DECODE_CAPACITY = 512
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_kernel_traffic.txt")
+PREFILL_PROFILE_FILE = os.path.join(ROOT, "profiles", "prefill_kernel_counters.txt")
+
+
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 
 
 def peaks():
     try:
-        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+        with open(PEAKS_FILE) as f:
             m = json.load(f)
         return float(m["hbm_gbs"]), "measured"
     except Exception:
         return 6800.0, "fallback"
+
+
+def tensor_peak():
+    """Dense bf16 TFLOP/s for a kernel timed alone (measured burst, else the
+    fallback figure)."""
+    try:
+        with open(PEAKS_FILE) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured bf16 burst (cuBLAS)"
+    except Exception:
+        return 1900.0, "fallback"
 
 
 def call_bytes(lens: np.ndarray, batch: int) -> int:
@@ -68,6 +82,91 @@ def source_hash() -> str:
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()
+
+
+def prefill_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "paged_kv_decode_append_gb300", "csrc")
+    for name in ("pkv_prefill.cu", "pkv_tcgen05.cuh", "pkv_device.cuh", "pkv_internal.h"):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def recorded_prefill_profile():
+    """Tensor-pipe share and DRAM bytes of the prefill kernel from the
+    committed ncu summary, if it was taken on the current kernel source."""
+    try:
+        rec = {}
+        with open(PREFILL_PROFILE_FILE) as f:
+            for line in f:
+                if ":" in line and not line.startswith("#"):
+                    k, v = line.split(":", 1)
+                    rec[k.strip()] = v.strip()
+        if rec.get("source_sha256") != prefill_source_hash():
+            return None
+        return {"tensor_pipe_pct": float(rec["tensor_pipe_pct"]), "dram_bytes": float(rec["dram_bytes"])}
+    except Exception:
+        return None
+
+
+def prefill_bench(dev, reps: int):
+    """The ragged causal prefill workload (B=8, Hq=48, Hkv=6, D=256, page 16
+    HND): one pkv_prefill_attn call per timed iteration (plan + kernel), CUDA
+    events around it, L2 flushed by a 512 MiB write before each call."""
+    import paged_kv_decode_append_gb300 as pkv
+    from paged_kv_decode_append_gb300 import workloads as wl
+
+    case = wl.ragged_prefill(device=dev)
+    q = case.q
+    T, Hq, Dh = q.shape
+    qo = torch.as_tensor(case.qo_indptr, device=dev)
+    kvl = torch.as_tensor(case.kv_lens, device=dev)
+    btp = torch.as_tensor(case.block_table, device=dev)
+    out = torch.empty_like(q)
+    lse = torch.empty((T, Hq), dtype=torch.float32, device=dev)
+    ws = pkv.prefill_workspace(case.batch, T, Hq, pkv.cache_desc(case.k_cache, case.layout), dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    ql = np.diff(case.qo_indptr).astype(np.int64)
+    kv = case.kv_lens.astype(np.int64)
+    pairs = Hq * int((ql * (2 * kv - ql + 1) // 2).sum())  # visited (query, key, head) triples
+    flops = 4 * Dh * pairs
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def call():
+        pkv.pkv_prefill_attn(case.k_cache, case.v_cache, q, qo, kvl, btp, case.softmax_scale, out=out, lse=lse,
+                             workspace=ws, err_flag=err, layout=case.layout)
+
+    for _ in range(3):
+        call()
+    torch.cuda.synchronize(dev)
+    times = []
+    for _ in range(reps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        call()
+        b.record(stream)
+        b.synchronize()
+        times.append(a.elapsed_time(b))
+    if int(err.item()) != 0:
+        raise RuntimeError(f"prefill reported error bits {int(err.item())}")
+    times = np.array(times)
+    ms = float(np.median(times))
+    tflops = flops / (ms * 1e-3) / 1e12
+    peak, peak_kind = tensor_peak()
+    prof = recorded_prefill_profile()
+    return {
+        "workload": "ragged causal paged prefill: B=8, Hq=48, Hkv=6, D=256, page 16 HND, "
+                    f"q_len {ql.min()}..{ql.max()}, kv_len {kv.min()}..{kv.max()} (seed 4)",
+        "tflops": tflops, "unit": "TFLOP/s", "peak": peak, "peak_kind": peak_kind,
+        "frac": tflops / peak, "ms_median": ms, "ms_best": float(times.min()), "reps": reps,
+        "flops": flops, "pairs": pairs, "flops_formula": "4 * head_dim * causal pairs",
+        "launches_per_call": 2, "l2": "flushed between calls (512 MiB write)",
+        "tensor_pipe_pct": None if prof is None else prof["tensor_pipe_pct"],
+        "dram_bytes_per_call": None if prof is None else prof["dram_bytes"],
+    }
 
 
 def recorded_traffic():
@@ -282,6 +381,9 @@ def main():
     ap.add_argument("--layout", default="shuffled", choices=["shuffled", "contiguous"])
     ap.add_argument("--e2e-steps", type=int, default=100)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--prefill-reps", type=int, default=20, help="timed prefill calls (0 = skip)")
+    ap.add_argument("--prefill-only", action="store_true",
+                    help="run only the prefill measurement on cuda:0 and print its JSON object")
     ap.add_argument("--no-overlap", action="store_true",
                     help="plain launches instead of programmatic dependent launch between layers")
     args = ap.parse_args()
@@ -289,6 +391,11 @@ def main():
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
         run_reference(args)
+        return
+    if args.prefill_only:
+        dev = torch.device("cuda:0")
+        torch.cuda.set_device(dev)
+        print(json.dumps({"prefill": prefill_bench(dev, max(args.prefill_reps, 1))}))
         return
 
     import paged_kv_decode_append_gb300 as pkv
@@ -420,6 +527,8 @@ def main():
     e2e_value = e_all / (e_ms * 1e-3) / 1e9
     del e_graphs
 
+    prefill = prefill_bench(dev, args.prefill_reps) if args.prefill_reps > 0 else None
+
     if rank != 0:
         return
     cpu = None
@@ -446,6 +555,7 @@ def main():
         "launch": "one CUDA graph per decode step (36 kernel launches" + (
             ")" if args.no_overlap else ", programmatic dependent launch between them)"),
         "cpu_baseline": cpu,
+        "prefill": prefill,
     }
     print(json.dumps(out))
 
