@@ -320,7 +320,10 @@ def cpu_baseline(sw, prompt_lens: np.ndarray, budget_s: float = 12.0, max_steps:
 
 
 def run_reference(args):
+    """The reference arm: the fp64 oracle timed on the host cores.  Under a
+    multi-rank launch rank 0 alone runs and prints; the others exit at once."""
     rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
     if rank != 0:
         return
     import oracle
@@ -351,7 +354,7 @@ def run_reference(args):
     total_t = float(sum(times))
     value = sum(nbytes) / total_t / 1e9
     out = {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": 1, "steps": args.steps,
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": 1e3 * total_t / len(times), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": workload_config(args),
