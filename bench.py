@@ -64,14 +64,14 @@ def tensor_peak():
         return 1900.0, "fallback"
 
 
-def call_bytes(lens: np.ndarray, batch: int) -> int:
+def call_bytes(lens: np.ndarray, batch: int, page_size: int = P) -> int:
     """Algorithmic bytes of one fused append + decode call (one layer):
     cached K/V read + q read + out write + new K/V read + append write +
     block-table entries read + seqlens read."""
     kv_read = int(lens.sum()) * 2 * HKV * D * 2
     q_out = 2 * batch * HQ * D * 2
     new_tok = 2 * batch * 2 * HKV * D * 2
-    table = 4 * int(((lens + 1 + P - 1) // P).sum())
+    table = 4 * int(((lens + 1 + page_size - 1) // page_size).sum())
     return kv_read + q_out + new_tok + table + 4 * batch
 
 
@@ -314,7 +314,20 @@ def cpu_baseline(sw, prompt_lens: np.ndarray, budget_s: float = 12.0, max_steps:
             if elapsed >= budget_s:
                 break
         step += 1
+    # the same oracle on one host thread, over the first layers of step 0
+    lens0 = prompt_lens.astype(np.int32)
+    inputs0 = wl.sweep_step_inputs(sw, 0, dev, layers=4)
+    one_bytes, one_t = 0, 0.0
+    for layer in range(4):
+        q, kn, vn = (wl.bits(t) for t in inputs0[layer])
+        k, v, bt = host[layer]
+        t0 = time.perf_counter()
+        oracle.decode(d, k, v, q, kn, vn, bt, lens0, sw.softmax_scale, nthreads=1)
+        one_t += time.perf_counter() - t0
+        one_bytes += call_bytes(lens0, sw.batch)
     return {"value": done_bytes / elapsed / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "single_thread_value": one_bytes / one_t / 1e9,
+            "single_thread_sample": "layers 0..3 of decode step 0, one host thread",
             "sample": f"{calls} layer calls (decode steps 0..{step - 1} of the 36-layer B={sw.batch} workload, all "
                       f"rows and heads), fp64 oracle with OpenMP over (row, head), {elapsed:.1f} s of oracle time"}
 
@@ -365,6 +378,63 @@ def run_reference(args):
     print(json.dumps(out))
 
 
+def single_layer_bench(kind: str, reps: int, warmup: int):
+    """One fused append + decode call per timed iteration on the Qwen3-4B-shaped
+    layer (B=32, page 16, lengths U[512,1024]) or the skewed batch (B=64, one
+    32,768-token row), CUDA events around each call, L2 flushed by a 512 MiB
+    write before it (a call reads 0.1-0.4 GB, about L2's size).  Prints one
+    JSON line in the main line's format."""
+    import paged_kv_decode_append_gb300 as pkv
+    from paged_kv_decode_append_gb300 import workloads as wl
+
+    dev = torch.device("cuda:0")
+    torch.cuda.set_device(dev)
+    case = (wl.qwen3_decode if kind == "qwen3" else wl.skewed_decode)(device=dev)
+    B, Hq, Dh = case.q.shape
+    bt = torch.as_tensor(case.block_table, device=dev)
+    lens = torch.as_tensor(case.cache_seqlens, device=dev)
+    out = torch.empty_like(case.q)
+    ws = pkv.decode_workspace(B, case.max_blocks, Hq, pkv.cache_desc(case.k_cache, case.layout), dev)
+    nbytes = call_bytes(case.cache_seqlens.astype(np.int64), B, case.page_size)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def call():
+        # the same slot is appended to every time (cache_seqlens is not advanced)
+        pkv.pkv_decode_attn(case.k_cache, case.v_cache, case.q, case.k_new, case.v_new, bt, lens,
+                            case.softmax_scale, out=out, workspace=ws, layout=case.layout)
+
+    for _ in range(warmup):
+        call()
+    torch.cuda.synchronize(dev)
+    times = []
+    with ClockSampler(0) as clocks:
+        for _ in range(reps):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            call()
+            b.record(stream)
+            b.synchronize()
+            times.append(a.elapsed_time(b))
+    times = np.array(times)
+    ms = float(np.median(times))
+    value = nbytes / (ms * 1e-3) / 1e9
+    peak, peak_kind = peaks()
+    name = ("Qwen3-4B-shaped layer decode: B=32, Hq=32, Hkv=8, D=128, page 16, lengths U[512,1024], 65,536-page "
+            "shuffled pool" if kind == "qwen3" else
+            "skewed-length decode: B=64, Hq=32, Hkv=8, D=128, page 16, one 32,768-token row, others "
+            "clip(lognormal(6.5,0.8),128,4096), 65,536-page shuffled pool")
+    print(json.dumps({
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": 1, "steps": reps, "warmup": warmup,
+        "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": name, "batch": B, "l2": "flushed between calls (512 MiB write)"},
+        "pct_of_hbm_peak": 100.0 * value / peak, "decode_tok_s_per_attn_layer": B / (ms * 1e-3),
+        "ms_best": float(times.min()), "algorithmic_bytes_per_call": nbytes, "peak": peak, "peak_kind": peak_kind,
+        "clocks": clocks.summary(), "gpu_launches": reps}))
+
+
 def workload_config(args):
     return {"workload": f"paged decode batch sweep B={args.batch} (Qwen3-4B-shaped: Hq=32, Hkv=8, D=128), "
                         f"page 128, {args.layout} pages, prompt U[64,512] + decode steps, 36 layer caches per step",
@@ -387,6 +457,8 @@ def main():
     ap.add_argument("--prefill-reps", type=int, default=20, help="timed prefill calls (0 = skip)")
     ap.add_argument("--prefill-only", action="store_true",
                     help="run only the prefill measurement on cuda:0 and print its JSON object")
+    ap.add_argument("--workload", default="sweep", choices=["sweep", "qwen3", "skewed"],
+                    help="sweep: the 36-layer batch sweep (default); qwen3 / skewed: one layer, timed per call")
     ap.add_argument("--no-overlap", action="store_true",
                     help="plain launches instead of programmatic dependent launch between layers")
     args = ap.parse_args()
@@ -394,6 +466,10 @@ def main():
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
         run_reference(args)
+        return
+    if args.workload != "sweep":
+        reps = 50 if args.steps == ap.get_default("steps") else args.steps
+        single_layer_bench(args.workload, reps, args.warmup)
         return
     if args.prefill_only:
         dev = torch.device("cuda:0")
@@ -421,7 +497,9 @@ def main():
     step_bytes = [L * call_bytes(lens_all[s], B) for s in range(DECODE_CAPACITY)]
     stream = torch.cuda.current_stream(dev)
 
-    flags = 0 if args.no_overlap else pkv.api.DECODE_OVERLAP_PROLOGUE
+    # layers of one step read different caches: the next layer may stream its
+    # K/V while the previous one finishes
+    flags = 0 if args.no_overlap else pkv.api.DECODE_OVERLAP_PROLOGUE | pkv.api.DECODE_EARLY_KV
 
     def layer_call(step, layer, q, kn, vn):
         pkv.pkv_decode_attn(sw.k_caches[layer], sw.v_caches[layer], q, kn, vn, bt, lens_dev[step % DECODE_CAPACITY],
@@ -493,6 +571,20 @@ def main():
     iso_gbs = float(np.sum(iso_bytes) / (iso_ms.sum() * 1e-3) / 1e9)
     del iso_ev
 
+    # Without graphs: the same steps as plain stream launches (36 per step).
+    eager_steps = min(20, args.steps)
+    torch.cuda.synchronize(dev)
+    ea, eb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    eager_bytes = 0
+    ea.record(stream)
+    for s in range(args.warmup, args.warmup + eager_steps):
+        for layer, (q, kn, vn) in enumerate(inputs[s % ring]):
+            layer_call(s, layer, q, kn, vn)
+        eager_bytes += step_bytes[s % DECODE_CAPACITY]
+    eb.record(stream)
+    torch.cuda.synchronize(dev)
+    eager_gbs = eager_bytes / (ea.elapsed_time(eb) * 1e-3) / 1e9
+
     # End to end through the public API: each step copies its q / k_new / v_new
     # for all layers from pinned host memory, runs the 36 calls and copies the
     # outputs back (one graph per step, like the timed region).
@@ -554,9 +646,11 @@ def main():
         "clocks": clocks.summary(),
         "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "steps": e2e_steps},
+        "eager": {"value": eager_gbs, "unit": "GB/s", "steps": eager_steps,
+                  "launch": "plain stream launches, no CUDA graph"},
         "gpu_launches": n_ev,
         "launch": "one CUDA graph per decode step (36 kernel launches" + (
-            ")" if args.no_overlap else ", programmatic dependent launch between them)"),
+            ")" if args.no_overlap else ", programmatic dependent launch between them, K/V streamed early)"),
         "cpu_baseline": cpu,
         "prefill": prefill,
     }

@@ -174,6 +174,16 @@ PKV_API pkv_status pkv_decode_attn(const pkv_cache_desc *desc, void *k_cache, vo
  * or block_table (for instance the layers of one decode step, which share
  * them).  Capturable in CUDA graphs. */
 
+#define PKV_DECODE_EARLY_KV 2u
+/* Only together with PKV_DECODE_OVERLAP_PROLOGUE: the kernel also streams the
+ * cached K/V (the tokens below cache_seqlens) before the preceding kernel has
+ * completed, so a layer's cache reads overlap the end of the previous kernel.
+ * q, k_new, v_new and every output (out, lse, the appended token, err_flag)
+ * still wait for it.  Use it when the immediately preceding kernel in the
+ * stream does not write this call's cache pages -- for instance the
+ * projection producing q / k_new / v_new, or the attention of another layer.
+ * Capturable in CUDA graphs. */
+
 /*
  * pkv_decode_attn_ex -- pkv_decode_attn with launch flags (PKV_DECODE_*).
  * flags = 0 behaves exactly like pkv_decode_attn.

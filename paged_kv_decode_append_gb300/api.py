@@ -17,7 +17,8 @@ NHD = 0
 HND = 1
 
 OK, EINVAL, EUNSUPPORTED, ECUDA, ENOPAGES, EWORKSPACE, ETOOBIG = range(7)
-DECODE_OVERLAP_PROLOGUE = 1  # pkv_decode_attn_ex flag (see include/pkv.h)
+DECODE_OVERLAP_PROLOGUE = 1  # pkv_decode_attn_ex flags (see include/pkv.h)
+DECODE_EARLY_KV = 2
 ERR_PAGE, ERR_OVERFLOW, ERR_TIMEOUT, ERR_QLEN = 1, 2, 4, 8
 
 

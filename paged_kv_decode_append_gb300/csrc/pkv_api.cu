@@ -251,7 +251,9 @@ pkv_status pkv_decode_attn_ex(const pkv_cache_desc *desc, void *k_cache, void *v
                               void *out, float *lse, void *workspace, size_t workspace_bytes, int32_t *err_flag,
                               void *stream, uint32_t flags)
 {
-    if ((flags & ~PKV_DECODE_OVERLAP_PROLOGUE) != 0)
+    if ((flags & ~(PKV_DECODE_OVERLAP_PROLOGUE | PKV_DECODE_EARLY_KV)) != 0)
+        return PKV_EINVAL;
+    if ((flags & PKV_DECODE_EARLY_KV) && !(flags & PKV_DECODE_OVERLAP_PROLOGUE))
         return PKV_EINVAL;
     const pkv_status st = check_desc(desc);
     if (st != PKV_OK)

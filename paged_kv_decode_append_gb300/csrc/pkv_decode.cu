@@ -75,7 +75,8 @@ struct KParams {
     int batch, num_q_heads, num_kv_heads, group, n_sub, units, max_blocks;
     int page_size, page_shift, num_pages, layout, box_tokens;
     int with_new, swizzle;
-    int pdl; // launched with programmatic dependent launch
+    int pdl;      // launched with programmatic dependent launch
+    int early_kv; // ... and the K/V cache may be read before the preceding grid completes
     float q_scale;
 };
 
@@ -380,7 +381,11 @@ __device__ void producer(const KParams &p, Smem<D, GC> &sm, const DecodeMaps *ma
     int win = have ? load_window(p.block_table + (int64_t)sg.b * p.max_blocks, sg.tok0 >> p.page_shift,
                                  (sg.tok1 - 1) >> p.page_shift, lane)
                    : 0;
-    wait_prior_grid(p); // page ids are loading; K/V and the error flag come after
+    // Page ids are loading.  K/V come after the preceding grid unless the
+    // caller declared that it does not write this call's cache; the error
+    // flag always does (below).
+    if (!p.early_kv)
+        wait_prior_grid(p);
     while (have && !*abort) {
         const int32_t *bt_row = p.block_table + (int64_t)sg.b * p.max_blocks;
         const int last_pg = (sg.tok1 - 1) >> p.page_shift;
@@ -451,8 +456,10 @@ __device__ void producer(const KParams &p, Smem<D, GC> &sm, const DecodeMaps *ma
                     }
                 }
             }
-            if (lane == 0 && bad)
+            if (lane == 0 && bad) {
+                wait_prior_grid(p);
                 set_error(p.err_flag, PKV_ERR_PAGE);
+            }
             __syncwarp();
             if (t == 0) { // next slice and its first page window, off the first tile's critical path
                 more = si.next(p, sm, nx);
@@ -1269,6 +1276,7 @@ cudaError_t launch_decode(const DecodeArgs &a, const DecodeMaps &maps, cudaStrea
     p.with_new = (a.k_new != nullptr) ? 1 : 0;
     p.swizzle = decode_swizzle(a.desc.page_size);
     p.pdl = (a.flags & PKV_DECODE_OVERLAP_PROLOGUE) ? 1 : 0;
+    p.early_kv = (a.flags & PKV_DECODE_EARLY_KV) ? 1 : 0;
     p.q_scale = a.q_scale;
     void *args[] = {&p, const_cast<DecodeMaps *>(&maps)};
     cudaLaunchConfig_t cfg = {};

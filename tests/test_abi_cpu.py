@@ -153,6 +153,17 @@ def test_decode_argument_errors_return_before_any_launch():
     assert _decode(lib, d, batch=2000) == pkv.api.EUNSUPPORTED
 
 
+def test_decode_flags():
+    lib = _lib.load()
+    d = CacheDesc(64, 16, 2, 128, 0)
+    args = (ctypes.byref(d), FAKE, FAKE, FAKE, None, None, FAKE, 4, FAKE, 0, 8, 0.1, FAKE, None, FAKE, 1 << 30,
+            None, None)
+    assert lib.pkv_decode_attn_ex(*args, pkv.api.DECODE_OVERLAP_PROLOGUE) == pkv.api.OK
+    assert lib.pkv_decode_attn_ex(*args, pkv.api.DECODE_OVERLAP_PROLOGUE | pkv.api.DECODE_EARLY_KV) == pkv.api.OK
+    assert lib.pkv_decode_attn_ex(*args, pkv.api.DECODE_EARLY_KV) == pkv.api.EINVAL  # needs the overlap launch
+    assert lib.pkv_decode_attn_ex(*args, 4) == pkv.api.EINVAL                        # unknown flag
+
+
 def test_append_argument_errors():
     lib = _lib.load()
     d = CacheDesc(64, 16, 2, 128, 0)

@@ -225,8 +225,9 @@ def test_large_batch_limit():
 @pytest.mark.parametrize("graph", [False, True])
 def test_overlap_prologue_launch_is_bit_identical(graph):
     """Back-to-back layers sharing one workspace, launched with programmatic
-    dependent launch (eagerly and inside a CUDA graph), give the same bits as
-    plain launches."""
+    dependent launch -- alone, and with the K/V stream started before the
+    preceding kernel completes -- eagerly and inside a CUDA graph, give the
+    same bits as plain launches."""
     layers = 3
     sw = wl.batch_sweep(32, device=DEV, contiguous=False, layers=layers)
     bt = torch.as_tensor(sw.block_table, device=DEV)
@@ -234,7 +235,8 @@ def test_overlap_prologue_launch_is_bit_identical(graph):
     desc = pkv.cache_desc(sw.k_caches[0])
     ins = wl.sweep_step_inputs(sw, 0, DEV)
     results = []
-    for flags in (0, pkv.api.DECODE_OVERLAP_PROLOGUE):
+    flag_sets = (0, pkv.api.DECODE_OVERLAP_PROLOGUE, pkv.api.DECODE_OVERLAP_PROLOGUE | pkv.api.DECODE_EARLY_KV)
+    for flags in flag_sets:
         kc = [k.clone() for k in sw.k_caches]
         vc = [v.clone() for v in sw.v_caches]
         ws = pkv.decode_workspace(32, sw.max_blocks, 32, desc, DEV)
@@ -255,10 +257,11 @@ def test_overlap_prologue_launch_is_bit_identical(graph):
             step()
         torch.cuda.synchronize()
         results.append((outs, lses, kc, vc))
-    (o0, l0, k0, v0), (o1, l1, k1, v1) = results
-    for layer in range(layers):
-        assert torch.isfinite(o0[layer].float()).all()
-        assert torch.equal(o0[layer].view(torch.int16), o1[layer].view(torch.int16))
-        assert torch.equal(l0[layer].view(torch.int32), l1[layer].view(torch.int32))
-        assert torch.equal(k0[layer].view(torch.int16), k1[layer].view(torch.int16))
-        assert torch.equal(v0[layer].view(torch.int16), v1[layer].view(torch.int16))
+    o0, l0, k0, v0 = results[0]
+    for o1, l1, k1, v1 in results[1:]:
+        for layer in range(layers):
+            assert torch.isfinite(o0[layer].float()).all()
+            assert torch.equal(o0[layer].view(torch.int16), o1[layer].view(torch.int16))
+            assert torch.equal(l0[layer].view(torch.int32), l1[layer].view(torch.int32))
+            assert torch.equal(k0[layer].view(torch.int16), k1[layer].view(torch.int16))
+            assert torch.equal(v0[layer].view(torch.int16), v1[layer].view(torch.int16))
