@@ -80,15 +80,17 @@ struct KParams {
     float q_scale;
 };
 
-template <int D>
+// K/V stages in flight per CTA, as many as keep two CTAs on an SM (head_dim
+// 128 with up to 4 heads per CTA: 5 stages, about 107 KB).
+template <int D, int GC>
 constexpr int stages_for()
 {
-    return D == 256 ? 3 : (D == 128 ? 4 : 6);
+    return D == 256 ? 3 : (D == 128 ? (GC <= 4 ? 5 : 4) : 6);
 }
 
 template <int D, int GC>
 struct Smem {
-    static constexpr int kStages = stages_for<D>();
+    static constexpr int kStages = stages_for<D, GC>();
     // [stage][K|V] tiles laid out [D/64][kTile][64] (128-byte rows, TMA
     // SWIZZLE_128B when the page size allows 8-row boxes)
     __nv_bfloat16 kv[kStages][2][kTile * D];
@@ -1140,6 +1142,10 @@ size_t smem_bytes()
 {
     return sizeof(Smem<D, GC>) + 1024;
 }
+
+// Two CTAs per SM: 228 KB of shared memory per SM, 1 KB of it reserved per CTA.
+static_assert(sizeof(Smem<128, 4>) + 1024 + 1024 <= 228 * 1024 / 2, "decode<128,4> must fit twice on an SM");
+static_assert(sizeof(Smem<128, 8>) + 1024 + 1024 <= 228 * 1024 / 2, "decode<128,8> must fit twice on an SM");
 
 struct KernelEntry {
     int D, GC;
