@@ -308,14 +308,20 @@ pkv_status pkv_decode_attn_ex(const pkv_cache_desc *desc, void *k_cache, void *v
     a.flags = flags;
 
     const int box = decode_box_tokens(desc->page_size);
-    const int small = box > kDecodeSmallBox ? kDecodeSmallBox : box;
-    const int swz = decode_swizzle(desc->page_size);
     DecodeMaps maps;
-    if (encode_pool_map(&maps.k, *desc, k_cache, box, 64, swz) != CUDA_SUCCESS ||
-        encode_pool_map(&maps.v, *desc, v_cache, box, 64, swz) != CUDA_SUCCESS ||
-        encode_pool_map(&maps.k8, *desc, k_cache, small, 64, swz) != CUDA_SUCCESS ||
-        encode_pool_map(&maps.v8, *desc, v_cache, small, 64, swz) != CUDA_SUCCESS)
-        return PKV_ECUDA;
+    if (decode_swizzle(desc->page_size)) { // pages of 8+ tokens: token-group boxes
+        if (encode_group_map(&maps.k, *desc, k_cache, box) != CUDA_SUCCESS ||
+            encode_group_map(&maps.v, *desc, v_cache, box) != CUDA_SUCCESS ||
+            encode_group_map(&maps.k8, *desc, k_cache, kDecodeSmallBox) != CUDA_SUCCESS ||
+            encode_group_map(&maps.v8, *desc, v_cache, kDecodeSmallBox) != CUDA_SUCCESS)
+            return PKV_ECUDA;
+    } else { // pages of 1, 2 or 4 tokens: unswizzled 64-column boxes
+        if (encode_pool_map(&maps.k, *desc, k_cache, box, 64, 0) != CUDA_SUCCESS ||
+            encode_pool_map(&maps.v, *desc, v_cache, box, 64, 0) != CUDA_SUCCESS)
+            return PKV_ECUDA;
+        maps.k8 = maps.k;
+        maps.v8 = maps.v;
+    }
     return launch_decode(a, maps, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PKV_OK : PKV_ECUDA;
 }
 

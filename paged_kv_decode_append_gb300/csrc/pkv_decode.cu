@@ -436,24 +436,33 @@ __device__ void producer(const KParams &p, Smem<D, GC> &sm, const DecodeMaps *ma
                         y = slot;
                         z = page * p.num_kv_heads + sg.kvh;
                     }
-                    // one 64-column box per 128-byte half row: [D/64][kTile][64]
-                    if (bx < nfull) {
+                    // A stage is [kTile / 8 token groups][D / 64 column blocks][8 rows][64]
+                    // (group_off: element offset of token row `row`'s group).
+                    auto group_off = [](int row) { return (row >> 3) * (8 * D); };
+                    if (p.swizzle) { // token-group boxes: all of head_dim for box (or 8) tokens at once
+                        if (bx < nfull) {
+                            const int off = group_off(bx * box);
+                            const int c3 = p.layout == PKV_NHD ? (page * p.page_size + slot) >> 3 : slot >> 3;
+                            const int c4 = p.layout == PKV_NHD ? sg.kvh : page * p.num_kv_heads + sg.kvh;
+                            tma_load_5d(sm.kv[s][0] + off, &maps->k, 0, 0, 0, c3, c4, &sm.full[s], policy);
+                            tma_load_5d(sm.kv[s][1] + off, &maps->v, 0, 0, 0, c3, c4, &sm.full[s], policy);
+                        } else { // the slice ends inside this box: 8-token groups up to its end
+                            for (int r = 0; r < tail_rows; r += kDecodeSmallBox) {
+                                const int off = group_off(bx * box + r);
+                                const int c3 = p.layout == PKV_NHD ? (page * p.page_size + slot + r) >> 3
+                                                                   : (slot + r) >> 3;
+                                const int c4 = p.layout == PKV_NHD ? sg.kvh : page * p.num_kv_heads + sg.kvh;
+                                tma_load_5d(sm.kv[s][0] + off, &maps->k8, 0, 0, 0, c3, c4, &sm.full[s], policy);
+                                tma_load_5d(sm.kv[s][1] + off, &maps->v8, 0, 0, 0, c3, c4, &sm.full[s], policy);
+                            }
+                        }
+                    } else { // pages of 1, 2 or 4 tokens: 64-column boxes inside one token group
+                        const int row = bx * box;
 #pragma unroll
                         for (int h = 0; h < D / 64; ++h) {
-                            const int off = (h * kTile + bx * box) * 64;
+                            const int off = group_off(row) + h * 512 + (row & 7) * 64;
                             tma_load_3d(sm.kv[s][0] + off, &maps->k, 64 * h, y, z, &sm.full[s], policy);
                             tma_load_3d(sm.kv[s][1] + off, &maps->v, 64 * h, y, z, &sm.full[s], policy);
-                        }
-                    } else { // the slice ends inside this box
-                        for (int r = 0; r < tail_rows; r += kDecodeSmallBox) {
-                            const int yr = p.layout == PKV_NHD ? y : y + r;
-                            const int zr = p.layout == PKV_NHD ? z + r : z;
-#pragma unroll
-                            for (int h = 0; h < D / 64; ++h) {
-                                const int off = (h * kTile + bx * box + r) * 64;
-                                tma_load_3d(sm.kv[s][0] + off, &maps->k8, 64 * h, yr, zr, &sm.full[s], policy);
-                                tma_load_3d(sm.kv[s][1] + off, &maps->v8, 64 * h, yr, zr, &sm.full[s], policy);
-                            }
                         }
                     }
                 }
@@ -533,12 +542,14 @@ __device__ __forceinline__ float2 unpack_bf16(uint32_t w)
 }
 
 // Shared-memory byte address of the 16-byte chunk `chunk` (0..D/8-1) of token
-// row `row` in a [D/64][kTile][64] tile; with swz = 7 the 128-byte rows are
-// stored TMA SWIZZLE_128B style (chunk index XOR row % 8).
+// row `row` in a [kTile/8][D/64][8][64] tile (8-token groups, each 8 rows of
+// every 64-column block); with swz = 7 the 128-byte rows are stored TMA
+// SWIZZLE_128B style (chunk index XOR row % 8).
+template <int D>
 __device__ __forceinline__ uint32_t tile_addr(uint32_t base, int row, int chunk, int swz)
 {
-    const int half = chunk >> 3, c = chunk & 7;
-    return base + (uint32_t)((half * kTile + row) * 128 + ((c ^ (row & swz)) << 4));
+    const int blk = chunk >> 3, c = chunk & 7;
+    return base + (uint32_t)((((row >> 3) * (D / 64) + blk) * 8 + (row & 7)) * 128 + ((c ^ (row & swz)) << 4));
 }
 
 template <int D, bool MASKED>
@@ -555,8 +566,8 @@ __device__ __forceinline__ void consume_tile(const __nv_bfloat16 *Kt, __nv_bfloa
         const int first = nv > row0 ? nv : row0;
         for (int i = lane; i < (row0 + 16 - first) * (D / 8); i += 32) {
             const int r = first + i / (D / 8), chunk = i % (D / 8);
-            *reinterpret_cast<uint4 *>(Vt + ((chunk >> 3) * kTile + r) * 64 + (chunk & 7) * 8) =
-                make_uint4(0u, 0u, 0u, 0u);
+            *reinterpret_cast<uint4 *>(Vt + (((r >> 3) * (D / 64) + (chunk >> 3)) * 8 + (r & 7)) * 64 +
+                                       (chunk & 7) * 8) = make_uint4(0u, 0u, 0u, 0u);
         }
         __syncwarp();
     }
@@ -566,7 +577,7 @@ __device__ __forceinline__ void consume_tile(const __nv_bfloat16 *Kt, __nv_bfloa
 #pragma unroll
     for (int ks = 0; ks < KS; ++ks) {
         uint32_t a[4];
-        ldsm_x4(tile_addr(kbase, krow, 2 * ks + (lane >> 4), swz), a);
+        ldsm_x4(tile_addr<D>(kbase, krow, 2 * ks + (lane >> 4), swz), a);
         if (ks & 1)
             mma_16816(sb, a, qf[ks][0], qf[ks][1]);
         else
@@ -627,7 +638,7 @@ __device__ __forceinline__ void consume_tile(const __nv_bfloat16 *Kt, __nv_bfloa
 #pragma unroll
     for (int mt = 0; mt < KS; ++mt) {
         uint32_t a[4];
-        ldsm_x4_trans(tile_addr(vbase, vrow, 2 * mt + vchunk, swz), a);
+        ldsm_x4_trans(tile_addr<D>(vbase, vrow, 2 * mt + vchunk, swz), a);
         mma_16816(acc[mt], a, bh0, bh1);
         mma_16816(acc[mt], a, bl0, bl1);
     }

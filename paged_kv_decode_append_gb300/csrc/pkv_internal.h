@@ -65,7 +65,9 @@ struct DecodeArgs {
 };
 
 // TMA descriptors of one decode call: K and V pools with full boxes
-// (decode_box_tokens rows) and with 8-row boxes for the ragged end of a slice.
+// (decode_box_tokens rows) and with 8-row boxes for the ragged end of a slice
+// -- token-group maps (encode_group_map) for pages of 8 tokens or more,
+// unswizzled 64-column boxes (encode_pool_map, no 8-row maps) below that.
 struct DecodeMaps {
     CUtensorMap k, v, k8, v8;
 };

@@ -114,6 +114,50 @@ def test_batch_sweep_steps(batch, contiguous):
         assert hashlib.sha256(host_v[layer].tobytes()).hexdigest() == _sha(sw.v_caches[layer])
 
 
+@pytest.mark.parametrize("batch,contiguous", [(8, False), (16, True), (32, False), (64, True), (128, False),
+                                              (256, True)])
+def test_batch_sweep_full_cycle(batch, contiguous):
+    """All 512 decode steps of the sweep on two layer caches: outputs against
+    the oracle at steps 0, 255 and 511 (on compact host copies of the GPU's
+    cache at that step), and every one of the 512 appended tokens of every row
+    bit-exact at the end (compact rows against a host scatter)."""
+    steps, check = wl.SWEEP_DECODE_STEPS, (0, 255, 511)
+    sw = wl.batch_sweep(batch, device=DEV, contiguous=contiguous, layers=2)
+    bt = torch.as_tensor(sw.block_table, device=DEV)
+    desc = pkv.cache_desc(sw.k_caches[0])
+    ws = pkv.decode_workspace(batch, sw.max_blocks, 32, desc, DEV)
+    rows = list(range(batch))
+    cap = sw.prompt_lens + steps
+    expect = [wl.compact_rows(sw.k_caches[layer], sw.v_caches[layer], sw.block_table, rows, cap, sw.page_size)
+              for layer in range(2)]
+    P = sw.page_size
+    for step in range(steps):
+        lens = (sw.prompt_lens + step).astype(np.int32)
+        sl = torch.as_tensor(lens, device=DEV)
+        for layer, (q, kn, vn) in enumerate(wl.sweep_step_inputs(sw, step, DEV, layers=2)):
+            # the host scatter of this step's appended token
+            ek, ev, ebt = expect[layer]
+            pg = ebt[np.arange(batch), lens // P]
+            ek[pg, lens % P] = wl.bits(kn)
+            ev[pg, lens % P] = wl.bits(vn)
+            if step in check:
+                hk, hv, hbt = wl.compact_rows(sw.k_caches[layer], sw.v_caches[layer], sw.block_table, rows, lens + 1, P)
+                od = oracle.CacheDesc(hk.shape[0], P, 8, 128, wl.NHD)
+                ref_out, ref_lse, err, _ = oracle.decode(od, hk, hv, wl.bits(q), wl.bits(kn), wl.bits(vn), hbt, lens,
+                                                         sw.softmax_scale)
+                assert err == 0
+            lse = torch.empty(batch, 32, dtype=torch.float32, device=DEV)
+            out = pkv.pkv_decode_attn(sw.k_caches[layer], sw.v_caches[layer], q, kn, vn, bt, sl, sw.softmax_scale,
+                                      lse=lse, workspace=ws, flags=pkv.api.DECODE_OVERLAP_PROLOGUE)
+            if step in check:
+                assert_close(f32(out), ref_out)
+                assert_lse_close(lse.cpu().numpy(), ref_lse)
+    for layer in range(2):
+        gk, gv, _ = wl.compact_rows(sw.k_caches[layer], sw.v_caches[layer], sw.block_table, rows, cap, P)
+        ek, ev, _ = expect[layer]
+        assert np.array_equal(gk, ek) and np.array_equal(gv, ev)
+
+
 def _random_case(seed, B, Hq, Hkv, D, P, lens, layout=wl.NHD, spare=7):
     g = torch.Generator().manual_seed(seed)
     lens = np.asarray(lens, np.int32)
