@@ -225,6 +225,53 @@ PKV_API pkv_status pkv_decode_attn_noalloc(const pkv_cache_desc *desc, void *k_c
                                            int32_t num_q_heads, float softmax_scale, void *out,
                                            float *lse, int32_t *err_flag, void *stream);
 
+/* ---------------------------------------------------------------------
+ * A whole decode step captured as a CUDA graph.
+ * Source: "flex_attention + paged KV + CUDA graphs vs vLLM", "Why this works"
+ * (one CUDA graph per batch bucket replays the step's launches; padding rows
+ * take a reserved null slot so that one graph serves every batch up to the
+ * bucket).  Here a padding row is inactive: cache_seqlens[b] < 0 (nothing is
+ * read or appended for it, its output is 0).
+ * --------------------------------------------------------------------- */
+
+/* Opaque captured decode step. */
+typedef struct pkv_decode_step pkv_decode_step;
+
+/* The bucket (graph batch size) serving `batch` rows: the smallest power of
+ * two that is >= max(batch, 8); 0 if batch is outside [1, 1024]. */
+PKV_API int32_t pkv_decode_bucket(int32_t batch);
+
+/*
+ * pkv_decode_step_create -- captures the pkv_decode_attn_ex calls of one
+ * decode step, layer l = 0 .. num_layers-1 in order, into a CUDA graph.  The
+ * layers share desc, block_table, cache_seqlens, batch (the bucket),
+ * num_q_heads, softmax_scale, workspace, err_flag and flags; each has its own
+ * k_caches[l], v_caches[l], q[l], k_new[l] / v_new[l] (both arrays NULL for
+ * attend-only), out[l] and lse[l] (lse NULL, or an array whose entries may be
+ * NULL).  All pointer arrays are host arrays of device pointers.
+ *  - The pointers are baked into the graph: every launch reads what the
+ *    buffers hold at launch time (write the step's q / k_new / v_new and
+ *    cache_seqlens there, then launch).
+ *  - Every argument error of the layer calls is returned before any CUDA
+ *    work; nothing is launched by this call.
+ *  - With PKV_DECODE_OVERLAP_PROLOGUE (and PKV_DECODE_EARLY_KV) the layers
+ *    overlap inside the graph as described for pkv_decode_attn_ex.
+ * On success *step_out owns the graph; free it with pkv_decode_step_destroy.
+ */
+PKV_API pkv_status pkv_decode_step_create(const pkv_cache_desc *desc, int32_t num_layers, void *const *k_caches,
+                                          void *const *v_caches, const void *const *q, const void *const *k_new,
+                                          const void *const *v_new, const int32_t *block_table,
+                                          int32_t max_blocks, const int32_t *cache_seqlens, int32_t batch,
+                                          int32_t num_q_heads, float softmax_scale, void *const *out,
+                                          float *const *lse, void *workspace, size_t workspace_bytes,
+                                          int32_t *err_flag, uint32_t flags, pkv_decode_step **step_out);
+
+/* Launches the captured step on `stream` (cudaStream_t). */
+PKV_API pkv_status pkv_decode_step_launch(pkv_decode_step *step, void *stream);
+
+/* Frees a captured step (NULL is allowed). */
+PKV_API void pkv_decode_step_destroy(pkv_decode_step *step);
+
 /*
  * pkv_prefill_workspace_size -- bytes of device workspace pkv_prefill_attn
  * needs (0 on invalid or unsupported arguments).  The workspace holds the

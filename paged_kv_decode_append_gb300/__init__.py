@@ -7,12 +7,14 @@ binding (``api``) and the seeded synthetic workload generators
 """
 from .api import (  # noqa: F401
     HND,
+    DecodeStep,
     NHD,
     PagePool,
     PkvError,
     cache_desc,
     decode_workspace,
     pkv_append,
+    pkv_decode_bucket,
     pkv_decode_attn,
     pkv_decode_workspace_size,
     pkv_pool_bytes,

@@ -39,6 +39,11 @@ SIGNATURES = {
     "pkv_decode_attn_ex": (I32, [DESC_P, P, P, P, P, P, P, I32, P, I32, I32, ctypes.c_float, P, P, P, SIZE, P, P,
                                  ctypes.c_uint32]),
     "pkv_decode_attn_noalloc": (I32, [DESC_P, P, P, P, P, P, P, I32, P, I32, I32, ctypes.c_float, P, P, P, P]),
+    "pkv_decode_bucket": (I32, [I32]),
+    "pkv_decode_step_create": (I32, [DESC_P, I32, P, P, P, P, P, P, I32, P, I32, I32, ctypes.c_float, P, P, P, SIZE,
+                                     P, ctypes.c_uint32, ctypes.POINTER(P)]),
+    "pkv_decode_step_launch": (I32, [P, P]),
+    "pkv_decode_step_destroy": (None, [P]),
     "pkv_prefill_workspace_size": (SIZE, [I32, I32, I32, DESC_P]),
     "pkv_prefill_attn": (I32, [DESC_P, P, P, P, P, P, P, I32, I32, I32, I32, ctypes.c_float, P, P, P, SIZE, P, P]),
     "pkv_pool_create": (P, [I32]),

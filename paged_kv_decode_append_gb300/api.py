@@ -149,6 +149,57 @@ def pkv_decode_attn_noalloc(k_cache, v_cache, q, k_new, v_new, block_table, cach
     return out
 
 
+def pkv_decode_bucket(batch: int) -> int:
+    """Graph batch size serving ``batch`` rows (0 if out of range)."""
+    return int(_lib.load().pkv_decode_bucket(batch))
+
+
+class DecodeStep:
+    """``pkv_decode_step_*``: every layer's fused append + decode of one step
+    captured once as a CUDA graph.  The tensors given here are baked in:
+    write each step's inputs (``q``, ``k_new``, ``v_new``, ``cache_seqlens``)
+    into them, then call :meth:`launch`."""
+
+    def __init__(self, k_caches, v_caches, q, k_new, v_new, block_table, cache_seqlens, softmax_scale: float, out,
+                 lse=None, workspace=None, err_flag=None, layout: int = NHD, flags: int = 0):
+        layers = len(k_caches)
+        if not (len(v_caches) == len(q) == len(out) == layers) or layers < 1:
+            raise ValueError("one k / v cache, q and out per layer")
+        for lst, n in ((k_caches, "k_caches"), (v_caches, "v_caches"), (q, "q"), (out, "out"),
+                       (k_new or [], "k_new"), (v_new or [], "v_new")):
+            for t in lst:
+                _bf16(t, n)
+        for t, n in ((block_table, "block_table"), (cache_seqlens, "cache_seqlens"), (err_flag, "err_flag")):
+            _i32(t, n)
+        desc = cache_desc(k_caches[0], layout)
+        B, Hq, D = q[0].shape
+        if workspace is None:
+            workspace = decode_workspace(B, block_table.shape[1], Hq, desc, q[0].device)
+        arr = ctypes.c_void_p * layers
+
+        def ptrs(lst):
+            return None if lst is None else arr(*[t.data_ptr() if t is not None else None for t in lst])
+
+        self._keep = (k_caches, v_caches, q, k_new, v_new, block_table, cache_seqlens, out, lse, workspace, err_flag)
+        self._lib = _lib.load()
+        handle = ctypes.c_void_p()
+        st = self._lib.pkv_decode_step_create(
+            ctypes.byref(desc), layers, ptrs(k_caches), ptrs(v_caches), ptrs(q), ptrs(k_new), ptrs(v_new),
+            _ptr(block_table), block_table.shape[1], _ptr(cache_seqlens), B, Hq, float(softmax_scale), ptrs(out),
+            ptrs(lse), _ptr(workspace), workspace.numel(), _ptr(err_flag), int(flags), ctypes.byref(handle))
+        _check(st, "pkv_decode_step_create")
+        self._h = handle
+        self.device = q[0].device
+
+    def launch(self) -> None:
+        _check(self._lib.pkv_decode_step_launch(self._h, _stream(self.device)), "pkv_decode_step_launch")
+
+    def __del__(self):
+        if getattr(self, "_h", None):
+            self._lib.pkv_decode_step_destroy(self._h)
+            self._h = None
+
+
 def pkv_prefill_workspace_size(batch: int, total_q: int, num_q_heads: int, desc: CacheDesc) -> int:
     return int(_lib.load().pkv_prefill_workspace_size(batch, total_q, num_q_heads, ctypes.byref(desc)))
 

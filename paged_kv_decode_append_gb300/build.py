@@ -20,7 +20,7 @@ BUILD_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(HERE, "libpkv.so")
 
 CUDA_SOURCES = ["pkv_decode.cu", "pkv_prefill.cu", "pkv_append.cu", "pkv_api.cu", "pkv_static.cu"]
-CXX_SOURCES = ["pkv_pool.cc"]
+CXX_SOURCES = ["pkv_pool.cc", "pkv_graph.cc"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

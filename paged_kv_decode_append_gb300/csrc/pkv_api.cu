@@ -153,6 +153,42 @@ CUresult encode_group_map(CUtensorMap *map, const pkv_cache_desc &d, void *base,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
+
+pkv_status decode_check(const pkv_cache_desc *desc, const void *k_cache, const void *v_cache, const void *q,
+                        const void *k_new, const void *v_new, const int32_t *block_table, int32_t max_blocks,
+                        const int32_t *cache_seqlens, int32_t batch, int32_t num_q_heads, float softmax_scale,
+                        const void *out, const void *workspace, size_t workspace_bytes, uint32_t flags,
+                        DecodeShape *shape)
+{
+    if ((flags & ~(PKV_DECODE_OVERLAP_PROLOGUE | PKV_DECODE_EARLY_KV)) != 0)
+        return PKV_EINVAL;
+    if ((flags & PKV_DECODE_EARLY_KV) && !(flags & PKV_DECODE_OVERLAP_PROLOGUE))
+        return PKV_EINVAL;
+    const pkv_status st = check_desc(desc);
+    if (st != PKV_OK)
+        return st;
+    if (batch < 0 || max_blocks < 1 || num_q_heads < 1 || !isfinite(softmax_scale))
+        return PKV_EINVAL;
+    if (batch > kMaxDecodeBatch)
+        return PKV_EUNSUPPORTED;
+    if ((k_new == nullptr) != (v_new == nullptr))
+        return PKV_EINVAL;
+    if (num_q_heads % desc->num_kv_heads != 0)
+        return PKV_EINVAL;
+    if (!decode_shape(batch, max_blocks, num_q_heads, *desc, shape))
+        return PKV_EUNSUPPORTED;
+    if (batch == 0)
+        return PKV_OK;
+    if (k_cache == nullptr || v_cache == nullptr || q == nullptr || out == nullptr || block_table == nullptr ||
+        cache_seqlens == nullptr)
+        return PKV_EINVAL;
+    if (!aligned16(k_cache) || !aligned16(v_cache) || !aligned16(q) || !aligned16(out) ||
+        (k_new != nullptr && (!aligned16(k_new) || !aligned16(v_new))))
+        return PKV_EINVAL;
+    if (workspace == nullptr || workspace_bytes < shape->bytes || !aligned16(workspace))
+        return PKV_EWORKSPACE;
+    return PKV_OK;
+}
 } // namespace pkv
 
 using namespace pkv;
@@ -251,34 +287,12 @@ pkv_status pkv_decode_attn_ex(const pkv_cache_desc *desc, void *k_cache, void *v
                               void *out, float *lse, void *workspace, size_t workspace_bytes, int32_t *err_flag,
                               void *stream, uint32_t flags)
 {
-    if ((flags & ~(PKV_DECODE_OVERLAP_PROLOGUE | PKV_DECODE_EARLY_KV)) != 0)
-        return PKV_EINVAL;
-    if ((flags & PKV_DECODE_EARLY_KV) && !(flags & PKV_DECODE_OVERLAP_PROLOGUE))
-        return PKV_EINVAL;
-    const pkv_status st = check_desc(desc);
-    if (st != PKV_OK)
-        return st;
-    if (batch < 0 || max_blocks < 1 || num_q_heads < 1 || !isfinite(softmax_scale))
-        return PKV_EINVAL;
-    if (batch > kMaxDecodeBatch)
-        return PKV_EUNSUPPORTED;
-    if ((k_new == nullptr) != (v_new == nullptr))
-        return PKV_EINVAL;
-    if (num_q_heads % desc->num_kv_heads != 0)
-        return PKV_EINVAL;
     DecodeShape shape;
-    if (!decode_shape(batch, max_blocks, num_q_heads, *desc, &shape))
-        return PKV_EUNSUPPORTED;
-    if (batch == 0)
-        return PKV_OK;
-    if (k_cache == nullptr || v_cache == nullptr || q == nullptr || out == nullptr || block_table == nullptr ||
-        cache_seqlens == nullptr)
-        return PKV_EINVAL;
-    if (!aligned16(k_cache) || !aligned16(v_cache) || !aligned16(q) || !aligned16(out) ||
-        (k_new != nullptr && (!aligned16(k_new) || !aligned16(v_new))))
-        return PKV_EINVAL;
-    if (workspace == nullptr || workspace_bytes < shape.bytes || !aligned16(workspace))
-        return PKV_EWORKSPACE;
+    const pkv_status st = decode_check(desc, k_cache, v_cache, q, k_new, v_new, block_table, max_blocks, cache_seqlens,
+                                       batch, num_q_heads, softmax_scale, out, workspace, workspace_bytes, flags,
+                                       &shape);
+    if (st != PKV_OK || batch == 0)
+        return st;
 
     const int dev = current_device();
     if (dev < 0)

@@ -76,6 +76,14 @@ constexpr int kDecodeSmallBox = 8;
 
 cudaError_t launch_decode(const DecodeArgs &a, const DecodeMaps &maps, cudaStream_t stream);
 
+// Every argument check of pkv_decode_attn_ex (no device access, no launch);
+// fills `shape` when the sizes are supported.
+pkv_status decode_check(const pkv_cache_desc *desc, const void *k_cache, const void *v_cache, const void *q,
+                        const void *k_new, const void *v_new, const int32_t *block_table, int32_t max_blocks,
+                        const int32_t *cache_seqlens, int32_t batch, int32_t num_q_heads, float softmax_scale,
+                        const void *out, const void *workspace, size_t workspace_bytes, uint32_t flags,
+                        DecodeShape *shape);
+
 struct AppendArgs {
     pkv_cache_desc desc;
     int page_shift;

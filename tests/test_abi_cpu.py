@@ -225,3 +225,36 @@ def test_prefill_argument_errors_return_before_any_launch():
     assert _prefill(lib, d, total_q=0) == pkv.api.OK
     assert _prefill(lib, d, batch=1025) == pkv.api.EUNSUPPORTED
     assert _prefill(lib, d, total_q=-1) == pkv.api.EINVAL
+
+
+def test_decode_bucket():
+    lib = _lib.load()
+    assert [lib.pkv_decode_bucket(b) for b in (1, 8, 9, 16, 17, 64, 65, 1000, 1024)] == \
+        [8, 8, 16, 16, 32, 64, 128, 1024, 1024]
+    assert lib.pkv_decode_bucket(0) == 0 and lib.pkv_decode_bucket(1025) == 0
+
+
+def test_decode_step_argument_errors_before_any_cuda_call():
+    lib = _lib.load()
+    d = CacheDesc(64, 16, 2, 128, 0)
+    arr = ctypes.c_void_p * 2
+    two = arr(0x10000, 0x10000)
+    out = ctypes.c_void_p()
+
+    def create(desc=d, layers=2, k=two, q=two, o=two, ws=FAKE, ws_bytes=1 << 30, batch=4, hq=8, flags=0, handle=True):
+        return lib.pkv_decode_step_create(ctypes.byref(desc), layers, k, k, q, None, None, FAKE, 4, FAKE, batch, hq,
+                                          0.1, o, None, ws, ws_bytes, None, flags,
+                                          ctypes.byref(out) if handle else None)
+
+    assert create(handle=False) == pkv.api.EINVAL
+    assert create(layers=0) == pkv.api.EINVAL
+    assert create(k=None) == pkv.api.EINVAL
+    assert create(q=arr(0x10000, 0)) == pkv.api.EINVAL                    # a missing layer pointer
+    assert create(q=arr(0x10000, 0x10008)) == pkv.api.EINVAL              # misaligned
+    assert create(desc=CacheDesc(64, 16, 2, 96, 0)) == pkv.api.EUNSUPPORTED
+    assert create(hq=6) == pkv.api.EUNSUPPORTED
+    assert create(ws=None) == pkv.api.EWORKSPACE
+    assert create(ws_bytes=64) == pkv.api.EWORKSPACE
+    assert create(flags=pkv.api.DECODE_EARLY_KV) == pkv.api.EINVAL
+    assert out.value is None
+    lib.pkv_decode_step_destroy(None)

@@ -158,6 +158,57 @@ def test_batch_sweep_full_cycle(batch, contiguous):
         assert np.array_equal(gk, ek) and np.array_equal(gv, ev)
 
 
+def test_decode_step_graph_with_padded_bucket():
+    """Three layers captured once as a decode-step graph for the 16-row bucket
+    of 13 live rows (rows 13..15 inactive), replayed for two steps with the
+    inputs rewritten in place: bit-identical to direct calls, padding rows 0 /
+    -inf, caches appended identically."""
+    live, layers = 13, 3
+    bucket = pkv.pkv_decode_bucket(live)
+    assert bucket == 16
+    sw = wl.batch_sweep(live, device=DEV, contiguous=False, layers=layers)
+    bt_live = sw.block_table
+    bt = torch.zeros(bucket, sw.max_blocks, dtype=torch.int32, device=DEV)
+    bt[:live] = torch.as_tensor(bt_live, device=DEV)
+    desc = pkv.cache_desc(sw.k_caches[0])
+    flags = pkv.api.DECODE_OVERLAP_PROLOGUE | pkv.api.DECODE_EARLY_KV
+    kc_g = [k.clone() for k in sw.k_caches]
+    vc_g = [v.clone() for v in sw.v_caches]
+    # graph buffers (bucket rows), written in place every step
+    q = [torch.zeros(bucket, 32, 128, dtype=torch.bfloat16, device=DEV) for _ in range(layers)]
+    kn = [torch.zeros(bucket, 8, 128, dtype=torch.bfloat16, device=DEV) for _ in range(layers)]
+    vn = [torch.zeros(bucket, 8, 128, dtype=torch.bfloat16, device=DEV) for _ in range(layers)]
+    out = [torch.empty(bucket, 32, 128, dtype=torch.bfloat16, device=DEV) for _ in range(layers)]
+    lse = [torch.empty(bucket, 32, dtype=torch.float32, device=DEV) for _ in range(layers)]
+    seq = torch.full((bucket,), -1, dtype=torch.int32, device=DEV)
+    ws = pkv.decode_workspace(bucket, sw.max_blocks, 32, desc, DEV)
+    step_graph = pkv.DecodeStep(kc_g, vc_g, q, kn, vn, bt, seq, sw.softmax_scale, out, lse=lse, workspace=ws,
+                                flags=flags)
+    ws_ref = pkv.decode_workspace(live, sw.max_blocks, 32, desc, DEV)
+    bt_ref = torch.as_tensor(bt_live, device=DEV)
+    for step in range(2):
+        lens = torch.as_tensor((sw.prompt_lens + step).astype(np.int32), device=DEV)
+        ins = wl.sweep_step_inputs(sw, step, DEV, layers=layers)
+        seq[:live] = lens
+        for layer, (qq, kk, vv) in enumerate(ins):
+            q[layer][:live] = qq
+            kn[layer][:live] = kk
+            vn[layer][:live] = vv
+        step_graph.launch()
+        for layer, (qq, kk, vv) in enumerate(ins):
+            ref_lse = torch.empty(live, 32, dtype=torch.float32, device=DEV)
+            ref = pkv.pkv_decode_attn(sw.k_caches[layer], sw.v_caches[layer], qq, kk, vv, bt_ref, lens,
+                                      sw.softmax_scale, lse=ref_lse, workspace=ws_ref)
+            torch.cuda.synchronize()
+            assert torch.equal(out[layer][:live].view(torch.int16), ref.view(torch.int16))
+            assert torch.equal(lse[layer][:live].view(torch.int32), ref_lse.view(torch.int32))
+            assert not out[layer][live:].float().any()
+            assert torch.isneginf(lse[layer][live:]).all()
+    for layer in range(layers):
+        assert torch.equal(kc_g[layer].view(torch.int16), sw.k_caches[layer].view(torch.int16))
+        assert torch.equal(vc_g[layer].view(torch.int16), sw.v_caches[layer].view(torch.int16))
+
+
 def _random_case(seed, B, Hq, Hkv, D, P, lens, layout=wl.NHD, spare=7):
     g = torch.Generator().manual_seed(seed)
     lens = np.asarray(lens, np.int32)
