@@ -585,42 +585,54 @@ def main():
     torch.cuda.synchronize(dev)
     eager_gbs = eager_bytes / (ea.elapsed_time(eb) * 1e-3) / 1e9
 
-    # End to end through the public API: each step copies its q / k_new / v_new
-    # for all layers from pinned host memory, runs the 36 calls and copies the
-    # outputs back (one graph per step, like the timed region).
+    # End to end through the public API: one pkv_decode_step graph (all 36
+    # layers) captured once over device input / output buffers; every step
+    # copies that step's q / k_new / v_new of all layers and its cache_seqlens
+    # from pinned host memory into them, launches the step and copies all
+    # outputs back -- one H2D copy, one seqlens copy, one launch, one D2H copy.
     e2e_steps = min(args.e2e_steps, args.steps)
-    h_in = [[tuple(t.cpu().pin_memory() for t in trip) for trip in inputs[r]] for r in range(2)]
-    h_out = [torch.empty(B, HQ, D, dtype=torch.bfloat16).pin_memory() for _ in range(L)]
-    d_in = [tuple(torch.empty_like(t) for t in trip) for trip in inputs[0]]
-    h2d = sum(t.numel() * 2 for trip in inputs[0] for t in trip)
-    d2h = L * B * HQ * D * 2
-    e_graphs = []
-    for s in range(e2e_steps):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g):
-            src = h_in[s % 2]
-            for layer in range(L):
-                for dst, hs in zip(d_in[layer], src[layer]):
-                    dst.copy_(hs, non_blocking=True)
-            for layer in range(L):
-                layer_call(s, layer, *d_in[layer])
-            for layer in range(L):
-                h_out[layer].copy_(outs[layer], non_blocking=True)
-        e_graphs.append(g)
+    per_layer = [B * HQ * D, B * HKV * D, B * HKV * D]
+    layer_elems = sum(per_layer)
+    d_in_all = torch.empty(L * layer_elems, dtype=torch.bfloat16, device=dev)
+    d_out_all = torch.empty(L * B * HQ * D, dtype=torch.bfloat16, device=dev)
+    d_seq = torch.empty(B, dtype=torch.int32, device=dev)
+
+    def split(buf, base):
+        q_, k_, v_ = torch.split(buf[base:base + layer_elems], per_layer)
+        return q_.view(B, HQ, D), k_.view(B, HKV, D), v_.view(B, HKV, D)
+
+    d_in = [split(d_in_all, layer * layer_elems) for layer in range(L)]
+    d_out = [d_out_all[layer * B * HQ * D:(layer + 1) * B * HQ * D].view(B, HQ, D) for layer in range(L)]
+    h_in = []
+    for r in range(2):  # two pinned input sets, alternated
+        h = torch.empty(L * layer_elems, dtype=torch.bfloat16).pin_memory()
+        for layer, trip in enumerate(inputs[r]):
+            for dst, t in zip(split(h, layer * layer_elems), trip):
+                dst.copy_(t.cpu())
+        h_in.append(h)
+    h_seq = [torch.as_tensor(lens_all[s % DECODE_CAPACITY]).pin_memory() for s in range(e2e_steps)]
+    h_out = torch.empty(L * B * HQ * D, dtype=torch.bfloat16).pin_memory()
+    h2d = d_in_all.numel() * 2 + B * 4
+    d2h = d_out_all.numel() * 2
+    step_graph = pkv.DecodeStep(sw.k_caches, sw.v_caches, [t[0] for t in d_in], [t[1] for t in d_in],
+                                [t[2] for t in d_in], bt, d_seq, sw.softmax_scale, d_out, workspace=ws, flags=flags)
     torch.cuda.synchronize(dev)
     barrier(world)
     e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e_bytes = 0
     e_start.record(stream)
     for s in range(e2e_steps):
-        e_graphs[s].replay()
+        d_in_all.copy_(h_in[s % 2], non_blocking=True)
+        d_seq.copy_(h_seq[s], non_blocking=True)
+        step_graph.launch()
+        h_out.copy_(d_out_all, non_blocking=True)
         e_bytes += step_bytes[s % DECODE_CAPACITY]
     e_end.record(stream)
     torch.cuda.synchronize(dev)
     e_ms = max_over_ranks(e_start.elapsed_time(e_end), world, dev)
     e_all = sum_over_ranks(float(e_bytes), world, dev)
     e2e_value = e_all / (e_ms * 1e-3) / 1e9
-    del e_graphs
+    del step_graph
 
     prefill = prefill_bench(dev, args.prefill_reps) if args.prefill_reps > 0 else None
 
@@ -645,7 +657,9 @@ def main():
                      "isolated_gbs": iso_gbs, "isolated_launches": int(iso_ms.size)},
         "clocks": clocks.summary(),
         "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "steps": e2e_steps},
+                "steps": e2e_steps,
+                "path": "pkv_decode_step graph of the 36 layers; per step pinned H2D of all inputs and "
+                        "cache_seqlens, one launch, D2H of all outputs"},
         "eager": {"value": eager_gbs, "unit": "GB/s", "steps": eager_steps,
                   "launch": "plain stream launches, no CUDA graph"},
         "gpu_launches": n_ev,

@@ -91,8 +91,8 @@ constexpr int stages_for()
 template <int D, int GC>
 struct Smem {
     static constexpr int kStages = stages_for<D, GC>();
-    // [stage][K|V] tiles laid out [D/64][kTile][64] (128-byte rows, TMA
-    // SWIZZLE_128B when the page size allows 8-row boxes)
+    // [stage][K|V] tiles laid out [kTile/8][D/64][8][64]: 8-token groups of
+    // 128-byte rows (TMA SWIZZLE_128B when the page size allows 8-row boxes)
     __nv_bfloat16 kv[kStages][2][kTile * D];
     // per-warp softmax states of a finished slice: o (unnormalised), m, l
     float red_o[kSlots][kWarps][GC][D];
