@@ -1,4 +1,5 @@
-"""fp64 CPU oracle for paged KV append, decode attention and causal prefill.
+"""fp64 CPU oracle for paged KV append, decode attention, causal prefill and
+the mixed step (chunked prefill and multi-token decode rows in one batch).
 
 TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
 CPU-baseline / reference legs of ``bench.py`` may import this package.  The
@@ -19,7 +20,10 @@ What it follows (page title, section):
   and the pair count ``Hq * sum q(2kv-q+1)/2``; HND page layout.
 * "flex_attention + paged KV + CUDA graphs vs vLLM", "What broke
   correctness": page 0 is a null slot; a row with no visible key gives
-  out = 0 and lse = -inf, never NaN.
+  out = 0 and lse = -inf, never NaN.  Same page, "What's left on the
+  table": vLLM interleaves prefill chunks and decode tokens within one step;
+  ``mixed`` is that step (append every row's new tokens, then the
+  end-aligned causal rule over the grown cache).
 
 Pins (tests under ``tests/test_oracle_*.py``) tie it to torch's fp64 SDPA on
 dense gathers, closed forms (scale 0, constant V, one key), page-permutation
@@ -45,6 +49,7 @@ NHD = 0
 HND = 1
 ERR_PAGE = 1
 ERR_OVERFLOW = 2
+ERR_QLEN = 8
 
 
 def build(force: bool = False) -> str:
@@ -95,6 +100,10 @@ def _load():
         lib.oracle_prefill.argtypes = [P, P, P, P, P, P, P, i32, i32, i32, ctypes.c_double,
                                        P, i32, P, P, P, i32]
         lib.oracle_prefill.restype = ctypes.c_int64
+        i64 = ctypes.c_int64
+        lib.oracle_mixed.argtypes = [P, P, P, P, P, P, P, i64, P, i32, P, i32, i32, i64, ctypes.c_double,
+                                     P, i32, P, P, P, i32]
+        lib.oracle_mixed.restype = i32
         lib.oracle_max_threads.argtypes = [i32]
         lib.oracle_max_threads.restype = i32
         _lib = lib
@@ -213,6 +222,37 @@ def prefill(desc: CacheDesc, k_cache, v_cache, q, qo_indptr, kv_lens, block_tabl
                                _ptr(bt), bt.shape[1], B, Hq, float(softmax_scale), _ptr(s), ns,
                                _ptr(out), _ptr(lse), _ptr(err_rows), int(nthreads))
     return out, lse, int(pairs), err_rows
+
+
+def mixed(desc: CacheDesc, k_cache, v_cache, q, k_new, v_new, qo_indptr, block_table, cache_seqlens,
+          softmax_scale, max_qlen=None, sel=None, nthreads: int = 0):
+    """One step of a mixed batch in fp64: row b appends its
+    ``qo_indptr[b+1] - qo_indptr[b]`` new tokens (when ``k_new``/``v_new``
+    ``[total_q, Hkv, D]`` are given) after its ``cache_seqlens[b]`` cached
+    ones, then its query i sees keys ``0 .. kv_b - q_b + i`` (end aligned).
+
+    ``k_cache``/``v_cache`` are modified in place (pass copies).  ``q`` is
+    ``[total_q, Hq, D]``; ``max_qlen`` (default: no limit) is the longest
+    query range accepted.  Returns ``(out [total_q,Hq,D], lse [total_q,Hq],
+    err_bits, err_rows)``; entries not computed (not in ``sel``, or owned by
+    no row) are NaN."""
+    lib = _load()
+    c = desc._c()
+    assert k_cache.flags.c_contiguous and v_cache.flags.c_contiguous
+    q = _u16(q, "q")
+    k_new, v_new = _u16(k_new, "k_new"), _u16(v_new, "v_new")
+    ip, bt, sl = _i32(qo_indptr), _i32(block_table), _i32(cache_seqlens)
+    T, Hq, D = q.shape
+    B = sl.shape[0]
+    out = np.full((T, Hq, D), np.nan)
+    lse = np.full((T, Hq), np.nan)
+    err_rows = np.zeros(B, np.int32)
+    s, ns = _sel(sel)
+    mq = (1 << 62) if max_qlen is None else int(max_qlen)
+    err = lib.oracle_mixed(ctypes.byref(c), _ptr(k_cache), _ptr(v_cache), _ptr(q), _ptr(k_new), _ptr(v_new),
+                           _ptr(ip), T, _ptr(bt), bt.shape[1], _ptr(sl), B, Hq, mq, float(softmax_scale),
+                           _ptr(s), ns, _ptr(out), _ptr(lse), _ptr(err_rows), int(nthreads))
+    return out, lse, err, err_rows
 
 
 def max_threads(nthreads: int = 0) -> int:

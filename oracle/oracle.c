@@ -1,6 +1,7 @@
 /*
  * oracle.c -- plain, slow, fp64 CPU oracle for paged KV append, single-token
- * decode attention and ragged end-aligned causal prefill.
+ * decode attention, ragged end-aligned causal prefill and the mixed step
+ * (chunked prefill and multi-token decode rows in one batch).
  *
  * TEST INFRASTRUCTURE ONLY.  Nothing in the product library links, loads or
  * calls this file; only the tests, the smoke check and the benchmark's CPU
@@ -54,6 +55,7 @@
 
 #define ORACLE_ERR_PAGE 1     /* a needed page id outside [1, num_pages) */
 #define ORACLE_ERR_OVERFLOW 2 /* tokens do not fit max_blocks * page_size */
+#define ORACLE_ERR_QLEN 8     /* a malformed query range or length */
 
 typedef struct {
     int32_t num_pages;
@@ -334,6 +336,105 @@ int64_t oracle_prefill(const oracle_cache *c, const uint16_t *k_cache, const uin
     free(row_err);
     free(row_of);
     return any_err ? -2 : pairs;
+}
+
+/*
+ * One step of a mixed batch: chunked prefill, multi-token and single-token
+ * decode rows together.  Row b brings q_b = qo_indptr[b+1] - qo_indptr[b]
+ * new tokens (query rows qo_indptr[b] .. qo_indptr[b+1]-1 of q, [total_q,
+ * Hq, D]) on top of L_b = cache_seqlens[b] cached tokens.
+ *  - With k_new / v_new ([total_q, Hkv, D]) the new tokens' K/V are written
+ *    at positions L_b .. L_b + q_b - 1 first (as oracle_append: only the
+ *    pages written are checked for the append) and the row holds
+ *    kv_b = L_b + q_b keys; without them the caller appended already and
+ *    kv_b = L_b.
+ *  - Query i of the row sees keys 0 .. kv_b - q_b + i (the end-aligned
+ *    causal rule of the FlashInfer page, code analysis part 1).
+ * Row fates, checked in this order:
+ *  - a query range outside [0, total_q] or reversed: ORACLE_ERR_QLEN, no
+ *    append, no output row is written;
+ *  - q_b == 0: nothing;
+ *  - q_b > max_qlen: ORACLE_ERR_QLEN, no append, out = 0, lse = -inf;
+ *  - L_b < 0 (inactive): no append, out = 0, lse = -inf, no error;
+ *  - kv_b < q_b (attend only): ORACLE_ERR_QLEN, out = 0, lse = -inf;
+ *  - overflow or a bad page among keys 0 .. kv_b - 1: the bit, out = 0,
+ *    lse = -inf (the append is dropped when its own pages fail).
+ * sel (optional) lists nsel (query row, head) pairs to compute; the appends
+ * of every row still happen.  Returns the OR of the error bits; err_rows[b]
+ * (optional) gets each row's.
+ */
+int oracle_mixed(const oracle_cache *c, uint16_t *k_cache, uint16_t *v_cache, const uint16_t *q,
+                 const uint16_t *k_new, const uint16_t *v_new, const int32_t *qo_indptr, int64_t total_q,
+                 const int32_t *block_table, int max_blocks, const int32_t *cache_seqlens, int batch,
+                 int num_q_heads, int64_t max_qlen, double scale, const int32_t *sel, int nsel,
+                 double *out, double *lse, int32_t *err_rows, int nthreads)
+{
+    int64_t H = c->num_kv_heads, D = c->head_dim;
+    int group = num_q_heads / c->num_kv_heads;
+    int with_new = (k_new != NULL && v_new != NULL);
+    int32_t *row_err = (int32_t *)calloc((size_t)(batch > 0 ? batch : 1), sizeof(int32_t));
+    int64_t *row_keys = (int64_t *)calloc((size_t)(batch > 0 ? batch : 1), sizeof(int64_t));
+    int32_t *row_of = (int32_t *)malloc((size_t)(total_q > 0 ? total_q : 1) * sizeof(int32_t));
+    int err_all = 0;
+    for (int64_t t = 0; t < total_q; t++)
+        row_of[t] = -1;
+
+    for (int b = 0; b < batch; b++) {
+        int64_t s = qo_indptr[b], e = qo_indptr[b + 1], qn = e - s;
+        int64_t L = cache_seqlens[b];
+        int err = 0;
+        row_keys[b] = 0;
+        if (s < 0 || e > total_q || qn < 0) {
+            row_err[b] = ORACLE_ERR_QLEN;
+            err_all |= ORACLE_ERR_QLEN;
+            continue; /* no valid query rows: nothing is written */
+        }
+        if (qn == 0)
+            continue;
+        for (int64_t t = s; t < e; t++)
+            row_of[t] = b;
+        if (qn > max_qlen) {
+            err = ORACLE_ERR_QLEN;
+        } else if (L >= 0) {
+            int64_t kv = with_new ? L + qn : L;
+            if (with_new && !range_check(c, block_table, max_blocks, b, L, L + qn))
+                write_tokens(c, k_cache, v_cache, k_new + s * H * D, v_new + s * H * D, qn,
+                             block_table, max_blocks, b, L);
+            if (kv < qn)
+                err = ORACLE_ERR_QLEN;
+            else
+                err = row_check(c, block_table, max_blocks, b, kv);
+            if (!err)
+                row_keys[b] = kv;
+        }
+        row_err[b] = err;
+        err_all |= err;
+    }
+
+    int64_t n_items = sel ? nsel : total_q * num_q_heads;
+    set_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t i = 0; i < n_items; i++) {
+        int64_t t = sel ? sel[2 * i] : i / num_q_heads;
+        int h = sel ? sel[2 * i + 1] : (int)(i % num_q_heads);
+        int b = row_of[t];
+        if (b < 0)
+            continue; /* no row owns this query row */
+        int64_t qn = qo_indptr[b + 1] - qo_indptr[b];
+        int64_t qi = t - qo_indptr[b];
+        int64_t n_keys = row_keys[b] > 0 ? row_keys[b] - qn + qi + 1 : 0;
+        double *scores = (double *)malloc((size_t)(n_keys > 0 ? n_keys : 1) * sizeof(double));
+        int64_t o = t * num_q_heads + h;
+        attend_row(c, k_cache, v_cache, block_table, max_blocks, b, h / group, n_keys,
+                   q + o * D, scale, out + o * D, lse + o, scores);
+        free(scores);
+    }
+    if (err_rows)
+        memcpy(err_rows, row_err, (size_t)batch * sizeof(int32_t));
+    free(row_err);
+    free(row_keys);
+    free(row_of);
+    return err_all;
 }
 
 /* Threads an OpenMP region of this build would use (1 without OpenMP). */

@@ -69,7 +69,7 @@ class PagedCase:
     v_new: torch.Tensor | None = None
     k_cache: torch.Tensor | None = None  # bf16 pool, NHD or HND
     v_cache: torch.Tensor | None = None
-    qo_indptr: np.ndarray | None = None  # prefill only, int32 [B+1]
+    qo_indptr: np.ndarray | None = None  # prefill / mixed step, int32 [B+1]
     kv_lens: np.ndarray | None = None  # prefill only, int32 [B]
     extra: dict = field(default_factory=dict)
 
@@ -251,6 +251,34 @@ def small_prefill(seed: int, q_lens, kv_lens, num_q_heads: int, num_kv_heads: in
                      np.zeros(B, np.int32), 1.0 / math.sqrt(head_dim),
                      q=_randn_bf16((int(indptr[-1]), num_q_heads, head_dim), g, "cpu").to(device),
                      qo_indptr=indptr, kv_lens=kv_lens)
+    _fill_cache(case, g, device, "cpu")
+    return case
+
+
+def mixed_step(seed: int, q_lens, cache_lens, num_q_heads: int, num_kv_heads: int, head_dim: int,
+               page_size: int, layout: int = NHD, extra_pages: int = 3, device="cpu") -> PagedCase:
+    """One step of a mixed batch: row b holds cache_lens[b] cached tokens
+    (negative: an inactive row) and brings q_lens[b] new tokens -- q, k_new
+    and v_new are [sum q_lens, H, D] with row b's tokens at qo_indptr[b] ..
+    qo_indptr[b+1]-1.  Pages for cache_lens[b] + q_lens[b] tokens come from a
+    seeded permutation; every slot without a cached token is NaN."""
+    g = _gen(seed)
+    q_lens = np.asarray(q_lens, np.int32)
+    L = np.asarray(cache_lens, np.int32)
+    B = len(q_lens)
+    P = page_size
+    indptr = np.concatenate([[0], np.cumsum(q_lens)]).astype(np.int32)
+    T = int(indptr[-1])
+    needed = (np.maximum(L, 0) + np.where(L >= 0, q_lens, 0) + P - 1) // P
+    num_pages = int(needed.sum()) + 1 + extra_pages
+    max_blocks = max(int(needed.max()) if B else 1, 1)
+    order = (torch.randperm(num_pages - 1, generator=g).numpy() + 1).astype(np.int32)
+    bt = assign_pages(needed, num_pages, max_blocks, order)
+    case = PagedCase("mixed", B, num_q_heads, num_kv_heads, head_dim, P, num_pages, layout, max_blocks, bt, L,
+                     1.0 / math.sqrt(head_dim), q=_randn_bf16((T, num_q_heads, head_dim), g, "cpu").to(device),
+                     qo_indptr=indptr)
+    case.k_new = _randn_bf16((T, num_kv_heads, head_dim), g, "cpu").to(device)
+    case.v_new = _randn_bf16((T, num_kv_heads, head_dim), g, "cpu").to(device)
     _fill_cache(case, g, device, "cpu")
     return case
 
