@@ -78,8 +78,9 @@ typedef enum {
 #define PKV_ERR_OVERFLOW 2 /* a row's tokens exceed max_blocks * page_size */
 #define PKV_ERR_TIMEOUT 4  /* an on-chip pipeline wait ran out of time: the call's outputs are
                               unspecified and its workspace must be zero-filled again */
-#define PKV_ERR_QLEN 8     /* prefill: a request with more queries than keys, a query range
-                              outside [0, total_q), or a decreasing qo_indptr */
+#define PKV_ERR_QLEN 8     /* prefill / mixed step: a request with more queries than keys (or
+                              than max_qlen), a query range outside [0, total_q), or a
+                              decreasing qo_indptr */
 
 /* Geometry of one K or V page pool (both share it).  page_size is a power of
  * two in [1, 256]; head_dim is 64, 128 or 256; num_pages >= 2 (page 0 is the
@@ -106,7 +107,9 @@ typedef struct pkv_pool pkv_pool;
  *  append_indptr     device int32 [batch + 1] (row b appends tokens
  *                    append_indptr[b] .. append_indptr[b+1]-1 of k_new at
  *                    positions cache_seqlens[b], cache_seqlens[b]+1, ...),
- *                    or NULL for exactly one token per row (T = batch).
+ *                    or NULL for exactly one token per row (T = batch).  A
+ *                    row whose range is reversed or leaves [0, T) appends
+ *                    nothing (no error bit).
  *  block_table       device int32 [batch, max_blocks].
  *  cache_seqlens     device int32 [batch]; not modified (the caller advances
  *                    it).
@@ -319,6 +322,75 @@ PKV_API pkv_status pkv_prefill_attn(const pkv_cache_desc *desc, const void *k_ca
                                     int32_t num_q_heads, int32_t total_q, float softmax_scale, void *out,
                                     float *lse, void *workspace, size_t workspace_bytes, int32_t *err_flag,
                                     void *stream);
+
+/* ---------------------------------------------------------------------
+ * One step of a mixed batch: chunked prefill, multi-token (speculative)
+ * decode and single-token decode rows in one call.
+ * Source: "flex_attention + paged KV + CUDA graphs vs vLLM", "What's left on
+ * the table" (vLLM interleaves prefill chunks and decode tokens within one
+ * step, where flex ran a separate prefill pass); the end-aligned causal rule
+ * of "[flashinfer] H100 D256 paged attention cuDNN auto-dispatch", code
+ * analysis part 1; the append of "mini-infer系统实战-06 True PagedAttention",
+ * section 1.
+ * --------------------------------------------------------------------- */
+
+/*
+ * pkv_mixed_workspace_size -- bytes of device workspace pkv_mixed_attn needs
+ * for these sizes (0 on invalid or unsupported arguments).  Like the decode
+ * workspace it must be zero-filled once before its first use; every
+ * completed call leaves it ready for the next (zero it again after
+ * PKV_ERR_TIMEOUT).  Calls that share a workspace must not run concurrently.
+ */
+PKV_API size_t pkv_mixed_workspace_size(int32_t batch, int32_t total_q, int32_t max_blocks, int32_t num_q_heads,
+                                        int32_t max_qlen, int32_t decode_max_qlen, const pkv_cache_desc *desc);
+
+/*
+ * pkv_mixed_attn -- append every row's new tokens, then attend: row b brings
+ * q_b = qo_indptr[b+1] - qo_indptr[b] tokens on top of L_b =
+ * cache_seqlens[b] cached ones (L_b is the length BEFORE this call; the
+ * caller advances it).
+ *
+ *  q                 device bf16 [total_q, num_q_heads, head_dim]; row b's
+ *                    queries are rows qo_indptr[b] .. qo_indptr[b+1]-1.
+ *  k_new, v_new      device bf16 [total_q, num_kv_heads, head_dim], or both
+ *                    NULL.  When given, row b's tokens are written at
+ *                    positions L_b .. L_b + q_b - 1 (as pkv_append: a row
+ *                    whose written pages or length fail appends nothing) and
+ *                    the row holds kv_b = L_b + q_b keys; otherwise the
+ *                    caller appended already and kv_b = L_b.
+ *  qo_indptr         device int32 [batch + 1].
+ *  max_qlen          longest q_b accepted (>= 1): a longer row appends
+ *                    nothing and gets PKV_ERR_QLEN with out = 0, lse = -inf.
+ *  decode_max_qlen   rows with 1 <= q_b <= decode_max_qlen run on the
+ *                    split-KV decode kernel (every K/V tile serves up to 8
+ *                    (query, head) pairs of a kv head); longer rows on the
+ *                    tensor-core prefill kernel, which needs page_size >= 8
+ *                    (PKV_EUNSUPPORTED if max_qlen > decode_max_qlen with
+ *                    smaller pages).  When max_qlen <= decode_max_qlen the
+ *                    prefill kernel is not launched at all.
+ *  out               device bf16 [total_q, num_q_heads, head_dim] (round to
+ *                    nearest even); lse fp32 [total_q, num_q_heads] natural
+ *                    log, or NULL.
+ *  workspace         pkv_mixed_workspace_size bytes (see there).
+ *  batch             0 .. 1024; total_q * num_q_heads < 2^31.
+ * Query i of row b attends keys 0 .. kv_b - q_b + i of its kv head (end
+ * aligned).  Row fates: q_b = 0 writes nothing; an inactive row (L_b < 0)
+ * appends nothing and gets out = 0, lse = -inf, no error; a query range that
+ * is reversed or leaves [0, total_q) sets PKV_ERR_QLEN and writes nothing for
+ * the row (with a decreasing qo_indptr the rows' outputs are unspecified);
+ * kv_b < q_b (attend only) gives PKV_ERR_QLEN; a row whose keys exceed
+ * max_blocks * page_size (PKV_ERR_OVERFLOW) or whose first
+ * ceil(kv_b / page_size) block_table entries hold a page outside
+ * [1, num_pages) (PKV_ERR_PAGE) gets out = 0 and lse = -inf.
+ * Launches up to three kernels on `stream` (append, decode, prefill); no
+ * host sync, no allocation, capturable in a CUDA graph.
+ */
+PKV_API pkv_status pkv_mixed_attn(const pkv_cache_desc *desc, void *k_cache, void *v_cache, const void *q,
+                                  const void *k_new, const void *v_new, const int32_t *qo_indptr,
+                                  const int32_t *block_table, int32_t max_blocks, const int32_t *cache_seqlens,
+                                  int32_t batch, int32_t num_q_heads, int32_t total_q, int32_t max_qlen,
+                                  int32_t decode_max_qlen, float softmax_scale, void *out, float *lse,
+                                  void *workspace, size_t workspace_bytes, int32_t *err_flag, void *stream);
 
 /* ---------------------------------------------------------------------
  * Host page-pool and block-table helpers (no device memory involved).

@@ -13,10 +13,14 @@ from .api import (  # noqa: F401
     PkvError,
     cache_desc,
     decode_workspace,
+    default_decode_max_qlen,
+    mixed_workspace,
     pkv_append,
     pkv_decode_bucket,
     pkv_decode_attn,
     pkv_decode_workspace_size,
+    pkv_mixed_attn,
+    pkv_mixed_workspace_size,
     pkv_pool_bytes,
     pkv_prefill_attn,
     pkv_prefill_workspace_size,

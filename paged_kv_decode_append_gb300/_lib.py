@@ -46,6 +46,9 @@ SIGNATURES = {
     "pkv_decode_step_destroy": (None, [P]),
     "pkv_prefill_workspace_size": (SIZE, [I32, I32, I32, DESC_P]),
     "pkv_prefill_attn": (I32, [DESC_P, P, P, P, P, P, P, I32, I32, I32, I32, ctypes.c_float, P, P, P, SIZE, P, P]),
+    "pkv_mixed_workspace_size": (SIZE, [I32, I32, I32, I32, I32, I32, DESC_P]),
+    "pkv_mixed_attn": (I32, [DESC_P, P, P, P, P, P, P, P, I32, P, I32, I32, I32, I32, I32, ctypes.c_float, P, P, P,
+                             SIZE, P, P]),
     "pkv_pool_create": (P, [I32]),
     "pkv_pool_destroy": (None, [P]),
     "pkv_pool_alloc": (I32, [P, I32, I32P]),

@@ -239,6 +239,63 @@ def pkv_prefill_attn(k_cache, v_cache, q, qo_indptr, kv_lens, block_table, softm
     return out
 
 
+def pkv_mixed_workspace_size(batch: int, total_q: int, max_blocks: int, num_q_heads: int, max_qlen: int,
+                             decode_max_qlen: int, desc: CacheDesc) -> int:
+    return int(_lib.load().pkv_mixed_workspace_size(batch, total_q, max_blocks, num_q_heads, max_qlen,
+                                                    decode_max_qlen, ctypes.byref(desc)))
+
+
+def default_decode_max_qlen(num_q_heads: int, num_kv_heads: int) -> int:
+    """Longest row the decode kernel takes by default in a mixed step: up to
+    16 (query, head) columns of a kv head (two decode units)."""
+    return max(1, 16 // max(1, num_q_heads // num_kv_heads))
+
+
+def mixed_workspace(batch: int, total_q: int, max_blocks: int, num_q_heads: int, max_qlen: int,
+                    decode_max_qlen: int, desc: CacheDesc, device) -> torch.Tensor:
+    """A zero-filled workspace for pkv_mixed_attn (reusable across calls)."""
+    n = pkv_mixed_workspace_size(batch, total_q, max_blocks, num_q_heads, max_qlen, decode_max_qlen, desc)
+    if n == 0:
+        raise PkvError(EUNSUPPORTED, "pkv_mixed_workspace_size")
+    return torch.zeros(n, dtype=torch.uint8, device=device)
+
+
+def pkv_mixed_attn(k_cache, v_cache, q, k_new, v_new, qo_indptr, block_table, cache_seqlens, softmax_scale: float,
+                   max_qlen: int, decode_max_qlen: int | None = None, out=None, lse=None, workspace=None,
+                   err_flag=None, layout: int = NHD) -> torch.Tensor:
+    """One step of a mixed batch: row b appends its ``qo_indptr[b+1] -
+    qo_indptr[b]`` new tokens (``k_new``/``v_new`` ``[total_q, Hkv, D]``, or
+    both None when already appended) after its ``cache_seqlens[b]`` cached
+    ones, then its query i attends keys ``0 .. kv_b - q_b + i``.  Rows of up
+    to ``decode_max_qlen`` queries run on the decode kernel, longer ones on
+    the prefill kernel.  Returns ``out`` ``[total_q, Hq, D]`` bf16."""
+    for t, n in ((k_cache, "k_cache"), (v_cache, "v_cache"), (q, "q"), (k_new, "k_new"), (v_new, "v_new"),
+                 (out, "out")):
+        _bf16(t, n)
+    for t, n in ((qo_indptr, "qo_indptr"), (block_table, "block_table"), (cache_seqlens, "cache_seqlens"),
+                 (err_flag, "err_flag")):
+        _i32(t, n)
+    if lse is not None and (lse.dtype != torch.float32 or not lse.is_contiguous()):
+        raise ValueError("lse: expected contiguous float32")
+    desc = cache_desc(k_cache, layout)
+    total_q, Hq, D = q.shape
+    B = cache_seqlens.shape[0]
+    if decode_max_qlen is None:
+        decode_max_qlen = default_decode_max_qlen(Hq, desc.num_kv_heads)
+    if out is None:
+        out = torch.empty_like(q)
+    if workspace is None:
+        workspace = mixed_workspace(B, total_q, block_table.shape[1], Hq, max_qlen, decode_max_qlen, desc,
+                                    q.device)
+    st = _lib.load().pkv_mixed_attn(
+        ctypes.byref(desc), _ptr(k_cache), _ptr(v_cache), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(qo_indptr),
+        _ptr(block_table), block_table.shape[1], _ptr(cache_seqlens), B, Hq, total_q, int(max_qlen),
+        int(decode_max_qlen), float(softmax_scale), _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel(),
+        _ptr(err_flag), _stream(q.device))
+    _check(st, "pkv_mixed_attn")
+    return out
+
+
 def pkv_pool_bytes(desc: CacheDesc) -> int:
     return int(_lib.load().pkv_pool_bytes(ctypes.byref(desc)))
 

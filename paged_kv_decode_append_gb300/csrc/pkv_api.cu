@@ -154,6 +154,64 @@ CUresult encode_group_map(CUtensorMap *map, const pkv_cache_desc &d, void *base,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 
+bool encode_decode_maps(const pkv_cache_desc &desc, void *k_cache, void *v_cache, DecodeMaps *maps)
+{
+    const int box = decode_box_tokens(desc.page_size);
+    if (decode_swizzle(desc.page_size)) { // pages of 8+ tokens: token-group boxes
+        return encode_group_map(&maps->k, desc, k_cache, box) == CUDA_SUCCESS &&
+               encode_group_map(&maps->v, desc, v_cache, box) == CUDA_SUCCESS &&
+               encode_group_map(&maps->k8, desc, k_cache, kDecodeSmallBox) == CUDA_SUCCESS &&
+               encode_group_map(&maps->v8, desc, v_cache, kDecodeSmallBox) == CUDA_SUCCESS;
+    }
+    // pages of 1, 2 or 4 tokens: unswizzled 64-column boxes
+    if (encode_pool_map(&maps->k, desc, k_cache, box, 64, 0) != CUDA_SUCCESS ||
+        encode_pool_map(&maps->v, desc, v_cache, box, 64, 0) != CUDA_SUCCESS)
+        return false;
+    maps->k8 = maps->k;
+    maps->v8 = maps->v;
+    return true;
+}
+
+// Static split of a mixed step: the decode kernel's multi-query shape, and
+// whether (and where in the workspace) the prefill kernel runs.
+struct MixedShape {
+    int dq;            // longest query range the decode kernel serves
+    bool prefill;      // rows longer than dq exist: the prefill kernel runs
+    DecodeShape dshape;
+    PrefillShape pshape;
+    size_t off_prefill; // prefill plan in the workspace
+    size_t bytes;
+};
+
+pkv_status mixed_shape(const pkv_cache_desc *desc, int32_t batch, int32_t total_q, int32_t max_blocks,
+                       int32_t num_q_heads, int32_t max_qlen, int32_t decode_max_qlen, MixedShape *m)
+{
+    const pkv_status st = check_desc(desc);
+    if (st != PKV_OK)
+        return st;
+    if (batch < 0 || total_q < 0 || max_blocks < 1 || num_q_heads < 1 || max_qlen < 1 || decode_max_qlen < 1)
+        return PKV_EINVAL;
+    if (num_q_heads % desc->num_kv_heads != 0)
+        return PKV_EINVAL;
+    if (batch > kMaxDecodeBatch || batch > kMaxPrefillBatch)
+        return PKV_EUNSUPPORTED;
+    // output rows (one per query and head) are numbered in int32
+    if ((int64_t)total_q * num_q_heads >= ((int64_t)1 << 31))
+        return PKV_EUNSUPPORTED;
+    m->dq = decode_max_qlen < max_qlen ? decode_max_qlen : max_qlen;
+    m->prefill = max_qlen > m->dq;
+    if (!decode_mq_shape(batch, max_blocks, num_q_heads, m->dq, *desc, &m->dshape))
+        return PKV_EUNSUPPORTED;
+    m->off_prefill = (m->dshape.bytes + 255) & ~size_t(255);
+    m->bytes = m->off_prefill;
+    if (m->prefill) {
+        if (!prefill_shape(batch, total_q, num_q_heads, *desc, &m->pshape))
+            return PKV_EUNSUPPORTED; // e.g. pages of fewer than 8 tokens
+        m->bytes += m->pshape.bytes;
+    }
+    return PKV_OK;
+}
+
 pkv_status decode_check(const pkv_cache_desc *desc, const void *k_cache, const void *v_cache, const void *q,
                         const void *k_new, const void *v_new, const int32_t *block_table, int32_t max_blocks,
                         const int32_t *cache_seqlens, int32_t batch, int32_t num_q_heads, float softmax_scale,
@@ -321,21 +379,9 @@ pkv_status pkv_decode_attn_ex(const pkv_cache_desc *desc, void *k_cache, void *v
     a.grid = decode_target_items(dev, desc->head_dim, shape.heads_per_cta);
     a.flags = flags;
 
-    const int box = decode_box_tokens(desc->page_size);
     DecodeMaps maps;
-    if (decode_swizzle(desc->page_size)) { // pages of 8+ tokens: token-group boxes
-        if (encode_group_map(&maps.k, *desc, k_cache, box) != CUDA_SUCCESS ||
-            encode_group_map(&maps.v, *desc, v_cache, box) != CUDA_SUCCESS ||
-            encode_group_map(&maps.k8, *desc, k_cache, kDecodeSmallBox) != CUDA_SUCCESS ||
-            encode_group_map(&maps.v8, *desc, v_cache, kDecodeSmallBox) != CUDA_SUCCESS)
-            return PKV_ECUDA;
-    } else { // pages of 1, 2 or 4 tokens: unswizzled 64-column boxes
-        if (encode_pool_map(&maps.k, *desc, k_cache, box, 64, 0) != CUDA_SUCCESS ||
-            encode_pool_map(&maps.v, *desc, v_cache, box, 64, 0) != CUDA_SUCCESS)
-            return PKV_ECUDA;
-        maps.k8 = maps.k;
-        maps.v8 = maps.v;
-    }
+    if (!encode_decode_maps(*desc, k_cache, v_cache, &maps))
+        return PKV_ECUDA;
     return launch_decode(a, maps, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PKV_OK : PKV_ECUDA;
 }
 
@@ -399,6 +445,134 @@ pkv_status pkv_prefill_attn(const pkv_cache_desc *desc, const void *k_cache, con
         encode_group_map(&maps.v, *desc, const_cast<void *>(v_cache), box) != CUDA_SUCCESS)
         return PKV_ECUDA;
     return launch_prefill(a, maps, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PKV_OK : PKV_ECUDA;
+}
+
+size_t pkv_mixed_workspace_size(int32_t batch, int32_t total_q, int32_t max_blocks, int32_t num_q_heads,
+                                int32_t max_qlen, int32_t decode_max_qlen, const pkv_cache_desc *desc)
+{
+    MixedShape m;
+    if (mixed_shape(desc, batch, total_q, max_blocks, num_q_heads, max_qlen, decode_max_qlen, &m) != PKV_OK)
+        return 0;
+    return m.bytes;
+}
+
+pkv_status pkv_mixed_attn(const pkv_cache_desc *desc, void *k_cache, void *v_cache, const void *q, const void *k_new,
+                          const void *v_new, const int32_t *qo_indptr, const int32_t *block_table, int32_t max_blocks,
+                          const int32_t *cache_seqlens, int32_t batch, int32_t num_q_heads, int32_t total_q,
+                          int32_t max_qlen, int32_t decode_max_qlen, float softmax_scale, void *out, float *lse,
+                          void *workspace, size_t workspace_bytes, int32_t *err_flag, void *stream)
+{
+    MixedShape m;
+    pkv_status st = mixed_shape(desc, batch, total_q, max_blocks, num_q_heads, max_qlen, decode_max_qlen, &m);
+    if (st != PKV_OK)
+        return st;
+    if (!isfinite(softmax_scale) || (k_new == nullptr) != (v_new == nullptr))
+        return PKV_EINVAL;
+    if (batch == 0)
+        return PKV_OK;
+    if (k_cache == nullptr || v_cache == nullptr || qo_indptr == nullptr || block_table == nullptr ||
+        cache_seqlens == nullptr || (total_q > 0 && (q == nullptr || out == nullptr)))
+        return PKV_EINVAL;
+    if (!aligned16(k_cache) || !aligned16(v_cache) || !aligned16(q) || !aligned16(out) ||
+        (k_new != nullptr && (!aligned16(k_new) || !aligned16(v_new))))
+        return PKV_EINVAL;
+    if (workspace == nullptr || workspace_bytes < m.bytes || !aligned16(workspace))
+        return PKV_EWORKSPACE;
+    const int dev = current_device();
+    if (dev < 0)
+        return PKV_ECUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const float q_scale = softmax_scale * 1.4426950408889634f;
+
+    // 1. the new tokens of every row into the cache (rows longer than max_qlen append nothing)
+    if (k_new != nullptr && total_q > 0) {
+        AppendArgs a;
+        a.desc = *desc;
+        a.page_shift = log2_exact(desc->page_size);
+        a.k_cache = k_cache;
+        a.v_cache = v_cache;
+        a.k_new = k_new;
+        a.v_new = v_new;
+        a.num_tokens = total_q;
+        a.append_indptr = qo_indptr;
+        a.block_table = block_table;
+        a.max_blocks = max_blocks;
+        a.cache_seqlens = cache_seqlens;
+        a.batch = batch;
+        a.err_flag = err_flag;
+        a.max_count = max_qlen;
+        if (launch_append(a, s) != cudaSuccess)
+            return PKV_ECUDA;
+    }
+
+    // 2. rows of 1 .. dq queries: the split-KV decode kernel, (query, head) columns
+    {
+        DecodeArgs a;
+        a.desc = *desc;
+        a.page_shift = log2_exact(desc->page_size);
+        a.batch = batch;
+        a.num_q_heads = num_q_heads;
+        a.max_blocks = max_blocks;
+        a.q_scale = q_scale;
+        a.block_table = block_table;
+        a.cache_seqlens = cache_seqlens;
+        a.q = q;
+        a.k_new = nullptr;
+        a.v_new = nullptr;
+        a.k_cache = k_cache;
+        a.v_cache = v_cache;
+        a.out = out;
+        a.lse = lse;
+        a.workspace = workspace;
+        a.err_flag = err_flag;
+        a.shape = m.dshape;
+        a.target_items = 0;
+        a.grid = decode_target_items(dev, desc->head_dim, m.dshape.heads_per_cta, true);
+        a.flags = 0;
+        a.qo_indptr = qo_indptr;
+        a.total_q = total_q;
+        a.mq_hi = m.dq;
+        a.mq_max = max_qlen;
+        a.mq_own_long = m.prefill ? 0 : 1;
+        a.mq_kv_add = k_new != nullptr ? 1 : 0;
+        DecodeMaps maps;
+        if (!encode_decode_maps(*desc, k_cache, v_cache, &maps))
+            return PKV_ECUDA;
+        if (launch_decode(a, maps, s) != cudaSuccess)
+            return PKV_ECUDA;
+    }
+
+    // 3. longer rows (prefill chunks): the tcgen05 prefill kernel over kv = L + q keys
+    if (m.prefill) {
+        PrefillArgs a;
+        a.desc = *desc;
+        a.batch = batch;
+        a.num_q_heads = num_q_heads;
+        a.total_q = total_q;
+        a.max_blocks = max_blocks;
+        a.q_scale = q_scale;
+        a.qo_indptr = qo_indptr;
+        a.kv_lens = nullptr;
+        a.block_table = block_table;
+        a.q = q;
+        a.out = out;
+        a.lse = lse;
+        a.workspace = static_cast<unsigned char *>(workspace) + m.off_prefill;
+        a.err_flag = err_flag;
+        a.shape = m.pshape;
+        a.cache_seqlens = cache_seqlens;
+        a.q_lo = m.dq;
+        a.q_max = max_qlen;
+        a.kv_add = k_new != nullptr ? 1 : 0;
+        const int box = prefill_box_tokens(desc->page_size);
+        PrefillMaps maps;
+        if (encode_group_map(&maps.k, *desc, k_cache, box) != CUDA_SUCCESS ||
+            encode_group_map(&maps.v, *desc, v_cache, box) != CUDA_SUCCESS)
+            return PKV_ECUDA;
+        if (launch_prefill(a, maps, s) != cudaSuccess)
+            return PKV_ECUDA;
+    }
+    return PKV_OK;
 }
 
 } // extern "C"

@@ -23,6 +23,7 @@ struct AParams {
     const int32_t *seqlens;
     int32_t *err_flag;
     int num_tokens, batch, max_blocks, page_size, page_shift, num_pages, num_kv_heads, head_dim, layout;
+    int max_count; // rows appending more tokens than this append nothing
 };
 
 // One CTA per new token.
@@ -52,8 +53,11 @@ __global__ void __launch_bounds__(kAppendThreads) append_kernel(const __grid_con
     __syncthreads();
     const int b = s_row, count = s_count;
     const int L = p.seqlens[b];
-    if (L < 0 || t - s_first >= count)
-        return; // inactive row (or a malformed indptr gap)
+    // inactive row; a token outside its row's range (a malformed indptr); a
+    // row whose range leaves [0, num_tokens) or that is longer than allowed
+    if (L < 0 || t < s_first || t - s_first >= count || s_first < 0 || count > p.num_tokens - s_first ||
+        count > p.max_count)
+        return;
     // validate the row's destination range [L, L + count)
     const int32_t *bt_row = p.block_table + (int64_t)b * p.max_blocks;
     int err = 0;
@@ -115,6 +119,7 @@ cudaError_t launch_append(const AppendArgs &a, cudaStream_t stream)
     p.num_kv_heads = a.desc.num_kv_heads;
     p.head_dim = a.desc.head_dim;
     p.layout = a.desc.layout;
+    p.max_count = a.max_count;
     append_kernel<<<a.num_tokens, kAppendThreads, 0, stream>>>(p);
     return cudaGetLastError();
 }

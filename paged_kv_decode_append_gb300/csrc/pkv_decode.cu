@@ -12,9 +12,10 @@
 //
 // GB300 design (one persistent CTA per resident slot, five warps):
 //  * producer warp: streams 32-token tiles of K and V of one kv head through
-//    a shared-memory ring with TMA (one box per page piece and 64-column
-//    half row, 128-byte swizzle, L2 evict-first); page ids are prefetched 32
-//    at a time into registers, one window (and one slice) ahead.
+//    a shared-memory ring with TMA (one box per page piece with all of
+//    head_dim, landing as 8-token groups, 128-byte swizzle, L2 evict-first);
+//    page ids are prefetched 32 at a time into registers, one window (and one
+//    slice) ahead.
 //  * two consumer warps: 16 token rows of every tile each, on tensor-core
 //    tiles (mma.sync m16n8k16, bf16 in, fp32 accumulate) with an online
 //    softmax in base 2; see consume_tile.  At the end of a slice they hand
@@ -35,6 +36,15 @@
 //    host.  A unit slice is always the first or the last slice of its CTA,
 //    so two workspace slots per CTA hold every partial.
 //  * Every block_table entry is range-checked before an address is formed.
+//
+// Multi-query rows (the decode rows of a mixed step, pkv_mixed_attn): row b
+// owns query rows qo_indptr[b] .. qo_indptr[b+1]-1 whose new tokens are
+// already in the cache, so it holds kv = L + q keys and its query i sees keys
+// 0 .. kv - q + i (the end-aligned causal rule of "[flashinfer] H100 D256
+// paged attention cuDNN auto-dispatch", code analysis part 1).  A unit's
+// columns are then (query, head) pairs, query-major, GC of them per unit:
+// every K/V tile read serves all of a kv head's heads for GC / G queries, and
+// the tiles past kv - q + 1 mask each column at its own limit.
 #include <math.h>
 
 #include "pkv_device.cuh"
@@ -56,7 +66,10 @@ constexpr float kNegInf = -INFINITY;
 
 static_assert(kTile == 16 * kWarps, "each consumer warp owns 16 rows of a tile");
 
-enum RowStatus { ROW_OK = 0, ROW_INACTIVE = 1, ROW_OVERFLOW = 2 };
+// ROW_QLEN: a malformed query length (multi-query rows): zero output.
+// ROW_NONE: no output of this kernel (no query, or a row another kernel of
+// the mixed step serves, or a query range outside [0, total_q)).
+enum RowStatus { ROW_OK = 0, ROW_INACTIVE = 1, ROW_OVERFLOW = 2, ROW_QLEN = 3, ROW_NONE = 4 };
 
 struct KParams {
     const int32_t *block_table;
@@ -78,6 +91,14 @@ struct KParams {
     int pdl;      // launched with programmatic dependent launch
     int early_kv; // ... and the K/V cache may be read before the preceding grid completes
     float q_scale;
+    // Multi-query rows: q / out / lse are [total_q, Hq, ...] and row b owns
+    // rows qo_indptr[b] .. qo_indptr[b+1]-1 (nullptr: one query per row).
+    const int32_t *qo_indptr;
+    int total_q, group_shift;
+    int mq_hi;       // rows with 1 <= q_len <= mq_hi are this kernel's
+    int mq_max;      // q_len > mq_max is malformed (PKV_ERR_QLEN) ...
+    int mq_own_long; // ... and zeroed here when no other kernel serves long rows
+    int mq_kv_add;   // 1: the row's new tokens are cached (kv = L + q_len); 0: kv = L
 };
 
 // K/V stages in flight per CTA, as many as keep two CTAs on an SM (head_dim
@@ -88,7 +109,7 @@ constexpr int stages_for()
     return D == 256 ? 3 : (D == 128 ? (GC <= 4 ? 5 : 4) : 6);
 }
 
-template <int D, int GC>
+template <int D, int GC, bool MQ>
 struct Smem {
     static constexpr int kStages = stages_for<D, GC>();
     // [stage][K|V] tiles laid out [kTile/8][D/64][8][64]: 8-token groups of
@@ -102,12 +123,13 @@ struct Smem {
     uint64_t epi_full[kSlots], epi_empty[kSlots];
     int32_t stage_bad[kStages];
     int32_t len[kMaxDecodeBatch];
+    int32_t qlen[MQ ? kMaxDecodeBatch : 1]; // multi-query rows: q_len (-1: range outside [0, total_q))
     int32_t rowtok[kMaxDecodeBatch + 1]; // prefix of cache tokens per row
     long long rowbase[kMaxDecodeBatch + 1]; // first work position of every row
     long long work;                      // units * rowtok[batch]
     long long slice;                     // work positions per CTA
     int32_t geff;                        // CTAs that own a token slice
-    int32_t n_empty;                     // rows without a cached token
+    int32_t n_empty;                     // rows with output units but no cached token
     int32_t abort;
 };
 
@@ -135,6 +157,35 @@ __device__ __forceinline__ int row_status(const KParams &p, int L)
     return ROW_OK;
 }
 
+// Status of a multi-query row with L cached tokens and qn queries (qn < 0:
+// a query range outside [0, total_q)); *kv gets the keys it holds.
+__device__ __forceinline__ int mq_row_status(const KParams &p, int L, int qn, int *kv)
+{
+    *kv = 0;
+    if (qn <= 0 || (qn > p.mq_hi && qn <= p.mq_max) || (qn > p.mq_max && !p.mq_own_long))
+        return ROW_NONE;
+    if (qn > p.mq_max)
+        return ROW_QLEN;
+    if (L < 0)
+        return ROW_INACTIVE;
+    const int64_t keys = (int64_t)L + (p.mq_kv_add ? qn : 0);
+    if (keys < qn)
+        return ROW_QLEN;
+    if (keys > (int64_t)p.max_blocks * p.page_size)
+        return ROW_OVERFLOW;
+    *kv = (int)keys;
+    return ROW_OK;
+}
+
+// Output units of a multi-query row: GC (query, head) columns per unit.
+template <int GC>
+__device__ __forceinline__ int mq_units(const KParams &p, int status, int qn)
+{
+    if (status == ROW_NONE)
+        return 0;
+    return p.num_kv_heads * (int)(((int64_t)qn * p.group + GC - 1) / GC);
+}
+
 // Mbarrier wait that also gives up when another warp of the CTA aborted.
 __device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, volatile int32_t *abort)
 {
@@ -158,12 +209,13 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, vo
 // Every CTA derives the same plan from cache_seqlens.  Work is laid out as a
 // line: every (row, kv head, head group) unit with n > 0 cached tokens takes
 // kSliceStartCost virtual positions followed by its n token positions, units
-// in row-major order.  CTA k takes positions [k * slice, (k+1) * slice),
+// in row-major order (multi-query rows: as many units per kv head as their
+// (query, head) columns need).  CTA k takes positions [k * slice, (k+1) * slice),
 // moved to token positions (see boundary), so the per-unit cost of starting
 // a slice (page ids, queries, a hand-off to the epilogue) is balanced along
 // with the tokens.
-template <int D, int GC>
-__device__ void build_plan(const KParams &p, Smem<D, GC> &sm)
+template <int D, int GC, bool MQ>
+__device__ void build_plan_rows(const KParams &p, Smem<D, GC, MQ> &sm)
 {
     for (int i = threadIdx.x; i < p.batch; i += kThreads)
         sm.len[i] = p.seqlens[i];
@@ -212,12 +264,83 @@ __device__ void build_plan(const KParams &p, Smem<D, GC> &sm)
     __syncthreads();
 }
 
+// Multi-query rows: units per row differ, so the work positions are summed directly.
+template <int D, int GC, bool MQ>
+__device__ void build_plan_mq(const KParams &p, Smem<D, GC, MQ> &sm)
+{
+    for (int i = threadIdx.x; i < p.batch; i += kThreads) {
+        sm.len[i] = p.seqlens[i];
+        const int s = p.qo_indptr[i], e = p.qo_indptr[i + 1];
+        sm.qlen[i] = (s < 0 || e > p.total_q || e < s) ? -1 : e - s;
+    }
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        const int lane = threadIdx.x;
+        int run = 0, empty = 0;
+        long long wrun = 0;
+        for (int base = 0; base < p.batch; base += 32) {
+            const int i = base + lane;
+            int n = 0, u = 0; // cached tokens read, output units
+            if (i < p.batch) {
+                int kv;
+                const int st = mq_row_status(p, sm.len[i], sm.qlen[i], &kv);
+                n = kv;
+                u = mq_units<GC>(p, st, sm.qlen[i]);
+            }
+            // work positions of the row: every unit costs the slice start plus its tokens
+            const long long w = n > 0 ? (long long)u * (n + kSliceStartCost) : 0;
+            empty += __popc(__ballot_sync(0xffffffffu, n == 0 && u > 0));
+            int incl = n;
+            long long wincl = w;
+            for (int o = 1; o < 32; o <<= 1) {
+                const int v = __shfl_up_sync(0xffffffffu, incl, o);
+                const long long wv = __shfl_up_sync(0xffffffffu, wincl, o);
+                if (lane >= o) {
+                    incl += v;
+                    wincl += wv;
+                }
+            }
+            if (i < p.batch) {
+                sm.rowtok[i] = run + incl - n;
+                sm.rowbase[i] = wrun + wincl - w;
+            }
+            run += __shfl_sync(0xffffffffu, incl, 31);
+            wrun += __shfl_sync(0xffffffffu, wincl, 31);
+        }
+        if (lane == 0) {
+            sm.rowtok[p.batch] = run;
+            sm.rowbase[p.batch] = wrun;
+            const long long work = wrun;
+            long long g = work / kMinSlice;
+            if (g > gridDim.x)
+                g = gridDim.x;
+            if (g < 1)
+                g = 1;
+            const long long slice = work > 0 ? (work + g - 1) / g : 1;
+            sm.work = work;
+            sm.slice = slice;
+            sm.n_empty = empty;
+            sm.geff = work > 0 ? (int)((work + slice - 1) / slice) : 1;
+        }
+    }
+    __syncthreads();
+}
+
+template <int D, int GC, bool MQ>
+__device__ __forceinline__ void build_plan(const KParams &p, Smem<D, GC, MQ> &sm)
+{
+    if constexpr (MQ)
+        build_plan_mq(p, sm);
+    else
+        build_plan_rows(p, sm);
+}
+
 // Unit containing work position x (x < work): row b, unit r in the row and
 // the offset rel inside the unit's kSliceStartCost + n positions; returns the
 // unit's first token position.  units * (row tokens + cost) < 2^31 (checked
 // on the host), so in-row math is 32-bit.
-template <int D, int GC>
-__device__ __forceinline__ long long locate(const KParams &p, const Smem<D, GC> &sm, long long x, int &b, int &r,
+template <int D, int GC, bool MQ>
+__device__ __forceinline__ long long locate(const KParams &p, const Smem<D, GC, MQ> &sm, long long x, int &b, int &r,
                                             int &rel)
 {
     int lo = 0, hi = p.batch - 1; // largest row starting at or before x (never an empty row)
@@ -240,8 +363,8 @@ __device__ __forceinline__ long long locate(const KParams &p, const Smem<D, GC> 
 // First position of CTA k's range (k in [0, geff]): k * slice moved to a
 // token position -- the unit's first token if it falls on the unit's virtual
 // positions, else rounded down to a multiple of the tile inside the unit.
-template <int D, int GC>
-__device__ __forceinline__ long long boundary(const KParams &p, const Smem<D, GC> &sm, int k)
+template <int D, int GC, bool MQ>
+__device__ __forceinline__ long long boundary(const KParams &p, const Smem<D, GC, MQ> &sm, int k)
 {
     const long long x = (long long)k * sm.slice;
     if (x >= sm.work)
@@ -254,8 +377,8 @@ __device__ __forceinline__ long long boundary(const KParams &p, const Smem<D, GC
 
 // CTA whose range holds token position x (x < work): close to x / slice, the
 // boundaries being at most kTile below or kSliceStartCost above k * slice.
-template <int D, int GC>
-__device__ __forceinline__ int owner_of(const KParams &p, const Smem<D, GC> &sm, long long x)
+template <int D, int GC, bool MQ>
+__device__ __forceinline__ int owner_of(const KParams &p, const Smem<D, GC, MQ> &sm, long long x)
 {
     int k = (int)(x / sm.slice);
     if (k > sm.geff - 1)
@@ -271,7 +394,37 @@ struct Seg {
     int b, r, kvh, sub, unit, L, status, tok0, tok1;
     long long u0; // unit's first token position
     int n;        // unit's cache tokens
+    int qn, qs;   // multi-query rows: queries and the first query row (else 1, b)
+    int mask_from; // first token some column of the unit may not see (n: none)
 };
+
+// Row-level fields of unit r of row b (everything but the token range).
+template <int D, int GC, bool MQ>
+__device__ __forceinline__ void seg_unit(const KParams &p, const Smem<D, GC, MQ> &sm, Seg &s, int b, int r)
+{
+    s.b = b;
+    s.r = r;
+    s.unit = b * p.units + r;
+    s.L = sm.len[b];
+    if constexpr (MQ) {
+        int kv;
+        s.qn = sm.qlen[b];
+        s.status = mq_row_status(p, s.L, s.qn, &kv);
+        const int n_sub = max(1, (int)(((int64_t)s.qn * p.group + GC - 1) / GC));
+        s.kvh = r / n_sub;
+        s.sub = r - s.kvh * n_sub;
+        s.qs = s.status == ROW_NONE ? 0 : p.qo_indptr[b];
+        // column c of the unit is query (sub * GC + c) >> group_shift, which sees kv - qn + query + 1 keys
+        s.mask_from = kv - s.qn + ((s.sub * GC) >> p.group_shift) + 1;
+    } else {
+        s.qn = 1;
+        s.qs = b;
+        s.status = row_status(p, s.L);
+        s.kvh = r / p.n_sub;
+        s.sub = r - s.kvh * p.n_sub;
+        s.mask_from = 0x7fffffff;
+    }
+}
 
 // Walks the slices of one CTA's range [pos0, end), one unit each.  The two
 // boundary slices come first (the range's first and last unit, the only ones
@@ -282,8 +435,8 @@ struct SegIter {
     long long t0_f, t0_l;
     int b_f, r_f, b_l, r_l;
     int stage; // 0: first slice, 1: last slice, 2: middle units, 3: done
-    template <int D, int GC>
-    __device__ __forceinline__ void init(const KParams &p, const Smem<D, GC> &sm, int k)
+    template <int D, int GC, bool MQ>
+    __device__ __forceinline__ void init(const KParams &p, const Smem<D, GC, MQ> &sm, int k)
     {
         stage = 3;
         if (k >= sm.geff)
@@ -301,24 +454,18 @@ struct SegIter {
         f_end = min(end, t0_f + (sm.rowtok[b_f + 1] - sm.rowtok[b_f]));
         stage = 0;
     }
-    template <int D, int GC>
-    __device__ __forceinline__ void fill(const KParams &p, const Smem<D, GC> &sm, Seg &s, int b, int r, long long t0,
+    template <int D, int GC, bool MQ>
+    __device__ __forceinline__ void fill(const KParams &p, const Smem<D, GC, MQ> &sm, Seg &s, int b, int r, long long t0,
                                          long long from, long long to)
     {
-        s.b = b;
-        s.r = r;
+        seg_unit(p, sm, s, b, r);
         s.u0 = t0;
         s.n = sm.rowtok[b + 1] - sm.rowtok[b];
         s.tok0 = (int)(from - t0);
         s.tok1 = (int)(to - t0);
-        s.kvh = r / p.n_sub;
-        s.sub = r - s.kvh * p.n_sub;
-        s.unit = b * p.units + r;
-        s.L = sm.len[b];
-        s.status = row_status(p, s.L);
     }
-    template <int D, int GC>
-    __device__ __forceinline__ bool next(const KParams &p, const Smem<D, GC> &sm, Seg &s)
+    template <int D, int GC, bool MQ>
+    __device__ __forceinline__ bool next(const KParams &p, const Smem<D, GC, MQ> &sm, Seg &s)
     {
         if (stage == 0) {
             fill(p, sm, s, b_f, r_f, t0_f, pos0, f_end);
@@ -364,10 +511,10 @@ __device__ __forceinline__ int load_window(const int32_t *bt_row, int first, int
     return first + lane <= last ? bt_row[first + lane] : 0;
 }
 
-template <int D, int GC>
-__device__ void producer(const KParams &p, Smem<D, GC> &sm, const DecodeMaps *maps)
+template <int D, int GC, bool MQ>
+__device__ void producer(const KParams &p, Smem<D, GC, MQ> &sm, const DecodeMaps *maps)
 {
-    constexpr int S = Smem<D, GC>::kStages;
+    constexpr int S = Smem<D, GC, MQ>::kStages;
     const int lane = threadIdx.x & 31;
     const uint64_t policy = l2_evict_first_policy();
     const int box = p.box_tokens;
@@ -552,10 +699,13 @@ __device__ __forceinline__ uint32_t tile_addr(uint32_t base, int row, int chunk,
     return base + (uint32_t)((((row >> 3) * (D / 64) + blk) * 8 + (row & 7)) * 128 + ((c ^ (row & swz)) << 4));
 }
 
-template <int D, bool MASKED>
-__device__ __forceinline__ void consume_tile(const __nv_bfloat16 *Kt, __nv_bfloat16 *Vt, int nv, int warp, int lane,
-                                             int swz, float scale, const uint32_t (&qf)[D / 16][2],
-                                             float (&acc)[D / 16][4], float (&m_run)[2], float (&l_run)[2])
+// MASKED: token rows >= nv hold no token, and column 2c + j (c = lane & 3)
+// sees only the tile's rows below lim[j] (multi-query rows; else lim >= nv).
+template <int D, bool MASKED, bool MQ>
+__device__ __forceinline__ void consume_tile(const __nv_bfloat16 *Kt, __nv_bfloat16 *Vt, int nv, int lim0, int lim1,
+                                             int warp, int lane, int swz, float scale,
+                                             const uint32_t (&qf)[D / 16][2], float (&acc)[D / 16][4],
+                                             float (&m_run)[2], float (&l_run)[2])
 {
     constexpr int KS = D / 16;
     const int row0 = warp * 16;
@@ -587,7 +737,17 @@ __device__ __forceinline__ void consume_tile(const __nv_bfloat16 *Kt, __nv_bfloa
 #pragma unroll
     for (int i = 0; i < 4; ++i)
         v[i] = (sa[i] + sb[i]) * scale;
-    if (MASKED) {
+    if constexpr (MASKED && MQ) {
+        const int e0 = min(nv, lim0), e1 = min(nv, lim1);
+        if (row0 + g >= e0)
+            v[0] = kNegInf;
+        if (row0 + g >= e1)
+            v[1] = kNegInf;
+        if (row0 + g + 8 >= e0)
+            v[2] = kNegInf;
+        if (row0 + g + 8 >= e1)
+            v[3] = kNegInf;
+    } else if constexpr (MASKED) {
         if (row0 + g >= nv)
             v[0] = v[1] = kNegInf;
         if (row0 + g + 8 >= nv)
@@ -652,27 +812,50 @@ __device__ __forceinline__ int slot_of(int kf, int j)
     return j == 0 ? 2 * kf + 1 : 2 * (kf + j);
 }
 
-// B fragments of Q^T for one slice: head g of the slice's head group (zero
-// beyond GC), dims 16ks + 2c (+8).
-template <int D, int GC>
+// Row of q / out / lse (one row per (query, head)) of column c of a unit, or
+// -1 for a column past the unit's (query, head) pairs.  Rows number fewer
+// than 2^31 (checked on the host).
+template <int GC, bool MQ>
+__device__ __forceinline__ int column_row(const KParams &p, const Seg &sg, int c)
+{
+    if constexpr (!MQ)
+        return sg.b * p.num_q_heads + sg.kvh * p.group + sg.sub * GC + c;
+    const int col = sg.sub * GC + c;
+    if (c >= GC || col >= sg.qn * p.group)
+        return -1;
+    return (sg.qs + (col >> p.group_shift)) * p.num_q_heads + sg.kvh * p.group + (col & (p.group - 1));
+}
+
+// Keys column c of a unit sees (multi-query rows; else all of them).
+template <int GC, bool MQ>
+__device__ __forceinline__ int column_keys(const KParams &p, const Seg &sg, int c)
+{
+    if constexpr (!MQ)
+        return 0x7fffffff;
+    return sg.mask_from + ((sg.sub * GC + c) >> p.group_shift) - ((sg.sub * GC) >> p.group_shift);
+}
+
+// B fragments of Q^T for one slice: column g of the unit (zero beyond its
+// columns), dims 16ks + 2c (+8).
+template <int D, int GC, bool MQ>
 __device__ __forceinline__ void load_q(const KParams &p, const Seg &sg, int lane, uint32_t (&qf)[D / 16][2])
 {
     const int g = lane >> 2, c = lane & 3;
-    const int h0 = sg.kvh * p.group + sg.sub * GC;
-    const uint32_t *qrow = reinterpret_cast<const uint32_t *>(p.q + ((int64_t)sg.b * p.num_q_heads + h0 + g) * D);
+    const int row = g < GC ? column_row<GC, MQ>(p, sg, g) : -1;
+    const uint32_t *qrow = reinterpret_cast<const uint32_t *>(p.q + (int64_t)(row < 0 ? 0 : row) * D);
 #pragma unroll
     for (int ks = 0; ks < D / 16; ++ks) {
-        qf[ks][0] = g < GC ? __ldg(qrow + 8 * ks + c) : 0u;
-        qf[ks][1] = g < GC ? __ldg(qrow + 8 * ks + 4 + c) : 0u;
+        qf[ks][0] = row >= 0 ? __ldg(qrow + 8 * ks + c) : 0u;
+        qf[ks][1] = row >= 0 ? __ldg(qrow + 8 * ks + 4 + c) : 0u;
     }
 }
 
 // Consumer warp: runs the tile loop of every slice of this CTA and hands each
 // slice's softmax state (o, m, l per head) to an epilogue warp.
-template <int D, int GC>
-__device__ void consumers(const KParams &p, Smem<D, GC> &sm)
+template <int D, int GC, bool MQ>
+__device__ void consumers(const KParams &p, Smem<D, GC, MQ> &sm)
 {
-    constexpr int S = Smem<D, GC>::kStages;
+    constexpr int S = Smem<D, GC, MQ>::kStages;
     constexpr int KS = D / 16;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, c = lane & 3;
@@ -685,7 +868,8 @@ __device__ void consumers(const KParams &p, Smem<D, GC> &sm)
     uint32_t qf[KS][2];
     wait_prior_grid(p);
     if (have)
-        load_q<D, GC>(p, sg, lane, qf);
+        load_q<D, GC, MQ>(p, sg, lane, qf);
+    int lim0 = have ? column_keys<GC, MQ>(p, sg, 2 * c) : 0, lim1 = have ? column_keys<GC, MQ>(p, sg, 2 * c + 1) : 0;
     uint32_t g_tile = 0;
     int seg_i = 0;
     while (have) {
@@ -706,13 +890,14 @@ __device__ void consumers(const KParams &p, Smem<D, GC> &sm)
                 break;
             }
             bad |= ((volatile int32_t *)sm.stage_bad)[s];
-            const int nv = min(kTile, sg.tok1 - (sg.tok0 + t * kTile));
-            if (nv == kTile) {
-                consume_tile<D, false>(sm.kv[s][0], sm.kv[s][1], nv, warp, lane, swz, p.q_scale, qf, acc, m_run,
-                                       l_run);
+            const int tstart = sg.tok0 + t * kTile;
+            const int nv = min(kTile, sg.tok1 - tstart);
+            if (nv == kTile && (!MQ || tstart + kTile <= sg.mask_from)) {
+                consume_tile<D, false, MQ>(sm.kv[s][0], sm.kv[s][1], nv, 0, 0, warp, lane, swz, p.q_scale, qf, acc,
+                                       m_run, l_run);
             } else {
-                consume_tile<D, true>(sm.kv[s][0], sm.kv[s][1], nv, warp, lane, swz, p.q_scale, qf, acc, m_run,
-                                      l_run);
+                consume_tile<D, true, MQ>(sm.kv[s][0], sm.kv[s][1], nv, lim0 - tstart, lim1 - tstart, warp, lane, swz,
+                                      p.q_scale, qf, acc, m_run, l_run);
                 // the zeroed V rows were written by the generic proxy; order
                 // them before the TMA that refills this stage
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -723,7 +908,7 @@ __device__ void consumers(const KParams &p, Smem<D, GC> &sm)
             if (t == 0) {
                 more = si.next(p, sm, nx);
                 if (more)
-                    load_q<D, GC>(p, nx, lane, qn);
+                    load_q<D, GC, MQ>(p, nx, lane, qn);
             }
         }
         if (!ok)
@@ -761,6 +946,10 @@ __device__ void consumers(const KParams &p, Smem<D, GC> &sm)
         ++seg_i;
         have = more;
         sg = nx;
+        if (have) {
+            lim0 = column_keys<GC, MQ>(p, sg, 2 * c);
+            lim1 = column_keys<GC, MQ>(p, sg, 2 * c + 1);
+        }
 #pragma unroll
         for (int ks = 0; ks < KS; ++ks) {
             qf[ks][0] = qn[ks][0];
@@ -828,16 +1017,17 @@ __device__ __forceinline__ void load_epi_inputs(const KParams &p, const Seg &sg,
 
 // Writes one unit's output: zeros for inactive / failed rows, otherwise
 // merges the new token (when given), performs the append and normalises.
-template <int D, int GC>
+template <int D, int GC, bool MQ>
 __device__ void finalize_warp(const KParams &p, const Seg &sg, EpiState<D, GC> &st, const EpiInputs<D, GC> &in,
                               int bad, int lane)
 {
     constexpr int EPT2 = EpiState<D, GC>::EPT2;
     constexpr int KP = EpiInputs<D, GC>::KP;
-    const int h0 = sg.kvh * p.group + sg.sub * GC;
     int err = 0;
     if (sg.status == ROW_OVERFLOW)
         err = PKV_ERR_OVERFLOW;
+    else if (sg.status == ROW_QLEN)
+        err = PKV_ERR_QLEN;
     else if (sg.status == ROW_OK && bad)
         err = PKV_ERR_PAGE;
     if (sg.status == ROW_OK && !err && p.with_new && (in.page < 1 || in.page >= p.num_pages))
@@ -901,22 +1091,54 @@ __device__ void finalize_warp(const KParams &p, const Seg &sg, EpiState<D, GC> &
         any[g] = live && st.L[g] > 0.f;
         inv[g] = any[g] ? 1.f / st.L[g] : 0.f;
     }
-    uint32_t *out = reinterpret_cast<uint32_t *>(p.out + ((int64_t)sg.b * p.num_q_heads + h0) * D);
+    if constexpr (!MQ) {
+        const int h0 = sg.kvh * p.group + sg.sub * GC;
+        uint32_t *out = reinterpret_cast<uint32_t *>(p.out + ((int64_t)sg.b * p.num_q_heads + h0) * D);
+#pragma unroll
+        for (int i = 0; i < EPT2; ++i) {
+            const int e = pair_elem<D>(lane, i), g = e / D;
+            out[e >> 1] = any[g] ? pack_bf16(st.o[i].x * inv[g], st.o[i].y * inv[g]) : 0u;
+        }
+        if (p.lse != nullptr && lane < GC) {
+            float M = kNegInf, L = 0.f;
+#pragma unroll
+            for (int g = 0; g < GC; ++g)
+                if (g == lane) {
+                    M = st.M[g];
+                    L = st.L[g];
+                }
+            const bool any = live && L > 0.f;
+            p.lse[(int64_t)sg.b * p.num_q_heads + h0 + lane] =
+                any ? (M + log2f(L)) * 0.69314718055994531f : kNegInf;
+        }
+        return;
+    }
+    // multi-query rows: output row of every column (-1: a column past the unit's (query, head) pairs)
+    int orow[GC];
+#pragma unroll
+    for (int g = 0; g < GC; ++g)
+        orow[g] = column_row<GC, MQ>(p, sg, g);
+    uint32_t *out = reinterpret_cast<uint32_t *>(p.out);
 #pragma unroll
     for (int i = 0; i < EPT2; ++i) {
         const int e = pair_elem<D>(lane, i), g = e / D;
-        out[e >> 1] = any[g] ? pack_bf16(st.o[i].x * inv[g], st.o[i].y * inv[g]) : 0u;
+        if (orow[g] >= 0)
+            out[((int64_t)orow[g] * D + e % D) >> 1] =
+                any[g] ? pack_bf16(st.o[i].x * inv[g], st.o[i].y * inv[g]) : 0u;
     }
     if (p.lse != nullptr && lane < GC) {
         float M = kNegInf, L = 0.f;
+        int row = -1;
 #pragma unroll
         for (int g = 0; g < GC; ++g)
             if (g == lane) {
                 M = st.M[g];
                 L = st.L[g];
+                row = orow[g];
             }
         const bool any = live && L > 0.f;
-        p.lse[(int64_t)sg.b * p.num_q_heads + h0 + lane] = any ? (M + log2f(L)) * 0.69314718055994531f : kNegInf;
+        if (row >= 0)
+            p.lse[row] = any ? (M + log2f(L)) * 0.69314718055994531f : kNegInf;
     }
 }
 
@@ -978,8 +1200,8 @@ __device__ int combine_warp(const KParams &p, EpiState<D, GC> &st, int kf, int n
     return bad;
 }
 
-template <int D, int GC>
-__device__ void epilogue(const KParams &p, Smem<D, GC> &sm, int ew)
+template <int D, int GC, bool MQ>
+__device__ void epilogue(const KParams &p, Smem<D, GC, MQ> &sm, int ew)
 {
     constexpr int EPT2 = EpiState<D, GC>::EPT2;
     const int lane = threadIdx.x & 31;
@@ -1035,7 +1257,7 @@ __device__ void epilogue(const KParams &p, Smem<D, GC> &sm, int ew)
         if (lane == 0)
             mbar_arrive(&sm.epi_empty[slot]); // consumers may refill this slot
         if (n == 1) {
-            finalize_warp<D, GC>(p, sg, st, in, bad, lane);
+            finalize_warp<D, GC, MQ>(p, sg, st, in, bad, lane);
             continue;
         }
         const int wslot = slot_of(kf, k - kf);
@@ -1062,31 +1284,31 @@ __device__ void epilogue(const KParams &p, Smem<D, GC> &sm, int ew)
         if (last) {
             __threadfence();
             bad = combine_warp<D, GC>(p, st, kf, n, lane);
-            finalize_warp<D, GC>(p, sg, st, in, bad, lane);
+            finalize_warp<D, GC, MQ>(p, sg, st, in, bad, lane);
             if (lane == 0)
                 p.tickets[sg.unit] = 0; // ready for the next call
         }
     }
-    // Units with no cached token (inactive, overflowing or empty rows) get
-    // their output (zeros, or the new token alone) here: empty unit e goes to
-    // CTA e % gridDim.x, epilogue warp (e / gridDim.x) % 2.
+    // Units with no cached token (inactive, overflowing or empty rows, and
+    // malformed multi-query rows) get their output (zeros, or the new token
+    // alone) here: empty unit e goes to CTA e % gridDim.x, epilogue warp
+    // (e / gridDim.x) % 2.
     if (!stopped && !*abort && sm.n_empty > 0) {
         const int G = (int)gridDim.x;
-        int e0 = 0; // empty units before row b
+        long long e0 = 0; // empty units before row b
         for (int b = 0; b < p.batch; ++b) {
             if (sm.rowtok[b + 1] != sm.rowtok[b])
                 continue;
-            for (int r = (int)(((long long)k - e0 % G + G) % G); r < p.units; r += G) {
-                if ((((long long)e0 + r) / G & 1) != ew)
+            int units = p.units;
+            if constexpr (MQ) {
+                int kv;
+                units = mq_units<GC>(p, mq_row_status(p, sm.len[b], sm.qlen[b], &kv), sm.qlen[b]);
+            }
+            for (int r = (int)(((long long)k - e0 % G + G) % G); r < units; r += G) {
+                if (((e0 + r) / G & 1) != ew)
                     continue;
                 Seg es;
-                es.b = b;
-                es.r = r;
-                es.kvh = r / p.n_sub;
-                es.sub = r - es.kvh * p.n_sub;
-                es.unit = b * p.units + r;
-                es.L = sm.len[b];
-                es.status = row_status(p, es.L);
+                seg_unit(p, sm, es, b, r);
                 es.tok0 = es.tok1 = 0;
                 es.u0 = 0;
                 es.n = 0;
@@ -1101,23 +1323,30 @@ __device__ void epilogue(const KParams &p, Smem<D, GC> &sm, int ew)
 #pragma unroll
                 for (int i = 0; i < EPT2; ++i)
                     st.o[i] = make_float2(0.f, 0.f);
-                finalize_warp<D, GC>(p, es, st, in, 0, lane);
+                finalize_warp<D, GC, MQ>(p, es, st, in, 0, lane);
             }
-            e0 += p.units;
+            e0 += units;
         }
     }
+    // multi-query rows whose query range lies outside [0, total_q): no output, one error bit
+    if (MQ && k == 0 && ew == 0 && lane == 0)
+        for (int b = 0; b < p.batch; ++b)
+            if (sm.qlen[b] < 0) {
+                set_error(p.err_flag, PKV_ERR_QLEN);
+                break;
+            }
     if (*abort && lane == 0)
         set_error(p.err_flag, PKV_ERR_TIMEOUT);
 }
 
-template <int D, int GC>
+template <int D, int GC, bool MQ>
 __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant__ KParams p,
                                                           const __grid_constant__ DecodeMaps maps)
 {
     extern __shared__ unsigned char smem_raw[];
-    Smem<D, GC> &sm = *reinterpret_cast<Smem<D, GC> *>(
+    Smem<D, GC, MQ> &sm = *reinterpret_cast<Smem<D, GC, MQ> *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    constexpr int S = Smem<D, GC>::kStages;
+    constexpr int S = Smem<D, GC, MQ>::kStages;
     const int warp = threadIdx.x >> 5;
     if (p.pdl && threadIdx.x == 0) // the next grid may start filling SMs this one frees
         asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -1148,37 +1377,42 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
         epilogue(p, sm, warp - kEpilogueWarp);
 }
 
-template <int D, int GC>
+template <int D, int GC, bool MQ>
 size_t smem_bytes()
 {
-    return sizeof(Smem<D, GC>) + 1024;
+    return sizeof(Smem<D, GC, MQ>) + 1024;
 }
 
 // Two CTAs per SM: 228 KB of shared memory per SM, 1 KB of it reserved per CTA.
-static_assert(sizeof(Smem<128, 4>) + 1024 + 1024 <= 228 * 1024 / 2, "decode<128,4> must fit twice on an SM");
-static_assert(sizeof(Smem<128, 8>) + 1024 + 1024 <= 228 * 1024 / 2, "decode<128,8> must fit twice on an SM");
+static_assert(sizeof(Smem<128, 4, true>) + 1024 + 1024 <= 228 * 1024 / 2, "decode<128,4> must fit twice on an SM");
+static_assert(sizeof(Smem<128, 8, true>) + 1024 + 1024 <= 228 * 1024 / 2, "decode<128,8> must fit twice on an SM");
 
 struct KernelEntry {
     int D, GC;
+    bool mq; // multi-query rows
     const void *fn;
     size_t smem;
 };
 
-template <int D, int GC>
+template <int D, int GC, bool MQ>
 KernelEntry entry()
 {
-    return KernelEntry{D, GC, reinterpret_cast<const void *>(&decode_kernel<D, GC>), smem_bytes<D, GC>()};
+    return KernelEntry{D, GC, MQ, reinterpret_cast<const void *>(&decode_kernel<D, GC, MQ>), smem_bytes<D, GC, MQ>()};
 }
 
 const KernelEntry kTable[] = {
-    entry<64, 1>(),  entry<64, 2>(),  entry<64, 4>(),  entry<64, 8>(),  entry<128, 1>(),  entry<128, 2>(),
-    entry<128, 4>(), entry<128, 8>(), entry<256, 1>(), entry<256, 2>(), entry<256, 4>(), entry<256, 8>(),
+    entry<64, 1, false>(),  entry<64, 2, false>(),  entry<64, 4, false>(),  entry<64, 8, false>(),
+    entry<128, 1, false>(), entry<128, 2, false>(), entry<128, 4, false>(), entry<128, 8, false>(),
+    entry<256, 1, false>(), entry<256, 2, false>(), entry<256, 4, false>(), entry<256, 8, false>(),
+    entry<64, 1, true>(),   entry<64, 2, true>(),   entry<64, 4, true>(),   entry<64, 8, true>(),
+    entry<128, 1, true>(),  entry<128, 2, true>(),  entry<128, 4, true>(),  entry<128, 8, true>(),
+    entry<256, 1, true>(),  entry<256, 2, true>(),  entry<256, 4, true>(),  entry<256, 8, true>(),
 };
 
-const KernelEntry *find_kernel(int D, int GC)
+const KernelEntry *find_kernel(int D, int GC, bool mq = false)
 {
     for (const KernelEntry &e : kTable)
-        if (e.D == D && e.GC == GC)
+        if (e.D == D && e.GC == GC && e.mq == mq)
             return &e;
     return nullptr;
 }
@@ -1207,18 +1441,14 @@ int decode_swizzle(int page_size)
     return page_size >= 8 ? 1 : 0;
 }
 
-bool decode_shape(int batch, int max_blocks, int num_q_heads, const pkv_cache_desc &d, DecodeShape *s)
+namespace {
+
+// Shared tail of decode_shape / decode_mq_shape once the columns per unit
+// (heads_per_cta) and units per row are set.
+bool finish_shape(int batch, int max_blocks, const pkv_cache_desc &d, DecodeShape *s)
 {
-    if (d.num_kv_heads <= 0 || num_q_heads % d.num_kv_heads != 0)
-        return false;
-    s->group = num_q_heads / d.num_kv_heads;
-    if (s->group & (s->group - 1))
-        return false; // power-of-two groups only
-    s->heads_per_cta = heads_per_cta(s->group);
     if (find_kernel(d.head_dim, s->heads_per_cta) == nullptr)
         return false;
-    s->n_sub = s->group / s->heads_per_cta;
-    s->units_per_row = d.num_kv_heads * s->n_sub;
     // the plan counts tokens of all rows, and work positions inside a row, in int32
     const int64_t row_tokens = (int64_t)max_blocks * d.page_size;
     if ((int64_t)batch * row_tokens >= ((int64_t)1 << 31) ||
@@ -1235,13 +1465,51 @@ bool decode_shape(int batch, int max_blocks, int num_q_heads, const pkv_cache_de
     return true;
 }
 
-int decode_target_items(int device, int head_dim, int heads_per_cta)
+} // namespace
+
+bool decode_shape(int batch, int max_blocks, int num_q_heads, const pkv_cache_desc &d, DecodeShape *s)
+{
+    if (d.num_kv_heads <= 0 || num_q_heads % d.num_kv_heads != 0)
+        return false;
+    s->group = num_q_heads / d.num_kv_heads;
+    if (s->group & (s->group - 1))
+        return false; // power-of-two groups only
+    s->heads_per_cta = heads_per_cta(s->group);
+    s->n_sub = s->group / s->heads_per_cta;
+    s->units_per_row = d.num_kv_heads * s->n_sub;
+    return finish_shape(batch, max_blocks, d, s);
+}
+
+bool decode_mq_shape(int batch, int max_blocks, int num_q_heads, int max_qlen, const pkv_cache_desc &d,
+                     DecodeShape *s)
+{
+    if (d.num_kv_heads <= 0 || num_q_heads % d.num_kv_heads != 0 || max_qlen < 1)
+        return false;
+    s->group = num_q_heads / d.num_kv_heads;
+    if (s->group & (s->group - 1))
+        return false;
+    // (query, head) columns of one kv head; a unit takes up to 8 (the MMA's N side)
+    const int64_t cols = (int64_t)s->group * max_qlen;
+    int gc = 1;
+    while (gc < cols && gc < 8)
+        gc <<= 1;
+    s->heads_per_cta = gc;
+    const int64_t n_sub = (cols + gc - 1) / gc;
+    if (n_sub * d.num_kv_heads >= ((int64_t)1 << 24))
+        return false;
+    s->n_sub = (int)n_sub;
+    s->units_per_row = d.num_kv_heads * s->n_sub;
+    return finish_shape(batch, max_blocks, d, s);
+}
+
+int decode_target_items(int device, int head_dim, int heads_per_cta, bool multi_query)
 {
     // Per device and kernel: opt in to the kernel's shared memory once and
     // size the persistent grid to the CTAs that fit on all SMs.
-    constexpr int kDevices = 64, kKernels = 16;
+    constexpr int kDevices = 64, kKernels = 32;
+    static_assert(sizeof(kTable) / sizeof(kTable[0]) <= kKernels, "grid cache too small");
     static int cache[kDevices][kKernels] = {};
-    const KernelEntry *e = find_kernel(head_dim, heads_per_cta);
+    const KernelEntry *e = find_kernel(head_dim, heads_per_cta, multi_query);
     if (e == nullptr || device < 0 || device >= kDevices)
         return 1;
     int &slot = cache[device][kernel_index(e)];
@@ -1260,7 +1528,7 @@ int decode_target_items(int device, int head_dim, int heads_per_cta)
 
 cudaError_t launch_decode(const DecodeArgs &a, const DecodeMaps &maps, cudaStream_t stream)
 {
-    const KernelEntry *e = find_kernel(a.desc.head_dim, a.shape.heads_per_cta);
+    const KernelEntry *e = find_kernel(a.desc.head_dim, a.shape.heads_per_cta, a.qo_indptr != nullptr);
     if (e == nullptr)
         return cudaErrorInvalidValue;
     KParams p;
@@ -1295,6 +1563,15 @@ cudaError_t launch_decode(const DecodeArgs &a, const DecodeMaps &maps, cudaStrea
     p.pdl = (a.flags & PKV_DECODE_OVERLAP_PROLOGUE) ? 1 : 0;
     p.early_kv = (a.flags & PKV_DECODE_EARLY_KV) ? 1 : 0;
     p.q_scale = a.q_scale;
+    p.qo_indptr = a.qo_indptr;
+    p.total_q = a.total_q;
+    p.group_shift = 0;
+    while ((1 << p.group_shift) < a.shape.group)
+        ++p.group_shift;
+    p.mq_hi = a.mq_hi;
+    p.mq_max = a.mq_max;
+    p.mq_own_long = a.mq_own_long;
+    p.mq_kv_add = a.mq_kv_add;
     void *args[] = {&p, const_cast<DecodeMaps *>(&maps)};
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(a.grid);

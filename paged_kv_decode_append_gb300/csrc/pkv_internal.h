@@ -38,9 +38,14 @@ struct DecodeShape {
 // Fills `s`; returns false for unsupported combinations.
 bool decode_shape(int batch, int max_blocks, int num_q_heads, const pkv_cache_desc &d, DecodeShape *s);
 
+// The same for multi-query rows of up to max_qlen queries each: a unit holds
+// up to 8 (query, head) columns of one kv head.
+bool decode_mq_shape(int batch, int max_blocks, int num_q_heads, int max_qlen, const pkv_cache_desc &d,
+                     DecodeShape *s);
+
 // Number of split-KV work items a call aims for on this device (a few per
 // resident CTA slot).
-int decode_target_items(int device, int head_dim, int heads_per_cta);
+int decode_target_items(int device, int head_dim, int heads_per_cta, bool multi_query = false);
 
 struct DecodeArgs {
     pkv_cache_desc desc;
@@ -62,6 +67,14 @@ struct DecodeArgs {
     int target_items;
     int grid;
     uint32_t flags; // PKV_DECODE_*
+    // Multi-query rows (shape from decode_mq_shape; q / out / lse are
+    // [total_q, Hq, ...]); qo_indptr nullptr: one query per row.
+    const int32_t *qo_indptr = nullptr;
+    int total_q = 0;
+    int mq_hi = 0;       // rows with 1 <= q_len <= mq_hi are served
+    int mq_max = 0;      // q_len > mq_max: PKV_ERR_QLEN ...
+    int mq_own_long = 0; // ... and zeroed by this kernel
+    int mq_kv_add = 0;   // 1: kv = L + q_len (new tokens cached); 0: kv = L
 };
 
 // TMA descriptors of one decode call: K and V pools with full boxes
@@ -75,6 +88,9 @@ struct DecodeMaps {
 constexpr int kDecodeSmallBox = 8;
 
 cudaError_t launch_decode(const DecodeArgs &a, const DecodeMaps &maps, cudaStream_t stream);
+
+// K / V tensor maps of one decode call over these pools (false if encoding failed).
+bool encode_decode_maps(const pkv_cache_desc &desc, void *k_cache, void *v_cache, DecodeMaps *maps);
 
 // Every argument check of pkv_decode_attn_ex (no device access, no launch);
 // fills `shape` when the sizes are supported.
@@ -98,6 +114,7 @@ struct AppendArgs {
     const int32_t *cache_seqlens;
     int batch;
     int32_t *err_flag;
+    int max_count = 0x7fffffff; // rows appending more tokens than this append nothing
 };
 
 cudaError_t launch_append(const AppendArgs &a, cudaStream_t stream);
@@ -154,6 +171,13 @@ struct PrefillArgs {
     void *workspace;
     int32_t *err_flag;
     PrefillShape shape;
+    // Mixed step: kv_lens unused; request b holds cache_seqlens[b] cached
+    // tokens and cache_seqlens[b] + kv_add * q keys; only requests with more
+    // than q_lo queries are served, more than q_max is malformed.
+    const int32_t *cache_seqlens = nullptr;
+    int q_lo = 0;
+    int q_max = 0x7fffffff;
+    int kv_add = 0;
 };
 
 // TMA descriptors of one prefill call: token-group boxes (encode_group_map)

@@ -58,6 +58,7 @@ constexpr int kPfRows = 128;    // M of every MMA
 constexpr int kPfTile = 64;     // kv tokens per tile
 constexpr int kPfBuckets = 4096; // plan: units are ordered by min(kv tiles, 4095)
 constexpr int kPlanThreads = 1024;
+constexpr int kPfZeroOnly = 0x100; // plan: a request whose output is zeroed without an error bit
 constexpr float kRescaleLog2 = 8.0f;
 constexpr float kLn2 = 0.693147180559945309f;
 
@@ -126,6 +127,11 @@ struct PfMapsDev {
 struct PfPlanParams {
     const int32_t *qo_indptr;
     const int32_t *kv_lens;
+    // Mixed step (kv_lens unused): request b holds cache_seqlens[b] cached
+    // tokens (< 0: inactive), kv = cache_seqlens[b] + kv_add * q keys; only
+    // requests with q_lo < q are this kernel's, q > q_max is malformed.
+    const int32_t *cache_seqlens;
+    int q_lo, q_max, kv_add;
     const int32_t *block_table;
     PfUnit *units;
     int32_t *n_pairs;
@@ -746,11 +752,34 @@ __global__ void __launch_bounds__(kPlanThreads) prefill_plan_kernel(const PfPlan
     __syncthreads();
 
     // 1. Validate every request (one warp per request).
+    const bool mixed = pp.cache_seqlens != nullptr;
     for (int b = warp; b < pp.batch; b += kPlanThreads / 32) {
-        const int s = pp.qo_indptr[b], e = pp.qo_indptr[b + 1], kv = pp.kv_lens[b];
-        const int64_t q = (int64_t)e - s;
+        int s = pp.qo_indptr[b], e = pp.qo_indptr[b + 1], kv = 0;
+        int64_t q = (int64_t)e - s;
         int bad = 0;
-        if (q != 0) {
+        if (mixed) {
+            // rows of the decode kernel, or with a range it reports, are not ours
+            if (s < 0 || e > pp.total_q || q <= pp.q_lo) {
+                s = e = 0;
+                q = 0;
+            } else if (q > pp.q_max) {
+                bad = PKV_ERR_QLEN;
+            } else {
+                const int L = pp.cache_seqlens[b];
+                const int64_t keys = (int64_t)L + (pp.kv_add ? q : 0);
+                if (L < 0)
+                    bad = kPfZeroOnly; // inactive: zero output, no error
+                else if (keys < q)
+                    bad = PKV_ERR_QLEN;
+                else if (keys > ((int64_t)pp.max_blocks << pp.page_shift))
+                    bad = PKV_ERR_OVERFLOW;
+                else
+                    kv = (int)keys;
+            }
+        } else {
+            kv = pp.kv_lens[b];
+        }
+        if (q != 0 && bad == 0) {
             if (s < 0 || e > pp.total_q || q < 0 || kv < q)
                 bad = PKV_ERR_QLEN;
             else if ((int64_t)kv > ((int64_t)pp.max_blocks << pp.page_shift))
@@ -772,7 +801,7 @@ __global__ void __launch_bounds__(kPlanThreads) prefill_plan_kernel(const PfPlan
             s_end[b] = e;
             s_kv[b] = kv;
             s_bad[b] = bad;
-            if (q < 0)
+            if (q < 0 && !mixed)
                 s_decreasing = 1;
         }
     }
@@ -870,7 +899,7 @@ __global__ void __launch_bounds__(kPlanThreads) prefill_plan_kernel(const PfPlan
         if (s_bad[b] == 0)
             continue;
         if (tid == 0)
-            set_error(pp.err_flag, s_bad[b]);
+            set_error(pp.err_flag, s_bad[b] & ~kPfZeroOnly);
         const int64_t lo = s_start[b] > 0 ? s_start[b] : 0;
         const int64_t hi = s_end[b] < pp.total_q ? s_end[b] : pp.total_q;
         if (hi <= lo)
@@ -981,6 +1010,10 @@ cudaError_t launch_prefill(const PrefillArgs &a, const PrefillMaps &maps, cudaSt
     PfPlanParams pp;
     pp.qo_indptr = a.qo_indptr;
     pp.kv_lens = a.kv_lens;
+    pp.cache_seqlens = a.cache_seqlens;
+    pp.q_lo = a.q_lo;
+    pp.q_max = a.q_max;
+    pp.kv_add = a.kv_add;
     pp.block_table = a.block_table;
     pp.units = units;
     pp.n_pairs = n_pairs;

@@ -258,3 +258,53 @@ def test_decode_step_argument_errors_before_any_cuda_call():
     assert create(flags=pkv.api.DECODE_EARLY_KV) == pkv.api.EINVAL
     assert out.value is None
     lib.pkv_decode_step_destroy(None)
+
+
+def _mixed(lib, desc, batch=2, hq=8, total_q=40, max_qlen=32, dq=4, ws=FAKE, ws_bytes=1 << 30, q=FAKE,
+           k_new=FAKE, v_new=FAKE, scale=0.1, max_blocks=4, qo=FAKE):
+    return lib.pkv_mixed_attn(ctypes.byref(desc), FAKE, FAKE, q, k_new, v_new, qo, FAKE, max_blocks, FAKE, batch, hq,
+                              total_q, max_qlen, dq, scale, FAKE, None, ws, ws_bytes, None, None)
+
+
+def test_mixed_workspace_size():
+    d = CacheDesc(65536, 16, 8, 128, 0)
+    decode_only = pkv.pkv_mixed_workspace_size(64, 256, 65, 32, 4, 4, d)
+    with_prefill = pkv.pkv_mixed_workspace_size(64, 256, 65, 32, 512, 4, d)
+    assert 0 < decode_only < with_prefill
+    # the decode part holds 8 (query, head) columns per unit once G * q > 4
+    assert decode_only >= pkv.pkv_decode_workspace_size(64, 65, 32, d)
+    assert pkv.pkv_mixed_workspace_size(64, 256, 65, 32, 0, 4, d) == 0        # max_qlen < 1
+    assert pkv.pkv_mixed_workspace_size(64, 256, 65, 32, 4, 0, d) == 0        # decode_max_qlen < 1
+    assert pkv.pkv_mixed_workspace_size(1025, 256, 65, 32, 4, 4, d) == 0
+    assert pkv.pkv_mixed_workspace_size(64, 1 << 26, 65, 32, 4, 4, d) == 0    # total_q * Hq >= 2^31
+    d4 = CacheDesc(65536, 4, 8, 128, 0)
+    assert pkv.pkv_mixed_workspace_size(64, 256, 65, 32, 4, 4, d4) > 0        # decode only: any page size
+    assert pkv.pkv_mixed_workspace_size(64, 256, 65, 32, 8, 4, d4) == 0       # prefill needs page >= 8
+
+
+def test_mixed_argument_errors_return_before_any_launch():
+    lib = _lib.load()
+    d = CacheDesc(64, 16, 2, 128, 1)
+    assert _mixed(lib, CacheDesc(64, 16, 2, 96, 1)) == pkv.api.EUNSUPPORTED   # head dim
+    assert _mixed(lib, CacheDesc(64, 4, 2, 128, 1)) == pkv.api.EUNSUPPORTED   # prefill rows, page 4
+    assert _mixed(lib, d, hq=7) == pkv.api.EINVAL                             # Hq % Hkv
+    assert _mixed(lib, d, hq=6) == pkv.api.EUNSUPPORTED                       # group 3
+    assert _mixed(lib, d, max_qlen=0) == pkv.api.EINVAL
+    assert _mixed(lib, d, dq=0) == pkv.api.EINVAL
+    assert _mixed(lib, d, q=None) == pkv.api.EINVAL
+    assert _mixed(lib, d, qo=None) == pkv.api.EINVAL
+    assert _mixed(lib, d, k_new=None) == pkv.api.EINVAL                       # one of the pair
+    assert _mixed(lib, d, q=ctypes.c_void_p(0x10008)) == pkv.api.EINVAL        # misaligned
+    assert _mixed(lib, d, scale=float("nan")) == pkv.api.EINVAL
+    assert _mixed(lib, d, ws=None) == pkv.api.EWORKSPACE
+    assert _mixed(lib, d, ws_bytes=16) == pkv.api.EWORKSPACE
+    assert _mixed(lib, d, batch=0) == pkv.api.OK
+    assert _mixed(lib, d, batch=1025) == pkv.api.EUNSUPPORTED
+    assert _mixed(lib, d, total_q=-1) == pkv.api.EINVAL
+
+
+def test_default_decode_max_qlen():
+    assert pkv.default_decode_max_qlen(32, 8) == 4   # Qwen3: 4 queries x 4 heads = 16 columns
+    assert pkv.default_decode_max_qlen(48, 6) == 2
+    assert pkv.default_decode_max_qlen(8, 8) == 16
+    assert pkv.default_decode_max_qlen(128, 1) == 1
