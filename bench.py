@@ -110,6 +110,91 @@ def recorded_prefill_profile():
         return None
 
 
+def mixed_bench(kind: str, reps: int, warmup: int, decode_max_qlen, dev=None) -> dict:
+    """One mixed step (pkv_mixed_attn: append + decode kernel + prefill
+    kernel) per timed iteration on the Qwen3-4B-shaped layer: speculative
+    decode (B=32 rows of 4 tokens on U[512,1024]) or a chunked-prefill step
+    (4 chunks of 496 tokens on prefixes U[0,2048] + 60 decode rows on
+    U[512,1024]).  CUDA events around each call, L2 flushed by a 512 MiB write
+    before it.  Prints one JSON line: GB/s of the step's algorithmic bytes and
+    TFLOP/s of its causal pairs, against the measured peaks.  Returns the
+    line as a dict."""
+    import paged_kv_decode_append_gb300 as pkv
+    from paged_kv_decode_append_gb300 import workloads as wl
+
+    if dev is None:
+        dev = torch.device("cuda:0")
+        torch.cuda.set_device(dev)
+    case = (wl.spec_decode if kind == "spec" else wl.chunked_mix)(device=dev)
+    q, kn, vn = case.q, case.k_new.to(dev), case.v_new.to(dev)
+    T, Hq, Dh = q.shape
+    B = case.batch
+    ql = np.diff(case.qo_indptr).astype(np.int64)
+    L = case.cache_seqlens.astype(np.int64)
+    max_qlen = int(ql.max())
+    dq = pkv.default_decode_max_qlen(Hq, case.num_kv_heads) if decode_max_qlen is None else int(decode_max_qlen)
+    qo = torch.as_tensor(case.qo_indptr, device=dev)
+    bt = torch.as_tensor(case.block_table, device=dev)
+    sl = torch.as_tensor(case.cache_seqlens, device=dev)
+    out = torch.empty_like(q)
+    lse = torch.empty((T, Hq), dtype=torch.float32, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    ws = pkv.mixed_workspace(B, T, case.max_blocks, Hq, max_qlen, dq, pkv.cache_desc(case.k_cache, case.layout),
+                             dev)
+    # algorithmic bytes: cached K/V read, new K/V read and appended, q read,
+    # out write, block-table entries and the two int32 row arrays
+    Hkv = case.num_kv_heads
+    nbytes = (int(L.sum()) * 2 * Hkv * Dh * 2 + 2 * T * 2 * Hkv * Dh * 2 + 2 * T * Hq * Dh * 2 +
+              4 * int(((L + ql + case.page_size - 1) // case.page_size).sum()) + 4 * (2 * B + 1))
+    pairs = Hq * int((ql * L + ql * (ql + 1) // 2).sum())  # query i of a row sees L + i + 1 keys
+    flops = 4 * Dh * pairs
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def call():
+        # the same slots are appended to every time (cache_seqlens is not advanced)
+        pkv.pkv_mixed_attn(case.k_cache, case.v_cache, q, kn, vn, qo, bt, sl, case.softmax_scale, max_qlen, dq,
+                           out=out, lse=lse, workspace=ws, err_flag=err, layout=case.layout)
+
+    for _ in range(warmup):
+        call()
+    torch.cuda.synchronize(dev)
+    times = []
+    with ClockSampler(0) as clocks:
+        for _ in range(reps):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            call()
+            b.record(stream)
+            b.synchronize()
+            times.append(a.elapsed_time(b))
+    if int(err.item()) != 0:
+        raise RuntimeError(f"mixed step reported error bits {int(err.item())}")
+    times = np.array(times)
+    ms = float(np.median(times))
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    tflops = flops / (ms * 1e-3) / 1e12
+    hbm, hbm_kind = peaks()
+    tpk, tpk_kind = tensor_peak()
+    n_prefill = int((ql > dq).sum())
+    launches = 1 + 1 + (2 if max_qlen > dq else 0)
+    name = ("speculative decode, Qwen3-4B-shaped layer: B=32 rows of 4 new tokens, Hq=32, Hkv=8, D=128, page 16, "
+            "cached lengths U[512,1024], 65,536-page shuffled pool" if kind == "spec" else
+            "chunked-prefill step, Qwen3-4B-shaped layer: 4 chunks of 496 tokens on prefixes U[0,2048] + 60 decode "
+            "rows on U[512,1024] (2,044 new tokens), Hq=32, Hkv=8, D=128, page 16, 65,536-page shuffled pool")
+    return {
+        "metric": "mixed-step GB/s (% of HBM peak) and TFLOP/s (% of bf16 peak)", "value": gbs, "unit": "GB/s",
+        "n_gpus": 1, "steps": reps, "warmup": warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": name, "batch": B, "total_q": T, "decode_max_qlen": dq,
+                   "rows_on_prefill_kernel": n_prefill, "l2": "flushed between calls (512 MiB write)"},
+        "pct_of_hbm_peak": 100.0 * gbs / hbm, "tflops": tflops, "pct_of_tensor_peak": 100.0 * tflops / tpk,
+        "algorithmic_bytes_per_call": nbytes, "flops_per_call": flops, "flops_formula": "4 * head_dim * causal pairs",
+        "ms_best": float(times.min()), "hbm_peak": hbm, "hbm_peak_kind": hbm_kind, "tensor_peak": tpk,
+        "tensor_peak_kind": tpk_kind, "clocks": clocks.summary(), "gpu_launches": reps * launches}
+
+
 def prefill_bench(dev, reps: int):
     """The ragged causal prefill workload (B=8, Hq=48, Hkv=6, D=256, page 16
     HND): one pkv_prefill_attn call per timed iteration (plan + kernel), CUDA
@@ -455,10 +540,15 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=100)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--prefill-reps", type=int, default=20, help="timed prefill calls (0 = skip)")
+    ap.add_argument("--mixed-reps", type=int, default=20,
+                    help="timed mixed-step calls per mixed workload in the default line (0 = skip)")
     ap.add_argument("--prefill-only", action="store_true",
                     help="run only the prefill measurement on cuda:0 and print its JSON object")
-    ap.add_argument("--workload", default="sweep", choices=["sweep", "qwen3", "skewed"],
-                    help="sweep: the 36-layer batch sweep (default); qwen3 / skewed: one layer, timed per call")
+    ap.add_argument("--workload", default="sweep", choices=["sweep", "qwen3", "skewed", "spec", "chunked"],
+                    help="sweep: the 36-layer batch sweep (default); qwen3 / skewed: one decode layer, timed per "
+                         "call; spec / chunked: one mixed step (pkv_mixed_attn), timed per call")
+    ap.add_argument("--decode-max-qlen", type=int, default=None,
+                    help="spec / chunked: longest row on the decode kernel (default: the library's)")
     ap.add_argument("--no-overlap", action="store_true",
                     help="plain launches instead of programmatic dependent launch between layers")
     args = ap.parse_args()
@@ -466,6 +556,10 @@ def main():
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
         run_reference(args)
+        return
+    if args.workload in ("spec", "chunked"):
+        reps = 50 if args.steps == ap.get_default("steps") else args.steps
+        print(json.dumps(mixed_bench(args.workload, reps, args.warmup, args.decode_max_qlen)))
         return
     if args.workload != "sweep":
         reps = 50 if args.steps == ap.get_default("steps") else args.steps
@@ -638,6 +732,14 @@ def main():
 
     if rank != 0:
         return
+    mixed = None
+    if args.mixed_reps > 0:  # one mixed step per call: speculative decode and a chunked-prefill step
+        keep = ("value", "unit", "pct_of_hbm_peak", "tflops", "pct_of_tensor_peak", "ms_per_step", "ms_best",
+                "steps", "config", "algorithmic_bytes_per_call", "flops_per_call", "clocks", "gpu_launches")
+        mixed = {}
+        for kind in ("spec", "chunked"):
+            line = mixed_bench(kind, args.mixed_reps, 3, None, dev)
+            mixed[kind] = {k: line[k] for k in keep}
     cpu = None
     if not args.no_cpu_baseline and world == 1:
         cpu = cpu_baseline(sw, sw.prompt_lens)
@@ -667,6 +769,7 @@ def main():
             ")" if args.no_overlap else ", programmatic dependent launch between them, K/V streamed early)"),
         "cpu_baseline": cpu,
         "prefill": prefill,
+        "mixed": mixed,
     }
     print(json.dumps(out))
 

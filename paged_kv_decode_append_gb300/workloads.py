@@ -23,6 +23,13 @@ Workload shapes follow the pages' workloads:
                   q uniform in [65, 1023], kv = q + uniform [0, 2048]
                   ("[flashinfer] H100 D256 paged attention cuDNN
                   auto-dispatch": HND, page 16, D=256, Hq up to 48).
+* ``spec``     -- speculative decode on the Qwen3-shaped layer: B=32 rows of
+                  4 new tokens on cached lengths U[512, 1024].
+* ``chunked``  -- a chunked-prefill serving step on the same layer: 4 chunks
+                  of 496 tokens on prefixes U[0, 2048] plus 60 decode rows on
+                  U[512, 1024] ("flex_attention + paged KV + CUDA graphs vs
+                  vLLM", "What's left on the table": prefill chunks and decode
+                  tokens interleaved in one step).
 
 Values are float32 N(0, 1) draws rounded to bf16 (round to nearest even).
 Every cache slot that holds no token yet -- page 0, unused pages, and the
@@ -205,6 +212,52 @@ def skewed_decode(device="cpu", seed: int = 3, batch: int = 64, long_len: int = 
     case.v_new = _randn_bf16((batch, Hkv, D), g, "cpu").to(device)
     _fill_cache(case, g, device, "cpu")
     return case
+
+
+def _serving_case(name: str, g: torch.Generator, q_lens: np.ndarray, L: np.ndarray, num_pages: int,
+                  device) -> PagedCase:
+    """A Qwen3-4B-shaped mixed step (Hq=32, Hkv=8, D=128, page 16, NHD): row b
+    holds L[b] cached tokens and brings q_lens[b] new ones; pages for all of
+    them from a seeded permutation of the num_pages pool."""
+    Hq, Hkv, D, P = 32, 8, 128, 16
+    B = len(q_lens)
+    indptr = np.concatenate([[0], np.cumsum(q_lens)]).astype(np.int32)
+    T = int(indptr[-1])
+    needed = (L + q_lens + P - 1) // P
+    max_blocks = int(needed.max())
+    order = (torch.randperm(num_pages - 1, generator=g).numpy() + 1).astype(np.int32)
+    bt = assign_pages(needed, num_pages, max_blocks, order)
+    case = PagedCase(name, B, Hq, Hkv, D, P, num_pages, NHD, max_blocks, bt, L.astype(np.int32),
+                     1.0 / math.sqrt(D), q=_randn_bf16((T, Hq, D), g, "cpu").to(device), qo_indptr=indptr)
+    case.k_new = _randn_bf16((T, Hkv, D), g, "cpu").to(device)
+    case.v_new = _randn_bf16((T, Hkv, D), g, "cpu").to(device)
+    _fill_cache(case, g, device, "cpu")
+    return case
+
+
+def spec_decode(device="cpu", seed: int = 6, batch: int = 32, q_len: int = 4, min_len: int = 512,
+                max_len: int = 1024, num_pages: int = 65536) -> PagedCase:
+    """Speculative decode on the Qwen3-4B-shaped layer: B=32 rows of q_len=4
+    new tokens each on cached lengths uniform in [512, 1024], 65,536-page
+    shuffled pool."""
+    g = _gen(seed)
+    L = torch.randint(min_len, max_len + 1, (batch,), generator=g).numpy().astype(np.int32)
+    return _serving_case("spec", g, np.full(batch, q_len, np.int32), L, num_pages, device)
+
+
+def chunked_mix(device="cpu", seed: int = 7, decode_rows: int = 60, chunks: int = 4, chunk_len: int = 496,
+                num_pages: int = 65536) -> PagedCase:
+    """A chunked-prefill serving step on the Qwen3-4B-shaped layer: `chunks`
+    prefill chunks of chunk_len tokens on cached prefixes uniform in
+    [0, 2048] (rows 0..chunks-1), then decode_rows single-token rows on
+    lengths uniform in [512, 1024] -- 2,044 new tokens in all, 65,536-page
+    shuffled pool."""
+    g = _gen(seed)
+    L_chunk = torch.randint(0, 2048 + 1, (chunks,), generator=g).numpy()
+    L_dec = torch.randint(512, 1024 + 1, (decode_rows,), generator=g).numpy()
+    q = np.concatenate([np.full(chunks, chunk_len), np.ones(decode_rows)]).astype(np.int32)
+    L = np.concatenate([L_chunk, L_dec]).astype(np.int32)
+    return _serving_case("chunked", g, q, L, num_pages, device)
 
 
 def ragged_prefill(device="cpu", seed: int = 4, batch: int = 8, num_pages: int = 4096,
