@@ -537,7 +537,7 @@ def main():
     ap.add_argument("--batch", type=int, default=64)
     ap.add_argument("--layers", type=int, default=36)
     ap.add_argument("--layout", default="shuffled", choices=["shuffled", "contiguous"])
-    ap.add_argument("--e2e-steps", type=int, default=100)
+    ap.add_argument("--e2e-steps", type=int, default=600)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--prefill-reps", type=int, default=20, help="timed prefill calls (0 = skip)")
     ap.add_argument("--mixed-reps", type=int, default=20,
@@ -679,24 +679,34 @@ def main():
     torch.cuda.synchronize(dev)
     eager_gbs = eager_bytes / (ea.elapsed_time(eb) * 1e-3) / 1e9
 
-    # End to end through the public API: one pkv_decode_step graph (all 36
-    # layers) captured once over device input / output buffers; every step
-    # copies that step's q / k_new / v_new of all layers and its cache_seqlens
-    # from pinned host memory into them, launches the step and copies all
-    # outputs back -- one H2D copy, one seqlens copy, one launch, one D2H copy.
+    # End to end through the public API: pkv_decode_step graphs (all 36 layers
+    # each) captured once over two sets of device input / output buffers.
+    # Every step copies that step's q / k_new / v_new of all layers and its
+    # cache_seqlens from pinned host memory into one set, launches the graph
+    # of that set and copies all its outputs back.  The copies run on their
+    # own streams, double-buffered: step s+1's inputs go up while step s
+    # computes, step s's outputs come down while step s+1 computes.  The timed
+    # region spans the first input copy to the last output copy; the steps are
+    # those the device-timed value covers (the first e2e_steps of them).
     e2e_steps = min(args.e2e_steps, args.steps)
+    s0 = args.warmup
     per_layer = [B * HQ * D, B * HKV * D, B * HKV * D]
     layer_elems = sum(per_layer)
-    d_in_all = torch.empty(L * layer_elems, dtype=torch.bfloat16, device=dev)
-    d_out_all = torch.empty(L * B * HQ * D, dtype=torch.bfloat16, device=dev)
-    d_seq = torch.empty(B, dtype=torch.int32, device=dev)
 
     def split(buf, base):
         q_, k_, v_ = torch.split(buf[base:base + layer_elems], per_layer)
         return q_.view(B, HQ, D), k_.view(B, HKV, D), v_.view(B, HKV, D)
 
-    d_in = [split(d_in_all, layer * layer_elems) for layer in range(L)]
-    d_out = [d_out_all[layer * B * HQ * D:(layer + 1) * B * HQ * D].view(B, HQ, D) for layer in range(L)]
+    sets = []
+    for _ in range(2):
+        d_in_all = torch.empty(L * layer_elems, dtype=torch.bfloat16, device=dev)
+        d_out_all = torch.empty(L * B * HQ * D, dtype=torch.bfloat16, device=dev)
+        d_seq = torch.empty(B, dtype=torch.int32, device=dev)
+        d_in = [split(d_in_all, layer * layer_elems) for layer in range(L)]
+        d_out = [d_out_all[layer * B * HQ * D:(layer + 1) * B * HQ * D].view(B, HQ, D) for layer in range(L)]
+        graph = pkv.DecodeStep(sw.k_caches, sw.v_caches, [t[0] for t in d_in], [t[1] for t in d_in],
+                               [t[2] for t in d_in], bt, d_seq, sw.softmax_scale, d_out, workspace=ws, flags=flags)
+        sets.append((d_in_all, d_out_all, d_seq, graph))
     h_in = []
     for r in range(2):  # two pinned input sets, alternated
         h = torch.empty(L * layer_elems, dtype=torch.bfloat16).pin_memory()
@@ -704,29 +714,50 @@ def main():
             for dst, t in zip(split(h, layer * layer_elems), trip):
                 dst.copy_(t.cpu())
         h_in.append(h)
-    h_seq = [torch.as_tensor(lens_all[s % DECODE_CAPACITY]).pin_memory() for s in range(e2e_steps)]
-    h_out = torch.empty(L * B * HQ * D, dtype=torch.bfloat16).pin_memory()
-    h2d = d_in_all.numel() * 2 + B * 4
-    d2h = d_out_all.numel() * 2
-    step_graph = pkv.DecodeStep(sw.k_caches, sw.v_caches, [t[0] for t in d_in], [t[1] for t in d_in],
-                                [t[2] for t in d_in], bt, d_seq, sw.softmax_scale, d_out, workspace=ws, flags=flags)
+    h_seq = [torch.as_tensor(lens_all[(s0 + i) % DECODE_CAPACITY]).pin_memory() for i in range(e2e_steps)]
+    h_out = [torch.empty(L * B * HQ * D, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    h2d = sets[0][0].numel() * 2 + B * 4
+    d2h = sets[0][1].numel() * 2
+    up, down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ev = lambda: torch.cuda.Event()  # noqa: E731
+    in_ready = [ev() for _ in range(e2e_steps)]
+    done = [ev() for _ in range(e2e_steps)]
+    out_read = [ev() for _ in range(e2e_steps)]
+
+    def upload(i):  # step i's inputs into set i % 2, once step i-2 (same set) is read and copied out
+        with torch.cuda.stream(up):
+            if i >= 2:
+                up.wait_event(out_read[i - 2])
+            d_in_all, _, d_seq, _ = sets[i % 2]
+            d_in_all.copy_(h_in[(s0 + i) % 2], non_blocking=True)
+            d_seq.copy_(h_seq[i], non_blocking=True)
+            in_ready[i].record(up)
+
     torch.cuda.synchronize(dev)
     barrier(world)
     e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e_bytes = 0
     e_start.record(stream)
-    for s in range(e2e_steps):
-        d_in_all.copy_(h_in[s % 2], non_blocking=True)
-        d_seq.copy_(h_seq[s], non_blocking=True)
-        step_graph.launch()
-        h_out.copy_(d_out_all, non_blocking=True)
-        e_bytes += step_bytes[s % DECODE_CAPACITY]
+    up.wait_stream(stream)
+    upload(0)
+    for i in range(e2e_steps):
+        if i + 1 < e2e_steps:
+            upload(i + 1)
+        stream.wait_event(in_ready[i])
+        sets[i % 2][3].launch()
+        done[i].record(stream)
+        with torch.cuda.stream(down):
+            down.wait_event(done[i])
+            h_out[i % 2].copy_(sets[i % 2][1], non_blocking=True)
+            out_read[i].record(down)
+        e_bytes += step_bytes[(s0 + i) % DECODE_CAPACITY]
+    stream.wait_stream(down)
     e_end.record(stream)
     torch.cuda.synchronize(dev)
     e_ms = max_over_ranks(e_start.elapsed_time(e_end), world, dev)
     e_all = sum_over_ranks(float(e_bytes), world, dev)
     e2e_value = e_all / (e_ms * 1e-3) / 1e9
-    del step_graph
+    del sets
 
     prefill = prefill_bench(dev, args.prefill_reps) if args.prefill_reps > 0 else None
 
@@ -760,8 +791,9 @@ def main():
         "clocks": clocks.summary(),
         "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "steps": e2e_steps,
-                "path": "pkv_decode_step graph of the 36 layers; per step pinned H2D of all inputs and "
-                        "cache_seqlens, one launch, D2H of all outputs"},
+                "path": "pkv_decode_step graphs of the 36 layers over two buffer sets; per step pinned H2D of "
+                        "all inputs and cache_seqlens, one graph launch, D2H of all outputs; copies on their own "
+                        "streams, double-buffered (step s+1's upload and step s-1's download overlap step s)"},
         "eager": {"value": eager_gbs, "unit": "GB/s", "steps": eager_steps,
                   "launch": "plain stream launches, no CUDA graph"},
         "gpu_launches": n_ev,
