@@ -215,3 +215,53 @@ def test_speculative_decode_qwen3_layer_sampled():
     t, h = np.array(sel).T
     assert_close(out[t, h], rout[t, h])
     assert_lse_close(lse[t, h], rlse[t, h])
+
+
+def _bench_workload_sampled(case, rows, max_qlen, tokens_per_row=None, seed=0):
+    """The full workload on the GPU in the bench's launch configuration (the
+    library's default decode_max_qlen); the oracle on a host copy of only the
+    sampled rows' pages, taken before the call (the oracle appends itself).
+    Checks the rows' appended slots bit for bit and sampled (token, head)
+    outputs within tolerance."""
+    dq = pkv.default_decode_max_qlen(case.num_q_heads, case.num_kv_heads)
+    ql = np.diff(case.qo_indptr)
+    need = case.cache_seqlens[rows] + ql[rows]
+    k0, v0, bt_sub = wl.compact_rows(case.k_cache, case.v_cache, case.block_table, rows, need, case.page_size)
+    out, lse, err, kc, vc = _run_gpu(case, max_qlen, dq)
+    assert err == 0
+    toks = [np.arange(case.qo_indptr[b], case.qo_indptr[b + 1]) for b in rows]
+    idx = np.concatenate(toks)
+    qo_sub = np.concatenate([[0], np.cumsum(ql[rows])]).astype(np.int32)
+    d = oracle.CacheDesc(k0.shape[0], case.page_size, case.num_kv_heads, case.head_dim, case.layout)
+    rng = np.random.default_rng(seed)
+    sel = []
+    for i, t in enumerate(toks):
+        pick = t if tokens_per_row is None or len(t) <= tokens_per_row else \
+            np.unique(np.concatenate([[t[0], t[-1]], rng.choice(t, tokens_per_row - 2, replace=False)]))
+        base = int(qo_sub[i]) - int(t[0])
+        sel += [(int(x) + base, h) for x in pick for h in rng.choice(case.num_q_heads, 4, replace=False)]
+    k_or, v_or = k0.copy(), v0.copy()
+    rout, rlse, rerr, _ = oracle.mixed(d, k_or, v_or, wl.bits(case.q)[idx], wl.bits(case.k_new)[idx],
+                                       wl.bits(case.v_new)[idx], qo_sub, bt_sub, case.cache_seqlens[rows],
+                                       case.softmax_scale, max_qlen=max_qlen, sel=sel)
+    assert rerr == 0
+    k1, v1, _ = wl.compact_rows(kc, vc, case.block_table, rows, need, case.page_size)
+    assert np.array_equal(k1, k_or) and np.array_equal(v1, v_or), "appended slots differ"
+    t_sub, h = np.array(sel).T
+    assert_close(out[idx[t_sub], h], rout[t_sub, h])
+    assert_lse_close(lse[idx[t_sub], h], rlse[t_sub, h])
+
+
+def test_spec_decode_bench_workload_sampled():
+    """bench.py --workload spec: B=32 rows of 4 tokens, Qwen3-shaped, page 16,
+    65,536-page shuffled pool; decode kernel (multi-query rows)."""
+    case = wl.spec_decode(device=DEV)
+    _bench_workload_sampled(case, [0, 7, 13, 22, 31], 4)
+
+
+def test_chunked_bench_workload_sampled():
+    """bench.py --workload chunked: 4 chunks of 496 tokens on prefixes
+    U[0,2048] + 60 decode rows; chunks on the prefill kernel, decode rows on
+    the decode kernel, in one call."""
+    case = wl.chunked_mix(device=DEV)
+    _bench_workload_sampled(case, [0, 3, 4, 30, 63], 496, tokens_per_row=12)
