@@ -125,13 +125,14 @@ CUresult encode_pool_map(CUtensorMap *map, const pkv_cache_desc &d, void *base, 
 
 
 
-CUresult encode_group_map(CUtensorMap *map, const pkv_cache_desc &d, void *base, int box_tokens)
+CUresult encode_group_map(CUtensorMap *map, const pkv_cache_desc &d, void *base, int box_tokens, int box_blocks)
 {
     PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
     if (enc == nullptr)
         return CUDA_ERROR_NOT_FOUND;
     const cuuint64_t D = (cuuint64_t)d.head_dim, P = (cuuint64_t)d.page_size, H = (cuuint64_t)d.num_kv_heads;
-    const cuuint32_t box[5] = {64, 8, (cuuint32_t)(D / 64), (cuuint32_t)(box_tokens / 8), 1};
+    const cuuint32_t blocks = box_blocks > 0 ? (cuuint32_t)box_blocks : (cuuint32_t)(D / 64);
+    const cuuint32_t box[5] = {64, 8, blocks, (cuuint32_t)(box_tokens / 8), 1};
     const cuuint32_t elem_strides[5] = {1, 1, 1, 1, 1};
     cuuint64_t dims[5], strides[4];
     if (d.layout == PKV_HND) { // [pages * Hkv][P][D]
@@ -439,10 +440,8 @@ pkv_status pkv_prefill_attn(const pkv_cache_desc *desc, const void *k_cache, con
     a.workspace = workspace;
     a.err_flag = err_flag;
     a.shape = shape;
-    const int box = prefill_box_tokens(desc->page_size);
     PrefillMaps maps;
-    if (encode_group_map(&maps.k, *desc, const_cast<void *>(k_cache), box) != CUDA_SUCCESS ||
-        encode_group_map(&maps.v, *desc, const_cast<void *>(v_cache), box) != CUDA_SUCCESS)
+    if (!encode_prefill_maps(*desc, k_cache, v_cache, &maps))
         return PKV_ECUDA;
     return launch_prefill(a, maps, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PKV_OK : PKV_ECUDA;
 }
@@ -564,10 +563,8 @@ pkv_status pkv_mixed_attn(const pkv_cache_desc *desc, void *k_cache, void *v_cac
         a.q_lo = m.dq;
         a.q_max = max_qlen;
         a.kv_add = k_new != nullptr ? 1 : 0;
-        const int box = prefill_box_tokens(desc->page_size);
         PrefillMaps maps;
-        if (encode_group_map(&maps.k, *desc, k_cache, box) != CUDA_SUCCESS ||
-            encode_group_map(&maps.v, *desc, v_cache, box) != CUDA_SUCCESS)
+        if (!encode_prefill_maps(*desc, k_cache, v_cache, &maps))
             return PKV_ECUDA;
         if (launch_prefill(a, maps, s) != cudaSuccess)
             return PKV_ECUDA;

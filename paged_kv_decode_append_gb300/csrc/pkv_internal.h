@@ -137,7 +137,8 @@ CUresult encode_pool_map(CUtensorMap *map, const pkv_cache_desc &d, void *base, 
 // bytes apart whichever page they come from.  5-D: (64 columns, 8 tokens,
 // column blocks, token groups, page-heads) over HND, (64 columns, 8 tokens,
 // column blocks, token groups across pages, heads) over NHD.
-CUresult encode_group_map(CUtensorMap *map, const pkv_cache_desc &d, void *base, int box_tokens);
+// box_blocks: 64-column blocks per box (0: all of head_dim).
+CUresult encode_group_map(CUtensorMap *map, const pkv_cache_desc &d, void *base, int box_tokens, int box_blocks = 0);
 
 int sm_count(int device);
 
@@ -189,6 +190,9 @@ struct PrefillMaps {
 cudaError_t launch_prefill(const PrefillArgs &a, const PrefillMaps &maps, cudaStream_t stream);
 
 int prefill_box_tokens(int page_size);
+
+// The K and V tensor maps the prefill kernel for this head_dim reads.
+bool encode_prefill_maps(const pkv_cache_desc &d, const void *k_cache, const void *v_cache, PrefillMaps *maps);
 
 
 } // namespace pkv

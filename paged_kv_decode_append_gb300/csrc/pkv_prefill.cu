@@ -9,32 +9,39 @@
 // h / (Hq / Hkv); softmax scale, output rounding and the error rules are
 // those of include/pkv.h.
 //
-// How (one persistent CTA per SM):
-//  - Work unit = (request, kv head, tile of 128/G queries).  The G query
-//    heads sharing a kv head times 128/G consecutive queries form the M = 128
-//    rows of every MMA (row r = query r/G, head r%G), so every K/V tile read
-//    from the pages serves all G heads.
-//  - A one-CTA plan kernel validates every request, lists the query tiles and
+// How (one persistent CTA per SM, clusters of two):
+//  - Work unit = (request, kv head, two consecutive tiles of 128/G queries).
+//    The G query heads sharing a kv head times 128/G consecutive queries form
+//    a CTA's 128 MMA rows (row r = query r/G, head r%G), so every K/V tile
+//    read from the pages serves all G heads.
+//  - A one-CTA plan kernel validates every request, lists the units and
 //    orders them by their number of 64-token kv tiles, longest first; the
-//    persistent CTAs take units in that order, snaking over the grid.
-//  - Warp roles: warp 0 loads the unit's K and V tiles, 64 tokens x head_dim
-//    each, with TMA into a ring of shared-memory stages (in the order the
-//    MMAs consume them); warp 1 owns TMEM and one of its threads issues the
-//    MMAs; warps 2-5 (one per TMEM lane quarter) load Q into TMEM and run the
-//    online softmax and the epilogue, one row per thread.
-//  - TMEM: the O [128 x D] fp32 accumulator at columns 0..D-1, two
-//    S [128 x 64] fp32 buffers after it (S of tile j+1 is computed while the
-//    softmax of tile j runs), then the unit's Q [128 x D] as bf16 pairs.
-//    Keeping Q out of shared memory leaves room for a deep K/V ring: the
-//    tiles come mostly from L2, and it takes several of them in flight to
-//    cover its latency.  The next unit's Q is written while the last PV
-//    MMAs of the current one run.
-//  - S = Q K^T (Q from TMEM, K-major K); the softmax writes P back into the
-//    tile's S columns of TMEM as two bf16 parts, p = hi + lo (about 16
-//    significant bits: a single bf16 P alone, 8 bits, leaves errors near
-//    2^-9 of the row's scale, well above 1e-2 of the small outputs that
-//    cancellation produces); O += P_hi V + P_lo V with P from TMEM and V as
-//    an MN-major operand (its rows are tokens, its columns head_dim).
+//    persistent clusters take units in that order, snaking over the grid.
+//  - head_dim 128 and 256 (prefill2_kernel): the cluster is a CTA pair
+//    whose MMAs (tcgen05.mma.cta_group::2, M = 256) cover both query tiles,
+//    issued by one thread of the even CTA.  Keys go in steps of 128.  For
+//    S = Q K^T (N = 128) the even CTA holds the step's first 64-key K tile
+//    and the odd CTA the second; for O += P V (N = head_dim) each CTA holds
+//    all 128 keys of its half of head_dim -- each SM stages half of every
+//    operand, and one instruction does twice the work of a single-CTA MMA
+//    with N = 64 (issuing one costs about the same whatever its shape).
+//    TMEM: O [128 x D] fp32 and two S [128 x 128] buffers (S of step t+1 is
+//    computed while the softmax of step t runs); Q [128 x D] in shared
+//    memory, K-major and swizzled.
+//  - head_dim 64 (prefill_kernel): one query tile per CTA, 64-key tiles,
+//    K / V shared by the cluster through TMA multicast, Q in TMEM.
+//  - Warp roles: warp 0 loads this CTA's K and V with TMA into a ring of
+//    shared-memory stages (in the order the MMAs consume them); warp 1 owns
+//    TMEM and one of its threads issues the MMAs (the odd CTA of a pair:
+//    relays its stage completions to it); warps 2-9 (two per TMEM lane
+//    quarter) run the online softmax and the epilogue, each thread on half
+//    of its row's columns.
+//  - The softmax writes P back over the S columns it has just read, as two
+//    bf16 parts, p = hi + lo (about 16 significant bits: a single bf16 P
+//    alone, 8 bits, leaves errors near 2^-9 of the row's scale, well above
+//    1e-2 of the small outputs that cancellation produces); O += P_hi V +
+//    P_lo V with P from TMEM and V as an MN-major operand (its rows are
+//    tokens, its columns head_dim).
 //  - Online softmax in base 2 on scores scaled by softmax_scale * log2(e).
 //    A row's O and running sum are rescaled only when its maximum grows by
 //    more than 8: until then the exponentials use the older maximum, which is
@@ -65,6 +72,7 @@ constexpr float kLn2 = 0.693147180559945309f;
 constexpr int kPfMaxStages = 12;
 
 template <int D> struct PfCfg {
+    static constexpr bool kPair = false;
     static constexpr int kChunks = D / 64;                                      // 128-byte column blocks of a row
     static constexpr int kStages = D == 256 ? 6 : kPfMaxStages; // K / V tiles in flight
     // A K or V stage is [8-token group][64-column block][8 rows][128 B]: for
@@ -82,14 +90,46 @@ template <int D> struct PfCfg {
     static constexpr uint32_t kColS = D;
     static constexpr uint32_t kColQ = D + 2 * kPfTile;     // D / 2 columns of bf16 pairs
     static constexpr uint32_t kTmemCols = (kColQ + D / 2) <= 256 ? 256 : 512;
+    // a V tile in a stage: all of head_dim (the same layout as K)
+    static constexpr uint32_t kItemBytes = kStageBytes;
+    static constexpr uint32_t kVGroupStride = kGroupStride;
+    static constexpr int kVChunks = kChunks;
 };
-static_assert(PfCfg<256>::kSmem <= 232448 && PfCfg<128>::kSmem <= 232448 && PfCfg<64>::kSmem <= 232448,
-              "prefill shared memory over the per-CTA limit");
-static_assert(PfCfg<256>::kColQ + 128 <= 512, "prefill TMEM columns");
 
-struct PfBars {
+// CTA pairs (head_dim 128 and 256), in steps of 128 keys (two 64-key tiles).
+// The pair's MMAs have M = 256 (one query tile per CTA) and read each operand
+// half from one CTA: for S = Q K^T (N = 128 keys) the even CTA holds the
+// step's first K tile and the odd CTA its second, all of head_dim; for
+// O += P V (N = head_dim) each CTA holds all 128 keys of its half of
+// head_dim.  Q sits in shared memory (TMEM holds O and two 128-column S
+// buffers).  An item is a step's K tile or its V half; both are
+// 64 * head_dim * 2 bytes.
+constexpr int kPfPairMaxStages = 12;
+constexpr int kPfStep = 2 * kPfTile; // keys per step
+template <int D> struct Pf2Cfg {
+    static_assert(D == 128 || D == 256, "pairs split head_dim into 64-column blocks");
+    static constexpr uint32_t kItemBytes = kPfTile * D * 2;
+    static constexpr int kStages = D == 256 ? 4 : 11;              // items in flight
+    static constexpr uint32_t kGroupStride = 8 * D * 2;            // K and Q: 8 rows x head_dim
+    static constexpr uint32_t kVGroupStride = 8 * (D / 2) * 2;     // V half: 8 keys x half of head_dim
+    static constexpr int kVChunks = D / 128;                       // 64-column blocks of a V half
+    static constexpr uint32_t kOffStage = 0;
+    static constexpr uint32_t kOffQ = kOffStage + kStages * kItemBytes;  // Q [128 rows][head_dim], K-major, swizzled
+    static constexpr uint32_t kOffBar = kOffQ + kPfRows * D * 2;
+    static constexpr uint32_t kOffXchg = kOffBar + 1024;
+    static constexpr uint32_t kSmem = kOffXchg + 3 * 1024 + 1024;
+    static constexpr uint32_t kColO = 0;
+    static constexpr uint32_t kColS = D;                           // two S buffers of kPfStep columns
+    static constexpr uint32_t kTmemCols = 512;
+};
+static_assert(Pf2Cfg<256>::kSmem <= 232448 && Pf2Cfg<128>::kSmem <= 232448, "pair prefill shared memory");
+static_assert(Pf2Cfg<256>::kColS + 2 * kPfStep <= 512, "pair prefill TMEM columns");
+
+template <int S>
+struct PfBarsT {
     uint64_t q_full, q_empty;
-    uint64_t full[kPfMaxStages], empty[kPfMaxStages];
+    uint64_t full[S], empty[S];
+    uint64_t peer_full[S]; // CTA pairs: the odd CTA's half of a stage has landed (relayed)
     uint64_t s_full[2], p_full[2], o_done[2];
     uint64_t o_free;
     uint64_t drain;
@@ -97,7 +137,10 @@ struct PfBars {
     uint32_t tmem_base;
     int32_t abort;
 };
+using PfBars = PfBarsT<kPfMaxStages>;
+using Pf2Bars = PfBarsT<kPfPairMaxStages>;
 static_assert(sizeof(PfBars) <= 512, "barrier block");
+static_assert(sizeof(Pf2Bars) <= 1024, "pair barrier block");
 
 // `cluster` consecutive query tiles of one request (all kv heads share it):
 // CTA rank r of a cluster takes query tile t * cluster + r.
@@ -168,16 +211,28 @@ __device__ __forceinline__ int pf_unit_at(int k, int cluster)
     return k * g + ((k & 1) ? g - 1 - c : c);
 }
 
-// Bounded barrier wait that also gives up when another role has aborted.
-__device__ __noinline__ bool pf_wait(uint64_t *bar, uint32_t parity, PfBars &bars, int32_t *err_flag)
+template <bool CL>
+__device__ __forceinline__ bool pf_try(uint64_t *bar, uint32_t parity)
 {
-    if (mbar_try_wait(bar, parity))
+    if constexpr (CL)
+        return mbar_try_wait_cluster(bar, parity);
+    else
+        return mbar_try_wait(bar, parity);
+}
+
+// Bounded barrier wait that also gives up when another role has aborted.
+// CL: acquire at cluster scope (barriers that another CTA's threads or MMAs
+// arrive on, in CTA pairs).
+template <bool CL, class Bars>
+__device__ __noinline__ bool pf_wait(uint64_t *bar, uint32_t parity, Bars &bars, int32_t *err_flag)
+{
+    if (pf_try<CL>(bar, parity))
         return true;
     const uint64_t start = globaltimer_ns();
     volatile int32_t *abort = &bars.abort;
     for (;;) {
         for (int i = 0; i < 64; ++i)
-            if (mbar_try_wait(bar, parity))
+            if (pf_try<CL>(bar, parity))
                 return true;
         if (*abort != 0)
             return false;
@@ -188,12 +243,17 @@ __device__ __noinline__ bool pf_wait(uint64_t *bar, uint32_t parity, PfBars &bar
         }
     }
 }
+__device__ __forceinline__ bool pf_wait(uint64_t *bar, uint32_t parity, PfBars &bars, int32_t *err_flag)
+{
+    return pf_wait<false>(bar, parity, bars, err_flag);
+}
 
 // pf_wait for a whole warp: every lane gets the same answer, so warp-collective
 // instructions after it are reached by all lanes or none.
-__device__ __forceinline__ bool pf_wait_all(uint64_t *bar, uint32_t parity, PfBars &bars, int32_t *err_flag)
+template <bool CL = false, class Bars>
+__device__ __forceinline__ bool pf_wait_all(uint64_t *bar, uint32_t parity, Bars &bars, int32_t *err_flag)
 {
-    const bool ok = pf_wait(bar, parity, bars, err_flag);
+    const bool ok = pf_wait<CL>(bar, parity, bars, err_flag);
     return __all_sync(0xffffffffu, ok);
 }
 
@@ -324,12 +384,11 @@ __device__ void pf_mma(const PfParams &p, uint8_t *smem, PfBars &bars, uint32_t 
                 tc_fence_after();
                 issued = true;
                 const uint32_t d = tmem + C::kColS + (uint32_t)(gt & 1) * kPfTile;
-                const uint32_t kb = st_base + stage * C::kStageBytes;
+                const uint64_t kd = tc_sw128_desc(st_base + stage * C::kStageBytes, 16, C::kGroupStride);
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint64_t b = tc_sw128_desc(kb + (kk >> 2) * 1024 + (kk & 3) * 32, 16, C::kGroupStride);
-                    tc_mma_bf16_ts(d, tmem + C::kColQ + kk * 8, b, kIdescS, kk > 0 ? 1u : 0u);
-                }
+                for (int kk = 0; kk < D / 16; ++kk)
+                    tc_mma_bf16_ts(d, tmem + C::kColQ + kk * 8, kd + (uint64_t)(((kk >> 2) * 1024 + (kk & 3) * 32) >> 4),
+                                   kIdescS, kk > 0 ? 1u : 0u);
                 tc_commit(&bars.s_full[gt & 1]);
                 if (p.cluster > 1) // the stage is refilled for the whole cluster
                     tc_commit_mc(&bars.empty[stage], cl_mask);
@@ -349,14 +408,14 @@ __device__ void pf_mma(const PfParams &p, uint8_t *smem, PfBars &bars, uint32_t 
                 if (!pf_wait(&bars.full[stage], (itg / C::kStages) & 1, bars, p.err_flag))
                     goto done;
                 tc_fence_after();
-                const uint32_t vb = st_base + stage * C::kStageBytes;
                 const uint32_t pt = tmem + C::kColS + (uint32_t)(gt & 1) * kPfTile; // P of tile gt
+                // V rows 16*k4 .. +15: two 8-row groups; N spans the column blocks (1024 B apart)
+                const uint64_t vd = tc_sw128_desc(st_base + stage * C::kStageBytes, 1024, C::kGroupStride);
 #pragma unroll
                 for (int kk = 0; kk < 2 * (kPfTile / 16); ++kk) { // hi part, then lo part
                     const int k4 = kk & (kPfTile / 16 - 1);      // 16-token K step
-                    // V rows 16*k4 .. +15: two 8-row groups; N spans the column blocks (1024 B apart)
-                    const uint64_t b = tc_sw128_desc(vb + (uint32_t)(2 * k4) * C::kGroupStride, 1024, C::kGroupStride);
-                    tc_mma_bf16_ts(tmem + C::kColO, pt + (kk >> 2) * (kPfTile / 2) + k4 * 8, b, kIdescO,
+                    tc_mma_bf16_ts(tmem + C::kColO, pt + (kk >> 2) * (kPfTile / 2) + k4 * 8,
+                                   vd + (uint64_t)((2 * k4 * C::kGroupStride) >> 4), kIdescO,
                                    (jv > 0 || kk > 0) ? 1u : 0u);
                 }
                 tc_commit(&bars.o_done[gt & 1]);
@@ -383,11 +442,10 @@ done:
 // Writes this thread's half of its row of a unit's Q tile (query r / G, head
 // r % G of the group; head_dim columns [half * D/2, (half+1) * D/2)) into TMEM
 // columns kColQ + half * D/4 .. as bf16 pairs; rows past total_q get 0.
-template <int D>
+template <int D, class C>
 __device__ __forceinline__ void pf_load_q(const PfParams &p, const PfUnit &un, int g, int r, int half,
                                           uint32_t t_row, int cl_rank)
 {
-    using C = PfCfg<D>;
     const int tok = un.q_start + (un.t * p.cluster + cl_rank) * p.q_tile + (r >> p.group_shift);
     const int head = g * (1 << p.group_shift) + (r & ((1 << p.group_shift) - 1));
     const bool in = tok < p.total_q;
@@ -426,17 +484,39 @@ __device__ __forceinline__ void pf_load_q(const PfParams &p, const PfUnit &un, i
 
 // Synchronises the two warps that share a TMEM lane quarter (their `phase`-th
 // meeting); bounded like every wait, false if it gave up.
-__device__ __forceinline__ bool pf_pair_sync(PfBars &bars, int quarter, uint32_t &phase, int32_t *err_flag)
+template <class Bars>
+__device__ __forceinline__ bool pf_pair_sync(Bars &bars, int quarter, uint32_t &phase, int32_t *err_flag)
 {
     mbar_arrive(&bars.pair[quarter]);
     return pf_wait_all(&bars.pair[quarter], (phase++) & 1, bars, err_flag);
 }
 
-template <int D>
-__device__ void pf_softmax(const PfParams &p, uint8_t *smem, PfBars &bars, uint32_t tmem, int n_units, int warp,
+// A softmax thread's arrival on a barrier the MMA thread waits on: every
+// thread arrives (one CTA), or -- CTA pairs -- each warp arrives once on the
+// barrier of the pair's even CTA (rank 0), whose MMA thread issues for both:
+// locally there, remotely from the odd CTA.  The thread's tcgen05 /
+// shared-memory writes are fenced before the call.
+template <bool PAIR>
+__device__ __forceinline__ void pf_arrive_mma(uint64_t *bar, int lane, int rank)
+{
+    if constexpr (PAIR) {
+        __syncwarp();
+        if (lane == 0) {
+            if (rank == 0)
+                mbar_arrive(bar);
+            else
+                mbar_arrive_remote(bar, 0);
+        }
+    } else {
+        mbar_arrive(bar);
+    }
+}
+
+template <int D, class C, class Bars>
+__device__ void pf_softmax(const PfParams &p, uint8_t *smem, Bars &bars, uint32_t tmem, int n_units, int warp,
                            int lane, int cl_rank)
 {
-    using C = PfCfg<D>;
+    constexpr bool PAIR = C::kPair;
     constexpr int kCols = kPfTile / 2;    // S columns of this thread
     const int quarter = warp & 3;         // TMEM lanes this warp may access
     const int half = (warp - 2) >> 2;     // which half of the row's columns
@@ -456,9 +536,9 @@ __device__ void pf_softmax(const PfParams &p, uint8_t *smem, PfBars &bars, uint3
         return;
     {
         const int grp = u / p.num_kv_heads;
-        pf_load_q<D>(p, p.units[grp], u - grp * p.num_kv_heads, r, half, t_row, cl_rank);
+        pf_load_q<D, C>(p, p.units[grp], u - grp * p.num_kv_heads, r, half, t_row, cl_rank);
         tc_fence_before();
-        mbar_arrive(&bars.q_full);
+        pf_arrive_mma<PAIR>(&bars.q_full, lane, cl_rank);
     }
     for (int k = 0;; ++k) {
         u = pf_unit_at(k, p.cluster);
@@ -476,7 +556,7 @@ __device__ void pf_softmax(const PfParams &p, uint8_t *smem, PfBars &bars, uint3
         float m_used = -INFINITY, l = 0.f; // l: this half's part of the row sum
         for (int j = 0; j < nt; ++j) {
             const int gt = gt0 + j;
-            if (!pf_wait_all(&bars.s_full[gt & 1], (gt >> 1) & 1, bars, p.err_flag))
+            if (!pf_wait_all<PAIR>(&bars.s_full[gt & 1], (gt >> 1) & 1, bars, p.err_flag))
                 return;
             tc_fence_after();
             // Raw scores of this half; a non-positive scale is applied here, a
@@ -542,7 +622,7 @@ __device__ void pf_softmax(const PfParams &p, uint8_t *smem, PfBars &bars, uint3
             const bool rescale_o = grow && j > 0;
             if (__any_sync(0xffffffffu, rescale_o)) {
                 const int gp = gt - 1;
-                if (!pf_wait_all(&bars.o_done[gp & 1], (gp >> 1) & 1, bars, p.err_flag))
+                if (!pf_wait_all<PAIR>(&bars.o_done[gp & 1], (gp >> 1) & 1, bars, p.err_flag))
                     return;
                 tc_fence_after();
                 const float a = rescale_o ? alpha : 1.f;
@@ -567,32 +647,32 @@ __device__ void pf_softmax(const PfParams &p, uint8_t *smem, PfBars &bars, uint3
             if (j * kPfTile + kPfTile > kv) {
                 const int itg = ib + pf_item_v(j, nt);
                 const int stage = itg % C::kStages;
-                if (!pf_wait_all(&bars.full[stage], (itg / C::kStages) & 1, bars, p.err_flag))
+                if (!pf_wait_all<PAIR>(&bars.full[stage], (itg / C::kStages) & 1, bars, p.err_flag))
                     return;
                 const int r0 = kv - j * kPfTile;
-                uint8_t *vb = smem + C::kOffStage + stage * C::kStageBytes;
-                // 16-byte pieces of rows r0..63, every 64-column block
-                for (int i = st; i < (kPfTile - r0) * C::kChunks * 8; i += kPfSoftmaxThreads) {
+                uint8_t *vb = smem + C::kOffStage + stage * C::kItemBytes;
+                // 16-byte pieces of rows r0..63, every 64-column block of the stage
+                for (int i = st; i < (kPfTile - r0) * C::kVChunks * 8; i += kPfSoftmaxThreads) {
                     const int piece = i & 7, rest = i >> 3;
-                    const int c = rest % C::kChunks, tt = r0 + rest / C::kChunks;
-                    *reinterpret_cast<uint4 *>(vb + (tt >> 3) * C::kGroupStride + c * 1024 + (tt & 7) * 128 +
+                    const int c = rest % C::kVChunks, tt = r0 + rest / C::kVChunks;
+                    *reinterpret_cast<uint4 *>(vb + (tt >> 3) * C::kVGroupStride + c * 1024 + (tt & 7) * 128 +
                                                piece * 16) = make_uint4(0u, 0u, 0u, 0u);
                 }
+                fence_proxy_async_smem(); // the zeros before the PV MMA's (async proxy) read
             }
-            fence_proxy_async_smem();
             tc_fence_before();
-            mbar_arrive(&bars.p_full[gt & 1]);
+            pf_arrive_mma<PAIR>(&bars.p_full[gt & 1], lane, cl_rank);
         }
         // The next unit's Q, once this unit's S MMAs have read theirs; the MMA
         // thread meanwhile runs this unit's last PV.
         if (u_next < n_units) {
-            if (!pf_wait_all(&bars.q_empty, k & 1, bars, p.err_flag))
+            if (!pf_wait_all<PAIR>(&bars.q_empty, k & 1, bars, p.err_flag))
                 return;
             tc_fence_after();
             const int pn = u_next / p.num_kv_heads;
-            pf_load_q<D>(p, p.units[pn], u_next - pn * p.num_kv_heads, r, half, t_row, cl_rank);
+            pf_load_q<D, C>(p, p.units[pn], u_next - pn * p.num_kv_heads, r, half, t_row, cl_rank);
             tc_fence_before();
-            mbar_arrive(&bars.q_full);
+            pf_arrive_mma<PAIR>(&bars.q_full, lane, cl_rank);
         }
         { // epilogue: O / l -> bf16 (this half's columns), lse
             float *xl = xchg + 4 * kPfRows;
@@ -603,7 +683,7 @@ __device__ void pf_softmax(const PfParams &p, uint8_t *smem, PfBars &bars, uint3
             if (!pf_pair_sync(bars, quarter, pair_phase, p.err_flag)) // both read before the next unit's sums overwrite
                 return;
             const int gl = gt0 + nt - 1;
-            if (!pf_wait_all(&bars.o_done[gl & 1], (gl >> 1) & 1, bars, p.err_flag))
+            if (!pf_wait_all<PAIR>(&bars.o_done[gl & 1], (gl >> 1) & 1, bars, p.err_flag))
                 return;
             tc_fence_after();
             const float inv = lt > 0.f ? 1.f / lt : 0.f;
@@ -628,7 +708,7 @@ __device__ void pf_softmax(const PfParams &p, uint8_t *smem, PfBars &bars, uint3
                 }
             }
             tc_fence_before();
-            mbar_arrive(&bars.o_free);
+            pf_arrive_mma<PAIR>(&bars.o_free, lane, cl_rank);
             if (half == 0 && valid && p.lse != nullptr)
                 p.lse[row] = (m_used + log2f(lt)) * kLn2;
         }
@@ -691,7 +771,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             pf_mma<D>(p, smem, bars, tmem, n_units);
         __syncwarp();
     } else
-        pf_softmax<D>(p, smem, bars, tmem, n_units, warp, lane, cl_rank);
+        pf_softmax<D, PfCfg<D>, PfBars>(p, smem, bars, tmem, n_units, warp, lane, cl_rank);
 
     tc_fence_before();
     if (p.cluster > 1)
@@ -701,6 +781,499 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     tc_fence_after();
     if (warp == kPfMmaWarp)
         tmem_dealloc(tmem, C::kTmemCols);
+}
+
+// ---------------------------------------------------------------- CTA pairs
+
+// Producer of one CTA of a pair, step by step (128 keys): item K_t is the
+// step's tile 2t + r (r = this CTA's rank), 64 keys with all of head_dim;
+// item V_t is all 128 keys of the step with columns [r D/2, (r+1) D/2).
+// Boxes of min(page, 64) tokens; items in the MMA's consumption order (K_0,
+// K_1, V_0, K_2, V_1, ...), each into this CTA's shared memory and onto its
+// own full barrier; a stage is refilled once the pair's MMA that read it has
+// completed.
+template <int D>
+__device__ void pf2_producer(const PfParams &p, const PfMapsDev &maps, uint8_t *smem, Pf2Bars &bars, int n_units,
+                             int lane, int rank)
+{
+    using C = Pf2Cfg<D>;
+    const int Hkv = p.num_kv_heads;
+    const int P = 1 << p.page_shift;
+    const int bsh = p.box_shift; // min(P, 64) tokens per box
+    const int BT = 1 << bsh;
+    const uint32_t kbox = (uint32_t)BT * D * 2, vbox = (uint32_t)BT * (D / 2) * 2;
+    const bool nhd = p.layout == PKV_NHD;
+    int ib = 0, issued = 0;
+    bool ok = true;
+    for (int k = 0; ok; ++k) {
+        const int u = pf_unit_at(k, p.cluster);
+        if (u >= n_units)
+            break;
+        const int grp = u / Hkv, g = u - grp * Hkv;
+        const PfUnit un = p.units[grp];
+        const int32_t *bt_row = p.block_table + (int64_t)un.b * p.max_blocks;
+        const int ns = (un.n_tiles + 1) >> 1, kv = un.kv_len;
+        // lane i holds the page of tokens 128t + i*BT .. (i < 128 / BT <= 16)
+        auto page_ids = [&](int t) {
+            const int tok = t * kPfStep + (lane << bsh);
+            int id = 0;
+            if ((lane << bsh) < kPfStep && t < ns && tok < kv)
+                id = __ldg(bt_row + (tok >> p.page_shift));
+            return id;
+        };
+        int ids_prev = 0, ids_cur = page_ids(0), ids_next = page_ids(1);
+        for (int t = 0; t <= ns && ok; ++t) {
+            for (int kind = 0; kind < 2; ++kind) { // K_t, then V_{t-1}
+                const int tt = kind == 0 ? t : t - 1;
+                if (kind == 0 ? (t >= ns) : (t < 1))
+                    continue;
+                const int itg = ib + (kind == 0 ? pf_item_k(tt) : pf_item_v(tt, ns));
+                const int stage = itg % C::kStages;
+                const int n = itg / C::kStages;
+                if (n > 0 && !pf_wait_all<true>(&bars.empty[stage], (n - 1) & 1, bars, p.err_flag)) {
+                    ok = false;
+                    break;
+                }
+                uint8_t *dst = smem + C::kOffStage + stage * C::kItemBytes;
+                const int ids = kind == 0 ? ids_cur : ids_prev;
+                const int t0 = kind == 0 ? tt * kPfStep + rank * kPfTile : tt * kPfStep;
+                const int span = kind == 0 ? kPfTile : kPfStep;
+                const int ntok = max(0, min(span, kv - t0));
+                const int nbox = (ntok + BT - 1) >> bsh;
+                const int lane0 = kind == 0 ? (rank * kPfTile) >> bsh : 0;
+                if (lane == 0) // an empty K tile (past kv) completes with no bytes
+                    mbar_arrive_expect_tx(&bars.full[stage], (uint32_t)nbox * (kind == 0 ? kbox : vbox));
+                for (int bx = 0; bx < nbox; ++bx) {
+                    const int page = __shfl_sync(0xffffffffu, ids, lane0 + bx);
+                    if (lane != 0)
+                        continue;
+                    const int slot = (t0 + (bx << bsh)) & (P - 1);
+                    const int c3 = nhd ? (page * P + slot) >> 3 : slot >> 3;
+                    const int c4 = nhd ? g : page * Hkv + g;
+                    if (kind == 0)
+                        tma_load_5d_local(dst + bx * kbox, &maps.k, 0, c3, c4, &bars.full[stage]);
+                    else
+                        tma_load_5d_local(dst + bx * vbox, &maps.v, rank * (D / 128), c3, c4, &bars.full[stage]);
+                }
+                issued = itg + 1;
+            }
+            ids_prev = ids_cur;
+            ids_cur = ids_next;
+            ids_next = page_ids(t + 2);
+        }
+        ib += 2 * ns;
+    }
+    // Copies still in flight, and the pair MMAs still reading the last stages.
+    for (int itg = issued > C::kStages ? issued - C::kStages : 0; itg < issued; ++itg) {
+        pf_wait<true>(&bars.full[itg % C::kStages], (itg / C::kStages) & 1, bars, p.err_flag);
+        pf_wait<true>(&bars.empty[itg % C::kStages], (itg / C::kStages) & 1, bars, p.err_flag);
+    }
+}
+
+// The odd CTA's MMA warp (one thread): tells the even CTA's MMA thread, item
+// by item, that this CTA's part of the stage has landed.
+template <int D>
+__device__ void pf2_relay(const PfParams &p, Pf2Bars &bars, int n_units)
+{
+    using C = Pf2Cfg<D>;
+    int items = 0;
+    for (int k = 0;; ++k) {
+        const int u = pf_unit_at(k, p.cluster);
+        if (u >= n_units)
+            break;
+        items += 2 * ((p.units[u / p.num_kv_heads].n_tiles + 1) >> 1);
+    }
+    for (int itg = 0; itg < items; ++itg) {
+        if (!pf_wait<true>(&bars.full[itg % C::kStages], (itg / C::kStages) & 1, bars, p.err_flag))
+            return;
+        mbar_arrive_remote(&bars.peer_full[itg % C::kStages], 0);
+    }
+}
+
+// The even CTA's MMA thread: per step, S = Q K^T (M = 256, N = 128, Q from
+// both CTAs' shared memory) into S buffer (step & 1), then O += P V for the
+// previous step (P from both CTAs' TMEM as hi and lo parts).  A stage is read
+// once both CTAs' parts have landed; every completion goes to both CTAs.
+template <int D>
+__device__ void pf2_mma(const PfParams &p, uint8_t *smem, Pf2Bars &bars, uint32_t tmem, int n_units)
+{
+    using C = Pf2Cfg<D>;
+    constexpr uint32_t kIdescS = tc_idesc_bf16(2 * kPfRows, kPfStep, false, false);
+    constexpr uint32_t kIdescO = tc_idesc_bf16(2 * kPfRows, D, false, true);
+    constexpr uint16_t kBoth = 3;
+    const uint32_t st_base = smem_addr(smem + C::kOffStage);
+    const uint64_t qd = tc_sw128_desc(smem_addr(smem + C::kOffQ), 16, C::kGroupStride);
+    int ib = 0, gs0 = 0;
+    uint32_t uc = 0;
+    bool issued = false;
+    auto stage_ready = [&](int itg) {
+        const int stage = itg % C::kStages;
+        const uint32_t par = (itg / C::kStages) & 1;
+        return pf_wait<true>(&bars.full[stage], par, bars, p.err_flag) &&
+               pf_wait<true>(&bars.peer_full[stage], par, bars, p.err_flag);
+    };
+    for (int k = 0;; ++k) {
+        const int u = pf_unit_at(k, p.cluster);
+        if (u >= n_units)
+            break;
+        const int ns = (p.units[u / p.num_kv_heads].n_tiles + 1) >> 1;
+        if (!pf_wait<true>(&bars.q_full, uc & 1, bars, p.err_flag))
+            goto done;
+        for (int t = 0; t <= ns; ++t) {
+            if (t < ns) { // S[gs & 1] = Q K_t^T
+                const int gs = gs0 + t;
+                const int itg = ib + pf_item_k(t);
+                const int stage = itg % C::kStages;
+                if (!stage_ready(itg))
+                    goto done;
+                tc_fence_after();
+                issued = true;
+                const uint32_t d = tmem + C::kColS + (uint32_t)(gs & 1) * kPfStep;
+                const uint64_t kd = tc_sw128_desc(st_base + stage * C::kItemBytes, 16, C::kGroupStride);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint64_t off = (uint64_t)(((kk >> 2) * 1024 + (kk & 3) * 32) >> 4);
+                    tc_mma_bf16_ss_pair(d, qd + off, kd + off, kIdescS, kk > 0 ? 1u : 0u);
+                }
+                tc_commit_pair_mc(&bars.s_full[gs & 1], kBoth);
+                tc_commit_pair_mc(&bars.empty[stage], kBoth);
+                if (t == ns - 1)
+                    tc_commit_pair_mc(&bars.q_empty, kBoth);
+            }
+            if (t >= 1) { // O += P_{t-1} V_{t-1}
+                const int tv = t - 1, gs = gs0 + tv;
+                if (!pf_wait<true>(&bars.p_full[gs & 1], (gs >> 1) & 1, bars, p.err_flag))
+                    goto done;
+                if (tv == 0 && uc > 0 && !pf_wait<true>(&bars.o_free, (uc - 1) & 1, bars, p.err_flag))
+                    goto done;
+                const int itg = ib + pf_item_v(tv, ns);
+                const int stage = itg % C::kStages;
+                if (!stage_ready(itg))
+                    goto done;
+                tc_fence_after();
+                const uint32_t pt = tmem + C::kColS + (uint32_t)(gs & 1) * kPfStep; // P of step gs
+                const uint64_t vd = tc_sw128_desc(st_base + stage * C::kItemBytes, 1024, C::kVGroupStride);
+#pragma unroll
+                for (int kk = 0; kk < 2 * (kPfStep / 16); ++kk) { // hi part, then lo part
+                    const int k8 = kk & (kPfStep / 16 - 1);      // 16-key step: keys 16 k8 .. +15
+                    // P layout (see pf2_softmax): key 16 k8 is in thread half k8 >> 2, chunk (k8 >> 1) & 1
+                    const uint32_t a = pt + 64 * (k8 >> 2) + 32 * ((k8 >> 1) & 1) + 8 * (k8 & 1) + 16 * (kk >> 3);
+                    tc_mma_bf16_ts_pair(tmem + C::kColO, a, vd + (uint64_t)((2 * k8 * C::kVGroupStride) >> 4),
+                                        kIdescO, (tv > 0 || kk > 0) ? 1u : 0u);
+                }
+                tc_commit_pair_mc(&bars.o_done[gs & 1], kBoth);
+                tc_commit_pair_mc(&bars.empty[stage], kBoth);
+            }
+        }
+        gs0 += ns;
+        ib += 2 * ns;
+        ++uc;
+    }
+done:
+    if (issued) {
+        tc_commit_pair(&bars.drain);
+        mbar_wait(&bars.drain, 0);
+    }
+}
+
+// Writes this thread's half of its row of a unit's Q tile into the shared
+// memory Q operand (K-major, 128-byte swizzled, the layout a TMA box of
+// 8-row groups writes): row r = query r / G, head r % G; rows past total_q 0.
+template <int D>
+__device__ __forceinline__ void pf2_load_q(const PfParams &p, const PfUnit &un, int g, int r, int half, uint8_t *q_smem,
+                                           int rank)
+{
+    using C = Pf2Cfg<D>;
+    const int tok = un.q_start + (un.t * p.cluster + rank) * p.q_tile + (r >> p.group_shift);
+    const int head = g * (1 << p.group_shift) + (r & ((1 << p.group_shift) - 1));
+    const bool in = tok < p.total_q;
+    const uint4 *src =
+        reinterpret_cast<const uint4 *>(p.q + ((int64_t)(in ? tok : 0) * p.num_q_heads + head) * D + half * (D / 2));
+    constexpr int kLoads = D / 16; // 16-byte chunks of half a row
+    uint4 v[kLoads];
+#pragma unroll
+    for (int i = 0; i < kLoads; ++i)
+        v[i] = in ? __ldg(src + i) : make_uint4(0u, 0u, 0u, 0u);
+    uint8_t *row = q_smem + (r >> 3) * C::kGroupStride + (r & 7) * 128;
+#pragma unroll
+    for (int i = 0; i < kLoads; ++i) {
+        const int c = half * kLoads + i; // chunk of the row: block c / 8, 16-byte column c % 8
+        *reinterpret_cast<uint4 *>(row + (c >> 3) * 1024 + (((c & 7) ^ (r & 7)) << 4)) = v[i];
+    }
+}
+
+// Softmax warps of one CTA of a pair, step by step: the same online softmax
+// as pf_softmax over 128-column S buffers.  Thread half h owns S columns
+// [64 h, 64 h + 64) in two 32-column chunks; chunk c's P is written over its
+// own columns, hi parts at 64 h + 32 c .. +15 and lo parts at .. +16 .. +31,
+// so the other half's S columns are never overwritten before they are read.
+template <int D>
+__device__ void pf2_softmax(const PfParams &p, uint8_t *smem, Pf2Bars &bars, uint32_t tmem, int n_units, int warp,
+                            int lane, int rank)
+{
+    using C = Pf2Cfg<D>;
+    constexpr int kChunk = 32;
+    const int quarter = warp & 3;         // TMEM lanes this warp may access
+    const int half = (warp - 2) >> 2;     // which half of the step's columns
+    const int r = quarter * 32 + lane;    // tile row = TMEM lane
+    const int st = half * kPfRows + r;    // index among the softmax threads
+    const uint32_t t_row = tmem + ((uint32_t)(quarter * 32) << 16);
+    float *xchg = reinterpret_cast<float *>(smem + C::kOffXchg);
+    uint8_t *q_smem = smem + C::kOffQ;
+    const int G = 1 << p.group_shift;
+    const int q_in_tile = r >> p.group_shift;
+    const int h_in_group = r & (G - 1);
+    const float qs = p.q_scale;
+    const float qse = qs > 0.f ? qs : 1.f;
+    int ib = 0, gs0 = 0;
+    uint32_t pair_phase = 0;
+
+    int u = pf_unit_at(0, p.cluster);
+    if (u >= n_units)
+        return;
+    {
+        const int grp = u / p.num_kv_heads;
+        pf2_load_q<D>(p, p.units[grp], u - grp * p.num_kv_heads, r, half, q_smem, rank);
+        fence_proxy_async_smem();
+        pf_arrive_mma<true>(&bars.q_full, lane, rank);
+    }
+    for (int k = 0;; ++k) {
+        u = pf_unit_at(k, p.cluster);
+        if (u >= n_units)
+            break;
+        const int grp = u / p.num_kv_heads, g = u - grp * p.num_kv_heads;
+        const PfUnit un = p.units[grp];
+        const int ns = (un.n_tiles + 1) >> 1, kv = un.kv_len;
+        const int t = un.t * p.cluster + rank;
+        const int qi = t * p.q_tile + q_in_tile;
+        const bool valid = qi < un.q_len;
+        const int limit = min(kv - un.q_len + qi, kv - 1);
+        const int limit_min = min(kv - un.q_len + t * p.q_tile, kv - 1);
+        const int u_next = pf_unit_at(k + 1, p.cluster);
+        float m_used = -INFINITY, l = 0.f;
+        for (int j = 0; j < ns; ++j) {
+            const int gs = gs0 + j;
+            if (!pf_wait_all<true>(&bars.s_full[gs & 1], (gs >> 1) & 1, bars, p.err_flag))
+                return;
+            tc_fence_after();
+            const uint32_t s_col = C::kColS + (uint32_t)(gs & 1) * kPfStep + half * (kPfStep / 2);
+            const bool masked = j * kPfStep + kPfStep - 1 > limit_min;
+            // raw scores of chunk c (a non-positive scale applied here, a positive one in the exponent)
+            auto load_chunk = [&](int c, float (&x)[kChunk]) {
+                uint32_t rr[32];
+                tmem_ld32(t_row + s_col + c * kChunk, rr);
+#pragma unroll
+                for (int i = 0; i < kChunk; ++i)
+                    x[i] = __uint_as_float(rr[i]);
+                if (!(qs > 0.f)) {
+#pragma unroll
+                    for (int i = 0; i < kChunk; ++i)
+                        x[i] *= qs;
+                }
+                if (masked) {
+                    const int tok0 = j * kPfStep + half * (kPfStep / 2) + c * kChunk;
+#pragma unroll
+                    for (int i = 0; i < kChunk; ++i)
+                        x[i] = (tok0 + i <= limit) ? x[i] : -INFINITY;
+                }
+            };
+            float mx = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                float x[kChunk];
+                load_chunk(c, x);
+#pragma unroll
+                for (int i = 0; i < kChunk; ++i)
+                    mx = fmaxf(mx, x[i]);
+            }
+            float *xm = xchg + (gs & 1) * (2 * kPfRows);
+            xm[half * kPfRows + r] = mx;
+            if (!pf_pair_sync(bars, quarter, pair_phase, p.err_flag))
+                return;
+            mx = fmaxf(mx, xm[(1 - half) * kPfRows + r]);
+            const float mt = mx * qse;
+            const bool grow = mt > m_used + kRescaleLog2;
+            float alpha = 1.f;
+            if (grow) {
+                alpha = ex2_approx(m_used - mt);
+                l *= alpha;
+                m_used = mt;
+            }
+            const float m_ref = m_used == -INFINITY ? 0.f : m_used;
+            const float2 q2 = make_float2(qse, qse), nm2 = make_float2(-m_ref, -m_ref);
+            float2 sum2 = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                float x[kChunk];
+                load_chunk(c, x);
+                uint32_t whi[kChunk / 2], wlo[kChunk / 2];
+#pragma unroll
+                for (int e = 0; e < kChunk / 2; ++e) {
+                    const float2 a = ffma2(make_float2(x[2 * e], x[2 * e + 1]), q2, nm2);
+                    const float2 pp = make_float2(ex2_approx(a.x), ex2_approx(a.y));
+                    sum2 = __fadd2_rn(sum2, pp);
+                    const __nv_bfloat162 hi = __floats2bfloat162_rn(pp.x, pp.y);
+                    const float2 hf = __bfloat1622float2(hi);
+                    const float2 d = __fadd2_rn(pp, make_float2(-hf.x, -hf.y));
+                    const __nv_bfloat162 lo = __floats2bfloat162_rn(d.x, d.y);
+                    whi[e] = *reinterpret_cast<const uint32_t *>(&hi);
+                    wlo[e] = *reinterpret_cast<const uint32_t *>(&lo);
+                }
+                tmem_st16(t_row + s_col + c * kChunk, whi);
+                tmem_st16(t_row + s_col + c * kChunk + kChunk / 2, wlo);
+            }
+            l += sum2.x + sum2.y;
+            const bool rescale_o = grow && j > 0;
+            if (__any_sync(0xffffffffu, rescale_o)) {
+                const int gp = gs - 1;
+                if (!pf_wait_all<true>(&bars.o_done[gp & 1], (gp >> 1) & 1, bars, p.err_flag))
+                    return;
+                tc_fence_after();
+                const float a = rescale_o ? alpha : 1.f;
+                for (int c = half * (D / 2); c < (half + 1) * (D / 2); c += 32) {
+                    uint32_t rr[32];
+                    tmem_ld32(t_row + C::kColO + c, rr);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        rr[i] = __float_as_uint(__uint_as_float(rr[i]) * a);
+                    tmem_st32(t_row + C::kColO + c, rr);
+                }
+            }
+            // V rows at and past kv in the step hold another token's or no data: zero them
+            if (j * kPfStep + kPfStep > kv) {
+                const int itg = ib + pf_item_v(j, ns);
+                const int stage = itg % C::kStages;
+                if (!pf_wait_all<true>(&bars.full[stage], (itg / C::kStages) & 1, bars, p.err_flag))
+                    return;
+                const int r0 = kv - j * kPfStep;
+                uint8_t *vb = smem + C::kOffStage + stage * C::kItemBytes;
+                for (int i = st; i < (kPfStep - r0) * C::kVChunks * 8; i += kPfSoftmaxThreads) {
+                    const int piece = i & 7, rest = i >> 3;
+                    const int c = rest % C::kVChunks, tt = r0 + rest / C::kVChunks;
+                    *reinterpret_cast<uint4 *>(vb + (tt >> 3) * C::kVGroupStride + c * 1024 + (tt & 7) * 128 +
+                                               piece * 16) = make_uint4(0u, 0u, 0u, 0u);
+                }
+                fence_proxy_async_smem();
+            }
+            tc_fence_before();
+            pf_arrive_mma<true>(&bars.p_full[gs & 1], lane, rank);
+        }
+        // The next unit's Q, once this unit's S MMAs have read the current one.
+        if (u_next < n_units) {
+            if (!pf_wait_all<true>(&bars.q_empty, k & 1, bars, p.err_flag))
+                return;
+            const int pn = u_next / p.num_kv_heads;
+            pf2_load_q<D>(p, p.units[pn], u_next - pn * p.num_kv_heads, r, half, q_smem, rank);
+            fence_proxy_async_smem();
+            pf_arrive_mma<true>(&bars.q_full, lane, rank);
+        }
+        { // epilogue: O / l -> bf16 (this half's columns), lse
+            float *xl = xchg + 4 * kPfRows;
+            xl[half * kPfRows + r] = l;
+            if (!pf_pair_sync(bars, quarter, pair_phase, p.err_flag))
+                return;
+            const float lt = l + xl[(1 - half) * kPfRows + r];
+            if (!pf_pair_sync(bars, quarter, pair_phase, p.err_flag))
+                return;
+            const int gl = gs0 + ns - 1;
+            if (!pf_wait_all<true>(&bars.o_done[gl & 1], (gl >> 1) & 1, bars, p.err_flag))
+                return;
+            tc_fence_after();
+            const float inv = lt > 0.f ? 1.f / lt : 0.f;
+            const int64_t row = (int64_t)(un.q_start + qi) * p.num_q_heads + g * G + h_in_group;
+            __nv_bfloat16 *orow = p.out + row * D;
+            for (int c = half * (D / 2); c < (half + 1) * (D / 2); c += 32) {
+                uint32_t rr[32];
+                tmem_ld32(t_row + C::kColO + c, rr);
+                uint32_t w[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    const __nv_bfloat162 h = __floats2bfloat162_rn(__uint_as_float(rr[2 * e]) * inv,
+                                                                   __uint_as_float(rr[2 * e + 1]) * inv);
+                    w[e] = *reinterpret_cast<const uint32_t *>(&h);
+                }
+                if (valid) {
+                    uint4 *dst = reinterpret_cast<uint4 *>(orow + c);
+                    dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+                    dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+                    dst[2] = make_uint4(w[8], w[9], w[10], w[11]);
+                    dst[3] = make_uint4(w[12], w[13], w[14], w[15]);
+                }
+            }
+            tc_fence_before();
+            pf_arrive_mma<true>(&bars.o_free, lane, rank);
+            if (half == 0 && valid && p.lse != nullptr)
+                p.lse[row] = (m_used + log2f(lt)) * kLn2;
+        }
+        gs0 += ns;
+        ib += 2 * ns;
+    }
+}
+
+template <int D>
+__global__ void __launch_bounds__(kPfThreads, 1)
+    prefill2_kernel(const __grid_constant__ PfParams p, const __grid_constant__ PfMapsDev maps)
+{
+    using C = Pf2Cfg<D>;
+    extern __shared__ unsigned char pf_smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(pf_smem_raw) + 1023) & ~uintptr_t(1023));
+    Pf2Bars &bars = *reinterpret_cast<Pf2Bars *>(smem + C::kOffBar);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int rank = (int)cluster_ctarank(); // clusters are exactly one pair
+    constexpr int kWarpArrivals = 2 * kPfSoftmaxWarps; // per-warp arrivals of both CTAs' softmax warps
+
+    if (threadIdx.x == 0) {
+        mbar_init(&bars.q_full, kWarpArrivals);
+        mbar_init(&bars.q_empty, 1);
+        for (int s = 0; s < C::kStages; ++s) {
+            mbar_init(&bars.full[s], 1);
+            mbar_init(&bars.empty[s], 1);
+            mbar_init(&bars.peer_full[s], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&bars.s_full[i], 1);
+            mbar_init(&bars.p_full[i], kWarpArrivals);
+            mbar_init(&bars.o_done[i], 1);
+        }
+        mbar_init(&bars.o_free, kWarpArrivals);
+        for (int i = 0; i < 4; ++i)
+            mbar_init(&bars.pair[i], 64);
+        mbar_init(&bars.drain, 1);
+        bars.abort = 0;
+        mbar_init_fence();
+    }
+    if (warp == kPfProducerWarp && lane == 0) {
+        prefetch_tensormap(&maps.k);
+        prefetch_tensormap(&maps.v);
+    }
+    if (warp == kPfMmaWarp) { // collective over the pair: both CTAs get the same columns
+        tmem_alloc_pair(&bars.tmem_base, C::kTmemCols);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before();
+    cluster_sync(); // both CTAs' barriers and TMEM are ready before anything crosses over
+    tc_fence_after();
+    const uint32_t tmem = bars.tmem_base;
+    const int n_units = *p.n_pairs * p.num_kv_heads;
+
+    if (warp == kPfProducerWarp)
+        pf2_producer<D>(p, maps, smem, bars, n_units, lane, rank);
+    else if (warp == kPfMmaWarp) {
+        if (lane == 0) {
+            if (rank == 0)
+                pf2_mma<D>(p, smem, bars, tmem, n_units);
+            else
+                pf2_relay<D>(p, bars, n_units);
+        }
+        __syncwarp();
+    } else
+        pf2_softmax<D>(p, smem, bars, tmem, n_units, warp, lane, rank);
+
+    tc_fence_before();
+    cluster_sync(); // the pair's last MMAs (on both CTAs' smem and TMEM) are complete
+    tc_fence_after();
+    if (warp == kPfMmaWarp)
+        tmem_dealloc_pair(tmem, C::kTmemCols);
 }
 
 // ---------------------------------------------------------------- plan
@@ -918,14 +1491,17 @@ __global__ void __launch_bounds__(kPlanThreads) prefill_plan_kernel(const PfPlan
 
 struct PfKernelEntry {
     int D;
+    bool pair; // CTA-pair kernel (cta_group::2): half-tile TMA maps
     const void *fn;
     uint32_t smem;
 };
 
+// head_dim 64 cannot be split into 64-column halves: one CTA per query tile,
+// K / V shared by the cluster through TMA multicast.  128 and 256: CTA pairs.
 const PfKernelEntry kPfTable[] = {
-    {64, reinterpret_cast<const void *>(&prefill_kernel<64>), PfCfg<64>::kSmem},
-    {128, reinterpret_cast<const void *>(&prefill_kernel<128>), PfCfg<128>::kSmem},
-    {256, reinterpret_cast<const void *>(&prefill_kernel<256>), PfCfg<256>::kSmem},
+    {64, false, reinterpret_cast<const void *>(&prefill_kernel<64>), PfCfg<64>::kSmem},
+    {128, true, reinterpret_cast<const void *>(&prefill2_kernel<128>), Pf2Cfg<128>::kSmem},
+    {256, true, reinterpret_cast<const void *>(&prefill2_kernel<256>), Pf2Cfg<256>::kSmem},
 };
 
 const PfKernelEntry *pf_find(int D)
@@ -1088,6 +1664,21 @@ cudaError_t launch_prefill(const PrefillArgs &a, const PrefillMaps &maps, cudaSt
 int prefill_box_tokens(int page_size)
 {
     return page_size < kPfTile ? page_size : kPfTile;
+}
+
+bool encode_prefill_maps(const pkv_cache_desc &d, const void *k_cache, const void *v_cache, PrefillMaps *maps)
+{
+    const PfKernelEntry *e = pf_find(d.head_dim);
+    if (e == nullptr)
+        return false;
+    void *k = const_cast<void *>(k_cache), *v = const_cast<void *>(v_cache);
+    const int box = prefill_box_tokens(d.page_size);
+    if (!e->pair)
+        return encode_group_map(&maps->k, d, k, box) == CUDA_SUCCESS &&
+               encode_group_map(&maps->v, d, v, box) == CUDA_SUCCESS;
+    // K: min(P, 64) keys with all of head_dim; V: min(P, 64) keys with half of head_dim
+    return encode_group_map(&maps->k, d, k, box) == CUDA_SUCCESS &&
+           encode_group_map(&maps->v, d, v, box, d.head_dim / 128) == CUDA_SUCCESS;
 }
 
 } // namespace pkv

@@ -248,6 +248,101 @@ __device__ __forceinline__ void tma_load_5d_mc(void *dst, const CUtensorMap *map
                  : "memory");
 }
 
+// --- CTA pairs (cta_group::2) ---------------------------------------------
+// A pair is CTA ranks 2i and 2i+1 of a cluster.  One thread of the even CTA
+// issues MMAs with M = 256: rows 0..127 of A and D live in the even CTA
+// (its smem / TMEM), rows 128..255 in the odd one at the same addresses, and
+// B is split along N -- columns 0..N/2-1 come from the even CTA's smem, the
+// rest from the odd CTA's, through the same descriptor.  Every tcgen05
+// allocation, MMA and commit of a kernel that pairs CTAs uses cta_group::2.
+
+// Collective over the pair: one warp of each CTA executes it; both receive
+// the same TMEM base address.
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t *dst_smem, uint32_t ncols)
+{
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(dst_smem)),
+                 "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish_pair()
+{
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols)
+{
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+// D (+)= A[tmem] * B[smem] over the pair (M = 256).
+__device__ __forceinline__ void tc_mma_bf16_ts_pair(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                                    uint32_t accumulate)
+{
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "setp.ne.b32 p, %4, 0;\n\t"
+                 "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+                 "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+                 : "memory");
+}
+// D (+)= A[smem] * B[smem] over the pair (M = 256; A rows 0..127 from the
+// even CTA's smem, 128..255 from the odd CTA's, through the same descriptor).
+__device__ __forceinline__ void tc_mma_bf16_ss_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                                    uint32_t accumulate)
+{
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "setp.ne.b32 p, %4, 0;\n\t"
+                 "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+                 "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+                 : "memory");
+}
+// Arrives once on the barrier at the same offset in every CTA of `cta_mask`
+// when the pair MMAs this thread issued before have completed.
+__device__ __forceinline__ void tc_commit_pair_mc(uint64_t *bar, uint16_t cta_mask)
+{
+    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::
+                     "r"(smem_addr(bar)),
+                 "h"(cta_mask)
+                 : "memory");
+}
+// The same on this CTA's barrier only.
+__device__ __forceinline__ void tc_commit_pair(uint64_t *bar)
+{
+    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_addr(bar))
+                 : "memory");
+}
+// Arrives on the barrier at the address of `bar` in CTA `rank` of the
+// cluster (default semantics: release, the barrier's CTA scope).  Writes the
+// barrier's waiter reads through tcgen05 (TMEM, or shared memory an MMA
+// reads) are ordered by the tcgen05 / proxy fences before the call.
+__device__ __forceinline__ void mbar_arrive_remote(uint64_t *bar, uint32_t rank)
+{
+    asm volatile("{\n\t.reg .b32 ra;\n\t"
+                 "mapa.shared::cluster.u32 ra, %0, %1;\n\t"
+                 "mbarrier.arrive.shared::cluster.b64 _, [ra];\n\t}" ::"r"(smem_addr(bar)),
+                 "r"(rank)
+                 : "memory");
+}
+// try_wait with acquire at cluster scope: for barriers other CTAs arrive on.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t *bar, uint32_t parity)
+{
+    uint32_t done;
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(done)
+                 : "r"(smem_addr(bar)), "r"(parity)
+                 : "memory");
+    return done != 0;
+}
+// 5-D tiled TMA load into this CTA's shared memory (default L2 policy); c2
+// selects the first 64-column block.
+__device__ __forceinline__ void tma_load_5d_local(void *dst, const CUtensorMap *map, int c2, int c3, int c4,
+                                                  uint64_t *bar)
+{
+    asm volatile("cp.async.bulk.tensor.5d.shared::cluster.global.mbarrier::complete_tx::bytes"
+                 " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(smem_addr(dst)),
+                 "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(0), "r"(c2), "r"(c3), "r"(c4), "r"(smem_addr(bar))
+                 : "memory");
+}
+
 __device__ __forceinline__ float ex2_approx(float x)
 {
     float y;
