@@ -53,6 +53,11 @@ SHAPES = [
     (256, 16, 1, 128, wl.NHD, [40, 9], [1000, 9]),                    # G 16: 8 queries per tile
     (64, 8, 1, 256, wl.NHD, [100], [600]),                            # page 256
     (128, 8, 2, 32, wl.HND, [64, 128, 63, 16], [64, 300, 127, 16]),   # tile-boundary lengths
+    # CTA-pair kernel edges: page 8 boxes, page 256, key counts whose last
+    # 128-key step leaves the odd CTA's K tile empty (kv % 128 in 1..64) or partial
+    (256, 16, 2, 8, wl.NHD, [70, 33], [193, 33]),
+    (128, 32, 8, 256, wl.HND, [100, 7], [640, 65]),
+    (128, 32, 4, 16, wl.NHD, [129, 256, 1], [129, 320, 129]),
 ]
 
 
