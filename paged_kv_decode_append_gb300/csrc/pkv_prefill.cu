@@ -493,8 +493,8 @@ __device__ __forceinline__ bool pf_pair_sync(Bars &bars, int quarter, uint32_t &
 
 // A softmax thread's arrival on a barrier the MMA thread waits on: every
 // thread arrives (one CTA), or -- CTA pairs -- each warp arrives once on the
-// barrier of the pair's even CTA (rank 0), whose MMA thread issues for both:
-// locally there, remotely from the odd CTA.  The thread's tcgen05 /
+// barrier of its pair's even CTA (rank & ~1), whose MMA thread issues for
+// both: locally there, remotely from the odd CTA.  The thread's tcgen05 /
 // shared-memory writes are fenced before the call.
 template <bool PAIR>
 __device__ __forceinline__ void pf_arrive_mma(uint64_t *bar, int lane, int rank)
@@ -502,10 +502,10 @@ __device__ __forceinline__ void pf_arrive_mma(uint64_t *bar, int lane, int rank)
     if constexpr (PAIR) {
         __syncwarp();
         if (lane == 0) {
-            if (rank == 0)
+            if ((rank & 1) == 0)
                 mbar_arrive(bar);
             else
-                mbar_arrive_remote(bar, 0);
+                mbar_arrive_remote(bar, (uint32_t)(rank & ~1));
         }
     } else {
         mbar_arrive(bar);
@@ -786,12 +786,16 @@ __global__ void __launch_bounds__(kPfThreads, 1)
 // ---------------------------------------------------------------- CTA pairs
 
 // Producer of one CTA of a pair, step by step (128 keys): item K_t is the
-// step's tile 2t + r (r = this CTA's rank), 64 keys with all of head_dim;
-// item V_t is all 128 keys of the step with columns [r D/2, (r+1) D/2).
-// Boxes of min(page, 64) tokens; items in the MMA's consumption order (K_0,
-// K_1, V_0, K_2, V_1, ...), each into this CTA's shared memory and onto its
-// own full barrier; a stage is refilled once the pair's MMA that read it has
-// completed.
+// step's tile 2t + r (r = the CTA's rank in its pair), 64 keys with all of
+// head_dim; item V_t is all 128 keys of the step with columns
+// [r D/2, (r+1) D/2).  Boxes of min(page, 64) tokens; items in the MMA's
+// consumption order (K_0, K_1, V_0, K_2, V_1, ...).  With clusters of two
+// pairs on consecutive query tiles of the same (request, kv head), CTA c and
+// CTA c ^ 2 need the same items, so each loads half of every item's boxes
+// with TMA multicast into both (the same shared-memory offset, completing on
+// both full barriers) -- half the TMA issues per SM, which pays where the
+// boxes are small (head_dim 128).  A stage is refilled once every pair's MMA
+// that read it has completed.
 template <int D>
 __device__ void pf2_producer(const PfParams &p, const PfMapsDev &maps, uint8_t *smem, Pf2Bars &bars, int n_units,
                              int lane, int rank)
@@ -803,6 +807,10 @@ __device__ void pf2_producer(const PfParams &p, const PfMapsDev &maps, uint8_t *
     const int BT = 1 << bsh;
     const uint32_t kbox = (uint32_t)BT * D * 2, vbox = (uint32_t)BT * (D / 2) * 2;
     const bool nhd = p.layout == PKV_NHD;
+    const int r2 = rank & 1;                                   // rank in the pair
+    const bool twin = p.cluster == 4;                          // a second pair shares every item
+    const uint16_t mc = (uint16_t)((1u << rank) | (1u << (rank ^ 2))); // this CTA and its twin in the other pair
+    const int share = rank >> 1;                              // which half of each item's boxes this CTA issues
     int ib = 0, issued = 0;
     bool ok = true;
     for (int k = 0; ok; ++k) {
@@ -836,24 +844,27 @@ __device__ void pf2_producer(const PfParams &p, const PfMapsDev &maps, uint8_t *
                 }
                 uint8_t *dst = smem + C::kOffStage + stage * C::kItemBytes;
                 const int ids = kind == 0 ? ids_cur : ids_prev;
-                const int t0 = kind == 0 ? tt * kPfStep + rank * kPfTile : tt * kPfStep;
+                const int t0 = kind == 0 ? tt * kPfStep + r2 * kPfTile : tt * kPfStep;
                 const int span = kind == 0 ? kPfTile : kPfStep;
                 const int ntok = max(0, min(span, kv - t0));
                 const int nbox = (ntok + BT - 1) >> bsh;
-                const int lane0 = kind == 0 ? (rank * kPfTile) >> bsh : 0;
-                if (lane == 0) // an empty K tile (past kv) completes with no bytes
+                const int lane0 = kind == 0 ? (r2 * kPfTile) >> bsh : 0;
+                if (lane == 0) // the whole item, whichever CTA issues each box; an empty K tile completes with none
                     mbar_arrive_expect_tx(&bars.full[stage], (uint32_t)nbox * (kind == 0 ? kbox : vbox));
                 for (int bx = 0; bx < nbox; ++bx) {
                     const int page = __shfl_sync(0xffffffffu, ids, lane0 + bx);
-                    if (lane != 0)
+                    if (lane != 0 || (twin && (bx & 1) != share))
                         continue;
                     const int slot = (t0 + (bx << bsh)) & (P - 1);
                     const int c3 = nhd ? (page * P + slot) >> 3 : slot >> 3;
                     const int c4 = nhd ? g : page * Hkv + g;
-                    if (kind == 0)
-                        tma_load_5d_local(dst + bx * kbox, &maps.k, 0, c3, c4, &bars.full[stage]);
+                    uint8_t *bdst = dst + bx * (kind == 0 ? kbox : vbox);
+                    const CUtensorMap *map = kind == 0 ? &maps.k : &maps.v;
+                    const int c2 = kind == 0 ? 0 : r2 * (D / 128);
+                    if (twin)
+                        tma_load_5d_mc(bdst, map, 0, 0, c2, c3, c4, &bars.full[stage], mc);
                     else
-                        tma_load_5d_local(dst + bx * vbox, &maps.v, rank * (D / 128), c3, c4, &bars.full[stage]);
+                        tma_load_5d_local(bdst, map, c2, c3, c4, &bars.full[stage]);
                 }
                 issued = itg + 1;
             }
@@ -886,7 +897,7 @@ __device__ void pf2_relay(const PfParams &p, Pf2Bars &bars, int n_units)
     for (int itg = 0; itg < items; ++itg) {
         if (!pf_wait<true>(&bars.full[itg % C::kStages], (itg / C::kStages) & 1, bars, p.err_flag))
             return;
-        mbar_arrive_remote(&bars.peer_full[itg % C::kStages], 0);
+        mbar_arrive_remote(&bars.peer_full[itg % C::kStages], (uint32_t)(cluster_ctarank() & ~1u));
     }
 }
 
@@ -900,7 +911,8 @@ __device__ void pf2_mma(const PfParams &p, uint8_t *smem, Pf2Bars &bars, uint32_
     using C = Pf2Cfg<D>;
     constexpr uint32_t kIdescS = tc_idesc_bf16(2 * kPfRows, kPfStep, false, false);
     constexpr uint32_t kIdescO = tc_idesc_bf16(2 * kPfRows, D, false, true);
-    constexpr uint16_t kBoth = 3;
+    const uint16_t kBoth = (uint16_t)(3u << (cluster_ctarank() & ~1u)); // this pair
+    const uint16_t kAll = (uint16_t)((1u << p.cluster) - 1u); // every CTA a stage's loads reach
     const uint32_t st_base = smem_addr(smem + C::kOffStage);
     const uint64_t qd = tc_sw128_desc(smem_addr(smem + C::kOffQ), 16, C::kGroupStride);
     int ib = 0, gs0 = 0;
@@ -936,7 +948,7 @@ __device__ void pf2_mma(const PfParams &p, uint8_t *smem, Pf2Bars &bars, uint32_
                     tc_mma_bf16_ss_pair(d, qd + off, kd + off, kIdescS, kk > 0 ? 1u : 0u);
                 }
                 tc_commit_pair_mc(&bars.s_full[gs & 1], kBoth);
-                tc_commit_pair_mc(&bars.empty[stage], kBoth);
+                tc_commit_pair_mc(&bars.empty[stage], kAll);
                 if (t == ns - 1)
                     tc_commit_pair_mc(&bars.q_empty, kBoth);
             }
@@ -962,7 +974,7 @@ __device__ void pf2_mma(const PfParams &p, uint8_t *smem, Pf2Bars &bars, uint32_
                                         kIdescO, (tv > 0 || kk > 0) ? 1u : 0u);
                 }
                 tc_commit_pair_mc(&bars.o_done[gs & 1], kBoth);
-                tc_commit_pair_mc(&bars.empty[stage], kBoth);
+                tc_commit_pair_mc(&bars.empty[stage], kAll);
             }
         }
         gs0 += ns;
@@ -1219,7 +1231,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(pf_smem_raw) + 1023) & ~uintptr_t(1023));
     Pf2Bars &bars = *reinterpret_cast<Pf2Bars *>(smem + C::kOffBar);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int rank = (int)cluster_ctarank(); // clusters are exactly one pair
+    const int rank = (int)cluster_ctarank(); // pairs are CTAs 0-1 (and 2-3)
     constexpr int kWarpArrivals = 2 * kPfSoftmaxWarps; // per-warp arrivals of both CTAs' softmax warps
 
     if (threadIdx.x == 0) {
@@ -1227,7 +1239,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         mbar_init(&bars.q_empty, 1);
         for (int s = 0; s < C::kStages; ++s) {
             mbar_init(&bars.full[s], 1);
-            mbar_init(&bars.empty[s], 1);
+            mbar_init(&bars.empty[s], p.cluster / 2); // the MMA thread of every pair
             mbar_init(&bars.peer_full[s], 1);
         }
         for (int i = 0; i < 2; ++i) {
@@ -1260,7 +1272,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         pf2_producer<D>(p, maps, smem, bars, n_units, lane, rank);
     else if (warp == kPfMmaWarp) {
         if (lane == 0) {
-            if (rank == 0)
+            if ((rank & 1) == 0)
                 pf2_mma<D>(p, smem, bars, tmem, n_units);
             else
                 pf2_relay<D>(p, bars, n_units);
@@ -1491,7 +1503,8 @@ __global__ void __launch_bounds__(kPlanThreads) prefill_plan_kernel(const PfPlan
 
 struct PfKernelEntry {
     int D;
-    bool pair; // CTA-pair kernel (cta_group::2): half-tile TMA maps
+    bool pair;   // CTA-pair kernel (cta_group::2): half-tile TMA maps
+    int cluster; // CTAs per cluster (one query tile each)
     const void *fn;
     uint32_t smem;
 };
@@ -1499,9 +1512,9 @@ struct PfKernelEntry {
 // head_dim 64 cannot be split into 64-column halves: one CTA per query tile,
 // K / V shared by the cluster through TMA multicast.  128 and 256: CTA pairs.
 const PfKernelEntry kPfTable[] = {
-    {64, false, reinterpret_cast<const void *>(&prefill_kernel<64>), PfCfg<64>::kSmem},
-    {128, true, reinterpret_cast<const void *>(&prefill2_kernel<128>), Pf2Cfg<128>::kSmem},
-    {256, true, reinterpret_cast<const void *>(&prefill2_kernel<256>), Pf2Cfg<256>::kSmem},
+    {64, false, 2, reinterpret_cast<const void *>(&prefill_kernel<64>), PfCfg<64>::kSmem},
+    {128, true, 4, reinterpret_cast<const void *>(&prefill2_kernel<128>), Pf2Cfg<128>::kSmem},
+    {256, true, 2, reinterpret_cast<const void *>(&prefill2_kernel<256>), Pf2Cfg<256>::kSmem},
 };
 
 const PfKernelEntry *pf_find(int D)
@@ -1511,9 +1524,6 @@ const PfKernelEntry *pf_find(int D)
             return &e;
     return nullptr;
 }
-
-// CTAs per cluster that share each K / V tile load (TMA multicast).
-constexpr int kPfCluster = 2;
 
 // Persistent grid size for clusters of `cl` CTAs: every cluster that can be
 // resident at once, in CTAs (set up once per device).
@@ -1604,7 +1614,7 @@ cudaError_t launch_prefill(const PrefillArgs &a, const PrefillMaps &maps, cudaSt
     pp.q_tile = a.shape.q_tile;
     pp.num_q_heads = a.num_q_heads;
     pp.head_dim = a.desc.head_dim;
-    pp.cluster = kPfCluster;
+    pp.cluster = e->cluster;
     pp.cap_pairs = a.shape.cap_pairs;
     prefill_plan_kernel<<<1, kPlanThreads, 0, stream>>>(pp);
     cudaError_t err = cudaGetLastError();
@@ -1628,7 +1638,7 @@ cudaError_t launch_prefill(const PrefillArgs &a, const PrefillMaps &maps, cudaSt
     p.page_shift = page_shift;
     p.box_shift = page_shift < 6 ? page_shift : 6;
     p.layout = a.desc.layout;
-    p.cluster = kPfCluster;
+    p.cluster = e->cluster;
     p.q_scale = a.q_scale;
     PfMapsDev m;
     m.k = maps.k;
@@ -1637,7 +1647,7 @@ cudaError_t launch_prefill(const PrefillArgs &a, const PrefillMaps &maps, cudaSt
     int dev = 0;
     if ((err = cudaGetDevice(&dev)) != cudaSuccess)
         return err;
-    const int cl = kPfCluster;
+    const int cl = e->cluster;
     int grid = pf_grid(dev, e, cl);
     const int64_t max_ctas = a.shape.cap_pairs * a.desc.num_kv_heads * cl; // one unit per cluster at least
     if (grid > max_ctas)
