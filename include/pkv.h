@@ -362,7 +362,7 @@ PKV_API size_t pkv_mixed_workspace_size(int32_t batch, int32_t total_q, int32_t 
  *  max_qlen          longest q_b accepted (>= 1): a longer row appends
  *                    nothing and gets PKV_ERR_QLEN with out = 0, lse = -inf.
  *  decode_max_qlen   rows with 1 <= q_b <= decode_max_qlen run on the
- *                    split-KV decode kernel (every K/V tile serves up to 8
+ *                    split-KV decode kernel (every K/V tile serves up to 16
  *                    (query, head) pairs of a kv head); longer rows on the
  *                    tensor-core prefill kernel, which needs page_size >= 8
  *                    (PKV_EUNSUPPORTED if max_qlen > decode_max_qlen with

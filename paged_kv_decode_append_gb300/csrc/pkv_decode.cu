@@ -44,7 +44,11 @@
 // paged attention cuDNN auto-dispatch", code analysis part 1).  A unit's
 // columns are then (query, head) pairs, query-major, GC of them per unit:
 // every K/V tile read serves all of a kv head's heads for GC / G queries, and
-// the tiles past kv - q + 1 mask each column at its own limit.
+// the tiles past kv - q + 1 mask each column at its own limit.  Up to 16
+// columns share one pass over the K/V tiles: a unit of more than 8 columns
+// gives each consumer warp 8 of them over all 32 rows of a tile (one MMA
+// n-tile each); both epilogue warps then finish it, 8 columns each, with a
+// combine ticket per half.
 #include <math.h>
 
 #include "pkv_device.cuh"
@@ -109,15 +113,25 @@ constexpr int stages_for()
     return D == 256 ? 3 : (D == 128 ? (GC <= 4 ? 5 : 4) : 6);
 }
 
+// Columns of one consumer warp's softmax state: a unit of up to 8 columns
+// splits its tile rows between the two warps (each holds every column); a
+// multi-query unit of 16 splits its columns (each warp 8 of them, all rows).
+template <int GC>
+constexpr int warp_cols()
+{
+    return GC > 8 ? 8 : GC;
+}
+
 template <int D, int GC, bool MQ>
 struct Smem {
     static constexpr int kStages = stages_for<D, GC>();
+    static constexpr int RC = warp_cols<GC>();
     // [stage][K|V] tiles laid out [kTile/8][D/64][8][64]: 8-token groups of
     // 128-byte rows (TMA SWIZZLE_128B when the page size allows 8-row boxes)
     __nv_bfloat16 kv[kStages][2][kTile * D];
     // per-warp softmax states of a finished slice: o (unnormalised), m, l
-    float red_o[kSlots][kWarps][GC][D];
-    float red_m[kSlots][kWarps][GC], red_l[kSlots][kWarps][GC];
+    float red_o[kSlots][kWarps][RC][D];
+    float red_m[kSlots][kWarps][RC], red_l[kSlots][kWarps][RC];
     int32_t red_bad[kSlots][kWarps];
     uint64_t full[kStages], empty[kStages];
     uint64_t epi_full[kSlots], epi_empty[kSlots];
@@ -804,6 +818,115 @@ __device__ __forceinline__ void consume_tile(const __nv_bfloat16 *Kt, __nv_bfloa
     }
 }
 
+// A 16-column unit's tile for one consumer warp: its 8 columns over all 32
+// token rows, as two 16-row halves that share one online-softmax update.
+// MASKED as in consume_tile; both warps zero the masked V rows they read
+// (the same zeros, written before either warp's own reads).
+template <int D, bool MASKED>
+__device__ __forceinline__ void consume_tile_wide(const __nv_bfloat16 *Kt, __nv_bfloat16 *Vt, int nv, int lim0,
+                                                  int lim1, int lane, int swz, float scale,
+                                                  const uint32_t (&qf)[D / 16][2], float (&acc)[D / 16][4],
+                                                  float (&m_run)[2], float (&l_run)[2])
+{
+    constexpr int KS = D / 16;
+    const int g = lane >> 2;
+    const uint32_t kbase = smem_addr(Kt), vbase = smem_addr(Vt);
+    if (MASKED && nv < kTile) {
+        for (int i = lane; i < (kTile - nv) * (D / 8); i += 32) {
+            const int r = nv + i / (D / 8), chunk = i % (D / 8);
+            *reinterpret_cast<uint4 *>(Vt + (((r >> 3) * (D / 64) + (chunk >> 3)) * 8 + (r & 7)) * 64 +
+                                       (chunk & 7) * 8) = make_uint4(0u, 0u, 0u, 0u);
+        }
+        __syncwarp();
+    }
+    // ---- S^T = K Q^T for rows 16h .. 16h + 15
+    float v[2][4];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+        const int krow = 16 * h + (lane & 15);
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+            uint32_t a[4];
+            ldsm_x4(tile_addr<D>(kbase, krow, 2 * ks + (lane >> 4), swz), a);
+            if (ks & 1)
+                mma_16816(sb, a, qf[ks][0], qf[ks][1]);
+            else
+                mma_16816(sa, a, qf[ks][0], qf[ks][1]);
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            v[h][i] = (sa[i] + sb[i]) * scale;
+        if constexpr (MASKED) {
+            const int e0 = min(nv, lim0), e1 = min(nv, lim1), r = 16 * h + g;
+            if (r >= e0)
+                v[h][0] = kNegInf;
+            if (r >= e1)
+                v[h][1] = kNegInf;
+            if (r + 8 >= e0)
+                v[h][2] = kNegInf;
+            if (r + 8 >= e1)
+                v[h][3] = kNegInf;
+        }
+    }
+    // ---- online softmax per column over both halves
+    float m_new[2];
+    bool grow = false;
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+        float mt = fmaxf(fmaxf(v[0][j], v[0][2 + j]), fmaxf(v[1][j], v[1][2 + j]));
+        mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 4));
+        mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 8));
+        mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 16));
+        m_new[j] = fmaxf(m_run[j], mt);
+        grow |= m_new[j] > m_run[j];
+    }
+    if (__any_sync(0xffffffffu, grow)) {
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const float a = m_new[j] == kNegInf ? 1.f : ex2(m_run[j] - m_new[j]);
+            l_run[j] *= a;
+#pragma unroll
+            for (int mt = 0; mt < KS; ++mt) {
+                acc[mt][j] *= a;
+                acc[mt][2 + j] *= a;
+            }
+            m_run[j] = m_new[j];
+        }
+    }
+    uint32_t bh[2][2], bl[2][2]; // P^T B fragments of each half: high and low bf16 parts
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        float pr[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float m = m_run[i & 1];
+            pr[i] = ex2(v[h][i] - (m == kNegInf ? 0.f : m));
+        }
+        l_run[0] += pr[0] + pr[2];
+        l_run[1] += pr[1] + pr[3];
+        const uint32_t h01 = pack_bf16(pr[0], pr[1]), h23 = pack_bf16(pr[2], pr[3]);
+        const float2 f01 = unpack_bf16(h01), f23 = unpack_bf16(h23);
+        const uint32_t l01 = pack_bf16(pr[0] - f01.x, pr[1] - f01.y), l23 = pack_bf16(pr[2] - f23.x, pr[3] - f23.y);
+        bh[h][0] = movmatrix_trans(h01);
+        bh[h][1] = movmatrix_trans(h23);
+        bl[h][0] = movmatrix_trans(l01);
+        bl[h][1] = movmatrix_trans(l23);
+    }
+    // ---- O^T += V^T P^T over both halves
+    const int vchunk = (lane >> 3) & 1;
+#pragma unroll
+    for (int mt = 0; mt < KS; ++mt) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            uint32_t a[4];
+            ldsm_x4_trans(tile_addr<D>(vbase, 16 * h + (lane & 7) + ((lane >> 4) << 3), 2 * mt + vchunk, swz), a);
+            mma_16816(acc[mt], a, bh[h][0], bh[h][1]);
+            mma_16816(acc[mt], a, bl[h][0], bl[h][1]);
+        }
+    }
+}
+
 // Workspace slot of slice j of a unit whose first slice belongs to CTA kf:
 // slice 0 is CTA kf's last slice (slot 2kf+1), slice j >= 1 is CTA kf+j's
 // first slice (slot 2(kf+j)).
@@ -835,13 +958,21 @@ __device__ __forceinline__ int column_keys(const KParams &p, const Seg &sg, int 
     return sg.mask_from + ((sg.sub * GC + c) >> p.group_shift) - ((sg.sub * GC) >> p.group_shift);
 }
 
-// B fragments of Q^T for one slice: column g of the unit (zero beyond its
-// columns), dims 16ks + 2c (+8).
+// (query, head) columns of a multi-query unit (GC > 8 kernels only).
+template <int GC>
+__device__ __forceinline__ int unit_cols(const KParams &p, const Seg &sg)
+{
+    return min(GC, sg.qn * p.group - sg.sub * GC);
+}
+
+// B fragments of Q^T for one slice: column cb + g of the unit (zero beyond
+// its columns), dims 16ks + 2c (+8).
 template <int D, int GC, bool MQ>
-__device__ __forceinline__ void load_q(const KParams &p, const Seg &sg, int lane, uint32_t (&qf)[D / 16][2])
+__device__ __forceinline__ void load_q(const KParams &p, const Seg &sg, int lane, uint32_t (&qf)[D / 16][2],
+                                       int cb = 0)
 {
     const int g = lane >> 2, c = lane & 3;
-    const int row = g < GC ? column_row<GC, MQ>(p, sg, g) : -1;
+    const int row = g < GC ? column_row<GC, MQ>(p, sg, cb + g) : -1;
     const uint32_t *qrow = reinterpret_cast<const uint32_t *>(p.q + (int64_t)(row < 0 ? 0 : row) * D);
 #pragma unroll
     for (int ks = 0; ks < D / 16; ++ks) {
@@ -857,6 +988,7 @@ __device__ void consumers(const KParams &p, Smem<D, GC, MQ> &sm)
 {
     constexpr int S = Smem<D, GC, MQ>::kStages;
     constexpr int KS = D / 16;
+    constexpr int RC = Smem<D, GC, MQ>::RC;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, c = lane & 3;
     const int swz = p.swizzle ? 7 : 0;
@@ -867,9 +999,18 @@ __device__ void consumers(const KParams &p, Smem<D, GC, MQ> &sm)
     bool have = si.next(p, sm, sg);
     uint32_t qf[KS][2];
     wait_prior_grid(p);
+    // a unit of more than 8 columns (GC = 16 only) splits its columns between
+    // the warps: this warp's first column is cb
+    bool wide = false;
+    int cb = 0;
+    if constexpr (GC > 8) {
+        wide = have && unit_cols<GC>(p, sg) > 8;
+        cb = wide ? 8 * warp : 0;
+    }
     if (have)
-        load_q<D, GC, MQ>(p, sg, lane, qf);
-    int lim0 = have ? column_keys<GC, MQ>(p, sg, 2 * c) : 0, lim1 = have ? column_keys<GC, MQ>(p, sg, 2 * c + 1) : 0;
+        load_q<D, GC, MQ>(p, sg, lane, qf, cb);
+    int lim0 = have ? column_keys<GC, MQ>(p, sg, cb + 2 * c) : 0;
+    int lim1 = have ? column_keys<GC, MQ>(p, sg, cb + 2 * c + 1) : 0;
     uint32_t g_tile = 0;
     int seg_i = 0;
     while (have) {
@@ -892,7 +1033,22 @@ __device__ void consumers(const KParams &p, Smem<D, GC, MQ> &sm)
             bad |= ((volatile int32_t *)sm.stage_bad)[s];
             const int tstart = sg.tok0 + t * kTile;
             const int nv = min(kTile, sg.tok1 - tstart);
-            if (nv == kTile && (!MQ || tstart + kTile <= sg.mask_from)) {
+            bool done = false;
+            if constexpr (GC > 8) {
+                if (wide) {
+                    if (nv == kTile && tstart + kTile <= sg.mask_from) {
+                        consume_tile_wide<D, false>(sm.kv[s][0], sm.kv[s][1], nv, 0, 0, lane, swz, p.q_scale, qf, acc,
+                                                    m_run, l_run);
+                    } else {
+                        consume_tile_wide<D, true>(sm.kv[s][0], sm.kv[s][1], nv, lim0 - tstart, lim1 - tstart, lane,
+                                                   swz, p.q_scale, qf, acc, m_run, l_run);
+                        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    }
+                    done = true;
+                }
+            }
+            if (done) {
+            } else if (nv == kTile && (!MQ || tstart + kTile <= sg.mask_from)) {
                 consume_tile<D, false, MQ>(sm.kv[s][0], sm.kv[s][1], nv, 0, 0, warp, lane, swz, p.q_scale, qf, acc,
                                        m_run, l_run);
             } else {
@@ -907,8 +1063,12 @@ __device__ void consumers(const KParams &p, Smem<D, GC, MQ> &sm)
                 mbar_arrive(&sm.empty[s]);
             if (t == 0) {
                 more = si.next(p, sm, nx);
-                if (more)
-                    load_q<D, GC, MQ>(p, nx, lane, qn);
+                if (more) {
+                    int ncb = 0;
+                    if constexpr (GC > 8)
+                        ncb = unit_cols<GC>(p, nx) > 8 ? 8 * warp : 0;
+                    load_q<D, GC, MQ>(p, nx, lane, qn, ncb);
+                }
             }
         }
         if (!ok)
@@ -926,7 +1086,7 @@ __device__ void consumers(const KParams &p, Smem<D, GC, MQ> &sm)
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
             const int h = 2 * c + j;
-            if (h < GC) {
+            if (h < RC) {
 #pragma unroll
                 for (int mt = 0; mt < KS; ++mt) {
                     sm.red_o[slot][warp][h][16 * mt + g] = acc[mt][j];
@@ -947,8 +1107,12 @@ __device__ void consumers(const KParams &p, Smem<D, GC, MQ> &sm)
         have = more;
         sg = nx;
         if (have) {
-            lim0 = column_keys<GC, MQ>(p, sg, 2 * c);
-            lim1 = column_keys<GC, MQ>(p, sg, 2 * c + 1);
+            if constexpr (GC > 8) {
+                wide = unit_cols<GC>(p, sg) > 8;
+                cb = wide ? 8 * warp : 0;
+            }
+            lim0 = column_keys<GC, MQ>(p, sg, cb + 2 * c);
+            lim1 = column_keys<GC, MQ>(p, sg, cb + 2 * c + 1);
         }
 #pragma unroll
         for (int ks = 0; ks < KS; ++ks) {
@@ -986,10 +1150,12 @@ struct EpiInputs {
     int page;
 };
 
-template <int D, int GC>
+template <int D, int GC, bool MQ>
 __device__ __forceinline__ void load_epi_inputs(const KParams &p, const Seg &sg, int lane, EpiInputs<D, GC> &in)
 {
     in.page = 0;
+    if constexpr (MQ)
+        return; // multi-query rows were appended by the caller: no new token here
     if (sg.status != ROW_OK || !p.with_new)
         return;
     const int h0 = sg.kvh * p.group + sg.sub * GC;
@@ -1017,9 +1183,11 @@ __device__ __forceinline__ void load_epi_inputs(const KParams &p, const Seg &sg,
 
 // Writes one unit's output: zeros for inactive / failed rows, otherwise
 // merges the new token (when given), performs the append and normalises.
-template <int D, int GC, bool MQ>
+// Multi-query units of UGC columns are written GC columns at a time, from
+// column col0.
+template <int D, int GC, bool MQ, int UGC = GC>
 __device__ void finalize_warp(const KParams &p, const Seg &sg, EpiState<D, GC> &st, const EpiInputs<D, GC> &in,
-                              int bad, int lane)
+                              int bad, int lane, int col0 = 0)
 {
     constexpr int EPT2 = EpiState<D, GC>::EPT2;
     constexpr int KP = EpiInputs<D, GC>::KP;
@@ -1117,7 +1285,7 @@ __device__ void finalize_warp(const KParams &p, const Seg &sg, EpiState<D, GC> &
     int orow[GC];
 #pragma unroll
     for (int g = 0; g < GC; ++g)
-        orow[g] = column_row<GC, MQ>(p, sg, g);
+        orow[g] = column_row<UGC, MQ>(p, sg, col0 + g);
     uint32_t *out = reinterpret_cast<uint32_t *>(p.out);
 #pragma unroll
     for (int i = 0; i < EPT2; ++i) {
@@ -1142,10 +1310,12 @@ __device__ void finalize_warp(const KParams &p, const Seg &sg, EpiState<D, GC> &
     }
 }
 
-// Merges the n slice partials of one unit into st; returns nonzero if any
-// slice met a bad page.  The loads of all slices are issued before the math.
+// Merges the n slice partials of one unit into st (columns col0 .. col0 +
+// GC - 1 of partials `stride` columns wide); returns nonzero if any slice met
+// a bad page.  The loads of all slices are issued before the math.
 template <int D, int GC>
-__device__ int combine_warp(const KParams &p, EpiState<D, GC> &st, int kf, int n, int lane)
+__device__ int combine_warp(const KParams &p, EpiState<D, GC> &st, int kf, int n, int lane, int stride = GC,
+                           int col0 = 0)
 {
     constexpr int EPT2 = EpiState<D, GC>::EPT2;
     constexpr int kBatch = EPT2 >= 16 ? 1 : (EPT2 >= 8 ? 2 : 4); // slices whose loads are in flight together
@@ -1167,8 +1337,8 @@ __device__ int combine_warp(const KParams &p, EpiState<D, GC> &st, int kf, int n
                 const int slot = slot_of(kf, j0 + jj);
 #pragma unroll
                 for (int g = 0; g < GC; ++g)
-                    ml[jj][g] = __ldcg(p.part_ml + (int64_t)slot * GC + g);
-                const float2 *po = reinterpret_cast<const float2 *>(p.part_o + (int64_t)slot * GC * D);
+                    ml[jj][g] = __ldcg(p.part_ml + (int64_t)slot * stride + col0 + g);
+                const float2 *po = reinterpret_cast<const float2 *>(p.part_o + ((int64_t)slot * stride + col0) * D);
 #pragma unroll
                 for (int i = 0; i < EPT2; ++i)
                     ov[jj][i] = __ldcg(po + (pair_elem<D>(lane, i) >> 1));
@@ -1200,10 +1370,81 @@ __device__ int combine_warp(const KParams &p, EpiState<D, GC> &st, int kf, int n
     return bad;
 }
 
+// Epilogue warps that read one hand-off slot before it is refilled: both in
+// kernels with 16-column units (a wide unit's two 8-column halves are
+// finished side by side), else the one that owns the slice.
+template <int GC>
+__host__ __device__ constexpr int kEpiReaders()
+{
+    return GC > 8 ? 2 : 1;
+}
+
+// A slice's softmax state from hand-off slot `slot`: the two consumer warps'
+// row halves merged, or (wide units) warp h's columns as they are.
+template <int D, int GC, bool MQ>
+__device__ __forceinline__ void slot_state(const Smem<D, GC, MQ> &sm, int slot, bool wide, int h, int lane,
+                                           EpiState<D, Smem<D, GC, MQ>::RC> &st)
+{
+    constexpr int RC = Smem<D, GC, MQ>::RC;
+    constexpr int EPT2 = EpiState<D, RC>::EPT2;
+    if (wide) {
+#pragma unroll
+        for (int g = 0; g < RC; ++g) {
+            st.M[g] = sm.red_m[slot][h][g];
+            st.L[g] = sm.red_l[slot][h][g];
+        }
+#pragma unroll
+        for (int i = 0; i < EPT2; ++i)
+            st.o[i] = *reinterpret_cast<const float2 *>(&(&sm.red_o[slot][h][0][0])[pair_elem<D>(lane, i)]);
+        return;
+    }
+    float w0[RC], w1[RC];
+#pragma unroll
+    for (int g = 0; g < RC; ++g) {
+        const float m0 = sm.red_m[slot][0][g], m1 = sm.red_m[slot][1][g];
+        const float M = fmaxf(m0, m1);
+        w0[g] = m0 == kNegInf ? 0.f : ex2(m0 - M);
+        w1[g] = m1 == kNegInf ? 0.f : ex2(m1 - M);
+        st.M[g] = M;
+        st.L[g] = w0[g] * sm.red_l[slot][0][g] + w1[g] * sm.red_l[slot][1][g];
+    }
+#pragma unroll
+    for (int i = 0; i < EPT2; ++i) {
+        const int e = pair_elem<D>(lane, i), g = e / D;
+        const float2 r0 = *reinterpret_cast<const float2 *>(&(&sm.red_o[slot][0][0][0])[e]);
+        const float2 r1 = *reinterpret_cast<const float2 *>(&(&sm.red_o[slot][1][0][0])[e]);
+        st.o[i] = make_float2(w0[g] * r0.x + w1[g] * r1.x, w0[g] * r0.y + w1[g] * r1.y);
+    }
+}
+
+// Writes a slice's state as split-KV partial `wslot` (columns col0 .. col0 +
+// GC - 1 of a partial `stride` columns wide); l = -1 marks a bad page.
+template <int D, int GC>
+__device__ __forceinline__ void write_partial(const KParams &p, const EpiState<D, GC> &st, int wslot, int stride,
+                                              int col0, int bad, int lane)
+{
+    constexpr int EPT2 = EpiState<D, GC>::EPT2;
+    float2 *po = reinterpret_cast<float2 *>(p.part_o + ((int64_t)wslot * stride + col0) * D);
+#pragma unroll
+    for (int i = 0; i < EPT2; ++i)
+        po[pair_elem<D>(lane, i) >> 1] = st.o[i];
+    if (lane < GC) {
+        float M = 0.f, L = 0.f;
+#pragma unroll
+        for (int g = 0; g < GC; ++g)
+            if (g == lane) {
+                M = st.M[g];
+                L = st.L[g];
+            }
+        p.part_ml[(int64_t)wslot * stride + col0 + lane] = make_float2(M, bad ? -1.f : L);
+    }
+}
+
 template <int D, int GC, bool MQ>
 __device__ void epilogue(const KParams &p, Smem<D, GC, MQ> &sm, int ew)
 {
-    constexpr int EPT2 = EpiState<D, GC>::EPT2;
+    constexpr int RC = Smem<D, GC, MQ>::RC; // columns per pass: a 16-column unit takes two passes
+    constexpr int EPT2 = EpiState<D, RC>::EPT2;
     const int lane = threadIdx.x & 31;
     const int k = (int)blockIdx.x;
     volatile int32_t *abort = &sm.abort;
@@ -1216,11 +1457,17 @@ __device__ void epilogue(const KParams &p, Smem<D, GC, MQ> &sm, int ew)
     while (si.next(p, sm, sg)) {
         const int mine = seg_i;
         ++seg_i;
-        if ((mine & 1) != ew)
+        // a wide unit (more than 8 columns) is finished by both warps, warp
+        // ew taking columns 8 ew .. 8 ew + 7; other slices by one warp
+        bool wide = false;
+        if constexpr (GC > 8)
+            wide = unit_cols<GC>(p, sg) > 8;
+        if (!wide && (mine & 1) != ew)
             continue;
         const int slot = mine & 1;
-        EpiInputs<D, GC> in;
-        load_epi_inputs<D, GC>(p, sg, lane, in);
+        const int h = wide ? ew : 0; // this warp's 8-column pass
+        EpiInputs<D, RC> in;
+        load_epi_inputs<D, RC, MQ>(p, sg, lane, in);
         // slices of this unit: kf .. kf + n - 1 (a slice from the unit's first
         // to its last token is the whole unit)
         int kf = k, n = 1;
@@ -1233,60 +1480,55 @@ __device__ void epilogue(const KParams &p, Smem<D, GC, MQ> &sm, int ew)
             stopped = true;
             break;
         }
-        // merge the two consumer warps' states
-        EpiState<D, GC> st;
-        float w0[GC], w1[GC];
-#pragma unroll
-        for (int g = 0; g < GC; ++g) {
-            const float m0 = sm.red_m[slot][0][g], m1 = sm.red_m[slot][1][g];
-            const float M = fmaxf(m0, m1);
-            w0[g] = m0 == kNegInf ? 0.f : ex2(m0 - M);
-            w1[g] = m1 == kNegInf ? 0.f : ex2(m1 - M);
-            st.M[g] = M;
-            st.L[g] = w0[g] * sm.red_l[slot][0][g] + w1[g] * sm.red_l[slot][1][g];
-        }
-#pragma unroll
-        for (int i = 0; i < EPT2; ++i) {
-            const int e = pair_elem<D>(lane, i), g = e / D;
-            const float2 r0 = *reinterpret_cast<const float2 *>(&(&sm.red_o[slot][0][0][0])[e]);
-            const float2 r1 = *reinterpret_cast<const float2 *>(&(&sm.red_o[slot][1][0][0])[e]);
-            st.o[i] = make_float2(w0[g] * r0.x + w1[g] * r1.x, w0[g] * r0.y + w1[g] * r1.y);
-        }
+        EpiState<D, RC> st;
+        slot_state(sm, slot, wide, h, lane, st);
         int bad = sm.red_bad[slot][0] | sm.red_bad[slot][1];
         __syncwarp();
-        if (lane == 0)
-            mbar_arrive(&sm.epi_empty[slot]); // consumers may refill this slot
-        if (n == 1) {
-            finalize_warp<D, GC, MQ>(p, sg, st, in, bad, lane);
-            continue;
+        if (lane == 0) { // consumers may refill this slot once every reader is done
+            if constexpr (kEpiReaders<GC>() == 1)
+                mbar_arrive(&sm.epi_empty[slot]);
+            else
+                mbar_arrive_cnt(&sm.epi_empty[slot], wide ? 1u : (uint32_t)kEpiReaders<GC>());
         }
-        const int wslot = slot_of(kf, k - kf);
-        float2 *po = reinterpret_cast<float2 *>(p.part_o + (int64_t)wslot * GC * D);
-#pragma unroll
-        for (int i = 0; i < EPT2; ++i)
-            po[pair_elem<D>(lane, i) >> 1] = st.o[i];
-        if (lane < GC) {
-            float M = 0.f, L = 0.f;
-#pragma unroll
-            for (int g = 0; g < GC; ++g)
-                if (g == lane) {
-                    M = st.M[g];
-                    L = st.L[g];
-                }
-            p.part_ml[(int64_t)wslot * GC + lane] = make_float2(M, bad ? -1.f : L);
-        }
-        __threadfence();
-        __syncwarp();
-        int last = 0;
-        if (lane == 0)
-            last = atomicAdd(&p.tickets[sg.unit], 1) == n - 1;
-        last = __shfl_sync(0xffffffffu, last, 0);
-        if (last) {
+        if constexpr (GC > 8) {
+            if (n == 1) {
+                finalize_warp<D, RC, MQ, GC>(p, sg, st, in, bad, lane, RC * h);
+                continue;
+            }
+            write_partial<D, RC>(p, st, slot_of(kf, k - kf), GC, RC * h, bad, lane);
             __threadfence();
-            bad = combine_warp<D, GC>(p, st, kf, n, lane);
-            finalize_warp<D, GC, MQ>(p, sg, st, in, bad, lane);
+            __syncwarp();
+            int32_t *ticket = p.tickets + 2 * sg.unit + h;
+            int last = 0;
             if (lane == 0)
-                p.tickets[sg.unit] = 0; // ready for the next call
+                last = atomicAdd(ticket, 1) == n - 1;
+            last = __shfl_sync(0xffffffffu, last, 0);
+            if (last) {
+                __threadfence();
+                bad = combine_warp<D, RC>(p, st, kf, n, lane, GC, RC * h);
+                finalize_warp<D, RC, MQ, GC>(p, sg, st, in, bad, lane, RC * h);
+                if (lane == 0)
+                    *ticket = 0; // ready for the next call
+            }
+        } else {
+            if (n == 1) {
+                finalize_warp<D, GC, MQ>(p, sg, st, in, bad, lane);
+                continue;
+            }
+            write_partial<D, GC>(p, st, slot_of(kf, k - kf), GC, 0, bad, lane);
+            __threadfence();
+            __syncwarp();
+            int last = 0;
+            if (lane == 0)
+                last = atomicAdd(&p.tickets[sg.unit], 1) == n - 1;
+            last = __shfl_sync(0xffffffffu, last, 0);
+            if (last) {
+                __threadfence();
+                bad = combine_warp<D, GC>(p, st, kf, n, lane);
+                finalize_warp<D, GC, MQ>(p, sg, st, in, bad, lane);
+                if (lane == 0)
+                    p.tickets[sg.unit] = 0; // ready for the next call
+            }
         }
     }
     // Units with no cached token (inactive, overflowing or empty rows, and
@@ -1312,18 +1554,23 @@ __device__ void epilogue(const KParams &p, Smem<D, GC, MQ> &sm, int ew)
                 es.tok0 = es.tok1 = 0;
                 es.u0 = 0;
                 es.n = 0;
-                EpiInputs<D, GC> in;
-                load_epi_inputs<D, GC>(p, es, lane, in);
-                EpiState<D, GC> st;
+                EpiInputs<D, RC> in;
+                load_epi_inputs<D, RC, MQ>(p, es, lane, in);
+                int npass_e = 1;
+                if constexpr (GC > 8)
+                    npass_e = unit_cols<GC>(p, es) > 8 ? 2 : 1;
+                for (int h = 0; h < npass_e; ++h) {
+                    EpiState<D, RC> st;
 #pragma unroll
-                for (int g = 0; g < GC; ++g) {
-                    st.M[g] = kNegInf;
-                    st.L[g] = 0.f;
+                    for (int g = 0; g < RC; ++g) {
+                        st.M[g] = kNegInf;
+                        st.L[g] = 0.f;
+                    }
+#pragma unroll
+                    for (int i = 0; i < EPT2; ++i)
+                        st.o[i] = make_float2(0.f, 0.f);
+                    finalize_warp<D, RC, MQ, GC>(p, es, st, in, 0, lane, RC * h);
                 }
-#pragma unroll
-                for (int i = 0; i < EPT2; ++i)
-                    st.o[i] = make_float2(0.f, 0.f);
-                finalize_warp<D, GC, MQ>(p, es, st, in, 0, lane);
             }
             e0 += units;
         }
@@ -1340,8 +1587,7 @@ __device__ void epilogue(const KParams &p, Smem<D, GC, MQ> &sm, int ew)
 }
 
 template <int D, int GC, bool MQ>
-__global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant__ KParams p,
-                                                          const __grid_constant__ DecodeMaps maps)
+__device__ __forceinline__ void decode_body(const KParams &p, const DecodeMaps &maps)
 {
     extern __shared__ unsigned char smem_raw[];
     Smem<D, GC, MQ> &sm = *reinterpret_cast<Smem<D, GC, MQ> *>(
@@ -1357,7 +1603,7 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
         }
         for (int s = 0; s < kSlots; ++s) {
             mbar_init(&sm.epi_full[s], kWarps);
-            mbar_init(&sm.epi_empty[s], 1);
+            mbar_init(&sm.epi_empty[s], kEpiReaders<GC>());
         }
         sm.abort = 0;
         mbar_init_fence();
@@ -1378,6 +1624,23 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
 }
 
 template <int D, int GC, bool MQ>
+__global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant__ KParams p,
+                                                          const __grid_constant__ DecodeMaps maps)
+{
+    decode_body<D, GC, MQ>(p, maps);
+}
+
+// 16-column multi-query units: the register bound keeps two CTAs on an SM
+// at head_dim <= 128 (the other instantiations fit two without it, or never
+// do at head_dim 256).
+template <int D, int GC, bool MQ>
+__global__ void __launch_bounds__(kThreads, D <= 128 ? 2 : 1) decode_kernel_wide(const __grid_constant__ KParams p,
+                                                                                 const __grid_constant__ DecodeMaps maps)
+{
+    decode_body<D, GC, MQ>(p, maps);
+}
+
+template <int D, int GC, bool MQ>
 size_t smem_bytes()
 {
     return sizeof(Smem<D, GC, MQ>) + 1024;
@@ -1386,6 +1649,7 @@ size_t smem_bytes()
 // Two CTAs per SM: 228 KB of shared memory per SM, 1 KB of it reserved per CTA.
 static_assert(sizeof(Smem<128, 4, true>) + 1024 + 1024 <= 228 * 1024 / 2, "decode<128,4> must fit twice on an SM");
 static_assert(sizeof(Smem<128, 8, true>) + 1024 + 1024 <= 228 * 1024 / 2, "decode<128,8> must fit twice on an SM");
+static_assert(sizeof(Smem<128, 16, true>) + 1024 + 1024 <= 228 * 1024 / 2, "decode<128,16> must fit twice on an SM");
 
 struct KernelEntry {
     int D, GC;
@@ -1397,7 +1661,12 @@ struct KernelEntry {
 template <int D, int GC, bool MQ>
 KernelEntry entry()
 {
-    return KernelEntry{D, GC, MQ, reinterpret_cast<const void *>(&decode_kernel<D, GC, MQ>), smem_bytes<D, GC, MQ>()};
+    const void *fn;
+    if constexpr (GC > 8)
+        fn = reinterpret_cast<const void *>(&decode_kernel_wide<D, GC, MQ>);
+    else
+        fn = reinterpret_cast<const void *>(&decode_kernel<D, GC, MQ>);
+    return KernelEntry{D, GC, MQ, fn, smem_bytes<D, GC, MQ>()};
 }
 
 const KernelEntry kTable[] = {
@@ -1407,6 +1676,7 @@ const KernelEntry kTable[] = {
     entry<64, 1, true>(),   entry<64, 2, true>(),   entry<64, 4, true>(),   entry<64, 8, true>(),
     entry<128, 1, true>(),  entry<128, 2, true>(),  entry<128, 4, true>(),  entry<128, 8, true>(),
     entry<256, 1, true>(),  entry<256, 2, true>(),  entry<256, 4, true>(),  entry<256, 8, true>(),
+    entry<64, 16, true>(),  entry<128, 16, true>(), entry<256, 16, true>(),
 };
 
 const KernelEntry *find_kernel(int D, int GC, bool mq = false)
@@ -1445,9 +1715,9 @@ namespace {
 
 // Shared tail of decode_shape / decode_mq_shape once the columns per unit
 // (heads_per_cta) and units per row are set.
-bool finish_shape(int batch, int max_blocks, const pkv_cache_desc &d, DecodeShape *s)
+bool finish_shape(int batch, int max_blocks, const pkv_cache_desc &d, bool multi_query, DecodeShape *s)
 {
-    if (find_kernel(d.head_dim, s->heads_per_cta) == nullptr)
+    if (find_kernel(d.head_dim, s->heads_per_cta, multi_query) == nullptr)
         return false;
     // the plan counts tokens of all rows, and work positions inside a row, in int32
     const int64_t row_tokens = (int64_t)max_blocks * d.page_size;
@@ -1458,7 +1728,8 @@ bool finish_shape(int batch, int max_blocks, const pkv_cache_desc &d, DecodeShap
     s->cap_items = 2 * (int64_t)kMaxGrid; // two partial slots per persistent CTA
     const int64_t units = (int64_t)batch * s->units_per_row;
     auto align = [](size_t x) { return (x + 255) & ~size_t(255); };
-    const size_t tickets = align(sizeof(int32_t) * (size_t)units);
+    // one combine ticket per unit (16-column units: one per 8-column half)
+    const size_t tickets = align(sizeof(int32_t) * (size_t)units * (s->heads_per_cta > 8 ? 2 : 1));
     s->off_ml = tickets;
     s->off_o = s->off_ml + align(sizeof(float2) * (size_t)s->cap_items * s->heads_per_cta);
     s->bytes = s->off_o + align(sizeof(float) * (size_t)s->cap_items * s->heads_per_cta * d.head_dim);
@@ -1477,7 +1748,7 @@ bool decode_shape(int batch, int max_blocks, int num_q_heads, const pkv_cache_de
     s->heads_per_cta = heads_per_cta(s->group);
     s->n_sub = s->group / s->heads_per_cta;
     s->units_per_row = d.num_kv_heads * s->n_sub;
-    return finish_shape(batch, max_blocks, d, s);
+    return finish_shape(batch, max_blocks, d, false, s);
 }
 
 bool decode_mq_shape(int batch, int max_blocks, int num_q_heads, int max_qlen, const pkv_cache_desc &d,
@@ -1488,10 +1759,11 @@ bool decode_mq_shape(int batch, int max_blocks, int num_q_heads, int max_qlen, c
     s->group = num_q_heads / d.num_kv_heads;
     if (s->group & (s->group - 1))
         return false;
-    // (query, head) columns of one kv head; a unit takes up to 8 (the MMA's N side)
+    // (query, head) columns of one kv head; a unit takes up to 16 (two 8-wide
+    // MMA n-tiles, one per consumer warp, over one pass of the K/V tiles)
     const int64_t cols = (int64_t)s->group * max_qlen;
     int gc = 1;
-    while (gc < cols && gc < 8)
+    while (gc < cols && gc < 16)
         gc <<= 1;
     s->heads_per_cta = gc;
     const int64_t n_sub = (cols + gc - 1) / gc;
@@ -1499,7 +1771,7 @@ bool decode_mq_shape(int batch, int max_blocks, int num_q_heads, int max_qlen, c
         return false;
     s->n_sub = (int)n_sub;
     s->units_per_row = d.num_kv_heads * s->n_sub;
-    return finish_shape(batch, max_blocks, d, s);
+    return finish_shape(batch, max_blocks, d, true, s);
 }
 
 int decode_target_items(int device, int head_dim, int heads_per_cta, bool multi_query)

@@ -124,6 +124,22 @@ def test_long_rows_split_across_ctas():
     _compare(case, _run_gpu(case, 4, 4), _run_oracle(case, 4))
 
 
+@pytest.mark.parametrize("geom", [(64, 16, 2, 32, wl.HND), (256, 16, 2, 16, wl.NHD), (128, 32, 8, 16, wl.HND)],
+                         ids=["D64-G8", "D256-G8", "D128-G4"])
+def test_wide_units_split_across_ctas(geom):
+    """Units of 9..16 (query, head) columns (one consumer warp per 8 columns,
+    over one K/V pass) on rows long enough to be split over many CTAs: their
+    partials are written and merged in two 8-column passes; a row of 24
+    columns takes a 16-column and an 8-column unit."""
+    D, Hq, Hkv, P, layout = geom
+    G = Hq // Hkv
+    q_lens = [16 // G, 24 // G, 1, 12 // G if G < 8 else 2, 16 // G]
+    case = wl.mixed_step(36 + D, q_lens, [9000, 4100, 7000, 31, 0], Hq, Hkv, D, P, layout, extra_pages=0,
+                         device=DEV)
+    dq = 24 // G
+    _compare(case, _run_gpu(case, dq, dq), _run_oracle(case, dq))
+
+
 def test_row_fates_match_oracle():
     # ok, inactive, too long, bad cached page (decode row), bad destination
     # page (prefill row), overflow, bad cached page (prefill row)
