@@ -483,8 +483,43 @@ pkv_status pkv_mixed_attn(const pkv_cache_desc *desc, void *k_cache, void *v_cac
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const float q_scale = softmax_scale * 1.4426950408889634f;
 
+    // Launch order: the prefill plan (when longer rows exist; it reads only
+    // the row arrays and the table), the append (a programmatic dependent of
+    // the plan: the two run side by side, and the append completes after the
+    // plan), the decode kernel (a programmatic dependent of the append: its
+    // plan and page-id prefetch overlap the append), then the prefill kernel.
+    PrefillArgs pa;
+    PrefillMaps pmaps;
+    if (m.prefill) {
+        pa.desc = *desc;
+        pa.batch = batch;
+        pa.num_q_heads = num_q_heads;
+        pa.total_q = total_q;
+        pa.max_blocks = max_blocks;
+        pa.q_scale = q_scale;
+        pa.qo_indptr = qo_indptr;
+        pa.kv_lens = nullptr;
+        pa.block_table = block_table;
+        pa.q = q;
+        pa.out = out;
+        pa.lse = lse;
+        pa.workspace = static_cast<unsigned char *>(workspace) + m.off_prefill;
+        pa.err_flag = err_flag;
+        pa.shape = m.pshape;
+        pa.cache_seqlens = cache_seqlens;
+        pa.q_lo = m.dq;
+        pa.q_max = max_qlen;
+        pa.kv_add = k_new != nullptr ? 1 : 0;
+        if (!encode_prefill_maps(*desc, k_cache, v_cache, &pmaps))
+            return PKV_ECUDA;
+        pa.phase = kPrefillPlan;
+        if (launch_prefill(pa, pmaps, s) != cudaSuccess)
+            return PKV_ECUDA;
+    }
+
     // 1. the new tokens of every row into the cache (rows longer than max_qlen append nothing)
-    if (k_new != nullptr && total_q > 0) {
+    const bool appended = k_new != nullptr && total_q > 0;
+    if (appended) {
         AppendArgs a;
         a.desc = *desc;
         a.page_shift = log2_exact(desc->page_size);
@@ -500,6 +535,7 @@ pkv_status pkv_mixed_attn(const pkv_cache_desc *desc, void *k_cache, void *v_cac
         a.batch = batch;
         a.err_flag = err_flag;
         a.max_count = max_qlen;
+        a.overlap_prior = m.prefill;
         if (launch_append(a, s) != cudaSuccess)
             return PKV_ECUDA;
     }
@@ -527,7 +563,9 @@ pkv_status pkv_mixed_attn(const pkv_cache_desc *desc, void *k_cache, void *v_cac
         a.shape = m.dshape;
         a.target_items = 0;
         a.grid = decode_target_items(dev, desc->head_dim, m.dshape.heads_per_cta, true);
-        a.flags = 0;
+        // after the append only: the user's kernel before this call may write
+        // the row arrays, which the overlapped prologue reads
+        a.flags = appended ? PKV_DECODE_OVERLAP_PROLOGUE : 0u;
         a.qo_indptr = qo_indptr;
         a.total_q = total_q;
         a.mq_hi = m.dq;
@@ -543,30 +581,8 @@ pkv_status pkv_mixed_attn(const pkv_cache_desc *desc, void *k_cache, void *v_cac
 
     // 3. longer rows (prefill chunks): the tcgen05 prefill kernel over kv = L + q keys
     if (m.prefill) {
-        PrefillArgs a;
-        a.desc = *desc;
-        a.batch = batch;
-        a.num_q_heads = num_q_heads;
-        a.total_q = total_q;
-        a.max_blocks = max_blocks;
-        a.q_scale = q_scale;
-        a.qo_indptr = qo_indptr;
-        a.kv_lens = nullptr;
-        a.block_table = block_table;
-        a.q = q;
-        a.out = out;
-        a.lse = lse;
-        a.workspace = static_cast<unsigned char *>(workspace) + m.off_prefill;
-        a.err_flag = err_flag;
-        a.shape = m.pshape;
-        a.cache_seqlens = cache_seqlens;
-        a.q_lo = m.dq;
-        a.q_max = max_qlen;
-        a.kv_add = k_new != nullptr ? 1 : 0;
-        PrefillMaps maps;
-        if (!encode_prefill_maps(*desc, k_cache, v_cache, &maps))
-            return PKV_ECUDA;
-        if (launch_prefill(a, maps, s) != cudaSuccess)
+        pa.phase = kPrefillMain;
+        if (launch_prefill(pa, pmaps, s) != cudaSuccess)
             return PKV_ECUDA;
     }
     return PKV_OK;

@@ -24,10 +24,11 @@ struct AParams {
     int32_t *err_flag;
     int num_tokens, batch, max_blocks, page_size, page_shift, num_pages, num_kv_heads, head_dim, layout;
     int max_count; // rows appending more tokens than this append nothing
+    int pdl_wait;  // launched as a programmatic dependent: wait for the preceding grid before exiting
 };
 
 // One CTA per new token.
-__global__ void __launch_bounds__(kAppendThreads) append_kernel(const __grid_constant__ AParams p)
+__device__ __forceinline__ void append_token(const AParams &p)
 {
     __shared__ int s_row, s_first, s_count;
     const int t = blockIdx.x;
@@ -95,6 +96,20 @@ __global__ void __launch_bounds__(kAppendThreads) append_kernel(const __grid_con
     }
 }
 
+// The next kernel in the stream may start as soon as every CTA has begun (it
+// waits for this grid's completion before touching what this grid writes).
+// With pdl_wait the grid itself overlaps the preceding kernel, which shares
+// no buffer with it, and completes only after that kernel, so that a kernel
+// waiting on this grid also waits on the one before.
+__global__ void __launch_bounds__(kAppendThreads) append_kernel(const __grid_constant__ AParams p)
+{
+    if (threadIdx.x == 0)
+        asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    append_token(p);
+    if (p.pdl_wait)
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 } // namespace
 
 cudaError_t launch_append(const AppendArgs &a, cudaStream_t stream)
@@ -120,8 +135,20 @@ cudaError_t launch_append(const AppendArgs &a, cudaStream_t stream)
     p.head_dim = a.desc.head_dim;
     p.layout = a.desc.layout;
     p.max_count = a.max_count;
-    append_kernel<<<a.num_tokens, kAppendThreads, 0, stream>>>(p);
-    return cudaGetLastError();
+    p.pdl_wait = a.overlap_prior ? 1 : 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(a.num_tokens);
+    cfg.blockDim = dim3(kAppendThreads);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    if (a.overlap_prior) {
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    void *args[] = {&p};
+    return cudaLaunchKernelExC(&cfg, reinterpret_cast<const void *>(&append_kernel), args);
 }
 
 } // namespace pkv

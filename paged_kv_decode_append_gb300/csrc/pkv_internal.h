@@ -115,6 +115,11 @@ struct AppendArgs {
     int batch;
     int32_t *err_flag;
     int max_count = 0x7fffffff; // rows appending more tokens than this append nothing
+    // Launch as a programmatic dependent of the preceding kernel: the two may
+    // run side by side, so that kernel must not write what the append reads
+    // or writes (k_new, v_new, the cache, indptr, cache_seqlens, block_table);
+    // the append grid still completes only after it.
+    bool overlap_prior = false;
 };
 
 cudaError_t launch_append(const AppendArgs &a, cudaStream_t stream);
@@ -179,7 +184,12 @@ struct PrefillArgs {
     int q_lo = 0;
     int q_max = 0x7fffffff;
     int kv_add = 0;
+    // Launches: kPrefillAll = the plan kernel then the attention kernel;
+    // kPrefillPlan / kPrefillMain one of them (the same arguments for both).
+    int phase = 0;
 };
+
+constexpr int kPrefillAll = 0, kPrefillPlan = 1, kPrefillMain = 2;
 
 // TMA descriptors of one prefill call: token-group boxes (encode_group_map)
 // of min(page_size, 64) tokens of the K and V pools.

@@ -1330,8 +1330,11 @@ __global__ void __launch_bounds__(kPlanThreads) prefill_plan_kernel(const PfPlan
     __shared__ int s_decreasing;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int P = 1 << pp.page_shift;
-    if (tid == 0)
+    if (tid == 0) {
+        // a programmatic dependent (the mixed step's append) may start now
+        asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
         s_decreasing = 0;
+    }
     for (int i = tid; i < kPfBuckets; i += kPlanThreads)
         s_hist[i] = 0;
     __syncthreads();
@@ -1616,10 +1619,12 @@ cudaError_t launch_prefill(const PrefillArgs &a, const PrefillMaps &maps, cudaSt
     pp.head_dim = a.desc.head_dim;
     pp.cluster = e->cluster;
     pp.cap_pairs = a.shape.cap_pairs;
-    prefill_plan_kernel<<<1, kPlanThreads, 0, stream>>>(pp);
-    cudaError_t err = cudaGetLastError();
-    if (err != cudaSuccess)
-        return err;
+    cudaError_t err = cudaSuccess;
+    if (a.phase != kPrefillMain) {
+        prefill_plan_kernel<<<1, kPlanThreads, 0, stream>>>(pp);
+        if ((err = cudaGetLastError()) != cudaSuccess || a.phase == kPrefillPlan)
+            return err;
+    }
 
     PfParams p;
     p.q = static_cast<const __nv_bfloat16 *>(a.q);
