@@ -59,6 +59,9 @@ namespace {
 constexpr int kPfSoftmaxWarps = 8; // two per TMEM lane quarter, each on half of a row's columns
 constexpr int kPfSoftmaxThreads = kPfSoftmaxWarps * 32;
 constexpr int kPfThreads = 64 + kPfSoftmaxThreads;
+// CTA-pair kernel: one more warp, a second producer (V items; warp 0 loads K)
+constexpr int kPf2VWarp = kPfThreads / 32;
+constexpr int kPf2Threads = kPfThreads + 32;
 constexpr int kPfProducerWarp = 0;
 constexpr int kPfMmaWarp = 1;
 constexpr int kPfRows = 128;    // M of every MMA
@@ -110,6 +113,15 @@ template <int D> struct Pf2Cfg {
     static_assert(D == 128 || D == 256, "pairs split head_dim into 64-column blocks");
     static constexpr uint32_t kItemBytes = kPfTile * D * 2;
     static constexpr int kStages = D == 256 ? 4 : 11;              // items in flight
+    // K items (one per step) and V items (one per step) have rings of their
+    // own, each filled by its own producer warp: the step's index gs picks
+    // the slot, K in [0, kKStages), V in [kKStages, kStages).
+    static constexpr int kKStages = kStages / 2;
+    static constexpr int kVStages = kStages - kKStages;
+    static __device__ __forceinline__ int k_slot(int gs) { return gs % kKStages; }
+    static __device__ __forceinline__ uint32_t k_par(int gs) { return (uint32_t)(gs / kKStages) & 1u; }
+    static __device__ __forceinline__ int v_slot(int gs) { return kKStages + gs % kVStages; }
+    static __device__ __forceinline__ uint32_t v_par(int gs) { return (uint32_t)(gs / kVStages) & 1u; }
     static constexpr uint32_t kGroupStride = 8 * D * 2;            // K and Q: 8 rows x head_dim
     static constexpr uint32_t kVGroupStride = 8 * (D / 2) * 2;     // V half: 8 keys x half of head_dim
     static constexpr int kVChunks = D / 128;                       // 64-column blocks of a V half
@@ -211,28 +223,19 @@ __device__ __forceinline__ int pf_unit_at(int k, int cluster)
     return k * g + ((k & 1) ? g - 1 - c : c);
 }
 
-template <bool CL>
-__device__ __forceinline__ bool pf_try(uint64_t *bar, uint32_t parity)
+// Bounded barrier wait that also gives up when another role has aborted:
+// the first test inline, the polling loop out of line.  The waits are
+// CTA-scoped, like those of every mbarrier that TMA, tcgen05.commit or a
+// peer CTA's remote arrive completes here (the data those signal is written
+// by the async proxy, or by tcgen05.st before the signalling fence).
+template <class Bars>
+__device__ __noinline__ bool pf_wait_slow(uint64_t *bar, uint32_t parity, Bars &bars, int32_t *err_flag)
 {
-    if constexpr (CL)
-        return mbar_try_wait_cluster(bar, parity);
-    else
-        return mbar_try_wait(bar, parity);
-}
-
-// Bounded barrier wait that also gives up when another role has aborted.
-// CL: acquire at cluster scope (barriers that another CTA's threads or MMAs
-// arrive on, in CTA pairs).
-template <bool CL, class Bars>
-__device__ __noinline__ bool pf_wait(uint64_t *bar, uint32_t parity, Bars &bars, int32_t *err_flag)
-{
-    if (pf_try<CL>(bar, parity))
-        return true;
     const uint64_t start = globaltimer_ns();
     volatile int32_t *abort = &bars.abort;
     for (;;) {
         for (int i = 0; i < 64; ++i)
-            if (pf_try<CL>(bar, parity))
+            if (mbar_try_wait(bar, parity))
                 return true;
         if (*abort != 0)
             return false;
@@ -242,6 +245,16 @@ __device__ __noinline__ bool pf_wait(uint64_t *bar, uint32_t parity, Bars &bars,
             return false;
         }
     }
+}
+
+// CL: the barrier is also arrived on from the other CTA of a pair (kept for
+// the call sites' documentation; the wait is the same).
+template <bool CL, class Bars>
+__device__ __forceinline__ bool pf_wait(uint64_t *bar, uint32_t parity, Bars &bars, int32_t *err_flag)
+{
+    if (mbar_try_wait(bar, parity))
+        return true;
+    return pf_wait_slow(bar, parity, bars, err_flag);
 }
 __device__ __forceinline__ bool pf_wait(uint64_t *bar, uint32_t parity, PfBars &bars, int32_t *err_flag)
 {
@@ -785,33 +798,39 @@ __global__ void __launch_bounds__(kPfThreads, 1)
 
 // ---------------------------------------------------------------- CTA pairs
 
-// Producer of one CTA of a pair, step by step (128 keys): item K_t is the
-// step's tile 2t + r (r = the CTA's rank in its pair), 64 keys with all of
-// head_dim; item V_t is all 128 keys of the step with columns
-// [r D/2, (r+1) D/2).  Boxes of min(page, 64) tokens; items in the MMA's
-// consumption order (K_0, K_1, V_0, K_2, V_1, ...).  With clusters of two
-// pairs on consecutive query tiles of the same (request, kv head), CTA c and
-// CTA c ^ 2 need the same items, so each loads half of every item's boxes
-// with TMA multicast into both (the same shared-memory offset, completing on
-// both full barriers) -- half the TMA issues per SM, which pays where the
-// boxes are small (head_dim 128).  A stage is refilled once every pair's MMA
-// that read it has completed.
+// Producers of one CTA of a pair, step by step (128 keys): warp `which` = 0
+// loads the K items, warp 1 the V items, each into a ring of its own.  Item
+// K_t is the step's tile 2t + r (r = the CTA's rank in its pair), 64 keys
+// with all of head_dim; item V_t is all 128 keys of the step with columns
+// [r D/2, (r+1) D/2).  Boxes of min(page, 64) tokens, one lane per box.
+// With clusters of two pairs on consecutive query tiles of the same
+// (request, kv head), CTA c and CTA c ^ 2 need the same items, so each loads
+// half of every item's boxes with TMA multicast into both (the same
+// shared-memory offset, completing on both full barriers) -- half the TMA
+// issues per SM, which pays where the boxes are small (head_dim 128).  A slot
+// is refilled once every pair's MMA that read it has completed.
 template <int D>
 __device__ void pf2_producer(const PfParams &p, const PfMapsDev &maps, uint8_t *smem, Pf2Bars &bars, int n_units,
-                             int lane, int rank)
+                             int lane, int rank, int which)
 {
     using C = Pf2Cfg<D>;
     const int Hkv = p.num_kv_heads;
     const int P = 1 << p.page_shift;
     const int bsh = p.box_shift; // min(P, 64) tokens per box
     const int BT = 1 << bsh;
-    const uint32_t kbox = (uint32_t)BT * D * 2, vbox = (uint32_t)BT * (D / 2) * 2;
+    const bool is_k = which == 0;
+    const uint32_t box = is_k ? (uint32_t)BT * D * 2 : (uint32_t)BT * (D / 2) * 2;
+    const CUtensorMap *map = is_k ? &maps.k : &maps.v;
+    const int ring = is_k ? C::kKStages : C::kVStages;
     const bool nhd = p.layout == PKV_NHD;
     const int r2 = rank & 1;                                   // rank in the pair
     const bool twin = p.cluster == 4;                          // a second pair shares every item
     const uint16_t mc = (uint16_t)((1u << rank) | (1u << (rank ^ 2))); // this CTA and its twin in the other pair
     const int share = rank >> 1;                              // which half of each item's boxes this CTA issues
-    int ib = 0, issued = 0;
+    const int c2 = is_k ? 0 : r2 * (D / 128);                 // V: this CTA's 64-column blocks
+    const int span = is_k ? kPfTile : kPfStep;                // tokens of an item
+    const int lane0 = is_k ? (r2 * kPfTile) >> bsh : 0;       // page lane of the item's first box
+    int gs = 0; // items issued so far (one per step)
     bool ok = true;
     for (int k = 0; ok; ++k) {
         const int u = pf_unit_at(k, p.cluster);
@@ -829,75 +848,75 @@ __device__ void pf2_producer(const PfParams &p, const PfMapsDev &maps, uint8_t *
                 id = __ldg(bt_row + (tok >> p.page_shift));
             return id;
         };
-        int ids_prev = 0, ids_cur = page_ids(0), ids_next = page_ids(1);
-        for (int t = 0; t <= ns && ok; ++t) {
-            for (int kind = 0; kind < 2; ++kind) { // K_t, then V_{t-1}
-                const int tt = kind == 0 ? t : t - 1;
-                if (kind == 0 ? (t >= ns) : (t < 1))
-                    continue;
-                const int itg = ib + (kind == 0 ? pf_item_k(tt) : pf_item_v(tt, ns));
-                const int stage = itg % C::kStages;
-                const int n = itg / C::kStages;
-                if (n > 0 && !pf_wait_all<true>(&bars.empty[stage], (n - 1) & 1, bars, p.err_flag)) {
-                    ok = false;
-                    break;
-                }
-                uint8_t *dst = smem + C::kOffStage + stage * C::kItemBytes;
-                const int ids = kind == 0 ? ids_cur : ids_prev;
-                const int t0 = kind == 0 ? tt * kPfStep + r2 * kPfTile : tt * kPfStep;
-                const int span = kind == 0 ? kPfTile : kPfStep;
-                const int ntok = max(0, min(span, kv - t0));
-                const int nbox = (ntok + BT - 1) >> bsh;
-                const int lane0 = kind == 0 ? (r2 * kPfTile) >> bsh : 0;
-                if (lane == 0) // the whole item, whichever CTA issues each box; an empty K tile completes with none
-                    mbar_arrive_expect_tx(&bars.full[stage], (uint32_t)nbox * (kind == 0 ? kbox : vbox));
-                for (int bx = 0; bx < nbox; ++bx) {
-                    const int page = __shfl_sync(0xffffffffu, ids, lane0 + bx);
-                    if (lane != 0 || (twin && (bx & 1) != share))
-                        continue;
-                    const int slot = (t0 + (bx << bsh)) & (P - 1);
-                    const int c3 = nhd ? (page * P + slot) >> 3 : slot >> 3;
-                    const int c4 = nhd ? g : page * Hkv + g;
-                    uint8_t *bdst = dst + bx * (kind == 0 ? kbox : vbox);
-                    const CUtensorMap *map = kind == 0 ? &maps.k : &maps.v;
-                    const int c2 = kind == 0 ? 0 : r2 * (D / 128);
-                    if (twin)
-                        tma_load_5d_mc(bdst, map, 0, 0, c2, c3, c4, &bars.full[stage], mc);
-                    else
-                        tma_load_5d_local(bdst, map, c2, c3, c4, &bars.full[stage]);
-                }
-                issued = itg + 1;
+        int ids_cur = page_ids(0), ids_next = page_ids(1);
+        for (int t = 0; t < ns; ++t, ++gs) {
+            const int slot = is_k ? C::k_slot(gs) : C::v_slot(gs);
+            const int n = gs / ring;
+            if (n > 0 && !pf_wait_all<true>(&bars.empty[slot], (n - 1) & 1, bars, p.err_flag)) {
+                ok = false;
+                break;
             }
-            ids_prev = ids_cur;
+            uint8_t *dst = smem + C::kOffStage + slot * C::kItemBytes;
+            const int t0 = t * kPfStep + (is_k ? r2 * kPfTile : 0);
+            const int ntok = max(0, min(span, kv - t0));
+            const int nbox = (ntok + BT - 1) >> bsh;
+            if (lane == 0) // the whole item, whichever CTA issues each box; an empty K tile completes with none
+                mbar_arrive_expect_tx(&bars.full[slot], (uint32_t)nbox * box);
+            // lane bx issues box bx (up to 16 per item), all in one warp instruction
+            const int page = __shfl_sync(0xffffffffu, ids_cur, (lane0 + lane) & 31);
+            const int bx = lane;
+            if (bx < nbox && !(twin && (bx & 1) != share)) {
+                const int tslot = (t0 + (bx << bsh)) & (P - 1);
+                const int c3 = nhd ? (page * P + tslot) >> 3 : tslot >> 3;
+                const int c4 = nhd ? g : page * Hkv + g;
+                uint8_t *bdst = dst + bx * box;
+                if (twin)
+                    tma_load_5d_mc(bdst, map, 0, 0, c2, c3, c4, &bars.full[slot], mc);
+                else
+                    tma_load_5d_local(bdst, map, c2, c3, c4, &bars.full[slot]);
+            }
             ids_cur = ids_next;
             ids_next = page_ids(t + 2);
         }
-        ib += 2 * ns;
     }
-    // Copies still in flight, and the pair MMAs still reading the last stages.
-    for (int itg = issued > C::kStages ? issued - C::kStages : 0; itg < issued; ++itg) {
-        pf_wait<true>(&bars.full[itg % C::kStages], (itg / C::kStages) & 1, bars, p.err_flag);
-        pf_wait<true>(&bars.empty[itg % C::kStages], (itg / C::kStages) & 1, bars, p.err_flag);
+    // Copies still in flight into this ring, and the pair MMAs still reading it.
+    for (int j = gs > ring ? gs - ring : 0; j < gs; ++j) {
+        const int slot = is_k ? C::k_slot(j) : C::v_slot(j);
+        const uint32_t par = is_k ? C::k_par(j) : C::v_par(j);
+        pf_wait<true>(&bars.full[slot], par, bars, p.err_flag);
+        pf_wait<true>(&bars.empty[slot], par, bars, p.err_flag);
     }
 }
 
 // The odd CTA's MMA warp (one thread): tells the even CTA's MMA thread, item
-// by item, that this CTA's part of the stage has landed.
+// by item in the order the MMAs read them (K_0, K_1, V_0, K_2, V_1, ...),
+// that this CTA's part of the slot has landed.
 template <int D>
 __device__ void pf2_relay(const PfParams &p, Pf2Bars &bars, int n_units)
 {
     using C = Pf2Cfg<D>;
-    int items = 0;
+    const uint32_t leader = (uint32_t)(cluster_ctarank() & ~1u);
+    int gs0 = 0;
     for (int k = 0;; ++k) {
         const int u = pf_unit_at(k, p.cluster);
         if (u >= n_units)
             break;
-        items += 2 * ((p.units[u / p.num_kv_heads].n_tiles + 1) >> 1);
-    }
-    for (int itg = 0; itg < items; ++itg) {
-        if (!pf_wait<true>(&bars.full[itg % C::kStages], (itg / C::kStages) & 1, bars, p.err_flag))
-            return;
-        mbar_arrive_remote(&bars.peer_full[itg % C::kStages], (uint32_t)(cluster_ctarank() & ~1u));
+        const int ns = (p.units[u / p.num_kv_heads].n_tiles + 1) >> 1;
+        for (int t = 0; t <= ns; ++t) {
+            if (t < ns) {
+                const int gs = gs0 + t;
+                if (!pf_wait<true>(&bars.full[C::k_slot(gs)], C::k_par(gs), bars, p.err_flag))
+                    return;
+                mbar_arrive_remote(&bars.peer_full[C::k_slot(gs)], leader);
+            }
+            if (t >= 1) {
+                const int gs = gs0 + t - 1;
+                if (!pf_wait<true>(&bars.full[C::v_slot(gs)], C::v_par(gs), bars, p.err_flag))
+                    return;
+                mbar_arrive_remote(&bars.peer_full[C::v_slot(gs)], leader);
+            }
+        }
+        gs0 += ns;
     }
 }
 
@@ -915,14 +934,12 @@ __device__ void pf2_mma(const PfParams &p, uint8_t *smem, Pf2Bars &bars, uint32_
     const uint16_t kAll = (uint16_t)((1u << p.cluster) - 1u); // every CTA a stage's loads reach
     const uint32_t st_base = smem_addr(smem + C::kOffStage);
     const uint64_t qd = tc_sw128_desc(smem_addr(smem + C::kOffQ), 16, C::kGroupStride);
-    int ib = 0, gs0 = 0;
+    int gs0 = 0;
     uint32_t uc = 0;
     bool issued = false;
-    auto stage_ready = [&](int itg) {
-        const int stage = itg % C::kStages;
-        const uint32_t par = (itg / C::kStages) & 1;
-        return pf_wait<true>(&bars.full[stage], par, bars, p.err_flag) &&
-               pf_wait<true>(&bars.peer_full[stage], par, bars, p.err_flag);
+    auto slot_ready = [&](int slot, uint32_t par) {
+        return pf_wait<true>(&bars.full[slot], par, bars, p.err_flag) &&
+               pf_wait<true>(&bars.peer_full[slot], par, bars, p.err_flag);
     };
     for (int k = 0;; ++k) {
         const int u = pf_unit_at(k, p.cluster);
@@ -934,9 +951,8 @@ __device__ void pf2_mma(const PfParams &p, uint8_t *smem, Pf2Bars &bars, uint32_
         for (int t = 0; t <= ns; ++t) {
             if (t < ns) { // S[gs & 1] = Q K_t^T
                 const int gs = gs0 + t;
-                const int itg = ib + pf_item_k(t);
-                const int stage = itg % C::kStages;
-                if (!stage_ready(itg))
+                const int stage = C::k_slot(gs);
+                if (!slot_ready(stage, C::k_par(gs)))
                     goto done;
                 tc_fence_after();
                 issued = true;
@@ -958,9 +974,8 @@ __device__ void pf2_mma(const PfParams &p, uint8_t *smem, Pf2Bars &bars, uint32_
                     goto done;
                 if (tv == 0 && uc > 0 && !pf_wait<true>(&bars.o_free, (uc - 1) & 1, bars, p.err_flag))
                     goto done;
-                const int itg = ib + pf_item_v(tv, ns);
-                const int stage = itg % C::kStages;
-                if (!stage_ready(itg))
+                const int stage = C::v_slot(gs);
+                if (!slot_ready(stage, C::v_par(gs)))
                     goto done;
                 tc_fence_after();
                 const uint32_t pt = tmem + C::kColS + (uint32_t)(gs & 1) * kPfStep; // P of step gs
@@ -978,7 +993,6 @@ __device__ void pf2_mma(const PfParams &p, uint8_t *smem, Pf2Bars &bars, uint32_
             }
         }
         gs0 += ns;
-        ib += 2 * ns;
         ++uc;
     }
 done:
@@ -1037,7 +1051,7 @@ __device__ void pf2_softmax(const PfParams &p, uint8_t *smem, Pf2Bars &bars, uin
     const int h_in_group = r & (G - 1);
     const float qs = p.q_scale;
     const float qse = qs > 0.f ? qs : 1.f;
-    int ib = 0, gs0 = 0;
+    int gs0 = 0;
     uint32_t pair_phase = 0;
 
     int u = pf_unit_at(0, p.cluster);
@@ -1153,9 +1167,8 @@ __device__ void pf2_softmax(const PfParams &p, uint8_t *smem, Pf2Bars &bars, uin
             }
             // V rows at and past kv in the step hold another token's or no data: zero them
             if (j * kPfStep + kPfStep > kv) {
-                const int itg = ib + pf_item_v(j, ns);
-                const int stage = itg % C::kStages;
-                if (!pf_wait_all<true>(&bars.full[stage], (itg / C::kStages) & 1, bars, p.err_flag))
+                const int stage = C::v_slot(gs);
+                if (!pf_wait_all<true>(&bars.full[stage], C::v_par(gs), bars, p.err_flag))
                     return;
                 const int r0 = kv - j * kPfStep;
                 uint8_t *vb = smem + C::kOffStage + stage * C::kItemBytes;
@@ -1218,12 +1231,11 @@ __device__ void pf2_softmax(const PfParams &p, uint8_t *smem, Pf2Bars &bars, uin
                 p.lse[row] = (m_used + log2f(lt)) * kLn2;
         }
         gs0 += ns;
-        ib += 2 * ns;
     }
 }
 
 template <int D>
-__global__ void __launch_bounds__(kPfThreads, 1)
+__global__ void __launch_bounds__(kPf2Threads, 1)
     prefill2_kernel(const __grid_constant__ PfParams p, const __grid_constant__ PfMapsDev maps)
 {
     using C = Pf2Cfg<D>;
@@ -1268,8 +1280,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     const uint32_t tmem = bars.tmem_base;
     const int n_units = *p.n_pairs * p.num_kv_heads;
 
-    if (warp == kPfProducerWarp)
-        pf2_producer<D>(p, maps, smem, bars, n_units, lane, rank);
+    if (warp == kPfProducerWarp || warp == kPf2VWarp)
+        pf2_producer<D>(p, maps, smem, bars, n_units, lane, rank, warp == kPfProducerWarp ? 0 : 1);
     else if (warp == kPfMmaWarp) {
         if (lane == 0) {
             if ((rank & 1) == 0)
@@ -1510,14 +1522,15 @@ struct PfKernelEntry {
     int cluster; // CTAs per cluster (one query tile each)
     const void *fn;
     uint32_t smem;
+    int threads;
 };
 
 // head_dim 64 cannot be split into 64-column halves: one CTA per query tile,
 // K / V shared by the cluster through TMA multicast.  128 and 256: CTA pairs.
 const PfKernelEntry kPfTable[] = {
-    {64, false, 2, reinterpret_cast<const void *>(&prefill_kernel<64>), PfCfg<64>::kSmem},
-    {128, true, 4, reinterpret_cast<const void *>(&prefill2_kernel<128>), Pf2Cfg<128>::kSmem},
-    {256, true, 2, reinterpret_cast<const void *>(&prefill2_kernel<256>), Pf2Cfg<256>::kSmem},
+    {64, false, 2, reinterpret_cast<const void *>(&prefill_kernel<64>), PfCfg<64>::kSmem, kPfThreads},
+    {128, true, 4, reinterpret_cast<const void *>(&prefill2_kernel<128>), Pf2Cfg<128>::kSmem, kPf2Threads},
+    {256, true, 2, reinterpret_cast<const void *>(&prefill2_kernel<256>), Pf2Cfg<256>::kSmem, kPf2Threads},
 };
 
 const PfKernelEntry *pf_find(int D)
@@ -1542,7 +1555,7 @@ int pf_grid(int device, const PfKernelEntry *e, int cl)
         if (cudaFuncSetAttribute(e->fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)e->smem) == cudaSuccess) {
             cudaLaunchConfig_t cfg = {};
             cfg.gridDim = dim3(sm_count(device));
-            cfg.blockDim = dim3(kPfThreads);
+            cfg.blockDim = dim3(e->threads);
             cfg.dynamicSmemBytes = e->smem;
             cudaLaunchAttribute attr[1];
             attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -1663,7 +1676,7 @@ cudaError_t launch_prefill(const PrefillArgs &a, const PrefillMaps &maps, cudaSt
     void *args[] = {&p, &m};
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(kPfThreads);
+    cfg.blockDim = dim3(e->threads);
     cfg.dynamicSmemBytes = e->smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];

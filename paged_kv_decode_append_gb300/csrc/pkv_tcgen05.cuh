@@ -320,18 +320,6 @@ __device__ __forceinline__ void mbar_arrive_remote(uint64_t *bar, uint32_t rank)
                  "r"(rank)
                  : "memory");
 }
-// try_wait with acquire at cluster scope: for barriers other CTAs arrive on.
-__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t *bar, uint32_t parity)
-{
-    uint32_t done;
-    asm volatile("{\n\t.reg .pred p;\n\t"
-                 "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-                 "selp.u32 %0, 1, 0, p;\n\t}"
-                 : "=r"(done)
-                 : "r"(smem_addr(bar)), "r"(parity)
-                 : "memory");
-    return done != 0;
-}
 // 5-D tiled TMA load into this CTA's shared memory (default L2 policy); c2
 // selects the first 64-column block.
 __device__ __forceinline__ void tma_load_5d_local(void *dst, const CUtensorMap *map, int c2, int c3, int c4,
