@@ -582,6 +582,7 @@ pkv_status pkv_mixed_attn(const pkv_cache_desc *desc, void *k_cache, void *v_cac
     // 3. longer rows (prefill chunks): the tcgen05 prefill kernel over kv = L + q keys
     if (m.prefill) {
         pa.phase = kPrefillMain;
+        pa.overlap_prior = true; // the decode kernel waited for the append, which waited for the plan
         if (launch_prefill(pa, pmaps, s) != cudaSuccess)
             return PKV_ECUDA;
     }

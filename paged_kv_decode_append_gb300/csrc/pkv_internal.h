@@ -187,6 +187,10 @@ struct PrefillArgs {
     // Launches: kPrefillAll = the plan kernel then the attention kernel;
     // kPrefillPlan / kPrefillMain one of them (the same arguments for both).
     int phase = 0;
+    // kPrefillMain only: the preceding kernel in the stream is one of this
+    // library's that waits (transitively) for the plan, so the attention
+    // kernel may start its set-up before that kernel ends.
+    bool overlap_prior = false;
 };
 
 constexpr int kPrefillAll = 0, kPrefillPlan = 1, kPrefillMain = 2;

@@ -173,6 +173,7 @@ struct PfParams {
     int group_shift, q_tile, page_shift, box_shift, layout;
     int cluster; // CTAs per cluster sharing every K / V tile (1, 2 or 4)
     float q_scale;
+    int pdl; // launched as a programmatic dependent: set up, then wait for the preceding grid
 };
 
 struct PfMapsDev {
@@ -774,6 +775,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     else
         __syncthreads();
     tc_fence_after();
+    if (p.pdl) // the plan (and, in a mixed step, the append) wrote what follows
+        asm volatile("griddepcontrol.wait;" ::: "memory");
     const uint32_t tmem = bars.tmem_base;
     const int n_units = *p.n_pairs * p.num_kv_heads;
 
@@ -1277,6 +1280,8 @@ __global__ void __launch_bounds__(kPf2Threads, 1)
     tc_fence_before();
     cluster_sync(); // both CTAs' barriers and TMEM are ready before anything crosses over
     tc_fence_after();
+    if (p.pdl) // the plan (and, in a mixed step, the append) wrote what follows
+        asm volatile("griddepcontrol.wait;" ::: "memory");
     const uint32_t tmem = bars.tmem_base;
     const int n_units = *p.n_pairs * p.num_kv_heads;
 
@@ -1658,6 +1663,9 @@ cudaError_t launch_prefill(const PrefillArgs &a, const PrefillMaps &maps, cudaSt
     p.layout = a.desc.layout;
     p.cluster = e->cluster;
     p.q_scale = a.q_scale;
+    // after this call's own plan kernel, or after a kernel of ours that
+    // waits for it (the mixed step's decode): set-up overlaps its end
+    p.pdl = (a.phase == kPrefillAll || a.overlap_prior) ? 1 : 0;
     PfMapsDev m;
     m.k = maps.k;
     m.v = maps.v;
@@ -1679,13 +1687,18 @@ cudaError_t launch_prefill(const PrefillArgs &a, const PrefillMaps &maps, cudaSt
     cfg.blockDim = dim3(e->threads);
     cfg.dynamicSmemBytes = e->smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = cl;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    if (p.pdl) {
+        attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[1].val.programmaticStreamSerializationAllowed = 1;
+        cfg.numAttrs = 2;
+    }
     return cudaLaunchKernelExC(&cfg, e->fn, args);
 }
 
