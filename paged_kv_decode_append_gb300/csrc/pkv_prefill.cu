@@ -1031,6 +1031,28 @@ __device__ __forceinline__ void pf2_load_q(const PfParams &p, const PfUnit &un, 
     }
 }
 
+// The same rows with asynchronous copies (cp.async, zeros for rows past
+// total_q): issued while the softmax of the unit's last step runs, completed
+// by cp_async_wait_all before the MMA thread is told.
+template <int D>
+__device__ __forceinline__ void pf2_load_q_async(const PfParams &p, const PfUnit &un, int g, int r, int half,
+                                                 uint8_t *q_smem, int rank)
+{
+    using C = Pf2Cfg<D>;
+    const int tok = un.q_start + (un.t * p.cluster + rank) * p.q_tile + (r >> p.group_shift);
+    const int head = g * (1 << p.group_shift) + (r & ((1 << p.group_shift) - 1));
+    const bool in = tok < p.total_q;
+    const uint4 *src =
+        reinterpret_cast<const uint4 *>(p.q + ((int64_t)(in ? tok : 0) * p.num_q_heads + head) * D + half * (D / 2));
+    constexpr int kLoads = D / 16; // 16-byte chunks of half a row
+    uint8_t *row = q_smem + (r >> 3) * C::kGroupStride + (r & 7) * 128;
+#pragma unroll
+    for (int i = 0; i < kLoads; ++i) {
+        const int c = half * kLoads + i; // chunk of the row: block c / 8, 16-byte column c % 8
+        cp_async16(row + (c >> 3) * 1024 + (((c & 7) ^ (r & 7)) << 4), src + i, in ? 16u : 0u);
+    }
+}
+
 // Softmax warps of one CTA of a pair, step by step: the same online softmax
 // as pf_softmax over 128-column S buffers.  Thread half h owns S columns
 // [64 h, 64 h + 64) in two 32-column chunks; chunk c's P is written over its
@@ -1085,6 +1107,11 @@ __device__ void pf2_softmax(const PfParams &p, uint8_t *smem, Pf2Bars &bars, uin
             if (!pf_wait_all<true>(&bars.s_full[gs & 1], (gs >> 1) & 1, bars, p.err_flag))
                 return;
             tc_fence_after();
+            if (j == ns - 1 && u_next < n_units) {
+                // this step's S MMAs were the unit's last reads of Q: fetch the next unit's
+                const int pn = u_next / p.num_kv_heads;
+                pf2_load_q_async<D>(p, p.units[pn], u_next - pn * p.num_kv_heads, r, half, q_smem, rank);
+            }
             const uint32_t s_col = C::kColS + (uint32_t)(gs & 1) * kPfStep + half * (kPfStep / 2);
             const bool masked = j * kPfStep + kPfStep - 1 > limit_min;
             // raw scores of chunk c (a non-positive scale applied here, a positive one in the exponent)
@@ -1186,12 +1213,11 @@ __device__ void pf2_softmax(const PfParams &p, uint8_t *smem, Pf2Bars &bars, uin
             tc_fence_before();
             pf_arrive_mma<true>(&bars.p_full[gs & 1], lane, rank);
         }
-        // The next unit's Q, once this unit's S MMAs have read the current one.
+        // The next unit's Q (copies issued at the last step) has landed.
         if (u_next < n_units) {
             if (!pf_wait_all<true>(&bars.q_empty, k & 1, bars, p.err_flag))
                 return;
-            const int pn = u_next / p.num_kv_heads;
-            pf2_load_q<D>(p, p.units[pn], u_next - pn * p.num_kv_heads, r, half, q_smem, rank);
+            cp_async_wait_all();
             fence_proxy_async_smem();
             pf_arrive_mma<true>(&bars.q_full, lane, rank);
         }
@@ -1295,8 +1321,10 @@ __global__ void __launch_bounds__(kPf2Threads, 1)
                 pf2_relay<D>(p, bars, n_units);
         }
         __syncwarp();
-    } else
+    } else {
         pf2_softmax<D>(p, smem, bars, tmem, n_units, warp, lane, rank);
+        cp_async_wait_all(); // a Q prefetch left in flight by an aborted unit
+    }
 
     tc_fence_before();
     cluster_sync(); // the pair's last MMAs (on both CTAs' smem and TMEM) are complete
