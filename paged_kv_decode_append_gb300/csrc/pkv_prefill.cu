@@ -31,11 +31,12 @@
 //  - head_dim 64 (prefill_kernel): one query tile per CTA, 64-key tiles,
 //    K / V shared by the cluster through TMA multicast, Q in TMEM.
 //  - Warp roles: warp 0 loads this CTA's K and V with TMA into a ring of
-//    shared-memory stages (in the order the MMAs consume them); warp 1 owns
-//    TMEM and one of its threads issues the MMAs (the odd CTA of a pair:
-//    relays its stage completions to it); warps 2-9 (two per TMEM lane
-//    quarter) run the online softmax and the epilogue, each thread on half
-//    of its row's columns.
+//    shared-memory stages (head_dim 64, in the order the MMAs consume them;
+//    CTA pairs: warp 0 the K ring, warp 10 the V ring); warp 1 owns TMEM and
+//    one of its threads issues the MMAs (the odd CTA of a pair: relays its
+//    stage completions to it); warps 2-9 (two per TMEM lane quarter) run the
+//    online softmax and the epilogue, each thread on half of its row's
+//    columns.
 //  - The softmax writes P back over the S columns it has just read, as two
 //    bf16 parts, p = hi + lo (about 16 significant bits: a single bf16 P
 //    alone, 8 bits, leaves errors near 2^-9 of the row's scale, well above
@@ -171,7 +172,7 @@ struct PfParams {
     int32_t *err_flag;
     int max_blocks, num_q_heads, num_kv_heads, total_q;
     int group_shift, q_tile, page_shift, box_shift, layout;
-    int cluster; // CTAs per cluster sharing every K / V tile (1, 2 or 4)
+    int cluster; // CTAs per cluster (1 or 2): a pair, or two single CTAs sharing every K / V tile
     float q_scale;
     int pdl; // launched as a programmatic dependent: set up, then wait for the preceding grid
 };
@@ -805,13 +806,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
 // loads the K items, warp 1 the V items, each into a ring of its own.  Item
 // K_t is the step's tile 2t + r (r = the CTA's rank in its pair), 64 keys
 // with all of head_dim; item V_t is all 128 keys of the step with columns
-// [r D/2, (r+1) D/2).  Boxes of min(page, 64) tokens, one lane per box.
-// With clusters of two pairs on consecutive query tiles of the same
-// (request, kv head), CTA c and CTA c ^ 2 need the same items, so each loads
-// half of every item's boxes with TMA multicast into both (the same
-// shared-memory offset, completing on both full barriers) -- half the TMA
-// issues per SM, which pays where the boxes are small (head_dim 128).  A slot
-// is refilled once every pair's MMA that read it has completed.
+// [r D/2, (r+1) D/2).  Boxes of min(page, 64) tokens, one lane per box.  A
+// slot is refilled once the pair's MMAs that read it have completed.
 template <int D>
 __device__ void pf2_producer(const PfParams &p, const PfMapsDev &maps, uint8_t *smem, Pf2Bars &bars, int n_units,
                              int lane, int rank, int which)
@@ -827,9 +823,6 @@ __device__ void pf2_producer(const PfParams &p, const PfMapsDev &maps, uint8_t *
     const int ring = is_k ? C::kKStages : C::kVStages;
     const bool nhd = p.layout == PKV_NHD;
     const int r2 = rank & 1;                                   // rank in the pair
-    const bool twin = p.cluster == 4;                          // a second pair shares every item
-    const uint16_t mc = (uint16_t)((1u << rank) | (1u << (rank ^ 2))); // this CTA and its twin in the other pair
-    const int share = rank >> 1;                              // which half of each item's boxes this CTA issues
     const int c2 = is_k ? 0 : r2 * (D / 128);                 // V: this CTA's 64-column blocks
     const int span = is_k ? kPfTile : kPfStep;                // tokens of an item
     const int lane0 = is_k ? (r2 * kPfTile) >> bsh : 0;       // page lane of the item's first box
@@ -863,20 +856,17 @@ __device__ void pf2_producer(const PfParams &p, const PfMapsDev &maps, uint8_t *
             const int t0 = t * kPfStep + (is_k ? r2 * kPfTile : 0);
             const int ntok = max(0, min(span, kv - t0));
             const int nbox = (ntok + BT - 1) >> bsh;
-            if (lane == 0) // the whole item, whichever CTA issues each box; an empty K tile completes with none
+            if (lane == 0) // the whole item; an empty K tile completes with none
                 mbar_arrive_expect_tx(&bars.full[slot], (uint32_t)nbox * box);
             // lane bx issues box bx (up to 16 per item), all in one warp instruction
             const int page = __shfl_sync(0xffffffffu, ids_cur, (lane0 + lane) & 31);
             const int bx = lane;
-            if (bx < nbox && !(twin && (bx & 1) != share)) {
+            if (bx < nbox) {
                 const int tslot = (t0 + (bx << bsh)) & (P - 1);
                 const int c3 = nhd ? (page * P + tslot) >> 3 : tslot >> 3;
                 const int c4 = nhd ? g : page * Hkv + g;
                 uint8_t *bdst = dst + bx * box;
-                if (twin)
-                    tma_load_5d_mc(bdst, map, 0, 0, c2, c3, c4, &bars.full[slot], mc);
-                else
-                    tma_load_5d_local(bdst, map, c2, c3, c4, &bars.full[slot]);
+                tma_load_5d_local(bdst, map, c2, c3, c4, &bars.full[slot]);
             }
             ids_cur = ids_next;
             ids_next = page_ids(t + 2);
@@ -934,7 +924,6 @@ __device__ void pf2_mma(const PfParams &p, uint8_t *smem, Pf2Bars &bars, uint32_
     constexpr uint32_t kIdescS = tc_idesc_bf16(2 * kPfRows, kPfStep, false, false);
     constexpr uint32_t kIdescO = tc_idesc_bf16(2 * kPfRows, D, false, true);
     const uint16_t kBoth = (uint16_t)(3u << (cluster_ctarank() & ~1u)); // this pair
-    const uint16_t kAll = (uint16_t)((1u << p.cluster) - 1u); // every CTA a stage's loads reach
     const uint32_t st_base = smem_addr(smem + C::kOffStage);
     const uint64_t qd = tc_sw128_desc(smem_addr(smem + C::kOffQ), 16, C::kGroupStride);
     int gs0 = 0;
@@ -967,7 +956,7 @@ __device__ void pf2_mma(const PfParams &p, uint8_t *smem, Pf2Bars &bars, uint32_
                     tc_mma_bf16_ss_pair(d, qd + off, kd + off, kIdescS, kk > 0 ? 1u : 0u);
                 }
                 tc_commit_pair_mc(&bars.s_full[gs & 1], kBoth);
-                tc_commit_pair_mc(&bars.empty[stage], kAll);
+                tc_commit_pair_mc(&bars.empty[stage], kBoth);
                 if (t == ns - 1)
                     tc_commit_pair_mc(&bars.q_empty, kBoth);
             }
@@ -992,7 +981,7 @@ __device__ void pf2_mma(const PfParams &p, uint8_t *smem, Pf2Bars &bars, uint32_
                                         kIdescO, (tv > 0 || kk > 0) ? 1u : 0u);
                 }
                 tc_commit_pair_mc(&bars.o_done[gs & 1], kBoth);
-                tc_commit_pair_mc(&bars.empty[stage], kAll);
+                tc_commit_pair_mc(&bars.empty[stage], kBoth);
             }
         }
         gs0 += ns;
@@ -1272,7 +1261,7 @@ __global__ void __launch_bounds__(kPf2Threads, 1)
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(pf_smem_raw) + 1023) & ~uintptr_t(1023));
     Pf2Bars &bars = *reinterpret_cast<Pf2Bars *>(smem + C::kOffBar);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int rank = (int)cluster_ctarank(); // pairs are CTAs 0-1 (and 2-3)
+    const int rank = (int)cluster_ctarank(); // 0: the even CTA of the pair, 1: the odd one
     constexpr int kWarpArrivals = 2 * kPfSoftmaxWarps; // per-warp arrivals of both CTAs' softmax warps
 
     if (threadIdx.x == 0) {
@@ -1280,7 +1269,7 @@ __global__ void __launch_bounds__(kPf2Threads, 1)
         mbar_init(&bars.q_empty, 1);
         for (int s = 0; s < C::kStages; ++s) {
             mbar_init(&bars.full[s], 1);
-            mbar_init(&bars.empty[s], p.cluster / 2); // the MMA thread of every pair
+            mbar_init(&bars.empty[s], 1); // the pair's MMA thread
             mbar_init(&bars.peer_full[s], 1);
         }
         for (int i = 0; i < 2; ++i) {
@@ -1562,7 +1551,7 @@ struct PfKernelEntry {
 // K / V shared by the cluster through TMA multicast.  128 and 256: CTA pairs.
 const PfKernelEntry kPfTable[] = {
     {64, false, 2, reinterpret_cast<const void *>(&prefill_kernel<64>), PfCfg<64>::kSmem, kPfThreads},
-    {128, true, 4, reinterpret_cast<const void *>(&prefill2_kernel<128>), Pf2Cfg<128>::kSmem, kPf2Threads},
+    {128, true, 2, reinterpret_cast<const void *>(&prefill2_kernel<128>), Pf2Cfg<128>::kSmem, kPf2Threads},
     {256, true, 2, reinterpret_cast<const void *>(&prefill2_kernel<256>), Pf2Cfg<256>::kSmem, kPf2Threads},
 };
 
