@@ -787,7 +787,8 @@ def main():
                      "peak_kind": peak_kind, "kernel": "pkv::decode_kernel<128,4>",
                      "algorithmic_bytes_per_launch": launch_bytes, "launch_ms_mean": kernel_ms,
                      "isolated_launch_ms_mean": float(iso_ms.mean()), "isolated_launch_ms_best": float(iso_ms.min()),
-                     "isolated_gbs": iso_gbs, "isolated_launches": int(iso_ms.size)},
+                     "isolated_gbs": iso_gbs, "isolated_launches": int(iso_ms.size),
+                     "isolated_steps": f"decode steps 0..{iso_steps - 1} (shorter caches than the timed region's mean)"},
         "clocks": clocks.summary(),
         "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "steps": e2e_steps,
