@@ -123,6 +123,10 @@ template <int D> struct Pf2Cfg {
     static __device__ __forceinline__ uint32_t k_par(int gs) { return (uint32_t)(gs / kKStages) & 1u; }
     static __device__ __forceinline__ int v_slot(int gs) { return kKStages + gs % kVStages; }
     static __device__ __forceinline__ uint32_t v_par(int gs) { return (uint32_t)(gs / kVStages) & 1u; }
+    // Rings of two slots: the item of step gs - 2 is the slot's previous one,
+    // and the step's own completion barrier (s_full / o_done of parity gs & 1,
+    // phase gs >> 1) releases it -- no separate commit to an empty barrier.
+    static constexpr bool kStepRelease = kKStages == 2 && kVStages == 2;
     static constexpr uint32_t kGroupStride = 8 * D * 2;            // K and Q: 8 rows x head_dim
     static constexpr uint32_t kVGroupStride = 8 * (D / 2) * 2;     // V half: 8 keys x half of head_dim
     static constexpr int kVChunks = D / 128;                       // 64-column blocks of a V half
@@ -826,6 +830,19 @@ __device__ void pf2_producer(const PfParams &p, const PfMapsDev &maps, uint8_t *
     const int c2 = is_k ? 0 : r2 * (D / 128);                 // V: this CTA's 64-column blocks
     const int span = is_k ? kPfTile : kPfStep;                // tokens of an item
     const int lane0 = is_k ? (r2 * kPfTile) >> bsh : 0;       // page lane of the item's first box
+    // barrier (and parity) that completes once the pair's MMAs have read the item of step j
+    auto released = [&](int j) -> uint64_t * {
+        if constexpr (C::kStepRelease)
+            return is_k ? &bars.s_full[j & 1] : &bars.o_done[j & 1];
+        else
+            return &bars.empty[is_k ? C::k_slot(j) : C::v_slot(j)];
+    };
+    auto released_par = [&](int j) -> uint32_t {
+        if constexpr (C::kStepRelease)
+            return (uint32_t)(j >> 1) & 1u;
+        else
+            return is_k ? C::k_par(j) : C::v_par(j);
+    };
     int gs = 0; // items issued so far (one per step)
     bool ok = true;
     for (int k = 0; ok; ++k) {
@@ -847,8 +864,7 @@ __device__ void pf2_producer(const PfParams &p, const PfMapsDev &maps, uint8_t *
         int ids_cur = page_ids(0), ids_next = page_ids(1);
         for (int t = 0; t < ns; ++t, ++gs) {
             const int slot = is_k ? C::k_slot(gs) : C::v_slot(gs);
-            const int n = gs / ring;
-            if (n > 0 && !pf_wait_all<true>(&bars.empty[slot], (n - 1) & 1, bars, p.err_flag)) {
+            if (gs >= ring && !pf_wait_all<true>(released(gs - ring), released_par(gs - ring), bars, p.err_flag)) {
                 ok = false;
                 break;
             }
@@ -877,7 +893,7 @@ __device__ void pf2_producer(const PfParams &p, const PfMapsDev &maps, uint8_t *
         const int slot = is_k ? C::k_slot(j) : C::v_slot(j);
         const uint32_t par = is_k ? C::k_par(j) : C::v_par(j);
         pf_wait<true>(&bars.full[slot], par, bars, p.err_flag);
-        pf_wait<true>(&bars.empty[slot], par, bars, p.err_flag);
+        pf_wait<true>(released(j), released_par(j), bars, p.err_flag);
     }
 }
 
@@ -956,7 +972,8 @@ __device__ void pf2_mma(const PfParams &p, uint8_t *smem, Pf2Bars &bars, uint32_
                     tc_mma_bf16_ss_pair(d, qd + off, kd + off, kIdescS, kk > 0 ? 1u : 0u);
                 }
                 tc_commit_pair_mc(&bars.s_full[gs & 1], kBoth);
-                tc_commit_pair_mc(&bars.empty[stage], kBoth);
+                if constexpr (!C::kStepRelease)
+                    tc_commit_pair_mc(&bars.empty[stage], kBoth);
                 if (t == ns - 1)
                     tc_commit_pair_mc(&bars.q_empty, kBoth);
             }
@@ -981,7 +998,8 @@ __device__ void pf2_mma(const PfParams &p, uint8_t *smem, Pf2Bars &bars, uint32_
                                         kIdescO, (tv > 0 || kk > 0) ? 1u : 0u);
                 }
                 tc_commit_pair_mc(&bars.o_done[gs & 1], kBoth);
-                tc_commit_pair_mc(&bars.empty[stage], kBoth);
+                if constexpr (!C::kStepRelease)
+                    tc_commit_pair_mc(&bars.empty[stage], kBoth);
             }
         }
         gs0 += ns;
