@@ -113,7 +113,7 @@ constexpr int kPfStep = 2 * kPfTile; // keys per step
 template <int D> struct Pf2Cfg {
     static_assert(D == 128 || D == 256, "pairs split head_dim into 64-column blocks");
     static constexpr uint32_t kItemBytes = kPfTile * D * 2;
-    static constexpr int kStages = D == 256 ? 4 : 11;              // items in flight
+    static constexpr int kStages = 4;                              // items in flight
     // K items (one per step) and V items (one per step) have rings of their
     // own, each filled by its own producer warp: the step's index gs picks
     // the slot, K in [0, kKStages), V in [kKStages, kStages).
