@@ -126,7 +126,7 @@ template <int D> struct Pf2Cfg {
     // Rings of two slots: the item of step gs - 2 is the slot's previous one,
     // and the step's own completion barrier (s_full / o_done of parity gs & 1,
     // phase gs >> 1) releases it -- no separate commit to an empty barrier.
-    static constexpr bool kStepRelease = kKStages == 2 && kVStages == 2;
+    static_assert(kKStages == 2 && kVStages == 2, "slots are released by the step barriers");
     static constexpr uint32_t kGroupStride = 8 * D * 2;            // K and Q: 8 rows x head_dim
     static constexpr uint32_t kVGroupStride = 8 * (D / 2) * 2;     // V half: 8 keys x half of head_dim
     static constexpr int kVChunks = D / 128;                       // 64-column blocks of a V half
@@ -831,18 +831,8 @@ __device__ void pf2_producer(const PfParams &p, const PfMapsDev &maps, uint8_t *
     const int span = is_k ? kPfTile : kPfStep;                // tokens of an item
     const int lane0 = is_k ? (r2 * kPfTile) >> bsh : 0;       // page lane of the item's first box
     // barrier (and parity) that completes once the pair's MMAs have read the item of step j
-    auto released = [&](int j) -> uint64_t * {
-        if constexpr (C::kStepRelease)
-            return is_k ? &bars.s_full[j & 1] : &bars.o_done[j & 1];
-        else
-            return &bars.empty[is_k ? C::k_slot(j) : C::v_slot(j)];
-    };
-    auto released_par = [&](int j) -> uint32_t {
-        if constexpr (C::kStepRelease)
-            return (uint32_t)(j >> 1) & 1u;
-        else
-            return is_k ? C::k_par(j) : C::v_par(j);
-    };
+    auto released = [&](int j) { return is_k ? &bars.s_full[j & 1] : &bars.o_done[j & 1]; };
+    auto released_par = [&](int j) { return (uint32_t)(j >> 1) & 1u; };
     int gs = 0; // items issued so far (one per step)
     bool ok = true;
     for (int k = 0; ok; ++k) {
@@ -971,11 +961,7 @@ __device__ void pf2_mma(const PfParams &p, uint8_t *smem, Pf2Bars &bars, uint32_
                     const uint64_t off = (uint64_t)(((kk >> 2) * 1024 + (kk & 3) * 32) >> 4);
                     tc_mma_bf16_ss_pair(d, qd + off, kd + off, kIdescS, kk > 0 ? 1u : 0u);
                 }
-                tc_commit_pair_mc(&bars.s_full[gs & 1], kBoth);
-                if constexpr (!C::kStepRelease)
-                    tc_commit_pair_mc(&bars.empty[stage], kBoth);
-                if (t == ns - 1)
-                    tc_commit_pair_mc(&bars.q_empty, kBoth);
+                tc_commit_pair_mc(&bars.s_full[gs & 1], kBoth); // the last one also frees Q
             }
             if (t >= 1) { // O += P_{t-1} V_{t-1}
                 const int tv = t - 1, gs = gs0 + tv;
@@ -998,8 +984,6 @@ __device__ void pf2_mma(const PfParams &p, uint8_t *smem, Pf2Bars &bars, uint32_
                                         kIdescO, (tv > 0 || kk > 0) ? 1u : 0u);
                 }
                 tc_commit_pair_mc(&bars.o_done[gs & 1], kBoth);
-                if constexpr (!C::kStepRelease)
-                    tc_commit_pair_mc(&bars.empty[stage], kBoth);
             }
         }
         gs0 += ns;
@@ -1222,8 +1206,6 @@ __device__ void pf2_softmax(const PfParams &p, uint8_t *smem, Pf2Bars &bars, uin
         }
         // The next unit's Q (copies issued at the last step) has landed.
         if (u_next < n_units) {
-            if (!pf_wait_all<true>(&bars.q_empty, k & 1, bars, p.err_flag))
-                return;
             cp_async_wait_all();
             fence_proxy_async_smem();
             pf_arrive_mma<true>(&bars.q_full, lane, rank);
@@ -1284,10 +1266,8 @@ __global__ void __launch_bounds__(kPf2Threads, 1)
 
     if (threadIdx.x == 0) {
         mbar_init(&bars.q_full, kWarpArrivals);
-        mbar_init(&bars.q_empty, 1);
         for (int s = 0; s < C::kStages; ++s) {
             mbar_init(&bars.full[s], 1);
-            mbar_init(&bars.empty[s], 1); // the pair's MMA thread
             mbar_init(&bars.peer_full[s], 1);
         }
         for (int i = 0; i < 2; ++i) {
