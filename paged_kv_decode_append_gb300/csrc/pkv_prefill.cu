@@ -134,7 +134,10 @@ template <int D> struct Pf2Cfg {
     static constexpr uint32_t kOffQ = kOffStage + kStages * kItemBytes;  // Q [128 rows][head_dim], K-major, swizzled
     static constexpr uint32_t kOffBar = kOffQ + kPfRows * D * 2;
     static constexpr uint32_t kOffXchg = kOffBar + 1024;
-    static constexpr uint32_t kSmem = kOffXchg + 3 * 1024 + 1024;
+    // epilogue staging: per softmax warp 32 rows x 32 bf16 columns (2 KB), so
+    // that the global stores of out are row-contiguous 64-byte pieces
+    static constexpr uint32_t kOffOut = kOffXchg + 3 * 1024;
+    static constexpr uint32_t kSmem = kOffOut + kPfSoftmaxWarps * 2048 + 1024;
     static constexpr uint32_t kColO = 0;
     static constexpr uint32_t kColS = D;                           // two S buffers of kPfStep columns
     static constexpr uint32_t kTmemCols = 512;
@@ -1224,7 +1227,13 @@ __device__ void pf2_softmax(const PfParams &p, uint8_t *smem, Pf2Bars &bars, uin
             tc_fence_after();
             const float inv = lt > 0.f ? 1.f / lt : 0.f;
             const int64_t row = (int64_t)(un.q_start + qi) * p.num_q_heads + g * G + h_in_group;
-            __nv_bfloat16 *orow = p.out + row * D;
+            // Chunk by chunk (32 columns): every thread's 64 bytes of its row into
+            // the warp's staging block (16-byte pieces XOR-swizzled by row), then
+            // 4 store rounds in which lanes 4 i .. 4 i + 3 write row 8 s + i's 64
+            // contiguous bytes -- 8 full 64-byte pieces per instruction instead
+            // of 32 scattered 16-byte ones.
+            uint8_t *stg = smem + C::kOffOut + (warp - 2) * 2048;
+            const int pc = lane & 3;
             for (int c = half * (D / 2); c < (half + 1) * (D / 2); c += 32) {
                 uint32_t rr[32];
                 tmem_ld32(t_row + C::kColO + c, rr);
@@ -1235,13 +1244,23 @@ __device__ void pf2_softmax(const PfParams &p, uint8_t *smem, Pf2Bars &bars, uin
                                                                    __uint_as_float(rr[2 * e + 1]) * inv);
                     w[e] = *reinterpret_cast<const uint32_t *>(&h);
                 }
-                if (valid) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(orow + c);
-                    dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-                    dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
-                    dst[2] = make_uint4(w[8], w[9], w[10], w[11]);
-                    dst[3] = make_uint4(w[12], w[13], w[14], w[15]);
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    *reinterpret_cast<uint4 *>(stg + lane * 64 + ((j ^ (lane & 3)) << 4)) =
+                        make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+                __syncwarp();
+#pragma unroll
+                for (int sr = 0; sr < 4; ++sr) {
+                    const int rw = 8 * sr + (lane >> 2);          // row of the warp's 32
+                    const int r2 = quarter * 32 + rw;             // tile row
+                    const int qi2 = t * p.q_tile + (r2 >> p.group_shift);
+                    const uint4 v = *reinterpret_cast<const uint4 *>(stg + rw * 64 + ((pc ^ (rw & 3)) << 4));
+                    if (qi2 < un.q_len) {
+                        const int64_t row2 = (int64_t)(un.q_start + qi2) * p.num_q_heads + g * G + (r2 & (G - 1));
+                        *reinterpret_cast<uint4 *>(p.out + row2 * D + c + pc * 8) = v;
+                    }
                 }
+                __syncwarp(); // the block is rewritten by the next chunk
             }
             tc_fence_before();
             pf_arrive_mma<true>(&bars.o_free, lane, rank);
