@@ -999,51 +999,31 @@ done:
     }
 }
 
-// Writes this thread's half of its row of a unit's Q tile into the shared
-// memory Q operand (K-major, 128-byte swizzled, the layout a TMA box of
-// 8-row groups writes): row r = query r / G, head r % G; rows past total_q 0.
+// A unit's Q tile into the shared-memory Q operand (K-major, 128-byte
+// swizzled, the layout a TMA box of 8-row groups writes): row r = query r / G,
+// head r % G; rows past total_q are zeros.  Asynchronous copies (cp.async,
+// completed by cp_async_wait_all): each softmax warp fetches its TMEM lane
+// quarter's 32 rows, its half of head_dim, with consecutive lanes on
+// consecutive 16-byte pieces of one row (32 / (D / 16) rows per instruction).
 template <int D>
-__device__ __forceinline__ void pf2_load_q(const PfParams &p, const PfUnit &un, int g, int r, int half, uint8_t *q_smem,
-                                           int rank)
+__device__ __forceinline__ void pf2_load_q_async(const PfParams &p, const PfUnit &un, int g, int quarter, int lane,
+                                                 int half, uint8_t *q_smem, int rank)
 {
     using C = Pf2Cfg<D>;
-    const int tok = un.q_start + (un.t * p.cluster + rank) * p.q_tile + (r >> p.group_shift);
-    const int head = g * (1 << p.group_shift) + (r & ((1 << p.group_shift) - 1));
-    const bool in = tok < p.total_q;
-    const uint4 *src =
-        reinterpret_cast<const uint4 *>(p.q + ((int64_t)(in ? tok : 0) * p.num_q_heads + head) * D + half * (D / 2));
-    constexpr int kLoads = D / 16; // 16-byte chunks of half a row
-    uint4 v[kLoads];
+    constexpr int kPieces = D / 16;           // 16-byte pieces of half a row
+    constexpr int kRows = 32 / kPieces;       // rows per instruction
+    const int pc = lane % kPieces;
+    const int c = half * kPieces + pc;        // 16-byte chunk of the row: block c / 8, column c % 8
 #pragma unroll
-    for (int i = 0; i < kLoads; ++i)
-        v[i] = in ? __ldg(src + i) : make_uint4(0u, 0u, 0u, 0u);
-    uint8_t *row = q_smem + (r >> 3) * C::kGroupStride + (r & 7) * 128;
-#pragma unroll
-    for (int i = 0; i < kLoads; ++i) {
-        const int c = half * kLoads + i; // chunk of the row: block c / 8, 16-byte column c % 8
-        *reinterpret_cast<uint4 *>(row + (c >> 3) * 1024 + (((c & 7) ^ (r & 7)) << 4)) = v[i];
-    }
-}
-
-// The same rows with asynchronous copies (cp.async, zeros for rows past
-// total_q): issued while the softmax of the unit's last step runs, completed
-// by cp_async_wait_all before the MMA thread is told.
-template <int D>
-__device__ __forceinline__ void pf2_load_q_async(const PfParams &p, const PfUnit &un, int g, int r, int half,
-                                                 uint8_t *q_smem, int rank)
-{
-    using C = Pf2Cfg<D>;
-    const int tok = un.q_start + (un.t * p.cluster + rank) * p.q_tile + (r >> p.group_shift);
-    const int head = g * (1 << p.group_shift) + (r & ((1 << p.group_shift) - 1));
-    const bool in = tok < p.total_q;
-    const uint4 *src =
-        reinterpret_cast<const uint4 *>(p.q + ((int64_t)(in ? tok : 0) * p.num_q_heads + head) * D + half * (D / 2));
-    constexpr int kLoads = D / 16; // 16-byte chunks of half a row
-    uint8_t *row = q_smem + (r >> 3) * C::kGroupStride + (r & 7) * 128;
-#pragma unroll
-    for (int i = 0; i < kLoads; ++i) {
-        const int c = half * kLoads + i; // chunk of the row: block c / 8, 16-byte column c % 8
-        cp_async16(row + (c >> 3) * 1024 + (((c & 7) ^ (r & 7)) << 4), src + i, in ? 16u : 0u);
+    for (int s = 0; s < 32 / kRows; ++s) {
+        const int r = quarter * 32 + kRows * s + lane / kPieces; // tile row
+        const int tok = un.q_start + (un.t * p.cluster + rank) * p.q_tile + (r >> p.group_shift);
+        const int head = g * (1 << p.group_shift) + (r & ((1 << p.group_shift) - 1));
+        const bool in = tok < p.total_q;
+        const uint4 *src = reinterpret_cast<const uint4 *>(p.q + ((int64_t)(in ? tok : 0) * p.num_q_heads + head) * D +
+                                                           half * (D / 2)) + pc;
+        uint8_t *dst = q_smem + (r >> 3) * C::kGroupStride + (r & 7) * 128 + (c >> 3) * 1024 + (((c & 7) ^ (r & 7)) << 4);
+        cp_async16(dst, src, in ? 16u : 0u);
     }
 }
 
@@ -1078,7 +1058,8 @@ __device__ void pf2_softmax(const PfParams &p, uint8_t *smem, Pf2Bars &bars, uin
         return;
     {
         const int grp = u / p.num_kv_heads;
-        pf2_load_q<D>(p, p.units[grp], u - grp * p.num_kv_heads, r, half, q_smem, rank);
+        pf2_load_q_async<D>(p, p.units[grp], u - grp * p.num_kv_heads, quarter, lane, half, q_smem, rank);
+        cp_async_wait_all();
         fence_proxy_async_smem();
         pf_arrive_mma<true>(&bars.q_full, lane, rank);
     }
@@ -1104,7 +1085,7 @@ __device__ void pf2_softmax(const PfParams &p, uint8_t *smem, Pf2Bars &bars, uin
             if (j == ns - 1 && u_next < n_units) {
                 // this step's S MMAs were the unit's last reads of Q: fetch the next unit's
                 const int pn = u_next / p.num_kv_heads;
-                pf2_load_q_async<D>(p, p.units[pn], u_next - pn * p.num_kv_heads, r, half, q_smem, rank);
+                pf2_load_q_async<D>(p, p.units[pn], u_next - pn * p.num_kv_heads, quarter, lane, half, q_smem, rank);
             }
             const uint32_t s_col = C::kColS + (uint32_t)(gs & 1) * kPfStep + half * (kPfStep / 2);
             const bool masked = j * kPfStep + kPfStep - 1 > limit_min;
