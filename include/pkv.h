@@ -315,6 +315,9 @@ PKV_API size_t pkv_prefill_workspace_size(int32_t batch, int32_t total_q, int32_
  * [1, num_pages) among its first ceil(kv_b / page_size) entries
  * (PKV_ERR_PAGE) gets out = 0 and lse = -inf on its query rows (those inside
  * [0, total_q)) and sets the bit in *err_flag.
+ * Launches two kernels on `stream`: a one-CTA plan (an ordinary launch) and
+ * the attention kernel, a programmatic dependent of the plan that waits for
+ * it before reading anything the plan or earlier work wrote.
  */
 PKV_API pkv_status pkv_prefill_attn(const pkv_cache_desc *desc, const void *k_cache, const void *v_cache,
                                     const void *q, const int32_t *qo_indptr, const int32_t *kv_lens,
@@ -382,8 +385,12 @@ PKV_API size_t pkv_mixed_workspace_size(int32_t batch, int32_t total_q, int32_t 
  * max_blocks * page_size (PKV_ERR_OVERFLOW) or whose first
  * ceil(kv_b / page_size) block_table entries hold a page outside
  * [1, num_pages) (PKV_ERR_PAGE) gets out = 0 and lse = -inf.
- * Launches up to three kernels on `stream` (append, decode, prefill); no
- * host sync, no allocation, capturable in a CUDA graph.
+ * Launches up to four kernels on `stream` (the prefill plan when a row may
+ * be longer than decode_max_qlen, the append, the decode kernel, the prefill
+ * kernel), chained by programmatic dependent launch; the first one is an
+ * ordinary launch, so everything earlier in the stream is complete before
+ * any of them reads its inputs.  No host sync, no allocation, capturable in
+ * a CUDA graph.
  */
 PKV_API pkv_status pkv_mixed_attn(const pkv_cache_desc *desc, void *k_cache, void *v_cache, const void *q,
                                   const void *k_new, const void *v_new, const int32_t *qo_indptr,
