@@ -271,8 +271,16 @@ def test_mixed_workspace_size():
     decode_only = pkv.pkv_mixed_workspace_size(64, 256, 65, 32, 4, 4, d)
     with_prefill = pkv.pkv_mixed_workspace_size(64, 256, 65, 32, 512, 4, d)
     assert 0 < decode_only < with_prefill
-    # the decode part holds 8 (query, head) columns per unit once G * q > 4
+    # the decode part: 16 (query, head) columns per unit once G * q > 8
+    # (partials 16 columns wide, two combine tickets per unit)
     assert decode_only >= pkv.pkv_decode_workspace_size(64, 65, 32, d)
+    eight_cols = pkv.pkv_mixed_workspace_size(64, 256, 65, 32, 2, 2, d)
+    assert 0 < eight_cols < decode_only
+    # every head_dim has 16-column multi-query kernels: shapes of 9..32 columns per kv head are accepted
+    for D in (64, 128, 256):
+        dd = CacheDesc(65536, 16, 8, D, 0)
+        for hq, dq in ((32, 3), (32, 4), (64, 2), (128, 1), (16, 8), (32, 8)):
+            assert pkv.pkv_mixed_workspace_size(64, 256, 65, hq, dq, dq, dd) > 0, (D, hq, dq)
     assert pkv.pkv_mixed_workspace_size(64, 256, 65, 32, 0, 4, d) == 0        # max_qlen < 1
     assert pkv.pkv_mixed_workspace_size(64, 256, 65, 32, 4, 0, d) == 0        # decode_max_qlen < 1
     assert pkv.pkv_mixed_workspace_size(1025, 256, 65, 32, 4, 4, d) == 0
