@@ -437,7 +437,7 @@ int oracle_mixed(const oracle_cache *c, uint16_t *k_cache, uint16_t *v_cache, co
     return err_all;
 }
 
-/* Threads an OpenMP region of this build would use (1 without OpenMP). */
+/* Threads an OpenMP region would use (1 when compiled without OpenMP). */
 int oracle_max_threads(int nthreads)
 {
 #ifdef _OPENMP
