@@ -4,15 +4,21 @@ Workload (one step = one decode step of a 36-layer Qwen3-4B-shaped model's
 attention): the batch sweep at B=64, Hq=32, Hkv=8, D=128, page 128, prompt
 uniform in [64, 512], 36 per-layer K/V pools sharing one block table,
 shuffled page layout.  Every step appends one token per row in every layer
-and attends over all cached tokens; lengths grow by one per step and wrap
-after 512 decode steps (the reserved capacity).  Each step reads ~5 GB of
-K/V, far above the 129 MB L2, so no flush is needed between steps.
+and attends over all cached tokens; decode step s (0 <= s < 512) attends
+prompt + s + 1 tokens per row.  The K timed steps are spread evenly over the
+whole 512-step cycle (timed step i runs decode step floor((i + 1/2) * 512 / K)),
+so the timed region measures the cycle's mean whatever K is.  Each step
+reads ~5 GB of K/V, far above the 129 MB L2, so no flush is needed between
+steps.
 
 Prints one JSON line.  `value` = algorithmic KV-path bytes / device time
 (GB/s) over the timed steps; `roofline` = the decode kernel's average
-launch (CUDA events around every launch); `e2e` = the same metric through
-the C ABI with the step's q / k_new / v_new copied from pinned host memory
-and the outputs copied back inside the timed region.
+launch (CUDA events around the timed region, which launches nothing else);
+`e2e` = the same metric through the C ABI with the step's q / k_new / v_new
+copied from pinned host memory and the outputs copied back inside the timed
+region.  Also in the line: the same sweep on contiguous pages, the two
+single-layer decode workloads (Qwen3-4B-shaped layer, skewed lengths), the
+ragged prefill and the two mixed-step workloads.
 
 `--impl reference` times the fp64 CPU oracle on the host cores instead
 (bounded samples of the same workload).
@@ -368,57 +374,69 @@ def sum_over_ranks(x: float, world: int, device) -> float:
     return float(t.item())
 
 
-def cpu_baseline(sw, prompt_lens: np.ndarray, budget_s: float = 12.0, max_steps: int = 64):
-    """Times the fp64 oracle (all host cores) on whole decode steps (all 36
-    layers, all rows and heads) from step 0 on, until `budget_s` of oracle
-    time is spent; returns GB/s of the same algorithmic bytes."""
+def timed_decode_steps(n: int) -> list:
+    """Decode steps of n timed iterations, spread evenly over the cycle:
+    iteration i runs step floor((i + 1/2) * 512 / n) (mod 512), so the mean
+    work of any n steps is the cycle's mean."""
+    return [int((i + 0.5) * DECODE_CAPACITY / n) % DECODE_CAPACITY for i in range(n)]
+
+
+def cpu_baseline(sw, steps: list, budget_s: float = 12.0, host_layers: int = 2):
+    """Times the fp64 oracle (all host cores) on whole layer calls (all rows
+    and heads) of the timed decode steps, in order, until `budget_s` of
+    oracle time is spent; returns GB/s of the same algorithmic bytes.  Every
+    layer call of a step costs the same, so the calls cycle over the first
+    `host_layers` layer pools (host copies of those only)."""
     import oracle
     from paged_kv_decode_append_gb300 import workloads as wl
 
     dev = sw.k_caches[0].device
     rows = list(range(sw.batch))
-    need = prompt_lens + max_steps + 1
+    need = sw.prompt_lens + DECODE_CAPACITY
     host = []
-    for layer in range(sw.layers):  # compact host copies, reused (and appended to) step after step
+    for layer in range(host_layers):
         k, v, bt = wl.compact_rows(sw.k_caches[layer], sw.v_caches[layer], sw.block_table, rows, need, P)
         host.append((k, v, bt))
     d = oracle.CacheDesc(host[0][0].shape[0], P, HKV, D, oracle.NHD)
     threads = oracle.max_threads(0)
-    done_bytes, elapsed, calls, step = 0, 0.0, 0, 0
-    while elapsed < budget_s and step < max_steps:
-        lens = (prompt_lens + step).astype(np.int32)
-        inputs = wl.sweep_step_inputs(sw, step, dev, layers=sw.layers)
-        for layer in range(sw.layers):
-            q, kn, vn = (wl.bits(t) for t in inputs[layer])
-            k, v, bt = host[layer]
-            t0 = time.perf_counter()
-            oracle.decode(d, k, v, q, kn, vn, bt, lens, sw.softmax_scale, nthreads=0)
-            elapsed += time.perf_counter() - t0
-            done_bytes += call_bytes(lens, sw.batch)
-            calls += 1
-            if elapsed >= budget_s:
-                break
-        step += 1
-    # the same oracle on one host thread, over the first layers of step 0
-    lens0 = prompt_lens.astype(np.int32)
-    inputs0 = wl.sweep_step_inputs(sw, 0, dev, layers=4)
-    one_bytes, one_t = 0, 0.0
-    for layer in range(4):
-        q, kn, vn = (wl.bits(t) for t in inputs0[layer])
+    done_bytes, elapsed, calls, used = 0, 0.0, 0, []
+    for i, step in enumerate(steps * 4):
+        if elapsed >= budget_s:
+            break
+        lens = (sw.prompt_lens + step).astype(np.int32)
+        layer = i % host_layers
+        q, kn, vn = (wl.bits(t) for t in wl.sweep_step_inputs(sw, step, dev, layers=layer + 1)[layer])
         k, v, bt = host[layer]
         t0 = time.perf_counter()
-        oracle.decode(d, k, v, q, kn, vn, bt, lens0, sw.softmax_scale, nthreads=1)
+        oracle.decode(d, k, v, q, kn, vn, bt, lens, sw.softmax_scale, nthreads=0)
+        elapsed += time.perf_counter() - t0
+        done_bytes += call_bytes(lens, sw.batch)
+        calls += 1
+        used.append(step)
+    # the same oracle on one host thread: the first two sampled calls
+    one_bytes, one_t = 0, 0.0
+    for i, step in enumerate(steps[:2]):
+        lens = (sw.prompt_lens + step).astype(np.int32)
+        layer = i % host_layers
+        q, kn, vn = (wl.bits(t) for t in wl.sweep_step_inputs(sw, step, dev, layers=layer + 1)[layer])
+        k, v, bt = host[layer]
+        t0 = time.perf_counter()
+        oracle.decode(d, k, v, q, kn, vn, bt, lens, sw.softmax_scale, nthreads=1)
         one_t += time.perf_counter() - t0
-        one_bytes += call_bytes(lens0, sw.batch)
+        one_bytes += call_bytes(lens, sw.batch)
     return {"value": done_bytes / elapsed / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
             "single_thread_value": one_bytes / one_t / 1e9,
-            "single_thread_sample": "layers 0..3 of decode step 0, one host thread",
-            "sample": f"{calls} layer calls (decode steps 0..{step - 1} of the 36-layer B={sw.batch} workload, all "
-                      f"rows and heads), fp64 oracle with OpenMP over (row, head), {elapsed:.1f} s of oracle time"}
+            "single_thread_sample": f"one layer call of decode steps {steps[:2]}, one host thread",
+            "sample": f"{calls} layer calls (one per timed decode step, steps {min(used)}..{max(used)} of the "
+                      f"512-step cycle, of the 36-layer B={sw.batch} workload, all rows and heads), fp64 oracle "
+                      f"with OpenMP over (row, head), {elapsed:.1f} s of oracle time"}
 
 
 def run_reference(args):
-    """The reference arm: the fp64 oracle timed on the host cores.  Under a
+    """The reference arm: the fp64 oracle timed on the host cores.  Each
+    timed step runs one layer call (all rows and heads) of the same decode
+    step the GPU arm times; a step of the 36-layer workload is that call
+    times 36 (every layer call of a step does the same work).  Under a
     multi-rank launch rank 0 alone runs and prints; the others exit at once."""
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -430,34 +448,35 @@ def run_reference(args):
     oracle.build()
     dev = "cuda" if torch.cuda.is_available() else "cpu"
     sw = wl.batch_sweep(args.batch, device=dev, contiguous=args.layout == "contiguous", layers=1,
-                        data_device=dev)
+                        data_device=dev, fill_decode=True)
     rows = list(range(sw.batch))
     threads = oracle.max_threads(0)
+    k, v, bt = wl.compact_rows(sw.k_caches[0], sw.v_caches[0], sw.block_table, rows,
+                               sw.prompt_lens + DECODE_CAPACITY, P)
+    d = oracle.CacheDesc(k.shape[0], P, HKV, D, oracle.NHD)
     times, nbytes = [], []
-    host = []
-    for s in range(args.warmup + args.steps):
-        lens = (sw.prompt_lens + (s % DECODE_CAPACITY)).astype(np.int32)
-        k, v, bt = wl.compact_rows(sw.k_caches[0], sw.v_caches[0], sw.block_table, rows, lens + 1, P)
-        q, kn, vn = (wl.bits(t) for t in wl.sweep_step_inputs(sw, s, dev, layers=1)[0])
-        host.append((k, v, bt, q, kn, vn, lens))
-        if len(host) > 2:
-            host.pop(0)
-        d = oracle.CacheDesc(k.shape[0], P, HKV, D, oracle.NHD)
+    steps = timed_decode_steps(args.warmup) + timed_decode_steps(args.steps)
+    for i, step in enumerate(steps):
+        lens = (sw.prompt_lens + step).astype(np.int32)
+        q, kn, vn = (wl.bits(t) for t in wl.sweep_step_inputs(sw, step, dev, layers=1)[0])
         t0 = time.perf_counter()
         oracle.decode(d, k, v, q, kn, vn, bt, lens, sw.softmax_scale, nthreads=0)
         dt = time.perf_counter() - t0
-        if s >= args.warmup:
+        if i >= args.warmup:
             times.append(dt)
             nbytes.append(call_bytes(lens, sw.batch))
     total_t = float(sum(times))
     value = sum(nbytes) / total_t / 1e9
     out = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": 1e3 * total_t / len(times), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "warmup": args.warmup, "ms_per_step": 1e3 * total_t / len(times) * args.layers,
+        "ms_per_layer_call": 1e3 * total_t / len(times),
+        "ms_per_step_basis": f"one layer call timed per step, times {args.layers} layers",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": workload_config(args),
         "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle",
-                         "sample": f"one layer per step (layer 0 of the 36), B={args.batch}, fp64 oracle"},
+                         "sample": f"one layer call per timed step (layer 0 of the 36, the GPU arm's decode steps), "
+                                   f"B={args.batch}, fp64 oracle"},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(out))
@@ -467,8 +486,8 @@ def single_layer_bench(kind: str, reps: int, warmup: int):
     """One fused append + decode call per timed iteration on the Qwen3-4B-shaped
     layer (B=32, page 16, lengths U[512,1024]) or the skewed batch (B=64, one
     32,768-token row), CUDA events around each call, L2 flushed by a 512 MiB
-    write before it (a call reads 0.1-0.4 GB, about L2's size).  Prints one
-    JSON line in the main line's format."""
+    write before it (a call reads 0.1-0.4 GB, about L2's size).  Returns a
+    dict in the main line's format (plus the streamed form of the call)."""
     import paged_kv_decode_append_gb300 as pkv
     from paged_kv_decode_append_gb300 import workloads as wl
 
@@ -511,14 +530,16 @@ def single_layer_bench(kind: str, reps: int, warmup: int):
             "shuffled pool" if kind == "qwen3" else
             "skewed-length decode: B=64, Hq=32, Hkv=8, D=128, page 16, one 32,768-token row, others "
             "clip(lognormal(6.5,0.8),128,4096), 65,536-page shuffled pool")
-    print(json.dumps({
+    del case, flush
+    torch.cuda.empty_cache()
+    return {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": 1, "steps": reps, "warmup": warmup,
         "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
         "config": {"workload": name, "batch": B, "l2": "flushed between calls (512 MiB write)"},
         "pct_of_hbm_peak": 100.0 * value / peak, "decode_tok_s_per_attn_layer": B / (ms * 1e-3),
         "ms_best": float(times.min()), "algorithmic_bytes_per_call": nbytes, "peak": peak, "peak_kind": peak_kind,
-        "clocks": clocks.summary(), "gpu_launches": reps, "streamed": streamed}))
+        "clocks": clocks.summary(), "gpu_launches": reps, "streamed": streamed}
 
 
 def streamed_layer_calls(case, bt, lens, out, ws, nbytes, peak, dev, rounds: int = 5):
@@ -569,28 +590,106 @@ def streamed_layer_calls(case, bt, lens, out, ws, nbytes, peak, dev, rounds: int
             "l2": f"{copies} rotating copies of the layer pool (copies x call bytes >= 4 x L2)"}
 
 
-def workload_config(args):
+def workload_config(args, layout=None):
+    steps = timed_decode_steps(args.steps)
+    layout = args.layout if layout is None else layout
     return {"workload": f"paged decode batch sweep B={args.batch} (Qwen3-4B-shaped: Hq=32, Hkv=8, D=128), "
-                        f"page 128, {args.layout} pages, prompt U[64,512] + decode steps, 36 layer caches per step",
+                        f"page 128, {layout} pages, prompt U[64,512] + decode steps of the 512-step cycle, "
+                        f"{args.layers} layer caches per step; {args.steps} timed steps spread over the cycle: "
+                        f"step floor((i + 1/2) * 512 / {args.steps}) for i < {args.steps} "
+                        f"(steps {min(steps)}..{max(steps)})",
             "batch": args.batch, "num_q_heads": HQ, "num_kv_heads": HKV, "head_dim": D, "page_size": P,
-            "layers": args.layers, "layout": args.layout,
+            "layers": args.layers, "layout": layout, "decode_steps_timed": [min(steps), max(steps)],
             "l2": "inputs larger than L2: every step streams 36 distinct layer caches (~5 GB)"}
+
+
+class Sweep:
+    """The 36-layer batch-sweep decode of one rank: pools, per-step inputs and
+    one CUDA graph per decode step (its layers' launches back to back)."""
+
+    def __init__(self, pkv, wl, args, dev, layout: str, seed: int, flags: int):
+        B, L = args.batch, args.layers
+        self.pkv, self.args, self.dev, self.B, self.L, self.flags = pkv, args, dev, B, L, flags
+        self.sw = wl.batch_sweep(B, device=dev, contiguous=layout == "contiguous", layers=L, seed=seed,
+                                 fill_decode=True)
+        self.bt = torch.as_tensor(self.sw.block_table, device=dev)
+        self.lens_all = (self.sw.prompt_lens[None, :] + np.arange(DECODE_CAPACITY)[:, None]).astype(np.int32)
+        self.lens_dev = torch.as_tensor(self.lens_all, device=dev)
+        desc = pkv.cache_desc(self.sw.k_caches[0])
+        self.ws = pkv.decode_workspace(B, self.sw.max_blocks, HQ, desc, dev)
+        ring = 8  # distinct per-step input sets, reused round-robin
+        self.inputs = [wl.sweep_step_inputs(self.sw, s, dev, layers=L) for s in range(ring)]
+        self.outs = [torch.empty(B, HQ, D, dtype=torch.bfloat16, device=dev) for _ in range(L)]
+        self.step_bytes = [L * call_bytes(self.lens_all[s], B) for s in range(DECODE_CAPACITY)]
+
+    def step_inputs(self, step):
+        return self.inputs[step % len(self.inputs)]
+
+    def layer_call(self, step, layer, q, kn, vn, flags=None):
+        self.pkv.pkv_decode_attn(self.sw.k_caches[layer], self.sw.v_caches[layer], q, kn, vn, self.bt,
+                                 self.lens_dev[step], self.sw.softmax_scale, out=self.outs[layer], workspace=self.ws,
+                                 flags=self.flags if flags is None else flags)
+
+    def graph(self, step):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for layer, (q, kn, vn) in enumerate(self.step_inputs(step)):
+                self.layer_call(step, layer, q, kn, vn)
+        return g
+
+    def timed(self, warm_steps, steps, world, local, clocks=True):
+        """Replays the graphs of `warm_steps`, then times `steps` back to back
+        (barrier + synchronize on both sides).  Returns (ms, bytes)."""
+        warm = [self.graph(s) for s in warm_steps]
+        graphs = [self.graph(s) for s in steps]
+        torch.cuda.synchronize(self.dev)
+        for g in warm:
+            g.replay()
+        torch.cuda.synchronize(self.dev)
+        barrier(world)
+        stream = torch.cuda.current_stream(self.dev)
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        total = 0
+        sampler = ClockSampler(local) if clocks else None
+        if sampler is not None:
+            sampler.__enter__()
+        try:
+            torch.cuda.synchronize(self.dev)
+            barrier(world)
+            torch.cuda.nvtx.range_push("timed")
+            start.record(stream)
+            for s, g in zip(steps, graphs):
+                g.replay()
+                total += self.step_bytes[s]
+            end.record(stream)
+            torch.cuda.nvtx.range_pop()
+            torch.cuda.synchronize(self.dev)
+            barrier(world)
+        finally:
+            if sampler is not None:
+                sampler.__exit__(None, None, None)
+        del warm, graphs
+        return start.elapsed_time(end), total, (sampler.summary() if sampler is not None else None)
 
 
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=600)
+    ap.add_argument("--steps", type=int, default=DECODE_CAPACITY)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--batch", type=int, default=64)
     ap.add_argument("--layers", type=int, default=36)
     ap.add_argument("--layout", default="shuffled", choices=["shuffled", "contiguous"])
-    ap.add_argument("--e2e-steps", type=int, default=600)
+    ap.add_argument("--e2e-steps", type=int, default=DECODE_CAPACITY)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--prefill-reps", type=int, default=20, help="timed prefill calls (0 = skip)")
     ap.add_argument("--mixed-reps", type=int, default=20,
                     help="timed mixed-step calls per mixed workload in the default line (0 = skip)")
+    ap.add_argument("--layer-reps", type=int, default=20,
+                    help="timed single-layer calls per single-layer workload in the default line (0 = skip)")
+    ap.add_argument("--no-contiguous", action="store_true",
+                    help="skip the contiguous-pages sweep of the default line")
     ap.add_argument("--prefill-only", action="store_true",
                     help="run only the prefill measurement on cuda:0 and print its JSON object")
     ap.add_argument("--workload", default="sweep", choices=["sweep", "qwen3", "skewed", "spec", "chunked"],
@@ -603,6 +702,8 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.steps < 1:
+        ap.error("--steps must be >= 1")
     if args.impl == "reference":
         run_reference(args)
         return
@@ -612,7 +713,7 @@ def main():
         return
     if args.workload != "sweep":
         reps = 50 if args.steps == ap.get_default("steps") else args.steps
-        single_layer_bench(args.workload, reps, args.warmup)
+        print(json.dumps(single_layer_bench(args.workload, reps, args.warmup)))
         return
     if args.prefill_only:
         dev = torch.device("cuda:0")
@@ -628,60 +729,20 @@ def main():
     dev = torch.device(f"cuda:{local}")
     torch.cuda.set_device(dev)
     B, L = args.batch, args.layers
-    sw = wl.batch_sweep(B, device=dev, contiguous=args.layout == "contiguous", layers=L, seed=2 + rank)
-    bt = torch.as_tensor(sw.block_table, device=dev)
-    lens_all = (sw.prompt_lens[None, :] + np.arange(DECODE_CAPACITY)[:, None]).astype(np.int32)
-    lens_dev = torch.as_tensor(lens_all, device=dev)
-    desc = pkv.cache_desc(sw.k_caches[0])
-    ws = pkv.decode_workspace(B, sw.max_blocks, HQ, desc, dev)
-    ring = 8  # distinct per-step input sets, reused round-robin
-    inputs = [wl.sweep_step_inputs(sw, s, dev, layers=L) for s in range(ring)]
-    outs = [torch.empty(B, HQ, D, dtype=torch.bfloat16, device=dev) for _ in range(L)]
-    step_bytes = [L * call_bytes(lens_all[s], B) for s in range(DECODE_CAPACITY)]
-    stream = torch.cuda.current_stream(dev)
-
     # layers of one step read different caches: the next layer may stream its
     # K/V while the previous one finishes
     flags = 0 if args.no_overlap else pkv.api.DECODE_OVERLAP_PROLOGUE | pkv.api.DECODE_EARLY_KV
+    sweep = Sweep(pkv, wl, args, dev, args.layout, 2 + rank, flags)
+    sw = sweep.sw
+    steps = timed_decode_steps(args.steps)
+    warm_steps = timed_decode_steps(args.warmup)
+    stream = torch.cuda.current_stream(dev)
 
-    def layer_call(step, layer, q, kn, vn):
-        pkv.pkv_decode_attn(sw.k_caches[layer], sw.v_caches[layer], q, kn, vn, bt, lens_dev[step % DECODE_CAPACITY],
-                            sw.softmax_scale, out=outs[layer], workspace=ws, flags=flags)
-
-    # One CUDA graph per decode step (its 36 layer launches back to back),
-    # captured up front and replayed back to back in the timed region.  The
-    # region holds this one kernel only, so its average launch duration is the
+    # The timed region: one CUDA graph per decode step, replayed back to back.
+    # It holds this one kernel only, so its average launch duration is the
     # region time over the launches.
-    n_steps = args.warmup + args.steps
-    graphs = []
-    for s in range(n_steps):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g):
-            for layer, (q, kn, vn) in enumerate(inputs[s % ring]):
-                layer_call(s, layer, q, kn, vn)
-        graphs.append(g)
-    torch.cuda.synchronize(dev)
-    for s in range(args.warmup):
-        graphs[s].replay()
-    torch.cuda.synchronize(dev)
-    barrier(world)
-
+    ms, total_bytes, clocks = sweep.timed(warm_steps, steps, world, local)
     n_ev = args.steps * L
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    total_bytes = 0
-    with ClockSampler(local) as clocks:
-        torch.cuda.synchronize(dev)
-        barrier(world)
-        torch.cuda.nvtx.range_push("timed")
-        start.record(stream)
-        for s in range(args.warmup, n_steps):
-            graphs[s].replay()
-            total_bytes += step_bytes[s % DECODE_CAPACITY]
-        end.record(stream)
-        torch.cuda.nvtx.range_pop()
-        torch.cuda.synchronize(dev)
-        barrier(world)
-    ms = start.elapsed_time(end)
     ms_max = max_over_ranks(ms, world, dev)
     all_bytes = sum_over_ranks(float(total_bytes), world, dev)
     value = all_bytes / (ms_max * 1e-3) / 1e9
@@ -690,40 +751,38 @@ def main():
     achieved = launch_bytes / (kernel_ms * 1e-3) / 1e9
     peak, peak_kind = peaks()
     traffic_ratio = recorded_traffic()
-    del graphs
 
     # Diagnostic: each launch alone (plain launch, CUDA events around it) for
-    # the first `iso_steps` steps, to show the duration of one kernel by itself.
-    iso_steps = min(20, args.steps)
+    # the first `iso_steps` timed steps, to show the duration of one kernel by itself.
+    iso_steps = steps[:min(20, len(steps))]
     iso_ev, iso_bytes = [], []
-    for s in range(iso_steps):
-        for layer, (q, kn, vn) in enumerate(inputs[s % ring]):
+    for s in iso_steps:
+        for layer, (q, kn, vn) in enumerate(sweep.step_inputs(s)):
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g):
-                pkv.pkv_decode_attn(sw.k_caches[layer], sw.v_caches[layer], q, kn, vn, bt,
-                                    lens_dev[s % DECODE_CAPACITY], sw.softmax_scale, out=outs[layer], workspace=ws)
+                sweep.layer_call(s, layer, q, kn, vn, flags=0)
             torch.cuda.synchronize(dev)
             a.record(stream)
             g.replay()
             b.record(stream)
             iso_ev.append((a, b, g))
-            iso_bytes.append(call_bytes(lens_all[s % DECODE_CAPACITY], B))
+            iso_bytes.append(call_bytes(sweep.lens_all[s], B))
     torch.cuda.synchronize(dev)
     iso_ms = np.array([a.elapsed_time(b) for a, b, _ in iso_ev])
     iso_gbs = float(np.sum(iso_bytes) / (iso_ms.sum() * 1e-3) / 1e9)
     del iso_ev
 
     # Without graphs: the same steps as plain stream launches (36 per step).
-    eager_steps = min(20, args.steps)
+    eager_steps = steps[:min(20, len(steps))]
     torch.cuda.synchronize(dev)
     ea, eb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     eager_bytes = 0
     ea.record(stream)
-    for s in range(args.warmup, args.warmup + eager_steps):
-        for layer, (q, kn, vn) in enumerate(inputs[s % ring]):
-            layer_call(s, layer, q, kn, vn)
-        eager_bytes += step_bytes[s % DECODE_CAPACITY]
+    for s in eager_steps:
+        for layer, (q, kn, vn) in enumerate(sweep.step_inputs(s)):
+            sweep.layer_call(s, layer, q, kn, vn)
+        eager_bytes += sweep.step_bytes[s]
     eb.record(stream)
     torch.cuda.synchronize(dev)
     eager_gbs = eager_bytes / (ea.elapsed_time(eb) * 1e-3) / 1e9
@@ -737,8 +796,8 @@ def main():
     # computes, step s's outputs come down while step s+1 computes.  The timed
     # region spans the first input copy to the last output copy; the steps are
     # those the device-timed value covers (the first e2e_steps of them).
-    e2e_steps = min(args.e2e_steps, args.steps)
-    s0 = args.warmup
+    e2e_list = steps[:min(args.e2e_steps, len(steps))]
+    e2e_steps = len(e2e_list)
     per_layer = [B * HQ * D, B * HKV * D, B * HKV * D]
     layer_elems = sum(per_layer)
 
@@ -754,16 +813,17 @@ def main():
         d_in = [split(d_in_all, layer * layer_elems) for layer in range(L)]
         d_out = [d_out_all[layer * B * HQ * D:(layer + 1) * B * HQ * D].view(B, HQ, D) for layer in range(L)]
         graph = pkv.DecodeStep(sw.k_caches, sw.v_caches, [t[0] for t in d_in], [t[1] for t in d_in],
-                               [t[2] for t in d_in], bt, d_seq, sw.softmax_scale, d_out, workspace=ws, flags=flags)
+                               [t[2] for t in d_in], sweep.bt, d_seq, sw.softmax_scale, d_out, workspace=sweep.ws,
+                               flags=flags)
         sets.append((d_in_all, d_out_all, d_seq, graph))
     h_in = []
     for r in range(2):  # two pinned input sets, alternated
         h = torch.empty(L * layer_elems, dtype=torch.bfloat16).pin_memory()
-        for layer, trip in enumerate(inputs[r]):
+        for layer, trip in enumerate(sweep.inputs[r]):
             for dst, t in zip(split(h, layer * layer_elems), trip):
                 dst.copy_(t.cpu())
         h_in.append(h)
-    h_seq = [torch.as_tensor(lens_all[(s0 + i) % DECODE_CAPACITY]).pin_memory() for i in range(e2e_steps)]
+    h_seq = [torch.as_tensor(sweep.lens_all[s]).pin_memory() for s in e2e_list]
     h_out = [torch.empty(L * B * HQ * D, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
     h2d = sets[0][0].numel() * 2 + B * 4
     d2h = sets[0][1].numel() * 2
@@ -778,7 +838,7 @@ def main():
             if i >= 2:
                 up.wait_event(out_read[i - 2])
             d_in_all, _, d_seq, _ = sets[i % 2]
-            d_in_all.copy_(h_in[(s0 + i) % 2], non_blocking=True)
+            d_in_all.copy_(h_in[i % 2], non_blocking=True)
             d_seq.copy_(h_seq[i], non_blocking=True)
             in_ready[i].record(up)
 
@@ -799,7 +859,7 @@ def main():
             down.wait_event(done[i])
             h_out[i % 2].copy_(sets[i % 2][1], non_blocking=True)
             out_read[i].record(down)
-        e_bytes += step_bytes[(s0 + i) % DECODE_CAPACITY]
+        e_bytes += sweep.step_bytes[e2e_list[i]]
     stream.wait_stream(down)
     e_end.record(stream)
     torch.cuda.synchronize(dev)
@@ -812,6 +872,32 @@ def main():
 
     if rank != 0:
         return
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        cpu = cpu_baseline(sw, steps)
+    del sweep, sw
+    torch.cuda.empty_cache()
+
+    contiguous = None
+    if not args.no_contiguous:  # the same sweep on sequentially reserved pages
+        other = "contiguous" if args.layout == "shuffled" else "shuffled"
+        csweep = Sweep(pkv, wl, args, dev, other, 2, flags)
+        c_ms, c_bytes, c_clocks = csweep.timed(warm_steps, steps, 1, local)
+        c_val = c_bytes / (c_ms * 1e-3) / 1e9
+        contiguous = {"layout": other, "value": c_val, "unit": "GB/s", "pct_of_hbm_peak": 100.0 * c_val / peak,
+                      "ms_per_step": c_ms / args.steps, "steps": args.steps,
+                      "algorithmic_bytes_per_launch": c_bytes / n_ev, "clocks": c_clocks,
+                      "gpu_launches": n_ev, "config": workload_config(args, other)}
+        del csweep
+        torch.cuda.empty_cache()
+    single = None
+    if args.layer_reps > 0:  # one layer per call: the Qwen3-4B-shaped layer and the skewed batch
+        keep = ("value", "unit", "pct_of_hbm_peak", "decode_tok_s_per_attn_layer", "ms_per_step", "ms_best",
+                "steps", "config", "algorithmic_bytes_per_call", "clocks", "gpu_launches", "streamed")
+        single = {}
+        for kind in ("qwen3", "skewed"):
+            line = single_layer_bench(kind, args.layer_reps, 3)
+            single[kind] = {k: line[k] for k in keep}
     mixed = None
     if args.mixed_reps > 0:  # one mixed step per call: speculative decode and a chunked-prefill step
         keep = ("value", "unit", "pct_of_hbm_peak", "tflops", "pct_of_tensor_peak", "ms_per_step", "ms_best",
@@ -820,9 +906,6 @@ def main():
         for kind in ("spec", "chunked"):
             line = mixed_bench(kind, args.mixed_reps, 3, None, dev)
             mixed[kind] = {k: line[k] for k in keep}
-    cpu = None
-    if not args.no_cpu_baseline and world == 1:
-        cpu = cpu_baseline(sw, sw.prompt_lens)
     steps_tok = B / (ms / args.steps / L * 1e-3)  # decode tokens/s per attention layer
     out = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
@@ -837,19 +920,21 @@ def main():
                      "algorithmic_bytes_per_launch": launch_bytes, "launch_ms_mean": kernel_ms,
                      "isolated_launch_ms_mean": float(iso_ms.mean()), "isolated_launch_ms_best": float(iso_ms.min()),
                      "isolated_gbs": iso_gbs, "isolated_launches": int(iso_ms.size),
-                     "isolated_steps": f"decode steps 0..{iso_steps - 1} (shorter caches than the timed region's mean)"},
-        "clocks": clocks.summary(),
+                     "isolated_steps": f"the first {len(iso_steps)} timed decode steps, each launch alone"},
+        "clocks": clocks,
         "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "steps": e2e_steps,
                 "path": "pkv_decode_step graphs of the 36 layers over two buffer sets; per step pinned H2D of "
                         "all inputs and cache_seqlens, one graph launch, D2H of all outputs; copies on their own "
                         "streams, double-buffered (step s+1's upload and step s-1's download overlap step s)"},
-        "eager": {"value": eager_gbs, "unit": "GB/s", "steps": eager_steps,
+        "eager": {"value": eager_gbs, "unit": "GB/s", "steps": len(eager_steps),
                   "launch": "plain stream launches, no CUDA graph"},
         "gpu_launches": n_ev,
         "launch": "one CUDA graph per decode step (36 kernel launches" + (
             ")" if args.no_overlap else ", programmatic dependent launch between them, K/V streamed early)"),
         "cpu_baseline": cpu,
+        "contiguous": contiguous,
+        "single_layer": single,
         "prefill": prefill,
         "mixed": mixed,
     }

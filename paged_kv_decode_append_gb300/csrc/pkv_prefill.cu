@@ -9,14 +9,16 @@
 // h / (Hq / Hkv); softmax scale, output rounding and the error rules are
 // those of include/pkv.h.
 //
-// How (one persistent CTA per SM, clusters of two):
-//  - Work unit = (request, kv head, two consecutive tiles of 128/G queries).
+// How (one persistent CTA per SM):
+//  - Work unit = (request, kv head, one query tile of 128/G queries per CTA
+//    of the cluster: two for a CTA pair).
 //    The G query heads sharing a kv head times 128/G consecutive queries form
 //    a CTA's 128 MMA rows (row r = query r/G, head r%G), so every K/V tile
 //    read from the pages serves all G heads.
 //  - A one-CTA plan kernel validates every request, lists the units and
 //    orders them by their number of 64-token kv tiles, longest first; the
-//    persistent clusters take units in that order, snaking over the grid.
+//    persistent clusters (or single CTAs) take units in that order, snaking
+//    over the grid.
 //  - head_dim 128 and 256 (prefill2_kernel): the cluster is a CTA pair
 //    whose MMAs (tcgen05.mma.cta_group::2, M = 256) cover both query tiles,
 //    issued by one thread of the even CTA.  Keys go in steps of 128.  For
@@ -28,8 +30,8 @@
 //    TMEM: O [128 x D] fp32 and two S [128 x 128] buffers (S of step t+1 is
 //    computed while the softmax of step t runs); Q [128 x D] in shared
 //    memory, K-major and swizzled.
-//  - head_dim 64 (prefill_kernel): one query tile per CTA, 64-key tiles,
-//    K / V shared by the cluster through TMA multicast, Q in TMEM.
+//  - head_dim 64 (prefill_kernel): one query tile per CTA (clusters of
+//    one), 64-key tiles, each CTA loading its own K / V tiles, Q in TMEM.
 //  - Warp roles: warp 0 loads this CTA's K and V with TMA into a ring of
 //    shared-memory stages (head_dim 64, in the order the MMAs consume them;
 //    CTA pairs: warp 0 the K ring, warp 10 the V ring); warp 1 owns TMEM and
@@ -179,7 +181,7 @@ struct PfParams {
     int32_t *err_flag;
     int max_blocks, num_q_heads, num_kv_heads, total_q;
     int group_shift, q_tile, page_shift, box_shift, layout;
-    int cluster; // CTAs per cluster (1 or 2): a pair, or two single CTAs sharing every K / V tile
+    int cluster; // CTAs per cluster: 2 for a CTA pair, 1 for the single-CTA kernel
     float q_scale;
     int pdl; // launched as a programmatic dependent: set up, then wait for the preceding grid
 };
@@ -281,21 +283,9 @@ __device__ __forceinline__ bool pf_wait_all(uint64_t *bar, uint32_t parity, Bars
 
 // ---------------------------------------------------------------- producer
 
-// Issues one box of an item (token-group map coordinates: token group `c3`,
-// page-head or head `c4`): the TMA load lands in this CTA and, in a cluster,
-// is multicast to the same offset of every CTA of it.
-__device__ __forceinline__ void pf_tma5(const PfParams &p, void *dst, const CUtensorMap *map, int c3, int c4,
-                                        uint64_t *bar)
-{
-    if (p.cluster > 1)
-        tma_load_5d_mc(dst, map, 0, 0, 0, c3, c4, bar, (uint16_t)((1u << p.cluster) - 1u));
-    else
-        tma_load_5d_plain(dst, map, 0, 0, 0, c3, c4, bar);
-}
-
 template <int D>
 __device__ void pf_producer(const PfParams &p, const PfMapsDev &maps, uint8_t *smem, PfBars &bars, int n_units,
-                            int lane, int cl_rank)
+                            int lane)
 {
     using C = PfCfg<D>;
     const int Hkv = p.num_kv_heads;
@@ -331,7 +321,7 @@ __device__ void pf_producer(const PfParams &p, const PfMapsDev &maps, uint8_t *s
                 const int itg = ib + (kind == 0 ? pf_item_k(jj) : pf_item_v(jj, nt));
                 const int stage = itg % C::kStages;
                 const int n = itg / C::kStages;
-                // The stage is free once every CTA of the cluster has released it.
+                // The stage is free once the MMAs that read it have completed.
                 if (n > 0 && !pf_wait_all(&bars.empty[stage], (n - 1) & 1, bars, p.err_flag)) {
                     ok = false;
                     break;
@@ -341,22 +331,23 @@ __device__ void pf_producer(const PfParams &p, const PfMapsDev &maps, uint8_t *s
                 const int nbox = (ntok + BT - 1) >> p.box_shift;
                 uint8_t *dst = smem + C::kOffStage + stage * C::kStageBytes;
                 const int ids = kind == 0 ? ids_cur : ids_prev;
-                if (lane == 0) // the whole item, whichever CTA of the cluster loads each part
+                if (lane == 0)
                     mbar_arrive_expect_tx(&bars.full[stage], (uint32_t)nbox * box_bytes);
                 // Sub-boxes: K (and V when a box is a whole tile) in 64-column
                 // boxes, [block][64 tokens][128 B], so the S MMA sees evenly
                 // spaced rows; V otherwise in page boxes, [box][block][BT][128 B].
                 const CUtensorMap *map = kind == 0 ? &maps.k : &maps.v;
-                const int own = p.cluster - 1; // box i belongs to CTA rank (i & own)
                 for (int bx = 0; bx < nbox; ++bx) {
                     const int page = __shfl_sync(0xffffffffu, ids, bx);
-                    if (lane != 0 || (bx & own) != cl_rank)
+                    if (lane != 0)
                         continue;
                     const int slot = (tok0 + bx * BT) & (P - 1);
                     if (nhd)
-                        pf_tma5(p, dst + bx * box_bytes, map, (page * P + slot) >> 3, g, &bars.full[stage]);
+                        tma_load_5d_plain(dst + bx * box_bytes, map, 0, 0, 0, (page * P + slot) >> 3, g,
+                                          &bars.full[stage]);
                     else
-                        pf_tma5(p, dst + bx * box_bytes, map, slot >> 3, page * Hkv + g, &bars.full[stage]);
+                        tma_load_5d_plain(dst + bx * box_bytes, map, 0, 0, 0, slot >> 3, page * Hkv + g,
+                                          &bars.full[stage]);
                 }
                 issued = itg + 1;
             }
@@ -366,14 +357,10 @@ __device__ void pf_producer(const PfParams &p, const PfMapsDev &maps, uint8_t *s
         }
         ib += 2 * nt;
     }
-    // Copies still in flight into this CTA, and (in a cluster) the peers'
-    // releases of the last stages: once they have arrived nothing of the
-    // cluster writes into this CTA any more.  Immediate unless a wait gave up.
-    for (int itg = issued > C::kStages ? issued - C::kStages : 0; itg < issued; ++itg) {
+    // Copies still in flight into this CTA: once they have landed nothing
+    // writes into its shared memory any more.  Immediate unless a wait gave up.
+    for (int itg = issued > C::kStages ? issued - C::kStages : 0; itg < issued; ++itg)
         pf_wait(&bars.full[itg % C::kStages], (itg / C::kStages) & 1, bars, p.err_flag);
-        if (p.cluster > 1)
-            pf_wait(&bars.empty[itg % C::kStages], (itg / C::kStages) & 1, bars, p.err_flag);
-    }
 }
 
 // ---------------------------------------------------------------- MMA issuer
@@ -388,7 +375,6 @@ __device__ void pf_mma(const PfParams &p, uint8_t *smem, PfBars &bars, uint32_t 
     int ib = 0, gt0 = 0;
     uint32_t uc = 0;
     bool issued = false;
-    const uint16_t cl_mask = (uint16_t)((1u << p.cluster) - 1u);
     for (int k = 0;; ++k) {
         const int u = pf_unit_at(k, p.cluster);
         if (u >= n_units)
@@ -412,10 +398,7 @@ __device__ void pf_mma(const PfParams &p, uint8_t *smem, PfBars &bars, uint32_t 
                     tc_mma_bf16_ts(d, tmem + C::kColQ + kk * 8, kd + (uint64_t)(((kk >> 2) * 1024 + (kk & 3) * 32) >> 4),
                                    kIdescS, kk > 0 ? 1u : 0u);
                 tc_commit(&bars.s_full[gt & 1]);
-                if (p.cluster > 1) // the stage is refilled for the whole cluster
-                    tc_commit_mc(&bars.empty[stage], cl_mask);
-                else
-                    tc_commit(&bars.empty[stage]);
+                tc_commit(&bars.empty[stage]);
                 if (j == nt - 1)
                     tc_commit(&bars.q_empty);
             }
@@ -441,10 +424,7 @@ __device__ void pf_mma(const PfParams &p, uint8_t *smem, PfBars &bars, uint32_t 
                                    (jv > 0 || kk > 0) ? 1u : 0u);
                 }
                 tc_commit(&bars.o_done[gt & 1]);
-                if (p.cluster > 1)
-                    tc_commit_mc(&bars.empty[stage], cl_mask);
-                else
-                    tc_commit(&bars.empty[stage]);
+                tc_commit(&bars.empty[stage]);
             }
         }
         gt0 += nt;
@@ -748,14 +728,13 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(pf_smem_raw) + 1023) & ~uintptr_t(1023));
     PfBars &bars = *reinterpret_cast<PfBars *>(smem + C::kOffBar);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int cl_rank = p.cluster > 1 ? (int)cluster_ctarank() : 0;
 
     if (threadIdx.x == 0) {
         mbar_init(&bars.q_full, kPfSoftmaxThreads);
         mbar_init(&bars.q_empty, 1);
         for (int s = 0; s < C::kStages; ++s) {
             mbar_init(&bars.full[s], 1);
-            mbar_init(&bars.empty[s], p.cluster); // released by the MMA of every CTA of the cluster
+            mbar_init(&bars.empty[s], 1); // released by this CTA's MMAs
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&bars.s_full[i], 1);
@@ -778,10 +757,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         tmem_relinquish();
     }
     tc_fence_before();
-    if (p.cluster > 1)
-        cluster_sync(); // peers' barriers are initialised before any multicast reaches them
-    else
-        __syncthreads();
+    __syncthreads();
     tc_fence_after();
     if (p.pdl) // the plan (and, in a mixed step, the append) wrote what follows
         asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -789,19 +765,16 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     const int n_units = *p.n_pairs * p.num_kv_heads;
 
     if (warp == kPfProducerWarp)
-        pf_producer<D>(p, maps, smem, bars, n_units, lane, cl_rank);
+        pf_producer<D>(p, maps, smem, bars, n_units, lane);
     else if (warp == kPfMmaWarp) {
         if (lane == 0)
             pf_mma<D>(p, smem, bars, tmem, n_units);
         __syncwarp();
     } else
-        pf_softmax<D, PfCfg<D>, PfBars>(p, smem, bars, tmem, n_units, warp, lane, cl_rank);
+        pf_softmax<D, PfCfg<D>, PfBars>(p, smem, bars, tmem, n_units, warp, lane, 0);
 
     tc_fence_before();
-    if (p.cluster > 1)
-        cluster_sync(); // no CTA leaves while a peer may still multicast into it
-    else
-        __syncthreads();
+    __syncthreads();
     tc_fence_after();
     if (warp == kPfMmaWarp)
         tmem_dealloc(tmem, C::kTmemCols);
@@ -1546,9 +1519,9 @@ struct PfKernelEntry {
 };
 
 // head_dim 64 cannot be split into 64-column halves: one CTA per query tile,
-// K / V shared by the cluster through TMA multicast.  128 and 256: CTA pairs.
+// each loading its own K / V tiles.  128 and 256: CTA pairs.
 const PfKernelEntry kPfTable[] = {
-    {64, false, 2, reinterpret_cast<const void *>(&prefill_kernel<64>), PfCfg<64>::kSmem, kPfThreads},
+    {64, false, 1, reinterpret_cast<const void *>(&prefill_kernel<64>), PfCfg<64>::kSmem, kPfThreads},
     {128, true, 2, reinterpret_cast<const void *>(&prefill2_kernel<128>), Pf2Cfg<128>::kSmem, kPf2Threads},
     {256, true, 2, reinterpret_cast<const void *>(&prefill2_kernel<256>), Pf2Cfg<256>::kSmem, kPf2Threads},
 };

@@ -58,22 +58,23 @@ extern "C" PKV_API pkv_status pkv_decode_attn_noalloc(const pkv_cache_desc *desc
                                                       int32_t num_q_heads, float softmax_scale, void *out, float *lse,
                                                       int32_t *err_flag, void *stream)
 {
-    const size_t need = pkv_decode_workspace_size(batch, max_blocks, num_q_heads, desc);
-    if (need == 0) // invalid or unsupported arguments: report exactly which
-        return pkv_decode_attn_ex(desc, k_cache, v_cache, q, k_new, v_new, block_table, max_blocks, cache_seqlens,
-                                  batch, num_q_heads, softmax_scale, out, lse, nullptr, 0, err_flag, stream, 0u);
-    if (need > kNoAllocScratchBytes)
+    // Every argument check of pkv_decode_attn first, with a placeholder for
+    // the workspace (an aligned non-null address and no size limit), so an
+    // invalid call gets the same status it would get there and touches
+    // nothing: not the shared array, not the stream.
+    DecodeShape shape;
+    const pkv_status st = decode_check(desc, k_cache, v_cache, q, k_new, v_new, block_table, max_blocks,
+                                       cache_seqlens, batch, num_q_heads, softmax_scale, out,
+                                       reinterpret_cast<const void *>(uintptr_t(256)), ~size_t(0), 0u, &shape);
+    if (st != PKV_OK || batch == 0)
+        return st;
+    if (shape.bytes > kNoAllocScratchBytes)
         return PKV_ETOOBIG;
-    if (batch == 0)
-        return PKV_OK;
     void *scratch = nullptr;
     if (scratch_address(&scratch) != cudaSuccess)
         return PKV_ECUDA;
     // The combine tickets at the front of the workspace must start at zero;
     // every call shares the array, so clear them on the call's stream.
-    DecodeShape shape;
-    if (!decode_shape(batch, max_blocks, num_q_heads, *desc, &shape))
-        return PKV_EUNSUPPORTED;
     if (cudaMemsetAsync(scratch, 0, shape.off_ml, static_cast<cudaStream_t>(stream)) != cudaSuccess)
         return PKV_ECUDA;
     return pkv_decode_attn_ex(desc, k_cache, v_cache, q, k_new, v_new, block_table, max_blocks, cache_seqlens, batch,

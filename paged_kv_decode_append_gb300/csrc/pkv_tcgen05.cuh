@@ -218,47 +218,6 @@ __device__ __forceinline__ void cluster_sync()
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
-// Like tc_commit, but arrives on the barrier at the same shared-memory offset
-// in every CTA of the cluster named by `cta_mask`.
-__device__ __forceinline__ void tc_commit_mc(uint64_t *bar, uint16_t cta_mask)
-{
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::
-                     "r"(smem_addr(bar)),
-                 "h"(cta_mask)
-                 : "memory");
-}
-
-// Tiled TMA loads multicast to the same shared-memory offset (data and
-// complete_tx on the barrier at the same offset) in every CTA of `cta_mask`.
-__device__ __forceinline__ void tma_load_3d_mc(void *dst, const CUtensorMap *map, int x, int y, int z, uint64_t *bar,
-                                               uint16_t cta_mask)
-{
-    asm volatile("cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
-                 " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_addr(dst)),
-                 "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_addr(bar)), "h"(cta_mask)
-                 : "memory");
-}
-
-__device__ __forceinline__ void tma_load_4d_mc(void *dst, const CUtensorMap *map, int c0, int c1, int c2, int c3,
-                                               uint64_t *bar, uint16_t cta_mask)
-{
-    asm volatile("cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
-                 " [%0], [%1, {%2, %3, %4, %5}], [%6], %7;" ::"r"(smem_addr(dst)),
-                 "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_addr(bar)),
-                 "h"(cta_mask)
-                 : "memory");
-}
-
-__device__ __forceinline__ void tma_load_5d_mc(void *dst, const CUtensorMap *map, int c0, int c1, int c2, int c3,
-                                               int c4, uint64_t *bar, uint16_t cta_mask)
-{
-    asm volatile("cp.async.bulk.tensor.5d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
-                 " [%0], [%1, {%2, %3, %4, %5, %6}], [%7], %8;" ::"r"(smem_addr(dst)),
-                 "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4),
-                 "r"(smem_addr(bar)), "h"(cta_mask)
-                 : "memory");
-}
-
 // --- CTA pairs (cta_group::2) ---------------------------------------------
 // A pair is CTA ranks 2i and 2i+1 of a cluster.  One thread of the even CTA
 // issues MMAs with M = 256: rows 0..127 of A and D live in the even CTA

@@ -360,12 +360,16 @@ class SweepCase:
 
 def batch_sweep(batch: int, device="cuda", contiguous: bool = True, layers: int = SWEEP_LAYERS,
                 decode_steps: int = SWEEP_DECODE_STEPS, seed: int | None = None,
-                data_device=None) -> SweepCase:
+                data_device=None, fill_decode: bool = False) -> SweepCase:
     """Batch-sweep state: prompt K/V pre-filled in every layer's pool, every
     slot past the prompt NaN.  Pages for prompt + ``decode_steps`` tokens are
     reserved up front, sequentially (contiguous) or from a seeded permutation
     (shuffled).  Random draws for the caches are made on ``data_device``
-    (default: ``device``) so multi-GB pools fill quickly."""
+    (default: ``device``) so multi-GB pools fill quickly.
+
+    fill_decode: also fill the ``decode_steps`` slots after the prompt with
+    seeded tokens, as earlier decode steps would have appended them, so that
+    any decode step can be run first and attends finite values only."""
     seed = 2 if seed is None else seed
     g = _gen(seed)
     data_device = device if data_device is None else data_device
@@ -380,8 +384,9 @@ def batch_sweep(batch: int, device="cuda", contiguous: bool = True, layers: int 
     else:
         order = (torch.randperm(num_pages - 1, generator=g).numpy() + 1).astype(np.int32)
     bt = assign_pages(needed, num_pages, max_blocks, order)
-    b_idx = np.concatenate([np.full(int(n), b, np.int64) for b, n in enumerate(prompt)])
-    t_idx = np.concatenate([np.arange(int(n), dtype=np.int64) for n in prompt])
+    filled = prompt + (decode_steps if fill_decode else 0)
+    b_idx = np.concatenate([np.full(int(n), b, np.int64) for b, n in enumerate(filled)])
+    t_idx = np.concatenate([np.arange(int(n), dtype=np.int64) for n in filled])
     pages, slots = bt[b_idx, t_idx // P], t_idx % P
     shape = (num_pages, P, Hkv, D)
     ks, vs = [], []

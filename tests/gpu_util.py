@@ -1,5 +1,7 @@
 """Helpers shared by the GPU parity tests: run the oracle on the same seeded
 inputs and compare within the stated tolerance."""
+import os
+
 import numpy as np
 import torch
 
@@ -9,14 +11,25 @@ from paged_kv_decode_append_gb300 import workloads as wl
 # Attention outputs (bf16 in, fp32 accumulate, bf16 out) must be within
 # max-abs 1e-2 and max-rel 1e-2 of the fp64 oracle.  Relative error is taken
 # over elements with |ref| >= 1e-2 (below that, fp32 rounding of the softmax
-# sum dominates any relative measure).  The bound applies to the computed
-# value; the bf16 output format then adds its own rounding of at most half an
-# ulp of the result (2^-9 |ref| relative), which the abs bound allows for
-# (it exceeds 1e-2 by itself once |ref| >= 4).
+# sum dominates any relative measure).  One allowance on the abs bound: the
+# output format is bf16, whose rounding alone moves a value by up to half an
+# ulp, 2^-9 |ref| relative; from |ref| >= 4 that half-ulp is 2^-6 > 1e-2, so
+# there (and only there) the abs bound is 1e-2 plus the half-ulp of ref.
 ATOL = 1e-2
 RTOL = 1e-2
 REL_FLOOR = 1e-2
 LSE_ATOL = 1e-2
+ULP_FROM = 4.0
+
+# (test, what, max-abs, max-rel, elements) of every comparison in this
+# session; conftest prints them after the run so the margins show in the log.
+MARGINS = []
+
+
+def _record(what, max_abs, max_rel, n):
+    test = os.environ.get("PYTEST_CURRENT_TEST", "?").split(" ")[0]
+    MARGINS.append((test, what, max_abs, max_rel, n))
+    print(f"{test} {what}: max-abs {max_abs:.3e} max-rel {max_rel:.3e} over {n} elements")
 
 
 def assert_close(got: np.ndarray, ref: np.ndarray, what: str = "out"):
@@ -28,8 +41,11 @@ def assert_close(got: np.ndarray, ref: np.ndarray, what: str = "out"):
     max_abs = float(err.max()) if err.size else 0.0
     big = np.abs(ref) >= REL_FLOOR
     max_rel = float((err[big] / np.abs(ref[big])).max()) if big.any() else 0.0
-    excess = err - (ATOL + bf16_half_ulp(ref))
-    assert not (excess > 0).any(), f"{what}: max-abs {max_abs:.3e} > {ATOL} + output rounding"
+    _record(what, max_abs, max_rel, int(err.size))
+    bound = np.where(np.abs(ref) >= ULP_FROM, ATOL + bf16_half_ulp(ref), ATOL)
+    excess = err - bound
+    assert not (excess > 0).any(), (f"{what}: max-abs {max_abs:.3e} > {ATOL} "
+                                    f"(+ bf16 output half-ulp where |ref| >= {ULP_FROM})")
     assert max_rel <= RTOL, f"{what}: max-rel {max_rel:.3e} > {RTOL}"
     return max_abs, max_rel
 
@@ -47,6 +63,7 @@ def assert_lse_close(got: np.ndarray, ref: np.ndarray):
     assert np.array_equal(np.isneginf(got), inf), "lse: -inf pattern differs"
     if (~inf).any():
         err = float(np.abs(got[~inf] - ref[~inf]).max())
+        _record("lse", err, 0.0, int((~inf).sum()))
         assert err <= LSE_ATOL, f"lse: max-abs {err:.3e}"
 
 

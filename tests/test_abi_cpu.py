@@ -191,6 +191,18 @@ def test_noalloc_rejects_problems_beyond_its_scratch():
     st = lib.pkv_decode_attn_noalloc(ctypes.byref(small), FAKE, FAKE, FAKE, None, None, FAKE, 4, FAKE, 4, 6 * 8, 0.1,
                                      FAKE, None, None, None)
     assert st == pkv.api.EUNSUPPORTED  # argument errors are those of pkv_decode_attn
+    # an invalid call that is also too big gets the argument error, not ETOOBIG
+    for args in ((None, FAKE), (FAKE, ctypes.c_void_p(0x10004))):  # null q; misaligned out
+        q, out = args
+        st = lib.pkv_decode_attn_noalloc(ctypes.byref(big), FAKE, FAKE, q, None, None, FAKE, 4, FAKE, 4, 64, 0.1,
+                                         out, None, None, None)
+        assert st == pkv.api.EINVAL
+    st = lib.pkv_decode_attn_noalloc(ctypes.byref(big), FAKE, FAKE, FAKE, None, None, FAKE, 4, FAKE, 4, 64,
+                                     float("nan"), FAKE, None, None, None)
+    assert st == pkv.api.EINVAL
+    st = lib.pkv_decode_attn_noalloc(ctypes.byref(big), FAKE, FAKE, FAKE, None, None, FAKE, 4, FAKE, 0, 64, 0.1,
+                                     FAKE, None, None, None)
+    assert st == pkv.api.OK  # an empty batch is valid and launches nothing
 
 
 def _prefill(lib, desc, batch=2, hq=8, total_q=40, ws=FAKE, ws_bytes=1 << 30, q=FAKE, scale=0.1, max_blocks=4):

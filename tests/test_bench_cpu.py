@@ -78,3 +78,16 @@ def test_call_bytes_counts_every_stream():
     new = 2 * B * 2 * bench.HKV * bench.D * 2                      # new K/V read and appended
     table = 4 * int(sum((L + 1 + bench.P - 1) // bench.P for L in lens))
     assert bench.call_bytes(lens, B) == kv + qo + new + table + 4 * B
+
+
+def test_timed_steps_span_the_whole_cycle():
+    cap = bench.DECODE_CAPACITY
+    assert bench.timed_decode_steps(cap) == list(range(cap))  # one full cycle: every step once
+    for k in (1, 3, 5, 20, 100, 600):
+        steps = bench.timed_decode_steps(k)
+        assert len(steps) == k and all(0 <= s < cap for s in steps)
+        if k <= cap:
+            assert steps == sorted(set(steps))  # distinct, in cycle order
+        # the mean decode step of the sample is the cycle's mean, within half a stride
+        assert abs(np.mean(steps) - (cap - 1) / 2) <= cap / (2 * k) + 0.5
+    assert bench.timed_decode_steps(20)[0] < 32 and bench.timed_decode_steps(20)[-1] > cap - 32

@@ -161,8 +161,10 @@ def test_batch_sweep_full_cycle(batch, contiguous):
 def test_decode_step_graph_with_padded_bucket():
     """Three layers captured once as a decode-step graph for the 16-row bucket
     of 13 live rows (rows 13..15 inactive), replayed for two steps with the
-    inputs rewritten in place: bit-identical to direct calls, padding rows 0 /
-    -inf, caches appended identically."""
+    inputs rewritten in place.  Every layer's live rows match the fp64 oracle
+    (which replays the same appends on its own host copies) within tolerance
+    and direct calls bit for bit; padding rows are exactly 0 with lse -inf;
+    the appended tokens are bit-exact against the oracle's copies."""
     live, layers = 13, 3
     bucket = pkv.pkv_decode_bucket(live)
     assert bucket == 16
@@ -186,6 +188,10 @@ def test_decode_step_graph_with_padded_bucket():
                                 flags=flags)
     ws_ref = pkv.decode_workspace(live, sw.max_blocks, 32, desc, DEV)
     bt_ref = torch.as_tensor(bt_live, device=DEV)
+    rows = list(range(live))
+    need = sw.prompt_lens + 2  # the pages both steps touch
+    host = [wl.compact_rows(kc_g[layer], vc_g[layer], bt_live, rows, need, sw.page_size) for layer in range(layers)]
+    od = oracle.CacheDesc(host[0][0].shape[0], sw.page_size, 8, 128, wl.NHD)
     for step in range(2):
         lens = torch.as_tensor((sw.prompt_lens + step).astype(np.int32), device=DEV)
         ins = wl.sweep_step_inputs(sw, step, DEV, layers=layers)
@@ -195,7 +201,14 @@ def test_decode_step_graph_with_padded_bucket():
             kn[layer][:live] = kk
             vn[layer][:live] = vv
         step_graph.launch()
+        torch.cuda.synchronize()
         for layer, (qq, kk, vv) in enumerate(ins):
+            hk, hv, hbt = host[layer]  # the oracle appends into its copies as well
+            o_out, o_lse, o_err, _ = oracle.decode(od, hk, hv, wl.bits(qq), wl.bits(kk), wl.bits(vv), hbt,
+                                                   lens.cpu().numpy(), sw.softmax_scale)
+            assert o_err == 0
+            assert_close(f32(out[layer][:live]), o_out, what=f"graph step {step} layer {layer}")
+            assert_lse_close(lse[layer][:live].cpu().numpy(), o_lse)
             ref_lse = torch.empty(live, 32, dtype=torch.float32, device=DEV)
             ref = pkv.pkv_decode_attn(sw.k_caches[layer], sw.v_caches[layer], qq, kk, vv, bt_ref, lens,
                                       sw.softmax_scale, lse=ref_lse, workspace=ws_ref)
@@ -207,6 +220,8 @@ def test_decode_step_graph_with_padded_bucket():
     for layer in range(layers):
         assert torch.equal(kc_g[layer].view(torch.int16), sw.k_caches[layer].view(torch.int16))
         assert torch.equal(vc_g[layer].view(torch.int16), sw.v_caches[layer].view(torch.int16))
+        gk, gv, _ = wl.compact_rows(kc_g[layer], vc_g[layer], bt_live, rows, need, sw.page_size)
+        assert np.array_equal(gk, host[layer][0]) and np.array_equal(gv, host[layer][1])
 
 
 def _random_case(seed, B, Hq, Hkv, D, P, lens, layout=wl.NHD, spare=7):
