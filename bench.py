@@ -381,7 +381,7 @@ def timed_decode_steps(n: int) -> list:
     return [int((i + 0.5) * DECODE_CAPACITY / n) % DECODE_CAPACITY for i in range(n)]
 
 
-def cpu_baseline(sw, steps: list, budget_s: float = 12.0, host_layers: int = 2):
+def cpu_baseline(sw, steps: list, budget_s: float = 12.0, host_layers: int = 2, max_calls: int = 4000):
     """Times the fp64 oracle (all host cores) on whole layer calls (all rows
     and heads) of the timed decode steps, in order, until `budget_s` of
     oracle time is spent; returns GB/s of the same algorithmic bytes.  Every
@@ -400,9 +400,10 @@ def cpu_baseline(sw, steps: list, budget_s: float = 12.0, host_layers: int = 2):
     d = oracle.CacheDesc(host[0][0].shape[0], P, HKV, D, oracle.NHD)
     threads = oracle.max_threads(0)
     done_bytes, elapsed, calls, used = 0, 0.0, 0, []
-    for i, step in enumerate(steps * 4):
+    for i in range(max_calls):  # the timed steps in order, cyclically, until the budget is spent
         if elapsed >= budget_s:
             break
+        step = steps[i % len(steps)]
         lens = (sw.prompt_lens + step).astype(np.int32)
         layer = i % host_layers
         q, kn, vn = (wl.bits(t) for t in wl.sweep_step_inputs(sw, step, dev, layers=layer + 1)[layer])
@@ -427,7 +428,7 @@ def cpu_baseline(sw, steps: list, budget_s: float = 12.0, host_layers: int = 2):
     return {"value": done_bytes / elapsed / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
             "single_thread_value": one_bytes / one_t / 1e9,
             "single_thread_sample": f"one layer call of decode steps {steps[:2]}, one host thread",
-            "sample": f"{calls} layer calls (one per timed decode step, steps {min(used)}..{max(used)} of the "
+            "sample": f"{calls} layer calls (the timed decode steps in turn, steps {min(used)}..{max(used)} of the "
                       f"512-step cycle, of the 36-layer B={sw.batch} workload, all rows and heads), fp64 oracle "
                       f"with OpenMP over (row, head), {elapsed:.1f} s of oracle time"}
 
