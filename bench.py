@@ -558,19 +558,21 @@ def streamed_layer_calls(case, bt, lens, out, ws, nbytes, peak, dev, rounds: int
                                               for _ in range(copies - 1)]
     n_calls = copies * max(1, 24 // copies)
     flags = pkv.api.DECODE_OVERLAP_PROLOGUE | pkv.api.DECODE_EARLY_KV
+    # the calls share cache_seqlens and block_table: the first makes the step plan, the others reuse it
+    call_flags = [flags | (pkv.api.DECODE_MAKE_PLAN if i == 0 else pkv.api.DECODE_USE_PLAN) for i in range(n_calls)]
     stream = torch.cuda.Stream(dev)
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.stream(stream):
         for i in range(copies):  # warm-up outside the graph (opt-in attributes, first-call set-up)
             k, v = pools[i]
             pkv.pkv_decode_attn(k, v, case.q, case.k_new, case.v_new, bt, lens, case.softmax_scale, out=out,
-                                workspace=ws, layout=case.layout, flags=flags)
+                                workspace=ws, layout=case.layout, flags=call_flags[i])
         stream.synchronize()
         with torch.cuda.graph(graph, stream=stream):
             for i in range(n_calls):
                 k, v = pools[i % copies]
                 pkv.pkv_decode_attn(k, v, case.q, case.k_new, case.v_new, bt, lens, case.softmax_scale, out=out,
-                                    workspace=ws, layout=case.layout, flags=flags)
+                                    workspace=ws, layout=case.layout, flags=call_flags[i])
         graph.replay()
         graph.replay()
         stream.synchronize()
@@ -587,7 +589,8 @@ def streamed_layer_calls(case, bt, lens, out, ws, nbytes, peak, dev, rounds: int
     return {"value": gbs, "unit": "GB/s", "pct_of_hbm_peak": 100.0 * gbs / peak, "ms_per_call": ms,
             "copies": int(copies), "calls_per_graph": int(n_calls), "replays": rounds,
             "launch": "one CUDA graph of back-to-back calls, programmatic dependent launch (overlapped prologue "
-                      "and early K/V stream), each call on the next of the rotating pool copies",
+                      "and early K/V stream), each call on the next of the rotating pool copies; the first call "
+                      "makes the step plan, the others reuse it",
             "l2": f"{copies} rotating copies of the layer pool (copies x call bytes >= 4 x L2)"}
 
 
@@ -608,9 +611,9 @@ class Sweep:
     """The 36-layer batch-sweep decode of one rank: pools, per-step inputs and
     one CUDA graph per decode step (its layers' launches back to back)."""
 
-    def __init__(self, pkv, wl, args, dev, layout: str, seed: int, flags: int):
+    def __init__(self, pkv, wl, args, dev, layout: str, seed: int, flags: int, plan: bool):
         B, L = args.batch, args.layers
-        self.pkv, self.args, self.dev, self.B, self.L, self.flags = pkv, args, dev, B, L, flags
+        self.pkv, self.args, self.dev, self.B, self.L, self.flags, self.plan = pkv, args, dev, B, L, flags, plan
         self.sw = wl.batch_sweep(B, device=dev, contiguous=layout == "contiguous", layers=L, seed=seed,
                                  fill_decode=True)
         self.bt = torch.as_tensor(self.sw.block_table, device=dev)
@@ -626,10 +629,18 @@ class Sweep:
     def step_inputs(self, step):
         return self.inputs[step % len(self.inputs)]
 
+    def layer_flags(self, layer):
+        """Launch flags of one layer of a step: with step plans, layer 0 makes
+        the plan (one extra small kernel) and every later layer reuses it."""
+        if not self.plan:
+            return self.flags
+        api = self.pkv.api
+        return self.flags | (api.DECODE_MAKE_PLAN if layer == 0 else api.DECODE_USE_PLAN)
+
     def layer_call(self, step, layer, q, kn, vn, flags=None):
         self.pkv.pkv_decode_attn(self.sw.k_caches[layer], self.sw.v_caches[layer], q, kn, vn, self.bt,
                                  self.lens_dev[step], self.sw.softmax_scale, out=self.outs[layer], workspace=self.ws,
-                                 flags=self.flags if flags is None else flags)
+                                 flags=self.layer_flags(layer) if flags is None else flags)
 
     def graph(self, step):
         g = torch.cuda.CUDAGraph()
@@ -700,6 +711,8 @@ def main():
                     help="spec / chunked: longest row on the decode kernel (default: the library's)")
     ap.add_argument("--no-overlap", action="store_true",
                     help="plain launches instead of programmatic dependent launch between layers")
+    ap.add_argument("--no-plan", action="store_true",
+                    help="every layer plans its work split itself (no step plan shared by the layers)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -733,17 +746,20 @@ def main():
     # layers of one step read different caches: the next layer may stream its
     # K/V while the previous one finishes
     flags = 0 if args.no_overlap else pkv.api.DECODE_OVERLAP_PROLOGUE | pkv.api.DECODE_EARLY_KV
-    sweep = Sweep(pkv, wl, args, dev, args.layout, 2 + rank, flags)
+    plan = not args.no_plan
+    sweep = Sweep(pkv, wl, args, dev, args.layout, 2 + rank, flags, plan)
     sw = sweep.sw
     steps = timed_decode_steps(args.steps)
     warm_steps = timed_decode_steps(args.warmup)
     stream = torch.cuda.current_stream(dev)
 
     # The timed region: one CUDA graph per decode step, replayed back to back.
-    # It holds this one kernel only, so its average launch duration is the
-    # region time over the launches.
+    # It holds the decode kernel's launches (plus, with step plans, one small
+    # plan kernel per step that runs beside layer 0), so the decode kernel's
+    # average launch duration is the region time over its launches.
     ms, total_bytes, clocks = sweep.timed(warm_steps, steps, world, local)
     n_ev = args.steps * L
+    n_launch = n_ev + (args.steps if plan else 0)
     ms_max = max_over_ranks(ms, world, dev)
     all_bytes = sum_over_ranks(float(total_bytes), world, dev)
     value = all_bytes / (ms_max * 1e-3) / 1e9
@@ -815,7 +831,7 @@ def main():
         d_out = [d_out_all[layer * B * HQ * D:(layer + 1) * B * HQ * D].view(B, HQ, D) for layer in range(L)]
         graph = pkv.DecodeStep(sw.k_caches, sw.v_caches, [t[0] for t in d_in], [t[1] for t in d_in],
                                [t[2] for t in d_in], sweep.bt, d_seq, sw.softmax_scale, d_out, workspace=sweep.ws,
-                               flags=flags)
+                               flags=flags | (pkv.api.DECODE_USE_PLAN if plan else 0))
         sets.append((d_in_all, d_out_all, d_seq, graph))
     h_in = []
     for r in range(2):  # two pinned input sets, alternated
@@ -882,13 +898,13 @@ def main():
     contiguous = None
     if not args.no_contiguous:  # the same sweep on sequentially reserved pages
         other = "contiguous" if args.layout == "shuffled" else "shuffled"
-        csweep = Sweep(pkv, wl, args, dev, other, 2, flags)
+        csweep = Sweep(pkv, wl, args, dev, other, 2, flags, plan)
         c_ms, c_bytes, c_clocks = csweep.timed(warm_steps, steps, 1, local)
         c_val = c_bytes / (c_ms * 1e-3) / 1e9
         contiguous = {"layout": other, "value": c_val, "unit": "GB/s", "pct_of_hbm_peak": 100.0 * c_val / peak,
                       "ms_per_step": c_ms / args.steps, "steps": args.steps,
                       "algorithmic_bytes_per_launch": c_bytes / n_ev, "clocks": c_clocks,
-                      "gpu_launches": n_ev, "config": workload_config(args, other)}
+                      "gpu_launches": n_launch, "config": workload_config(args, other)}
         del csweep
         torch.cuda.empty_cache()
     single = None
@@ -930,9 +946,10 @@ def main():
                         "streams, double-buffered (step s+1's upload and step s-1's download overlap step s)"},
         "eager": {"value": eager_gbs, "unit": "GB/s", "steps": len(eager_steps),
                   "launch": "plain stream launches, no CUDA graph"},
-        "gpu_launches": n_ev,
-        "launch": "one CUDA graph per decode step (36 kernel launches" + (
-            ")" if args.no_overlap else ", programmatic dependent launch between them, K/V streamed early)"),
+        "gpu_launches": n_launch,
+        "launch": "one CUDA graph per decode step (36 decode kernel launches" + (
+            "" if args.no_overlap else ", programmatic dependent launch between them, K/V streamed early") + (
+            "; layer 0 also launches the step plan kernel and layers 1-35 reuse its plan)" if plan else ")"),
         "cpu_baseline": cpu,
         "contiguous": contiguous,
         "single_layer": single,

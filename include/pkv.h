@@ -81,6 +81,10 @@ typedef enum {
 #define PKV_ERR_QLEN 8     /* prefill / mixed step: a request with more queries than keys (or
                               than max_qlen), a query range outside [0, total_q), or a
                               decreasing qo_indptr */
+#define PKV_ERR_PLAN 16    /* decode with PKV_DECODE_USE_PLAN: the workspace held no plan for
+                              this call's sizes (the call planned for itself; outputs are
+                              valid), or the plan's lengths differ from cache_seqlens (a stale
+                              plan: outputs and appends are unspecified) */
 
 /* Geometry of one K or V page pool (both share it).  page_size is a power of
  * two in [1, 256]; head_dim is 64, 128 or 256; num_pages >= 2 (page 0 is the
@@ -125,7 +129,8 @@ PKV_API pkv_status pkv_append(const pkv_cache_desc *desc, void *k_cache, void *v
 /*
  * pkv_decode_workspace_size -- bytes of device workspace pkv_decode_attn
  * needs for these sizes (0 on invalid arguments).  The workspace holds the
- * split-KV partial results and one combine ticket per (row, kv head).  It
+ * split-KV partial results, one combine ticket per (row, kv head) and room
+ * for one step plan (see PKV_DECODE_MAKE_PLAN; the plan needs no zeroing).  It
  * must be zero-filled once before its first use (e.g. cudaMemsetAsync);
  * every completed call leaves the tickets at zero again, so it can be reused
  * by later calls with the same or smaller sizes.  After a call that raised
@@ -186,6 +191,33 @@ PKV_API pkv_status pkv_decode_attn(const pkv_cache_desc *desc, void *k_cache, vo
  * stream does not write this call's cache pages -- for instance the
  * projection producing q / k_new / v_new, or the attention of another layer.
  * Capturable in CUDA graphs. */
+
+#define PKV_DECODE_MAKE_PLAN 4u
+/* Step plans.  The work split of a decode call (which CTA streams which
+ * tokens of which row, and its first page ids) depends only on
+ * cache_seqlens, block_table and the sizes, so every layer of one decode
+ * step shares it.  With PKV_DECODE_MAKE_PLAN the call also writes its plan
+ * into the workspace: a small plan kernel runs before the decode kernel
+ * (an ordinary launch, so everything earlier in the stream has completed
+ * when it reads cache_seqlens and block_table).  The decode kernel itself
+ * plans as without the flag.  Source: "flex_attention + paged KV + CUDA
+ * graphs vs vLLM", "Why this works" (the per-step metadata is built once
+ * and every layer of the step replays against it). */
+
+#define PKV_DECODE_USE_PLAN 8u
+/* The call takes its plan from the workspace instead of deriving it, so its
+ * CTAs reach their first K/V load one dependent memory round trip after they
+ * start.  The workspace must hold the plan of an earlier PKV_DECODE_MAKE_PLAN
+ * call on the same stream, made with the same desc, batch, max_blocks,
+ * num_q_heads and (non-)NULL k_new, and with cache_seqlens and block_table
+ * holding the same values then as now (the layers of one decode step).
+ * Every decode kernel signals its dependents only after the kernel before
+ * it has completed, so the plan kernel has completed before any later
+ * launch starts.  A plan made for other sizes (or none) is not used: the
+ * call plans for itself and sets PKV_ERR_PLAN.  A plan whose lengths differ
+ * from cache_seqlens sets PKV_ERR_PLAN too; then the outputs and appended
+ * tokens are unspecified (every address stays inside the pools and the
+ * workspace).  Not together with PKV_DECODE_MAKE_PLAN. */
 
 /*
  * pkv_decode_attn_ex -- pkv_decode_attn with launch flags (PKV_DECODE_*).
@@ -259,6 +291,8 @@ PKV_API int32_t pkv_decode_bucket(int32_t batch);
  *    work; nothing is launched by this call.
  *  - With PKV_DECODE_OVERLAP_PROLOGUE (and PKV_DECODE_EARLY_KV) the layers
  *    overlap inside the graph as described for pkv_decode_attn_ex.
+ *  - With PKV_DECODE_USE_PLAN the first layer is captured with
+ *    PKV_DECODE_MAKE_PLAN instead and every later layer reuses its plan.
  * On success *step_out owns the graph; free it with pkv_decode_step_destroy.
  */
 PKV_API pkv_status pkv_decode_step_create(const pkv_cache_desc *desc, int32_t num_layers, void *const *k_caches,

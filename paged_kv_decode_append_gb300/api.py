@@ -19,7 +19,9 @@ HND = 1
 OK, EINVAL, EUNSUPPORTED, ECUDA, ENOPAGES, EWORKSPACE, ETOOBIG = range(7)
 DECODE_OVERLAP_PROLOGUE = 1  # pkv_decode_attn_ex flags (see include/pkv.h)
 DECODE_EARLY_KV = 2
-ERR_PAGE, ERR_OVERFLOW, ERR_TIMEOUT, ERR_QLEN = 1, 2, 4, 8
+DECODE_MAKE_PLAN = 4
+DECODE_USE_PLAN = 8
+ERR_PAGE, ERR_OVERFLOW, ERR_TIMEOUT, ERR_QLEN, ERR_PLAN = 1, 2, 4, 8, 16
 
 
 class PkvError(RuntimeError):

@@ -219,9 +219,12 @@ pkv_status decode_check(const pkv_cache_desc *desc, const void *k_cache, const v
                         const void *out, const void *workspace, size_t workspace_bytes, uint32_t flags,
                         DecodeShape *shape)
 {
-    if ((flags & ~(PKV_DECODE_OVERLAP_PROLOGUE | PKV_DECODE_EARLY_KV)) != 0)
+    if ((flags & ~(PKV_DECODE_OVERLAP_PROLOGUE | PKV_DECODE_EARLY_KV | PKV_DECODE_MAKE_PLAN |
+                   PKV_DECODE_USE_PLAN)) != 0)
         return PKV_EINVAL;
     if ((flags & PKV_DECODE_EARLY_KV) && !(flags & PKV_DECODE_OVERLAP_PROLOGUE))
+        return PKV_EINVAL;
+    if ((flags & PKV_DECODE_MAKE_PLAN) && (flags & PKV_DECODE_USE_PLAN))
         return PKV_EINVAL;
     const pkv_status st = check_desc(desc);
     if (st != PKV_OK)

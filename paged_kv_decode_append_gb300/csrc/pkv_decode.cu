@@ -103,6 +103,11 @@ struct KParams {
     int mq_max;      // q_len > mq_max is malformed (PKV_ERR_QLEN) ...
     int mq_own_long; // ... and zeroed here when no other kernel serves long rows
     int mq_kv_add;   // 1: the row's new tokens are cached (kv = L + q_len); 0: kv = L
+    // Step plans (plain rows only): the plan region of the workspace this
+    // launch reads its plan from (PKV_DECODE_USE_PLAN), or the one the plan
+    // kernel writes (PKV_DECODE_MAKE_PLAN); nullptr otherwise.
+    const unsigned char *plan_in;
+    unsigned char *plan_out;
 };
 
 // K/V stages in flight per CTA, as many as keep two CTAs on an SM (head_dim
@@ -124,6 +129,8 @@ constexpr int warp_cols()
 
 template <int D, int GC, bool MQ>
 struct Smem {
+    static constexpr int kGC = GC;
+    static constexpr bool kMQ = MQ;
     static constexpr int kStages = stages_for<D, GC>();
     static constexpr int RC = warp_cols<GC>();
     // [stage][K|V] tiles laid out [kTile/8][D/64][8][64]: 8-token groups of
@@ -145,6 +152,7 @@ struct Smem {
     int32_t geff;                        // CTAs that own a token slice
     int32_t n_empty;                     // rows with output units but no cached token
     int32_t abort;
+    int32_t plan_state;                  // 0: planned here, 1: step plan used, 2: step plan rejected
 };
 
 // Programmatic dependent launch: wait for the preceding grid (and its memory)
@@ -228,8 +236,8 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, vo
 // moved to token positions (see boundary), so the per-unit cost of starting
 // a slice (page ids, queries, a hand-off to the epilogue) is balanced along
 // with the tokens.
-template <int D, int GC, bool MQ>
-__device__ void build_plan_rows(const KParams &p, Smem<D, GC, MQ> &sm)
+template <class SM>
+__device__ void build_plan_rows(const KParams &p, SM &sm, int grid)
 {
     for (int i = threadIdx.x; i < p.batch; i += kThreads)
         sm.len[i] = p.seqlens[i];
@@ -264,8 +272,8 @@ __device__ void build_plan_rows(const KParams &p, Smem<D, GC, MQ> &sm)
             sm.rowbase[p.batch] = (long long)p.units * ((long long)run + (long long)kSliceStartCost * nonempty);
             const long long work = (long long)p.units * ((long long)run + (long long)kSliceStartCost * nonempty);
             long long g = work / kMinSlice;
-            if (g > gridDim.x)
-                g = gridDim.x;
+            if (g > grid)
+                g = grid;
             if (g < 1)
                 g = 1;
             const long long slice = work > 0 ? (work + g - 1) / g : 1;
@@ -279,9 +287,10 @@ __device__ void build_plan_rows(const KParams &p, Smem<D, GC, MQ> &sm)
 }
 
 // Multi-query rows: units per row differ, so the work positions are summed directly.
-template <int D, int GC, bool MQ>
-__device__ void build_plan_mq(const KParams &p, Smem<D, GC, MQ> &sm)
+template <class SM>
+__device__ void build_plan_mq(const KParams &p, SM &sm, int grid)
 {
+    constexpr int GC = SM::kGC;
     for (int i = threadIdx.x; i < p.batch; i += kThreads) {
         sm.len[i] = p.seqlens[i];
         const int s = p.qo_indptr[i], e = p.qo_indptr[i + 1];
@@ -326,8 +335,8 @@ __device__ void build_plan_mq(const KParams &p, Smem<D, GC, MQ> &sm)
             sm.rowbase[p.batch] = wrun;
             const long long work = wrun;
             long long g = work / kMinSlice;
-            if (g > gridDim.x)
-                g = gridDim.x;
+            if (g > grid)
+                g = grid;
             if (g < 1)
                 g = 1;
             const long long slice = work > 0 ? (work + g - 1) / g : 1;
@@ -340,22 +349,22 @@ __device__ void build_plan_mq(const KParams &p, Smem<D, GC, MQ> &sm)
     __syncthreads();
 }
 
-template <int D, int GC, bool MQ>
-__device__ __forceinline__ void build_plan(const KParams &p, Smem<D, GC, MQ> &sm)
+// grid: the CTAs of the decode launch the plan is for.
+template <class SM>
+__device__ __forceinline__ void build_plan(const KParams &p, SM &sm, int grid)
 {
-    if constexpr (MQ)
-        build_plan_mq(p, sm);
+    if constexpr (SM::kMQ)
+        build_plan_mq(p, sm, grid);
     else
-        build_plan_rows(p, sm);
+        build_plan_rows(p, sm, grid);
 }
 
 // Unit containing work position x (x < work): row b, unit r in the row and
 // the offset rel inside the unit's kSliceStartCost + n positions; returns the
 // unit's first token position.  units * (row tokens + cost) < 2^31 (checked
 // on the host), so in-row math is 32-bit.
-template <int D, int GC, bool MQ>
-__device__ __forceinline__ long long locate(const KParams &p, const Smem<D, GC, MQ> &sm, long long x, int &b, int &r,
-                                            int &rel)
+template <class SM>
+__device__ __forceinline__ long long locate(const KParams &p, const SM &sm, long long x, int &b, int &r, int &rel)
 {
     int lo = 0, hi = p.batch - 1; // largest row starting at or before x (never an empty row)
     while (lo < hi) {
@@ -377,8 +386,8 @@ __device__ __forceinline__ long long locate(const KParams &p, const Smem<D, GC, 
 // First position of CTA k's range (k in [0, geff]): k * slice moved to a
 // token position -- the unit's first token if it falls on the unit's virtual
 // positions, else rounded down to a multiple of the tile inside the unit.
-template <int D, int GC, bool MQ>
-__device__ __forceinline__ long long boundary(const KParams &p, const Smem<D, GC, MQ> &sm, int k)
+template <class SM>
+__device__ __forceinline__ long long boundary(const KParams &p, const SM &sm, int k)
 {
     const long long x = (long long)k * sm.slice;
     if (x >= sm.work)
@@ -391,8 +400,8 @@ __device__ __forceinline__ long long boundary(const KParams &p, const Smem<D, GC
 
 // CTA whose range holds token position x (x < work): close to x / slice, the
 // boundaries being at most kTile below or kSliceStartCost above k * slice.
-template <int D, int GC, bool MQ>
-__device__ __forceinline__ int owner_of(const KParams &p, const Smem<D, GC, MQ> &sm, long long x)
+template <class SM>
+__device__ __forceinline__ int owner_of(const KParams &p, const SM &sm, long long x)
 {
     int k = (int)(x / sm.slice);
     if (k > sm.geff - 1)
@@ -413,9 +422,11 @@ struct Seg {
 };
 
 // Row-level fields of unit r of row b (everything but the token range).
-template <int D, int GC, bool MQ>
-__device__ __forceinline__ void seg_unit(const KParams &p, const Smem<D, GC, MQ> &sm, Seg &s, int b, int r)
+template <class SM>
+__device__ __forceinline__ void seg_unit(const KParams &p, const SM &sm, Seg &s, int b, int r)
 {
+    constexpr int GC = SM::kGC;
+    constexpr bool MQ = SM::kMQ;
     s.b = b;
     s.r = r;
     s.unit = b * p.units + r;
@@ -449,8 +460,8 @@ struct SegIter {
     long long t0_f, t0_l;
     int b_f, r_f, b_l, r_l;
     int stage; // 0: first slice, 1: last slice, 2: middle units, 3: done
-    template <int D, int GC, bool MQ>
-    __device__ __forceinline__ void init(const KParams &p, const Smem<D, GC, MQ> &sm, int k)
+    template <class SM>
+    __device__ __forceinline__ void init(const KParams &p, const SM &sm, int k)
     {
         stage = 3;
         if (k >= sm.geff)
@@ -468,8 +479,8 @@ struct SegIter {
         f_end = min(end, t0_f + (sm.rowtok[b_f + 1] - sm.rowtok[b_f]));
         stage = 0;
     }
-    template <int D, int GC, bool MQ>
-    __device__ __forceinline__ void fill(const KParams &p, const Smem<D, GC, MQ> &sm, Seg &s, int b, int r, long long t0,
+    template <class SM>
+    __device__ __forceinline__ void fill(const KParams &p, const SM &sm, Seg &s, int b, int r, long long t0,
                                          long long from, long long to)
     {
         seg_unit(p, sm, s, b, r);
@@ -478,8 +489,8 @@ struct SegIter {
         s.tok0 = (int)(from - t0);
         s.tok1 = (int)(to - t0);
     }
-    template <int D, int GC, bool MQ>
-    __device__ __forceinline__ bool next(const KParams &p, const Smem<D, GC, MQ> &sm, Seg &s)
+    template <class SM>
+    __device__ __forceinline__ bool next(const KParams &p, const SM &sm, Seg &s)
     {
         if (stage == 0) {
             fill(p, sm, s, b_f, r_f, t0_f, pos0, f_end);
@@ -518,6 +529,72 @@ struct SegIter {
     }
 };
 
+// ---------------------------------------------------------------- step plans
+// A step plan (PKV_DECODE_MAKE_PLAN) is the shared-memory plan above written
+// to the workspace, plus one record per CTA of the decode launch: its
+// SegIter after the first slice was taken, that slice, and the page ids of
+// the slice's first window.  A later launch of the same step
+// (PKV_DECODE_USE_PLAN) copies the plan instead of deriving it, and its
+// producer issues the first tile straight from the record.
+constexpr uint32_t kPlanMagic = 0x31564b50u; // "PKV1"
+constexpr int kPlanRecBytes = 256;
+
+struct PlanHeader {
+    uint32_t magic;
+    int32_t batch, units, grid, max_blocks, page_size, with_new, num_kv_heads;
+    long long work, slice;
+    int32_t geff, n_empty;
+};
+
+struct PlanRec {
+    SegIter si; // after the first next()
+    int32_t have, b, kvh, tok0, tok1;
+    int32_t pages[32];
+};
+static_assert(sizeof(PlanRec) <= kPlanRecBytes, "plan record");
+static_assert(sizeof(PlanHeader) <= 256, "plan header");
+
+// Offsets (bytes, from the plan region's start) of a plan for `batch` rows.
+struct PlanLayout {
+    size_t len, rowtok, rowbase, recs, bytes;
+};
+
+__host__ __device__ inline PlanLayout plan_layout(int batch)
+{
+    auto al = [](size_t x) { return (x + 255) & ~size_t(255); };
+    PlanLayout l;
+    l.len = 256;
+    l.rowtok = l.len + al(4 * (size_t)batch);
+    l.rowbase = l.rowtok + al(4 * ((size_t)batch + 1));
+    l.recs = l.rowbase + al(8 * ((size_t)batch + 1));
+    l.bytes = l.recs + (size_t)kMaxGrid * kPlanRecBytes;
+    return l;
+}
+
+// The plan's header matches this launch (every thread takes the same decision).
+__device__ __forceinline__ bool plan_matches(const KParams &p, const PlanHeader *h)
+{
+    return __ldcg(&h->magic) == kPlanMagic && __ldcg(&h->batch) == p.batch && __ldcg(&h->units) == p.units &&
+           __ldcg(&h->grid) == (int)gridDim.x && __ldcg(&h->max_blocks) == p.max_blocks &&
+           __ldcg(&h->page_size) == p.page_size && __ldcg(&h->with_new) == p.with_new &&
+           __ldcg(&h->num_kv_heads) == p.num_kv_heads;
+}
+
+// Copy of a plain-old-data record from global memory, bypassing L1 (the plan
+// of an earlier kernel).
+template <class T>
+__device__ __forceinline__ T ldcg_pod(const T *src)
+{
+    static_assert(sizeof(T) % 4 == 0, "whole words");
+    T v;
+    const int *s = reinterpret_cast<const int *>(src);
+    int *d = reinterpret_cast<int *>(&v);
+#pragma unroll
+    for (int i = 0; i < (int)(sizeof(T) / 4); ++i)
+        d[i] = __ldcg(s + i);
+    return v;
+}
+
 // ---------------------------------------------------------------- producer
 // Page ids of 32 consecutive blocks of a row, one per lane (0 past `last`).
 __device__ __forceinline__ int load_window(const int32_t *bt_row, int first, int last, int lane)
@@ -525,8 +602,11 @@ __device__ __forceinline__ int load_window(const int32_t *bt_row, int first, int
     return first + lane <= last ? bt_row[first + lane] : 0;
 }
 
+// rec: this CTA's record of a step plan.  Its first slice is then issued
+// before the shared-memory plan is ready; the producer meets the other warps
+// (named barrier 1) right after that first tile.
 template <int D, int GC, bool MQ>
-__device__ void producer(const KParams &p, Smem<D, GC, MQ> &sm, const DecodeMaps *maps)
+__device__ void producer(const KParams &p, Smem<D, GC, MQ> &sm, const DecodeMaps *maps, const PlanRec *rec)
 {
     constexpr int S = Smem<D, GC, MQ>::kStages;
     const int lane = threadIdx.x & 31;
@@ -537,13 +617,37 @@ __device__ void producer(const KParams &p, Smem<D, GC, MQ> &sm, const DecodeMaps
     uint32_t g_tile = 0;
     volatile int32_t *abort = &sm.abort;
     SegIter si;
-    si.init(p, sm, blockIdx.x);
     Seg sg, nx;
-    bool have = si.next(p, sm, sg);
-    // first window of the current slice, prefetched one slice ahead
-    int win = have ? load_window(p.block_table + (int64_t)sg.b * p.max_blocks, sg.tok0 >> p.page_shift,
+    bool have;
+    int win; // first window of the current slice, prefetched one slice ahead
+    if (rec != nullptr) {
+        si = ldcg_pod(&rec->si);
+        have = __ldcg(&rec->have) != 0;
+        sg.b = __ldcg(&rec->b);
+        sg.kvh = __ldcg(&rec->kvh);
+        sg.tok0 = __ldcg(&rec->tok0);
+        sg.tok1 = __ldcg(&rec->tok1);
+        win = __ldcg(&rec->pages[lane]);
+        // the record is only trusted as far as its addresses go: a bad row or
+        // kv head fails like a bad page (below), never forms an address
+        if (have && (sg.b < 0 || sg.b >= p.batch || sg.kvh < 0 || sg.kvh >= p.num_kv_heads || sg.tok0 < 0 ||
+                     sg.tok1 <= sg.tok0 || sg.tok1 > p.max_blocks * p.page_size)) {
+            have = false;
+            if (lane == 0)
+                sm.abort = 1;
+        }
+    } else {
+        si.init(p, sm, blockIdx.x);
+        have = si.next(p, sm, sg);
+        win = have ? load_window(p.block_table + (int64_t)sg.b * p.max_blocks, sg.tok0 >> p.page_shift,
                                  (sg.tok1 - 1) >> p.page_shift, lane)
                    : 0;
+    }
+    bool met = rec == nullptr; // met the other warps at named barrier 1
+    // live page ids of the record's window (checked against it once loaded)
+    int live0 = 0, rec0 = win;
+    const int32_t *rec_row = have ? p.block_table + (int64_t)sg.b * p.max_blocks : nullptr;
+    const int rec_first = have ? sg.tok0 >> p.page_shift : 0, rec_last = have ? (sg.tok1 - 1) >> p.page_shift : -1;
     // Page ids are loading.  K/V come after the preceding grid unless the
     // caller declared that it does not write this call's cache; the error
     // flag always does (below).
@@ -634,16 +738,30 @@ __device__ void producer(const KParams &p, Smem<D, GC, MQ> &sm, const DecodeMaps
             }
             __syncwarp();
             if (t == 0) { // next slice and its first page window, off the first tile's critical path
+                if (!met) {
+                    named_sync(1, kThreads); // the shared-memory plan is ready
+                    met = true;
+                    live0 = load_window(rec_row, rec_first, rec_last, lane);
+                }
                 more = si.next(p, sm, nx);
                 nwin = more ? load_window(p.block_table + (int64_t)nx.b * p.max_blocks, nx.tok0 >> p.page_shift,
                                           (nx.tok1 - 1) >> p.page_shift, lane)
                             : 0;
             }
         }
+        if (rec_row != nullptr) { // the record's window against the live table
+            if (__any_sync(0xffffffffu, live0 != rec0) && lane == 0) {
+                wait_prior_grid(p);
+                set_error(p.err_flag, PKV_ERR_PLAN);
+            }
+            rec_row = nullptr;
+        }
         have = more;
         sg = nx;
         win = nwin;
     }
+    if (!met)
+        named_sync(1, kThreads); // no tile issued: still meet the other warps
     // After an abort, let copies already issued land before the CTA exits.
     if (*abort && lane == 0) {
         const uint32_t first = g_tile > (uint32_t)S ? g_tile - S : 0;
@@ -999,6 +1117,11 @@ __device__ void consumers(const KParams &p, Smem<D, GC, MQ> &sm)
     bool have = si.next(p, sm, sg);
     uint32_t qf[KS][2];
     wait_prior_grid(p);
+    // Dependents may start only now that the grid before this one has
+    // completed: a later launch that reads a step plan before its own wait
+    // then finds the plan kernel (two or more launches back) complete.
+    if (p.pdl && threadIdx.x == 0)
+        asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     // a unit of more than 8 columns (GC = 16 only) splits its columns between
     // the warps: this warp's first column is cb
     bool wide = false;
@@ -1454,6 +1577,14 @@ __device__ void epilogue(const KParams &p, Smem<D, GC, MQ> &sm, int ew)
     int seg_i = 0;
     bool stopped = false;
     wait_prior_grid(p);
+    if (k == 0 && ew == 0) { // a step plan that was rejected, or whose lengths are stale
+        int bad = sm.plan_state == 2;
+        if (sm.plan_state == 1)
+            for (int i = lane; i < p.batch; i += 32)
+                bad |= p.seqlens[i] != sm.len[i];
+        if (__any_sync(0xffffffffu, bad) && lane == 0)
+            set_error(p.err_flag, PKV_ERR_PLAN);
+    }
     while (si.next(p, sm, sg)) {
         const int mine = seg_i;
         ++seg_i;
@@ -1587,26 +1718,77 @@ __device__ void epilogue(const KParams &p, Smem<D, GC, MQ> &sm, int ew)
 }
 
 template <int D, int GC, bool MQ>
+__device__ __forceinline__ void init_barriers(Smem<D, GC, MQ> &sm)
+{
+    constexpr int S = Smem<D, GC, MQ>::kStages;
+    for (int s = 0; s < S; ++s) {
+        mbar_init(&sm.full[s], 1);
+        mbar_init(&sm.empty[s], kWarps);
+    }
+    for (int s = 0; s < kSlots; ++s) {
+        mbar_init(&sm.epi_full[s], kWarps);
+        mbar_init(&sm.epi_empty[s], kEpiReaders<GC>());
+    }
+    sm.abort = 0;
+    mbar_init_fence();
+}
+
+template <int D, int GC, bool MQ>
 __device__ __forceinline__ void decode_body(const KParams &p, const DecodeMaps &maps)
 {
     extern __shared__ unsigned char smem_raw[];
     Smem<D, GC, MQ> &sm = *reinterpret_cast<Smem<D, GC, MQ> *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    constexpr int S = Smem<D, GC, MQ>::kStages;
     const int warp = threadIdx.x >> 5;
-    if (p.pdl && threadIdx.x == 0) // the next grid may start filling SMs this one frees
-        asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    // A step plan: taken when its header matches this launch (plain rows).
+    bool from_plan = false;
+    if constexpr (!MQ)
+        from_plan = p.plan_in != nullptr && plan_matches(p, reinterpret_cast<const PlanHeader *>(p.plan_in));
+    if (from_plan) {
+        if (warp == kProducerWarp) {
+            if ((threadIdx.x & 31) == 0) {
+                init_barriers(sm);
+                sm.plan_state = 1;
+                prefetch_tensormap(&maps.k);
+                prefetch_tensormap(&maps.v);
+                prefetch_tensormap(&maps.k8);
+                prefetch_tensormap(&maps.v8);
+            }
+            __syncwarp();
+            const PlanRec *rec = reinterpret_cast<const PlanRec *>(p.plan_in + plan_layout(p.batch).recs) + blockIdx.x;
+            producer(p, sm, &maps, rec); // meets the others at named barrier 1 after its first tile
+            return;
+        }
+        // the other warps copy the plan into shared memory meanwhile
+        const PlanLayout lay = plan_layout(p.batch);
+        const PlanHeader *h = reinterpret_cast<const PlanHeader *>(p.plan_in);
+        const int t = threadIdx.x < kProducerWarp * 32 ? threadIdx.x : threadIdx.x - 32; // 0 .. 127
+        constexpr int kCopy = kThreads - 32;
+        const int32_t *len = reinterpret_cast<const int32_t *>(p.plan_in + lay.len);
+        const int32_t *rowtok = reinterpret_cast<const int32_t *>(p.plan_in + lay.rowtok);
+        const long long *rowbase = reinterpret_cast<const long long *>(p.plan_in + lay.rowbase);
+        for (int i = t; i < p.batch; i += kCopy)
+            sm.len[i] = __ldcg(len + i);
+        for (int i = t; i <= p.batch; i += kCopy) {
+            sm.rowtok[i] = __ldcg(rowtok + i);
+            sm.rowbase[i] = __ldcg(rowbase + i);
+        }
+        if (t == 0) {
+            sm.work = __ldcg(&h->work);
+            sm.slice = __ldcg(&h->slice);
+            sm.geff = __ldcg(&h->geff);
+            sm.n_empty = __ldcg(&h->n_empty);
+        }
+        named_sync(1, kThreads); // plan and barriers ready
+        if (warp < kWarps)
+            consumers(p, sm);
+        else
+            epilogue(p, sm, warp - kEpilogueWarp);
+        return;
+    }
     if (threadIdx.x == 0) {
-        for (int s = 0; s < S; ++s) {
-            mbar_init(&sm.full[s], 1);
-            mbar_init(&sm.empty[s], kWarps);
-        }
-        for (int s = 0; s < kSlots; ++s) {
-            mbar_init(&sm.epi_full[s], kWarps);
-            mbar_init(&sm.epi_empty[s], kEpiReaders<GC>());
-        }
-        sm.abort = 0;
-        mbar_init_fence();
+        init_barriers(sm);
+        sm.plan_state = p.plan_in != nullptr ? 2 : 0;
     }
     if (threadIdx.x == kProducerWarp * 32) {
         prefetch_tensormap(&maps.k);
@@ -1614,13 +1796,78 @@ __device__ __forceinline__ void decode_body(const KParams &p, const DecodeMaps &
         prefetch_tensormap(&maps.k8);
         prefetch_tensormap(&maps.v8);
     }
-    build_plan(p, sm); // ends with __syncthreads()
+    build_plan(p, sm, (int)gridDim.x); // ends with __syncthreads()
     if (warp < kWarps)
         consumers(p, sm);
     else if (warp == kProducerWarp)
-        producer(p, sm, &maps);
+        producer(p, sm, &maps, nullptr);
     else
         epilogue(p, sm, warp - kEpilogueWarp);
+}
+
+// The plan kernel of PKV_DECODE_MAKE_PLAN: builds the plan of a decode launch
+// of `grid` CTAs (as every CTA of that launch would) and writes it to
+// p.plan_out, one record per CTA (one warp per record).  An ordinary launch;
+// it lets the decode kernel after it start at once (that kernel plans for
+// itself and does not read this plan).
+template <int D, int GC>
+__global__ void __launch_bounds__(kThreads) decode_plan_kernel(const __grid_constant__ KParams p, int grid)
+{
+    extern __shared__ unsigned char smem_raw[];
+    Smem<D, GC, false> &sm = *reinterpret_cast<Smem<D, GC, false> *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    if (threadIdx.x == 0)
+        asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    build_plan(p, sm, grid); // ends with __syncthreads()
+    const PlanLayout lay = plan_layout(p.batch);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    constexpr int kWarpsAll = kThreads / 32;
+    PlanRec *recs = reinterpret_cast<PlanRec *>(p.plan_out + lay.recs);
+    for (int k = blockIdx.x * kWarpsAll + warp; k < grid; k += gridDim.x * kWarpsAll) {
+        SegIter si;
+        si.init(p, sm, k);
+        Seg sg;
+        const bool have = si.next(p, sm, sg);
+        const int win = have ? load_window(p.block_table + (int64_t)sg.b * p.max_blocks, sg.tok0 >> p.page_shift,
+                                           (sg.tok1 - 1) >> p.page_shift, lane)
+                             : 0;
+        PlanRec *r = recs + k;
+        r->pages[lane] = win;
+        if (lane == 0) {
+            r->si = si;
+            r->have = have ? 1 : 0;
+            r->b = have ? sg.b : 0;
+            r->kvh = have ? sg.kvh : 0;
+            r->tok0 = have ? sg.tok0 : 0;
+            r->tok1 = have ? sg.tok1 : 0;
+        }
+    }
+    if (blockIdx.x != 0)
+        return;
+    int32_t *len = reinterpret_cast<int32_t *>(p.plan_out + lay.len);
+    int32_t *rowtok = reinterpret_cast<int32_t *>(p.plan_out + lay.rowtok);
+    long long *rowbase = reinterpret_cast<long long *>(p.plan_out + lay.rowbase);
+    for (int i = threadIdx.x; i < p.batch; i += kThreads)
+        len[i] = sm.len[i];
+    for (int i = threadIdx.x; i <= p.batch; i += kThreads) {
+        rowtok[i] = sm.rowtok[i];
+        rowbase[i] = sm.rowbase[i];
+    }
+    if (threadIdx.x == 0) {
+        PlanHeader *h = reinterpret_cast<PlanHeader *>(p.plan_out);
+        h->magic = kPlanMagic;
+        h->batch = p.batch;
+        h->units = p.units;
+        h->grid = grid;
+        h->max_blocks = p.max_blocks;
+        h->page_size = p.page_size;
+        h->with_new = p.with_new;
+        h->num_kv_heads = p.num_kv_heads;
+        h->work = sm.work;
+        h->slice = sm.slice;
+        h->geff = sm.geff;
+        h->n_empty = sm.n_empty;
+    }
 }
 
 template <int D, int GC, bool MQ>
@@ -1656,17 +1903,21 @@ struct KernelEntry {
     bool mq; // multi-query rows
     const void *fn;
     size_t smem;
+    const void *plan_fn; // its step-plan kernel (plain rows), same shared memory
 };
 
 template <int D, int GC, bool MQ>
 KernelEntry entry()
 {
     const void *fn;
+    const void *plan_fn = nullptr;
     if constexpr (GC > 8)
         fn = reinterpret_cast<const void *>(&decode_kernel_wide<D, GC, MQ>);
     else
         fn = reinterpret_cast<const void *>(&decode_kernel<D, GC, MQ>);
-    return KernelEntry{D, GC, MQ, fn, smem_bytes<D, GC, MQ>()};
+    if constexpr (!MQ)
+        plan_fn = reinterpret_cast<const void *>(&decode_plan_kernel<D, GC>);
+    return KernelEntry{D, GC, MQ, fn, smem_bytes<D, GC, MQ>(), plan_fn};
 }
 
 const KernelEntry kTable[] = {
@@ -1714,7 +1965,8 @@ int decode_swizzle(int page_size)
 namespace {
 
 // Shared tail of decode_shape / decode_mq_shape once the columns per unit
-// (heads_per_cta) and units per row are set.
+// (heads_per_cta) and units per row are set.  Plain rows get room for a step
+// plan after the partials.
 bool finish_shape(int batch, int max_blocks, const pkv_cache_desc &d, bool multi_query, DecodeShape *s)
 {
     if (find_kernel(d.head_dim, s->heads_per_cta, multi_query) == nullptr)
@@ -1733,10 +1985,20 @@ bool finish_shape(int batch, int max_blocks, const pkv_cache_desc &d, bool multi
     s->off_ml = tickets;
     s->off_o = s->off_ml + align(sizeof(float2) * (size_t)s->cap_items * s->heads_per_cta);
     s->bytes = s->off_o + align(sizeof(float) * (size_t)s->cap_items * s->heads_per_cta * d.head_dim);
+    s->off_plan = 0;
+    if (!multi_query) {
+        s->off_plan = s->bytes;
+        s->bytes += align(plan_layout(batch).bytes);
+    }
     return true;
 }
 
 } // namespace
+
+size_t decode_plan_bytes(int batch)
+{
+    return plan_layout(batch).bytes;
+}
 
 bool decode_shape(int batch, int max_blocks, int num_q_heads, const pkv_cache_desc &d, DecodeShape *s)
 {
@@ -1787,6 +2049,8 @@ int decode_target_items(int device, int head_dim, int heads_per_cta, bool multi_
     int &slot = cache[device][kernel_index(e)];
     if (slot == 0) {
         int occ = 1;
+        if (e->plan_fn != nullptr)
+            (void)cudaFuncSetAttribute(e->plan_fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)e->smem);
         if (cudaFuncSetAttribute(e->fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)e->smem) != cudaSuccess ||
             cudaFuncSetAttribute(e->fn, cudaFuncAttributePreferredSharedMemoryCarveout,
                                  cudaSharedmemCarveoutMaxShared) != cudaSuccess ||
@@ -1844,6 +2108,21 @@ cudaError_t launch_decode(const DecodeArgs &a, const DecodeMaps &maps, cudaStrea
     p.mq_max = a.mq_max;
     p.mq_own_long = a.mq_own_long;
     p.mq_kv_add = a.mq_kv_add;
+    unsigned char *plan = a.shape.off_plan != 0 ? ws + a.shape.off_plan : nullptr;
+    p.plan_in = (a.flags & PKV_DECODE_USE_PLAN) ? plan : nullptr;
+    p.plan_out = nullptr;
+    if ((a.flags & PKV_DECODE_MAKE_PLAN) && plan != nullptr && e->plan_fn != nullptr) {
+        // the step plan first: an ordinary launch, one warp per record
+        KParams pp = p;
+        pp.plan_out = plan;
+        int grid = a.grid;
+        void *pargs[] = {&pp, &grid};
+        const int per_cta = kThreads / 32;
+        const cudaError_t err = cudaLaunchKernel(e->plan_fn, dim3((a.grid + per_cta - 1) / per_cta), dim3(kThreads),
+                                                 pargs, e->smem, stream);
+        if (err != cudaSuccess)
+            return err;
+    }
     void *args[] = {&p, const_cast<DecodeMaps *>(&maps)};
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(a.grid);

@@ -62,6 +62,8 @@ pkv_status pkv_decode_step_create(const pkv_cache_desc *desc, int32_t num_layers
         return PKV_EINVAL;
     if ((k_new == nullptr) != (v_new == nullptr))
         return PKV_EINVAL;
+    if (flags & PKV_DECODE_MAKE_PLAN)
+        return PKV_EINVAL; // the step makes its plan itself (PKV_DECODE_USE_PLAN)
     if (k_new != nullptr && (!all_set(k_new, num_layers) || !all_set(v_new, num_layers)))
         return PKV_EINVAL;
     // Every argument check of the layer calls, before any CUDA work.
@@ -85,11 +87,17 @@ pkv_status pkv_decode_step_create(const pkv_cache_desc *desc, int32_t num_layers
         cudaStreamDestroy(cap);
         return PKV_ECUDA;
     }
-    for (int32_t l = 0; l < num_layers && st == PKV_OK; ++l)
+    // With PKV_DECODE_USE_PLAN the first layer makes the step plan that the
+    // others reuse (all layers share cache_seqlens and block_table).
+    for (int32_t l = 0; l < num_layers && st == PKV_OK; ++l) {
+        uint32_t f = flags;
+        if (l == 0 && (flags & PKV_DECODE_USE_PLAN))
+            f = (flags & ~PKV_DECODE_USE_PLAN) | PKV_DECODE_MAKE_PLAN;
         st = pkv_decode_attn_ex(desc, k_caches[l], v_caches[l], q[l], k_new ? k_new[l] : nullptr,
                                 v_new ? v_new[l] : nullptr, block_table, max_blocks, cache_seqlens, batch,
                                 num_q_heads, softmax_scale, out[l], lse ? lse[l] : nullptr, workspace,
-                                workspace_bytes, err_flag, cap, flags);
+                                workspace_bytes, err_flag, cap, f);
+    }
     const cudaError_t end = cudaStreamEndCapture(cap, &graph);
     if (st == PKV_OK && end != cudaSuccess)
         st = PKV_ECUDA;

@@ -32,8 +32,14 @@ struct DecodeShape {
     int units_per_row;  // num_kv_heads * n_sub
     int chunk_max;      // largest chunk in tokens (multiple of kDecodeTile)
     int64_t cap_items;  // partial-result slots in the workspace
-    size_t off_ml, off_o, bytes;
+    size_t off_ml, off_o;
+    size_t off_plan;    // step plan (PKV_DECODE_MAKE_PLAN / USE_PLAN); 0: no room for one
+    size_t bytes;
 };
+
+// Bytes of the step plan a workspace holds for `batch` rows (a header, the
+// per-row prefix arrays and one record per CTA of the persistent grid).
+size_t decode_plan_bytes(int batch);
 
 // Fills `s`; returns false for unsupported combinations.
 bool decode_shape(int batch, int max_blocks, int num_q_heads, const pkv_cache_desc &d, DecodeShape *s);

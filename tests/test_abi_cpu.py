@@ -161,7 +161,26 @@ def test_decode_flags():
     assert lib.pkv_decode_attn_ex(*args, pkv.api.DECODE_OVERLAP_PROLOGUE) == pkv.api.OK
     assert lib.pkv_decode_attn_ex(*args, pkv.api.DECODE_OVERLAP_PROLOGUE | pkv.api.DECODE_EARLY_KV) == pkv.api.OK
     assert lib.pkv_decode_attn_ex(*args, pkv.api.DECODE_EARLY_KV) == pkv.api.EINVAL  # needs the overlap launch
-    assert lib.pkv_decode_attn_ex(*args, 4) == pkv.api.EINVAL                        # unknown flag
+    assert lib.pkv_decode_attn_ex(*args, 16) == pkv.api.EINVAL                       # unknown flag
+    for f in (pkv.api.DECODE_MAKE_PLAN, pkv.api.DECODE_USE_PLAN,
+              pkv.api.DECODE_USE_PLAN | pkv.api.DECODE_OVERLAP_PROLOGUE | pkv.api.DECODE_EARLY_KV):
+        assert lib.pkv_decode_attn_ex(*args, f) == pkv.api.OK
+    assert lib.pkv_decode_attn_ex(*args, pkv.api.DECODE_MAKE_PLAN | pkv.api.DECODE_USE_PLAN) == pkv.api.EINVAL
+
+
+def test_decode_workspace_holds_a_step_plan():
+    """The decode workspace ends with room for one step plan: a 256-byte
+    header, the per-row arrays and a 256-byte record per persistent CTA (at
+    most 2048), whatever the sizes."""
+    d = CacheDesc(64, 128, 8, 128, 0)
+    for batch in (1, 64, 1024):
+        plan = 256 + 256 * ((4 * batch + 255) // 256) + 256 * ((4 * (batch + 1) + 255) // 256) + \
+            256 * ((8 * (batch + 1) + 255) // 256) + 2048 * 256
+        # before it: a ticket per (row, kv head), then (m, l) and o partials of 4 heads
+        # for two slots of each of 2048 persistent CTAs
+        al = lambda x: 256 * ((x + 255) // 256)  # noqa: E731
+        base = al(4 * batch * 8) + al(8 * 4096 * 4) + al(4 * 4096 * 4 * 128)
+        assert pkv.pkv_decode_workspace_size(batch, 9, 32, d) == base + plan
 
 
 def test_append_argument_errors():
@@ -268,6 +287,7 @@ def test_decode_step_argument_errors_before_any_cuda_call():
     assert create(ws=None) == pkv.api.EWORKSPACE
     assert create(ws_bytes=64) == pkv.api.EWORKSPACE
     assert create(flags=pkv.api.DECODE_EARLY_KV) == pkv.api.EINVAL
+    assert create(flags=pkv.api.DECODE_MAKE_PLAN) == pkv.api.EINVAL       # the step makes its own plan
     assert out.value is None
     lib.pkv_decode_step_destroy(None)
 

@@ -158,7 +158,8 @@ def test_batch_sweep_full_cycle(batch, contiguous):
         assert np.array_equal(gk, ek) and np.array_equal(gv, ev)
 
 
-def test_decode_step_graph_with_padded_bucket():
+@pytest.mark.parametrize("use_plan", [False, True])
+def test_decode_step_graph_with_padded_bucket(use_plan):
     """Three layers captured once as a decode-step graph for the 16-row bucket
     of 13 live rows (rows 13..15 inactive), replayed for two steps with the
     inputs rewritten in place.  Every layer's live rows match the fp64 oracle
@@ -174,6 +175,9 @@ def test_decode_step_graph_with_padded_bucket():
     bt[:live] = torch.as_tensor(bt_live, device=DEV)
     desc = pkv.cache_desc(sw.k_caches[0])
     flags = pkv.api.DECODE_OVERLAP_PROLOGUE | pkv.api.DECODE_EARLY_KV
+    if use_plan:  # layer 0 makes the step plan, layers 1.. reuse it
+        flags |= pkv.api.DECODE_USE_PLAN
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
     kc_g = [k.clone() for k in sw.k_caches]
     vc_g = [v.clone() for v in sw.v_caches]
     # graph buffers (bucket rows), written in place every step
@@ -185,7 +189,7 @@ def test_decode_step_graph_with_padded_bucket():
     seq = torch.full((bucket,), -1, dtype=torch.int32, device=DEV)
     ws = pkv.decode_workspace(bucket, sw.max_blocks, 32, desc, DEV)
     step_graph = pkv.DecodeStep(kc_g, vc_g, q, kn, vn, bt, seq, sw.softmax_scale, out, lse=lse, workspace=ws,
-                                flags=flags)
+                                err_flag=err, flags=flags)
     ws_ref = pkv.decode_workspace(live, sw.max_blocks, 32, desc, DEV)
     bt_ref = torch.as_tensor(bt_live, device=DEV)
     rows = list(range(live))
@@ -222,6 +226,132 @@ def test_decode_step_graph_with_padded_bucket():
         assert torch.equal(vc_g[layer].view(torch.int16), sw.v_caches[layer].view(torch.int16))
         gk, gv, _ = wl.compact_rows(kc_g[layer], vc_g[layer], bt_live, rows, need, sw.page_size)
         assert np.array_equal(gk, host[layer][0]) and np.array_equal(gv, host[layer][1])
+    assert int(err.item()) == 0
+
+
+def _plan_flags(layer):
+    base = pkv.api.DECODE_OVERLAP_PROLOGUE | pkv.api.DECODE_EARLY_KV
+    return base | (pkv.api.DECODE_MAKE_PLAN if layer == 0 else pkv.api.DECODE_USE_PLAN)
+
+
+@pytest.mark.parametrize("batch,contiguous", [(8, False), (64, False), (256, True)])
+def test_step_plan_reuse_is_bit_identical(batch, contiguous):
+    """Three layers per step, layer 0 with PKV_DECODE_MAKE_PLAN and layers 1-2
+    with PKV_DECODE_USE_PLAN, against the same calls planning for themselves
+    (flags 0) on copies of the pools: the same work split, so outputs, lse and
+    appended caches are bit-identical, and no error bit is raised.  One layer
+    of the first step is also checked against the oracle."""
+    layers = 3
+    sw = wl.batch_sweep(batch, device=DEV, contiguous=contiguous, layers=layers)
+    bt = torch.as_tensor(sw.block_table, device=DEV)
+    desc = pkv.cache_desc(sw.k_caches[0])
+    ws_p = pkv.decode_workspace(batch, sw.max_blocks, 32, desc, DEV)
+    ws_r = pkv.decode_workspace(batch, sw.max_blocks, 32, desc, DEV)
+    kc = [k.clone() for k in sw.k_caches]
+    vc = [v.clone() for v in sw.v_caches]
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    rows = list(range(batch))
+    for step in (0, 1, 7):
+        lens = (sw.prompt_lens + step).astype(np.int32)
+        sl = torch.as_tensor(lens, device=DEV)
+        ins = wl.sweep_step_inputs(sw, step, DEV, layers=layers)
+        if step == 0:
+            hk, hv, hbt = wl.compact_rows(sw.k_caches[1], sw.v_caches[1], sw.block_table, rows, lens + 1,
+                                          sw.page_size)
+        outs = []
+        for layer, (q, kn, vn) in enumerate(ins):
+            lse = torch.empty(batch, 32, dtype=torch.float32, device=DEV)
+            o = pkv.pkv_decode_attn(kc[layer], vc[layer], q, kn, vn, bt, sl, sw.softmax_scale, lse=lse,
+                                    workspace=ws_p, err_flag=err, flags=_plan_flags(layer))
+            outs.append((o, lse))
+        for layer, (q, kn, vn) in enumerate(ins):
+            lse = torch.empty(batch, 32, dtype=torch.float32, device=DEV)
+            o = pkv.pkv_decode_attn(sw.k_caches[layer], sw.v_caches[layer], q, kn, vn, bt, sl, sw.softmax_scale,
+                                    lse=lse, workspace=ws_r)
+            torch.cuda.synchronize()
+            assert torch.equal(outs[layer][0].view(torch.int16), o.view(torch.int16))
+            assert torch.equal(outs[layer][1].view(torch.int32), lse.view(torch.int32))
+            if step == 0 and layer == 1:
+                od = oracle.CacheDesc(hk.shape[0], sw.page_size, 8, 128, wl.NHD)
+                r_out, r_lse, r_err, _ = oracle.decode(od, hk, hv, wl.bits(q), wl.bits(kn), wl.bits(vn), hbt, lens,
+                                                       sw.softmax_scale)
+                assert r_err == 0
+                assert_close(f32(outs[layer][0]), r_out, what="plan reuse")
+                assert_lse_close(outs[layer][1].cpu().numpy(), r_lse)
+    assert int(err.item()) == 0
+    for layer in range(layers):
+        assert torch.equal(kc[layer].view(torch.int16), sw.k_caches[layer].view(torch.int16))
+        assert torch.equal(vc[layer].view(torch.int16), sw.v_caches[layer].view(torch.int16))
+
+
+def test_step_plan_reuse_skewed_split_units():
+    """The skewed batch (one 32,768-token row split over many CTAs, combined by
+    log-sum-exp): a second layer that reuses the first layer's plan gives the
+    bits of a self-planned call, within tolerance of the oracle."""
+    case = wl.skewed_decode(device=DEV)
+    bt = torch.as_tensor(case.block_table, device=DEV)
+    sl = torch.as_tensor(case.cache_seqlens, device=DEV)
+    desc = pkv.cache_desc(case.k_cache)
+    ws = pkv.decode_workspace(case.batch, case.max_blocks, 32, desc, DEV)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    ref_out, ref_lse, ref_err, _ = oracle_decode_compact(case)
+    k2, v2 = case.k_cache.clone(), case.v_cache.clone()
+    # layer 0 (makes the plan) on the copy, layer 1 (reuses it) on the original pools
+    pkv.pkv_decode_attn(k2, v2, case.q, case.k_new, case.v_new, bt, sl, case.softmax_scale, workspace=ws,
+                        err_flag=err, flags=_plan_flags(0))
+    lse = torch.empty(case.batch, 32, dtype=torch.float32, device=DEV)
+    out = pkv.pkv_decode_attn(case.k_cache, case.v_cache, case.q, case.k_new, case.v_new, bt, sl,
+                              case.softmax_scale, lse=lse, workspace=ws, err_flag=err, flags=_plan_flags(1))
+    lse_r = torch.empty(case.batch, 32, dtype=torch.float32, device=DEV)
+    ws_r = pkv.decode_workspace(case.batch, case.max_blocks, 32, desc, DEV)
+    out_r = pkv.pkv_decode_attn(k2, v2, case.q, None, None, bt, sl + 1, case.softmax_scale, lse=lse_r,
+                                workspace=ws_r)  # attend-only over the copy that layer 0 appended to
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0 and ref_err == 0
+    assert_close(f32(out), ref_out, what="skewed plan reuse")
+    assert_lse_close(lse.cpu().numpy(), ref_lse)
+    assert torch.equal(k2.view(torch.int16), case.k_cache.view(torch.int16))
+    assert_close(f32(out_r), f32(out).astype(np.float64), what="attend-only after the append")
+
+
+def test_step_plan_mismatch_and_stale_lengths_raise_plan_bit():
+    """A plan made for another batch is not used (the call plans for itself:
+    exact outputs, PKV_ERR_PLAN set); a plan whose lengths differ from
+    cache_seqlens is detected (PKV_ERR_PLAN set)."""
+    sw = wl.batch_sweep(16, device=DEV, contiguous=False, layers=2)
+    bt = torch.as_tensor(sw.block_table, device=DEV)
+    desc = pkv.cache_desc(sw.k_caches[0])
+    ws = pkv.decode_workspace(16, sw.max_blocks, 32, desc, DEV)
+    lens = torch.as_tensor(sw.prompt_lens.astype(np.int32), device=DEV)
+    (q, kn, vn), _ = wl.sweep_step_inputs(sw, 0, DEV, layers=2)
+    kc, vc = sw.k_caches[0].clone(), sw.v_caches[0].clone()
+    # a plan for the first 8 rows only, then a 16-row call that asks for a plan
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    pkv.pkv_decode_attn(kc, vc, q[:8].contiguous(), kn[:8].contiguous(), vn[:8].contiguous(), bt[:8].contiguous(),
+                        lens[:8].contiguous(), sw.softmax_scale, workspace=ws, err_flag=err,
+                        flags=pkv.api.DECODE_MAKE_PLAN)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    kc, vc = sw.k_caches[0].clone(), sw.v_caches[0].clone()
+    kr, vr = sw.k_caches[0].clone(), sw.v_caches[0].clone()
+    out = pkv.pkv_decode_attn(kc, vc, q, kn, vn, bt, lens, sw.softmax_scale, workspace=ws, err_flag=err,
+                              flags=pkv.api.DECODE_USE_PLAN)
+    ref = pkv.pkv_decode_attn(kr, vr, q, kn, vn, bt, lens, sw.softmax_scale)
+    torch.cuda.synchronize()
+    assert int(err.item()) == pkv.api.ERR_PLAN
+    assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
+    assert torch.equal(kc.view(torch.int16), kr.view(torch.int16))
+    # a plan of these sizes, then lengths one longer without a new plan
+    err.zero_()
+    kc, vc = sw.k_caches[0].clone(), sw.v_caches[0].clone()
+    pkv.pkv_decode_attn(kc, vc, q, kn, vn, bt, lens, sw.softmax_scale, workspace=ws, err_flag=err,
+                        flags=pkv.api.DECODE_MAKE_PLAN)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    pkv.pkv_decode_attn(kc, vc, q, kn, vn, bt, lens + 1, sw.softmax_scale, workspace=ws, err_flag=err,
+                        flags=pkv.api.DECODE_USE_PLAN)
+    torch.cuda.synchronize()
+    assert int(err.item()) & pkv.api.ERR_PLAN
 
 
 def _random_case(seed, B, Hq, Hkv, D, P, lens, layout=wl.NHD, spare=7):
