@@ -602,9 +602,9 @@ __device__ __forceinline__ int load_window(const int32_t *bt_row, int first, int
     return first + lane <= last ? bt_row[first + lane] : 0;
 }
 
-// rec: this CTA's record of a step plan.  Its first slice is then issued
-// before the shared-memory plan is ready; the producer meets the other warps
-// (named barrier 1) right after that first tile.
+// rec: this CTA's record of a step plan (its SegIter, first slice and first
+// page ids, already loaded into registers): the first tile is issued without
+// a search of the plan or a block_table load.
 template <int D, int GC, bool MQ>
 __device__ void producer(const KParams &p, Smem<D, GC, MQ> &sm, const DecodeMaps *maps, const PlanRec *rec)
 {
@@ -628,8 +628,9 @@ __device__ void producer(const KParams &p, Smem<D, GC, MQ> &sm, const DecodeMaps
         sg.tok0 = __ldcg(&rec->tok0);
         sg.tok1 = __ldcg(&rec->tok1);
         win = __ldcg(&rec->pages[lane]);
-        // the record is only trusted as far as its addresses go: a bad row or
-        // kv head fails like a bad page (below), never forms an address
+        // the record is only trusted as far as its addresses go: one that
+        // names no valid row, kv head or token range stops the CTA (the other
+        // warps' bounded waits then end, PKV_ERR_TIMEOUT), never forms an address
         if (have && (sg.b < 0 || sg.b >= p.batch || sg.kvh < 0 || sg.kvh >= p.num_kv_heads || sg.tok0 < 0 ||
                      sg.tok1 <= sg.tok0 || sg.tok1 > p.max_blocks * p.page_size)) {
             have = false;
@@ -643,10 +644,10 @@ __device__ void producer(const KParams &p, Smem<D, GC, MQ> &sm, const DecodeMaps
                                  (sg.tok1 - 1) >> p.page_shift, lane)
                    : 0;
     }
-    bool met = rec == nullptr; // met the other warps at named barrier 1
-    // live page ids of the record's window (checked against it once loaded)
-    int live0 = 0, rec0 = win;
-    const int32_t *rec_row = have ? p.block_table + (int64_t)sg.b * p.max_blocks : nullptr;
+    // live page ids of the record's window, checked against it after the first slice
+    int live0 = 0;
+    const int rec0 = win;
+    const int32_t *rec_row = rec != nullptr && have ? p.block_table + (int64_t)sg.b * p.max_blocks : nullptr;
     const int rec_first = have ? sg.tok0 >> p.page_shift : 0, rec_last = have ? (sg.tok1 - 1) >> p.page_shift : -1;
     // Page ids are loading.  K/V come after the preceding grid unless the
     // caller declared that it does not write this call's cache; the error
@@ -738,11 +739,8 @@ __device__ void producer(const KParams &p, Smem<D, GC, MQ> &sm, const DecodeMaps
             }
             __syncwarp();
             if (t == 0) { // next slice and its first page window, off the first tile's critical path
-                if (!met) {
-                    named_sync(1, kThreads); // the shared-memory plan is ready
-                    met = true;
+                if (rec_row != nullptr)
                     live0 = load_window(rec_row, rec_first, rec_last, lane);
-                }
                 more = si.next(p, sm, nx);
                 nwin = more ? load_window(p.block_table + (int64_t)nx.b * p.max_blocks, nx.tok0 >> p.page_shift,
                                           (nx.tok1 - 1) >> p.page_shift, lane)
@@ -760,8 +758,6 @@ __device__ void producer(const KParams &p, Smem<D, GC, MQ> &sm, const DecodeMaps
         sg = nx;
         win = nwin;
     }
-    if (!met)
-        named_sync(1, kThreads); // no tile issued: still meet the other warps
     // After an abort, let copies already issued land before the CTA exits.
     if (*abort && lane == 0) {
         const uint32_t first = g_tile > (uint32_t)S ? g_tile - S : 0;
@@ -1739,56 +1735,74 @@ __device__ __forceinline__ void decode_body(const KParams &p, const DecodeMaps &
     extern __shared__ unsigned char smem_raw[];
     Smem<D, GC, MQ> &sm = *reinterpret_cast<Smem<D, GC, MQ> *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    const int warp = threadIdx.x >> 5;
-    // A step plan: taken when its header matches this launch (plain rows).
-    bool from_plan = false;
-    if constexpr (!MQ)
-        from_plan = p.plan_in != nullptr && plan_matches(p, reinterpret_cast<const PlanHeader *>(p.plan_in));
-    if (from_plan) {
-        if (warp == kProducerWarp) {
-            if ((threadIdx.x & 31) == 0) {
-                init_barriers(sm);
-                sm.plan_state = 1;
-                prefetch_tensormap(&maps.k);
-                prefetch_tensormap(&maps.v);
-                prefetch_tensormap(&maps.k8);
-                prefetch_tensormap(&maps.v8);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const PlanRec *rec = nullptr;
+    if constexpr (!MQ) {
+        if (p.plan_in != nullptr) {
+            // A step plan.  The producer warp alone decides whether it matches
+            // this launch, loading the header and its CTA's record together;
+            // the other warps copy the plan's arrays into shared memory
+            // meanwhile (harmless if it is rejected: planning overwrites them).
+            // Every thread meets at named barrier 1 exactly once, after which
+            // all read the one decision.
+            const PlanLayout lay = plan_layout(p.batch);
+            if (warp == kProducerWarp) {
+                if (lane == 0) {
+                    init_barriers(sm);
+                    prefetch_tensormap(&maps.k);
+                    prefetch_tensormap(&maps.v);
+                    prefetch_tensormap(&maps.k8);
+                    prefetch_tensormap(&maps.v8);
+                }
+                const bool ok = __shfl_sync(0xffffffffu,
+                                            plan_matches(p, reinterpret_cast<const PlanHeader *>(p.plan_in)), 0);
+                if (lane == 0)
+                    sm.plan_state = ok ? 1 : 2;
+                rec = reinterpret_cast<const PlanRec *>(p.plan_in + lay.recs) + blockIdx.x;
+            } else {
+                const PlanHeader *h = reinterpret_cast<const PlanHeader *>(p.plan_in);
+                const int t = threadIdx.x < kProducerWarp * 32 ? threadIdx.x : threadIdx.x - 32; // 0 .. 127
+                constexpr int kCopy = kThreads - 32;
+                const int32_t *len = reinterpret_cast<const int32_t *>(p.plan_in + lay.len);
+                const int32_t *rowtok = reinterpret_cast<const int32_t *>(p.plan_in + lay.rowtok);
+                const long long *rowbase = reinterpret_cast<const long long *>(p.plan_in + lay.rowbase);
+                for (int i = t; i < p.batch; i += kCopy)
+                    sm.len[i] = __ldcg(len + i);
+                for (int i = t; i <= p.batch; i += kCopy) {
+                    sm.rowtok[i] = __ldcg(rowtok + i);
+                    sm.rowbase[i] = __ldcg(rowbase + i);
+                }
+                if (t == 0) {
+                    sm.work = __ldcg(&h->work);
+                    sm.slice = __ldcg(&h->slice);
+                    sm.geff = __ldcg(&h->geff);
+                    sm.n_empty = __ldcg(&h->n_empty);
+                }
             }
-            __syncwarp();
-            const PlanRec *rec = reinterpret_cast<const PlanRec *>(p.plan_in + plan_layout(p.batch).recs) + blockIdx.x;
-            producer(p, sm, &maps, rec); // meets the others at named barrier 1 after its first tile
+            named_sync(1, kThreads); // the decision, the barriers and (if taken) the plan are ready
+            if (sm.plan_state == 1) {
+                if (warp < kWarps)
+                    consumers(p, sm);
+                else if (warp == kProducerWarp)
+                    producer(p, sm, &maps, rec);
+                else
+                    epilogue(p, sm, warp - kEpilogueWarp);
+                return;
+            }
+            // rejected: plan here, as without a step plan (barriers are initialised)
+            build_plan(p, sm, (int)gridDim.x); // ends with __syncthreads()
+            if (warp < kWarps)
+                consumers(p, sm);
+            else if (warp == kProducerWarp)
+                producer(p, sm, &maps, nullptr);
+            else
+                epilogue(p, sm, warp - kEpilogueWarp);
             return;
         }
-        // the other warps copy the plan into shared memory meanwhile
-        const PlanLayout lay = plan_layout(p.batch);
-        const PlanHeader *h = reinterpret_cast<const PlanHeader *>(p.plan_in);
-        const int t = threadIdx.x < kProducerWarp * 32 ? threadIdx.x : threadIdx.x - 32; // 0 .. 127
-        constexpr int kCopy = kThreads - 32;
-        const int32_t *len = reinterpret_cast<const int32_t *>(p.plan_in + lay.len);
-        const int32_t *rowtok = reinterpret_cast<const int32_t *>(p.plan_in + lay.rowtok);
-        const long long *rowbase = reinterpret_cast<const long long *>(p.plan_in + lay.rowbase);
-        for (int i = t; i < p.batch; i += kCopy)
-            sm.len[i] = __ldcg(len + i);
-        for (int i = t; i <= p.batch; i += kCopy) {
-            sm.rowtok[i] = __ldcg(rowtok + i);
-            sm.rowbase[i] = __ldcg(rowbase + i);
-        }
-        if (t == 0) {
-            sm.work = __ldcg(&h->work);
-            sm.slice = __ldcg(&h->slice);
-            sm.geff = __ldcg(&h->geff);
-            sm.n_empty = __ldcg(&h->n_empty);
-        }
-        named_sync(1, kThreads); // plan and barriers ready
-        if (warp < kWarps)
-            consumers(p, sm);
-        else
-            epilogue(p, sm, warp - kEpilogueWarp);
-        return;
     }
     if (threadIdx.x == 0) {
         init_barriers(sm);
-        sm.plan_state = p.plan_in != nullptr ? 2 : 0;
+        sm.plan_state = 0;
     }
     if (threadIdx.x == kProducerWarp * 32) {
         prefetch_tensormap(&maps.k);
