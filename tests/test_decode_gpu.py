@@ -315,9 +315,10 @@ def test_step_plan_reuse_skewed_split_units():
 
 
 def test_step_plan_mismatch_and_stale_lengths_raise_plan_bit():
-    """A plan made for another batch is not used (the call plans for itself:
-    exact outputs, PKV_ERR_PLAN set); a plan whose lengths differ from
-    cache_seqlens is detected (PKV_ERR_PLAN set)."""
+    """A plan made for another call shape (attend-only, no new token) is not
+    used by a fused append + decode call: that call plans for itself, gives
+    the exact outputs and sets PKV_ERR_PLAN.  A plan whose lengths differ
+    from cache_seqlens is detected (PKV_ERR_PLAN set)."""
     sw = wl.batch_sweep(16, device=DEV, contiguous=False, layers=2)
     bt = torch.as_tensor(sw.block_table, device=DEV)
     desc = pkv.cache_desc(sw.k_caches[0])
@@ -325,10 +326,9 @@ def test_step_plan_mismatch_and_stale_lengths_raise_plan_bit():
     lens = torch.as_tensor(sw.prompt_lens.astype(np.int32), device=DEV)
     (q, kn, vn), _ = wl.sweep_step_inputs(sw, 0, DEV, layers=2)
     kc, vc = sw.k_caches[0].clone(), sw.v_caches[0].clone()
-    # a plan for the first 8 rows only, then a 16-row call that asks for a plan
+    # an attend-only plan, then a fused call that asks for a plan (same workspace layout)
     err = torch.zeros(1, dtype=torch.int32, device=DEV)
-    pkv.pkv_decode_attn(kc, vc, q[:8].contiguous(), kn[:8].contiguous(), vn[:8].contiguous(), bt[:8].contiguous(),
-                        lens[:8].contiguous(), sw.softmax_scale, workspace=ws, err_flag=err,
+    pkv.pkv_decode_attn(kc, vc, q, None, None, bt, lens, sw.softmax_scale, workspace=ws, err_flag=err,
                         flags=pkv.api.DECODE_MAKE_PLAN)
     torch.cuda.synchronize()
     assert int(err.item()) == 0
