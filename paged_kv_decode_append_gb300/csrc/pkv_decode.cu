@@ -552,6 +552,13 @@ struct PlanRec {
     int32_t pages[32];
 };
 static_assert(sizeof(PlanRec) <= kPlanRecBytes, "plan record");
+
+// A CTA's record as its producer warp holds it (win: page id `lane` of the
+// first window).
+struct RecRegs {
+    SegIter si;
+    int have, b, kvh, tok0, tok1, win;
+};
 static_assert(sizeof(PlanHeader) <= 256, "plan header");
 
 // Offsets (bytes, from the plan region's start) of a plan for `batch` rows.
@@ -603,10 +610,11 @@ __device__ __forceinline__ int load_window(const int32_t *bt_row, int first, int
 }
 
 // rec: this CTA's record of a step plan (its SegIter, first slice and first
-// page ids, already loaded into registers): the first tile is issued without
-// a search of the plan or a block_table load.
+// page ids), loaded into registers before the shared-memory plan is ready.
+// The first tile is then issued at once; the producer meets the other warps
+// at named barrier 2 (the plan written to shared memory) right after it.
 template <int D, int GC, bool MQ>
-__device__ void producer(const KParams &p, Smem<D, GC, MQ> &sm, const DecodeMaps *maps, const PlanRec *rec)
+__device__ void producer(const KParams &p, Smem<D, GC, MQ> &sm, const DecodeMaps *maps, const RecRegs *rec)
 {
     constexpr int S = Smem<D, GC, MQ>::kStages;
     const int lane = threadIdx.x & 31;
@@ -621,13 +629,13 @@ __device__ void producer(const KParams &p, Smem<D, GC, MQ> &sm, const DecodeMaps
     bool have;
     int win; // first window of the current slice, prefetched one slice ahead
     if (rec != nullptr) {
-        si = ldcg_pod(&rec->si);
-        have = __ldcg(&rec->have) != 0;
-        sg.b = __ldcg(&rec->b);
-        sg.kvh = __ldcg(&rec->kvh);
-        sg.tok0 = __ldcg(&rec->tok0);
-        sg.tok1 = __ldcg(&rec->tok1);
-        win = __ldcg(&rec->pages[lane]);
+        si = rec->si;
+        have = rec->have != 0;
+        sg.b = rec->b;
+        sg.kvh = rec->kvh;
+        sg.tok0 = rec->tok0;
+        sg.tok1 = rec->tok1;
+        win = rec->win;
         // the record is only trusted as far as its addresses go: one that
         // names no valid row, kv head or token range stops the CTA (the other
         // warps' bounded waits then end, PKV_ERR_TIMEOUT), never forms an address
@@ -644,6 +652,7 @@ __device__ void producer(const KParams &p, Smem<D, GC, MQ> &sm, const DecodeMaps
                                  (sg.tok1 - 1) >> p.page_shift, lane)
                    : 0;
     }
+    bool met = rec == nullptr; // met the other warps at named barrier 2
     // live page ids of the record's window, checked against it after the first slice
     int live0 = 0;
     const int rec0 = win;
@@ -739,6 +748,10 @@ __device__ void producer(const KParams &p, Smem<D, GC, MQ> &sm, const DecodeMaps
             }
             __syncwarp();
             if (t == 0) { // next slice and its first page window, off the first tile's critical path
+                if (!met) {
+                    named_sync(2, kThreads); // the shared-memory plan is written
+                    met = true;
+                }
                 if (rec_row != nullptr)
                     live0 = load_window(rec_row, rec_first, rec_last, lane);
                 more = si.next(p, sm, nx);
@@ -758,6 +771,8 @@ __device__ void producer(const KParams &p, Smem<D, GC, MQ> &sm, const DecodeMaps
         sg = nx;
         win = nwin;
     }
+    if (!met)
+        named_sync(2, kThreads); // no tile issued: still meet the other warps
     // After an abort, let copies already issued land before the CTA exits.
     if (*abort && lane == 0) {
         const uint32_t first = g_tile > (uint32_t)S ? g_tile - S : 0;
@@ -1736,16 +1751,19 @@ __device__ __forceinline__ void decode_body(const KParams &p, const DecodeMaps &
     Smem<D, GC, MQ> &sm = *reinterpret_cast<Smem<D, GC, MQ> *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const PlanRec *rec = nullptr;
     if constexpr (!MQ) {
         if (p.plan_in != nullptr) {
             // A step plan.  The producer warp alone decides whether it matches
-            // this launch, loading the header and its CTA's record together;
-            // the other warps copy the plan's arrays into shared memory
-            // meanwhile (harmless if it is rejected: planning overwrites them).
-            // Every thread meets at named barrier 1 exactly once, after which
-            // all read the one decision.
+            // this launch, from the header it loads together with its CTA's
+            // record, publishes the decision (named barrier 1, without
+            // waiting) and, if taken, issues its first tile at once.  The
+            // other warps load the plan's arrays into registers meanwhile and
+            // write them to shared memory once the plan is taken (named
+            // barrier 2, which the producer joins after that first tile).
+            // Every thread passes barrier 1 once, and barrier 2 once when the
+            // plan is taken; a rejected plan is replaced by planning here.
             const PlanLayout lay = plan_layout(p.batch);
+            const PlanHeader *h = reinterpret_cast<const PlanHeader *>(p.plan_in);
             if (warp == kProducerWarp) {
                 if (lane == 0) {
                     init_barriers(sm);
@@ -1754,40 +1772,74 @@ __device__ __forceinline__ void decode_body(const KParams &p, const DecodeMaps &
                     prefetch_tensormap(&maps.k8);
                     prefetch_tensormap(&maps.v8);
                 }
-                const bool ok = __shfl_sync(0xffffffffu,
-                                            plan_matches(p, reinterpret_cast<const PlanHeader *>(p.plan_in)), 0);
+                const PlanRec *rp = reinterpret_cast<const PlanRec *>(p.plan_in + lay.recs) + blockIdx.x;
+                RecRegs rec;
+                rec.si = ldcg_pod(&rp->si);
+                rec.have = __ldcg(&rp->have);
+                rec.b = __ldcg(&rp->b);
+                rec.kvh = __ldcg(&rp->kvh);
+                rec.tok0 = __ldcg(&rp->tok0);
+                rec.tok1 = __ldcg(&rp->tok1);
+                rec.win = __ldcg(&rp->pages[lane]);
+                const bool ok = __shfl_sync(0xffffffffu, plan_matches(p, h), 0);
                 if (lane == 0)
                     sm.plan_state = ok ? 1 : 2;
-                rec = reinterpret_cast<const PlanRec *>(p.plan_in + lay.recs) + blockIdx.x;
+                __syncwarp();
+                named_arrive(1, kThreads);
+                if (ok) {
+                    producer(p, sm, &maps, &rec);
+                    return;
+                }
             } else {
-                const PlanHeader *h = reinterpret_cast<const PlanHeader *>(p.plan_in);
-                const int t = threadIdx.x < kProducerWarp * 32 ? threadIdx.x : threadIdx.x - 32; // 0 .. 127
+                // this thread's share of the arrays, at most kMaxDecodeBatch + 1 rows
                 constexpr int kCopy = kThreads - 32;
+                constexpr int kPer = (kMaxDecodeBatch + 1 + kCopy - 1) / kCopy;
+                const int t = threadIdx.x < kProducerWarp * 32 ? threadIdx.x : threadIdx.x - 32; // 0 .. 127
                 const int32_t *len = reinterpret_cast<const int32_t *>(p.plan_in + lay.len);
                 const int32_t *rowtok = reinterpret_cast<const int32_t *>(p.plan_in + lay.rowtok);
                 const long long *rowbase = reinterpret_cast<const long long *>(p.plan_in + lay.rowbase);
-                for (int i = t; i < p.batch; i += kCopy)
-                    sm.len[i] = __ldcg(len + i);
-                for (int i = t; i <= p.batch; i += kCopy) {
-                    sm.rowtok[i] = __ldcg(rowtok + i);
-                    sm.rowbase[i] = __ldcg(rowbase + i);
+                int r_len[kPer], r_tok[kPer];
+                long long r_base[kPer];
+#pragma unroll
+                for (int j = 0; j < kPer; ++j) {
+                    const int i = t + j * kCopy;
+                    r_len[j] = i < p.batch ? __ldcg(len + i) : 0;
+                    r_tok[j] = i <= p.batch ? __ldcg(rowtok + i) : 0;
+                    r_base[j] = i <= p.batch ? __ldcg(rowbase + i) : 0;
                 }
+                long long work = 0, slice = 0;
+                int geff = 0, n_empty = 0;
                 if (t == 0) {
-                    sm.work = __ldcg(&h->work);
-                    sm.slice = __ldcg(&h->slice);
-                    sm.geff = __ldcg(&h->geff);
-                    sm.n_empty = __ldcg(&h->n_empty);
+                    work = __ldcg(&h->work);
+                    slice = __ldcg(&h->slice);
+                    geff = __ldcg(&h->geff);
+                    n_empty = __ldcg(&h->n_empty);
                 }
-            }
-            named_sync(1, kThreads); // the decision, the barriers and (if taken) the plan are ready
-            if (sm.plan_state == 1) {
-                if (warp < kWarps)
-                    consumers(p, sm);
-                else if (warp == kProducerWarp)
-                    producer(p, sm, &maps, rec);
-                else
-                    epilogue(p, sm, warp - kEpilogueWarp);
-                return;
+                named_sync(1, kThreads); // the producer's decision
+                if (sm.plan_state == 1) {
+#pragma unroll
+                    for (int j = 0; j < kPer; ++j) {
+                        const int i = t + j * kCopy;
+                        if (i < p.batch)
+                            sm.len[i] = r_len[j];
+                        if (i <= p.batch) {
+                            sm.rowtok[i] = r_tok[j];
+                            sm.rowbase[i] = r_base[j];
+                        }
+                    }
+                    if (t == 0) {
+                        sm.work = work;
+                        sm.slice = slice;
+                        sm.geff = geff;
+                        sm.n_empty = n_empty;
+                    }
+                    named_sync(2, kThreads); // the plan is in shared memory
+                    if (warp < kWarps)
+                        consumers(p, sm);
+                    else
+                        epilogue(p, sm, warp - kEpilogueWarp);
+                    return;
+                }
             }
             // rejected: plan here, as without a step plan (barriers are initialised)
             build_plan(p, sm, (int)gridDim.x); // ends with __syncthreads()

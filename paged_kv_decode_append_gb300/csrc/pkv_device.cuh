@@ -127,6 +127,12 @@ __device__ __forceinline__ void named_sync(int id, int count)
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
+// Arrival at a named barrier of `count` threads without waiting for it.
+__device__ __forceinline__ void named_arrive(int id, int count)
+{
+    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 // Two bf16 packed in a 32-bit word -> two fp32 (exact; low half first).
 __device__ __forceinline__ float2 bf16x2_to_float2(uint32_t w)
 {
