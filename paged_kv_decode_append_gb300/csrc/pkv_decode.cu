@@ -1274,19 +1274,40 @@ __device__ __forceinline__ int pair_elem(int lane, int i)
 }
 
 // Everything a unit's finish reads from global memory besides the partials,
-// loaded into registers before the slice's softmax state arrives.
+// loaded into registers before the slice's softmax state arrives, and the new
+// token's scores computed from them meanwhile.
 template <int D, int GC>
 struct EpiInputs {
     static constexpr int KP = D / 64;                // bf16 pairs of one row per lane
     static constexpr int CH = (2 * D / 8 + 31) / 32; // 16-byte append chunks per lane
-    uint32_t q2[GC][KP], k2[KP], v2[KP];
+    uint32_t v2[KP];
     uint4 chunk[CH];
     int page;
+    float sn[GC]; // (q . k_new) * scale * log2 e of every head
 };
+
+// Loads issued where they stand: the volatile asm keeps them ahead of the
+// barrier wait that follows, so their latency overlaps it.
+__device__ __forceinline__ uint32_t ld_pinned(const void *ptr)
+{
+    uint32_t v;
+    asm volatile("ld.global.nc.b32 %0, [%1];" : "=r"(v) : "l"(ptr));
+    return v;
+}
+
+__device__ __forceinline__ uint4 ld_pinned4(const void *ptr)
+{
+    uint4 v;
+    asm volatile("ld.global.nc.v4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(ptr));
+    return v;
+}
 
 template <int D, int GC, bool MQ>
 __device__ __forceinline__ void load_epi_inputs(const KParams &p, const Seg &sg, int lane, EpiInputs<D, GC> &in)
 {
+    constexpr int KP = EpiInputs<D, GC>::KP;
     in.page = 0;
     if constexpr (MQ)
         return; // multi-query rows were appended by the caller: no new token here
@@ -1295,13 +1316,15 @@ __device__ __forceinline__ void load_epi_inputs(const KParams &p, const Seg &sg,
     const int h0 = sg.kvh * p.group + sg.sub * GC;
     const __nv_bfloat16 *kn = p.k_new + ((int64_t)sg.b * p.num_kv_heads + sg.kvh) * D;
     const __nv_bfloat16 *vn = p.v_new + ((int64_t)sg.b * p.num_kv_heads + sg.kvh) * D;
+    uint32_t q2[GC][KP], k2[KP];
 #pragma unroll
-    for (int j = 0; j < EpiInputs<D, GC>::KP; ++j) {
-        in.k2[j] = reinterpret_cast<const uint32_t *>(kn)[lane + 32 * j];
-        in.v2[j] = reinterpret_cast<const uint32_t *>(vn)[lane + 32 * j];
+    for (int j = 0; j < KP; ++j) {
+        k2[j] = ld_pinned(reinterpret_cast<const uint32_t *>(kn) + lane + 32 * j);
+        in.v2[j] = ld_pinned(reinterpret_cast<const uint32_t *>(vn) + lane + 32 * j);
 #pragma unroll
         for (int g = 0; g < GC; ++g)
-            in.q2[g][j] = reinterpret_cast<const uint32_t *>(p.q + ((int64_t)sg.b * p.num_q_heads + h0 + g) * D)[lane + 32 * j];
+            q2[g][j] = ld_pinned(reinterpret_cast<const uint32_t *>(p.q + ((int64_t)sg.b * p.num_q_heads + h0 + g) * D) +
+                                 lane + 32 * j);
     }
     constexpr int kVec = D / 8;
 #pragma unroll
@@ -1309,10 +1332,23 @@ __device__ __forceinline__ void load_epi_inputs(const KParams &p, const Seg &sg,
         const int cix = lane + 32 * ci;
         in.chunk[ci] = make_uint4(0u, 0u, 0u, 0u);
         if (cix < 2 * kVec)
-            in.chunk[ci] = cix < kVec ? reinterpret_cast<const uint4 *>(kn)[cix]
-                                      : reinterpret_cast<const uint4 *>(vn)[cix - kVec];
+            in.chunk[ci] = ld_pinned4(cix < kVec ? reinterpret_cast<const uint4 *>(kn) + cix
+                                                 : reinterpret_cast<const uint4 *>(vn) + (cix - kVec));
     }
-    in.page = p.block_table[(int64_t)sg.b * p.max_blocks + (sg.L >> p.page_shift)];
+    in.page = (int)ld_pinned(p.block_table + (int64_t)sg.b * p.max_blocks + (sg.L >> p.page_shift));
+    // the new token's scores, off the path that follows the state's arrival
+#pragma unroll
+    for (int g = 0; g < GC; ++g) {
+        float s = 0.f;
+#pragma unroll
+        for (int j = 0; j < KP; ++j) {
+            const float2 qv = unpack_bf16(q2[g][j]), kv = unpack_bf16(k2[j]);
+            s = fmaf(qv.x, kv.x, fmaf(qv.y, kv.y, s));
+        }
+        for (int o = 16; o > 0; o >>= 1)
+            s += __shfl_xor_sync(0xffffffffu, s, o);
+        in.sn[g] = s * p.q_scale;
+    }
 }
 
 // Writes one unit's output: zeros for inactive / failed rows, otherwise
@@ -1338,19 +1374,7 @@ __device__ void finalize_warp(const KParams &p, const Seg &sg, EpiState<D, GC> &
     if (lane == 0 && err)
         set_error(p.err_flag, err);
     if (live && p.with_new) {
-        float sn[GC]; // (q . k_new) * scale * log2 e
-#pragma unroll
-        for (int g = 0; g < GC; ++g) {
-            float s = 0.f;
-#pragma unroll
-            for (int j = 0; j < KP; ++j) {
-                const float2 qv = unpack_bf16(in.q2[g][j]), kv = unpack_bf16(in.k2[j]);
-                s = fmaf(qv.x, kv.x, fmaf(qv.y, kv.y, s));
-            }
-            for (int o = 16; o > 0; o >>= 1)
-                s += __shfl_xor_sync(0xffffffffu, s, o);
-            sn[g] = s * p.q_scale;
-        }
+        const float *sn = in.sn; // (q . k_new) * scale * log2 e
         if (sg.sub == 0) { // the append: one bit copy per kv head
             constexpr int kVec = D / 8;
             const int slot = sg.L & (p.page_size - 1);
