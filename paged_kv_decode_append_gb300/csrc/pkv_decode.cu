@@ -45,10 +45,10 @@
 // columns are then (query, head) pairs, query-major, GC of them per unit:
 // every K/V tile read serves all of a kv head's heads for GC / G queries, and
 // the tiles past kv - q + 1 mask each column at its own limit.  Up to 16
-// columns share one pass over the K/V tiles: a unit of more than 8 columns
-// gives each consumer warp 8 of them over all 32 rows of a tile (one MMA
-// n-tile each); both epilogue warps then finish it, 8 columns each, with a
-// combine ticket per half.
+// columns share one pass over the K/V tiles: kernels with 16-column units run
+// four consumer warps, one per (16-row half, 8-column group) of a tile (one
+// MMA n-tile each); both epilogue warps then finish a unit, 8 columns each,
+// with a combine ticket per half.
 #include <math.h>
 
 #include "pkv_device.cuh"
@@ -57,10 +57,22 @@
 namespace pkv {
 namespace {
 
-constexpr int kWarps = 2;                    // consumer warps, 16 token rows each
+constexpr int kWarps = 2;                    // consumer warps of units up to 8 columns, 16 token rows each
 constexpr int kProducerWarp = kWarps;        // warp 2
 constexpr int kEpilogueWarp = kWarps + 1;    // warps 3 and 4
 constexpr int kThreads = (kWarps + 3) * 32;
+
+// Warp roles of one instantiation.  Units of up to 8 columns: two consumer
+// warps, one per 16-row half of every tile.  16-column units: four, warp w
+// on row half w & 1 of the tile and columns 8 (w >> 1) .. 8 (w >> 1) + 7.
+// Then the producer warp and two epilogue warps.
+template <int GC>
+struct Roles {
+    static constexpr int kCons = GC > 8 ? 4 : 2;
+    static constexpr int kProducer = kCons;
+    static constexpr int kEpi = kCons + 1;
+    static constexpr int kThreads = (kCons + 3) * 32;
+};
 constexpr int kTile = kDecodeTile; // tokens per pipeline tile
 constexpr int kMaxGrid = 2048;     // persistent CTAs at most (workspace sizing)
 constexpr int kSliceStartCost = 64; // work positions charged per unit for starting a slice
@@ -115,12 +127,10 @@ struct KParams {
 template <int D, int GC>
 constexpr int stages_for()
 {
-    return D == 256 ? 3 : (D == 128 ? (GC <= 4 ? 5 : 4) : 6);
+    return D == 256 ? 3 : (D == 128 ? (GC <= 4 ? 5 : (GC <= 8 ? 4 : 3)) : 6);
 }
 
-// Columns of one consumer warp's softmax state: a unit of up to 8 columns
-// splits its tile rows between the two warps (each holds every column); a
-// multi-query unit of 16 splits its columns (each warp 8 of them, all rows).
+// Columns of one consumer warp's softmax state: 8 at most (one MMA n-tile).
 template <int GC>
 constexpr int warp_cols()
 {
@@ -137,9 +147,10 @@ struct Smem {
     // 128-byte rows (TMA SWIZZLE_128B when the page size allows 8-row boxes)
     __nv_bfloat16 kv[kStages][2][kTile * D];
     // per-warp softmax states of a finished slice: o (unnormalised), m, l
-    float red_o[kSlots][kWarps][RC][D];
-    float red_m[kSlots][kWarps][RC], red_l[kSlots][kWarps][RC];
-    int32_t red_bad[kSlots][kWarps];
+    static constexpr int CW = Roles<GC>::kCons;
+    float red_o[kSlots][CW][RC][D];
+    float red_m[kSlots][CW][RC], red_l[kSlots][CW][RC];
+    int32_t red_bad[kSlots][CW];
     uint64_t full[kStages], empty[kStages];
     uint64_t epi_full[kSlots], epi_empty[kSlots];
     int32_t stage_bad[kStages];
@@ -239,7 +250,7 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, vo
 template <class SM>
 __device__ void build_plan_rows(const KParams &p, SM &sm, int grid)
 {
-    for (int i = threadIdx.x; i < p.batch; i += kThreads)
+    for (int i = threadIdx.x; i < p.batch; i += blockDim.x)
         sm.len[i] = p.seqlens[i];
     __syncthreads();
     if (threadIdx.x < 32) {
@@ -291,7 +302,7 @@ template <class SM>
 __device__ void build_plan_mq(const KParams &p, SM &sm, int grid)
 {
     constexpr int GC = SM::kGC;
-    for (int i = threadIdx.x; i < p.batch; i += kThreads) {
+    for (int i = threadIdx.x; i < p.batch; i += blockDim.x) {
         sm.len[i] = p.seqlens[i];
         const int s = p.qo_indptr[i], e = p.qo_indptr[i + 1];
         sm.qlen[i] = (s < 0 || e > p.total_q || e < s) ? -1 : e - s;
@@ -749,7 +760,7 @@ __device__ void producer(const KParams &p, Smem<D, GC, MQ> &sm, const DecodeMaps
             __syncwarp();
             if (t == 0) { // next slice and its first page window, off the first tile's critical path
                 if (!met) {
-                    named_sync(2, kThreads); // the shared-memory plan is written
+                    named_sync(2, Roles<GC>::kThreads); // the shared-memory plan is written
                     met = true;
                 }
                 if (rec_row != nullptr)
@@ -772,7 +783,7 @@ __device__ void producer(const KParams &p, Smem<D, GC, MQ> &sm, const DecodeMaps
         win = nwin;
     }
     if (!met)
-        named_sync(2, kThreads); // no tile issued: still meet the other warps
+        named_sync(2, Roles<GC>::kThreads); // no tile issued: still meet the other warps
     // After an abort, let copies already issued land before the CTA exits.
     if (*abort && lane == 0) {
         const uint32_t first = g_tile > (uint32_t)S ? g_tile - S : 0;
@@ -844,14 +855,16 @@ __device__ __forceinline__ uint32_t tile_addr(uint32_t base, int row, int chunk,
 
 // MASKED: token rows >= nv hold no token, and column 2c + j (c = lane & 3)
 // sees only the tile's rows below lim[j] (multi-query rows; else lim >= nv).
+// half: the 16-row half of the tile this warp takes.  Warps that share a half
+// (16-column units) zero the same masked V rows, each before its own reads.
 template <int D, bool MASKED, bool MQ>
 __device__ __forceinline__ void consume_tile(const __nv_bfloat16 *Kt, __nv_bfloat16 *Vt, int nv, int lim0, int lim1,
-                                             int warp, int lane, int swz, float scale,
+                                             int half, int lane, int swz, float scale,
                                              const uint32_t (&qf)[D / 16][2], float (&acc)[D / 16][4],
                                              float (&m_run)[2], float (&l_run)[2])
 {
     constexpr int KS = D / 16;
-    const int row0 = warp * 16;
+    const int row0 = half * 16;
     const int g = lane >> 2;
     const uint32_t kbase = smem_addr(Kt), vbase = smem_addr(Vt);
     if (MASKED && nv < row0 + 16) {
@@ -947,115 +960,6 @@ __device__ __forceinline__ void consume_tile(const __nv_bfloat16 *Kt, __nv_bfloa
     }
 }
 
-// A 16-column unit's tile for one consumer warp: its 8 columns over all 32
-// token rows, as two 16-row halves that share one online-softmax update.
-// MASKED as in consume_tile; both warps zero the masked V rows they read
-// (the same zeros, written before either warp's own reads).
-template <int D, bool MASKED>
-__device__ __forceinline__ void consume_tile_wide(const __nv_bfloat16 *Kt, __nv_bfloat16 *Vt, int nv, int lim0,
-                                                  int lim1, int lane, int swz, float scale,
-                                                  const uint32_t (&qf)[D / 16][2], float (&acc)[D / 16][4],
-                                                  float (&m_run)[2], float (&l_run)[2])
-{
-    constexpr int KS = D / 16;
-    const int g = lane >> 2;
-    const uint32_t kbase = smem_addr(Kt), vbase = smem_addr(Vt);
-    if (MASKED && nv < kTile) {
-        for (int i = lane; i < (kTile - nv) * (D / 8); i += 32) {
-            const int r = nv + i / (D / 8), chunk = i % (D / 8);
-            *reinterpret_cast<uint4 *>(Vt + (((r >> 3) * (D / 64) + (chunk >> 3)) * 8 + (r & 7)) * 64 +
-                                       (chunk & 7) * 8) = make_uint4(0u, 0u, 0u, 0u);
-        }
-        __syncwarp();
-    }
-    // ---- S^T = K Q^T for rows 16h .. 16h + 15
-    float v[2][4];
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
-        const int krow = 16 * h + (lane & 15);
-#pragma unroll
-        for (int ks = 0; ks < KS; ++ks) {
-            uint32_t a[4];
-            ldsm_x4(tile_addr<D>(kbase, krow, 2 * ks + (lane >> 4), swz), a);
-            if (ks & 1)
-                mma_16816(sb, a, qf[ks][0], qf[ks][1]);
-            else
-                mma_16816(sa, a, qf[ks][0], qf[ks][1]);
-        }
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-            v[h][i] = (sa[i] + sb[i]) * scale;
-        if constexpr (MASKED) {
-            const int e0 = min(nv, lim0), e1 = min(nv, lim1), r = 16 * h + g;
-            if (r >= e0)
-                v[h][0] = kNegInf;
-            if (r >= e1)
-                v[h][1] = kNegInf;
-            if (r + 8 >= e0)
-                v[h][2] = kNegInf;
-            if (r + 8 >= e1)
-                v[h][3] = kNegInf;
-        }
-    }
-    // ---- online softmax per column over both halves
-    float m_new[2];
-    bool grow = false;
-#pragma unroll
-    for (int j = 0; j < 2; ++j) {
-        float mt = fmaxf(fmaxf(v[0][j], v[0][2 + j]), fmaxf(v[1][j], v[1][2 + j]));
-        mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 4));
-        mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 8));
-        mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 16));
-        m_new[j] = fmaxf(m_run[j], mt);
-        grow |= m_new[j] > m_run[j];
-    }
-    if (__any_sync(0xffffffffu, grow)) {
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-            const float a = m_new[j] == kNegInf ? 1.f : ex2(m_run[j] - m_new[j]);
-            l_run[j] *= a;
-#pragma unroll
-            for (int mt = 0; mt < KS; ++mt) {
-                acc[mt][j] *= a;
-                acc[mt][2 + j] *= a;
-            }
-            m_run[j] = m_new[j];
-        }
-    }
-    uint32_t bh[2][2], bl[2][2]; // P^T B fragments of each half: high and low bf16 parts
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        float pr[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const float m = m_run[i & 1];
-            pr[i] = ex2(v[h][i] - (m == kNegInf ? 0.f : m));
-        }
-        l_run[0] += pr[0] + pr[2];
-        l_run[1] += pr[1] + pr[3];
-        const uint32_t h01 = pack_bf16(pr[0], pr[1]), h23 = pack_bf16(pr[2], pr[3]);
-        const float2 f01 = unpack_bf16(h01), f23 = unpack_bf16(h23);
-        const uint32_t l01 = pack_bf16(pr[0] - f01.x, pr[1] - f01.y), l23 = pack_bf16(pr[2] - f23.x, pr[3] - f23.y);
-        bh[h][0] = movmatrix_trans(h01);
-        bh[h][1] = movmatrix_trans(h23);
-        bl[h][0] = movmatrix_trans(l01);
-        bl[h][1] = movmatrix_trans(l23);
-    }
-    // ---- O^T += V^T P^T over both halves
-    const int vchunk = (lane >> 3) & 1;
-#pragma unroll
-    for (int mt = 0; mt < KS; ++mt) {
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            uint32_t a[4];
-            ldsm_x4_trans(tile_addr<D>(vbase, 16 * h + (lane & 7) + ((lane >> 4) << 3), 2 * mt + vchunk, swz), a);
-            mma_16816(acc[mt], a, bh[h][0], bh[h][1]);
-            mma_16816(acc[mt], a, bl[h][0], bl[h][1]);
-        }
-    }
-}
-
 // Workspace slot of slice j of a unit whose first slice belongs to CTA kf:
 // slice 0 is CTA kf's last slice (slot 2kf+1), slice j >= 1 is CTA kf+j's
 // first slice (slot 2(kf+j)).
@@ -1121,6 +1025,11 @@ __device__ void consumers(const KParams &p, Smem<D, GC, MQ> &sm)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, c = lane & 3;
     const int swz = p.swizzle ? 7 : 0;
+    // this warp's row half of every tile and first column of every unit
+    // (columns past a unit's (query, head) pairs get q = 0; their results
+    // are not read)
+    const int half = warp & 1;
+    const int cb = GC > 8 ? 8 * (warp >> 1) : 0;
     volatile int32_t *abort = &sm.abort;
     SegIter si;
     si.init(p, sm, blockIdx.x);
@@ -1133,14 +1042,6 @@ __device__ void consumers(const KParams &p, Smem<D, GC, MQ> &sm)
     // then finds the plan kernel (two or more launches back) complete.
     if (p.pdl && threadIdx.x == 0)
         asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    // a unit of more than 8 columns (GC = 16 only) splits its columns between
-    // the warps: this warp's first column is cb
-    bool wide = false;
-    int cb = 0;
-    if constexpr (GC > 8) {
-        wide = have && unit_cols<GC>(p, sg) > 8;
-        cb = wide ? 8 * warp : 0;
-    }
     if (have)
         load_q<D, GC, MQ>(p, sg, lane, qf, cb);
     int lim0 = have ? column_keys<GC, MQ>(p, sg, cb + 2 * c) : 0;
@@ -1167,26 +1068,11 @@ __device__ void consumers(const KParams &p, Smem<D, GC, MQ> &sm)
             bad |= ((volatile int32_t *)sm.stage_bad)[s];
             const int tstart = sg.tok0 + t * kTile;
             const int nv = min(kTile, sg.tok1 - tstart);
-            bool done = false;
-            if constexpr (GC > 8) {
-                if (wide) {
-                    if (nv == kTile && tstart + kTile <= sg.mask_from) {
-                        consume_tile_wide<D, false>(sm.kv[s][0], sm.kv[s][1], nv, 0, 0, lane, swz, p.q_scale, qf, acc,
-                                                    m_run, l_run);
-                    } else {
-                        consume_tile_wide<D, true>(sm.kv[s][0], sm.kv[s][1], nv, lim0 - tstart, lim1 - tstart, lane,
-                                                   swz, p.q_scale, qf, acc, m_run, l_run);
-                        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                    }
-                    done = true;
-                }
-            }
-            if (done) {
-            } else if (nv == kTile && (!MQ || tstart + kTile <= sg.mask_from)) {
-                consume_tile<D, false, MQ>(sm.kv[s][0], sm.kv[s][1], nv, 0, 0, warp, lane, swz, p.q_scale, qf, acc,
+            if (nv == kTile && (!MQ || tstart + kTile <= sg.mask_from)) {
+                consume_tile<D, false, MQ>(sm.kv[s][0], sm.kv[s][1], nv, 0, 0, half, lane, swz, p.q_scale, qf, acc,
                                        m_run, l_run);
             } else {
-                consume_tile<D, true, MQ>(sm.kv[s][0], sm.kv[s][1], nv, lim0 - tstart, lim1 - tstart, warp, lane, swz,
+                consume_tile<D, true, MQ>(sm.kv[s][0], sm.kv[s][1], nv, lim0 - tstart, lim1 - tstart, half, lane, swz,
                                       p.q_scale, qf, acc, m_run, l_run);
                 // the zeroed V rows were written by the generic proxy; order
                 // them before the TMA that refills this stage
@@ -1197,12 +1083,8 @@ __device__ void consumers(const KParams &p, Smem<D, GC, MQ> &sm)
                 mbar_arrive(&sm.empty[s]);
             if (t == 0) {
                 more = si.next(p, sm, nx);
-                if (more) {
-                    int ncb = 0;
-                    if constexpr (GC > 8)
-                        ncb = unit_cols<GC>(p, nx) > 8 ? 8 * warp : 0;
-                    load_q<D, GC, MQ>(p, nx, lane, qn, ncb);
-                }
+                if (more)
+                    load_q<D, GC, MQ>(p, nx, lane, qn, cb);
             }
         }
         if (!ok)
@@ -1241,10 +1123,6 @@ __device__ void consumers(const KParams &p, Smem<D, GC, MQ> &sm)
         have = more;
         sg = nx;
         if (have) {
-            if constexpr (GC > 8) {
-                wide = unit_cols<GC>(p, sg) > 8;
-                cb = wide ? 8 * warp : 0;
-            }
             lim0 = column_keys<GC, MQ>(p, sg, cb + 2 * c);
             lim1 = column_keys<GC, MQ>(p, sg, cb + 2 * c + 1);
         }
@@ -1537,40 +1415,30 @@ __host__ __device__ constexpr int kEpiReaders()
     return GC > 8 ? 2 : 1;
 }
 
-// A slice's softmax state from hand-off slot `slot`: the two consumer warps'
-// row halves merged, or (wide units) warp h's columns as they are.
+// A slice's softmax state from hand-off slot `slot`: the two row halves of
+// column group h (consumer warps 2h and 2h + 1) merged.
 template <int D, int GC, bool MQ>
-__device__ __forceinline__ void slot_state(const Smem<D, GC, MQ> &sm, int slot, bool wide, int h, int lane,
+__device__ __forceinline__ void slot_state(const Smem<D, GC, MQ> &sm, int slot, int h, int lane,
                                            EpiState<D, Smem<D, GC, MQ>::RC> &st)
 {
     constexpr int RC = Smem<D, GC, MQ>::RC;
     constexpr int EPT2 = EpiState<D, RC>::EPT2;
-    if (wide) {
-#pragma unroll
-        for (int g = 0; g < RC; ++g) {
-            st.M[g] = sm.red_m[slot][h][g];
-            st.L[g] = sm.red_l[slot][h][g];
-        }
-#pragma unroll
-        for (int i = 0; i < EPT2; ++i)
-            st.o[i] = *reinterpret_cast<const float2 *>(&(&sm.red_o[slot][h][0][0])[pair_elem<D>(lane, i)]);
-        return;
-    }
+    const int w = 2 * h;
     float w0[RC], w1[RC];
 #pragma unroll
     for (int g = 0; g < RC; ++g) {
-        const float m0 = sm.red_m[slot][0][g], m1 = sm.red_m[slot][1][g];
+        const float m0 = sm.red_m[slot][w][g], m1 = sm.red_m[slot][w + 1][g];
         const float M = fmaxf(m0, m1);
         w0[g] = m0 == kNegInf ? 0.f : ex2(m0 - M);
         w1[g] = m1 == kNegInf ? 0.f : ex2(m1 - M);
         st.M[g] = M;
-        st.L[g] = w0[g] * sm.red_l[slot][0][g] + w1[g] * sm.red_l[slot][1][g];
+        st.L[g] = w0[g] * sm.red_l[slot][w][g] + w1[g] * sm.red_l[slot][w + 1][g];
     }
 #pragma unroll
     for (int i = 0; i < EPT2; ++i) {
         const int e = pair_elem<D>(lane, i), g = e / D;
-        const float2 r0 = *reinterpret_cast<const float2 *>(&(&sm.red_o[slot][0][0][0])[e]);
-        const float2 r1 = *reinterpret_cast<const float2 *>(&(&sm.red_o[slot][1][0][0])[e]);
+        const float2 r0 = *reinterpret_cast<const float2 *>(&(&sm.red_o[slot][w][0][0])[e]);
+        const float2 r1 = *reinterpret_cast<const float2 *>(&(&sm.red_o[slot][w + 1][0][0])[e]);
         st.o[i] = make_float2(w0[g] * r0.x + w1[g] * r1.x, w0[g] * r0.y + w1[g] * r1.y);
     }
 }
@@ -1647,8 +1515,8 @@ __device__ void epilogue(const KParams &p, Smem<D, GC, MQ> &sm, int ew)
             break;
         }
         EpiState<D, RC> st;
-        slot_state(sm, slot, wide, h, lane, st);
-        int bad = sm.red_bad[slot][0] | sm.red_bad[slot][1];
+        slot_state(sm, slot, h, lane, st);
+        int bad = sm.red_bad[slot][2 * h] | sm.red_bad[slot][2 * h + 1];
         __syncwarp();
         if (lane == 0) { // consumers may refill this slot once every reader is done
             if constexpr (kEpiReaders<GC>() == 1)
@@ -1758,10 +1626,10 @@ __device__ __forceinline__ void init_barriers(Smem<D, GC, MQ> &sm)
     constexpr int S = Smem<D, GC, MQ>::kStages;
     for (int s = 0; s < S; ++s) {
         mbar_init(&sm.full[s], 1);
-        mbar_init(&sm.empty[s], kWarps);
+        mbar_init(&sm.empty[s], Roles<GC>::kCons);
     }
     for (int s = 0; s < kSlots; ++s) {
-        mbar_init(&sm.epi_full[s], kWarps);
+        mbar_init(&sm.epi_full[s], Roles<GC>::kCons);
         mbar_init(&sm.epi_empty[s], kEpiReaders<GC>());
     }
     sm.abort = 0;
@@ -1775,6 +1643,7 @@ __device__ __forceinline__ void decode_body(const KParams &p, const DecodeMaps &
     Smem<D, GC, MQ> &sm = *reinterpret_cast<Smem<D, GC, MQ> *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    using R = Roles<GC>;
     if constexpr (!MQ) {
         if (p.plan_in != nullptr) {
             // A step plan.  The producer warp alone decides whether it matches
@@ -1788,7 +1657,7 @@ __device__ __forceinline__ void decode_body(const KParams &p, const DecodeMaps &
             // plan is taken; a rejected plan is replaced by planning here.
             const PlanLayout lay = plan_layout(p.batch);
             const PlanHeader *h = reinterpret_cast<const PlanHeader *>(p.plan_in);
-            if (warp == kProducerWarp) {
+            if (warp == R::kProducer) {
                 if (lane == 0) {
                     init_barriers(sm);
                     prefetch_tensormap(&maps.k);
@@ -1809,16 +1678,16 @@ __device__ __forceinline__ void decode_body(const KParams &p, const DecodeMaps &
                 if (lane == 0)
                     sm.plan_state = ok ? 1 : 2;
                 __syncwarp();
-                named_arrive(1, kThreads);
+                named_arrive(1, R::kThreads);
                 if (ok) {
                     producer(p, sm, &maps, &rec);
                     return;
                 }
             } else {
                 // this thread's share of the arrays, at most kMaxDecodeBatch + 1 rows
-                constexpr int kCopy = kThreads - 32;
+                constexpr int kCopy = R::kThreads - 32;
                 constexpr int kPer = (kMaxDecodeBatch + 1 + kCopy - 1) / kCopy;
-                const int t = threadIdx.x < kProducerWarp * 32 ? threadIdx.x : threadIdx.x - 32; // 0 .. 127
+                const int t = threadIdx.x < R::kProducer * 32 ? threadIdx.x : threadIdx.x - 32; // 0 .. kCopy - 1
                 const int32_t *len = reinterpret_cast<const int32_t *>(p.plan_in + lay.len);
                 const int32_t *rowtok = reinterpret_cast<const int32_t *>(p.plan_in + lay.rowtok);
                 const long long *rowbase = reinterpret_cast<const long long *>(p.plan_in + lay.rowbase);
@@ -1839,7 +1708,7 @@ __device__ __forceinline__ void decode_body(const KParams &p, const DecodeMaps &
                     geff = __ldcg(&h->geff);
                     n_empty = __ldcg(&h->n_empty);
                 }
-                named_sync(1, kThreads); // the producer's decision
+                named_sync(1, R::kThreads); // the producer's decision
                 if (sm.plan_state == 1) {
 #pragma unroll
                     for (int j = 0; j < kPer; ++j) {
@@ -1857,22 +1726,22 @@ __device__ __forceinline__ void decode_body(const KParams &p, const DecodeMaps &
                         sm.geff = geff;
                         sm.n_empty = n_empty;
                     }
-                    named_sync(2, kThreads); // the plan is in shared memory
-                    if (warp < kWarps)
+                    named_sync(2, R::kThreads); // the plan is in shared memory
+                    if (warp < R::kCons)
                         consumers(p, sm);
                     else
-                        epilogue(p, sm, warp - kEpilogueWarp);
+                        epilogue(p, sm, warp - R::kEpi);
                     return;
                 }
             }
             // rejected: plan here, as without a step plan (barriers are initialised)
             build_plan(p, sm, (int)gridDim.x); // ends with __syncthreads()
-            if (warp < kWarps)
+            if (warp < R::kCons)
                 consumers(p, sm);
-            else if (warp == kProducerWarp)
+            else if (warp == R::kProducer)
                 producer(p, sm, &maps, nullptr);
             else
-                epilogue(p, sm, warp - kEpilogueWarp);
+                epilogue(p, sm, warp - R::kEpi);
             return;
         }
     }
@@ -1880,19 +1749,19 @@ __device__ __forceinline__ void decode_body(const KParams &p, const DecodeMaps &
         init_barriers(sm);
         sm.plan_state = 0;
     }
-    if (threadIdx.x == kProducerWarp * 32) {
+    if (threadIdx.x == R::kProducer * 32) {
         prefetch_tensormap(&maps.k);
         prefetch_tensormap(&maps.v);
         prefetch_tensormap(&maps.k8);
         prefetch_tensormap(&maps.v8);
     }
     build_plan(p, sm, (int)gridDim.x); // ends with __syncthreads()
-    if (warp < kWarps)
+    if (warp < R::kCons)
         consumers(p, sm);
-    else if (warp == kProducerWarp)
+    else if (warp == R::kProducer)
         producer(p, sm, &maps, nullptr);
     else
-        epilogue(p, sm, warp - kEpilogueWarp);
+        epilogue(p, sm, warp - R::kEpi);
 }
 
 // The plan kernel of PKV_DECODE_MAKE_PLAN: builds the plan of a decode launch
@@ -1967,12 +1836,12 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
     decode_body<D, GC, MQ>(p, maps);
 }
 
-// 16-column multi-query units: the register bound keeps two CTAs on an SM
-// at head_dim <= 128 (the other instantiations fit two without it, or never
-// do at head_dim 256).
+// 16-column multi-query units (seven warps): the register bound keeps two
+// CTAs on an SM at head_dim <= 128 (2 x 224 threads x 144 registers <= 65,536);
+// head_dim 256 runs one CTA per SM.
 template <int D, int GC, bool MQ>
-__global__ void __launch_bounds__(kThreads, D <= 128 ? 2 : 1) decode_kernel_wide(const __grid_constant__ KParams p,
-                                                                                 const __grid_constant__ DecodeMaps maps)
+__global__ void __launch_bounds__(Roles<GC>::kThreads) __maxnreg__(D <= 128 ? 144 : 255)
+    decode_kernel_wide(const __grid_constant__ KParams p, const __grid_constant__ DecodeMaps maps)
 {
     decode_body<D, GC, MQ>(p, maps);
 }
@@ -1994,6 +1863,7 @@ struct KernelEntry {
     const void *fn;
     size_t smem;
     const void *plan_fn; // its step-plan kernel (plain rows), same shared memory
+    int threads;         // block size of the decode kernel
 };
 
 template <int D, int GC, bool MQ>
@@ -2007,7 +1877,7 @@ KernelEntry entry()
         fn = reinterpret_cast<const void *>(&decode_kernel<D, GC, MQ>);
     if constexpr (!MQ)
         plan_fn = reinterpret_cast<const void *>(&decode_plan_kernel<D, GC>);
-    return KernelEntry{D, GC, MQ, fn, smem_bytes<D, GC, MQ>(), plan_fn};
+    return KernelEntry{D, GC, MQ, fn, smem_bytes<D, GC, MQ>(), plan_fn, Roles<GC>::kThreads};
 }
 
 const KernelEntry kTable[] = {
@@ -2144,7 +2014,7 @@ int decode_target_items(int device, int head_dim, int heads_per_cta, bool multi_
         if (cudaFuncSetAttribute(e->fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)e->smem) != cudaSuccess ||
             cudaFuncSetAttribute(e->fn, cudaFuncAttributePreferredSharedMemoryCarveout,
                                  cudaSharedmemCarveoutMaxShared) != cudaSuccess ||
-            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, e->fn, kThreads, e->smem) != cudaSuccess || occ < 1)
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, e->fn, e->threads, e->smem) != cudaSuccess || occ < 1)
             occ = 1;
         const int t = sm_count(device) * occ;
         slot = t > kMaxGrid ? kMaxGrid : t;
@@ -2216,7 +2086,7 @@ cudaError_t launch_decode(const DecodeArgs &a, const DecodeMaps &maps, cudaStrea
     void *args[] = {&p, const_cast<DecodeMaps *>(&maps)};
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(a.grid);
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3(e->threads);
     cfg.dynamicSmemBytes = e->smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
