@@ -1347,14 +1347,17 @@ __device__ void finalize_warp(const KParams &p, const Seg &sg, EpiState<D, GC> &
 }
 
 // Merges the n slice partials of one unit into st (columns col0 .. col0 +
-// GC - 1 of partials `stride` columns wide); returns nonzero if any slice met
-// a bad page.  The loads of all slices are issued before the math.
-template <int D, int GC>
+// GC - 1 of partials `stride` columns wide), all but slice `skip` (-1: none);
+// returns nonzero if any merged slice met a bad page.  The loads of all
+// slices are issued before the math.
+template <int D, int GC, int kBatchMax = 4>
 __device__ int combine_warp(const KParams &p, EpiState<D, GC> &st, int kf, int n, int lane, int stride = GC,
-                           int col0 = 0)
+                           int col0 = 0, int skip = -1)
 {
     constexpr int EPT2 = EpiState<D, GC>::EPT2;
-    constexpr int kBatch = EPT2 >= 16 ? 1 : (EPT2 >= 8 ? 2 : 4); // slices whose loads are in flight together
+    // slices whose loads are in flight together
+    constexpr int kBatch0 = EPT2 >= 16 ? 1 : (EPT2 >= 8 ? 2 : 4);
+    constexpr int kBatch = kBatch0 < kBatchMax ? kBatch0 : kBatchMax;
     int bad = 0;
 #pragma unroll
     for (int g = 0; g < GC; ++g) {
@@ -1369,7 +1372,7 @@ __device__ int combine_warp(const KParams &p, EpiState<D, GC> &st, int kf, int n
         float2 ov[kBatch][EPT2];
 #pragma unroll
         for (int jj = 0; jj < kBatch; ++jj) {
-            if (j0 + jj < n) {
+            if (j0 + jj < n && j0 + jj != skip) {
                 const int slot = slot_of(kf, j0 + jj);
 #pragma unroll
                 for (int g = 0; g < GC; ++g)
@@ -1384,6 +1387,8 @@ __device__ int combine_warp(const KParams &p, EpiState<D, GC> &st, int kf, int n
         for (int jj = 0; jj < kBatch; ++jj) {
             if (j0 + jj >= n)
                 break;
+            if (j0 + jj == skip)
+                continue;
             float a[GC], b[GC];
 #pragma unroll
             for (int g = 0; g < GC; ++g) {
@@ -1466,6 +1471,73 @@ __device__ __forceinline__ void write_partial(const KParams &p, const EpiState<D
     }
 }
 
+// st = the log-sum-exp merge of st and o (two states of the same columns).
+template <int D, int GC>
+__device__ __forceinline__ void merge_state(EpiState<D, GC> &st, const EpiState<D, GC> &o, int lane)
+{
+    constexpr int EPT2 = EpiState<D, GC>::EPT2;
+    float a[GC], b[GC];
+#pragma unroll
+    for (int g = 0; g < GC; ++g) {
+        const float M = fmaxf(st.M[g], o.M[g]);
+        a[g] = st.M[g] == kNegInf ? 0.f : ex2(st.M[g] - M);
+        b[g] = o.M[g] == kNegInf ? 0.f : ex2(o.M[g] - M);
+        st.L[g] = st.L[g] * a[g] + o.L[g] * b[g];
+        st.M[g] = M;
+    }
+#pragma unroll
+    for (int i = 0; i < EPT2; ++i) {
+        const int g = pair_elem<D>(lane, i) / D;
+        st.o[i].x = st.o[i].x * a[g] + o.o[i].x * b[g];
+        st.o[i].y = st.o[i].y * a[g] + o.o[i].y * b[g];
+    }
+}
+
+__device__ __forceinline__ int ld_acquire(const int32_t *ptr)
+{
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(ptr) : "memory");
+    return v;
+}
+
+// The merge ahead of wait_slice, one slice's loads at a time (it runs while
+// the slice streams; kept out of line so the waiting loop stays small).
+template <int D, int GC>
+__device__ __noinline__ int merge_ahead(const KParams &p, EpiState<D, GC> &pre, int kf, int n, int lane, int stride,
+                                        int col0, int skip)
+{
+    return combine_warp<D, GC, 1>(p, pre, kf, n, lane, stride, col0, skip);
+}
+
+// Waits for hand-off slot `slot` (parity `par`) like wait_or_abort.  For a
+// slice of a split unit it watches the unit's ticket meanwhile: once every
+// other slice has arrived (ticket == n - 1), this slice is the last one, and
+// the others' partials are merged into `pre` while this one still streams.
+template <int D, int GC>
+__device__ __forceinline__ bool wait_slice(const KParams &p, uint64_t *bar, uint32_t par, volatile int32_t *abort,
+                                           const int32_t *ticket, int kf, int n, int jown, int lane, int stride,
+                                           int col0, EpiState<D, GC> &pre, bool &have_pre, int &pre_bad)
+{
+    if (mbar_try_wait(bar, par))
+        return true;
+    const uint64_t start = globaltimer_ns();
+    for (;;) {
+        if (n > 1 && !have_pre && ld_acquire(ticket) == n - 1) {
+            pre_bad = merge_ahead<D, GC>(p, pre, kf, n, lane, stride, col0, jown);
+            have_pre = true;
+        }
+        for (int i = 0; i < 32; ++i)
+            if (mbar_try_wait(bar, par))
+                return true;
+        if (*abort)
+            return false;
+        if (globaltimer_ns() - start > kWaitLimitNs) {
+            *abort = 1;
+            return false;
+        }
+    }
+}
+
 template <int D, int GC, bool MQ>
 __device__ void epilogue(const KParams &p, Smem<D, GC, MQ> &sm, int ew)
 {
@@ -1510,7 +1582,14 @@ __device__ void epilogue(const KParams &p, Smem<D, GC, MQ> &sm, int ew)
             const int kl = sg.tok1 == sg.n ? k : owner_of(p, sm, sg.u0 + sg.n - 1);
             n = kl - kf + 1;
         }
-        if (!wait_or_abort(&sm.epi_full[slot], (mine >> 1) & 1u, abort)) {
+        // this warp's ticket and partial columns of the unit
+        int32_t *ticket = GC > 8 ? p.tickets + 2 * sg.unit + h : p.tickets + sg.unit;
+        const int col0 = GC > 8 ? RC * h : 0;
+        EpiState<D, RC> pre; // the other slices, merged ahead when they arrive first
+        bool have_pre = false;
+        int pre_bad = 0;
+        if (!wait_slice<D, RC>(p, &sm.epi_full[slot], (mine >> 1) & 1u, abort, ticket, kf, n, k - kf, lane, GC, col0,
+                               pre, have_pre, pre_bad)) {
             stopped = true;
             break;
         }
@@ -1523,6 +1602,17 @@ __device__ void epilogue(const KParams &p, Smem<D, GC, MQ> &sm, int ew)
                 mbar_arrive(&sm.epi_empty[slot]);
             else
                 mbar_arrive_cnt(&sm.epi_empty[slot], wide ? 1u : (uint32_t)kEpiReaders<GC>());
+        }
+        if (have_pre) { // every other slice is in: the last merge, no ticket
+            merge_state(st, pre, lane);
+            if constexpr (GC > 8)
+                finalize_warp<D, RC, MQ, GC>(p, sg, st, in, bad | pre_bad, lane, RC * h);
+            else
+                finalize_warp<D, GC, MQ>(p, sg, st, in, bad | pre_bad, lane);
+            __syncwarp();
+            if (lane == 0)
+                *ticket = 0; // ready for the next call
+            continue;
         }
         if constexpr (GC > 8) {
             if (n == 1) {
@@ -1837,10 +1927,11 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
 }
 
 // 16-column multi-query units (seven warps): the register bound keeps two
-// CTAs on an SM at head_dim <= 128 (2 x 224 threads x 144 registers <= 65,536);
-// head_dim 256 runs one CTA per SM.
+// CTAs on an SM at head_dim <= 128 (each of the SM's four register files
+// then holds four warps: 128 registers a thread); head_dim 256 runs one CTA
+// per SM.
 template <int D, int GC, bool MQ>
-__global__ void __launch_bounds__(Roles<GC>::kThreads) __maxnreg__(D <= 128 ? 144 : 255)
+__global__ void __launch_bounds__(Roles<GC>::kThreads, D <= 128 ? 2 : 1)
     decode_kernel_wide(const __grid_constant__ KParams p, const __grid_constant__ DecodeMaps maps)
 {
     decode_body<D, GC, MQ>(p, maps);
