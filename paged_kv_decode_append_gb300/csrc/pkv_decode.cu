@@ -1346,6 +1346,36 @@ __device__ void finalize_warp(const KParams &p, const Seg &sg, EpiState<D, GC> &
     }
 }
 
+// One log-sum-exp step: st (the running merge) takes in a partial with
+// (m, l) pairs `ml` (l < 0: a slice that met a bad page) and outputs `ov`.
+// Every merge of partials goes through this one expression, so that equal
+// operands in equal roles give equal bits.  Returns nonzero for a bad slice.
+template <int D, int GC>
+__device__ __forceinline__ int lse_step(EpiState<D, GC> &st, const float2 (&ml)[GC],
+                                        const float2 (&ov)[EpiState<D, GC>::EPT2], int lane)
+{
+    constexpr int EPT2 = EpiState<D, GC>::EPT2;
+    int bad = 0;
+    float a[GC], b[GC];
+#pragma unroll
+    for (int g = 0; g < GC; ++g) {
+        bad |= ml[g].y < 0.f;
+        const float l = fmaxf(ml[g].y, 0.f);
+        const float Mn = fmaxf(st.M[g], ml[g].x);
+        a[g] = st.M[g] == kNegInf ? 0.f : ex2(st.M[g] - Mn);
+        b[g] = ml[g].x == kNegInf ? 0.f : ex2(ml[g].x - Mn);
+        st.L[g] = st.L[g] * a[g] + l * b[g];
+        st.M[g] = Mn;
+    }
+#pragma unroll
+    for (int i = 0; i < EPT2; ++i) {
+        const int g = pair_elem<D>(lane, i) / D;
+        st.o[i].x = st.o[i].x * a[g] + ov[i].x * b[g];
+        st.o[i].y = st.o[i].y * a[g] + ov[i].y * b[g];
+    }
+    return bad;
+}
+
 // Merges the n slice partials of one unit into st (columns col0 .. col0 +
 // GC - 1 of partials `stride` columns wide), all but slice `skip` (-1: none);
 // returns nonzero if any merged slice met a bad page.  The loads of all
@@ -1389,23 +1419,7 @@ __device__ int combine_warp(const KParams &p, EpiState<D, GC> &st, int kf, int n
                 break;
             if (j0 + jj == skip)
                 continue;
-            float a[GC], b[GC];
-#pragma unroll
-            for (int g = 0; g < GC; ++g) {
-                bad |= ml[jj][g].y < 0.f;
-                const float l = fmaxf(ml[jj][g].y, 0.f);
-                const float Mn = fmaxf(st.M[g], ml[jj][g].x);
-                a[g] = st.M[g] == kNegInf ? 0.f : ex2(st.M[g] - Mn);
-                b[g] = ml[jj][g].x == kNegInf ? 0.f : ex2(ml[jj][g].x - Mn);
-                st.L[g] = st.L[g] * a[g] + l * b[g];
-                st.M[g] = Mn;
-            }
-#pragma unroll
-            for (int i = 0; i < EPT2; ++i) {
-                const int g = pair_elem<D>(lane, i) / D;
-                st.o[i].x = st.o[i].x * a[g] + ov[jj][i].x * b[g];
-                st.o[i].y = st.o[i].y * a[g] + ov[jj][i].y * b[g];
-            }
+            bad |= lse_step<D, GC>(st, ml[jj], ov[jj], lane);
         }
     }
     return bad;
@@ -1471,26 +1485,16 @@ __device__ __forceinline__ void write_partial(const KParams &p, const EpiState<D
     }
 }
 
-// st = the log-sum-exp merge of st and o (two states of the same columns).
+// acc takes in the state inc (of the same columns) as combine_warp would take
+// in inc's partial: the same lse_step, so the bits equal that merge's.
 template <int D, int GC>
-__device__ __forceinline__ void merge_state(EpiState<D, GC> &st, const EpiState<D, GC> &o, int lane)
+__device__ __forceinline__ void merge_in(EpiState<D, GC> &acc, const EpiState<D, GC> &inc, int lane)
 {
-    constexpr int EPT2 = EpiState<D, GC>::EPT2;
-    float a[GC], b[GC];
+    float2 ml[GC];
 #pragma unroll
-    for (int g = 0; g < GC; ++g) {
-        const float M = fmaxf(st.M[g], o.M[g]);
-        a[g] = st.M[g] == kNegInf ? 0.f : ex2(st.M[g] - M);
-        b[g] = o.M[g] == kNegInf ? 0.f : ex2(o.M[g] - M);
-        st.L[g] = st.L[g] * a[g] + o.L[g] * b[g];
-        st.M[g] = M;
-    }
-#pragma unroll
-    for (int i = 0; i < EPT2; ++i) {
-        const int g = pair_elem<D>(lane, i) / D;
-        st.o[i].x = st.o[i].x * a[g] + o.o[i].x * b[g];
-        st.o[i].y = st.o[i].y * a[g] + o.o[i].y * b[g];
-    }
+    for (int g = 0; g < GC; ++g)
+        ml[g] = make_float2(inc.M[g], inc.L[g]);
+    (void)lse_step<D, GC>(acc, ml, inc.o, lane);
 }
 
 __device__ __forceinline__ int ld_acquire(const int32_t *ptr)
@@ -1522,7 +1526,9 @@ __device__ __forceinline__ bool wait_slice(const KParams &p, uint64_t *bar, uint
         return true;
     const uint64_t start = globaltimer_ns();
     for (;;) {
-        if (n > 1 && !have_pre && ld_acquire(ticket) == n - 1) {
+        // the merge order stays the slot order: the other slice of a pair, or
+        // all the others when this slice is the unit's last
+        if ((n == 2 || (n > 2 && jown == n - 1)) && !have_pre && ld_acquire(ticket) == n - 1) {
             pre_bad = merge_ahead<D, GC>(p, pre, kf, n, lane, stride, col0, jown);
             have_pre = true;
         }
@@ -1604,7 +1610,13 @@ __device__ void epilogue(const KParams &p, Smem<D, GC, MQ> &sm, int ew)
                 mbar_arrive_cnt(&sm.epi_empty[slot], wide ? 1u : (uint32_t)kEpiReaders<GC>());
         }
         if (have_pre) { // every other slice is in: the last merge, no ticket
-            merge_state(st, pre, lane);
+            // in slot order, the lower slot taking in the higher one
+            if (k - kf == 0) {
+                merge_in(st, pre, lane);
+            } else {
+                merge_in(pre, st, lane);
+                st = pre;
+            }
             if constexpr (GC > 8)
                 finalize_warp<D, RC, MQ, GC>(p, sg, st, in, bad | pre_bad, lane, RC * h);
             else
