@@ -1522,19 +1522,29 @@ __device__ __forceinline__ bool wait_slice(const KParams &p, uint64_t *bar, uint
                                            const int32_t *ticket, int kf, int n, int jown, int lane, int stride,
                                            int col0, EpiState<D, GC> &pre, bool &have_pre, int &pre_bad)
 {
-    if (mbar_try_wait(bar, par))
+    // the merge order stays the slot order: the other slice of a pair, or
+    // all the others when this slice is the unit's last
+    const bool watch = n == 2 || (n > 2 && jown == n - 1);
+    if (!watch && mbar_try_wait(bar, par))
         return true;
     const uint64_t start = globaltimer_ns();
     for (;;) {
-        // the merge order stays the slot order: the other slice of a pair, or
-        // all the others when this slice is the unit's last
-        if ((n == 2 || (n > 2 && jown == n - 1)) && !have_pre && ld_acquire(ticket) == n - 1) {
-            pre_bad = merge_ahead<D, GC>(p, pre, kf, n, lane, stride, col0, jown);
-            have_pre = true;
+        if (watch && !have_pre) {
+            // the ticket load is in flight while the barrier is tested
+            // without suspending
+            const int t = ld_acquire(ticket);
+            for (int i = 0; i < 16; ++i)
+                if (mbar_test_wait(bar, par))
+                    return true;
+            if (t == n - 1) {
+                pre_bad = merge_ahead<D, GC>(p, pre, kf, n, lane, stride, col0, jown);
+                have_pre = true;
+            }
+        } else {
+            for (int i = 0; i < 32; ++i)
+                if (mbar_try_wait(bar, par))
+                    return true;
         }
-        for (int i = 0; i < 32; ++i)
-            if (mbar_try_wait(bar, par))
-                return true;
         if (*abort)
             return false;
         if (globaltimer_ns() - start > kWaitLimitNs) {
