@@ -79,6 +79,8 @@ constexpr int kSliceStartCost = 64; // work positions charged per unit for start
 constexpr int kMinSlice = 192;      // work positions per CTA at least (> kSliceStartCost + kTile)
 constexpr int kSlots = 2;          // consumer -> epilogue hand-off buffers
 constexpr float kNegInf = -INFINITY;
+// Growth of a score over the running maximum (base 2) that moves the maximum.
+constexpr float kLazyMax = 8.f;
 
 static_assert(kTile == 16 * kWarps, "each consumer warp owns 16 rows of a tile");
 
@@ -909,29 +911,31 @@ __device__ __forceinline__ void consume_tile(const __nv_bfloat16 *Kt, __nv_bfloa
         if (row0 + g + 8 >= nv)
             v[2] = v[3] = kNegInf;
     }
-    // ---- online softmax per head column (reduce over the 8 row groups)
-    float m_new[2];
+    // ---- online softmax per head column.  Lazy maximum: the running maximum
+    // moves (a reduction over the 8 row groups, then a rescale) only when a
+    // score exceeds it by more than kLazyMax; until then the exponentials use
+    // the older maximum, which is exact in real arithmetic and keeps every
+    // p below 2^kLazyMax.
     bool grow = false;
 #pragma unroll
-    for (int j = 0; j < 2; ++j) {
-        float mt = fmaxf(v[j], v[2 + j]);
-        mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 4));
-        mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 8));
-        mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 16));
-        m_new[j] = fmaxf(m_run[j], mt);
-        grow |= m_new[j] > m_run[j];
-    }
+    for (int j = 0; j < 2; ++j)
+        grow |= fmaxf(v[j], v[2 + j]) > m_run[j] + kLazyMax;
     if (__any_sync(0xffffffffu, grow)) {
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
-            const float a = m_new[j] == kNegInf ? 1.f : ex2(m_run[j] - m_new[j]);
+            float mt = fmaxf(v[j], v[2 + j]);
+            mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 4));
+            mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 8));
+            mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 16));
+            const float m_new = fmaxf(m_run[j], mt);
+            const float a = m_new == kNegInf ? 1.f : ex2(m_run[j] - m_new);
             l_run[j] *= a;
 #pragma unroll
-            for (int mt = 0; mt < KS; ++mt) {
-                acc[mt][j] *= a;
-                acc[mt][2 + j] *= a;
+            for (int mt2 = 0; mt2 < KS; ++mt2) {
+                acc[mt2][j] *= a;
+                acc[mt2][2 + j] *= a;
             }
-            m_run[j] = m_new[j];
+            m_run[j] = m_new;
         }
     }
     float pr[4];
