@@ -45,10 +45,10 @@
 // columns are then (query, head) pairs, query-major, GC of them per unit:
 // every K/V tile read serves all of a kv head's heads for GC / G queries, and
 // the tiles past kv - q + 1 mask each column at its own limit.  Up to 16
-// columns share one pass over the K/V tiles: kernels with 16-column units run
-// four consumer warps, one per (16-row half, 8-column group) of a tile (one
-// MMA n-tile each); both epilogue warps then finish a unit, 8 columns each,
-// with a combine ticket per half.
+// columns share one pass over the K/V tiles: a unit of more than 8 columns
+// gives each consumer warp 8 of them over all 32 rows of a tile (one MMA
+// n-tile each); both epilogue warps then finish it, 8 columns each, with a
+// combine ticket per half.
 #include <math.h>
 
 #include "pkv_device.cuh"
@@ -62,13 +62,12 @@ constexpr int kProducerWarp = kWarps;        // warp 2
 constexpr int kEpilogueWarp = kWarps + 1;    // warps 3 and 4
 constexpr int kThreads = (kWarps + 3) * 32;
 
-// Warp roles of one instantiation.  Units of up to 8 columns: two consumer
-// warps, one per 16-row half of every tile.  16-column units: four, warp w
-// on row half w & 1 of the tile and columns 8 (w >> 1) .. 8 (w >> 1) + 7.
-// Then the producer warp and two epilogue warps.
+// Warp roles of one instantiation: two consumer warps (units of up to 8
+// columns: one per 16-row half of every tile; 16-column units: one per
+// 8-column half, over all 32 rows), the producer warp and two epilogue warps.
 template <int GC>
 struct Roles {
-    static constexpr int kCons = GC > 8 ? 4 : 2;
+    static constexpr int kCons = 2;
     static constexpr int kProducer = kCons;
     static constexpr int kEpi = kCons + 1;
     static constexpr int kThreads = (kCons + 3) * 32;
@@ -129,7 +128,7 @@ struct KParams {
 template <int D, int GC>
 constexpr int stages_for()
 {
-    return D == 256 ? 3 : (D == 128 ? (GC <= 4 ? 5 : (GC <= 8 ? 4 : 3)) : 6);
+    return D == 256 ? 3 : (D == 128 ? (GC <= 4 ? 5 : 4) : 6);
 }
 
 // Columns of one consumer warp's softmax state: 8 at most (one MMA n-tile).
@@ -964,6 +963,114 @@ __device__ __forceinline__ void consume_tile(const __nv_bfloat16 *Kt, __nv_bfloa
     }
 }
 
+// A 16-column unit's tile for one consumer warp: its 8 columns over all 32
+// token rows, as two 16-row halves that share one online-softmax update.
+// MASKED as in consume_tile; both warps zero the masked V rows they read
+// (the same zeros, written before either warp's own reads).
+template <int D, bool MASKED>
+__device__ __forceinline__ void consume_tile_wide(const __nv_bfloat16 *Kt, __nv_bfloat16 *Vt, int nv, int lim0,
+                                                  int lim1, int lane, int swz, float scale,
+                                                  const uint32_t (&qf)[D / 16][2], float (&acc)[D / 16][4],
+                                                  float (&m_run)[2], float (&l_run)[2])
+{
+    constexpr int KS = D / 16;
+    const int g = lane >> 2;
+    const uint32_t kbase = smem_addr(Kt), vbase = smem_addr(Vt);
+    if (MASKED && nv < kTile) {
+        for (int i = lane; i < (kTile - nv) * (D / 8); i += 32) {
+            const int r = nv + i / (D / 8), chunk = i % (D / 8);
+            *reinterpret_cast<uint4 *>(Vt + (((r >> 3) * (D / 64) + (chunk >> 3)) * 8 + (r & 7)) * 64 +
+                                       (chunk & 7) * 8) = make_uint4(0u, 0u, 0u, 0u);
+        }
+        __syncwarp();
+    }
+    // ---- S^T = K Q^T for rows 16h .. 16h + 15
+    float v[2][4];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+        const int krow = 16 * h + (lane & 15);
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+            uint32_t a[4];
+            ldsm_x4(tile_addr<D>(kbase, krow, 2 * ks + (lane >> 4), swz), a);
+            if (ks & 1)
+                mma_16816(sb, a, qf[ks][0], qf[ks][1]);
+            else
+                mma_16816(sa, a, qf[ks][0], qf[ks][1]);
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            v[h][i] = (sa[i] + sb[i]) * scale;
+        if constexpr (MASKED) {
+            const int e0 = min(nv, lim0), e1 = min(nv, lim1), r = 16 * h + g;
+            if (r >= e0)
+                v[h][0] = kNegInf;
+            if (r >= e1)
+                v[h][1] = kNegInf;
+            if (r + 8 >= e0)
+                v[h][2] = kNegInf;
+            if (r + 8 >= e1)
+                v[h][3] = kNegInf;
+        }
+    }
+    // ---- online softmax per column over both halves (lazy maximum, as in
+    // consume_tile)
+    bool grow = false;
+#pragma unroll
+    for (int j = 0; j < 2; ++j)
+        grow |= fmaxf(fmaxf(v[0][j], v[0][2 + j]), fmaxf(v[1][j], v[1][2 + j])) > m_run[j] + kLazyMax;
+    if (__any_sync(0xffffffffu, grow)) {
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            float mt = fmaxf(fmaxf(v[0][j], v[0][2 + j]), fmaxf(v[1][j], v[1][2 + j]));
+            mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 4));
+            mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 8));
+            mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 16));
+            const float m_new = fmaxf(m_run[j], mt);
+            const float a = m_new == kNegInf ? 1.f : ex2(m_run[j] - m_new);
+            l_run[j] *= a;
+#pragma unroll
+            for (int mt2 = 0; mt2 < KS; ++mt2) {
+                acc[mt2][j] *= a;
+                acc[mt2][2 + j] *= a;
+            }
+            m_run[j] = m_new;
+        }
+    }
+    uint32_t bh[2][2], bl[2][2]; // P^T B fragments of each half: high and low bf16 parts
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        float pr[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float m = m_run[i & 1];
+            pr[i] = ex2(v[h][i] - (m == kNegInf ? 0.f : m));
+        }
+        l_run[0] += pr[0] + pr[2];
+        l_run[1] += pr[1] + pr[3];
+        const uint32_t h01 = pack_bf16(pr[0], pr[1]), h23 = pack_bf16(pr[2], pr[3]);
+        const float2 f01 = unpack_bf16(h01), f23 = unpack_bf16(h23);
+        const uint32_t l01 = pack_bf16(pr[0] - f01.x, pr[1] - f01.y), l23 = pack_bf16(pr[2] - f23.x, pr[3] - f23.y);
+        bh[h][0] = movmatrix_trans(h01);
+        bh[h][1] = movmatrix_trans(h23);
+        bl[h][0] = movmatrix_trans(l01);
+        bl[h][1] = movmatrix_trans(l23);
+    }
+    // ---- O^T += V^T P^T over both halves
+    const int vchunk = (lane >> 3) & 1;
+#pragma unroll
+    for (int mt = 0; mt < KS; ++mt) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            uint32_t a[4];
+            ldsm_x4_trans(tile_addr<D>(vbase, 16 * h + (lane & 7) + ((lane >> 4) << 3), 2 * mt + vchunk, swz), a);
+            mma_16816(acc[mt], a, bh[h][0], bh[h][1]);
+            mma_16816(acc[mt], a, bl[h][0], bl[h][1]);
+        }
+    }
+}
+
 // Workspace slot of slice j of a unit whose first slice belongs to CTA kf:
 // slice 0 is CTA kf's last slice (slot 2kf+1), slice j >= 1 is CTA kf+j's
 // first slice (slot 2(kf+j)).
@@ -1029,11 +1136,6 @@ __device__ void consumers(const KParams &p, Smem<D, GC, MQ> &sm)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, c = lane & 3;
     const int swz = p.swizzle ? 7 : 0;
-    // this warp's row half of every tile and first column of every unit
-    // (columns past a unit's (query, head) pairs get q = 0; their results
-    // are not read)
-    const int half = warp & 1;
-    const int cb = GC > 8 ? 8 * (warp >> 1) : 0;
     volatile int32_t *abort = &sm.abort;
     SegIter si;
     si.init(p, sm, blockIdx.x);
@@ -1046,6 +1148,14 @@ __device__ void consumers(const KParams &p, Smem<D, GC, MQ> &sm)
     // then finds the plan kernel (two or more launches back) complete.
     if (p.pdl && threadIdx.x == 0)
         asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    // a unit of more than 8 columns (GC = 16 only) splits its columns between
+    // the warps: this warp's first column is cb
+    bool wide = false;
+    int cb = 0;
+    if constexpr (GC > 8) {
+        wide = have && unit_cols<GC>(p, sg) > 8;
+        cb = wide ? 8 * warp : 0;
+    }
     if (have)
         load_q<D, GC, MQ>(p, sg, lane, qf, cb);
     int lim0 = have ? column_keys<GC, MQ>(p, sg, cb + 2 * c) : 0;
@@ -1072,11 +1182,26 @@ __device__ void consumers(const KParams &p, Smem<D, GC, MQ> &sm)
             bad |= ((volatile int32_t *)sm.stage_bad)[s];
             const int tstart = sg.tok0 + t * kTile;
             const int nv = min(kTile, sg.tok1 - tstart);
-            if (nv == kTile && (!MQ || tstart + kTile <= sg.mask_from)) {
-                consume_tile<D, false, MQ>(sm.kv[s][0], sm.kv[s][1], nv, 0, 0, half, lane, swz, p.q_scale, qf, acc,
+            bool done = false;
+            if constexpr (GC > 8) {
+                if (wide) {
+                    if (nv == kTile && tstart + kTile <= sg.mask_from) {
+                        consume_tile_wide<D, false>(sm.kv[s][0], sm.kv[s][1], nv, 0, 0, lane, swz, p.q_scale, qf, acc,
+                                                    m_run, l_run);
+                    } else {
+                        consume_tile_wide<D, true>(sm.kv[s][0], sm.kv[s][1], nv, lim0 - tstart, lim1 - tstart, lane,
+                                                   swz, p.q_scale, qf, acc, m_run, l_run);
+                        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    }
+                    done = true;
+                }
+            }
+            if (done) {
+            } else if (nv == kTile && (!MQ || tstart + kTile <= sg.mask_from)) {
+                consume_tile<D, false, MQ>(sm.kv[s][0], sm.kv[s][1], nv, 0, 0, warp, lane, swz, p.q_scale, qf, acc,
                                        m_run, l_run);
             } else {
-                consume_tile<D, true, MQ>(sm.kv[s][0], sm.kv[s][1], nv, lim0 - tstart, lim1 - tstart, half, lane, swz,
+                consume_tile<D, true, MQ>(sm.kv[s][0], sm.kv[s][1], nv, lim0 - tstart, lim1 - tstart, warp, lane, swz,
                                       p.q_scale, qf, acc, m_run, l_run);
                 // the zeroed V rows were written by the generic proxy; order
                 // them before the TMA that refills this stage
@@ -1087,8 +1212,12 @@ __device__ void consumers(const KParams &p, Smem<D, GC, MQ> &sm)
                 mbar_arrive(&sm.empty[s]);
             if (t == 0) {
                 more = si.next(p, sm, nx);
-                if (more)
-                    load_q<D, GC, MQ>(p, nx, lane, qn, cb);
+                if (more) {
+                    int ncb = 0;
+                    if constexpr (GC > 8)
+                        ncb = unit_cols<GC>(p, nx) > 8 ? 8 * warp : 0;
+                    load_q<D, GC, MQ>(p, nx, lane, qn, ncb);
+                }
             }
         }
         if (!ok)
@@ -1127,6 +1256,10 @@ __device__ void consumers(const KParams &p, Smem<D, GC, MQ> &sm)
         have = more;
         sg = nx;
         if (have) {
+            if constexpr (GC > 8) {
+                wide = unit_cols<GC>(p, sg) > 8;
+                cb = wide ? 8 * warp : 0;
+            }
             lim0 = column_keys<GC, MQ>(p, sg, cb + 2 * c);
             lim1 = column_keys<GC, MQ>(p, sg, cb + 2 * c + 1);
         }
@@ -1438,30 +1571,40 @@ __host__ __device__ constexpr int kEpiReaders()
     return GC > 8 ? 2 : 1;
 }
 
-// A slice's softmax state from hand-off slot `slot`: the two row halves of
-// column group h (consumer warps 2h and 2h + 1) merged.
+// A slice's softmax state from hand-off slot `slot`: the two consumer warps'
+// row halves merged, or (wide units) warp h's columns as they are.
 template <int D, int GC, bool MQ>
-__device__ __forceinline__ void slot_state(const Smem<D, GC, MQ> &sm, int slot, int h, int lane,
+__device__ __forceinline__ void slot_state(const Smem<D, GC, MQ> &sm, int slot, bool wide, int h, int lane,
                                            EpiState<D, Smem<D, GC, MQ>::RC> &st)
 {
     constexpr int RC = Smem<D, GC, MQ>::RC;
     constexpr int EPT2 = EpiState<D, RC>::EPT2;
-    const int w = 2 * h;
+    if (wide) {
+#pragma unroll
+        for (int g = 0; g < RC; ++g) {
+            st.M[g] = sm.red_m[slot][h][g];
+            st.L[g] = sm.red_l[slot][h][g];
+        }
+#pragma unroll
+        for (int i = 0; i < EPT2; ++i)
+            st.o[i] = *reinterpret_cast<const float2 *>(&(&sm.red_o[slot][h][0][0])[pair_elem<D>(lane, i)]);
+        return;
+    }
     float w0[RC], w1[RC];
 #pragma unroll
     for (int g = 0; g < RC; ++g) {
-        const float m0 = sm.red_m[slot][w][g], m1 = sm.red_m[slot][w + 1][g];
+        const float m0 = sm.red_m[slot][0][g], m1 = sm.red_m[slot][1][g];
         const float M = fmaxf(m0, m1);
         w0[g] = m0 == kNegInf ? 0.f : ex2(m0 - M);
         w1[g] = m1 == kNegInf ? 0.f : ex2(m1 - M);
         st.M[g] = M;
-        st.L[g] = w0[g] * sm.red_l[slot][w][g] + w1[g] * sm.red_l[slot][w + 1][g];
+        st.L[g] = w0[g] * sm.red_l[slot][0][g] + w1[g] * sm.red_l[slot][1][g];
     }
 #pragma unroll
     for (int i = 0; i < EPT2; ++i) {
         const int e = pair_elem<D>(lane, i), g = e / D;
-        const float2 r0 = *reinterpret_cast<const float2 *>(&(&sm.red_o[slot][w][0][0])[e]);
-        const float2 r1 = *reinterpret_cast<const float2 *>(&(&sm.red_o[slot][w + 1][0][0])[e]);
+        const float2 r0 = *reinterpret_cast<const float2 *>(&(&sm.red_o[slot][0][0][0])[e]);
+        const float2 r1 = *reinterpret_cast<const float2 *>(&(&sm.red_o[slot][1][0][0])[e]);
         st.o[i] = make_float2(w0[g] * r0.x + w1[g] * r1.x, w0[g] * r0.y + w1[g] * r1.y);
     }
 }
@@ -1614,8 +1757,8 @@ __device__ void epilogue(const KParams &p, Smem<D, GC, MQ> &sm, int ew)
             break;
         }
         EpiState<D, RC> st;
-        slot_state(sm, slot, h, lane, st);
-        int bad = sm.red_bad[slot][2 * h] | sm.red_bad[slot][2 * h + 1];
+        slot_state(sm, slot, wide, h, lane, st);
+        int bad = sm.red_bad[slot][0] | sm.red_bad[slot][1];
         __syncwarp();
         if (lane == 0) { // consumers may refill this slot once every reader is done
             if constexpr (kEpiReaders<GC>() == 1)
@@ -1952,10 +2095,9 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant_
     decode_body<D, GC, MQ>(p, maps);
 }
 
-// 16-column multi-query units (seven warps): the register bound keeps two
-// CTAs on an SM at head_dim <= 128 (each of the SM's four register files
-// then holds four warps: 128 registers a thread); head_dim 256 runs one CTA
-// per SM.
+// 16-column multi-query units: the register bound keeps two CTAs on an SM
+// at head_dim <= 128 (the other instantiations fit two without it, or never
+// do at head_dim 256).
 template <int D, int GC, bool MQ>
 __global__ void __launch_bounds__(Roles<GC>::kThreads, D <= 128 ? 2 : 1)
     decode_kernel_wide(const __grid_constant__ KParams p, const __grid_constant__ DecodeMaps maps)
