@@ -1109,22 +1109,6 @@ __device__ __forceinline__ int unit_cols(const KParams &p, const Seg &sg)
     return min(GC, sg.qn * p.group - sg.sub * GC);
 }
 
-// L2 prefetch of the q rows a slice's columns cb .. cb + GC - 1 read (two
-// 128-byte lines per row at head_dim 128), one line per lane.  Issued before
-// the wait for the preceding grid: a hint only (L2 is where every write to q
-// lands), so the loads after the wait find the rows in L2.
-template <int D, int GC, bool MQ>
-__device__ __forceinline__ void prefetch_q(const KParams &p, const Seg &sg, int lane, int cb = 0)
-{
-    constexpr int kLines = D * 2 / 128; // 128-byte lines per q row
-    constexpr int kCols = GC > 8 ? 8 : GC;
-    if (lane < kCols * kLines) {
-        const int row = column_row<GC, MQ>(p, sg, cb + lane / kLines);
-        if (row >= 0)
-            asm volatile("prefetch.global.L2 [%0];" ::"l"(p.q + (int64_t)row * D + (lane % kLines) * 64));
-    }
-}
-
 // B fragments of Q^T for one slice: column cb + g of the unit (zero beyond
 // its columns), dims 16ks + 2c (+8).
 template <int D, int GC, bool MQ>
@@ -1158,12 +1142,6 @@ __device__ void consumers(const KParams &p, Smem<D, GC, MQ> &sm)
     Seg sg, nx;
     bool have = si.next(p, sm, sg);
     uint32_t qf[KS][2];
-    if (p.pdl && have) { // the first slice's queries into L2 meanwhile
-        int pcb = 0;
-        if constexpr (GC > 8)
-            pcb = unit_cols<GC>(p, sg) > 8 ? 8 * warp : 0;
-        prefetch_q<D, GC, MQ>(p, sg, lane, pcb);
-    }
     wait_prior_grid(p);
     // Dependents may start only now that the grid before this one has
     // completed: a later launch that reads a step plan before its own wait
@@ -1736,19 +1714,6 @@ __device__ void epilogue(const KParams &p, Smem<D, GC, MQ> &sm, int ew)
     Seg sg;
     int seg_i = 0;
     bool stopped = false;
-    if (p.pdl && p.with_new) { // this warp's first slice's new token into L2 meanwhile (a hint, as prefetch_q)
-        constexpr int kLines = D * 2 / 128;
-        SegIter pk = si;
-        Seg ps;
-        bool h = pk.next(p, sm, ps);
-        if (h && ew == 1)
-            h = pk.next(p, sm, ps);
-        if (h && lane < 2 * kLines) {
-            const __nv_bfloat16 *row = (lane < kLines ? p.k_new : p.v_new) +
-                                       ((int64_t)ps.b * p.num_kv_heads + ps.kvh) * D + (lane % kLines) * 64;
-            asm volatile("prefetch.global.L2 [%0];" ::"l"(row));
-        }
-    }
     wait_prior_grid(p);
     if (k == 0 && ew == 0) { // a step plan that was rejected, or whose lengths are stale
         int bad = sm.plan_state == 2;
