@@ -1895,7 +1895,10 @@ __device__ __forceinline__ void init_barriers(Smem<D, GC, MQ> &sm)
     mbar_init_fence();
 }
 
-template <int D, int GC, bool MQ>
+// PLAN: the instantiation that can start from a step plan (PKV_DECODE_USE_PLAN);
+// the plain one carries no code of that path, which keeps the start of a
+// lone launch (whose instructions come from memory) short.
+template <int D, int GC, bool MQ, bool PLAN>
 __device__ __forceinline__ void decode_body(const KParams &p, const DecodeMaps &maps)
 {
     extern __shared__ unsigned char smem_raw[];
@@ -1903,7 +1906,7 @@ __device__ __forceinline__ void decode_body(const KParams &p, const DecodeMaps &
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     using R = Roles<GC>;
-    if constexpr (!MQ) {
+    if constexpr (!MQ && PLAN) {
         if (p.plan_in != nullptr) {
             // A step plan.  The producer warp alone decides whether it matches
             // this launch, from the header it loads together with its CTA's
@@ -2088,11 +2091,11 @@ __global__ void __launch_bounds__(kThreads) decode_plan_kernel(const __grid_cons
     }
 }
 
-template <int D, int GC, bool MQ>
+template <int D, int GC, bool MQ, bool PLAN>
 __global__ void __launch_bounds__(kThreads) decode_kernel(const __grid_constant__ KParams p,
                                                           const __grid_constant__ DecodeMaps maps)
 {
-    decode_body<D, GC, MQ>(p, maps);
+    decode_body<D, GC, MQ, PLAN>(p, maps);
 }
 
 // 16-column multi-query units: the register bound keeps two CTAs on an SM
@@ -2102,7 +2105,7 @@ template <int D, int GC, bool MQ>
 __global__ void __launch_bounds__(Roles<GC>::kThreads, D <= 128 ? 2 : 1)
     decode_kernel_wide(const __grid_constant__ KParams p, const __grid_constant__ DecodeMaps maps)
 {
-    decode_body<D, GC, MQ>(p, maps);
+    decode_body<D, GC, MQ, false>(p, maps);
 }
 
 template <int D, int GC, bool MQ>
@@ -2119,24 +2122,27 @@ static_assert(sizeof(Smem<128, 16, true>) + 1024 + 1024 <= 228 * 1024 / 2, "deco
 struct KernelEntry {
     int D, GC;
     bool mq; // multi-query rows
-    const void *fn;
+    const void *fn;      // the decode kernel
     size_t smem;
     const void *plan_fn; // its step-plan kernel (plain rows), same shared memory
-    int threads;         // block size of the decode kernel
+    const void *use_fn;  // the decode kernel that starts from a step plan (plain rows)
+    int threads;         // block size of the decode kernels
 };
 
 template <int D, int GC, bool MQ>
 KernelEntry entry()
 {
     const void *fn;
-    const void *plan_fn = nullptr;
+    const void *plan_fn = nullptr, *use_fn = nullptr;
     if constexpr (GC > 8)
         fn = reinterpret_cast<const void *>(&decode_kernel_wide<D, GC, MQ>);
     else
-        fn = reinterpret_cast<const void *>(&decode_kernel<D, GC, MQ>);
-    if constexpr (!MQ)
+        fn = reinterpret_cast<const void *>(&decode_kernel<D, GC, MQ, false>);
+    if constexpr (!MQ) {
         plan_fn = reinterpret_cast<const void *>(&decode_plan_kernel<D, GC>);
-    return KernelEntry{D, GC, MQ, fn, smem_bytes<D, GC, MQ>(), plan_fn, Roles<GC>::kThreads};
+        use_fn = reinterpret_cast<const void *>(&decode_kernel<D, GC, MQ, true>);
+    }
+    return KernelEntry{D, GC, MQ, fn, smem_bytes<D, GC, MQ>(), plan_fn, use_fn, Roles<GC>::kThreads};
 }
 
 const KernelEntry kTable[] = {
@@ -2267,14 +2273,24 @@ int decode_target_items(int device, int head_dim, int heads_per_cta, bool multi_
         return 1;
     int &slot = cache[device][kernel_index(e)];
     if (slot == 0) {
-        int occ = 1;
+        // The plain and the plan-using kernels take the same grid (a plan is
+        // made for, and checked against, the grid): the CTAs both fit.
+        auto fits = [&](const void *fn) {
+            int occ = 1;
+            if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)e->smem) != cudaSuccess ||
+                cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                     cudaSharedmemCarveoutMaxShared) != cudaSuccess ||
+                cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, fn, e->threads, e->smem) != cudaSuccess || occ < 1)
+                occ = 1;
+            return occ;
+        };
+        int occ = fits(e->fn);
+        if (e->use_fn != nullptr) {
+            const int o2 = fits(e->use_fn);
+            occ = o2 < occ ? o2 : occ;
+        }
         if (e->plan_fn != nullptr)
             (void)cudaFuncSetAttribute(e->plan_fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)e->smem);
-        if (cudaFuncSetAttribute(e->fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)e->smem) != cudaSuccess ||
-            cudaFuncSetAttribute(e->fn, cudaFuncAttributePreferredSharedMemoryCarveout,
-                                 cudaSharedmemCarveoutMaxShared) != cudaSuccess ||
-            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, e->fn, e->threads, e->smem) != cudaSuccess || occ < 1)
-            occ = 1;
         const int t = sm_count(device) * occ;
         slot = t > kMaxGrid ? kMaxGrid : t;
     }
@@ -2343,6 +2359,7 @@ cudaError_t launch_decode(const DecodeArgs &a, const DecodeMaps &maps, cudaStrea
             return err;
     }
     void *args[] = {&p, const_cast<DecodeMaps *>(&maps)};
+    const void *fn = p.plan_in != nullptr && e->use_fn != nullptr ? e->use_fn : e->fn;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(a.grid);
     cfg.blockDim = dim3(e->threads);
@@ -2355,7 +2372,7 @@ cudaError_t launch_decode(const DecodeArgs &a, const DecodeMaps &maps, cudaStrea
         cfg.attrs = attr;
         cfg.numAttrs = 1;
     }
-    return cudaLaunchKernelExC(&cfg, e->fn, args);
+    return cudaLaunchKernelExC(&cfg, fn, args);
 }
 
 } // namespace pkv
