@@ -933,7 +933,7 @@ def main():
         "decode_tok_s_per_attn_layer": steps_tok * world,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": None if traffic_ratio is None else traffic_ratio * launch_bytes,
-                     "peak_kind": peak_kind, "kernel": "pkv::decode_kernel<128,4>",
+                     "peak_kind": peak_kind, "kernel": "pkv::decode_kernel<128,4> (layers 1-35 of a step: the instantiation that starts from the step plan)",
                      "algorithmic_bytes_per_launch": launch_bytes, "launch_ms_mean": kernel_ms,
                      "isolated_launch_ms_mean": float(iso_ms.mean()), "isolated_launch_ms_best": float(iso_ms.min()),
                      "isolated_gbs": iso_gbs, "isolated_launches": int(iso_ms.size),
