@@ -201,14 +201,15 @@ def mixed_bench(kind: str, reps: int, warmup: int, decode_max_qlen, dev=None) ->
         "tensor_peak_kind": tpk_kind, "clocks": clocks.summary(), "gpu_launches": reps * launches}
 
 
-def prefill_bench(dev, reps: int):
+def prefill_bench(dev, reps: int, head_dim: int = 256):
     """The ragged causal prefill workload (B=8, Hq=48, Hkv=6, D=256, page 16
-    HND): one pkv_prefill_attn call per timed iteration (plan + kernel), CUDA
-    events around it, L2 flushed by a 512 MiB write before each call."""
+    HND; head_dim 128 or 64 for the other kernels, same lengths): one
+    pkv_prefill_attn call per timed iteration (plan + kernel), CUDA events
+    around it, L2 flushed by a 512 MiB write before each call."""
     import paged_kv_decode_append_gb300 as pkv
     from paged_kv_decode_append_gb300 import workloads as wl
 
-    case = wl.ragged_prefill(device=dev)
+    case = wl.ragged_prefill(device=dev, head_dim=head_dim)
     q = case.q
     T, Hq, Dh = q.shape
     qo = torch.as_tensor(case.qo_indptr, device=dev)
@@ -247,9 +248,9 @@ def prefill_bench(dev, reps: int):
     ms = float(np.median(times))
     tflops = flops / (ms * 1e-3) / 1e12
     peak, peak_kind = tensor_peak()
-    prof = recorded_prefill_profile()
+    prof = recorded_prefill_profile() if head_dim == 256 else None
     return {
-        "workload": "ragged causal paged prefill: B=8, Hq=48, Hkv=6, D=256, page 16 HND, "
+        "workload": f"ragged causal paged prefill: B=8, Hq=48, Hkv=6, D={head_dim}, page 16 HND, "
                     f"q_len {ql.min()}..{ql.max()}, kv_len {kv.min()}..{kv.max()} (seed 4)",
         "tflops": tflops, "unit": "TFLOP/s", "peak": peak, "peak_kind": peak_kind,
         "frac": tflops / peak, "ms_median": ms, "ms_best": float(times.min()), "reps": reps,
@@ -886,6 +887,11 @@ def main():
     del sets
 
     prefill = prefill_bench(dev, args.prefill_reps) if args.prefill_reps > 0 else None
+    prefill_other = None
+    if args.prefill_reps > 0:  # the other prefill kernels on the same lengths
+        keep = ("tflops", "frac", "ms_median", "ms_best", "reps", "flops", "workload")
+        prefill_other = {f"d{hd}": {k: v for k, v in prefill_bench(dev, args.prefill_reps, hd).items() if k in keep}
+                         for hd in (128, 64)}
 
     if rank != 0:
         return
@@ -954,6 +960,7 @@ def main():
         "contiguous": contiguous,
         "single_layer": single,
         "prefill": prefill,
+        "prefill_other": prefill_other,
         "mixed": mixed,
     }
     print(json.dumps(out))
