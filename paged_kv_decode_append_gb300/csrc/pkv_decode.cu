@@ -13,7 +13,8 @@
 // GB300 design (one persistent CTA per resident slot, five warps):
 //  * producer warp: streams 32-token tiles of K and V of one kv head through
 //    a shared-memory ring with TMA (one box per page piece with all of
-//    head_dim, landing as 8-token groups, 128-byte swizzle, L2 evict-first);
+//    head_dim, landing as 8-token groups, 128-byte swizzle, L2 evict-first;
+//    the lanes issue a tile's boxes together, one box each);
 //    page ids are prefetched 32 at a time into registers, one window (and one
 //    slice) ahead.
 //  * two consumer warps: 16 token rows of every tile each, on tensor-core
@@ -711,9 +712,10 @@ __device__ void producer(const KParams &p, Smem<D, GC, MQ> &sm, const DecodeMaps
                 mbar_arrive_expect_tx(&sm.full[s], 2u * rows * D * 2u);
             }
             __syncwarp();
-            for (int bx = 0; bx < nbox; ++bx) {
-                const int page = __shfl_sync(0xffffffffu, mine, bx);
-                if (lane == 0 && ((okmask >> bx) & 1u)) {
+            // one lane per box (after lane 0's expect_tx, ordered by the __syncwarp above)
+            {
+                const int bx = lane, page = mine;
+                if (bx < nbox && ((okmask >> bx) & 1u)) {
                     const int slot = (tile0 + bx * box) & (p.page_size - 1);
                     int y, z;
                     if (p.layout == PKV_NHD) {
