@@ -138,7 +138,14 @@ def mixed_bench(kind: str, reps: int, warmup: int, decode_max_qlen, dev=None) ->
     ql = np.diff(case.qo_indptr).astype(np.int64)
     L = case.cache_seqlens.astype(np.int64)
     max_qlen = int(ql.max())
-    dq = pkv.default_decode_max_qlen(Hq, case.num_kv_heads) if decode_max_qlen is None else int(decode_max_qlen)
+    # decode_max_qlen is the caller's choice: rows of up to that many queries
+    # take the decode kernel.  The chunked step's decode rows hold one token
+    # each, so it passes 1 (the one-query instantiation); the library default
+    # sizes the decode units for speculative rows of up to 16 / G queries
+    if decode_max_qlen is None:
+        dq = 1 if kind == "chunked" else pkv.default_decode_max_qlen(Hq, case.num_kv_heads)
+    else:
+        dq = int(decode_max_qlen)
     qo = torch.as_tensor(case.qo_indptr, device=dev)
     bt = torch.as_tensor(case.block_table, device=dev)
     sl = torch.as_tensor(case.cache_seqlens, device=dev)
@@ -709,7 +716,8 @@ def main():
                     help="sweep: the 36-layer batch sweep (default); qwen3 / skewed: one decode layer, timed per "
                          "call; spec / chunked: one mixed step (pkv_mixed_attn), timed per call")
     ap.add_argument("--decode-max-qlen", type=int, default=None,
-                    help="spec / chunked: longest row on the decode kernel (default: the library's)")
+                    help="spec / chunked: longest row on the decode kernel (default: 1 for chunked, whose "
+                         "decode rows are single-token; the library's for spec)")
     ap.add_argument("--no-overlap", action="store_true",
                     help="plain launches instead of programmatic dependent launch between layers")
     ap.add_argument("--no-plan", action="store_true",
