@@ -1646,6 +1646,18 @@ __device__ __forceinline__ void merge_in(EpiState<D, GC> &acc, const EpiState<D,
     (void)lse_step<D, GC>(acc, ml, inc.o, lane);
 }
 
+// A split unit's ticket: release orders this warp's partial stores (all lanes,
+// joined by the __syncwarp before it) ahead of the increment; acquire orders
+// the last arriver's reads of the other partials (after the __syncwarp that
+// follows) behind it.  One atomic in place of a sequentially consistent fence
+// on each side.
+__device__ __forceinline__ int atom_add_acq_rel(int32_t *ptr, int v)
+{
+    int old;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(ptr), "r"(v) : "memory");
+    return old;
+}
+
 __device__ __forceinline__ int ld_acquire(const int32_t *ptr)
 {
     int v;
@@ -1791,15 +1803,14 @@ __device__ void epilogue(const KParams &p, Smem<D, GC, MQ> &sm, int ew)
                 continue;
             }
             write_partial<D, RC>(p, st, slot_of(kf, k - kf), GC, RC * h, bad, lane);
-            __threadfence();
             __syncwarp();
             int32_t *ticket = p.tickets + 2 * sg.unit + h;
             int last = 0;
             if (lane == 0)
-                last = atomicAdd(ticket, 1) == n - 1;
+                last = atom_add_acq_rel(ticket, 1) == n - 1;
+            __syncwarp();
             last = __shfl_sync(0xffffffffu, last, 0);
             if (last) {
-                __threadfence();
                 bad = combine_warp<D, RC>(p, st, kf, n, lane, GC, RC * h);
                 finalize_warp<D, RC, MQ, GC>(p, sg, st, in, bad, lane, RC * h);
                 if (lane == 0)
@@ -1811,14 +1822,13 @@ __device__ void epilogue(const KParams &p, Smem<D, GC, MQ> &sm, int ew)
                 continue;
             }
             write_partial<D, GC>(p, st, slot_of(kf, k - kf), GC, 0, bad, lane);
-            __threadfence();
             __syncwarp();
             int last = 0;
             if (lane == 0)
-                last = atomicAdd(&p.tickets[sg.unit], 1) == n - 1;
+                last = atom_add_acq_rel(&p.tickets[sg.unit], 1) == n - 1;
+            __syncwarp();
             last = __shfl_sync(0xffffffffu, last, 0);
             if (last) {
-                __threadfence();
                 bad = combine_warp<D, GC>(p, st, kf, n, lane);
                 finalize_warp<D, GC, MQ>(p, sg, st, in, bad, lane);
                 if (lane == 0)
